@@ -1,0 +1,157 @@
+"""Oracle for paged decode attention, cache write, block copy and the block manager.
+
+TEST INFRASTRUCTURE ONLY.  Only ``tests/``, ``__graft_entry__.smoke()`` and the
+CPU-baseline / reference legs of ``bench.py`` may import this package.  The
+product (``paged_kv_cache_100_gb300``) never imports it, and this package never
+imports the product: the two share no code.
+
+``pa_oracle.c`` is a plain fp64 C restatement of what the pages define (see the
+header of that file for the page/section each function follows); this module
+only compiles it with the host C compiler and marshals numpy arrays into it.
+``block_manager_model`` is a plain-Python model of the host block manager.
+
+Element types: float32 arrays are passed as float32; bfloat16 arrays are passed
+as ``numpy.uint16`` arrays holding the raw 16-bit patterns.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+import threading
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "pa_oracle.c")
+_BUILD_DIR = os.path.join(_HERE, "_build")
+_LIB_PATH = os.path.join(_BUILD_DIR, "liboracle.so")
+
+_lock = threading.Lock()
+_lib = None
+
+F32 = 0
+BF16 = 1
+
+
+def build(force: bool = False) -> str:
+    """Compile ``pa_oracle.c`` into ``oracle/_build/liboracle.so`` (gcc, OpenMP)."""
+    os.makedirs(_BUILD_DIR, exist_ok=True)
+    if (not force and os.path.exists(_LIB_PATH)
+            and os.path.getmtime(_LIB_PATH) >= os.path.getmtime(_SRC)):
+        return _LIB_PATH
+    tmp = _LIB_PATH + f".tmp{os.getpid()}"
+    cmd = ["gcc", "-O2", "-std=c11", "-fPIC", "-shared", "-fopenmp", "-fno-fast-math",
+           _SRC, "-o", tmp, "-lm"]
+    subprocess.run(cmd, check=True)
+    os.replace(tmp, _LIB_PATH)
+    return _LIB_PATH
+
+
+def _load():
+    global _lib
+    with _lock:
+        if _lib is None:
+            lib = ctypes.CDLL(build())
+            vp, i32, dbl = ctypes.c_void_p, ctypes.c_int, ctypes.c_double
+            lib.pao_paged_decode.argtypes = [vp, vp, vp, vp, i32, vp, vp, i32, i32, i32, i32,
+                                             i32, i32, i32, dbl, vp, i32, i32]
+            lib.pao_paged_decode.restype = i32
+            lib.pao_cache_write.argtypes = [vp, vp, vp, vp, vp, i32, i32, i32, i32, i32, i32]
+            lib.pao_cache_write.restype = i32
+            lib.pao_block_copy.argtypes = [vp, vp, vp, i32, i32, i32, i32, i32, i32]
+            lib.pao_block_copy.restype = i32
+            lib.pao_max_threads.argtypes = []
+            lib.pao_max_threads.restype = i32
+            _lib = lib
+        return _lib
+
+
+def _dtype_code(a: np.ndarray) -> int:
+    if a.dtype == np.float32:
+        return F32
+    if a.dtype == np.uint16:
+        return BF16
+    raise TypeError(f"oracle expects float32 or uint16 (bfloat16 bits), got {a.dtype}")
+
+
+def _ptr(a: np.ndarray):
+    return a.ctypes.data_as(ctypes.c_void_p)
+
+
+def max_threads() -> int:
+    return int(_load().pao_max_threads())
+
+
+def paged_decode(query, key_cache, value_cache, block_tables, context_lens, scale,
+                 sel=None, threads: int = 1) -> np.ndarray:
+    """fp64 paged decode attention.
+
+    query [B][Hq][D]; key_cache/value_cache [NB][Hkv][BS][D]; block_tables int32
+    [B][max_blocks]; context_lens int32 [B].  Returns float64 [B][Hq][D], or
+    [n][D] for the (b, h) pairs of ``sel`` (an int array of shape [n, 2]).
+    """
+    lib = _load()
+    query = np.ascontiguousarray(query)
+    key_cache = np.ascontiguousarray(key_cache)
+    value_cache = np.ascontiguousarray(value_cache)
+    code = _dtype_code(query)
+    if _dtype_code(key_cache) != code or _dtype_code(value_cache) != code:
+        raise TypeError("query, key_cache and value_cache must share one element type")
+    block_tables = np.ascontiguousarray(block_tables, dtype=np.int32)
+    context_lens = np.ascontiguousarray(context_lens, dtype=np.int32)
+    B, Hq, D = query.shape
+    NB, Hkv, BS, D2 = key_cache.shape
+    if D2 != D or value_cache.shape != key_cache.shape:
+        raise ValueError("shape mismatch between query and caches")
+    if block_tables.ndim != 2 or block_tables.shape[0] != B or context_lens.shape != (B,):
+        raise ValueError("block_tables must be [B][max_blocks] and context_lens [B]")
+    if sel is None:
+        out = np.zeros((B, Hq, D), dtype=np.float64)
+        sel_arr, n_sel = None, 0
+    else:
+        sel_arr = np.ascontiguousarray(np.asarray(sel, dtype=np.int32).reshape(-1, 2))
+        n_sel = sel_arr.shape[0]
+        out = np.zeros((n_sel, D), dtype=np.float64)
+    rc = lib.pao_paged_decode(_ptr(out), _ptr(query), _ptr(key_cache), _ptr(value_cache), code,
+                              _ptr(block_tables), _ptr(context_lens), B, Hq, Hkv, D, BS,
+                              block_tables.shape[1], NB, float(scale),
+                              None if sel_arr is None else _ptr(sel_arr), n_sel, int(threads))
+    if rc != 0:
+        raise ValueError(f"oracle paged_decode failed with code {rc}")
+    return out
+
+
+def cache_write(key_cache, value_cache, key, value, slot_mapping) -> None:
+    """In-place cache write into numpy pools [NB][Hkv][BS][D] from [T][Hkv][D] rows."""
+    lib = _load()
+    for a in (key_cache, value_cache):
+        if not a.flags.c_contiguous:
+            raise ValueError("pools must be C-contiguous (written in place)")
+    key = np.ascontiguousarray(key)
+    value = np.ascontiguousarray(value)
+    slot_mapping = np.ascontiguousarray(slot_mapping, dtype=np.int64)
+    NB, Hkv, BS, D = key_cache.shape
+    if key.dtype != key_cache.dtype or value.dtype != key_cache.dtype:
+        raise TypeError("rows and pools must share one element type")
+    T = slot_mapping.shape[0]
+    if key.shape != (T, Hkv, D) or value.shape != (T, Hkv, D):
+        raise ValueError("key/value must be [T][Hkv][D]")
+    rc = lib.pao_cache_write(_ptr(key_cache), _ptr(value_cache), _ptr(key), _ptr(value),
+                             _ptr(slot_mapping), T, Hkv, D, BS, NB, key_cache.itemsize)
+    if rc != 0:
+        raise ValueError(f"oracle cache_write failed with code {rc}")
+
+
+def block_copy(key_cache, value_cache, pairs) -> None:
+    """In-place block copy; ``pairs`` is an int array [P][2] of (src, dst)."""
+    lib = _load()
+    for a in (key_cache, value_cache):
+        if not a.flags.c_contiguous:
+            raise ValueError("pools must be C-contiguous (written in place)")
+    pairs = np.ascontiguousarray(np.asarray(pairs, dtype=np.int32).reshape(-1, 2))
+    NB, Hkv, BS, D = key_cache.shape
+    rc = lib.pao_block_copy(_ptr(key_cache), _ptr(value_cache), _ptr(pairs), pairs.shape[0],
+                            Hkv, D, BS, NB, key_cache.itemsize)
+    if rc != 0:
+        raise ValueError(f"oracle block_copy failed with code {rc}")

@@ -1,0 +1,268 @@
+/*
+ * Oracle for paged decode attention, cache write and block copy.
+ *
+ * TEST INFRASTRUCTURE ONLY.  Nothing in the product path may link, load or
+ * call this file; only the tests, the package smoke check and the bench's
+ * CPU-baseline leg use it.  It shares no code, header, table or helper with
+ * the CUDA library: it is a plain, slow, fp64 restatement of what the pages
+ * define, written so that it can be checked against them by eye.
+ *
+ * Sources (page title, section):
+ *  - "KV cache: la memoria de trabajo que sostiene la inferencia LLM",
+ *    "El mecanismo en sí (en cristiano)": the new token's query is multiplied
+ *    against the keys of all previous tokens, normalised with a softmax, and
+ *    the values are weighted by it.
+ *  - "Cómo funciona realmente vLLM (y por qué lo necesitas)", "PagedAttention: la paginación del
+ *    sistema operativo aplicada a la GPU": paging changes only how the K/V of
+ *    a sequence are addressed, never the attention arithmetic.
+ *  - "PagedAttention por dentro", "El modelo de bloques" and "La tabla de
+ *    páginas (block table)": a block holds K and V of 16 consecutive tokens of
+ *    one sequence; token t of a sequence lives in the physical block listed at
+ *    position floor(t / 16) of the sequence's block table.
+ *  - same page, "La tabla de páginas (block table)": a new token is written into the slot
+ *    of its block (cache write).
+ *  - same page, "Copy-on-write para sampling paralelo": on divergence only the
+ *    last shared block is copied (block copy).
+ *  - "KV cache: la memoria de trabajo que sostiene la inferencia LLM", "Trucos para que el cuaderno sea más fino":
+ *    under GQA query heads share K/V in groups; query head h reads KV head
+ *    floor(h / (Hq / Hkv)).
+ *
+ * Layout (the pages do not fix one; this is the library's documented layout):
+ *   key_cache / value_cache : [num_blocks][num_kv_heads][block_size][head_dim]
+ *   query                   : [num_seqs][num_q_heads][head_dim]
+ *   block_tables            : int32 [num_seqs][max_blocks]
+ *   context_lens            : int32 [num_seqs]
+ *   slot_mapping            : int64 [num_tokens], slot = block * block_size + offset,
+ *                             a negative slot means "no write"
+ * Element types: dtype 0 = float32, dtype 1 = bfloat16 (raw 16-bit patterns).
+ * Every element is widened exactly to double before any arithmetic.
+ */
+#include <math.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+#ifdef _OPENMP
+#include <omp.h>
+#endif
+
+#define PAO_OK 0
+#define PAO_ERR_ARG 1
+#define PAO_ERR_INDEX 2
+#define PAO_ERR_NOMEM 3
+
+/* Widen one stored element to double.  bfloat16 is the upper half of an IEEE
+ * binary32, so shifting its 16 bits up by 16 gives the float exactly. */
+static double widen(const void *base, int64_t idx, int dtype)
+{
+    if (dtype == 0) {
+        return (double)((const float *)base)[idx];
+    } else {
+        uint32_t bits = ((uint32_t)((const uint16_t *)base)[idx]) << 16;
+        float f;
+        memcpy(&f, &bits, sizeof f);
+        return (double)f;
+    }
+}
+
+/* Attention of one query head of one sequence over its paged context.
+ * Two passes over the scores (maximum, then normalised weights), exactly the
+ * textbook softmax(q K^T * scale) V with the K/V rows gathered through the
+ * block table in logical token order. */
+static int attend_one(double *out, const void *query, const void *key_cache,
+                      const void *value_cache, int dtype,
+                      const int32_t *block_tables, const int32_t *context_lens,
+                      int b, int h, int num_q_heads, int num_kv_heads,
+                      int head_dim, int block_size, int max_blocks,
+                      int num_blocks, double scale)
+{
+    const int group = num_q_heads / num_kv_heads;
+    const int kvh = h / group;
+    const int L = context_lens[b];
+    int d, t;
+
+    for (d = 0; d < head_dim; ++d)
+        out[d] = 0.0;
+    if (L == 0)
+        return PAO_OK;
+    if (L < 0 || (int64_t)L > (int64_t)max_blocks * block_size)
+        return PAO_ERR_INDEX;
+
+    double *score = (double *)malloc(sizeof(double) * (size_t)L);
+    int64_t *row = (int64_t *)malloc(sizeof(int64_t) * (size_t)L);
+    if (!score || !row) {
+        free(score);
+        free(row);
+        return PAO_ERR_NOMEM;
+    }
+
+    /* Gather: logical token t -> (physical block, offset inside it). */
+    for (t = 0; t < L; ++t) {
+        int logical_block = t / block_size;
+        int offset = t % block_size;
+        int32_t phys = block_tables[(int64_t)b * max_blocks + logical_block];
+        if (phys < 0 || phys >= num_blocks) {
+            free(score);
+            free(row);
+            return PAO_ERR_INDEX;
+        }
+        row[t] = (((int64_t)phys * num_kv_heads + kvh) * block_size + offset) * head_dim;
+    }
+
+    /* Scores s_t = scale * <q, k_t>. */
+    const int64_t qbase = ((int64_t)b * num_q_heads + h) * head_dim;
+    for (t = 0; t < L; ++t) {
+        double dot = 0.0;
+        for (d = 0; d < head_dim; ++d)
+            dot += widen(query, qbase + d, dtype) * widen(key_cache, row[t] + d, dtype);
+        score[t] = scale * dot;
+    }
+
+    /* Softmax: subtract the maximum, exponentiate, normalise. */
+    double mx = score[0];
+    for (t = 1; t < L; ++t)
+        if (score[t] > mx)
+            mx = score[t];
+    double denom = 0.0;
+    for (t = 0; t < L; ++t)
+        denom += exp(score[t] - mx);
+
+    /* Output: the softmax-weighted sum of the value rows. */
+    for (t = 0; t < L; ++t) {
+        double w = exp(score[t] - mx) / denom;
+        for (d = 0; d < head_dim; ++d)
+            out[d] += w * widen(value_cache, row[t] + d, dtype);
+    }
+
+    free(score);
+    free(row);
+    return PAO_OK;
+}
+
+/*
+ * Paged decode attention.
+ *   out : double; [num_seqs][num_q_heads][head_dim] when sel == NULL,
+ *         otherwise [n_sel][head_dim] for the (b, h) pairs listed in sel
+ *         (sel holds 2 * n_sel int32 values: b0, h0, b1, h1, ...).
+ *   num_threads : OpenMP threads over (b, h) pairs; 1 = serial.
+ * Returns 0, or a nonzero code for bad arguments or an out-of-range table
+ * entry (the oracle never reads outside the pools).
+ */
+int pao_paged_decode(double *out, const void *query, const void *key_cache,
+                     const void *value_cache, int dtype,
+                     const int32_t *block_tables, const int32_t *context_lens,
+                     int num_seqs, int num_q_heads, int num_kv_heads,
+                     int head_dim, int block_size, int max_blocks,
+                     int num_blocks, double scale, const int32_t *sel,
+                     int n_sel, int num_threads)
+{
+    if (!out || !query || !key_cache || !value_cache || !block_tables || !context_lens)
+        return PAO_ERR_ARG;
+    if (dtype != 0 && dtype != 1)
+        return PAO_ERR_ARG;
+    if (num_seqs < 0 || num_q_heads <= 0 || num_kv_heads <= 0 || head_dim <= 0 ||
+        block_size <= 0 || max_blocks < 0 || num_blocks < 0)
+        return PAO_ERR_ARG;
+    if (num_q_heads % num_kv_heads != 0)
+        return PAO_ERR_ARG;
+
+    const int64_t n_pairs = sel ? (int64_t)n_sel : (int64_t)num_seqs * num_q_heads;
+    int status = PAO_OK;
+    int64_t i;
+    (void)num_threads;
+#ifdef _OPENMP
+#pragma omp parallel for schedule(dynamic, 1) num_threads(num_threads > 0 ? num_threads : 1)
+#endif
+    for (i = 0; i < n_pairs; ++i) {
+        int b, h;
+        if (sel) {
+            b = sel[2 * i];
+            h = sel[2 * i + 1];
+        } else {
+            b = (int)(i / num_q_heads);
+            h = (int)(i % num_q_heads);
+        }
+        int rc;
+        if (b < 0 || b >= num_seqs || h < 0 || h >= num_q_heads)
+            rc = PAO_ERR_ARG;
+        else
+            rc = attend_one(out + i * head_dim, query, key_cache, value_cache, dtype,
+                            block_tables, context_lens, b, h, num_q_heads,
+                            num_kv_heads, head_dim, block_size, max_blocks,
+                            num_blocks, scale);
+        if (rc != PAO_OK) {
+#ifdef _OPENMP
+#pragma omp critical
+#endif
+            status = rc;
+        }
+    }
+    return status;
+}
+
+/*
+ * Cache write: each new token i whose slot s_i is not negative has its K and V
+ * rows (all KV heads) copied into offset s_i % block_size of physical block
+ * s_i / block_size.  key / value are [num_tokens][num_kv_heads][head_dim].
+ * Tokens are applied in index order.
+ */
+int pao_cache_write(void *key_cache, void *value_cache, const void *key,
+                    const void *value, const int64_t *slot_mapping,
+                    int num_tokens, int num_kv_heads, int head_dim,
+                    int block_size, int num_blocks, int elem_bytes)
+{
+    if (!key_cache || !value_cache || !key || !value || (!slot_mapping && num_tokens > 0))
+        return PAO_ERR_ARG;
+    const int64_t row_bytes = (int64_t)head_dim * elem_bytes;
+    int i, kvh;
+    for (i = 0; i < num_tokens; ++i) {
+        int64_t s = slot_mapping[i];
+        if (s < 0)
+            continue;
+        if (s >= (int64_t)num_blocks * block_size)
+            return PAO_ERR_INDEX;
+        int64_t blk = s / block_size;
+        int64_t off = s % block_size;
+        for (kvh = 0; kvh < num_kv_heads; ++kvh) {
+            int64_t dst = ((blk * num_kv_heads + kvh) * block_size + off) * row_bytes;
+            int64_t src = ((int64_t)i * num_kv_heads + kvh) * row_bytes;
+            memcpy((char *)key_cache + dst, (const char *)key + src, (size_t)row_bytes);
+            memcpy((char *)value_cache + dst, (const char *)value + src, (size_t)row_bytes);
+        }
+    }
+    return PAO_OK;
+}
+
+/*
+ * Block copy (copy-on-write): for each pair (src, dst), in list order, the
+ * whole physical block dst of both pools becomes a copy of block src.
+ * pairs holds 2 * num_pairs int32 values: src0, dst0, src1, dst1, ...
+ */
+int pao_block_copy(void *key_cache, void *value_cache, const int32_t *pairs,
+                   int num_pairs, int num_kv_heads, int head_dim,
+                   int block_size, int num_blocks, int elem_bytes)
+{
+    if (!key_cache || !value_cache || (!pairs && num_pairs > 0))
+        return PAO_ERR_ARG;
+    const int64_t block_bytes = (int64_t)num_kv_heads * block_size * head_dim * elem_bytes;
+    int p;
+    for (p = 0; p < num_pairs; ++p) {
+        int32_t src = pairs[2 * p], dst = pairs[2 * p + 1];
+        if (src < 0 || src >= num_blocks || dst < 0 || dst >= num_blocks)
+            return PAO_ERR_INDEX;
+        memmove((char *)key_cache + dst * block_bytes, (const char *)key_cache + src * block_bytes,
+                (size_t)block_bytes);
+        memmove((char *)value_cache + dst * block_bytes,
+                (const char *)value_cache + src * block_bytes, (size_t)block_bytes);
+    }
+    return PAO_OK;
+}
+
+/* Threads OpenMP would use by default (1 when built without OpenMP). */
+int pao_max_threads(void)
+{
+#ifdef _OPENMP
+    return omp_get_max_threads();
+#else
+    return 1;
+#endif
+}

@@ -1,0 +1,84 @@
+"""Plant plausible mistakes in the oracle's C source and check that a pin catches each.
+
+Each mutant is compiled from a text-edited copy of ``oracle/pa_oracle.c`` into a
+temporary library, swapped in for the real one, and the pin tests of
+``test_oracle_pins`` are run against it: at least one must fail.  This runs on
+the CPU only.
+"""
+import ctypes
+import os
+import subprocess
+
+import pytest
+
+import oracle
+from tests import test_oracle_pins as pins
+
+SRC = os.path.join(os.path.dirname(oracle.__file__), "pa_oracle.c")
+
+MUTANTS = {
+    "drop_scale": ("score[t] = scale * dot;", "score[t] = dot;"),
+    "kv_head_modulo": ("const int kvh = h / group;", "const int kvh = h % num_kv_heads;"),
+    "offset_shift": ("int offset = t % block_size;", "int offset = (t + 1) % block_size;"),
+    "block_index": ("int logical_block = t / block_size;",
+                    "int logical_block = (t / block_size) % 2;"),
+    "short_context": ("const int L = context_lens[b];",
+                      "const int L = context_lens[b] - (context_lens[b] > 1);"),
+    "softmax_sign": ("double w = exp(score[t] - mx) / denom;",
+                     "double w = exp(mx - score[t]) / denom;"),
+    "no_normalise": ("double w = exp(score[t] - mx) / denom;", "double w = exp(score[t] - mx);"),
+    "bf16_shift": ("<< 16;", "<< 15;"),
+    "write_offset": ("int64_t off = s % block_size;", "int64_t off = (s + 1) % block_size;"),
+    "write_skips_v": ("memcpy((char *)value_cache + dst, (const char *)value + src, (size_t)row_bytes);",
+                      ";"),
+    "copy_skips_v": ("memmove((char *)value_cache + dst * block_bytes,", "(void)(value_cache + dst * block_bytes,"),
+}
+
+PIN_FUNCS = [
+    lambda g: pins.test_matches_library_attention_on_contiguous_tokens(4, 4, 4, 64, [1, 17, 33, 64], 0.125),
+    lambda g: pins.test_matches_library_attention_on_contiguous_tokens(3, 8, 2, 128, [15, 16, 100], 0.0883883),
+    lambda g: pins.test_bf16_inputs_widen_exactly(),
+    lambda g: pins.test_one_token_context_returns_its_value_exactly(),
+    lambda g: pins.test_zero_query_averages_the_context(),
+    lambda g: pins.test_dominant_key_selects_its_token(17),
+    lambda g: pins.test_worked_block_table_reads_only_its_session(g),
+    lambda g: pins.test_gqa_equals_mha_with_repeated_kv_heads(),
+    lambda g: pins.test_cache_write_places_each_row_in_its_slot_and_nothing_else(),
+    lambda g: pins.test_cache_write_then_decode_sees_the_new_token(),
+    lambda g: pins.test_block_copy_duplicates_whole_blocks_and_cow_is_invisible_to_decode(),
+]
+
+
+def _compile(tmp_path, name, text):
+    src = tmp_path / f"{name}.c"
+    src.write_text(text)
+    so = tmp_path / f"lib{name}.so"
+    subprocess.run(["gcc", "-O1", "-std=c11", "-fPIC", "-shared", "-fopenmp", str(src), "-o",
+                    str(so), "-lm"], check=True)
+    return str(so)
+
+
+@pytest.mark.parametrize("name", sorted(MUTANTS))
+def test_pins_catch_planted_mistake(name, tmp_path, golden_dir, monkeypatch):
+    text = open(SRC).read()
+    old, new = MUTANTS[name]
+    assert old in text, f"mutation anchor for {name} not found"
+    so = _compile(tmp_path, name, text.replace(old, new))
+    real = oracle._load()
+    mutant = ctypes.CDLL(so)
+    for fn in ("pao_paged_decode", "pao_cache_write", "pao_block_copy", "pao_max_threads"):
+        getattr(mutant, fn).argtypes = getattr(real, fn).argtypes
+        getattr(mutant, fn).restype = getattr(real, fn).restype
+    monkeypatch.setattr(oracle, "_lib", mutant)
+    failures = 0
+    for pin in PIN_FUNCS:
+        try:
+            pin(golden_dir)
+        except (AssertionError, ValueError):
+            failures += 1
+    assert failures > 0, f"no pin caught the planted mistake {name!r}"
+
+
+def test_unmutated_source_passes_every_pin(golden_dir):
+    for pin in PIN_FUNCS:
+        pin(golden_dir)

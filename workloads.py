@@ -1,0 +1,264 @@
+"""Seeded synthetic inputs for paged decode attention.
+
+This module only draws inputs: sequence lengths, block tables built from a
+shuffled pool, slot lists and normally distributed Q/K/V values.  It holds none
+of the attention, cache-write or block-copy arithmetic, so the oracle and the
+CUDA path can both be fed from it without sharing any of that code.
+
+Workloads (all block_size 16, layout [num_blocks][num_kv_heads][16][head_dim]):
+
+  tiny           1 layer, 4 heads MHA, head_dim 64, fp32, 4 sequences with
+                 context lengths {1, 17, 33, 64}, a 16-block pool assigned by a
+                 seeded permutation, values N(0, 1), scale 1/8.
+  llama7b_mha    32 heads MHA, head_dim 128, bf16, batch 64, context lengths
+                 uniform in [128, 2048], pool 1.1x the blocks in use, block
+                 tables are contiguous slices of a shuffled pool, values N(0, 1).
+  llama70b_gqa   64 query / 8 KV heads, head_dim 128, bf16, batch 256, context
+                 lengths uniform in [512, 4096], values N(0, 0.5) (0.5 read as
+                 the standard deviation).
+  long_splitk    32 heads MHA, head_dim 128, bf16, batch 8, context 32768 for
+                 every sequence, partition size 512, values N(0, 1).
+  shared_prefix  32 query / 8 KV heads, head_dim 128, bf16, batch 128; every
+                 block table starts with the same 64 blocks (a 1024-token
+                 prefix) followed by its own suffix blocks (suffix lengths
+                 uniform in [16, 1024]); the first 16 sequences get a private
+                 copy of the last prefix block (copy-on-write pairs).
+
+A decode step appends one new token per sequence at position ``context_lens[b]``
+(its slot is in ``slot_mapping``) and then attends over ``context_lens[b] + 1``
+tokens.  The tables therefore already hold the block that position needs.
+"""
+from __future__ import annotations
+
+import math
+from dataclasses import dataclass, field
+
+import numpy as np
+
+BLOCK_SIZE = 16
+
+
+@dataclass
+class Workload:
+    name: str
+    num_seqs: int
+    num_q_heads: int
+    num_kv_heads: int
+    head_dim: int
+    dtype: str                      # "f32" or "bf16"
+    value_std: float
+    context_lens: np.ndarray        # int32 [B]: tokens already in the cache
+    block_tables: np.ndarray        # int32 [B][max_blocks]; -1 past the used entries
+    num_blocks: int
+    slot_mapping: np.ndarray        # int64 [B]: slot of the appended token
+    cow_pairs: np.ndarray = field(default_factory=lambda: np.zeros((0, 2), np.int32))
+    partition_size: int = 512
+    seed: int = 0
+    block_size: int = BLOCK_SIZE
+
+    @property
+    def scale(self) -> float:
+        return 1.0 / math.sqrt(self.head_dim)
+
+    @property
+    def group(self) -> int:
+        return self.num_q_heads // self.num_kv_heads
+
+    @property
+    def max_blocks(self) -> int:
+        return self.block_tables.shape[1]
+
+    @property
+    def step_context_lens(self) -> np.ndarray:
+        """Context lengths seen by the decode that follows the step's append."""
+        return (self.context_lens + 1).astype(np.int32)
+
+    @property
+    def elem_bytes(self) -> int:
+        return 4 if self.dtype == "f32" else 2
+
+    def pool_shape(self):
+        return (self.num_blocks, self.num_kv_heads, self.block_size, self.head_dim)
+
+
+def _blocks(n_tokens) -> np.ndarray:
+    return -(-np.asarray(n_tokens, dtype=np.int64) // BLOCK_SIZE)
+
+
+def _tables_from_slices(order: np.ndarray, need: np.ndarray) -> np.ndarray:
+    """Block tables made of consecutive slices of ``order`` (one slice per sequence)."""
+    B = need.shape[0]
+    width = int(need.max()) if B else 0
+    tables = np.full((B, width), -1, dtype=np.int32)
+    pos = 0
+    for b in range(B):
+        n = int(need[b])
+        tables[b, :n] = order[pos:pos + n]
+        pos += n
+    return tables
+
+
+def _append_slots(tables: np.ndarray, lens: np.ndarray) -> np.ndarray:
+    B = lens.shape[0]
+    pos = lens.astype(np.int64)
+    phys = tables[np.arange(B), pos // BLOCK_SIZE].astype(np.int64)
+    return phys * BLOCK_SIZE + pos % BLOCK_SIZE
+
+
+def make_workload(name: str, seed: int = 0) -> Workload:
+    rng = np.random.Generator(np.random.PCG64(seed))
+    if name == "tiny":
+        lens = np.array([1, 17, 33, 64], dtype=np.int32)
+        num_blocks = 16
+        order = rng.permutation(num_blocks).astype(np.int32)
+        need = _blocks(lens + 1)          # room for the appended token too
+        tables = _tables_from_slices(order, need)
+        return Workload(name, 4, 4, 4, 64, "f32", 1.0, lens, tables, num_blocks,
+                        _append_slots(tables, lens), partition_size=512, seed=seed)
+
+    if name in ("llama7b_mha", "llama70b_gqa", "long_splitk"):
+        if name == "llama7b_mha":
+            B, Hq, Hkv, std = 64, 32, 32, 1.0
+            lens = rng.integers(128, 2048, size=B, endpoint=True).astype(np.int32)
+        elif name == "llama70b_gqa":
+            B, Hq, Hkv, std = 256, 64, 8, 0.5
+            lens = rng.integers(512, 4096, size=B, endpoint=True).astype(np.int32)
+        else:
+            B, Hq, Hkv, std = 8, 32, 32, 1.0
+            lens = np.full(B, 32768, dtype=np.int32)
+        need = _blocks(lens + 1)
+        num_blocks = int(math.ceil(1.1 * int(need.sum())))
+        order = rng.permutation(num_blocks).astype(np.int32)
+        tables = _tables_from_slices(order, need)
+        return Workload(name, B, Hq, Hkv, 128, "bf16", std, lens, tables, num_blocks,
+                        _append_slots(tables, lens), partition_size=512, seed=seed)
+
+    if name == "shared_prefix":
+        B, Hq, Hkv, prefix_blocks, n_cow = 128, 32, 8, 64, 16
+        suffix = rng.integers(16, 1024, size=B, endpoint=True).astype(np.int64)
+        lens = (prefix_blocks * BLOCK_SIZE + suffix).astype(np.int32)
+        own = _blocks(lens.astype(np.int64) + 1) - prefix_blocks
+        used = prefix_blocks + int(own.sum()) + n_cow
+        num_blocks = int(math.ceil(1.1 * used))
+        order = rng.permutation(num_blocks).astype(np.int32)
+        prefix = order[:prefix_blocks]
+        suffix_tables = _tables_from_slices(order[prefix_blocks:], own)
+        width = prefix_blocks + suffix_tables.shape[1]
+        tables = np.full((B, width), -1, dtype=np.int32)
+        tables[:, :prefix_blocks] = prefix
+        tables[:, prefix_blocks:] = suffix_tables
+        fresh = order[prefix_blocks + int(own.sum()):prefix_blocks + int(own.sum()) + n_cow]
+        cow = np.stack([np.full(n_cow, prefix[-1], dtype=np.int32), fresh], axis=1)
+        tables[:n_cow, prefix_blocks - 1] = fresh   # these sequences read their copy
+        return Workload(name, B, Hq, Hkv, 128, "bf16", 1.0, lens, tables, num_blocks,
+                        _append_slots(tables, lens), cow_pairs=cow.astype(np.int32),
+                        partition_size=512, seed=seed)
+
+    raise KeyError(f"unknown workload {name!r}")
+
+
+WORKLOADS = ("tiny", "llama7b_mha", "llama70b_gqa", "long_splitk", "shared_prefix")
+
+
+def custom_workload(num_seqs, num_q_heads, num_kv_heads, head_dim, context_lens, dtype="bf16",
+                    value_std=1.0, spare_blocks=4, seed=0, name="custom") -> Workload:
+    """A workload with given lengths; block tables are slices of a shuffled pool."""
+    rng = np.random.Generator(np.random.PCG64(seed))
+    lens = np.asarray(context_lens, dtype=np.int32).reshape(num_seqs)
+    need = _blocks(lens.astype(np.int64) + 1)
+    num_blocks = int(need.sum()) + int(spare_blocks)
+    order = rng.permutation(num_blocks).astype(np.int32)
+    tables = _tables_from_slices(order, need)
+    return Workload(name, num_seqs, num_q_heads, num_kv_heads, head_dim, dtype, value_std, lens,
+                    tables, num_blocks, _append_slots(tables, lens), seed=seed)
+
+
+# ---------------------------------------------------------------------------
+# Values
+# ---------------------------------------------------------------------------
+
+def to_bf16_bits(x: np.ndarray) -> np.ndarray:
+    """Round float32 values to bfloat16 (round to nearest even); returns uint16 bits."""
+    import torch
+    t = torch.from_numpy(np.ascontiguousarray(x, dtype=np.float32)).to(torch.bfloat16)
+    return t.view(torch.int16).numpy().view(np.uint16)
+
+
+def bf16_bits_to_f32(bits: np.ndarray) -> np.ndarray:
+    return (np.asarray(bits, dtype=np.uint16).astype(np.uint32) << 16).view(np.float32)
+
+
+@dataclass
+class HostValues:
+    query: np.ndarray        # [B][Hq][D]   float32 or uint16 (bf16 bits)
+    key_cache: np.ndarray    # [NB][Hkv][16][D]
+    value_cache: np.ndarray
+    key_new: np.ndarray      # [B][Hkv][D]  the appended token's K
+    value_new: np.ndarray
+
+
+def host_values(wl: Workload, seed: int | None = None, poison_unused: bool = True) -> HostValues:
+    """Normally distributed values drawn on the host (numpy PCG64).
+
+    With ``poison_unused`` every slot that holds no context token (past the last
+    token of each sequence, and blocks no table uses) is filled with NaN, so a
+    kernel that reads one shows it in its output.
+    """
+    rng = np.random.Generator(np.random.PCG64(wl.seed + 1 if seed is None else seed))
+    B, Hq, Hkv, D = wl.num_seqs, wl.num_q_heads, wl.num_kv_heads, wl.head_dim
+
+    def draw(shape):
+        return (rng.standard_normal(shape, dtype=np.float32) * np.float32(wl.value_std))
+
+    q = draw((B, Hq, D))
+    kc = draw(wl.pool_shape())
+    vc = draw(wl.pool_shape())
+    kn = draw((B, Hkv, D))
+    vn = draw((B, Hkv, D))
+    if poison_unused:
+        mask = used_slot_mask(wl)
+        kc[~mask] = np.nan
+        vc[~mask] = np.nan
+    if wl.dtype == "bf16":
+        q, kc, vc, kn, vn = (to_bf16_bits(a) for a in (q, kc, vc, kn, vn))
+    return HostValues(q, kc, vc, kn, vn)
+
+
+def used_slot_mask(wl: Workload, lens=None) -> np.ndarray:
+    """bool [NB][16]: True where a slot holds one of the first ``lens[b]`` tokens."""
+    lens = wl.context_lens if lens is None else np.asarray(lens)
+    mask = np.zeros((wl.num_blocks, wl.block_size), dtype=bool)
+    for b in range(wl.num_seqs):
+        L = int(lens[b])
+        nb = -(-L // wl.block_size)
+        for j in range(nb):
+            phys = int(wl.block_tables[b, j])
+            fill = min(wl.block_size, L - j * wl.block_size)
+            mask[phys, :fill] = True
+    return mask[:, None, :].repeat(wl.num_kv_heads, axis=1)
+
+
+def device_values(wl: Workload, device, seed: int | None = None):
+    """The same kinds of values drawn on a CUDA device with a seeded torch generator.
+
+    Returns torch tensors (query, key_cache, value_cache, key_new, value_new) in the
+    workload's dtype.  Used where the pools are too large to draw on the host.
+    """
+    import torch
+    g = torch.Generator(device=device)
+    g.manual_seed(wl.seed + 1 if seed is None else seed)
+    tdt = torch.float32 if wl.dtype == "f32" else torch.bfloat16
+    B, Hq, Hkv, D = wl.num_seqs, wl.num_q_heads, wl.num_kv_heads, wl.head_dim
+
+    def draw(shape):
+        out = torch.empty(shape, dtype=tdt, device=device)
+        flat = out.view(-1)
+        chunk = 1 << 26
+        for s in range(0, flat.numel(), chunk):
+            n = min(chunk, flat.numel() - s)
+            tmp = torch.randn(n, generator=g, device=device, dtype=torch.float32)
+            flat[s:s + n].copy_(tmp.mul_(wl.value_std))
+        return out
+
+    return (draw((B, Hq, D)), draw(wl.pool_shape()), draw(wl.pool_shape()),
+            draw((B, Hkv, D)), draw((B, Hkv, D)))
