@@ -1,0 +1,556 @@
+"""Benchmark of one paged-decode step on GB300.
+
+A step is one pass of the whole hot path over one batch: the cache write of one
+new token per sequence, the copy-on-write block copies of the workload (if it
+has any) and paged decode attention over the grown contexts (split-K partition
+kernel + merge kernel).  The default workload is the Llama-7B-shaped decode
+layer (32 heads MHA, head_dim 128, bf16, batch 64, context lengths uniform in
+[128, 2048], block tables drawn from a shuffled pool 1.1x the blocks in use).
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl reference]
+
+Prints one JSON line.  Under torchrun every rank runs its own copy of the
+workload (weak scaling, no collective on the data path); rank 0 prints.
+``--impl reference`` times the fp64 oracle on the host cores instead.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import workloads as W  # noqa: E402
+
+METRIC = "paged decode attention tokens/s and KV GB/s (% of GB300 HBM peak), 1 GPU"
+NOMINAL_HBM_GBS = 7900.0     # GB300 HBM3e nominal
+FALLBACK_HBM_GBS = 6800.0    # earlier GB300 measurement, used only without MEASURED_PEAKS.json
+L2_BYTES = 129 * 10**6
+
+
+# ---------------------------------------------------------------------------
+# Byte accounting ("KV cache: la memoria de trabajo que sostiene la inferencia
+# LLM", section "El precio: cuánto pesa la mochila": K and V of every token,
+# 2 * layers * kv_heads * head_dim * bytes per element)
+# ---------------------------------------------------------------------------
+def kv_bytes_per_token(n_layers, n_kv_heads, head_dim, bytes_per_elem=2) -> int:
+    return 2 * n_layers * n_kv_heads * head_dim * bytes_per_elem
+
+
+def decode_algorithmic_bytes(wl: W.Workload, lens=None) -> dict:
+    """Least bytes one decode call moves: K/V of every context token, Q, O, tables, lengths."""
+    lens = wl.step_context_lens if lens is None else np.asarray(lens)
+    lens = lens.astype(np.int64)
+    e = wl.elem_bytes
+    kv = int(lens.sum()) * kv_bytes_per_token(1, wl.num_kv_heads, wl.head_dim, e)
+    q = wl.num_seqs * wl.num_q_heads * wl.head_dim * e
+    tables = int((-(-lens // 16)).sum()) * 4 + 4 * wl.num_seqs
+    return {"kv": kv, "q": q, "o": q, "tables": tables, "total": kv + 2 * q + tables}
+
+
+def unique_kv_bytes(wl: W.Workload, lens=None) -> int:
+    """K/V bytes of distinct (block, slot) pairs read: shared prefix blocks count once."""
+    lens = wl.step_context_lens if lens is None else np.asarray(lens)
+    seen = {}
+    for b in range(wl.num_seqs):
+        L = int(lens[b])
+        for j in range(-(-L // 16)):
+            phys = int(wl.block_tables[b, j])
+            seen[phys] = max(seen.get(phys, 0), min(16, L - 16 * j))
+    return sum(seen.values()) * kv_bytes_per_token(1, wl.num_kv_heads, wl.head_dim, wl.elem_bytes)
+
+
+def step_write_bytes(wl: W.Workload) -> int:
+    row = wl.num_kv_heads * wl.head_dim * wl.elem_bytes
+    cow = int(wl.cow_pairs.shape[0]) * wl.num_kv_heads * 16 * wl.head_dim * wl.elem_bytes * 2
+    return 2 * 2 * wl.num_seqs * row + 2 * cow
+
+
+# ---------------------------------------------------------------------------
+# Distributed plumbing (weak scaling: no collective on the data path)
+# ---------------------------------------------------------------------------
+def dist_env():
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return rank, world, local
+
+
+def init_dist(backend: str):
+    import torch.distributed as dist
+    rank, world, _ = dist_env()
+    if world > 1 and not dist.is_initialized():
+        dist.init_process_group(backend=backend)
+    return rank, world
+
+
+def max_over_ranks(x: float, device=None) -> float:
+    import torch
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
+        return float(x)
+    t = torch.tensor([float(x)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def barrier():
+    import torch.distributed as dist
+    if dist.is_available() and dist.is_initialized():
+        dist.barrier()
+
+
+# ---------------------------------------------------------------------------
+# Peaks, clocks, traffic
+# ---------------------------------------------------------------------------
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            p = json.load(f)
+        return float(p["hbm_gbs"]), "measured"
+    except Exception:
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+class ClockSampler:
+    """nvidia-smi samples of SM clock and throttle reasons while the timed region runs."""
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.tmp = tempfile.NamedTemporaryFile(mode="w+", suffix=".csv", delete=False)
+        self.proc = None
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(gpu_index), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "100"], stdout=self.tmp,
+                stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+
+    def wait_first(self, timeout=5.0):
+        t0 = time.time()
+        while self.proc is not None and time.time() - t0 < timeout:
+            self.tmp.flush()
+            if os.path.getsize(self.tmp.name) > 0:
+                return
+            time.sleep(0.02)
+
+    def mark(self):
+        self.tmp.flush()
+        return os.path.getsize(self.tmp.name)
+
+    def stop(self, start_offset: int):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+        self.tmp.flush()
+        with open(self.tmp.name) as f:
+            f.seek(start_offset)
+            lines = [ln.strip() for ln in f if ln.strip()]
+        os.unlink(self.tmp.name)
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in lines:
+            parts = [p.strip() for p in ln.split(",")]
+            if len(parts) < 8:
+                continue
+            try:
+                sm.append(float(parts[0]))
+                mx.append(float(parts[1]))
+            except ValueError:
+                continue
+            for name, val in zip(names, parts[4:8]):
+                if val.lower() == "active":
+                    reasons.add(name)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+def kernel_source_hash() -> str:
+    h = hashlib.sha256()
+    for f in ("pa_decode.cu", "pa_device.cuh", "pa_internal.h"):
+        with open(os.path.join(ROOT, "paged_kv_cache_100_gb300", "csrc", f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def measured_traffic(workload: str):
+    """DRAM bytes per pa_decode call from the committed ncu summary, if it still
+    describes the current kernel source (else None)."""
+    path = os.path.join(ROOT, "profiles", "decode_traffic.json")
+    try:
+        with open(path) as f:
+            rec = json.load(f)
+        entry = rec[workload]
+        if entry.get("kernel_source_hash") != kernel_source_hash():
+            return None
+        return float(entry["dram_bytes_per_call"])
+    except Exception:
+        return None
+
+
+# ---------------------------------------------------------------------------
+# GPU arm
+# ---------------------------------------------------------------------------
+def run_gpu(args):
+    import torch
+    rank, world, local = dist_env()
+    if world > 1:
+        torch.cuda.set_device(local)
+        init_dist("nccl")
+    dev = torch.device("cuda", local if world > 1 else 0)
+    torch.cuda.set_device(dev)
+    from paged_kv_cache_100_gb300.build import build
+    if rank == 0 or world == 1:
+        build()
+    barrier()
+    import paged_kv_cache_100_gb300 as pkv
+
+    wl = W.make_workload(args.workload, seed=args.seed)
+    q, kc, vc, kn, vn = W.device_values(wl, dev, seed=args.seed + 17 + rank)
+    bt = torch.from_numpy(wl.block_tables).to(dev)
+    lens = torch.from_numpy(wl.step_context_lens).to(dev)
+    slots = torch.from_numpy(wl.slot_mapping).to(dev)
+    pairs = torch.from_numpy(wl.cow_pairs).to(dev)
+    has_cow = wl.cow_pairs.shape[0] > 0
+    P = args.partition_size or wl.partition_size
+    out = torch.empty_like(q)
+    ws = torch.empty(max(pkv.decode_workspace_bytes(wl.num_seqs, wl.num_q_heads, wl.head_dim,
+                                                    wl.max_blocks, P), 16),
+                     dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream(dev)
+
+    def step(ev_pre=None, ev_post=None):
+        pkv.cache_write(kc, vc, kn, vn, slots)
+        if has_cow:
+            pkv.block_copy(kc, vc, pairs)
+        if ev_pre is not None:
+            ev_pre.record(stream)
+        pkv.decode(q, kc, vc, bt, lens, wl.scale, out=out, partition_size=P, workspace=ws)
+        if ev_post is not None:
+            ev_post.record(stream)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize(dev)
+
+    K = args.steps
+    pre = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
+    post = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    sampler = ClockSampler(dev.index if dev.index is not None else 0) if rank == 0 else None
+    if sampler:
+        sampler.wait_first()
+        off = sampler.mark()
+    barrier()
+    torch.cuda.synchronize(dev)
+    launches0 = pkv.launch_count()
+    e0.record(stream)
+    for i in range(K):
+        step(pre[i], post[i])
+    e1.record(stream)
+    torch.cuda.synchronize(dev)
+    barrier()
+    launches = pkv.launch_count() - launches0
+    clocks = sampler.stop(off) if sampler else None
+    ms_total = e0.elapsed_time(e1)
+    decode_ms = sum(a.elapsed_time(b) for a, b in zip(pre, post)) / K
+    ms_total = max_over_ranks(ms_total, dev)
+    decode_ms = max_over_ranks(decode_ms, dev)
+    ms_per_step = ms_total / K
+
+    # end to end through the public API: pinned host inputs in, output back, every step
+    e2e = run_e2e(args, pkv, wl, q, kc, vc, kn, vn, dev, stream, P, ws)
+
+    if rank != 0:
+        return None
+    bytes_decode = decode_algorithmic_bytes(wl)
+    peak, peak_kind = load_peaks()
+    achieved = bytes_decode["total"] / (decode_ms * 1e-3) / 1e9
+    tokens_per_s = wl.num_seqs * world / (ms_per_step * 1e-3)
+    traffic = measured_traffic(args.workload)
+    line = {
+        "metric": METRIC,
+        "value": tokens_per_s,
+        "unit": "tokens/s",
+        "n_gpus": world,
+        "steps": K,
+        "warmup": args.warmup,
+        "ms_per_step": ms_per_step,
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": wl.dtype,
+        "data": "synthetic (seeded; N(0, %g) values, shuffled block pool)" % wl.value_std,
+        "config": workload_config(wl, P, world),
+        "decode_ms": decode_ms,
+        "kv_gbs": bytes_decode["kv"] / (decode_ms * 1e-3) / 1e9,
+        "decode_gbs": achieved,
+        "context_tokens_per_s": float(wl.step_context_lens.sum()) * world / (ms_per_step * 1e-3),
+        "hbm_frac_of_measured": achieved / peak if peak_kind == "measured" else None,
+        "hbm_frac_of_nominal_7900": achieved / NOMINAL_HBM_GBS,
+        "roofline": {
+            "kernel": "pa_decode (partition kernel + merge kernel, one C-ABI call)",
+            "bound": "hbm",
+            "achieved": achieved,
+            "peak": peak,
+            "peak_source": f"{peak_kind} (MEASURED_PEAKS.json hbm_gbs)" if peak_kind == "measured"
+            else "fallback 6800 GB/s",
+            "unit": "GB/s",
+            "frac": achieved / peak,
+            "traffic": traffic,
+            "algorithmic_bytes_per_call": bytes_decode["total"],
+        },
+        "gpu_launches": int(launches),
+        "clocks": clocks,
+        "e2e": e2e,
+    }
+    if wl.cow_pairs.shape[0] or args.workload == "shared_prefix":
+        line["unique_kv_bytes"] = unique_kv_bytes(wl)
+    if not args.no_cpu_baseline and world == 1:
+        line["cpu_baseline"] = cpu_baseline(args, wl, q, kc, vc, budget_s=args.cpu_seconds)
+    return line
+
+
+def workload_config(wl, P, world):
+    lens = wl.step_context_lens
+    return {
+        "workload": wl.name,
+        "num_seqs_per_gpu": wl.num_seqs,
+        "global_batch": wl.num_seqs * world,
+        "num_q_heads": wl.num_q_heads,
+        "num_kv_heads": wl.num_kv_heads,
+        "head_dim": wl.head_dim,
+        "block_size": wl.block_size,
+        "context_lens_min_max_mean": [int(lens.min()), int(lens.max()), float(lens.mean())],
+        "num_blocks": wl.num_blocks,
+        "partition_size": P,
+        "cow_pairs_per_step": int(wl.cow_pairs.shape[0]),
+        "parallelism": f"weak scaling, {world} independent replica(s)",
+        "l2": "inputs larger than L2: %.2f GB of K/V read per step vs 129 MB L2"
+              % (decode_algorithmic_bytes(wl)["kv"] / 1e9),
+    }
+
+
+def run_e2e(args, pkv, wl, q, kc, vc, kn, vn, dev, stream, P, ws):
+    """Same step through the public API with host inputs: H2D of the step's inputs
+    (query, new K/V rows, slots, tables, lengths, copy pairs) and D2H of the output
+    inside the timed region."""
+    import torch
+    host = {
+        "q": q.cpu().pin_memory(), "kn": kn.cpu().pin_memory(), "vn": vn.cpu().pin_memory(),
+        "slots": torch.from_numpy(wl.slot_mapping).pin_memory(),
+        "bt": torch.from_numpy(wl.block_tables).pin_memory(),
+        "lens": torch.from_numpy(wl.step_context_lens).pin_memory(),
+        "pairs": torch.from_numpy(wl.cow_pairs).pin_memory(),
+    }
+    devb = {k: torch.empty_like(v, device=dev) for k, v in host.items()}
+    out = torch.empty_like(q)
+    out_host = torch.empty(out.shape, dtype=out.dtype).pin_memory()
+    has_cow = wl.cow_pairs.shape[0] > 0
+    h2d = sum(v.numel() * v.element_size() for k, v in host.items() if k != "pairs" or has_cow)
+    d2h = out.numel() * out.element_size()
+
+    def step():
+        for k, v in host.items():
+            if k == "pairs" and not has_cow:
+                continue
+            devb[k].copy_(v, non_blocking=True)
+        pkv.cache_write(kc, vc, devb["kn"], devb["vn"], devb["slots"])
+        if has_cow:
+            pkv.block_copy(kc, vc, devb["pairs"])
+        pkv.decode(devb["q"], kc, vc, devb["bt"], devb["lens"], wl.scale, out=out,
+                   partition_size=P, workspace=ws)
+        out_host.copy_(out, non_blocking=True)
+
+    for _ in range(max(3, args.warmup // 10)):
+        step()
+    torch.cuda.synchronize(dev)
+    K = max(1, min(args.steps, args.e2e_steps))
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    barrier()
+    e0.record(stream)
+    for _ in range(K):
+        step()
+    e1.record(stream)
+    torch.cuda.synchronize(dev)
+    barrier()
+    ms = max_over_ranks(e0.elapsed_time(e1) / K, dev)
+    _, world, _ = dist_env()
+    return {"value": wl.num_seqs * world / (ms * 1e-3), "unit": "tokens/s", "ms_per_step": ms,
+            "steps": K, "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h)}
+
+
+# ---------------------------------------------------------------------------
+# CPU baseline: the fp64 oracle on the host cores over a bounded sample
+# ---------------------------------------------------------------------------
+def _compact(wl, seqs, kc_host_fn):
+    lens = wl.step_context_lens[seqs].astype(np.int64)
+    need = -(-lens // 16)
+    tabs = np.full((len(seqs), int(need.max())), -1, dtype=np.int32)
+    for i, b in enumerate(seqs):
+        tabs[i, :need[i]] = wl.block_tables[b, :need[i]]
+    used = np.unique(tabs[tabs >= 0])
+    remap = np.full(wl.num_blocks, -1, dtype=np.int64)
+    remap[used] = np.arange(used.size)
+    new = np.where(tabs >= 0, remap[np.maximum(tabs, 0)], -1).astype(np.int32)
+    return used, new, lens.astype(np.int32)
+
+
+def _bits(t):
+    import torch
+    if t.dtype == torch.bfloat16:
+        return t.contiguous().view(torch.int16).cpu().numpy().view(np.uint16)
+    return t.contiguous().cpu().numpy()
+
+
+def cpu_baseline(args, wl, q, kc, vc, budget_s=10.0):
+    import torch
+    import oracle
+    threads = oracle.max_threads()
+    rng = np.random.default_rng(3)
+    n_seq = min(wl.num_seqs, 8)
+    seqs = np.sort(rng.choice(wl.num_seqs, size=n_seq, replace=False))
+    used, tabs, lens = _compact(wl, seqs, None)
+    idx = torch.from_numpy(used.astype(np.int64)).to(kc.device)
+    kch, vch = _bits(kc.index_select(0, idx)), _bits(vc.index_select(0, idx))
+    qh = _bits(q[torch.from_numpy(seqs).to(q.device)])
+    t0 = time.perf_counter()
+    reps = 0
+    while True:
+        oracle.paged_decode(qh, kch, vch, tabs, lens, wl.scale, threads=threads)
+        reps += 1
+        if time.perf_counter() - t0 >= budget_s:
+            break
+    dt = time.perf_counter() - t0
+    # scale the sample's time to the whole batch by context tokens
+    frac = float(lens.sum()) / float(wl.step_context_lens.sum())
+    t_batch = dt / reps / frac
+    return {"value": wl.num_seqs / t_batch, "unit": "tokens/s", "cores": threads, "kind": "oracle",
+            "sample": f"{n_seq} of {wl.num_seqs} sequences (all {wl.num_q_heads} heads, "
+                      f"{int(lens.sum())} context tokens) x {reps} repetitions in {dt:.1f} s; "
+                      "time scaled to the batch by context tokens"}
+
+
+# ---------------------------------------------------------------------------
+# Reference arm: the oracle, as it stands, on the host cores
+# ---------------------------------------------------------------------------
+def run_reference(args):
+    rank, world, _ = dist_env()
+    if world > 1 and rank != 0:
+        return None
+    import oracle
+    oracle.build()
+    wl = W.make_workload(args.workload, seed=args.seed)
+    threads = oracle.max_threads()
+    # a bounded sample: a few sequences of the workload drawn on the host; each
+    # step decodes one of them (all heads), cycling through the sample
+    rng = np.random.default_rng(5)
+    n_seq = min(wl.num_seqs, 8)
+    seqs = np.sort(rng.choice(wl.num_seqs, size=n_seq, replace=False))
+    used, tabs, lens = _compact(wl, seqs, None)
+    vrng = np.random.Generator(np.random.PCG64(args.seed + 99))
+    shape = (used.size, wl.num_kv_heads, 16, wl.head_dim)
+
+    def draw(s):
+        x = vrng.standard_normal(s, dtype=np.float32) * np.float32(wl.value_std)
+        return W.to_bf16_bits(x) if wl.dtype == "bf16" else x
+
+    kch, vch = draw(shape), draw(shape)
+    qh = draw((n_seq, wl.num_q_heads, wl.head_dim))
+    for _ in range(args.warmup):
+        oracle.paged_decode(qh[:1], kch, vch, tabs[:1], lens[:1], wl.scale, threads=threads)
+    steps = args.steps
+    tokens = 0
+    ctx = 0
+    t0 = time.perf_counter()
+    deadline = t0 + args.reference_seconds
+    done = 0
+    for i in range(steps):
+        j = i % n_seq
+        oracle.paged_decode(qh[j:j + 1], kch, vch, tabs[j:j + 1], lens[j:j + 1], wl.scale,
+                            threads=threads)
+        tokens += 1
+        ctx += int(lens[j])
+        done += 1
+        if time.perf_counter() > deadline:
+            break
+    dt = time.perf_counter() - t0
+    # tokens/s of the whole batch at this rate of context tokens per second
+    batch_ctx = float(wl.step_context_lens.sum())
+    value = wl.num_seqs / (batch_ctx / (ctx / dt))
+    sample = (f"{done} steps, each one sequence of {n_seq} sampled ({int(lens.sum())} context "
+              f"tokens in the sample), all {wl.num_q_heads} heads; rate scaled to the "
+              f"{wl.num_seqs}-sequence batch by context tokens")
+    return {
+        "impl": "reference",
+        "metric": METRIC,
+        "value": value,
+        "unit": "tokens/s",
+        "n_gpus": world,
+        "steps": done,
+        "warmup": args.warmup,
+        "ms_per_step": dt / max(done, 1) * 1e3,
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "f64",
+        "data": "synthetic (seeded)",
+        "config": workload_config(wl, args.partition_size or wl.partition_size, world),
+        "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": threads, "kind": "oracle",
+                         "sample": sample},
+        "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--warmup", type=int, default=50)
+    ap.add_argument("--workload", default="llama7b_mha", choices=W.WORKLOADS)
+    ap.add_argument("--partition-size", type=int, default=0)
+    ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
+    ap.add_argument("--seed", type=int, default=0)
+    ap.add_argument("--e2e-steps", type=int, default=1000)
+    ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    ap.add_argument("--reference-seconds", type=float, default=60.0)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args(argv)
+    if args.warmup < 3:
+        ap.error("--warmup must be at least 3")
+    line = run_reference(args) if args.impl == "reference" else run_gpu(args)
+    if line is not None:
+        print(json.dumps(line), flush=True)
+    try:
+        import torch.distributed as dist
+        if dist.is_available() and dist.is_initialized():
+            dist.destroy_process_group()
+    except Exception:
+        pass
+
+
+if __name__ == "__main__":
+    main()

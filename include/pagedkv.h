@@ -1,0 +1,216 @@
+/*
+ * pagedkv.h - C ABI of the paged KV-cache decode library for GB300 (sm_103a).
+ *
+ * The library implements the decode hot path of PagedAttention as described in
+ * "PagedAttention por dentro: bloques, tabla de páginas, evicción y el estado
+ * del arte del KV cache en 2026" (sections "El modelo de bloques", "La tabla de
+ * páginas (block table)", "El pool de bloques", "Copy-on-write para sampling
+ * paralelo", "El kernel CUDA"): the K/V of every sequence live in fixed
+ * 16-token physical blocks scattered through a pool, and a per-sequence block
+ * table maps logical block j (tokens 16j .. 16j+15) to its physical block.
+ *
+ * Conventions shared by every entry point
+ * --------------------------------------
+ *  - Memory: the caller owns all memory.  Pointers documented as "device" must
+ *    point to CUDA device memory of the current device; the library allocates
+ *    nothing and keeps no pointer after a call returns.
+ *  - Streams: `stream` is a cudaStream_t passed as void* (NULL = the legacy
+ *    default stream).  Kernels are enqueued asynchronously on it; a PA_OK
+ *    return means the work was enqueued, not that it finished.
+ *  - Layouts (row-major, no padding):
+ *      key_cache, value_cache : [num_blocks][num_kv_heads][block_size][head_dim]
+ *      query, out             : [num_seqs][num_q_heads][head_dim]
+ *      block_tables           : int32 [num_seqs][max_blocks_per_seq]; only the
+ *                               first ceil(context_len / block_size) entries of
+ *                               a row are read
+ *      context_lens           : int32 [num_seqs]
+ *      key, value (new rows)  : [num_tokens][num_kv_heads][head_dim]
+ *      slot_mapping           : int64 [num_tokens]; slot = block * block_size + offset
+ *  - block_size must be 16 (the block size the pages use).
+ *  - GQA: query head h reads KV head h / (num_q_heads / num_kv_heads)
+ *    ("KV cache: la memoria de trabajo que sostiene la inferencia LLM",
+ *    section "Trucos para que el cuaderno sea más fino").
+ *  - Argument errors are detected synchronously on the host and returned as a
+ *    status; nothing is enqueued then.  Index values held in device memory
+ *    (table entries, context lengths, slots, copy pairs) are checked by the
+ *    kernels: an out-of-range value is never dereferenced; it is replaced as
+ *    each entry point documents and, when `device_status` is not NULL, the
+ *    matching PA_DEV_* bit is OR-ed into that device int32 (zero it first).
+ *  - Kernels never trap.  Every wait inside a kernel is bounded (about one
+ *    second); if one gives up, PA_DEV_TIMEOUT is set and the kernel returns.
+ */
+#ifndef PAGEDKV_H_
+#define PAGEDKV_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum pa_status {
+    PA_OK = 0,
+    PA_ERR_INVALID_ARG = 1,  /* null pointer, bad size, misaligned pointer, ... */
+    PA_ERR_UNSUPPORTED = 2,  /* valid arguments this build has no kernel for */
+    PA_ERR_CUDA = 3,         /* a CUDA call failed; see pa_last_error() */
+    PA_ERR_NO_BLOCKS = 4,    /* block manager: the pool has no free block */
+    PA_ERR_WORKSPACE = 5,    /* workspace missing or smaller than required */
+    PA_ERR_NOT_FOUND = 6     /* block manager: unknown or duplicate sequence id */
+} pa_status;
+
+typedef enum pa_dtype {
+    PA_DTYPE_F32 = 0,        /* IEEE binary32 */
+    PA_DTYPE_BF16 = 1        /* bfloat16 */
+} pa_dtype;
+
+/* Bits OR-ed into the optional device status word. */
+#define PA_DEV_BAD_BLOCK_ID    1  /* a table entry outside [0, num_blocks) */
+#define PA_DEV_BAD_CONTEXT_LEN 2  /* context_len < 0 or > max_blocks_per_seq * block_size */
+#define PA_DEV_BAD_SLOT        4  /* slot >= num_blocks * block_size */
+#define PA_DEV_BAD_COPY_PAIR   8  /* a copy pair index outside [0, num_blocks) */
+#define PA_DEV_TIMEOUT        16  /* a bounded in-kernel wait gave up */
+
+/* Human-readable name of a status. Never NULL. */
+const char *pa_status_string(pa_status status);
+
+/* Message of the last PA_ERR_CUDA on the calling thread ("" if none). */
+const char *pa_last_error(void);
+
+/* ABI version (major * 100 + minor). */
+int pa_version(void);
+
+/* Number of kernels this library has launched in this process (all threads). */
+uint64_t pa_launch_count(void);
+
+/* Partition size pa_decode uses when it is given partition_size = 0. */
+int pa_default_partition_size(void);
+
+/*
+ * Bytes of workspace pa_decode needs for the split-K partials.  Returns 0 when
+ * no sequence can span more than one partition (no workspace needed).
+ * max_blocks_per_seq bounds the context length (max_blocks_per_seq * block_size).
+ * partition_size: 0 = library default, else a multiple of 16 in [16, 16384].
+ * Returns (size_t)-1 for invalid arguments.
+ */
+size_t pa_decode_workspace_bytes(int num_seqs, int num_q_heads, int head_dim,
+                                 int max_blocks_per_seq, int block_size, int partition_size);
+
+/*
+ * Paged decode attention: for every sequence b and query head h,
+ *   out[b][h] = sum_t softmax_t(scale * <query[b][h], K_t>) * V_t
+ * over the context_lens[b] tokens of sequence b, where token t's K/V row is
+ * key_cache/value_cache[block_tables[b][t / 16]][h / group][t % 16].
+ * Source: "KV cache: la memoria de trabajo que sostiene la inferencia LLM",
+ * section "El mecanismo en sí (en cristiano)" (the attention of one new token),
+ * and "PagedAttention por dentro", sections "La tabla de páginas (block table)"
+ * and "El kernel CUDA" (the block-table indirection, processed block by block).
+ *
+ *  out, query        device, dtype elements, [num_seqs][num_q_heads][head_dim]
+ *  key_cache,
+ *  value_cache       device, dtype elements, 16-byte aligned
+ *  block_tables      device int32 [num_seqs][max_blocks_per_seq]
+ *  context_lens      device int32 [num_seqs]
+ *  head_dim          bf16: 64 or 128; f32: 32, 64, 128 or 256
+ *  num_q_heads       a multiple of num_kv_heads; bf16 needs group <= 16
+ *  scale             the softmax scale (usually 1/sqrt(head_dim))
+ *  partition_size    tokens per split-K partition: 0 = default, else a
+ *                    multiple of 16 in [16, 16384].  A sequence longer than
+ *                    one partition is processed by several CTAs whose partial
+ *                    (max, sum, output) are merged by a second kernel.
+ *  workspace         device scratch of at least pa_decode_workspace_bytes(...)
+ *                    bytes (may be NULL when that is 0), 16-byte aligned
+ *  device_status     device int32 or NULL (see PA_DEV_*)
+ * Arithmetic: fp32 accumulation; bf16 output rounded to nearest even.
+ * context_len 0 gives a zero output row.  A table entry out of range is read
+ * as block 0 and flagged; a context length out of range is clamped to
+ * [0, max_blocks_per_seq * 16] and flagged.
+ */
+pa_status pa_decode(void *out, const void *query, const void *key_cache, const void *value_cache,
+                    const int32_t *block_tables, const int32_t *context_lens, int num_seqs,
+                    int num_q_heads, int num_kv_heads, int head_dim, int block_size,
+                    int max_blocks_per_seq, int num_blocks, float scale, pa_dtype dtype,
+                    int partition_size, void *workspace, size_t workspace_bytes,
+                    int32_t *device_status, void *stream);
+
+/*
+ * Cache write: for every new token i with slot_mapping[i] >= 0, copies its K
+ * and V rows (all KV heads) into offset slot % 16 of physical block slot / 16:
+ *   key_cache[slot / 16][kvh][slot % 16][:] = key[i][kvh][:]   (same for V)
+ * Source: "PagedAttention por dentro", section "La tabla de páginas (block
+ * table)" (a new token is written into the free slot of its block).
+ *  key, value      device [num_tokens][num_kv_heads][head_dim], 16-byte aligned
+ *  slot_mapping    device int64 [num_tokens]; negative = skip (padding)
+ *  head_dim        head_dim * element size must be a multiple of 16 bytes
+ * Bit-exact copy.  Two tokens with the same slot race (one of them wins).
+ * A slot >= num_blocks * 16 is skipped and flagged.
+ */
+pa_status pa_cache_write(void *key_cache, void *value_cache, const void *key, const void *value,
+                         const int64_t *slot_mapping, int num_tokens, int num_kv_heads,
+                         int head_dim, int block_size, int num_blocks, pa_dtype dtype,
+                         int32_t *device_status, void *stream);
+
+/*
+ * Block copy for copy-on-write: for every pair p, physical block dst becomes a
+ * bit-exact copy of block src in both pools (all KV heads, all 16 slots).
+ * Source: "PagedAttention por dentro", section "Copy-on-write para sampling
+ * paralelo" (on divergence only the last shared block is copied).
+ *  src_dst     device int32 [num_pairs][2] = (src, dst)
+ * Pairs run concurrently: no dst may appear twice or equal another pair's src
+ * (the host block manager never emits such lists); src == dst is a no-op.
+ * A pair with an index out of range is skipped and flagged.
+ */
+pa_status pa_block_copy(void *key_cache, void *value_cache, const int32_t *src_dst, int num_pairs,
+                        int num_kv_heads, int head_dim, int block_size, int num_blocks,
+                        pa_dtype dtype, int32_t *device_status, void *stream);
+
+/*
+ * Host block manager: one pool of num_blocks blocks of block_size tokens,
+ * per-sequence block tables, reference counts and copy-on-write.
+ * Source: "PagedAttention por dentro", sections "La tabla de páginas (block
+ * table)" (growth rule: a sequence holding N tokens writes its next token into
+ * its last block when N mod 16 != 0, otherwise it appends a new block taken
+ * from the pool), "El pool de bloques" (one global pool) and "Copy-on-write
+ * para sampling paralelo" (forked sequences share blocks; only the shared
+ * block about to change is copied).
+ * Allocation order is deterministic: the free list is a stack that first hands
+ * out 0, 1, 2, ...; a freed block is the next one handed out; pa_bm_free_seq
+ * releases a table from its last entry to its first.
+ * Host memory only; no CUDA call.  A handle is not thread-safe.
+ * Operations that fail change nothing.
+ */
+typedef struct pa_bm pa_bm;
+
+pa_bm *pa_bm_create(int num_blocks, int block_size);   /* NULL on bad arguments */
+void pa_bm_destroy(pa_bm *bm);
+/* New sequence with room for num_tokens tokens (all or nothing). */
+pa_status pa_bm_alloc_seq(pa_bm *bm, int seq, int num_tokens);
+/* child shares every block of parent (reference counts + 1). */
+pa_status pa_bm_fork(pa_bm *bm, int parent, int child);
+/* Room for one more token: *slot receives its slot; when the last block was
+ * shared it is first copied: *cow_src / *cow_dst receive the pair, else -1. */
+pa_status pa_bm_append_slot(pa_bm *bm, int seq, int64_t *slot, int32_t *cow_src, int32_t *cow_dst);
+/* Copy-on-write of one logical block; the pair is (-1, -1) if it was private. */
+pa_status pa_bm_make_private(pa_bm *bm, int seq, int logical_block, int32_t *cow_src,
+                             int32_t *cow_dst);
+pa_status pa_bm_free_seq(pa_bm *bm, int seq);
+int pa_bm_num_free(const pa_bm *bm);
+int pa_bm_num_tokens(const pa_bm *bm, int seq);       /* -1 if unknown */
+int pa_bm_ref_count(const pa_bm *bm, int block);      /* -1 if out of range */
+/* Copies up to cap entries of seq's table to out; returns its length, -1 if unknown. */
+int pa_bm_table(const pa_bm *bm, int seq, int32_t *out, int cap);
+/* One decode step for n sequences: appends a slot to each, in order.
+ * slots [n]; cow_pairs receives up to n (src, dst) pairs, *num_cow their count.
+ * Stops at the first failure: *num_done = sequences appended before it. */
+pa_status pa_bm_append_slots(pa_bm *bm, const int32_t *seqs, int n, int64_t *slots,
+                             int32_t *cow_pairs, int *num_cow, int *num_done);
+/* Dense host block tables [n][max_blocks] (-1 past each table's end) and
+ * context lengths [n] for the listed sequences. */
+pa_status pa_bm_fill_tables(const pa_bm *bm, const int32_t *seqs, int n, int32_t *tables,
+                            int max_blocks, int32_t *context_lens);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* PAGEDKV_H_ */

@@ -1,0 +1,241 @@
+"""Paged KV-cache decode attention for GB300 (sm_103a).
+
+A thin binding over the C ABI of ``include/pagedkv.h`` (library
+``_build/libpagedkv.so``): every function here only turns torch tensors into
+pointers and sizes and calls the library; all of the computation runs in the
+library's CUDA kernels.  There is no CPU fallback.
+
+    import paged_kv_cache_100_gb300 as pkv
+    pkv.cache_write(key_cache, value_cache, k_new, v_new, slot_mapping)
+    pkv.block_copy(key_cache, value_cache, cow_pairs)
+    out = pkv.decode(query, key_cache, value_cache, block_tables, context_lens)
+
+Layouts: pools [num_blocks][num_kv_heads][16][head_dim]; query/out
+[num_seqs][num_q_heads][head_dim]; block_tables int32 [num_seqs][max_blocks];
+context_lens int32 [num_seqs]; new rows [num_tokens][num_kv_heads][head_dim];
+slot_mapping int64 [num_tokens]; copy pairs int32 [num_pairs][2].
+"""
+from __future__ import annotations
+
+import ctypes
+import math
+
+from . import _lib
+from ._lib import PagedKVError, check, lib  # noqa: F401
+
+BLOCK_SIZE = 16
+
+__all__ = ["decode", "decode_workspace_bytes", "cache_write", "block_copy", "launch_count",
+           "BlockManager", "PagedKVError", "BLOCK_SIZE", "library_path"]
+
+
+def library_path() -> str:
+    return _lib.LIB_PATH
+
+
+def _torch():
+    import torch
+    return torch
+
+
+def _dtype_code(t) -> int:
+    torch = _torch()
+    if t.dtype == torch.float32:
+        return _lib.PA_DTYPE_F32
+    if t.dtype == torch.bfloat16:
+        return _lib.PA_DTYPE_BF16
+    raise TypeError(f"unsupported element type {t.dtype} (float32 or bfloat16)")
+
+
+def _dev(t, name, dtype=None):
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    if dtype is not None and t.dtype != dtype:
+        raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
+    return t.data_ptr()
+
+
+def _stream(stream, device):
+    torch = _torch()
+    s = torch.cuda.current_stream(device) if stream is None else stream
+    return ctypes.c_void_p(s.cuda_stream)
+
+
+def _status_ptr(status):
+    torch = _torch()
+    if status is None:
+        return None
+    _dev(status, "status", torch.int32)
+    return status.data_ptr()
+
+
+def launch_count() -> int:
+    """Kernels the library has launched in this process."""
+    return int(lib().pa_launch_count())
+
+
+def decode_workspace_bytes(num_seqs, num_q_heads, head_dim, max_blocks_per_seq,
+                           partition_size=0) -> int:
+    n = lib().pa_decode_workspace_bytes(num_seqs, num_q_heads, head_dim, max_blocks_per_seq,
+                                        BLOCK_SIZE, partition_size)
+    if n == ctypes.c_size_t(-1).value:
+        raise ValueError("invalid arguments for pa_decode_workspace_bytes")
+    return int(n)
+
+
+def decode(query, key_cache, value_cache, block_tables, context_lens, scale=None, *, out=None,
+           partition_size=0, workspace=None, status=None, stream=None):
+    """Paged decode attention (``pa_decode``); returns ``out``."""
+    torch = _torch()
+    B, Hq, D = query.shape
+    NB, Hkv, BS, D2 = key_cache.shape
+    if BS != BLOCK_SIZE or D2 != D or tuple(value_cache.shape) != tuple(key_cache.shape):
+        raise ValueError("pools must be [num_blocks][num_kv_heads][16][head_dim] like query")
+    if block_tables.dim() != 2 or block_tables.shape[0] != B or tuple(context_lens.shape) != (B,):
+        raise ValueError("block_tables must be [num_seqs][max_blocks], context_lens [num_seqs]")
+    code = _dtype_code(query)
+    if key_cache.dtype != query.dtype or value_cache.dtype != query.dtype:
+        raise TypeError("query and pools must share one element type")
+    if scale is None:
+        scale = 1.0 / math.sqrt(D)
+    if out is None:
+        out = torch.empty_like(query)
+    elif out.shape != query.shape or out.dtype != query.dtype:
+        raise ValueError("out must match query")
+    max_blocks = block_tables.shape[1]
+    need = decode_workspace_bytes(B, Hq, D, max_blocks, partition_size)
+    ws_ptr, ws_bytes = None, 0
+    if need > 0:
+        if workspace is None:
+            workspace = torch.empty(need, dtype=torch.uint8, device=query.device)
+        ws_ptr = _dev(workspace, "workspace")
+        ws_bytes = workspace.numel() * workspace.element_size()
+    rc = lib().pa_decode(
+        _dev(out, "out"), _dev(query, "query"), _dev(key_cache, "key_cache"),
+        _dev(value_cache, "value_cache"), _dev(block_tables, "block_tables", torch.int32),
+        _dev(context_lens, "context_lens", torch.int32), B, Hq, Hkv, D, BLOCK_SIZE, max_blocks,
+        NB, float(scale), code, int(partition_size), ws_ptr, ws_bytes, _status_ptr(status),
+        _stream(stream, query.device))
+    check(rc, "pa_decode")
+    return out
+
+
+def cache_write(key_cache, value_cache, key, value, slot_mapping, *, status=None, stream=None):
+    """Scatter new tokens' K/V rows into their slots (``pa_cache_write``)."""
+    torch = _torch()
+    NB, Hkv, BS, D = key_cache.shape
+    T = slot_mapping.shape[0]
+    if tuple(key.shape) != (T, Hkv, D) or tuple(value.shape) != (T, Hkv, D):
+        raise ValueError("key/value must be [num_tokens][num_kv_heads][head_dim]")
+    code = _dtype_code(key_cache)
+    for t, n in ((value_cache, "value_cache"), (key, "key"), (value, "value")):
+        if t.dtype != key_cache.dtype:
+            raise TypeError(f"{n} must be {key_cache.dtype}")
+    rc = lib().pa_cache_write(
+        _dev(key_cache, "key_cache"), _dev(value_cache, "value_cache"), _dev(key, "key"),
+        _dev(value, "value"), _dev(slot_mapping, "slot_mapping", torch.int64), T, Hkv, D, BS, NB,
+        code, _status_ptr(status), _stream(stream, key_cache.device))
+    check(rc, "pa_cache_write")
+
+
+def block_copy(key_cache, value_cache, src_dst, *, status=None, stream=None):
+    """Copy whole physical blocks (copy-on-write pairs) in both pools (``pa_block_copy``)."""
+    torch = _torch()
+    NB, Hkv, BS, D = key_cache.shape
+    P = src_dst.shape[0]
+    if src_dst.dim() != 2 or src_dst.shape[1] != 2:
+        raise ValueError("src_dst must be [num_pairs][2]")
+    rc = lib().pa_block_copy(
+        _dev(key_cache, "key_cache"), _dev(value_cache, "value_cache"),
+        _dev(src_dst, "src_dst", torch.int32), P, Hkv, D, BS, NB, _dtype_code(key_cache),
+        _status_ptr(status), _stream(stream, key_cache.device))
+    check(rc, "pa_block_copy")
+
+
+class BlockManager:
+    """Host block manager (``pa_bm_*``): pool, block tables, ref counts, copy-on-write."""
+
+    def __init__(self, num_blocks: int, block_size: int = BLOCK_SIZE):
+        self._h = lib().pa_bm_create(num_blocks, block_size)
+        if not self._h:
+            raise ValueError("bad pool geometry")
+        self.num_blocks = num_blocks
+        self.block_size = block_size
+
+    def close(self):
+        if self._h:
+            lib().pa_bm_destroy(self._h)
+            self._h = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+    def alloc_seq(self, seq: int, num_tokens: int) -> None:
+        check(lib().pa_bm_alloc_seq(self._h, seq, num_tokens), "pa_bm_alloc_seq")
+
+    def fork(self, parent: int, child: int) -> None:
+        check(lib().pa_bm_fork(self._h, parent, child), "pa_bm_fork")
+
+    def append_slot(self, seq: int):
+        slot, src, dst = ctypes.c_int64(), ctypes.c_int32(), ctypes.c_int32()
+        check(lib().pa_bm_append_slot(self._h, seq, ctypes.byref(slot), ctypes.byref(src),
+                                      ctypes.byref(dst)), "pa_bm_append_slot")
+        return slot.value, (None if src.value < 0 else (src.value, dst.value))
+
+    def make_private(self, seq: int, logical_block: int):
+        src, dst = ctypes.c_int32(), ctypes.c_int32()
+        check(lib().pa_bm_make_private(self._h, seq, logical_block, ctypes.byref(src),
+                                       ctypes.byref(dst)), "pa_bm_make_private")
+        return None if src.value < 0 else (src.value, dst.value)
+
+    def free_seq(self, seq: int) -> None:
+        check(lib().pa_bm_free_seq(self._h, seq), "pa_bm_free_seq")
+
+    def num_free(self) -> int:
+        return int(lib().pa_bm_num_free(self._h))
+
+    def num_tokens(self, seq: int) -> int:
+        n = lib().pa_bm_num_tokens(self._h, seq)
+        if n < 0:
+            raise KeyError(seq)
+        return int(n)
+
+    def ref_count(self, block: int) -> int:
+        return int(lib().pa_bm_ref_count(self._h, block))
+
+    def table(self, seq: int) -> list:
+        n = lib().pa_bm_table(self._h, seq, None, 0)
+        if n < 0:
+            raise KeyError(seq)
+        buf = (ctypes.c_int32 * max(n, 1))()
+        lib().pa_bm_table(self._h, seq, ctypes.cast(buf, ctypes.c_void_p), n)
+        return list(buf[:n])
+
+    def append_slots(self, seqs):
+        """One decode step: returns (slots int64 [n], cow pairs int32 [k][2]) as numpy arrays."""
+        import numpy as np
+        seqs = np.ascontiguousarray(seqs, dtype=np.int32)
+        n = seqs.shape[0]
+        slots = np.empty(n, dtype=np.int64)
+        pairs = np.empty((max(n, 1), 2), dtype=np.int32)
+        ncow, ndone = ctypes.c_int(), ctypes.c_int()
+        rc = lib().pa_bm_append_slots(self._h, seqs.ctypes.data, n, slots.ctypes.data,
+                                      pairs.ctypes.data, ctypes.byref(ncow), ctypes.byref(ndone))
+        check(rc, f"pa_bm_append_slots (done {ndone.value} of {n})")
+        return slots, pairs[:ncow.value].copy()
+
+    def fill_tables(self, seqs, max_blocks: int):
+        """Dense block tables [n][max_blocks] (-1 padded) and context lengths [n] (numpy)."""
+        import numpy as np
+        seqs = np.ascontiguousarray(seqs, dtype=np.int32)
+        n = seqs.shape[0]
+        tables = np.empty((n, max_blocks), dtype=np.int32)
+        lens = np.empty(n, dtype=np.int32)
+        check(lib().pa_bm_fill_tables(self._h, seqs.ctypes.data, n, tables.ctypes.data,
+                                      max_blocks, lens.ctypes.data), "pa_bm_fill_tables")
+        return tables, lens

@@ -1,0 +1,187 @@
+// Cache write and copy-on-write block copy, plus the library's small ABI helpers.
+//
+// Cache write ("PagedAttention por dentro", section "La tabla de páginas
+// (block table)"): the new token of a sequence goes into the free slot of its
+// last block, or into the first slot of a freshly appended block; the host
+// block manager turns that rule into one slot per token, and this kernel
+// scatters each token's K/V rows there.
+//
+// Block copy (same page, section "Copy-on-write para sampling paralelo"): when
+// a sequence is about to modify a block it shares, only that block is copied.
+//
+// Both are pure bandwidth kernels: 16-byte vector loads and stores, one thread
+// per 16-byte chunk, index checks before every access.
+#include <cuda_runtime.h>
+
+#include <atomic>
+#include <cstdio>
+#include <cstring>
+
+#include "pa_device.cuh"
+#include "pa_internal.h"
+
+namespace pa {
+
+namespace {
+
+std::atomic<uint64_t> g_launches{0};
+thread_local char g_last_error[256] = "";
+
+// One thread per 16-byte chunk of one (token, KV head) row of K and of V.
+__global__ void __launch_bounds__(256)
+pa_cache_write_kernel(uint4 *__restrict__ kc, uint4 *__restrict__ vc,
+                      const uint4 *__restrict__ key, const uint4 *__restrict__ value,
+                      const int64_t *__restrict__ slot_mapping, int num_tokens, int num_kv_heads,
+                      int chunks_per_row, int num_blocks, int32_t *status) {
+    const int64_t idx = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+    const int64_t per_token = (int64_t)num_kv_heads * chunks_per_row;
+    if (idx >= (int64_t)num_tokens * per_token) return;
+    const int64_t i = idx / per_token;
+    const int64_t rem = idx - i * per_token;          // kvh * chunks_per_row + chunk
+    const int64_t slot = slot_mapping[i];
+    if (slot < 0) return;
+    if (slot >= (int64_t)num_blocks * kBlockSize) {
+        if (rem == 0) report(status, PA_DEV_BAD_SLOT);
+        return;
+    }
+    const int64_t blk = slot / kBlockSize;
+    const int64_t off = slot - blk * kBlockSize;
+    const int64_t kvh = rem / chunks_per_row;
+    const int64_t ch = rem - kvh * chunks_per_row;
+    const int64_t dst = ((blk * num_kv_heads + kvh) * kBlockSize + off) * chunks_per_row + ch;
+    kc[dst] = key[idx];
+    vc[dst] = value[idx];
+}
+
+// grid.x = pair, grid.y = slice of the block; every thread copies up to
+// kChunksPerThread 16-byte chunks of K and of V.
+constexpr int kCopyThreads = 256;
+constexpr int kChunksPerThread = 4;
+
+__global__ void __launch_bounds__(kCopyThreads)
+pa_block_copy_kernel(uint4 *__restrict__ kc, uint4 *__restrict__ vc,
+                     const int32_t *__restrict__ src_dst, int64_t chunks_per_block, int num_blocks,
+                     int32_t *status) {
+    const int32_t src = src_dst[2 * blockIdx.x];
+    const int32_t dst = src_dst[2 * blockIdx.x + 1];
+    if ((unsigned)src >= (unsigned)num_blocks || (unsigned)dst >= (unsigned)num_blocks) {
+        if (blockIdx.y == 0 && threadIdx.x == 0) report(status, PA_DEV_BAD_COPY_PAIR);
+        return;
+    }
+    if (src == dst) return;
+    const int64_t first = (int64_t)blockIdx.y * kCopyThreads * kChunksPerThread + threadIdx.x;
+    const uint4 *ks = kc + (int64_t)src * chunks_per_block;
+    const uint4 *vs = vc + (int64_t)src * chunks_per_block;
+    uint4 *kd = kc + (int64_t)dst * chunks_per_block;
+    uint4 *vd = vc + (int64_t)dst * chunks_per_block;
+    uint4 kb[kChunksPerThread], vb[kChunksPerThread];
+#pragma unroll
+    for (int u = 0; u < kChunksPerThread; ++u) {
+        const int64_t c = first + (int64_t)u * kCopyThreads;
+        if (c < chunks_per_block) {
+            kb[u] = ks[c];
+            vb[u] = vs[c];
+        }
+    }
+#pragma unroll
+    for (int u = 0; u < kChunksPerThread; ++u) {
+        const int64_t c = first + (int64_t)u * kCopyThreads;
+        if (c < chunks_per_block) {
+            kd[c] = kb[u];
+            vd[c] = vb[u];
+        }
+    }
+}
+
+int elem_bytes(pa_dtype dtype) { return dtype == PA_DTYPE_F32 ? 4 : 2; }
+
+}  // namespace
+
+void count_launches(uint64_t n) { g_launches.fetch_add(n, std::memory_order_relaxed); }
+
+pa_status cuda_failure(cudaError_t err, const char *where) {
+    std::snprintf(g_last_error, sizeof g_last_error, "%s: %s (%d)", where, cudaGetErrorString(err),
+                  (int)err);
+    return PA_ERR_CUDA;
+}
+
+}  // namespace pa
+
+using namespace pa;
+
+extern "C" const char *pa_status_string(pa_status status) {
+    switch (status) {
+    case PA_OK: return "PA_OK";
+    case PA_ERR_INVALID_ARG: return "PA_ERR_INVALID_ARG";
+    case PA_ERR_UNSUPPORTED: return "PA_ERR_UNSUPPORTED";
+    case PA_ERR_CUDA: return "PA_ERR_CUDA";
+    case PA_ERR_NO_BLOCKS: return "PA_ERR_NO_BLOCKS";
+    case PA_ERR_WORKSPACE: return "PA_ERR_WORKSPACE";
+    case PA_ERR_NOT_FOUND: return "PA_ERR_NOT_FOUND";
+    default: return "PA_ERR_UNKNOWN";
+    }
+}
+
+extern "C" const char *pa_last_error(void) { return g_last_error; }
+
+extern "C" int pa_version(void) { return 100; }
+
+extern "C" uint64_t pa_launch_count(void) { return g_launches.load(std::memory_order_relaxed); }
+
+extern "C" pa_status pa_cache_write(void *key_cache, void *value_cache, const void *key,
+                                    const void *value, const int64_t *slot_mapping, int num_tokens,
+                                    int num_kv_heads, int head_dim, int block_size, int num_blocks,
+                                    pa_dtype dtype, int32_t *device_status, void *stream) {
+    if (num_tokens < 0 || num_kv_heads <= 0 || head_dim <= 0 || block_size != kBlockSize ||
+        num_blocks <= 0)
+        return PA_ERR_INVALID_ARG;
+    if (dtype != PA_DTYPE_F32 && dtype != PA_DTYPE_BF16) return PA_ERR_INVALID_ARG;
+    const int row_bytes = head_dim * elem_bytes(dtype);
+    if (row_bytes % 16 != 0) return PA_ERR_UNSUPPORTED;
+    if (num_tokens == 0) return PA_OK;
+    if (!key_cache || !value_cache || !key || !value || !slot_mapping) return PA_ERR_INVALID_ARG;
+    if (!aligned16(key_cache) || !aligned16(value_cache) || !aligned16(key) || !aligned16(value) ||
+        (reinterpret_cast<uintptr_t>(slot_mapping) & 7u))
+        return PA_ERR_INVALID_ARG;
+    const int chunks = row_bytes / 16;
+    const int64_t total = (int64_t)num_tokens * num_kv_heads * chunks;
+    const int64_t grid = (total + 255) / 256;
+    if (grid >= ((int64_t)1 << 31)) return PA_ERR_UNSUPPORTED;
+    pa_cache_write_kernel<<<(unsigned)grid, 256, 0, static_cast<cudaStream_t>(stream)>>>(
+        static_cast<uint4 *>(key_cache), static_cast<uint4 *>(value_cache),
+        static_cast<const uint4 *>(key), static_cast<const uint4 *>(value), slot_mapping,
+        num_tokens, num_kv_heads, chunks, num_blocks, device_status);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return cuda_failure(e, "pa_cache_write_kernel launch");
+    count_launches(1);
+    return PA_OK;
+}
+
+extern "C" pa_status pa_block_copy(void *key_cache, void *value_cache, const int32_t *src_dst,
+                                   int num_pairs, int num_kv_heads, int head_dim, int block_size,
+                                   int num_blocks, pa_dtype dtype, int32_t *device_status,
+                                   void *stream) {
+    if (num_pairs < 0 || num_kv_heads <= 0 || head_dim <= 0 || block_size != kBlockSize ||
+        num_blocks <= 0)
+        return PA_ERR_INVALID_ARG;
+    if (dtype != PA_DTYPE_F32 && dtype != PA_DTYPE_BF16) return PA_ERR_INVALID_ARG;
+    const int64_t block_bytes = (int64_t)num_kv_heads * kBlockSize * head_dim * elem_bytes(dtype);
+    if (block_bytes % 16 != 0) return PA_ERR_UNSUPPORTED;
+    if (num_pairs == 0) return PA_OK;
+    if (!key_cache || !value_cache || !src_dst) return PA_ERR_INVALID_ARG;
+    if (!aligned16(key_cache) || !aligned16(value_cache) ||
+        (reinterpret_cast<uintptr_t>(src_dst) & 3u))
+        return PA_ERR_INVALID_ARG;
+    const int64_t chunks = block_bytes / 16;
+    const int64_t per_cta = (int64_t)kCopyThreads * kChunksPerThread;
+    const int64_t slices = (chunks + per_cta - 1) / per_cta;
+    if (slices > 65535) return PA_ERR_UNSUPPORTED;
+    dim3 grid((unsigned)num_pairs, (unsigned)slices);
+    pa_block_copy_kernel<<<grid, kCopyThreads, 0, static_cast<cudaStream_t>(stream)>>>(
+        static_cast<uint4 *>(key_cache), static_cast<uint4 *>(value_cache), src_dst, chunks,
+        num_blocks, device_status);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return cuda_failure(e, "pa_block_copy_kernel launch");
+    count_launches(1);
+    return PA_OK;
+}

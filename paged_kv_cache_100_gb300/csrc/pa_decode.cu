@@ -1,0 +1,875 @@
+// Paged decode attention for GB300 (sm_103a).
+//
+// What is computed ("KV cache: la memoria de trabajo que sostiene la inferencia
+// LLM", section "El mecanismo en sí (en cristiano)"): the new token's query is
+// multiplied against the keys of every context token, normalised with a
+// softmax and used to weight the values.  Where the keys and values live
+// ("PagedAttention por dentro", sections "La tabla de páginas (block table)"
+// and "El kernel CUDA"): in 16-token physical blocks found through the
+// sequence's block table, processed block by block.
+//
+// Work decomposition.  One CTA handles one (sequence, KV head, partition),
+// where a partition is a run of `partition_size` logical tokens (split-K).
+// Each warp of the CTA owns every NW-th block of the partition and runs its
+// own TMA pipeline: lane 0 issues tiled tensor loads of the block's K and V
+// tiles (16 rows x head_dim, 128-byte swizzled) into a ring of STAGES shared
+// memory slots, completion is tracked by one mbarrier per slot, and the warp
+// consumes the slots in order with an online (running max / running sum)
+// softmax in fp32.  At the end the warps' states are merged in shared memory;
+// a sequence that fits in one partition is written directly, otherwise the
+// partition's (max, sum, unnormalised output) go to the workspace and a second
+// kernel merges the partitions.
+//
+// Consumers:
+//   * MHA (one query head per KV head): CUDA-core fp32 FMAs.  Each lane owns
+//     8 head-dim elements of half (D=128) or a quarter (D=64) of the block's
+//     rows; dot products are finished with a butterfly reduction that leaves
+//     one row's score per lane pair.
+//   * GQA (2..16 query heads share a KV head): the group makes Q.K^T and P.V
+//     dense 16-row tiles, so they run on the tensor cores (mma.sync m16n8k16,
+//     bf16 in, fp32 accumulate); query heads are the M rows, tokens and
+//     head-dim elements the N/K dimensions.  One K/V pass serves the group
+//     ("Trucos para que el cuaderno sea más fino": query heads share K/V).
+//   * fp32 caches: a plain CUDA-core kernel, one query head per CTA.
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <cudaTypedefs.h>
+#include <math.h>
+
+#include <atomic>
+#include <mutex>
+
+#include "pa_device.cuh"
+#include "pa_internal.h"
+
+namespace pa {
+
+namespace {
+
+constexpr uint32_t kFull = 0xffffffffu;
+constexpr float kLog2e = 1.4426950408889634f;
+
+struct DecodeArgs {
+    void *out;
+    const void *query;
+    const int32_t *block_tables;
+    const int32_t *context_lens;
+    float *part_o;      // [rows][head_dim], rows = (b * Hq + h) * max_parts + part
+    float2 *part_ml;    // [rows] = (running max in log2 units, running sum)
+    int32_t *status;
+    int num_seqs;
+    int num_q_heads;
+    int num_kv_heads;
+    int max_blocks;     // block-table row length
+    int num_blocks;     // pool size
+    int part_blocks;    // partition size in blocks
+    int max_parts;      // partitions of the longest possible context
+    float scale_log2;   // softmax scale * log2(e)
+};
+
+// The (sequence, head, partition) a CTA works on, with its token range.
+struct Work {
+    int b, head, part;
+    int L;          // context length (clamped)
+    int nparts;     // partitions of this sequence (1 when L == 0)
+    int blk0;       // first logical block of the partition
+    int nblk;       // blocks in the partition
+};
+
+__device__ __forceinline__ bool cta_work(const DecodeArgs &a, int heads_axis, Work &w) {
+    int idx = blockIdx.x;
+    w.part = idx % a.max_parts;
+    idx /= a.max_parts;
+    w.head = idx % heads_axis;
+    w.b = idx / heads_axis;
+    int L = a.context_lens[w.b];
+    const int lmax = a.max_blocks * kBlockSize;
+    if (L < 0 || L > lmax) {
+        if (threadIdx.x == 0 && w.part == 0 && w.head == 0) report(a.status, PA_DEV_BAD_CONTEXT_LEN);
+        L = L < 0 ? 0 : lmax;
+    }
+    w.L = L;
+    const int seq_blocks = (L + kBlockSize - 1) / kBlockSize;
+    w.nparts = seq_blocks == 0 ? 1 : (seq_blocks + a.part_blocks - 1) / a.part_blocks;
+    if (w.part >= w.nparts) return false;
+    w.blk0 = w.part * a.part_blocks;
+    const int end = min(w.blk0 + a.part_blocks, seq_blocks);
+    w.nblk = max(end - w.blk0, 0);
+    return true;
+}
+
+template <typename T>
+__device__ __forceinline__ void store_out(T *p, float v);
+template <>
+__device__ __forceinline__ void store_out<float>(float *p, float v) { *p = v; }
+template <>
+__device__ __forceinline__ void store_out<__nv_bfloat16>(__nv_bfloat16 *p, float v) {
+    *p = __float2bfloat16_rn(v);
+}
+
+// Merges the NW per-warp states of a CTA (rows x D accumulators in shared
+// memory, one (max, sum) per row and warp) and writes either the final output
+// (single partition) or the partition's partial state.
+template <typename OutT, int NW>
+__device__ __forceinline__ void merge_and_store(const DecodeArgs &a, const Work &w, int first_head,
+                                                int rows, int D, const float *acc_base,
+                                                int acc_warp_stride, const float *s_m,
+                                                const float *s_l, int row_stride) {
+    for (int idx = threadIdx.x; idx < rows * D; idx += NW * 32) {
+        const int r = idx / D;
+        const int d = idx - r * D;
+        float M = -INFINITY;
+#pragma unroll
+        for (int k = 0; k < NW; ++k) M = fmaxf(M, s_m[k * row_stride + r]);
+        float O = 0.f, Lsum = 0.f;
+#pragma unroll
+        for (int k = 0; k < NW; ++k) {
+            const float mk = s_m[k * row_stride + r];
+            const float wk = (mk == -INFINITY) ? 0.f : exp2f(mk - M);
+            Lsum += wk * s_l[k * row_stride + r];
+            O += wk * acc_base[k * acc_warp_stride + r * D + d];
+        }
+        const int h = first_head + r;
+        if (w.nparts == 1) {
+            OutT *out = static_cast<OutT *>(a.out) + ((size_t)w.b * a.num_q_heads + h) * D + d;
+            store_out<OutT>(out, Lsum > 0.f ? O / Lsum : 0.f);
+        } else {
+            const size_t row = ((size_t)w.b * a.num_q_heads + h) * a.max_parts + w.part;
+            a.part_o[row * D + d] = O;
+            if (d == 0) a.part_ml[row] = make_float2(M, Lsum);
+        }
+    }
+}
+
+// ---------------------------------------------------------------------------
+// Consumers for bf16 tiles staged by TMA with 128-byte swizzle.  A tile of one
+// block is 16 rows x D bf16, stored as D/64 sub-tiles of [16][64] (2 KiB each);
+// 16-byte chunk c of row r of a sub-tile sits at chunk (c ^ (r & 7)).
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ uint32_t swz(uint32_t tile, int row, int chunk) {
+    return tile + (uint32_t)((chunk >> 3) * 2048 + row * 128 + (((chunk & 7) ^ (row & 7)) << 4));
+}
+
+__device__ __forceinline__ uint4 lds128(uint32_t addr) {
+    uint4 v;
+    asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+                 : "r"(addr));
+    return v;
+}
+
+__device__ __forceinline__ float dot8(const float (&q)[8], uint4 k) {
+    float s = q[0] * bf16lo(k.x);
+    s = fmaf(q[1], bf16hi(k.x), s);
+    s = fmaf(q[2], bf16lo(k.y), s);
+    s = fmaf(q[3], bf16hi(k.y), s);
+    s = fmaf(q[4], bf16lo(k.z), s);
+    s = fmaf(q[5], bf16hi(k.z), s);
+    s = fmaf(q[6], bf16lo(k.w), s);
+    s = fmaf(q[7], bf16hi(k.w), s);
+    return s;
+}
+
+__device__ __forceinline__ void axpy8(float (&acc)[8], float p, uint4 v) {
+    acc[0] = fmaf(p, bf16lo(v.x), acc[0]);
+    acc[1] = fmaf(p, bf16hi(v.x), acc[1]);
+    acc[2] = fmaf(p, bf16lo(v.y), acc[2]);
+    acc[3] = fmaf(p, bf16hi(v.y), acc[3]);
+    acc[4] = fmaf(p, bf16lo(v.z), acc[4]);
+    acc[5] = fmaf(p, bf16hi(v.z), acc[5]);
+    acc[6] = fmaf(p, bf16lo(v.w), acc[6]);
+    acc[7] = fmaf(p, bf16hi(v.w), acc[7]);
+}
+
+// One query head per KV head.  Lane layout: chunk c = lane % CH owns head-dim
+// elements [8c, 8c+8); row group rg = lane / CH owns rows [rg*RPL, rg*RPL+RPL).
+template <int D>
+struct MhaConsumer {
+    static constexpr int CH = D / 8;
+    static constexpr int RG = 32 / CH;
+    static constexpr int RPL = 16 / RG;
+    static constexpr int ROWS = 1;     // query heads per warp state
+    static_assert(RPL * 2 == CH, "lane layout");
+
+    float q[8];
+    float acc[8];
+    float m, l;
+    int lane, c, rg;
+
+    __device__ __forceinline__ void init(const DecodeArgs &a, const Work &w, int lane_) {
+        lane = lane_;
+        c = lane & (CH - 1);
+        rg = lane / CH;
+        const __nv_bfloat16 *qrow =
+            static_cast<const __nv_bfloat16 *>(a.query) + ((size_t)w.b * a.num_q_heads + w.head) * D;
+        const uint4 raw = *reinterpret_cast<const uint4 *>(qrow + 8 * c);
+        const uint32_t words[4] = {raw.x, raw.y, raw.z, raw.w};
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+            q[2 * e] = bf16lo(words[e]) * a.scale_log2;
+            q[2 * e + 1] = bf16hi(words[e]) * a.scale_log2;
+        }
+#pragma unroll
+        for (int e = 0; e < 8; ++e) acc[e] = 0.f;
+        m = -INFINITY;
+        l = 0.f;
+    }
+
+    __device__ __forceinline__ void block(uint32_t ktile, uint32_t vtile, int nvalid) {
+        float v[RPL];
+#pragma unroll
+        for (int i = 0; i < RPL; ++i) v[i] = dot8(q, lds128(swz(ktile, rg * RPL + i, c)));
+        // Butterfly: after the step with mask M a lane keeps the half of its
+        // values selected by (lane & M); the last step (mask 1) completes the sum.
+#pragma unroll
+        for (int M = CH / 2, n = RPL; M >= 2; M >>= 1, n >>= 1) {
+            const bool upper = (lane & M) != 0;
+#pragma unroll
+            for (int k = 0; k < n / 2; ++k) {
+                const float send = upper ? v[k] : v[k + n / 2];
+                const float keep = upper ? v[k + n / 2] : v[k];
+                v[k] = keep + __shfl_xor_sync(kFull, send, M);
+            }
+        }
+        float s = v[0] + __shfl_xor_sync(kFull, v[0], 1);
+        const int row = rg * RPL + ((lane & (CH - 1)) >> 1);
+        s = row < nvalid ? s : -INFINITY;
+        float bmax = s;
+#pragma unroll
+        for (int M = 2; M < 32; M <<= 1) bmax = fmaxf(bmax, __shfl_xor_sync(kFull, bmax, M));
+        const float m_new = fmaxf(m, bmax);
+        const float alpha = exp2f(m - m_new);
+        const float p = exp2f(s - m_new);
+        l = l * alpha + ((lane & 1) ? 0.f : p);
+        m = m_new;
+#pragma unroll
+        for (int e = 0; e < 8; ++e) acc[e] *= alpha;
+#pragma unroll
+        for (int i = 0; i < RPL; ++i) {
+            const int r = rg * RPL + i;
+            const float pr = __shfl_sync(kFull, p, rg * CH + 2 * i);
+            const uint4 vv = lds128(swz(vtile, r, c));
+            if (r < nvalid) axpy8(acc, pr, vv);
+        }
+    }
+
+    // Writes this warp's state: acc[ROWS][D] floats at `acc_out`, (m, l) per row.
+    __device__ __forceinline__ void finish(float *acc_out, float *m_out, float *l_out) {
+#pragma unroll
+        for (int M = CH; M < 32; M <<= 1)
+#pragma unroll
+            for (int e = 0; e < 8; ++e) acc[e] += __shfl_xor_sync(kFull, acc[e], M);
+#pragma unroll
+        for (int M = 1; M < 32; M <<= 1) l += __shfl_xor_sync(kFull, l, M);
+        if (lane < CH) {
+            float4 *dst = reinterpret_cast<float4 *>(acc_out + 8 * c);
+            dst[0] = make_float4(acc[0], acc[1], acc[2], acc[3]);
+            dst[1] = make_float4(acc[4], acc[5], acc[6], acc[7]);
+        }
+        if (lane == 0) {
+            m_out[0] = m;
+            l_out[0] = l;
+        }
+    }
+};
+
+// 2..16 query heads per KV head on the tensor cores.  Fragment owner:
+// g = lane / 4 (query-head row g and g + 8), t = lane % 4.
+template <int D, int G>
+struct GqaConsumer {
+    static constexpr int KS = D / 16;   // k-steps of Q.K^T
+    static constexpr int NT = D / 8;    // n-tiles of P.V
+    static constexpr bool HI = G > 8;   // rows 8..15 hold real heads
+    static constexpr int ROWS = G;
+
+    uint32_t qa[KS][4];
+    float o[NT][4];
+    float m0, m1, l0, l1;
+    float scale_log2;
+    int lane, g, t;
+
+    __device__ __forceinline__ void init(const DecodeArgs &a, const Work &w, int lane_) {
+        lane = lane_;
+        g = lane >> 2;
+        t = lane & 3;
+        scale_log2 = a.scale_log2;
+        const __nv_bfloat16 *qg = static_cast<const __nv_bfloat16 *>(a.query) +
+                                  ((size_t)w.b * a.num_q_heads + (size_t)w.head * G) * D;
+        const uint32_t *q0 = reinterpret_cast<const uint32_t *>(qg + (size_t)g * D);
+        const uint32_t *q1 = reinterpret_cast<const uint32_t *>(qg + (size_t)(g + 8) * D);
+#pragma unroll
+        for (int ks = 0; ks < KS; ++ks) {
+            const bool r0 = g < G, r1 = HI && (g + 8 < G);
+            qa[ks][0] = r0 ? q0[(16 * ks + 2 * t) / 2] : 0u;
+            qa[ks][2] = r0 ? q0[(16 * ks + 8 + 2 * t) / 2] : 0u;
+            qa[ks][1] = r1 ? q1[(16 * ks + 2 * t) / 2] : 0u;
+            qa[ks][3] = r1 ? q1[(16 * ks + 8 + 2 * t) / 2] : 0u;
+        }
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt) o[nt][0] = o[nt][1] = o[nt][2] = o[nt][3] = 0.f;
+        m0 = m1 = -INFINITY;
+        l0 = l1 = 0.f;
+    }
+
+    __device__ __forceinline__ void block(uint32_t ktile, uint32_t vtile, int nvalid) {
+        float s[2][4];
+#pragma unroll
+        for (int j = 0; j < 2; ++j) s[j][0] = s[j][1] = s[j][2] = s[j][3] = 0.f;
+        const int mi = lane >> 3, rr = lane & 7;
+#pragma unroll
+        for (int kk = 0; kk < D / 32; ++kk) {
+#pragma unroll
+            for (int j = 0; j < 2; ++j) {
+                uint32_t b[4];
+                ldsm_x4(b, swz(ktile, 8 * j + rr, 4 * kk + mi));
+                mma_bf16_16816(s[j], qa[2 * kk], b[0], b[1]);
+                mma_bf16_16816(s[j], qa[2 * kk + 1], b[2], b[3]);
+            }
+        }
+#pragma unroll
+        for (int j = 0; j < 2; ++j)
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                const int tok = 8 * j + 2 * t + (e & 1);
+                s[j][e] = tok < nvalid ? s[j][e] * scale_log2 : -INFINITY;
+            }
+        float mx0 = fmaxf(fmaxf(s[0][0], s[0][1]), fmaxf(s[1][0], s[1][1]));
+        mx0 = fmaxf(mx0, __shfl_xor_sync(kFull, mx0, 1));
+        mx0 = fmaxf(mx0, __shfl_xor_sync(kFull, mx0, 2));
+        const float mn0 = fmaxf(m0, mx0);
+        const float a0 = exp2f(m0 - mn0);
+        m0 = mn0;
+        float mn1 = 0.f, a1 = 1.f;
+        if (HI) {
+            float mx1 = fmaxf(fmaxf(s[0][2], s[0][3]), fmaxf(s[1][2], s[1][3]));
+            mx1 = fmaxf(mx1, __shfl_xor_sync(kFull, mx1, 1));
+            mx1 = fmaxf(mx1, __shfl_xor_sync(kFull, mx1, 2));
+            mn1 = fmaxf(m1, mx1);
+            a1 = exp2f(m1 - mn1);
+            m1 = mn1;
+        }
+        float p[2][4];
+#pragma unroll
+        for (int j = 0; j < 2; ++j) {
+            p[j][0] = exp2f(s[j][0] - mn0);
+            p[j][1] = exp2f(s[j][1] - mn0);
+            p[j][2] = HI ? exp2f(s[j][2] - mn1) : 0.f;
+            p[j][3] = HI ? exp2f(s[j][3] - mn1) : 0.f;
+        }
+        l0 = l0 * a0 + (p[0][0] + p[0][1]) + (p[1][0] + p[1][1]);
+        if (HI) l1 = l1 * a1 + (p[0][2] + p[0][3]) + (p[1][2] + p[1][3]);
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt) {
+            o[nt][0] *= a0;
+            o[nt][1] *= a0;
+            if (HI) {
+                o[nt][2] *= a1;
+                o[nt][3] *= a1;
+            }
+        }
+        uint32_t pa[4];
+        pa[0] = pack_bf16x2(p[0][0], p[0][1]);
+        pa[1] = HI ? pack_bf16x2(p[0][2], p[0][3]) : 0u;
+        pa[2] = pack_bf16x2(p[1][0], p[1][1]);
+        pa[3] = HI ? pack_bf16x2(p[1][2], p[1][3]) : 0u;
+        if (nvalid < 16) {
+            // Rows past the context may hold anything (even NaN): zero them so
+            // that 0 * row stays 0 in the tensor-core sum.
+            const int zrows = 16 - nvalid;
+            for (int i = lane; i < zrows * (D / 8); i += 32) {
+                const int r = nvalid + i / (D / 8);
+                const int ch = i % (D / 8);
+                asm volatile("st.shared.v4.u32 [%0], {%1, %1, %1, %1};" ::"r"(swz(vtile, r, ch)),
+                             "r"(0u)
+                             : "memory");
+            }
+            __syncwarp();
+        }
+#pragma unroll
+        for (int dd = 0; dd < D / 16; ++dd) {
+            uint32_t b[4];
+            ldsm_x4_trans(b, swz(vtile, (mi & 1) * 8 + rr, 2 * dd + (mi >> 1)));
+            mma_bf16_16816(o[2 * dd], pa, b[0], b[1]);
+            mma_bf16_16816(o[2 * dd + 1], pa, b[2], b[3]);
+        }
+    }
+
+    __device__ __forceinline__ void finish(float *acc_out, float *m_out, float *l_out) {
+        l0 += __shfl_xor_sync(kFull, l0, 1);
+        l0 += __shfl_xor_sync(kFull, l0, 2);
+        if (HI) {
+            l1 += __shfl_xor_sync(kFull, l1, 1);
+            l1 += __shfl_xor_sync(kFull, l1, 2);
+        }
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt) {
+            const int d = 8 * nt + 2 * t;
+            if (g < G) *reinterpret_cast<float2 *>(acc_out + g * D + d) = make_float2(o[nt][0], o[nt][1]);
+            if (HI && g + 8 < G)
+                *reinterpret_cast<float2 *>(acc_out + (g + 8) * D + d) = make_float2(o[nt][2], o[nt][3]);
+        }
+        if (t == 0) {
+            if (g < G) {
+                m_out[g] = m0;
+                l_out[g] = l0;
+            }
+            if (HI && g + 8 < G) {
+                m_out[g + 8] = m1;
+                l_out[g + 8] = l1;
+            }
+        }
+    }
+};
+
+template <int D, int NW, int STAGES>
+struct TmaLayout {
+    static constexpr int kTileBytes = 16 * D * 2;
+    static constexpr int kStageBytes = 2 * kTileBytes;
+    static constexpr int kStagesBytes = NW * STAGES * kStageBytes;
+    static constexpr int kRowsMax = 16;   // rows of the merge state per warp
+    static size_t smem_bytes(int part_blocks) {
+        return 1024 /* alignment slack */ + kStagesBytes + NW * STAGES * sizeof(uint64_t) +
+               (size_t)part_blocks * sizeof(int32_t) + 2 * NW * kRowsMax * sizeof(float) + 16;
+    }
+};
+
+// bf16 kernel: one CTA per (sequence, KV head, partition); NW warps, each with
+// its own STAGES-deep TMA ring.
+template <int D, class Consumer, int NW, int STAGES>
+__global__ void __launch_bounds__(NW * 32)
+pa_decode_bf16_kernel(const __grid_constant__ CUtensorMap kmap,
+                      const __grid_constant__ CUtensorMap vmap, const DecodeArgs a) {
+    using Lay = TmaLayout<D, NW, STAGES>;
+    Work w;
+    if (!cta_work(a, a.num_kv_heads, w)) return;
+
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                                ~uintptr_t(1023));
+    uint8_t *stages = smem;
+    uint64_t *bars = reinterpret_cast<uint64_t *>(stages + Lay::kStagesBytes);
+    int32_t *s_table = reinterpret_cast<int32_t *>(bars + NW * STAGES);
+    float *s_m = reinterpret_cast<float *>(s_table + a.part_blocks);
+    float *s_l = s_m + NW * Lay::kRowsMax;
+    __shared__ int s_fail;
+
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+
+    if (threadIdx.x == 0) {
+        s_fail = 0;
+        tma_prefetch_desc(&kmap);
+        tma_prefetch_desc(&vmap);
+    }
+    const int32_t *trow = a.block_tables + (size_t)w.b * a.max_blocks + w.blk0;
+    for (int i = threadIdx.x; i < w.nblk; i += NW * 32) {
+        int phys = trow[i];
+        if ((unsigned)phys >= (unsigned)a.num_blocks) {
+            report(a.status, PA_DEV_BAD_BLOCK_ID);
+            phys = 0;
+        }
+        s_table[i] = phys;
+    }
+    uint64_t *my_bars = bars + warp * STAGES;
+    uint8_t *my_stages = stages + warp * STAGES * Lay::kStageBytes;
+    if (lane == 0) {
+#pragma unroll
+        for (int s = 0; s < STAGES; ++s) mbar_init(&my_bars[s], 1);
+        fence_mbar_init();
+    }
+    __syncthreads();
+
+    Consumer cons;
+    cons.init(a, w, lane);
+
+    const int my_count = w.nblk > warp ? (w.nblk - warp + NW - 1) / NW : 0;
+    const int row_base = w.head * kBlockSize;   // + phys * Hkv * 16
+
+    auto issue = [&](int it) {
+        const int s = it % STAGES;
+        const int phys = s_table[warp + it * NW];
+        const int y = phys * a.num_kv_heads * kBlockSize + row_base;
+        uint8_t *kt = my_stages + s * Lay::kStageBytes;
+        uint8_t *vt = kt + Lay::kTileBytes;
+        mbar_arrive_expect_tx(&my_bars[s], Lay::kStageBytes);
+#pragma unroll
+        for (int x = 0; x < D; x += 64) {
+            tma_load_2d(kt + (x / 64) * 2048, &kmap, x, y, &my_bars[s]);
+            tma_load_2d(vt + (x / 64) * 2048, &vmap, x, y, &my_bars[s]);
+        }
+    };
+
+    if (lane == 0)
+        for (int it = 0; it < STAGES && it < my_count; ++it) issue(it);
+
+    bool ok = true;
+    int it = 0;
+    for (; it < my_count; ++it) {
+        const int s = it % STAGES;
+        const bool done = mbar_wait_bounded(&my_bars[s], (it / STAGES) & 1);
+        if (!__all_sync(kFull, done)) {
+            ok = false;
+            break;
+        }
+        const int tok0 = (w.blk0 + warp + it * NW) * kBlockSize;
+        const int nvalid = min(kBlockSize, w.L - tok0);
+        const uint32_t kt = smem_u32(my_stages + s * Lay::kStageBytes);
+        cons.block(kt, kt + Lay::kTileBytes, nvalid);
+        __syncwarp();
+        if (lane == 0 && it + STAGES < my_count) {
+            fence_proxy_async_smem();
+            issue(it + STAGES);
+        }
+    }
+    if (!ok) {
+        // Give every copy still in flight a bounded chance to land before the
+        // CTA's shared memory is released, then drop this CTA's result.
+        for (int k = it; k < my_count && k < it + STAGES; ++k)
+            (void)mbar_wait_bounded(&my_bars[k % STAGES], (k / STAGES) & 1);
+        if (lane == 0) {
+            report(a.status, PA_DEV_TIMEOUT);
+            s_fail = 1;
+        }
+    }
+
+    float *acc_out = reinterpret_cast<float *>(my_stages);   // the ring is idle now
+    cons.finish(acc_out, s_m + warp * Lay::kRowsMax, s_l + warp * Lay::kRowsMax);
+    if (my_count == 0 && lane == 0) {
+        for (int r = 0; r < Consumer::ROWS; ++r) {
+            s_m[warp * Lay::kRowsMax + r] = -INFINITY;
+            s_l[warp * Lay::kRowsMax + r] = 0.f;
+        }
+    }
+    __syncthreads();
+    if (s_fail) return;
+    merge_and_store<__nv_bfloat16, NW>(a, w, w.head * Consumer::ROWS, Consumer::ROWS, D,
+                                       reinterpret_cast<const float *>(stages),
+                                       STAGES * Lay::kStageBytes / 4, s_m, s_l, Lay::kRowsMax);
+}
+
+// fp32 kernel: one CTA per (sequence, query head, partition); lane owns
+// head-dim elements lane + 32 e.  Plain loads; online softmax per token.
+template <int D, int NW>
+__global__ void __launch_bounds__(NW * 32) pa_decode_f32_kernel(const float *__restrict__ kc,
+                                                                const float *__restrict__ vc,
+                                                                const DecodeArgs a) {
+    constexpr int EPL = D / 32;
+    Work w;
+    if (!cta_work(a, a.num_q_heads, w)) return;
+    __shared__ float s_acc[NW][D];
+    __shared__ float s_m[NW], s_l[NW];
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int group = a.num_q_heads / a.num_kv_heads;
+    const int kvh = w.head / group;
+    const float *qrow = static_cast<const float *>(a.query) + ((size_t)w.b * a.num_q_heads + w.head) * D;
+    float q[EPL], acc[EPL];
+#pragma unroll
+    for (int e = 0; e < EPL; ++e) {
+        q[e] = qrow[lane + 32 * e] * a.scale_log2;
+        acc[e] = 0.f;
+    }
+    float m = -INFINITY, l = 0.f;
+    const int32_t *trow = a.block_tables + (size_t)w.b * a.max_blocks + w.blk0;
+    for (int j = warp; j < w.nblk; j += NW) {
+        int phys = trow[j];
+        if ((unsigned)phys >= (unsigned)a.num_blocks) {
+            if (lane == 0) report(a.status, PA_DEV_BAD_BLOCK_ID);
+            phys = 0;
+        }
+        const int tok0 = (w.blk0 + j) * kBlockSize;
+        const int nvalid = min(kBlockSize, w.L - tok0);
+        const size_t base = (((size_t)phys * a.num_kv_heads + kvh) * kBlockSize) * D;
+        for (int r = 0; r < nvalid; ++r) {
+            const float *krow = kc + base + (size_t)r * D;
+            const float *vrow = vc + base + (size_t)r * D;
+            float s = 0.f;
+#pragma unroll
+            for (int e = 0; e < EPL; ++e) s = fmaf(q[e], krow[lane + 32 * e], s);
+#pragma unroll
+            for (int M = 16; M >= 1; M >>= 1) s += __shfl_xor_sync(kFull, s, M);
+            const float m_new = fmaxf(m, s);
+            const float alpha = exp2f(m - m_new);
+            const float p = exp2f(s - m_new);
+            l = l * alpha + p;
+#pragma unroll
+            for (int e = 0; e < EPL; ++e) acc[e] = fmaf(p, vrow[lane + 32 * e], acc[e] * alpha);
+            m = m_new;
+        }
+    }
+#pragma unroll
+    for (int e = 0; e < EPL; ++e) s_acc[warp][lane + 32 * e] = acc[e];
+    if (lane == 0) {
+        s_m[warp] = m;
+        s_l[warp] = l;
+    }
+    __syncthreads();
+    merge_and_store<float, NW>(a, w, w.head, 1, D, &s_acc[0][0], D, s_m, s_l, 1);
+}
+
+// Merges the partitions of every (sequence, query head) that has more than one.
+template <typename OutT>
+__global__ void __launch_bounds__(128) pa_reduce_kernel(const DecodeArgs a, int D) {
+    grid_dependency_wait();
+    const int b = blockIdx.x / a.num_q_heads;
+    const int h = blockIdx.x - b * a.num_q_heads;
+    int L = a.context_lens[b];
+    const int lmax = a.max_blocks * kBlockSize;
+    L = L < 0 ? 0 : (L > lmax ? lmax : L);
+    const int seq_blocks = (L + kBlockSize - 1) / kBlockSize;
+    const int nparts = seq_blocks == 0 ? 1 : (seq_blocks + a.part_blocks - 1) / a.part_blocks;
+    if (nparts <= 1) return;
+    const size_t row0 = ((size_t)b * a.num_q_heads + h) * a.max_parts;
+    extern __shared__ float s_w[];   // [nparts] weights
+    __shared__ float s_M, s_L;
+    if (threadIdx.x < 32) {
+        float M = -INFINITY;
+        for (int p = threadIdx.x; p < nparts; p += 32) M = fmaxf(M, a.part_ml[row0 + p].x);
+#pragma unroll
+        for (int k = 16; k >= 1; k >>= 1) M = fmaxf(M, __shfl_xor_sync(kFull, M, k));
+        float Lsum = 0.f;
+        for (int p = threadIdx.x; p < nparts; p += 32) {
+            const float2 ml = a.part_ml[row0 + p];
+            const float wgt = ml.x == -INFINITY ? 0.f : exp2f(ml.x - M);
+            s_w[p] = wgt;
+            Lsum += wgt * ml.y;
+        }
+#pragma unroll
+        for (int k = 16; k >= 1; k >>= 1) Lsum += __shfl_xor_sync(kFull, Lsum, k);
+        if (threadIdx.x == 0) {
+            s_M = M;
+            s_L = Lsum;
+        }
+    }
+    __syncthreads();
+    const float inv = s_L > 0.f ? 1.f / s_L : 0.f;
+    OutT *out = static_cast<OutT *>(a.out) + ((size_t)b * a.num_q_heads + h) * D;
+    for (int d = threadIdx.x; d < D; d += blockDim.x) {
+        float O = 0.f;
+        for (int p = 0; p < nparts; ++p) O = fmaf(s_w[p], a.part_o[(row0 + p) * D + d], O);
+        store_out<OutT>(out + d, s_L > 0.f ? O * inv : 0.f);
+    }
+}
+
+// ---------------------------------------------------------------------------
+// Host side
+// ---------------------------------------------------------------------------
+PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void *p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                             &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+    });
+    return fn;
+}
+
+// 2-D view of a pool as [num_blocks * num_kv_heads * 16 rows][head_dim] bf16,
+// loaded as boxes of 16 rows x 64 elements with 128-byte swizzle.
+bool encode_pool_map(CUtensorMap *map, const void *pool, int64_t rows, int D) {
+    auto enc = tensor_map_encoder();
+    if (enc == nullptr) return false;
+    cuuint64_t dims[2] = {(cuuint64_t)D, (cuuint64_t)rows};
+    cuuint64_t strides[1] = {(cuuint64_t)D * 2};
+    cuuint32_t box[2] = {64, 16};
+    cuuint32_t estr[2] = {1, 1};
+    CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(pool), dims,
+                     strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                     CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
+
+template <typename K>
+cudaError_t allow_smem(K kernel, size_t bytes) {
+    return cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes);
+}
+
+constexpr int kNW = 4;
+
+template <int D, class Consumer, int STAGES>
+pa_status launch_bf16(const DecodeArgs &a, const void *kc, const void *vc, int64_t rows,
+                      cudaStream_t stream) {
+    CUtensorMap kmap, vmap;
+    if (!encode_pool_map(&kmap, kc, rows, D) || !encode_pool_map(&vmap, vc, rows, D))
+        return cuda_failure(cudaErrorInvalidValue, "cuTensorMapEncodeTiled");
+    const size_t smem = TmaLayout<D, kNW, STAGES>::smem_bytes(a.part_blocks);
+    auto kernel = pa_decode_bf16_kernel<D, Consumer, kNW, STAGES>;
+    cudaError_t e = allow_smem(kernel, smem);
+    if (e != cudaSuccess) return cuda_failure(e, "cudaFuncSetAttribute(decode)");
+    const int64_t grid = (int64_t)a.num_seqs * a.num_kv_heads * a.max_parts;
+    kernel<<<(unsigned)grid, kNW * 32, smem, stream>>>(kmap, vmap, a);
+    e = cudaGetLastError();
+    if (e != cudaSuccess) return cuda_failure(e, "pa_decode_bf16_kernel launch");
+    count_launches(1);
+    return PA_OK;
+}
+
+template <int D, int G>
+pa_status launch_gqa(const DecodeArgs &a, const void *kc, const void *vc, int64_t rows,
+                     cudaStream_t stream) {
+    return launch_bf16<D, GqaConsumer<D, G>, 3>(a, kc, vc, rows, stream);
+}
+
+template <int D>
+pa_status dispatch_bf16(int group, const DecodeArgs &a, const void *kc, const void *vc,
+                        int64_t rows, cudaStream_t stream) {
+    switch (group) {
+    case 1: return launch_bf16<D, MhaConsumer<D>, 3>(a, kc, vc, rows, stream);
+    case 2: return launch_gqa<D, 2>(a, kc, vc, rows, stream);
+    case 3: return launch_gqa<D, 3>(a, kc, vc, rows, stream);
+    case 4: return launch_gqa<D, 4>(a, kc, vc, rows, stream);
+    case 5: return launch_gqa<D, 5>(a, kc, vc, rows, stream);
+    case 6: return launch_gqa<D, 6>(a, kc, vc, rows, stream);
+    case 7: return launch_gqa<D, 7>(a, kc, vc, rows, stream);
+    case 8: return launch_gqa<D, 8>(a, kc, vc, rows, stream);
+    case 12: return launch_gqa<D, 12>(a, kc, vc, rows, stream);
+    case 16: return launch_gqa<D, 16>(a, kc, vc, rows, stream);
+    default: return PA_ERR_UNSUPPORTED;
+    }
+}
+
+template <int D>
+pa_status launch_f32(const DecodeArgs &a, const void *kc, const void *vc, cudaStream_t stream) {
+    const int64_t grid = (int64_t)a.num_seqs * a.num_q_heads * a.max_parts;
+    pa_decode_f32_kernel<D, kNW><<<(unsigned)grid, kNW * 32, 0, stream>>>(
+        static_cast<const float *>(kc), static_cast<const float *>(vc), a);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return cuda_failure(e, "pa_decode_f32_kernel launch");
+    count_launches(1);
+    return PA_OK;
+}
+
+template <typename OutT>
+pa_status launch_reduce(const DecodeArgs &a, int D, cudaStream_t stream) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)(a.num_seqs * a.num_q_heads));
+    cfg.blockDim = dim3(128);
+    cfg.dynamicSmemBytes = (size_t)a.max_parts * sizeof(float);
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    auto kernel = pa_reduce_kernel<OutT>;
+    if (cfg.dynamicSmemBytes > 48 * 1024) {
+        cudaError_t e = allow_smem(kernel, cfg.dynamicSmemBytes);
+        if (e != cudaSuccess) return cuda_failure(e, "cudaFuncSetAttribute(reduce)");
+    }
+    cudaError_t e = cudaLaunchKernelEx(&cfg, kernel, a, D);
+    if (e != cudaSuccess) return cuda_failure(e, "pa_reduce_kernel launch");
+    count_launches(1);
+    return PA_OK;
+}
+
+int resolve_partition(int partition_size) {
+    const int p = partition_size == 0 ? kDefaultPartition : partition_size;
+    if (p < kBlockSize || p > kMaxPartition || p % kBlockSize != 0) return -1;
+    return p;
+}
+
+size_t workspace_for(int num_seqs, int num_q_heads, int head_dim, int max_parts) {
+    if (max_parts <= 1) return 0;
+    const size_t rows = (size_t)num_seqs * num_q_heads * max_parts;
+    const size_t o_bytes = (rows * head_dim * sizeof(float) + 255) & ~size_t(255);
+    return o_bytes + rows * sizeof(float2);
+}
+
+}  // namespace
+}  // namespace pa
+
+using namespace pa;
+
+extern "C" int pa_default_partition_size(void) { return kDefaultPartition; }
+
+extern "C" size_t pa_decode_workspace_bytes(int num_seqs, int num_q_heads, int head_dim,
+                                            int max_blocks_per_seq, int block_size,
+                                            int partition_size) {
+    const int p = resolve_partition(partition_size);
+    if (p < 0 || num_seqs < 0 || num_q_heads <= 0 || head_dim <= 0 || max_blocks_per_seq < 0 ||
+        block_size != kBlockSize)
+        return (size_t)-1;
+    const int part_blocks = p / kBlockSize;
+    const int max_parts = max(1, (max_blocks_per_seq + part_blocks - 1) / part_blocks);
+    return workspace_for(num_seqs, num_q_heads, head_dim, max_parts);
+}
+
+extern "C" pa_status pa_decode(void *out, const void *query, const void *key_cache,
+                               const void *value_cache, const int32_t *block_tables,
+                               const int32_t *context_lens, int num_seqs, int num_q_heads,
+                               int num_kv_heads, int head_dim, int block_size,
+                               int max_blocks_per_seq, int num_blocks, float scale, pa_dtype dtype,
+                               int partition_size, void *workspace, size_t workspace_bytes,
+                               int32_t *device_status, void *stream) {
+    if (num_seqs < 0 || num_q_heads <= 0 || num_kv_heads <= 0 || block_size != kBlockSize ||
+        max_blocks_per_seq < 0 || num_blocks <= 0 || num_q_heads % num_kv_heads != 0 ||
+        !(scale == scale))
+        return PA_ERR_INVALID_ARG;
+    if (dtype != PA_DTYPE_F32 && dtype != PA_DTYPE_BF16) return PA_ERR_INVALID_ARG;
+    const int p = resolve_partition(partition_size);
+    if (p < 0) return PA_ERR_INVALID_ARG;
+    if (num_seqs == 0) return PA_OK;
+    if (!out || !query || !key_cache || !value_cache || !block_tables || !context_lens)
+        return PA_ERR_INVALID_ARG;
+    if (!aligned16(out) || !aligned16(query) || !aligned16(key_cache) || !aligned16(value_cache))
+        return PA_ERR_INVALID_ARG;
+    const int group = num_q_heads / num_kv_heads;
+    if (dtype == PA_DTYPE_BF16) {
+        if (head_dim != 64 && head_dim != 128) return PA_ERR_UNSUPPORTED;
+        if (group > 16) return PA_ERR_UNSUPPORTED;
+    } else {
+        if (head_dim != 32 && head_dim != 64 && head_dim != 128 && head_dim != 256)
+            return PA_ERR_UNSUPPORTED;
+    }
+    const int64_t rows = (int64_t)num_blocks * num_kv_heads * kBlockSize;
+    if (rows >= ((int64_t)1 << 31)) return PA_ERR_UNSUPPORTED;
+    const int part_blocks = p / kBlockSize;
+    const int max_parts = max(1, (max_blocks_per_seq + part_blocks - 1) / part_blocks);
+    const int heads_axis = dtype == PA_DTYPE_BF16 ? num_kv_heads : num_q_heads;
+    if ((int64_t)num_seqs * heads_axis * max_parts >= ((int64_t)1 << 31)) return PA_ERR_UNSUPPORTED;
+    const size_t need = workspace_for(num_seqs, num_q_heads, head_dim, max_parts);
+    if (need > 0 && (workspace == nullptr || workspace_bytes < need || !aligned16(workspace)))
+        return PA_ERR_WORKSPACE;
+
+    DecodeArgs a;
+    a.out = out;
+    a.query = query;
+    a.block_tables = block_tables;
+    a.context_lens = context_lens;
+    a.part_o = static_cast<float *>(workspace);
+    a.part_ml = need > 0 ? reinterpret_cast<float2 *>(
+                               static_cast<uint8_t *>(workspace) +
+                               (((size_t)num_seqs * num_q_heads * max_parts * head_dim * sizeof(float) +
+                                 255) & ~size_t(255)))
+                         : nullptr;
+    a.status = device_status;
+    a.num_seqs = num_seqs;
+    a.num_q_heads = num_q_heads;
+    a.num_kv_heads = num_kv_heads;
+    a.max_blocks = max_blocks_per_seq;
+    a.num_blocks = num_blocks;
+    a.part_blocks = part_blocks;
+    a.max_parts = max_parts;
+    a.scale_log2 = scale * kLog2e;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+
+    pa_status s;
+    if (dtype == PA_DTYPE_BF16) {
+        s = head_dim == 64 ? dispatch_bf16<64>(group, a, key_cache, value_cache, rows, st)
+                           : dispatch_bf16<128>(group, a, key_cache, value_cache, rows, st);
+    } else {
+        switch (head_dim) {
+        case 32: s = launch_f32<32>(a, key_cache, value_cache, st); break;
+        case 64: s = launch_f32<64>(a, key_cache, value_cache, st); break;
+        case 128: s = launch_f32<128>(a, key_cache, value_cache, st); break;
+        default: s = launch_f32<256>(a, key_cache, value_cache, st); break;
+        }
+    }
+    if (s != PA_OK || max_parts <= 1) return s;
+    return dtype == PA_DTYPE_BF16 ? launch_reduce<__nv_bfloat16>(a, head_dim, st)
+                                  : launch_reduce<float>(a, head_dim, st);
+}
