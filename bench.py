@@ -20,9 +20,7 @@ import hashlib
 import json
 import os
 import statistics
-import subprocess
 import sys
-import tempfile
 import time
 
 import numpy as np
@@ -125,64 +123,94 @@ def load_peaks():
 
 
 class ClockSampler:
-    """nvidia-smi samples of SM clock and throttle reasons while the timed region runs."""
-    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
-              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
-              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+    """SM clock and throttle-reason samples taken while the timed region runs.
 
-    def __init__(self, gpu_index: int):
-        self.tmp = tempfile.NamedTemporaryFile(mode="w+", suffix=".csv", delete=False)
-        self.proc = None
+    Reads NVML (the library nvidia-smi uses) every 20 ms from a background
+    thread.  Read-only: no clock or other GPU setting is changed.
+    """
+    REASONS = {0x4: "sw_power_cap", 0x8: "hw_slowdown", 0x20: "sw_thermal_slowdown",
+               0x40: "hw_thermal_slowdown", 0x80: "hw_power_brake_slowdown"}
+
+    def __init__(self, gpu_index: int, pci_bus_id: str | None = None, period_s: float = 0.02):
+        import threading
+        self.samples = []
+        self.recording = False
+        self._stop = threading.Event()
+        self._nvml = None
         try:
-            self.proc = subprocess.Popen(
-                ["nvidia-smi", "-i", str(gpu_index), f"--query-gpu={self.FIELDS}",
-                 "--format=csv,noheader,nounits", "-lms", "100"], stdout=self.tmp,
-                stderr=subprocess.DEVNULL)
+            import ctypes
+            nv = ctypes.CDLL("libnvidia-ml.so.1")
+            if nv.nvmlInit_v2() != 0:
+                raise OSError("nvmlInit failed")
+            h = ctypes.c_void_p()
+            ok = False
+            if pci_bus_id:
+                ok = nv.nvmlDeviceGetHandleByPciBusId_v2(pci_bus_id.encode(), ctypes.byref(h)) == 0
+            if not ok and nv.nvmlDeviceGetHandleByIndex_v2(ctypes.c_uint(gpu_index),
+                                                           ctypes.byref(h)) != 0:
+                raise OSError("no NVML handle")
+            self._nvml, self._h, self._ct = nv, h, ctypes
+            mx = ctypes.c_uint()
+            nv.nvmlDeviceGetMaxClockInfo(h, 1, ctypes.byref(mx))
+            self.max_mhz = float(mx.value)
         except Exception:
-            self.proc = None
+            self._nvml = None
+        self._thread = threading.Thread(target=self._run, args=(period_s,), daemon=True)
+        self._thread.start()
 
-    def wait_first(self, timeout=5.0):
-        t0 = time.time()
-        while self.proc is not None and time.time() - t0 < timeout:
-            self.tmp.flush()
-            if os.path.getsize(self.tmp.name) > 0:
-                return
-            time.sleep(0.02)
+    def _read(self):
+        ct, nv = self._ct, self._nvml
+        clk = ct.c_uint()
+        nv.nvmlDeviceGetClockInfo(self._h, 1, ct.byref(clk))
+        reasons = ct.c_ulonglong()
+        fn = getattr(nv, "nvmlDeviceGetCurrentClocksEventReasons", None) or \
+            getattr(nv, "nvmlDeviceGetCurrentClocksThrottleReasons")
+        fn(self._h, ct.byref(reasons))
+        return float(clk.value), int(reasons.value)
 
-    def mark(self):
-        self.tmp.flush()
-        return os.path.getsize(self.tmp.name)
+    def _run(self, period_s):
+        if self._nvml is None:
+            return
+        while not self._stop.is_set():
+            if self.recording:
+                try:
+                    self.samples.append(self._read())
+                except Exception:
+                    pass
+            self._stop.wait(period_s)
 
-    def stop(self, start_offset: int):
-        if self.proc is not None:
-            self.proc.terminate()
+    def start(self):
+        self.recording = True
+
+    def stop(self):
+        if self._nvml is not None and not self.samples:
             try:
-                self.proc.wait(timeout=5)
+                self.samples.append(self._read())       # at least one reading at the end
             except Exception:
-                self.proc.kill()
-        self.tmp.flush()
-        with open(self.tmp.name) as f:
-            f.seek(start_offset)
-            lines = [ln.strip() for ln in f if ln.strip()]
-        os.unlink(self.tmp.name)
-        sm, mx, reasons = [], [], set()
-        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        for ln in lines:
-            parts = [p.strip() for p in ln.split(",")]
-            if len(parts) < 8:
-                continue
-            try:
-                sm.append(float(parts[0]))
-                mx.append(float(parts[1]))
-            except ValueError:
-                continue
-            for name, val in zip(names, parts[4:8]):
-                if val.lower() == "active":
+                pass
+        self.recording = False
+        self._stop.set()
+        self._thread.join(timeout=2)
+        if not self.samples:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0,
+                    "source": "unavailable"}
+        reasons = set()
+        for _, bits in self.samples:
+            for bit, name in self.REASONS.items():
+                if bits & bit:
                     reasons.add(name)
-        if not sm:
-            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
-        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "reasons": sorted(reasons),
-                "samples": len(sm)}
+        return {"sm_mhz": statistics.median(c for c, _ in self.samples),
+                "sm_max_mhz": self.max_mhz, "reasons": sorted(reasons),
+                "samples": len(self.samples), "source": "NVML, 20 ms period"}
+
+
+def pci_bus_id(dev):
+    try:
+        import torch
+        p = torch.cuda.get_device_properties(dev)
+        return "%08x:%02x:%02x.0" % (p.pci_domain_id, p.pci_bus_id, p.pci_device_id)
+    except Exception:
+        return None
 
 
 def kernel_source_hash() -> str:
@@ -258,13 +286,12 @@ def run_gpu(args):
     post = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
     e0 = torch.cuda.Event(enable_timing=True)
     e1 = torch.cuda.Event(enable_timing=True)
-    sampler = ClockSampler(dev.index if dev.index is not None else 0) if rank == 0 else None
-    if sampler:
-        sampler.wait_first()
-        off = sampler.mark()
+    sampler = ClockSampler(dev.index or 0, pci_bus_id(dev)) if rank == 0 else None
     barrier()
     torch.cuda.synchronize(dev)
     launches0 = pkv.launch_count()
+    if sampler:
+        sampler.start()
     e0.record(stream)
     for i in range(K):
         step(pre[i], post[i])
@@ -272,7 +299,7 @@ def run_gpu(args):
     torch.cuda.synchronize(dev)
     barrier()
     launches = pkv.launch_count() - launches0
-    clocks = sampler.stop(off) if sampler else None
+    clocks = sampler.stop() if sampler else None
     ms_total = e0.elapsed_time(e1)
     decode_ms = sum(a.elapsed_time(b) for a, b in zip(pre, post)) / K
     ms_total = max_over_ranks(ms_total, dev)
@@ -528,7 +555,7 @@ def run_reference(args):
 def main(argv=None):
     ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--steps", type=int, default=3000)
     ap.add_argument("--warmup", type=int, default=50)
     ap.add_argument("--workload", default="llama7b_mha", choices=W.WORKLOADS)
     ap.add_argument("--partition-size", type=int, default=0)

@@ -368,11 +368,18 @@ struct GqaConsumer {
                 o[nt][3] *= a1;
             }
         }
-        uint32_t pa[4];
-        pa[0] = pack_bf16x2(p[0][0], p[0][1]);
-        pa[1] = HI ? pack_bf16x2(p[0][2], p[0][3]) : 0u;
-        pa[2] = pack_bf16x2(p[1][0], p[1][1]);
-        pa[3] = HI ? pack_bf16x2(p[1][2], p[1][3]) : 0u;
+        // P enters the tensor cores as bf16; a single rounding would perturb each
+        // weight by up to 2^-9, so P is split into a bf16 head and a bf16 residual
+        // (P = hi + lo up to 2^-18 relative) and both are multiplied by V.
+        uint32_t pa[4], pl[4];
+        split_bf16x2(p[0][0], p[0][1], pa[0], pl[0]);
+        split_bf16x2(p[1][0], p[1][1], pa[2], pl[2]);
+        if (HI) {
+            split_bf16x2(p[0][2], p[0][3], pa[1], pl[1]);
+            split_bf16x2(p[1][2], p[1][3], pa[3], pl[3]);
+        } else {
+            pa[1] = pa[3] = pl[1] = pl[3] = 0u;
+        }
         if (nvalid < 16) {
             // Rows past the context may hold anything (even NaN): zero them so
             // that 0 * row stays 0 in the tensor-core sum.
@@ -392,6 +399,8 @@ struct GqaConsumer {
             ldsm_x4_trans(b, swz(vtile, (mi & 1) * 8 + rr, 2 * dd + (mi >> 1)));
             mma_bf16_16816(o[2 * dd], pa, b[0], b[1]);
             mma_bf16_16816(o[2 * dd + 1], pa, b[2], b[3]);
+            mma_bf16_16816(o[2 * dd], pl, b[0], b[1]);
+            mma_bf16_16816(o[2 * dd + 1], pl, b[2], b[3]);
         }
     }
 

@@ -135,4 +135,13 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
     return *reinterpret_cast<uint32_t *>(&v);
 }
 
+// x = head + residual: head is x rounded to bf16, residual is the exact fp32
+// remainder rounded to bf16 (relative error of the pair about 2^-18).
+__device__ __forceinline__ void split_bf16x2(float x0, float x1, uint32_t &head, uint32_t &rest) {
+    head = pack_bf16x2(x0, x1);
+    const float r0 = x0 - bf16lo(head);
+    const float r1 = x1 - bf16hi(head);
+    rest = pack_bf16x2(r0, r1);
+}
+
 }  // namespace pa
