@@ -134,6 +134,40 @@ pa_status pa_decode(void *out, const void *query, const void *key_cache, const v
                     int32_t *device_status, void *stream);
 
 /*
+ * Size of the library-owned scratch array used by pa_decode_static_scratch
+ * (32 MiB of device global memory on every device that loads the library).
+ */
+#define PA_STATIC_SCRATCH_BYTES (32u << 20)
+
+/*
+ * pa_decode without caller scratch.  The pages have no counterpart: this is an
+ * interface addition for callers that cannot allocate device memory at call
+ * time - their device memory is reserved up front by another allocator, or a
+ * cudaMalloc / cudaFree (with its implicit device synchronisation) is not
+ * acceptable where they run, or they are handed only inputs and outputs.
+ * Arguments, layouts, results and error behaviour are those of pa_decode;
+ * the split-K partials go to a fixed library-owned device array of
+ * PA_STATIC_SCRATCH_BYTES instead of a workspace.  Nothing is allocated.
+ *  - Size limit: when pa_decode_workspace_bytes(...) for these arguments
+ *    exceeds PA_STATIC_SCRATCH_BYTES the call returns PA_ERR_WORKSPACE and
+ *    enqueues nothing (use pa_decode with a workspace, or a larger
+ *    partition_size, then).
+ *  - Set-up: the first call on a device that needs scratch looks up the
+ *    array's device address (cudaGetSymbolAddress) with that device current;
+ *    make that first call before any stream capture.
+ *  - Sharing: every call on a device uses the same array and leaves its last
+ *    contents there.  No part of it has to start at zero.  Calls that overlap
+ *    on the GPU (other streams, other host threads) race on it; serialise them.
+ */
+pa_status pa_decode_static_scratch(void *out, const void *query, const void *key_cache,
+                                   const void *value_cache, const int32_t *block_tables,
+                                   const int32_t *context_lens, int num_seqs, int num_q_heads,
+                                   int num_kv_heads, int head_dim, int block_size,
+                                   int max_blocks_per_seq, int num_blocks, float scale,
+                                   pa_dtype dtype, int partition_size, int32_t *device_status,
+                                   void *stream);
+
+/*
  * Cache write: for every new token i with slot_mapping[i] >= 0, copies its K
  * and V rows (all KV heads) into offset slot % 16 of physical block slot / 16:
  *   key_cache[slot / 16][kvh][slot % 16][:] = key[i][kvh][:]   (same for V)

@@ -34,6 +34,8 @@ SIGNATURES = {
     "pa_decode_workspace_bytes": (sz, [i32, i32, i32, i32, i32, i32]),
     "pa_decode": (i32, [vp, vp, vp, vp, vp, vp, i32, i32, i32, i32, i32, i32, i32, f32, i32, i32,
                         vp, sz, vp, vp]),
+    "pa_decode_static_scratch": (i32, [vp, vp, vp, vp, vp, vp, i32, i32, i32, i32, i32, i32, i32,
+                                       f32, i32, i32, vp, vp]),
     "pa_cache_write": (i32, [vp, vp, vp, vp, vp, i32, i32, i32, i32, i32, i32, vp, vp]),
     "pa_block_copy": (i32, [vp, vp, vp, i32, i32, i32, i32, i32, i32, vp, vp]),
     "pa_bm_create": (vp, [i32, i32]),
