@@ -83,18 +83,26 @@ int pa_version(void);
 /* Number of kernels this library has launched in this process (all threads). */
 uint64_t pa_launch_count(void);
 
-/* Partition size pa_decode uses when it is given partition_size = 0. */
-int pa_default_partition_size(void);
+/*
+ * Partition size pa_decode uses when it is given partition_size = 0: the
+ * largest of 2048, 1024, 512, 256, 128 tokens for which
+ * num_seqs * heads * ceil(max_blocks_per_seq * 16 / size) reaches four CTAs
+ * per SM of the current device (heads = num_kv_heads for bf16, num_q_heads
+ * for f32).  Returns -1 for invalid arguments.
+ */
+int pa_decode_partition_size(int num_seqs, int num_q_heads, int num_kv_heads,
+                             int max_blocks_per_seq, pa_dtype dtype);
 
 /*
  * Bytes of workspace pa_decode needs for the split-K partials.  Returns 0 when
  * no sequence can span more than one partition (no workspace needed).
  * max_blocks_per_seq bounds the context length (max_blocks_per_seq * block_size).
- * partition_size: 0 = library default, else a multiple of 16 in [16, 16384].
- * Returns (size_t)-1 for invalid arguments.
+ * partition_size: 0 = library choice (pa_decode_partition_size), else a
+ * multiple of 16 in [16, 16384].  Returns (size_t)-1 for invalid arguments.
  */
-size_t pa_decode_workspace_bytes(int num_seqs, int num_q_heads, int head_dim,
-                                 int max_blocks_per_seq, int block_size, int partition_size);
+size_t pa_decode_workspace_bytes(int num_seqs, int num_q_heads, int num_kv_heads, int head_dim,
+                                 int max_blocks_per_seq, int block_size, int partition_size,
+                                 pa_dtype dtype);
 
 /*
  * Paged decode attention: for every sequence b and query head h,
@@ -112,9 +120,11 @@ size_t pa_decode_workspace_bytes(int num_seqs, int num_q_heads, int head_dim,
  *  block_tables      device int32 [num_seqs][max_blocks_per_seq]
  *  context_lens      device int32 [num_seqs]
  *  head_dim          bf16: 64 or 128; f32: 32, 64, 128 or 256
- *  num_q_heads       a multiple of num_kv_heads; bf16 needs group <= 16
+ *  num_q_heads       a multiple of num_kv_heads; bf16 needs the group
+ *                    (num_q_heads / num_kv_heads) in {1, ..., 8, 12, 16}
  *  scale             the softmax scale (usually 1/sqrt(head_dim))
- *  partition_size    tokens per split-K partition: 0 = default, else a
+ *  partition_size    tokens per split-K partition: 0 = library choice
+ *                    (pa_decode_partition_size), else a
  *                    multiple of 16 in [16, 16384].  A sequence longer than
  *                    one partition is processed by several CTAs whose partial
  *                    (max, sum, output) are merged by a second kernel.

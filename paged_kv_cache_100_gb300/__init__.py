@@ -25,7 +25,7 @@ from ._lib import PagedKVError, check, lib  # noqa: F401
 
 BLOCK_SIZE = 16
 
-__all__ = ["decode", "decode_workspace_bytes", "cache_write", "block_copy", "launch_count",
+__all__ = ["decode", "decode_workspace_bytes", "decode_partition_size", "cache_write", "block_copy", "launch_count",
            "BlockManager", "PagedKVError", "BLOCK_SIZE", "library_path"]
 
 
@@ -76,10 +76,22 @@ def launch_count() -> int:
     return int(lib().pa_launch_count())
 
 
-def decode_workspace_bytes(num_seqs, num_q_heads, head_dim, max_blocks_per_seq,
-                           partition_size=0) -> int:
-    n = lib().pa_decode_workspace_bytes(num_seqs, num_q_heads, head_dim, max_blocks_per_seq,
-                                        BLOCK_SIZE, partition_size)
+def decode_partition_size(num_seqs, num_q_heads, num_kv_heads, max_blocks_per_seq,
+                          dtype="bf16") -> int:
+    """Partition size (tokens) pa_decode picks when given partition_size=0."""
+    code = _lib.PA_DTYPE_BF16 if str(dtype) in ("bf16", "torch.bfloat16") else _lib.PA_DTYPE_F32
+    n = lib().pa_decode_partition_size(num_seqs, num_q_heads, num_kv_heads, max_blocks_per_seq,
+                                       code)
+    if n < 0:
+        raise ValueError("invalid arguments for pa_decode_partition_size")
+    return int(n)
+
+
+def decode_workspace_bytes(num_seqs, num_q_heads, num_kv_heads, head_dim, max_blocks_per_seq,
+                           partition_size=0, dtype="bf16") -> int:
+    code = _lib.PA_DTYPE_BF16 if str(dtype) in ("bf16", "torch.bfloat16") else _lib.PA_DTYPE_F32
+    n = lib().pa_decode_workspace_bytes(num_seqs, num_q_heads, num_kv_heads, head_dim,
+                                        max_blocks_per_seq, BLOCK_SIZE, partition_size, code)
     if n == ctypes.c_size_t(-1).value:
         raise ValueError("invalid arguments for pa_decode_workspace_bytes")
     return int(n)
@@ -105,7 +117,7 @@ def decode(query, key_cache, value_cache, block_tables, context_lens, scale=None
     elif out.shape != query.shape or out.dtype != query.dtype:
         raise ValueError("out must match query")
     max_blocks = block_tables.shape[1]
-    need = decode_workspace_bytes(B, Hq, D, max_blocks, partition_size)
+    need = decode_workspace_bytes(B, Hq, Hkv, D, max_blocks, partition_size, query.dtype)
     ws_ptr, ws_bytes = None, 0
     if need > 0:
         if workspace is None:

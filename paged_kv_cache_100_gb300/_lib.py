@@ -9,7 +9,9 @@ import os
 import threading
 
 HERE = os.path.dirname(os.path.abspath(__file__))
-LIB_PATH = os.path.join(HERE, "_build", "libpagedkv.so")
+# PAGEDKV_LIBRARY may point at another build of the same library (e.g. a
+# variant compiled with different tile parameters).
+LIB_PATH = os.environ.get("PAGEDKV_LIBRARY") or os.path.join(HERE, "_build", "libpagedkv.so")
 
 _lock = threading.Lock()
 _lib = None
@@ -30,8 +32,8 @@ SIGNATURES = {
     "pa_last_error": (ctypes.c_char_p, []),
     "pa_version": (i32, []),
     "pa_launch_count": (u64, []),
-    "pa_default_partition_size": (i32, []),
-    "pa_decode_workspace_bytes": (sz, [i32, i32, i32, i32, i32, i32]),
+    "pa_decode_partition_size": (i32, [i32, i32, i32, i32, i32]),
+    "pa_decode_workspace_bytes": (sz, [i32, i32, i32, i32, i32, i32, i32, i32]),
     "pa_decode": (i32, [vp, vp, vp, vp, vp, vp, i32, i32, i32, i32, i32, i32, i32, f32, i32, i32,
                         vp, sz, vp, vp]),
     "pa_decode_static_scratch": (i32, [vp, vp, vp, vp, vp, vp, i32, i32, i32, i32, i32, i32, i32,

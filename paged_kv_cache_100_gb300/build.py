@@ -28,25 +28,32 @@ def _nvcc() -> str:
     raise RuntimeError("nvcc not found")
 
 
-def _stale() -> bool:
-    if not os.path.exists(LIB):
+def _stale(lib: str) -> bool:
+    if not os.path.exists(lib):
         return True
-    t = os.path.getmtime(LIB)
+    t = os.path.getmtime(lib)
     deps = [os.path.join(CSRC, f) for f in CU_SOURCES + CPP_SOURCES + HEADERS]
     deps += [os.path.join(INCLUDE, "pagedkv.h"), os.path.abspath(__file__)]
     return any(os.path.getmtime(d) > t for d in deps)
 
 
-def build(force: bool = False, verbose_ptxas: bool = False) -> str:
-    if not force and not _stale():
-        return LIB
-    os.makedirs(BUILD, exist_ok=True)
+def build(force: bool = False, verbose_ptxas: bool = False, defines=(), build_dir=None) -> str:
+    """Compile and link the library; returns its path.
+
+    ``defines`` (e.g. ``["PA_DECODE_STAGES=2"]``) and ``build_dir`` produce a
+    variant build elsewhere; the default build is ``_build/libpagedkv.so``.
+    """
+    bdir = build_dir or BUILD
+    lib = os.path.join(bdir, "libpagedkv.so")
+    if not force and not _stale(lib):
+        return lib
+    os.makedirs(bdir, exist_ok=True)
     nvcc = _nvcc()
-    common = ["-O3", "-std=c++17", "-I", INCLUDE, "-I", CSRC]
+    common = ["-O3", "-std=c++17", "-I", INCLUDE, "-I", CSRC] + [f"-D{d}" for d in defines]
     jobs = []
     objs = []
     for src in CU_SOURCES:
-        obj = os.path.join(BUILD, src + ".o")
+        obj = os.path.join(bdir, src + ".o")
         cmd = [nvcc, *ARCH, *common, "-lineinfo", "-Xcompiler", "-fPIC", "-c",
                os.path.join(CSRC, src), "-o", obj]
         if verbose_ptxas:
@@ -54,7 +61,7 @@ def build(force: bool = False, verbose_ptxas: bool = False) -> str:
         jobs.append((cmd, src))
         objs.append(obj)
     for src in CPP_SOURCES:
-        obj = os.path.join(BUILD, src + ".o")
+        obj = os.path.join(bdir, src + ".o")
         cmd = ["g++", "-O2", "-std=c++17", "-fPIC", "-Wall", "-I", INCLUDE, "-c",
                os.path.join(CSRC, src), "-o", obj]
         jobs.append((cmd, src))
@@ -71,10 +78,10 @@ def build(force: bool = False, verbose_ptxas: bool = False) -> str:
             failed.append(src)
     if failed:
         raise RuntimeError(f"compilation failed: {', '.join(failed)}")
-    tmp = LIB + f".tmp{os.getpid()}"
+    tmp = lib + f".tmp{os.getpid()}"
     subprocess.run([nvcc, *ARCH, "-shared", "-o", tmp, *objs], check=True)
-    os.replace(tmp, LIB)
-    return LIB
+    os.replace(tmp, lib)
+    return lib
 
 
 if __name__ == "__main__":

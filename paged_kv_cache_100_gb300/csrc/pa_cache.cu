@@ -10,7 +10,9 @@
 // a sequence is about to modify a block it shares, only that block is copied.
 //
 // Both are pure bandwidth kernels: 16-byte vector loads and stores, one thread
-// per 16-byte chunk, index checks before every access.
+// per 16-byte chunk, index checks before every access.  They are launched
+// chained to the previous kernel of the stream (programmatic dependent launch)
+// and wait for it before touching memory.
 #include <cuda_runtime.h>
 
 #include <atomic>
@@ -33,6 +35,8 @@ pa_cache_write_kernel(uint4 *__restrict__ kc, uint4 *__restrict__ vc,
                       const uint4 *__restrict__ key, const uint4 *__restrict__ value,
                       const int64_t *__restrict__ slot_mapping, int num_tokens, int num_kv_heads,
                       int chunks_per_row, int num_blocks, int32_t *status) {
+    grid_dependency_wait();
+    grid_dependents_launch();
     const int64_t idx = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
     const int64_t per_token = (int64_t)num_kv_heads * chunks_per_row;
     if (idx >= (int64_t)num_tokens * per_token) return;
@@ -62,6 +66,8 @@ __global__ void __launch_bounds__(kCopyThreads)
 pa_block_copy_kernel(uint4 *__restrict__ kc, uint4 *__restrict__ vc,
                      const int32_t *__restrict__ src_dst, int64_t chunks_per_block, int num_blocks,
                      int32_t *status) {
+    grid_dependency_wait();
+    grid_dependents_launch();
     const int32_t src = src_dst[2 * blockIdx.x];
     const int32_t dst = src_dst[2 * blockIdx.x + 1];
     if ((unsigned)src >= (unsigned)num_blocks || (unsigned)dst >= (unsigned)num_blocks) {
@@ -147,11 +153,11 @@ extern "C" pa_status pa_cache_write(void *key_cache, void *value_cache, const vo
     const int64_t total = (int64_t)num_tokens * num_kv_heads * chunks;
     const int64_t grid = (total + 255) / 256;
     if (grid >= ((int64_t)1 << 31)) return PA_ERR_UNSUPPORTED;
-    pa_cache_write_kernel<<<(unsigned)grid, 256, 0, static_cast<cudaStream_t>(stream)>>>(
+    cudaError_t e = launch_chained(
+        pa_cache_write_kernel, dim3((unsigned)grid), dim3(256), 0, static_cast<cudaStream_t>(stream),
         static_cast<uint4 *>(key_cache), static_cast<uint4 *>(value_cache),
         static_cast<const uint4 *>(key), static_cast<const uint4 *>(value), slot_mapping,
         num_tokens, num_kv_heads, chunks, num_blocks, device_status);
-    cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return cuda_failure(e, "pa_cache_write_kernel launch");
     count_launches(1);
     return PA_OK;
@@ -177,10 +183,10 @@ extern "C" pa_status pa_block_copy(void *key_cache, void *value_cache, const int
     const int64_t slices = (chunks + per_cta - 1) / per_cta;
     if (slices > 65535) return PA_ERR_UNSUPPORTED;
     dim3 grid((unsigned)num_pairs, (unsigned)slices);
-    pa_block_copy_kernel<<<grid, kCopyThreads, 0, static_cast<cudaStream_t>(stream)>>>(
+    cudaError_t e = launch_chained(
+        pa_block_copy_kernel, grid, dim3(kCopyThreads), 0, static_cast<cudaStream_t>(stream),
         static_cast<uint4 *>(key_cache), static_cast<uint4 *>(value_cache), src_dst, chunks,
         num_blocks, device_status);
-    cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return cuda_failure(e, "pa_block_copy_kernel launch");
     count_launches(1);
     return PA_OK;

@@ -37,6 +37,7 @@
 #include <cudaTypedefs.h>
 #include <math.h>
 
+#include <algorithm>
 #include <atomic>
 #include <mutex>
 
@@ -450,6 +451,8 @@ __global__ void __launch_bounds__(NW * 32)
 pa_decode_bf16_kernel(const __grid_constant__ CUtensorMap kmap,
                       const __grid_constant__ CUtensorMap vmap, const DecodeArgs a) {
     using Lay = TmaLayout<D, NW, STAGES>;
+    grid_dependency_wait();
+    grid_dependents_launch();
     Work w;
     if (!cta_work(a, a.num_kv_heads, w)) return;
 
@@ -564,6 +567,8 @@ __global__ void __launch_bounds__(NW * 32) pa_decode_f32_kernel(const float *__r
                                                                 const float *__restrict__ vc,
                                                                 const DecodeArgs a) {
     constexpr int EPL = D / 32;
+    grid_dependency_wait();
+    grid_dependents_launch();
     Work w;
     if (!cta_work(a, a.num_q_heads, w)) return;
     __shared__ float s_acc[NW][D];
@@ -620,6 +625,7 @@ __global__ void __launch_bounds__(NW * 32) pa_decode_f32_kernel(const float *__r
 template <typename OutT>
 __global__ void __launch_bounds__(128) pa_reduce_kernel(const DecodeArgs a, int D) {
     grid_dependency_wait();
+    grid_dependents_launch();
     const int b = blockIdx.x / a.num_q_heads;
     const int h = blockIdx.x - b * a.num_q_heads;
     int L = a.context_lens[b];
@@ -697,7 +703,18 @@ cudaError_t allow_smem(K kernel, size_t bytes) {
     return cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes);
 }
 
-constexpr int kNW = 4;
+// Warps per CTA and TMA stages per warp of the bf16 kernels (compile-time
+// tunables).  At head_dim 128, 4 warps x 2 stages x 8 KiB lets three CTAs
+// (twelve consumer warps) share an SM; measured on GB300 this streams faster
+// than fewer, deeper rings (4 x 3, 4 x 4, 8 x 2, 8 x 3, 2 x 6).
+#ifndef PA_DECODE_WARPS
+#define PA_DECODE_WARPS 4
+#endif
+#ifndef PA_DECODE_STAGES
+#define PA_DECODE_STAGES 2
+#endif
+constexpr int kNW = PA_DECODE_WARPS;
+constexpr int kStages = PA_DECODE_STAGES;
 
 template <int D, class Consumer, int STAGES>
 pa_status launch_bf16(const DecodeArgs &a, const void *kc, const void *vc, int64_t rows,
@@ -710,8 +727,7 @@ pa_status launch_bf16(const DecodeArgs &a, const void *kc, const void *vc, int64
     cudaError_t e = allow_smem(kernel, smem);
     if (e != cudaSuccess) return cuda_failure(e, "cudaFuncSetAttribute(decode)");
     const int64_t grid = (int64_t)a.num_seqs * a.num_kv_heads * a.max_parts;
-    kernel<<<(unsigned)grid, kNW * 32, smem, stream>>>(kmap, vmap, a);
-    e = cudaGetLastError();
+    e = launch_chained(kernel, dim3((unsigned)grid), dim3(kNW * 32), smem, stream, kmap, vmap, a);
     if (e != cudaSuccess) return cuda_failure(e, "pa_decode_bf16_kernel launch");
     count_launches(1);
     return PA_OK;
@@ -720,14 +736,14 @@ pa_status launch_bf16(const DecodeArgs &a, const void *kc, const void *vc, int64
 template <int D, int G>
 pa_status launch_gqa(const DecodeArgs &a, const void *kc, const void *vc, int64_t rows,
                      cudaStream_t stream) {
-    return launch_bf16<D, GqaConsumer<D, G>, 3>(a, kc, vc, rows, stream);
+    return launch_bf16<D, GqaConsumer<D, G>, kStages>(a, kc, vc, rows, stream);
 }
 
 template <int D>
 pa_status dispatch_bf16(int group, const DecodeArgs &a, const void *kc, const void *vc,
                         int64_t rows, cudaStream_t stream) {
     switch (group) {
-    case 1: return launch_bf16<D, MhaConsumer<D>, 3>(a, kc, vc, rows, stream);
+    case 1: return launch_bf16<D, MhaConsumer<D>, kStages>(a, kc, vc, rows, stream);
     case 2: return launch_gqa<D, 2>(a, kc, vc, rows, stream);
     case 3: return launch_gqa<D, 3>(a, kc, vc, rows, stream);
     case 4: return launch_gqa<D, 4>(a, kc, vc, rows, stream);
@@ -744,9 +760,9 @@ pa_status dispatch_bf16(int group, const DecodeArgs &a, const void *kc, const vo
 template <int D>
 pa_status launch_f32(const DecodeArgs &a, const void *kc, const void *vc, cudaStream_t stream) {
     const int64_t grid = (int64_t)a.num_seqs * a.num_q_heads * a.max_parts;
-    pa_decode_f32_kernel<D, kNW><<<(unsigned)grid, kNW * 32, 0, stream>>>(
-        static_cast<const float *>(kc), static_cast<const float *>(vc), a);
-    cudaError_t e = cudaGetLastError();
+    cudaError_t e = launch_chained(pa_decode_f32_kernel<D, kNW>, dim3((unsigned)grid),
+                                   dim3(kNW * 32), 0, stream, static_cast<const float *>(kc),
+                                   static_cast<const float *>(vc), a);
     if (e != cudaSuccess) return cuda_failure(e, "pa_decode_f32_kernel launch");
     count_launches(1);
     return PA_OK;
@@ -754,29 +770,49 @@ pa_status launch_f32(const DecodeArgs &a, const void *kc, const void *vc, cudaSt
 
 template <typename OutT>
 pa_status launch_reduce(const DecodeArgs &a, int D, cudaStream_t stream) {
-    cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3((unsigned)(a.num_seqs * a.num_q_heads));
-    cfg.blockDim = dim3(128);
-    cfg.dynamicSmemBytes = (size_t)a.max_parts * sizeof(float);
-    cfg.stream = stream;
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-    attr[0].val.programmaticStreamSerializationAllowed = 1;
-    cfg.attrs = attr;
-    cfg.numAttrs = 1;
+    const size_t smem = (size_t)a.max_parts * sizeof(float);
     auto kernel = pa_reduce_kernel<OutT>;
-    if (cfg.dynamicSmemBytes > 48 * 1024) {
-        cudaError_t e = allow_smem(kernel, cfg.dynamicSmemBytes);
+    if (smem > 48 * 1024) {
+        cudaError_t e = allow_smem(kernel, smem);
         if (e != cudaSuccess) return cuda_failure(e, "cudaFuncSetAttribute(reduce)");
     }
-    cudaError_t e = cudaLaunchKernelEx(&cfg, kernel, a, D);
+    cudaError_t e = launch_chained(kernel, dim3((unsigned)(a.num_seqs * a.num_q_heads)), dim3(128),
+                                   smem, stream, a, D);
     if (e != cudaSuccess) return cuda_failure(e, "pa_reduce_kernel launch");
     count_launches(1);
     return PA_OK;
 }
 
-int resolve_partition(int partition_size) {
-    const int p = partition_size == 0 ? kDefaultPartition : partition_size;
+// Streaming multiprocessors of the current device (GB300's 152 when the
+// runtime cannot tell, e.g. in a process without a GPU).
+int sm_count() {
+    int dev = 0, n = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0) {
+        (void)cudaGetLastError();
+        return 152;
+    }
+    return n;
+}
+
+// Partition size for partition_size == 0: the largest of 2048 .. 128 tokens
+// that still gives at least four CTAs per SM (two waves of two resident CTAs)
+// when every sequence is as long as the table allows.  Long partitions amortise
+// each CTA's fixed cost (table slice, pipeline fill, merge); enough CTAs keep
+// every SM streaming to the end.
+int auto_partition(int num_seqs, int heads_axis, int max_blocks) {
+    const int64_t target = 4LL * sm_count();
+    for (int p = 2048; p > 128; p /= 2) {
+        const int pb = p / kBlockSize;
+        const int64_t parts = std::max(1, (max_blocks + pb - 1) / pb);
+        if ((int64_t)num_seqs * heads_axis * parts >= target) return p;
+    }
+    return 128;
+}
+
+int resolve_partition(int partition_size, int num_seqs, int heads_axis, int max_blocks) {
+    const int p = partition_size == 0 ? auto_partition(num_seqs, heads_axis, max_blocks)
+                                      : partition_size;
     if (p < kBlockSize || p > kMaxPartition || p % kBlockSize != 0) return -1;
     return p;
 }
@@ -793,15 +829,25 @@ size_t workspace_for(int num_seqs, int num_q_heads, int head_dim, int max_parts)
 
 using namespace pa;
 
-extern "C" int pa_default_partition_size(void) { return kDefaultPartition; }
+extern "C" int pa_decode_partition_size(int num_seqs, int num_q_heads, int num_kv_heads,
+                                        int max_blocks_per_seq, pa_dtype dtype) {
+    if (num_seqs < 0 || num_q_heads <= 0 || num_kv_heads <= 0 || max_blocks_per_seq < 0 ||
+        (dtype != PA_DTYPE_F32 && dtype != PA_DTYPE_BF16))
+        return -1;
+    const int heads_axis = dtype == PA_DTYPE_BF16 ? num_kv_heads : num_q_heads;
+    return auto_partition(num_seqs, heads_axis, max_blocks_per_seq);
+}
 
-extern "C" size_t pa_decode_workspace_bytes(int num_seqs, int num_q_heads, int head_dim,
-                                            int max_blocks_per_seq, int block_size,
-                                            int partition_size) {
-    const int p = resolve_partition(partition_size);
-    if (p < 0 || num_seqs < 0 || num_q_heads <= 0 || head_dim <= 0 || max_blocks_per_seq < 0 ||
-        block_size != kBlockSize)
+extern "C" size_t pa_decode_workspace_bytes(int num_seqs, int num_q_heads, int num_kv_heads,
+                                            int head_dim, int max_blocks_per_seq, int block_size,
+                                            int partition_size, pa_dtype dtype) {
+    if (num_seqs < 0 || num_q_heads <= 0 || num_kv_heads <= 0 || head_dim <= 0 ||
+        max_blocks_per_seq < 0 || block_size != kBlockSize ||
+        (dtype != PA_DTYPE_F32 && dtype != PA_DTYPE_BF16))
         return (size_t)-1;
+    const int heads_axis = dtype == PA_DTYPE_BF16 ? num_kv_heads : num_q_heads;
+    const int p = resolve_partition(partition_size, num_seqs, heads_axis, max_blocks_per_seq);
+    if (p < 0) return (size_t)-1;
     const int part_blocks = p / kBlockSize;
     const int max_parts = max(1, (max_blocks_per_seq + part_blocks - 1) / part_blocks);
     return workspace_for(num_seqs, num_q_heads, head_dim, max_parts);
@@ -819,9 +865,13 @@ extern "C" pa_status pa_decode(void *out, const void *query, const void *key_cac
         !(scale == scale))
         return PA_ERR_INVALID_ARG;
     if (dtype != PA_DTYPE_F32 && dtype != PA_DTYPE_BF16) return PA_ERR_INVALID_ARG;
-    const int p = resolve_partition(partition_size);
-    if (p < 0) return PA_ERR_INVALID_ARG;
+    const int heads_axis = dtype == PA_DTYPE_BF16 ? num_kv_heads : num_q_heads;
+    if (partition_size != 0 &&
+        (partition_size < kBlockSize || partition_size > kMaxPartition || partition_size % kBlockSize))
+        return PA_ERR_INVALID_ARG;
     if (num_seqs == 0) return PA_OK;
+    const int p = resolve_partition(partition_size, num_seqs, heads_axis, max_blocks_per_seq);
+    if (p < 0) return PA_ERR_INVALID_ARG;
     if (!out || !query || !key_cache || !value_cache || !block_tables || !context_lens)
         return PA_ERR_INVALID_ARG;
     if (!aligned16(out) || !aligned16(query) || !aligned16(key_cache) || !aligned16(value_cache))
@@ -838,7 +888,6 @@ extern "C" pa_status pa_decode(void *out, const void *query, const void *key_cac
     if (rows >= ((int64_t)1 << 31)) return PA_ERR_UNSUPPORTED;
     const int part_blocks = p / kBlockSize;
     const int max_parts = max(1, (max_blocks_per_seq + part_blocks - 1) / part_blocks);
-    const int heads_axis = dtype == PA_DTYPE_BF16 ? num_kv_heads : num_q_heads;
     if ((int64_t)num_seqs * heads_axis * max_parts >= ((int64_t)1 << 31)) return PA_ERR_UNSUPPORTED;
     const size_t need = workspace_for(num_seqs, num_q_heads, head_dim, max_parts);
     if (need > 0 && (workspace == nullptr || workspace_bytes < need || !aligned16(workspace)))

@@ -60,8 +60,9 @@ extern "C" pa_status pa_decode_static_scratch(void *out, const void *query, cons
                                               int num_blocks, float scale, pa_dtype dtype,
                                               int partition_size, int32_t *device_status,
                                               void *stream) {
-    const size_t need = pa_decode_workspace_bytes(num_seqs, num_q_heads, head_dim,
-                                                  max_blocks_per_seq, block_size, partition_size);
+    const size_t need = pa_decode_workspace_bytes(num_seqs, num_q_heads, num_kv_heads, head_dim,
+                                                  max_blocks_per_seq, block_size, partition_size,
+                                                  dtype);
     if (need == (size_t)-1) return PA_ERR_INVALID_ARG;
     if (need > (size_t)PA_STATIC_SCRATCH_BYTES) return PA_ERR_WORKSPACE;
     void *scratch = nullptr;

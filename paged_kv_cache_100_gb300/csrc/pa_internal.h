@@ -4,12 +4,13 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <utility>
+
 #include "pagedkv.h"
 
 namespace pa {
 
 constexpr int kBlockSize = 16;            // tokens per physical block
-constexpr int kDefaultPartition = 512;    // tokens per split-K partition by default
 constexpr int kMaxPartition = 16384;      // largest partition (its table slice lives in smem)
 
 // Adds n to the process-wide launch counter returned by pa_launch_count().
@@ -19,5 +20,26 @@ void count_launches(uint64_t n);
 pa_status cuda_failure(cudaError_t err, const char *where);
 
 inline bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+// Launches a kernel with programmatic stream serialisation: it may be scheduled
+// while the previous kernel in the stream is still running.  Every kernel of
+// this library starts with griddepcontrol.wait (nothing before it reads global
+// memory), so ordering with earlier work is kept; what overlaps is only the
+// launch and CTA set-up of one kernel with the tail of the one before.
+template <typename... KArgs, typename... Args>
+cudaError_t launch_chained(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                           cudaStream_t stream, Args &&...args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
+}
 
 }  // namespace pa

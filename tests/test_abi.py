@@ -56,22 +56,35 @@ def test_status_strings(lib):
     assert lib.pa_status_string(5) == b"PA_ERR_WORKSPACE"
     assert lib.pa_status_string(99) == b"PA_ERR_UNKNOWN"
     assert lib.pa_version() >= 100
-    assert lib.pa_default_partition_size() == 512
+
+
+def test_partition_size_choice(lib):
+    f = lib.pa_decode_partition_size
+    # batch 64 x 32 KV heads at 2048 tokens: plenty of CTAs with the longest partitions
+    assert f(64, 32, 32, 129, 1) == 2048
+    # one short sequence: no partition count reaches four CTAs per SM, smallest choice
+    assert f(1, 8, 8, 4, 1) == 128
+    # few sequences, long contexts: partitions shrink until there are enough CTAs
+    p = f(2, 8, 8, 2048, 1)
+    assert 128 <= p < 2048 and 2 * 8 * (-(-2048 * 16 // p)) >= 4 * 152
+    # f32 counts query heads, bf16 KV heads
+    assert f(8, 32, 4, 256, 0) >= f(8, 32, 4, 256, 1)
+    assert f(-1, 4, 4, 4, 1) == -1 and f(1, 4, 4, 4, 9) == -1
 
 
 def test_workspace_size_rules(lib):
     f = lib.pa_decode_workspace_bytes
     # one partition covers every sequence: nothing needed
-    assert f(64, 32, 128, 32, 16, 512) == 0
-    assert f(64, 32, 128, 32, 16, 0) == 0
-    # 129 blocks -> 2 partitions of 512 tokens
-    rows = 64 * 32 * 5
-    need = f(64, 32, 128, 129 + 256, 16, 512)
+    assert f(64, 32, 32, 128, 32, 16, 512, 1) == 0
+    # 129 + 256 blocks -> 13 partitions of 512 tokens
+    rows = 64 * 32 * 13
+    need = f(64, 32, 32, 128, 129 + 256, 16, 512, 1)
     assert need >= rows * (128 * 4 + 8)
     bad = ctypes.c_size_t(-1).value
-    assert f(1, 1, 128, 4, 16, 100) == bad          # not a multiple of 16
-    assert f(1, 1, 128, 4, 8, 0) == bad             # block size must be 16
-    assert f(1, 1, 128, 4, 16, 32768) == bad        # above the largest partition
+    assert f(1, 1, 1, 128, 4, 16, 100, 1) == bad          # not a multiple of 16
+    assert f(1, 1, 1, 128, 4, 8, 0, 1) == bad             # block size must be 16
+    assert f(1, 1, 1, 128, 4, 16, 32768, 1) == bad        # above the largest partition
+    assert f(1, 1, 1, 128, 4, 16, 512, 5) == bad          # unknown dtype
 
 
 def _decode_args(**over):

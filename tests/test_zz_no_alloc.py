@@ -44,7 +44,7 @@ def test_static_scratch_matches_workspace_decode_twice(built, hq, hkv):
     lens = [1, 100, 513, 1500, 3000]                  # several partitions of 256 tokens
     wl = W.custom_workload(len(lens), hq, hkv, 128, lens, dtype="bf16", seed=hq + hkv)
     partition_size = 256
-    assert pkv.decode_workspace_bytes(wl.num_seqs, hq, 128, wl.max_blocks, partition_size) > 0
+    assert pkv.decode_workspace_bytes(wl.num_seqs, hq, hkv, 128, wl.max_blocks, partition_size) > 0
     status = torch.zeros(1, dtype=torch.int32, device="cuda")
     for call in range(2):
         hv = W.host_values(wl, seed=100 + call)      # new inputs for each call
@@ -68,7 +68,7 @@ def test_static_scratch_rejects_requests_beyond_its_size(built):
     lib = pkv.lib()
     # 64 sequences x 64 heads x 64 partitions of 16 tokens need far more than the array
     wl = W.custom_workload(64, 64, 8, 128, [1024] * 64, dtype="bf16", seed=1)
-    need = pkv.decode_workspace_bytes(64, 64, 128, wl.max_blocks, 16)
+    need = pkv.decode_workspace_bytes(64, 64, 8, 128, wl.max_blocks, 16)
     assert need > (32 << 20)
     q = torch.zeros(64, 64, 128, dtype=torch.bfloat16, device="cuda")
     kc = torch.zeros(wl.num_blocks, 8, 16, 128, dtype=torch.bfloat16, device="cuda")

@@ -17,7 +17,7 @@ Workloads (all block_size 16, layout [num_blocks][num_kv_heads][16][head_dim]):
                  lengths uniform in [512, 4096], values N(0, 0.5) (0.5 read as
                  the standard deviation).
   long_splitk    32 heads MHA, head_dim 128, bf16, batch 8, context 32768 for
-                 every sequence, partition size 512, values N(0, 1).
+                 every sequence, split-K partitions of 512 tokens, values N(0, 1).
   shared_prefix  32 query / 8 KV heads, head_dim 128, bf16, batch 128; every
                  block table starts with the same 64 blocks (a 1024-token
                  prefix) followed by its own suffix blocks (suffix lengths
@@ -52,7 +52,7 @@ class Workload:
     num_blocks: int
     slot_mapping: np.ndarray        # int64 [B]: slot of the appended token
     cow_pairs: np.ndarray = field(default_factory=lambda: np.zeros((0, 2), np.int32))
-    partition_size: int = 512
+    partition_size: int = 0         # 0 = the library's choice
     seed: int = 0
     block_size: int = BLOCK_SIZE
 
@@ -114,7 +114,7 @@ def make_workload(name: str, seed: int = 0) -> Workload:
         need = _blocks(lens + 1)          # room for the appended token too
         tables = _tables_from_slices(order, need)
         return Workload(name, 4, 4, 4, 64, "f32", 1.0, lens, tables, num_blocks,
-                        _append_slots(tables, lens), partition_size=512, seed=seed)
+                        _append_slots(tables, lens), seed=seed)
 
     if name in ("llama7b_mha", "llama70b_gqa", "long_splitk"):
         if name == "llama7b_mha":
@@ -131,7 +131,8 @@ def make_workload(name: str, seed: int = 0) -> Workload:
         order = rng.permutation(num_blocks).astype(np.int32)
         tables = _tables_from_slices(order, need)
         return Workload(name, B, Hq, Hkv, 128, "bf16", std, lens, tables, num_blocks,
-                        _append_slots(tables, lens), partition_size=512, seed=seed)
+                        _append_slots(tables, lens),
+                        partition_size=512 if name == "long_splitk" else 0, seed=seed)
 
     if name == "shared_prefix":
         B, Hq, Hkv, prefix_blocks, n_cow = 128, 32, 8, 64, 16
@@ -151,8 +152,7 @@ def make_workload(name: str, seed: int = 0) -> Workload:
         cow = np.stack([np.full(n_cow, prefix[-1], dtype=np.int32), fresh], axis=1)
         tables[:n_cow, prefix_blocks - 1] = fresh   # these sequences read their copy
         return Workload(name, B, Hq, Hkv, 128, "bf16", 1.0, lens, tables, num_blocks,
-                        _append_slots(tables, lens), cow_pairs=cow.astype(np.int32),
-                        partition_size=512, seed=seed)
+                        _append_slots(tables, lens), cow_pairs=cow.astype(np.int32), seed=seed)
 
     raise KeyError(f"unknown workload {name!r}")
 
