@@ -26,9 +26,10 @@
 //     rows; dot products are finished with a butterfly reduction that leaves
 //     one row's score per lane pair.
 //   * GQA (2..16 query heads share a KV head): the group makes Q.K^T and P.V
-//     dense 16-row tiles, so they run on the tensor cores (mma.sync m16n8k16,
-//     bf16 in, fp32 accumulate); query heads are the M rows, tokens and
-//     head-dim elements the N/K dimensions.  One K/V pass serves the group
+//     dense tiles, so they run on the tensor cores (mma.sync m16n8k16, bf16
+//     in, fp32 accumulate).  Groups of up to 8 use the transposed form (the
+//     block's 16 tokens are the M rows, the heads the 8 N columns); groups of
+//     9..16 put the heads on the M rows.  One K/V pass serves the group
 //     ("Trucos para que el cuaderno sea más fino": query heads share K/V).
 //   * fp32 caches: a plain CUDA-core kernel, one query head per CTA.
 #include <cuda.h>
@@ -432,6 +433,138 @@ struct GqaConsumer {
     }
 };
 
+// 2..8 query heads per KV head on the tensor cores, transposed: the block's 16
+// tokens are the M rows and the query heads the N = 8 columns, so
+//   S^T[16 tok x 8 heads] = K[16 x D] . Q^T[D x 8]        (D/16 mma)
+//   O^T[D x 8 heads]     += V^T[D x 16 tok] . P^T[16 x 8]  (D/16 m-tiles, x2 for hi/lo)
+// and no M row is padding.  The S^T accumulators become the B operand of the
+// second product after a warp-wide 8x8 transpose (movmatrix).  Fragment
+// owner: g = lane / 4, t = lane % 4; this lane holds tokens g and g + 8 for
+// query heads 2t and 2t + 1.
+template <int D, int G>
+struct GqaTConsumer {
+    static_assert(G >= 2 && G <= 8, "one n-tile of query heads");
+    static constexpr int KS = D / 16;   // k-steps of S^T and m-tiles of O^T
+    static constexpr int ROWS = G;
+
+    uint32_t qb[KS][2];
+    float o[KS][4];
+    float m0, m1, l0, l1;               // heads 2t and 2t + 1
+    float scale_log2;
+    int lane, g, t;
+
+    __device__ __forceinline__ void init(const DecodeArgs &a, const Work &w, int lane_) {
+        lane = lane_;
+        g = lane >> 2;
+        t = lane & 3;
+        scale_log2 = a.scale_log2;
+        const __nv_bfloat16 *qg = static_cast<const __nv_bfloat16 *>(a.query) +
+                                  ((size_t)w.b * a.num_q_heads + (size_t)w.head * G) * D;
+        const uint32_t *qrow = reinterpret_cast<const uint32_t *>(qg + (size_t)g * D);
+#pragma unroll
+        for (int ks = 0; ks < KS; ++ks) {
+            qb[ks][0] = g < G ? qrow[(16 * ks + 2 * t) / 2] : 0u;
+            qb[ks][1] = g < G ? qrow[(16 * ks + 8 + 2 * t) / 2] : 0u;
+        }
+#pragma unroll
+        for (int mt = 0; mt < KS; ++mt) o[mt][0] = o[mt][1] = o[mt][2] = o[mt][3] = 0.f;
+        m0 = m1 = -INFINITY;
+        l0 = l1 = 0.f;
+    }
+
+    __device__ __forceinline__ void block(uint32_t ktile, uint32_t vtile, int nvalid) {
+        const int mi = lane >> 3, rr = lane & 7;
+        float s[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+        for (int ks = 0; ks < KS; ++ks) {
+            uint32_t a[4];
+            ldsm_x4(a, swz(ktile, (mi & 1) * 8 + rr, 2 * ks + (mi >> 1)));
+            mma_bf16_16816(s, a, qb[ks][0], qb[ks][1]);
+        }
+        const bool v0 = g < nvalid, v1 = g + 8 < nvalid;
+        s[0] = v0 ? s[0] * scale_log2 : -INFINITY;
+        s[1] = v0 ? s[1] * scale_log2 : -INFINITY;
+        s[2] = v1 ? s[2] * scale_log2 : -INFINITY;
+        s[3] = v1 ? s[3] * scale_log2 : -INFINITY;
+        float mx0 = fmaxf(s[0], s[2]), mx1 = fmaxf(s[1], s[3]);
+#pragma unroll
+        for (int M = 4; M < 32; M <<= 1) {
+            mx0 = fmaxf(mx0, __shfl_xor_sync(kFull, mx0, M));
+            mx1 = fmaxf(mx1, __shfl_xor_sync(kFull, mx1, M));
+        }
+        const float mn0 = fmaxf(m0, mx0), mn1 = fmaxf(m1, mx1);
+        const float a0 = exp2f(m0 - mn0), a1 = exp2f(m1 - mn1);
+        m0 = mn0;
+        m1 = mn1;
+        const float p0 = exp2f(s[0] - mn0), p1 = exp2f(s[1] - mn1);
+        const float p2 = exp2f(s[2] - mn0), p3 = exp2f(s[3] - mn1);
+        l0 = l0 * a0 + (p0 + p2);
+        l1 = l1 * a1 + (p1 + p3);
+#pragma unroll
+        for (int mt = 0; mt < KS; ++mt) {
+            o[mt][0] *= a0;
+            o[mt][1] *= a1;
+            o[mt][2] *= a0;
+            o[mt][3] *= a1;
+        }
+        // P enters the tensor cores as bf16 head + bf16 residual (see GqaConsumer).
+        uint32_t top_hi, top_lo, bot_hi, bot_lo;
+        split_bf16x2(p0, p1, top_hi, top_lo);   // token g
+        split_bf16x2(p2, p3, bot_hi, bot_lo);   // token g + 8
+        const uint32_t bh0 = movmatrix_trans(top_hi), bh1 = movmatrix_trans(bot_hi);
+        const uint32_t bl0 = movmatrix_trans(top_lo), bl1 = movmatrix_trans(bot_lo);
+        if (nvalid < 16) {
+            const int zrows = 16 - nvalid;
+            for (int i = lane; i < zrows * (D / 8); i += 32) {
+                const int r = nvalid + i / (D / 8);
+                const int ch = i % (D / 8);
+                asm volatile("st.shared.v4.u32 [%0], {%1, %1, %1, %1};" ::"r"(swz(vtile, r, ch)),
+                             "r"(0u)
+                             : "memory");
+            }
+            __syncwarp();
+        }
+#pragma unroll
+        for (int mt = 0; mt < KS; ++mt) {
+            uint32_t a[4];
+            ldsm_x4_trans(a, swz(vtile, (mi >> 1) * 8 + rr, 2 * mt + (mi & 1)));
+            mma_bf16_16816(o[mt], a, bh0, bh1);
+            mma_bf16_16816(o[mt], a, bl0, bl1);
+        }
+    }
+
+    __device__ __forceinline__ void finish(float *acc_out, float *m_out, float *l_out) {
+#pragma unroll
+        for (int M = 4; M < 32; M <<= 1) {
+            l0 += __shfl_xor_sync(kFull, l0, M);
+            l1 += __shfl_xor_sync(kFull, l1, M);
+        }
+        const int h0 = 2 * t, h1 = 2 * t + 1;
+#pragma unroll
+        for (int mt = 0; mt < KS; ++mt) {
+            const int d = 16 * mt + g;
+            if (h0 < G) {
+                acc_out[h0 * D + d] = o[mt][0];
+                acc_out[h0 * D + d + 8] = o[mt][2];
+            }
+            if (h1 < G) {
+                acc_out[h1 * D + d] = o[mt][1];
+                acc_out[h1 * D + d + 8] = o[mt][3];
+            }
+        }
+        if (g == 0) {
+            if (h0 < G) {
+                m_out[h0] = m0;
+                l_out[h0] = l0;
+            }
+            if (h1 < G) {
+                m_out[h1] = m1;
+                l_out[h1] = l1;
+            }
+        }
+    }
+};
+
 template <int D, int NW, int STAGES>
 struct TmaLayout {
     static constexpr int kTileBytes = 16 * D * 2;
@@ -704,30 +837,47 @@ cudaError_t allow_smem(K kernel, size_t bytes) {
 }
 
 // Warps per CTA and TMA stages per warp of the bf16 kernels (compile-time
-// tunables).  At head_dim 128, 4 warps x 2 stages x 8 KiB lets three CTAs
-// (twelve consumer warps) share an SM; measured on GB300 this streams faster
-// than fewer, deeper rings (4 x 3, 4 x 4, 8 x 2, 8 x 3, 2 x 6).
-#ifndef PA_DECODE_WARPS
-#define PA_DECODE_WARPS 4
+// tunables, one pair per consumer).  What sets the speed on GB300 is the
+// number of consumer warps resident per SM, not the depth of each ring:
+//  * MHA (72 registers): 8 warps x 1 stage x 8 KiB = 64 KiB, three CTAs and 24
+//    warps per SM;
+//  * GQA groups of 9..16 (heads-as-rows consumer, about 140 registers, so at
+//    most ~14 warps per SM): 4 warps x 2 stages, three CTAs, 12 warps per SM;
+//  * GQA groups of 2..8 (transposed consumer): PA_GQA_WARPS x PA_GQA_STAGES.
+// (Measured alternatives at head_dim 128: 4x1, 2x2, 3x2, 4x3, 4x4, 8x2, 8x3,
+// 2x6 all streamed slower for the consumer they were tried on.)
+#ifndef PA_MHA_WARPS
+#define PA_MHA_WARPS 8
 #endif
-#ifndef PA_DECODE_STAGES
-#define PA_DECODE_STAGES 2
+#ifndef PA_MHA_STAGES
+#define PA_MHA_STAGES 1
 #endif
-constexpr int kNW = PA_DECODE_WARPS;
-constexpr int kStages = PA_DECODE_STAGES;
+#ifndef PA_GQA_WARPS
+#define PA_GQA_WARPS 4
+#endif
+#ifndef PA_GQA_STAGES
+#define PA_GQA_STAGES 2
+#endif
+#ifndef PA_GQA16_WARPS
+#define PA_GQA16_WARPS 4
+#endif
+#ifndef PA_GQA16_STAGES
+#define PA_GQA16_STAGES 2
+#endif
+constexpr int kNW = 4;   // fp32 kernel
 
-template <int D, class Consumer, int STAGES>
+template <int D, class Consumer, int NW, int STAGES>
 pa_status launch_bf16(const DecodeArgs &a, const void *kc, const void *vc, int64_t rows,
                       cudaStream_t stream) {
     CUtensorMap kmap, vmap;
     if (!encode_pool_map(&kmap, kc, rows, D) || !encode_pool_map(&vmap, vc, rows, D))
         return cuda_failure(cudaErrorInvalidValue, "cuTensorMapEncodeTiled");
-    const size_t smem = TmaLayout<D, kNW, STAGES>::smem_bytes(a.part_blocks);
-    auto kernel = pa_decode_bf16_kernel<D, Consumer, kNW, STAGES>;
+    const size_t smem = TmaLayout<D, NW, STAGES>::smem_bytes(a.part_blocks);
+    auto kernel = pa_decode_bf16_kernel<D, Consumer, NW, STAGES>;
     cudaError_t e = allow_smem(kernel, smem);
     if (e != cudaSuccess) return cuda_failure(e, "cudaFuncSetAttribute(decode)");
     const int64_t grid = (int64_t)a.num_seqs * a.num_kv_heads * a.max_parts;
-    e = launch_chained(kernel, dim3((unsigned)grid), dim3(kNW * 32), smem, stream, kmap, vmap, a);
+    e = launch_chained(kernel, dim3((unsigned)grid), dim3(NW * 32), smem, stream, kmap, vmap, a);
     if (e != cudaSuccess) return cuda_failure(e, "pa_decode_bf16_kernel launch");
     count_launches(1);
     return PA_OK;
@@ -736,14 +886,19 @@ pa_status launch_bf16(const DecodeArgs &a, const void *kc, const void *vc, int64
 template <int D, int G>
 pa_status launch_gqa(const DecodeArgs &a, const void *kc, const void *vc, int64_t rows,
                      cudaStream_t stream) {
-    return launch_bf16<D, GqaConsumer<D, G>, kStages>(a, kc, vc, rows, stream);
+    if constexpr (G <= 8)
+        return launch_bf16<D, GqaTConsumer<D, G>, PA_GQA_WARPS, PA_GQA_STAGES>(a, kc, vc, rows,
+                                                                             stream);
+    else
+        return launch_bf16<D, GqaConsumer<D, G>, PA_GQA16_WARPS, PA_GQA16_STAGES>(a, kc, vc, rows,
+                                                                                stream);
 }
 
 template <int D>
 pa_status dispatch_bf16(int group, const DecodeArgs &a, const void *kc, const void *vc,
                         int64_t rows, cudaStream_t stream) {
     switch (group) {
-    case 1: return launch_bf16<D, MhaConsumer<D>, kStages>(a, kc, vc, rows, stream);
+    case 1: return launch_bf16<D, MhaConsumer<D>, PA_MHA_WARPS, PA_MHA_STAGES>(a, kc, vc, rows, stream);
     case 2: return launch_gqa<D, 2>(a, kc, vc, rows, stream);
     case 3: return launch_gqa<D, 3>(a, kc, vc, rows, stream);
     case 4: return launch_gqa<D, 4>(a, kc, vc, rows, stream);
