@@ -85,7 +85,7 @@ uint64_t pa_launch_count(void);
 
 /*
  * Partition size pa_decode uses when it is given partition_size = 0: the
- * largest of 2048, 1024, 512, 256, 128 tokens for which
+ * largest of 4096, 2048, 1024, 512, 256, 128 tokens for which
  * num_seqs * heads * ceil(max_blocks_per_seq * 16 / size) reaches four CTAs
  * per SM of the current device (heads = num_kv_heads for bf16, num_q_heads
  * for f32).  Returns -1 for invalid arguments.

@@ -79,12 +79,16 @@ struct Work {
     int nblk;       // blocks in the partition
 };
 
+// CTAs are numbered partition-major: every sequence's first partition comes
+// first and the shorter trailing partitions (and the empty ones of short
+// sequences) last, so the grid's tail is made of the smallest pieces.
 __device__ __forceinline__ bool cta_work(const DecodeArgs &a, int heads_axis, Work &w) {
     int idx = blockIdx.x;
-    w.part = idx % a.max_parts;
-    idx /= a.max_parts;
-    w.head = idx % heads_axis;
+    const int per_part = a.num_seqs * heads_axis;
+    w.part = idx / per_part;
+    idx -= w.part * per_part;
     w.b = idx / heads_axis;
+    w.head = idx - w.b * heads_axis;
     int L = a.context_lens[w.b];
     const int lmax = a.max_blocks * kBlockSize;
     if (L < 0 || L > lmax) {
@@ -950,14 +954,17 @@ int sm_count() {
     return n;
 }
 
-// Partition size for partition_size == 0: the largest of 2048 .. 128 tokens
-// that still gives at least four CTAs per SM (two waves of two resident CTAs)
-// when every sequence is as long as the table allows.  Long partitions amortise
-// each CTA's fixed cost (table slice, pipeline fill, merge); enough CTAs keep
-// every SM streaming to the end.
+// Partition size for partition_size == 0: the largest of kAutoPartitionMax
+// .. 128 tokens that still gives at least four CTAs per SM when every
+// sequence is as long as the table allows.  Long partitions amortise each
+// CTA's fixed cost (table slice, pipeline fill, merge) and need fewer
+// partials; enough CTAs keep every SM streaming to the end.
+#ifndef PA_AUTO_PARTITION_MAX
+#define PA_AUTO_PARTITION_MAX 4096
+#endif
 int auto_partition(int num_seqs, int heads_axis, int max_blocks) {
     const int64_t target = 4LL * sm_count();
-    for (int p = 2048; p > 128; p /= 2) {
+    for (int p = PA_AUTO_PARTITION_MAX; p > 128; p /= 2) {
         const int pb = p / kBlockSize;
         const int64_t parts = std::max(1, (max_blocks + pb - 1) / pb);
         if ((int64_t)num_seqs * heads_axis * parts >= target) return p;

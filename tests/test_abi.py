@@ -60,13 +60,14 @@ def test_status_strings(lib):
 
 def test_partition_size_choice(lib):
     f = lib.pa_decode_partition_size
-    # batch 64 x 32 KV heads at 2048 tokens: plenty of CTAs with the longest partitions
-    assert f(64, 32, 32, 129, 1) == 2048
+    # batch 64 x 32 KV heads up to 2064 tokens: plenty of CTAs with the longest partitions
+    assert f(64, 32, 32, 129, 1) == 4096
+    assert f(8, 32, 32, 129, 1) == 1024
     # one short sequence: no partition count reaches four CTAs per SM, smallest choice
     assert f(1, 8, 8, 4, 1) == 128
     # few sequences, long contexts: partitions shrink until there are enough CTAs
     p = f(2, 8, 8, 2048, 1)
-    assert 128 <= p < 2048 and 2 * 8 * (-(-2048 * 16 // p)) >= 4 * 152
+    assert 128 <= p < 4096 and 2 * 8 * (-(-2048 * 16 // p)) >= 4 * 152
     # f32 counts query heads, bf16 KV heads
     assert f(8, 32, 4, 256, 0) >= f(8, 32, 4, 256, 1)
     assert f(-1, 4, 4, 4, 1) == -1 and f(1, 4, 4, 4, 9) == -1
