@@ -32,6 +32,7 @@ _lib = None
 
 F32 = 0
 BF16 = 1
+FP8_E4M3 = 2
 
 
 def build(force: bool = False) -> str:
@@ -57,6 +58,16 @@ def _load():
             lib.pao_paged_decode.argtypes = [vp, vp, vp, vp, i32, vp, vp, i32, i32, i32, i32,
                                              i32, i32, i32, dbl, vp, i32, i32]
             lib.pao_paged_decode.restype = i32
+            lib.pao_paged_decode_ex.argtypes = [vp, vp, i32, vp, vp, i32, vp, vp, vp, vp, i32,
+                                                i32, i32, i32, i32, i32, i32, dbl, vp, i32, i32]
+            lib.pao_paged_decode_ex.restype = i32
+            lib.pao_cache_write_fp8.argtypes = [vp, vp, vp, vp, vp, i32, i32, i32, i32, i32, vp,
+                                                vp]
+            lib.pao_cache_write_fp8.restype = i32
+            lib.pao_e4m3_value.argtypes = [ctypes.c_uint8]
+            lib.pao_e4m3_value.restype = dbl
+            lib.pao_e4m3_encode.argtypes = [ctypes.c_float]
+            lib.pao_e4m3_encode.restype = ctypes.c_uint8
             lib.pao_cache_write.argtypes = [vp, vp, vp, vp, vp, i32, i32, i32, i32, i32, i32]
             lib.pao_cache_write.restype = i32
             lib.pao_block_copy.argtypes = [vp, vp, vp, i32, i32, i32, i32, i32, i32]
@@ -72,7 +83,10 @@ def _dtype_code(a: np.ndarray) -> int:
         return F32
     if a.dtype == np.uint16:
         return BF16
-    raise TypeError(f"oracle expects float32 or uint16 (bfloat16 bits), got {a.dtype}")
+    if a.dtype == np.uint8:
+        return FP8_E4M3
+    raise TypeError(f"oracle expects float32, uint16 (bfloat16 bits) or uint8 (E4M3 codes), "
+                    f"got {a.dtype}")
 
 
 def _ptr(a: np.ndarray):
@@ -84,20 +98,28 @@ def max_threads() -> int:
 
 
 def paged_decode(query, key_cache, value_cache, block_tables, context_lens, scale,
-                 sel=None, threads: int = 1) -> np.ndarray:
+                 sel=None, threads: int = 1, k_scales=None, v_scales=None) -> np.ndarray:
     """fp64 paged decode attention.
 
-    query [B][Hq][D]; key_cache/value_cache [NB][Hkv][BS][D]; block_tables int32
-    [B][max_blocks]; context_lens int32 [B].  Returns float64 [B][Hq][D], or
-    [n][D] for the (b, h) pairs of ``sel`` (an int array of shape [n, 2]).
+    query [B][Hq][D] (float32 or bfloat16 bits); key_cache/value_cache
+    [NB][Hkv][BS][D] of the same type, or E4M3 codes (uint8) with per-KV-head
+    ``k_scales`` / ``v_scales``; block_tables int32 [B][max_blocks]; context_lens
+    int32 [B].  Returns float64 [B][Hq][D], or [n][D] for the (b, h) pairs of
+    ``sel`` (an int array of shape [n, 2]).
     """
     lib = _load()
     query = np.ascontiguousarray(query)
     key_cache = np.ascontiguousarray(key_cache)
     value_cache = np.ascontiguousarray(value_cache)
-    code = _dtype_code(query)
-    if _dtype_code(key_cache) != code or _dtype_code(value_cache) != code:
-        raise TypeError("query, key_cache and value_cache must share one element type")
+    q_code = _dtype_code(query)
+    kv_code = _dtype_code(key_cache)
+    if _dtype_code(value_cache) != kv_code:
+        raise TypeError("key_cache and value_cache must share one element type")
+    if kv_code == FP8_E4M3:
+        if k_scales is None or v_scales is None:
+            raise ValueError("E4M3 pools need k_scales and v_scales")
+    elif q_code != kv_code:
+        raise TypeError("query and unquantised pools must share one element type")
     block_tables = np.ascontiguousarray(block_tables, dtype=np.int32)
     context_lens = np.ascontiguousarray(context_lens, dtype=np.int32)
     B, Hq, D = query.shape
@@ -106,6 +128,10 @@ def paged_decode(query, key_cache, value_cache, block_tables, context_lens, scal
         raise ValueError("shape mismatch between query and caches")
     if block_tables.ndim != 2 or block_tables.shape[0] != B or context_lens.shape != (B,):
         raise ValueError("block_tables must be [B][max_blocks] and context_lens [B]")
+    ks = vs = None
+    if kv_code == FP8_E4M3:
+        ks = np.ascontiguousarray(k_scales, dtype=np.float32).reshape(Hkv)
+        vs = np.ascontiguousarray(v_scales, dtype=np.float32).reshape(Hkv)
     if sel is None:
         out = np.zeros((B, Hq, D), dtype=np.float64)
         sel_arr, n_sel = None, 0
@@ -113,13 +139,54 @@ def paged_decode(query, key_cache, value_cache, block_tables, context_lens, scal
         sel_arr = np.ascontiguousarray(np.asarray(sel, dtype=np.int32).reshape(-1, 2))
         n_sel = sel_arr.shape[0]
         out = np.zeros((n_sel, D), dtype=np.float64)
-    rc = lib.pao_paged_decode(_ptr(out), _ptr(query), _ptr(key_cache), _ptr(value_cache), code,
-                              _ptr(block_tables), _ptr(context_lens), B, Hq, Hkv, D, BS,
-                              block_tables.shape[1], NB, float(scale),
-                              None if sel_arr is None else _ptr(sel_arr), n_sel, int(threads))
+    rc = lib.pao_paged_decode_ex(out.ctypes.data, query.ctypes.data, q_code, key_cache.ctypes.data,
+                                 value_cache.ctypes.data, kv_code,
+                                 None if ks is None else ks.ctypes.data,
+                                 None if vs is None else vs.ctypes.data,
+                                 block_tables.ctypes.data, context_lens.ctypes.data, B, Hq, Hkv,
+                                 D, BS, block_tables.shape[1], NB, float(scale),
+                                 None if sel_arr is None else sel_arr.ctypes.data, n_sel,
+                                 int(threads))
     if rc != 0:
         raise ValueError(f"oracle paged_decode failed with code {rc}")
     return out
+
+
+def e4m3_value(codes) -> np.ndarray:
+    """float64 values of E4M3 codes (NaN for the two NaN codes)."""
+    lib = _load()
+    c = np.asarray(codes, dtype=np.uint8)
+    return np.array([lib.pao_e4m3_value(int(x)) for x in c.reshape(-1)]).reshape(c.shape)
+
+
+def e4m3_encode(values) -> np.ndarray:
+    """E4M3 codes of float32 values (nearest, ties to even, saturating at 448)."""
+    lib = _load()
+    v = np.asarray(values, dtype=np.float32)
+    return np.array([lib.pao_e4m3_encode(float(x)) for x in v.reshape(-1)],
+                    dtype=np.uint8).reshape(v.shape)
+
+
+def cache_write_fp8(key_cache, value_cache, key, value, slot_mapping, k_scales, v_scales):
+    """In-place quantising cache write: bfloat16 rows [T][Hkv][D] into E4M3 pools."""
+    lib = _load()
+    for a in (key_cache, value_cache):
+        if not a.flags.c_contiguous or a.dtype != np.uint8:
+            raise ValueError("pools must be C-contiguous uint8 (written in place)")
+    key = np.ascontiguousarray(key, dtype=np.uint16)
+    value = np.ascontiguousarray(value, dtype=np.uint16)
+    slot_mapping = np.ascontiguousarray(slot_mapping, dtype=np.int64)
+    NB, Hkv, BS, D = key_cache.shape
+    T = slot_mapping.shape[0]
+    if key.shape != (T, Hkv, D) or value.shape != (T, Hkv, D):
+        raise ValueError("key/value must be [T][Hkv][D]")
+    ks = np.ascontiguousarray(k_scales, dtype=np.float32).reshape(Hkv)
+    vs = np.ascontiguousarray(v_scales, dtype=np.float32).reshape(Hkv)
+    rc = lib.pao_cache_write_fp8(key_cache.ctypes.data, value_cache.ctypes.data, key.ctypes.data,
+                                 value.ctypes.data, slot_mapping.ctypes.data, T, Hkv, D, BS, NB,
+                                 ks.ctypes.data, vs.ctypes.data)
+    if rc != 0:
+        raise ValueError(f"oracle cache_write_fp8 failed with code {rc}")
 
 
 def cache_write(key_cache, value_cache, key, value, slot_mapping) -> None:

@@ -34,7 +34,13 @@
  *   context_lens            : int32 [num_seqs]
  *   slot_mapping            : int64 [num_tokens], slot = block * block_size + offset,
  *                             a negative slot means "no write"
- * Element types: dtype 0 = float32, dtype 1 = bfloat16 (raw 16-bit patterns).
+ * Element types: dtype 0 = float32, dtype 1 = bfloat16 (raw 16-bit patterns),
+ * dtype 2 = FP8 E4M3 codes (K/V pools only, each KV head with its own scale:
+ * the stored value is code_value * scale[kv_head]).  The pages name FP8
+ * caches ("KV cache: la memoria de trabajo que sostiene la inferencia LLM",
+ * "Trucos para que el cuaderno sea más fino": quantising the cache to FP8
+ * halves it); the format itself is the E4M3 ("E4M3FN") encoding of the OCP
+ * 8-bit floating point specification.
  * Every element is widened exactly to double before any arithmetic.
  */
 #include <math.h>
@@ -50,17 +56,76 @@
 #define PAO_ERR_INDEX 2
 #define PAO_ERR_NOMEM 3
 
+/* Value of an E4M3 code: 1 sign bit, 4 exponent bits with bias 7, 3 mantissa
+ * bits; exponent field 0 holds subnormals (m * 2^-9); S.1111.111 is NaN; there
+ * are no infinities (the largest finite value is 1.75 * 2^8 = 448). */
+double pao_e4m3_value(uint8_t code)
+{
+    const int sign = code >> 7, e = (code >> 3) & 15, m = code & 7;
+    double v;
+    if (e == 15 && m == 7)
+        return NAN;
+    if (e == 0)
+        v = ldexp((double)m, -9);
+    else
+        v = ldexp(1.0 + m / 8.0, e - 7);
+    return sign ? -v : v;
+}
+
+/* Nearest integer to y >= 0, halfway cases to the even integer. */
+static double round_half_even(double y)
+{
+    double fl = floor(y);
+    double diff = y - fl;
+    if (diff > 0.5)
+        return fl + 1.0;
+    if (diff < 0.5)
+        return fl;
+    return fmod(fl, 2.0) == 0.0 ? fl : fl + 1.0;
+}
+
+/* E4M3 code of a float: the nearest E4M3 value (ties to an even mantissa);
+ * magnitudes of 448 or more give +-448 (saturation); NaN gives 0x7F. */
+uint8_t pao_e4m3_encode(float x)
+{
+    if (x != x)
+        return 0x7F;
+    const int sign = signbit(x) ? 1 : 0;
+    const double a = fabs((double)x);
+    uint8_t mag;
+    if (a >= 448.0) {
+        mag = 0x7E;
+    } else if (a < ldexp(1.0, -6)) {
+        /* subnormal range: multiples of 2^-9 (8 of them reach the smallest normal) */
+        const int n = (int)round_half_even(a * 512.0);
+        mag = (uint8_t)(n == 8 ? (1 << 3) : n);
+    } else {
+        int e2;
+        (void)frexp(a, &e2);              /* a = f * 2^e2, f in [0.5, 1) */
+        int E = e2 - 1;                   /* a in [2^E, 2^(E+1)) */
+        int n = (int)round_half_even(a / ldexp(1.0, E - 3));   /* 8 .. 16 */
+        if (n == 16) {
+            E += 1;
+            n = 8;
+        }
+        mag = (uint8_t)(((E + 7) << 3) | (n - 8));
+    }
+    return (uint8_t)((sign << 7) | mag);
+}
+
 /* Widen one stored element to double.  bfloat16 is the upper half of an IEEE
  * binary32, so shifting its 16 bits up by 16 gives the float exactly. */
 static double widen(const void *base, int64_t idx, int dtype)
 {
     if (dtype == 0) {
         return (double)((const float *)base)[idx];
-    } else {
+    } else if (dtype == 1) {
         uint32_t bits = ((uint32_t)((const uint16_t *)base)[idx]) << 16;
         float f;
         memcpy(&f, &bits, sizeof f);
         return (double)f;
+    } else {
+        return pao_e4m3_value(((const uint8_t *)base)[idx]);
     }
 }
 
@@ -68,11 +133,11 @@ static double widen(const void *base, int64_t idx, int dtype)
  * Two passes over the scores (maximum, then normalised weights), exactly the
  * textbook softmax(q K^T * scale) V with the K/V rows gathered through the
  * block table in logical token order. */
-static int attend_one(double *out, const void *query, const void *key_cache,
-                      const void *value_cache, int dtype,
-                      const int32_t *block_tables, const int32_t *context_lens,
-                      int b, int h, int num_q_heads, int num_kv_heads,
-                      int head_dim, int block_size, int max_blocks,
+static int attend_one(double *out, const void *query, int q_dtype, const void *key_cache,
+                      const void *value_cache, int kv_dtype, const float *k_scales,
+                      const float *v_scales, const int32_t *block_tables,
+                      const int32_t *context_lens, int b, int h, int num_q_heads,
+                      int num_kv_heads, int head_dim, int block_size, int max_blocks,
                       int num_blocks, double scale)
 {
     const int group = num_q_heads / num_kv_heads;
@@ -108,12 +173,16 @@ static int attend_one(double *out, const void *query, const void *key_cache,
         row[t] = (((int64_t)phys * num_kv_heads + kvh) * block_size + offset) * head_dim;
     }
 
+    /* Stored K/V values are code_value * per-head scale for FP8 pools. */
+    const double ks = k_scales ? (double)k_scales[kvh] : 1.0;
+    const double vs = v_scales ? (double)v_scales[kvh] : 1.0;
+
     /* Scores s_t = scale * <q, k_t>. */
     const int64_t qbase = ((int64_t)b * num_q_heads + h) * head_dim;
     for (t = 0; t < L; ++t) {
         double dot = 0.0;
         for (d = 0; d < head_dim; ++d)
-            dot += widen(query, qbase + d, dtype) * widen(key_cache, row[t] + d, dtype);
+            dot += widen(query, qbase + d, q_dtype) * (widen(key_cache, row[t] + d, kv_dtype) * ks);
         score[t] = scale * dot;
     }
 
@@ -130,7 +199,7 @@ static int attend_one(double *out, const void *query, const void *key_cache,
     for (t = 0; t < L; ++t) {
         double w = exp(score[t] - mx) / denom;
         for (d = 0; d < head_dim; ++d)
-            out[d] += w * widen(value_cache, row[t] + d, dtype);
+            out[d] += w * (widen(value_cache, row[t] + d, kv_dtype) * vs);
     }
 
     free(score);
@@ -143,21 +212,23 @@ static int attend_one(double *out, const void *query, const void *key_cache,
  *   out : double; [num_seqs][num_q_heads][head_dim] when sel == NULL,
  *         otherwise [n_sel][head_dim] for the (b, h) pairs listed in sel
  *         (sel holds 2 * n_sel int32 values: b0, h0, b1, h1, ...).
+ *   q_dtype, kv_dtype : element types of the query and of the pools; for
+ *         FP8 pools k_scales / v_scales hold one scale per KV head (NULL = 1).
  *   num_threads : OpenMP threads over (b, h) pairs; 1 = serial.
  * Returns 0, or a nonzero code for bad arguments or an out-of-range table
  * entry (the oracle never reads outside the pools).
  */
-int pao_paged_decode(double *out, const void *query, const void *key_cache,
-                     const void *value_cache, int dtype,
-                     const int32_t *block_tables, const int32_t *context_lens,
-                     int num_seqs, int num_q_heads, int num_kv_heads,
-                     int head_dim, int block_size, int max_blocks,
-                     int num_blocks, double scale, const int32_t *sel,
-                     int n_sel, int num_threads)
+int pao_paged_decode_ex(double *out, const void *query, int q_dtype, const void *key_cache,
+                        const void *value_cache, int kv_dtype, const float *k_scales,
+                        const float *v_scales, const int32_t *block_tables,
+                        const int32_t *context_lens, int num_seqs, int num_q_heads,
+                        int num_kv_heads, int head_dim, int block_size, int max_blocks,
+                        int num_blocks, double scale, const int32_t *sel, int n_sel,
+                        int num_threads)
 {
     if (!out || !query || !key_cache || !value_cache || !block_tables || !context_lens)
         return PAO_ERR_ARG;
-    if (dtype != 0 && dtype != 1)
+    if (q_dtype < 0 || q_dtype > 1 || kv_dtype < 0 || kv_dtype > 2)
         return PAO_ERR_ARG;
     if (num_seqs < 0 || num_q_heads <= 0 || num_kv_heads <= 0 || head_dim <= 0 ||
         block_size <= 0 || max_blocks < 0 || num_blocks < 0)
@@ -185,10 +256,9 @@ int pao_paged_decode(double *out, const void *query, const void *key_cache,
         if (b < 0 || b >= num_seqs || h < 0 || h >= num_q_heads)
             rc = PAO_ERR_ARG;
         else
-            rc = attend_one(out + i * head_dim, query, key_cache, value_cache, dtype,
-                            block_tables, context_lens, b, h, num_q_heads,
-                            num_kv_heads, head_dim, block_size, max_blocks,
-                            num_blocks, scale);
+            rc = attend_one(out + i * head_dim, query, q_dtype, key_cache, value_cache, kv_dtype,
+                            k_scales, v_scales, block_tables, context_lens, b, h, num_q_heads,
+                            num_kv_heads, head_dim, block_size, max_blocks, num_blocks, scale);
         if (rc != PAO_OK) {
 #ifdef _OPENMP
 #pragma omp critical
@@ -197,6 +267,23 @@ int pao_paged_decode(double *out, const void *query, const void *key_cache,
         }
     }
     return status;
+}
+
+/* Paged decode attention with query and pools of one element type (0 or 1). */
+int pao_paged_decode(double *out, const void *query, const void *key_cache,
+                     const void *value_cache, int dtype,
+                     const int32_t *block_tables, const int32_t *context_lens,
+                     int num_seqs, int num_q_heads, int num_kv_heads,
+                     int head_dim, int block_size, int max_blocks,
+                     int num_blocks, double scale, const int32_t *sel,
+                     int n_sel, int num_threads)
+{
+    if (dtype != 0 && dtype != 1)
+        return PAO_ERR_ARG;
+    return pao_paged_decode_ex(out, query, dtype, key_cache, value_cache, dtype, NULL, NULL,
+                               block_tables, context_lens, num_seqs, num_q_heads, num_kv_heads,
+                               head_dim, block_size, max_blocks, num_blocks, scale, sel, n_sel,
+                               num_threads);
 }
 
 /*
@@ -227,6 +314,45 @@ int pao_cache_write(void *key_cache, void *value_cache, const void *key,
             int64_t src = ((int64_t)i * num_kv_heads + kvh) * row_bytes;
             memcpy((char *)key_cache + dst, (const char *)key + src, (size_t)row_bytes);
             memcpy((char *)value_cache + dst, (const char *)value + src, (size_t)row_bytes);
+        }
+    }
+    return PAO_OK;
+}
+
+/*
+ * Cache write into FP8 pools: every element x of a new token's bfloat16 K (V)
+ * row is quantised to the E4M3 code of the float32 quotient x / scale[kv_head]
+ * (IEEE single-precision division, then pao_e4m3_encode) and stored at the
+ * token's slot, as pao_cache_write does for unquantised rows.
+ */
+int pao_cache_write_fp8(uint8_t *key_cache, uint8_t *value_cache, const uint16_t *key,
+                        const uint16_t *value, const int64_t *slot_mapping, int num_tokens,
+                        int num_kv_heads, int head_dim, int block_size, int num_blocks,
+                        const float *k_scales, const float *v_scales)
+{
+    if (!key_cache || !value_cache || !key || !value || !k_scales || !v_scales ||
+        (!slot_mapping && num_tokens > 0))
+        return PAO_ERR_ARG;
+    int i, kvh, d;
+    for (i = 0; i < num_tokens; ++i) {
+        int64_t s = slot_mapping[i];
+        if (s < 0)
+            continue;
+        if (s >= (int64_t)num_blocks * block_size)
+            return PAO_ERR_INDEX;
+        int64_t blk = s / block_size;
+        int64_t off = s % block_size;
+        for (kvh = 0; kvh < num_kv_heads; ++kvh) {
+            int64_t dst = ((blk * num_kv_heads + kvh) * block_size + off) * head_dim;
+            int64_t src = ((int64_t)i * num_kv_heads + kvh) * head_dim;
+            for (d = 0; d < head_dim; ++d) {
+                float kx = (float)widen(key, src + d, 1);
+                float vx = (float)widen(value, src + d, 1);
+                float kq = kx / k_scales[kvh];
+                float vq = vx / v_scales[kvh];
+                key_cache[dst + d] = pao_e4m3_encode(kq);
+                value_cache[dst + d] = pao_e4m3_encode(vq);
+            }
         }
     }
     return PAO_OK;

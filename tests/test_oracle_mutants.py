@@ -31,10 +31,25 @@ MUTANTS = {
     "write_offset": ("int64_t off = s % block_size;", "int64_t off = (s + 1) % block_size;"),
     "write_skips_v": ("memcpy((char *)value_cache + dst, (const char *)value + src, (size_t)row_bytes);",
                       ";"),
+    "e4m3_subnormal_step": ("v = ldexp((double)m, -9);", "v = ldexp((double)m, -8);"),
+    "e4m3_bias": ("v = ldexp(1.0 + m / 8.0, e - 7);", "v = ldexp(1.0 + m / 8.0, e - 8);"),
+    "e4m3_ties_away": ("return fmod(fl, 2.0) == 0.0 ? fl : fl + 1.0;", "return fl + 1.0;"),
+    "e4m3_no_saturation": ("mag = 0x7E;", "mag = 0x7F;"),
+    "fp8_k_scale_ignored": ("const double ks = k_scales ? (double)k_scales[kvh] : 1.0;",
+                            "const double ks = 1.0;"),
+    "fp8_write_multiplies": ("float kq = kx / k_scales[kvh];", "float kq = kx * k_scales[kvh];"),
     "copy_skips_v": ("memmove((char *)value_cache + dst * block_bytes,", "(void)(value_cache + dst * block_bytes,"),
 }
 
+from tests import test_oracle_fp8_pins as fp8pins  # noqa: E402
+
 PIN_FUNCS = [
+    lambda g: fp8pins.test_every_code_value_matches_torch(),
+    lambda g: fp8pins.test_encode_matches_torch_below_overflow(),
+    lambda g: fp8pins.test_encode_saturates_and_keeps_nan(),
+    lambda g: fp8pins.test_every_finite_code_round_trips(),
+    lambda g: fp8pins.test_fp8_decode_equals_library_attention_on_dequantised_values(8, 2, 128),
+    lambda g: fp8pins.test_fp8_cache_write_codes_match_torch_quantisation(),
     lambda g: pins.test_matches_library_attention_on_contiguous_tokens(4, 4, 4, 64, [1, 17, 33, 64], 0.125),
     lambda g: pins.test_matches_library_attention_on_contiguous_tokens(3, 8, 2, 128, [15, 16, 100], 0.0883883),
     lambda g: pins.test_bf16_inputs_widen_exactly(),
@@ -66,7 +81,9 @@ def test_pins_catch_planted_mistake(name, tmp_path, golden_dir, monkeypatch):
     so = _compile(tmp_path, name, text.replace(old, new))
     real = oracle._load()
     mutant = ctypes.CDLL(so)
-    for fn in ("pao_paged_decode", "pao_cache_write", "pao_block_copy", "pao_max_threads"):
+    for fn in ("pao_paged_decode", "pao_paged_decode_ex", "pao_cache_write",
+               "pao_cache_write_fp8", "pao_e4m3_value", "pao_e4m3_encode", "pao_block_copy",
+               "pao_max_threads"):
         getattr(mutant, fn).argtypes = getattr(real, fn).argtypes
         getattr(mutant, fn).restype = getattr(real, fn).restype
     monkeypatch.setattr(oracle, "_lib", mutant)
