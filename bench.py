@@ -46,18 +46,19 @@ def kv_bytes_per_token(n_layers, n_kv_heads, head_dim, bytes_per_elem=2) -> int:
     return 2 * n_layers * n_kv_heads * head_dim * bytes_per_elem
 
 
-def decode_algorithmic_bytes(wl: W.Workload, lens=None) -> dict:
+def decode_algorithmic_bytes(wl: W.Workload, lens=None, kv_elem_bytes=None) -> dict:
     """Least bytes one decode call moves: K/V of every context token, Q, O, tables, lengths."""
     lens = wl.step_context_lens if lens is None else np.asarray(lens)
     lens = lens.astype(np.int64)
     e = wl.elem_bytes
-    kv = int(lens.sum()) * kv_bytes_per_token(1, wl.num_kv_heads, wl.head_dim, e)
+    kv = int(lens.sum()) * kv_bytes_per_token(1, wl.num_kv_heads, wl.head_dim,
+                                              kv_elem_bytes or e)
     q = wl.num_seqs * wl.num_q_heads * wl.head_dim * e
     tables = int((-(-lens // 16)).sum()) * 4 + 4 * wl.num_seqs
     return {"kv": kv, "q": q, "o": q, "tables": tables, "total": kv + 2 * q + tables}
 
 
-def unique_kv_bytes(wl: W.Workload, lens=None) -> int:
+def unique_kv_bytes(wl: W.Workload, lens=None, kv_elem_bytes=None) -> int:
     """K/V bytes of distinct (block, slot) pairs read: shared prefix blocks count once."""
     lens = wl.step_context_lens if lens is None else np.asarray(lens)
     seen = {}
@@ -66,7 +67,8 @@ def unique_kv_bytes(wl: W.Workload, lens=None) -> int:
         for j in range(-(-L // 16)):
             phys = int(wl.block_tables[b, j])
             seen[phys] = max(seen.get(phys, 0), min(16, L - 16 * j))
-    return sum(seen.values()) * kv_bytes_per_token(1, wl.num_kv_heads, wl.head_dim, wl.elem_bytes)
+    return sum(seen.values()) * kv_bytes_per_token(1, wl.num_kv_heads, wl.head_dim,
+                                                   kv_elem_bytes or wl.elem_bytes)
 
 
 def step_write_bytes(wl: W.Workload) -> int:
@@ -239,6 +241,28 @@ def measured_traffic(workload: str):
 # ---------------------------------------------------------------------------
 # GPU arm
 # ---------------------------------------------------------------------------
+class StepOps:
+    """The library calls of one step for bf16 (or f32) pools or FP8 pools."""
+
+    def __init__(self, pkv, wl, kc, vc, ks, vs, P, ws):
+        self.pkv, self.wl, self.kc, self.vc, self.ks, self.vs = pkv, wl, kc, vc, ks, vs
+        self.P, self.ws = P, ws
+        self.fp8 = ks is not None
+
+    def write(self, kn, vn, slots):
+        if self.fp8:
+            self.pkv.cache_write_fp8(self.kc, self.vc, kn, vn, slots, self.ks, self.vs)
+        else:
+            self.pkv.cache_write(self.kc, self.vc, kn, vn, slots)
+
+    def decode(self, q, bt, lens, out):
+        if self.fp8:
+            self.pkv.decode_fp8(q, self.kc, self.vc, self.ks, self.vs, bt, lens, self.wl.scale,
+                                out=out, partition_size=self.P, workspace=self.ws)
+        else:
+            self.pkv.decode(q, self.kc, self.vc, bt, lens, self.wl.scale, out=out,
+                            partition_size=self.P, workspace=self.ws)
+
 def run_gpu(args):
     import torch
     rank, world, local = dist_env()
@@ -254,27 +278,34 @@ def run_gpu(args):
     import paged_kv_cache_100_gb300 as pkv
 
     wl = W.make_workload(args.workload, seed=args.seed)
-    q, kc, vc, kn, vn = W.device_values(wl, dev, seed=args.seed + 17 + rank)
+    fp8 = args.kv_dtype == "fp8"
+    if fp8:
+        q, kc, vc, kn, vn, ks, vs = W.fp8_device_values(wl, dev, seed=args.seed + 17 + rank)
+    else:
+        q, kc, vc, kn, vn = W.device_values(wl, dev, seed=args.seed + 17 + rank)
+        ks = vs = None
     bt = torch.from_numpy(wl.block_tables).to(dev)
     lens = torch.from_numpy(wl.step_context_lens).to(dev)
     slots = torch.from_numpy(wl.slot_mapping).to(dev)
     pairs = torch.from_numpy(wl.cow_pairs).to(dev)
     has_cow = wl.cow_pairs.shape[0] > 0
+    kv_dtype = "fp8" if fp8 else wl.dtype
     P = args.partition_size or wl.partition_size or pkv.decode_partition_size(
-        wl.num_seqs, wl.num_q_heads, wl.num_kv_heads, wl.max_blocks, wl.dtype)
+        wl.num_seqs, wl.num_q_heads, wl.num_kv_heads, wl.max_blocks, kv_dtype)
     out = torch.empty_like(q)
     ws = torch.empty(max(pkv.decode_workspace_bytes(wl.num_seqs, wl.num_q_heads, wl.num_kv_heads,
-                                                    wl.head_dim, wl.max_blocks, P, wl.dtype), 16),
+                                                    wl.head_dim, wl.max_blocks, P, kv_dtype), 16),
                      dtype=torch.uint8, device=dev)
     stream = torch.cuda.current_stream(dev)
+    ops = StepOps(pkv, wl, kc, vc, ks, vs, P, ws)
 
     def step(ev_pre=None, ev_post=None):
-        pkv.cache_write(kc, vc, kn, vn, slots)
+        ops.write(kn, vn, slots)
         if has_cow:
             pkv.block_copy(kc, vc, pairs)
         if ev_pre is not None:
             ev_pre.record(stream)
-        pkv.decode(q, kc, vc, bt, lens, wl.scale, out=out, partition_size=P, workspace=ws)
+        ops.decode(q, bt, lens, out)
         if ev_post is not None:
             ev_post.record(stream)
 
@@ -318,12 +349,13 @@ def run_gpu(args):
     ms_per_step = ms_total / K
 
     # end to end through the public API: pinned host inputs in, output back, every step
-    e2e = run_e2e(args, pkv, wl, q, kc, vc, kn, vn, dev, stream, P, ws)
+    e2e = run_e2e(args, pkv, wl, q, kc, vc, kn, vn, dev, stream, ops)
 
     if rank != 0:
         return None
-    logical = decode_algorithmic_bytes(wl)
-    unique_kv = unique_kv_bytes(wl)
+    kv_e = 1 if fp8 else None
+    logical = decode_algorithmic_bytes(wl, kv_elem_bytes=kv_e)
+    unique_kv = unique_kv_bytes(wl, kv_elem_bytes=kv_e)
     hbm_bytes = logical["total"] - logical["kv"] + unique_kv
     peak, peak_kind = load_peaks()
     achieved = hbm_bytes / (decode_ms * 1e-3) / 1e9
@@ -340,9 +372,9 @@ def run_gpu(args):
         "higher_is_better": True,
         "scaling": "weak",
         "vs_baseline": None,
-        "dtype": wl.dtype,
+        "dtype": "fp8_e4m3 K/V, bf16 Q/O" if fp8 else wl.dtype,
         "data": "synthetic (seeded; N(0, %g) values, shuffled block pool)" % wl.value_std,
-        "config": workload_config(wl, P, world),
+        "config": workload_config(wl, P, world, kv_dtype),
         "decode_ms": decode_ms,
         "ms_per_step_with_call_events": ms_step_with_events,
         "kv_gbs": unique_kv / (decode_ms * 1e-3) / 1e9,
@@ -373,14 +405,17 @@ def run_gpu(args):
         line["logical_kv_bytes"] = logical["kv"]
         line["unique_kv_bytes"] = unique_kv
     if not args.no_cpu_baseline and world == 1:
-        line["cpu_baseline"] = cpu_baseline(args, wl, q, kc, vc, budget_s=args.cpu_seconds)
+        line["cpu_baseline"] = cpu_baseline(args, wl, q, kc, vc, budget_s=args.cpu_seconds,
+                                            ks=ks, vs=vs)
     return line
 
 
-def workload_config(wl, P, world):
+def workload_config(wl, P, world, kv_dtype=None):
     lens = wl.step_context_lens
+    kv_e = 1 if kv_dtype == "fp8" else None
     return {
-        "workload": wl.name,
+        "workload": wl.name + ("+fp8_kv" if kv_dtype == "fp8" else ""),
+        "kv_dtype": kv_dtype or wl.dtype,
         "num_seqs_per_gpu": wl.num_seqs,
         "global_batch": wl.num_seqs * world,
         "num_q_heads": wl.num_q_heads,
@@ -393,11 +428,11 @@ def workload_config(wl, P, world):
         "cow_pairs_per_step": int(wl.cow_pairs.shape[0]),
         "parallelism": f"weak scaling, {world} independent replica(s)",
         "l2": "inputs larger than L2: %.2f GB of K/V read per step vs 129 MB L2"
-              % (decode_algorithmic_bytes(wl)["kv"] / 1e9),
+              % (decode_algorithmic_bytes(wl, kv_elem_bytes=kv_e)["kv"] / 1e9),
     }
 
 
-def run_e2e(args, pkv, wl, q, kc, vc, kn, vn, dev, stream, P, ws):
+def run_e2e(args, pkv, wl, q, kc, vc, kn, vn, dev, stream, ops):
     """Same step through the public API with host inputs: H2D of the step's inputs
     (query, new K/V rows, slots, tables, lengths, copy pairs) and D2H of the output
     inside the timed region."""
@@ -421,11 +456,10 @@ def run_e2e(args, pkv, wl, q, kc, vc, kn, vn, dev, stream, P, ws):
             if k == "pairs" and not has_cow:
                 continue
             devb[k].copy_(v, non_blocking=True)
-        pkv.cache_write(kc, vc, devb["kn"], devb["vn"], devb["slots"])
+        ops.write(devb["kn"], devb["vn"], devb["slots"])
         if has_cow:
             pkv.block_copy(kc, vc, devb["pairs"])
-        pkv.decode(devb["q"], kc, vc, devb["bt"], devb["lens"], wl.scale, out=out,
-                   partition_size=P, workspace=ws)
+        ops.decode(devb["q"], devb["bt"], devb["lens"], out)
         out_host.copy_(out, non_blocking=True)
 
     for _ in range(max(3, args.warmup // 10)):
@@ -470,7 +504,7 @@ def _bits(t):
     return t.contiguous().cpu().numpy()
 
 
-def cpu_baseline(args, wl, q, kc, vc, budget_s=10.0):
+def cpu_baseline(args, wl, q, kc, vc, budget_s=10.0, ks=None, vs=None):
     import torch
     import oracle
     threads = oracle.max_threads()
@@ -483,8 +517,9 @@ def cpu_baseline(args, wl, q, kc, vc, budget_s=10.0):
     qh = _bits(q[torch.from_numpy(seqs).to(q.device)])
     t0 = time.perf_counter()
     reps = 0
+    scales = {} if ks is None else {"k_scales": ks.cpu().numpy(), "v_scales": vs.cpu().numpy()}
     while True:
-        oracle.paged_decode(qh, kch, vch, tabs, lens, wl.scale, threads=threads)
+        oracle.paged_decode(qh, kch, vch, tabs, lens, wl.scale, threads=threads, **scales)
         reps += 1
         if time.perf_counter() - t0 >= budget_s:
             break
@@ -524,8 +559,15 @@ def run_reference(args):
 
     kch, vch = draw(shape), draw(shape)
     qh = draw((n_seq, wl.num_q_heads, wl.head_dim))
+    scales = {}
+    if getattr(args, "kv_dtype", "bf16") == "fp8":
+        s8 = W.fp8_scales(wl)
+        kch = W.to_e4m3_codes(W.bf16_bits_to_f32(kch), s8)
+        vch = W.to_e4m3_codes(W.bf16_bits_to_f32(vch), s8)
+        scales = {"k_scales": s8, "v_scales": s8}
     for _ in range(args.warmup):
-        oracle.paged_decode(qh[:1], kch, vch, tabs[:1], lens[:1], wl.scale, threads=threads)
+        oracle.paged_decode(qh[:1], kch, vch, tabs[:1], lens[:1], wl.scale, threads=threads,
+                            **scales)
     steps = args.steps
     tokens = 0
     ctx = 0
@@ -535,7 +577,7 @@ def run_reference(args):
     for i in range(steps):
         j = i % n_seq
         oracle.paged_decode(qh[j:j + 1], kch, vch, tabs[j:j + 1], lens[j:j + 1], wl.scale,
-                            threads=threads)
+                            threads=threads, **scales)
         tokens += 1
         ctx += int(lens[j])
         done += 1
@@ -563,7 +605,7 @@ def run_reference(args):
         "dtype": "f64",
         "data": "synthetic (seeded)",
         "config": workload_config(wl, args.partition_size or wl.partition_size or "library choice",
-                                  world),
+                                  world, getattr(args, "kv_dtype", "bf16")),
         "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": threads, "kind": "oracle",
                          "sample": sample},
         "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0,
@@ -578,6 +620,8 @@ def main(argv=None):
     ap.add_argument("--warmup", type=int, default=50)
     ap.add_argument("--workload", default="llama7b_mha", choices=W.WORKLOADS)
     ap.add_argument("--partition-size", type=int, default=0)
+    ap.add_argument("--kv-dtype", default="bf16", choices=["bf16", "fp8"],
+                    help="element type of the K/V pools (fp8 = E4M3 with per-head scales)")
     ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
     ap.add_argument("--seed", type=int, default=0)
     ap.add_argument("--e2e-steps", type=int, default=1000)

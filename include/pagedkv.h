@@ -61,7 +61,8 @@ typedef enum pa_status {
 
 typedef enum pa_dtype {
     PA_DTYPE_F32 = 0,        /* IEEE binary32 */
-    PA_DTYPE_BF16 = 1        /* bfloat16 */
+    PA_DTYPE_BF16 = 1,       /* bfloat16 */
+    PA_DTYPE_FP8_E4M3 = 2    /* FP8 E4M3 codes (pools only; see pa_decode_fp8) */
 } pa_dtype;
 
 /* Bits OR-ed into the optional device status word. */
@@ -87,8 +88,8 @@ uint64_t pa_launch_count(void);
  * Partition size pa_decode uses when it is given partition_size = 0: the
  * largest of 4096, 2048, 1024, 512, 256, 128 tokens for which
  * num_seqs * heads * ceil(max_blocks_per_seq * 16 / size) reaches four CTAs
- * per SM of the current device (heads = num_kv_heads for bf16, num_q_heads
- * for f32).  Returns -1 for invalid arguments.
+ * per SM of the current device (heads = num_kv_heads for bf16 and FP8 pools,
+ * num_q_heads for f32).  Returns -1 for invalid arguments.
  */
 int pa_decode_partition_size(int num_seqs, int num_q_heads, int num_kv_heads,
                              int max_blocks_per_seq, pa_dtype dtype);
@@ -142,6 +143,50 @@ pa_status pa_decode(void *out, const void *query, const void *key_cache, const v
                     int max_blocks_per_seq, int num_blocks, float scale, pa_dtype dtype,
                     int partition_size, void *workspace, size_t workspace_bytes,
                     int32_t *device_status, void *stream);
+
+/*
+ * Paged decode attention over FP8 pools.  The pages name quantising the KV
+ * cache to FP8 as halving it ("KV cache: la memoria de trabajo que sostiene la
+ * inferencia LLM", section "Trucos para que el cuaderno sea más fino"); the
+ * code format is E4M3 ("E4M3FN" of the OCP 8-bit floating point
+ * specification: 1 sign, 4 exponent bits with bias 7, 3 mantissa bits, no
+ * infinities, largest finite 448).
+ *  key_cache,
+ *  value_cache       device E4M3 codes [num_blocks][num_kv_heads][16][head_dim]
+ *  k_scales,
+ *  v_scales          device float [num_kv_heads]: the value a code stands for
+ *                    is code_value * scale of its KV head
+ *  query, out        device bfloat16, as in pa_decode
+ * Everything else is as in pa_decode (partition_size, workspace with
+ * pa_decode_workspace_bytes(..., PA_DTYPE_FP8_E4M3), device_status, stream).
+ * Supported: head_dim 128, group (num_q_heads / num_kv_heads) 1..8.
+ * Arithmetic: codes are widened exactly; the query is rounded to f16 once
+ * (exact for |q| in [2^-14, 65504]); accumulation is fp32.
+ */
+pa_status pa_decode_fp8(void *out, const void *query, const void *key_cache,
+                        const void *value_cache, const float *k_scales, const float *v_scales,
+                        const int32_t *block_tables, const int32_t *context_lens, int num_seqs,
+                        int num_q_heads, int num_kv_heads, int head_dim, int block_size,
+                        int max_blocks_per_seq, int num_blocks, float scale, int partition_size,
+                        void *workspace, size_t workspace_bytes, int32_t *device_status,
+                        void *stream);
+
+/*
+ * Cache write into FP8 pools: as pa_cache_write, but each element x of the
+ * new bfloat16 rows is stored as the E4M3 code of the float32 quotient
+ * x / scale[kv_head] (IEEE single-precision division, then rounding to the
+ * nearest E4M3 value with ties to an even mantissa; magnitudes of 448 or more
+ * saturate to +-448; NaN stays NaN).
+ *  key, value        device bfloat16 [num_tokens][num_kv_heads][head_dim]
+ *  k_scales,
+ *  v_scales          device float [num_kv_heads]
+ *  head_dim          a multiple of 16
+ */
+pa_status pa_cache_write_fp8(void *key_cache, void *value_cache, const void *key,
+                             const void *value, const int64_t *slot_mapping,
+                             const float *k_scales, const float *v_scales, int num_tokens,
+                             int num_kv_heads, int head_dim, int block_size, int num_blocks,
+                             int32_t *device_status, void *stream);
 
 /*
  * Size of the library-owned scratch array used by pa_decode_static_scratch

@@ -25,8 +25,9 @@ from ._lib import PagedKVError, check, lib  # noqa: F401
 
 BLOCK_SIZE = 16
 
-__all__ = ["decode", "decode_workspace_bytes", "decode_partition_size", "cache_write", "block_copy", "launch_count",
-           "BlockManager", "PagedKVError", "BLOCK_SIZE", "library_path"]
+__all__ = ["decode", "decode_fp8", "decode_workspace_bytes", "decode_partition_size",
+           "cache_write", "cache_write_fp8", "block_copy", "launch_count", "BlockManager",
+           "PagedKVError", "BLOCK_SIZE", "library_path"]
 
 
 def library_path() -> str:
@@ -44,7 +45,15 @@ def _dtype_code(t) -> int:
         return _lib.PA_DTYPE_F32
     if t.dtype == torch.bfloat16:
         return _lib.PA_DTYPE_BF16
-    raise TypeError(f"unsupported element type {t.dtype} (float32 or bfloat16)")
+    if t.dtype in (torch.uint8, torch.float8_e4m3fn):
+        return _lib.PA_DTYPE_FP8_E4M3
+    raise TypeError(f"unsupported element type {t.dtype} (float32, bfloat16, or E4M3 codes as "
+                    "uint8 / float8_e4m3fn)")
+
+
+def _is_fp8(t) -> bool:
+    torch = _torch()
+    return t.dtype in (torch.uint8, torch.float8_e4m3fn)
 
 
 def _dev(t, name, dtype=None):
@@ -76,10 +85,19 @@ def launch_count() -> int:
     return int(lib().pa_launch_count())
 
 
+def _code_of(dtype) -> int:
+    name = str(dtype)
+    if name in ("bf16", "torch.bfloat16"):
+        return _lib.PA_DTYPE_BF16
+    if name in ("fp8", "fp8_e4m3", "torch.uint8", "torch.float8_e4m3fn"):
+        return _lib.PA_DTYPE_FP8_E4M3
+    return _lib.PA_DTYPE_F32
+
+
 def decode_partition_size(num_seqs, num_q_heads, num_kv_heads, max_blocks_per_seq,
                           dtype="bf16") -> int:
     """Partition size (tokens) pa_decode picks when given partition_size=0."""
-    code = _lib.PA_DTYPE_BF16 if str(dtype) in ("bf16", "torch.bfloat16") else _lib.PA_DTYPE_F32
+    code = _code_of(dtype)
     n = lib().pa_decode_partition_size(num_seqs, num_q_heads, num_kv_heads, max_blocks_per_seq,
                                        code)
     if n < 0:
@@ -89,7 +107,7 @@ def decode_partition_size(num_seqs, num_q_heads, num_kv_heads, max_blocks_per_se
 
 def decode_workspace_bytes(num_seqs, num_q_heads, num_kv_heads, head_dim, max_blocks_per_seq,
                            partition_size=0, dtype="bf16") -> int:
-    code = _lib.PA_DTYPE_BF16 if str(dtype) in ("bf16", "torch.bfloat16") else _lib.PA_DTYPE_F32
+    code = _code_of(dtype)
     n = lib().pa_decode_workspace_bytes(num_seqs, num_q_heads, num_kv_heads, head_dim,
                                         max_blocks_per_seq, BLOCK_SIZE, partition_size, code)
     if n == ctypes.c_size_t(-1).value:
@@ -132,6 +150,64 @@ def decode(query, key_cache, value_cache, block_tables, context_lens, scale=None
         _stream(stream, query.device))
     check(rc, "pa_decode")
     return out
+
+
+def decode_fp8(query, key_cache, value_cache, k_scales, v_scales, block_tables, context_lens,
+               scale=None, *, out=None, partition_size=0, workspace=None, status=None,
+               stream=None):
+    """Paged decode attention over E4M3 pools (``pa_decode_fp8``); returns ``out`` (bf16)."""
+    torch = _torch()
+    B, Hq, D = query.shape
+    NB, Hkv, BS, D2 = key_cache.shape
+    if BS != BLOCK_SIZE or D2 != D or tuple(value_cache.shape) != tuple(key_cache.shape):
+        raise ValueError("pools must be [num_blocks][num_kv_heads][16][head_dim] like query")
+    if not (_is_fp8(key_cache) and _is_fp8(value_cache)) or query.dtype != torch.bfloat16:
+        raise TypeError("pa_decode_fp8 takes E4M3 pools and a bfloat16 query")
+    if tuple(k_scales.shape) != (Hkv,) or tuple(v_scales.shape) != (Hkv,):
+        raise ValueError("k_scales / v_scales must be [num_kv_heads]")
+    if block_tables.dim() != 2 or block_tables.shape[0] != B or tuple(context_lens.shape) != (B,):
+        raise ValueError("block_tables must be [num_seqs][max_blocks], context_lens [num_seqs]")
+    if scale is None:
+        scale = 1.0 / math.sqrt(D)
+    if out is None:
+        out = torch.empty_like(query)
+    max_blocks = block_tables.shape[1]
+    need = decode_workspace_bytes(B, Hq, Hkv, D, max_blocks, partition_size, "fp8")
+    ws_ptr, ws_bytes = None, 0
+    if need > 0:
+        if workspace is None:
+            workspace = torch.empty(need, dtype=torch.uint8, device=query.device)
+        ws_ptr = _dev(workspace, "workspace")
+        ws_bytes = workspace.numel() * workspace.element_size()
+    rc = lib().pa_decode_fp8(
+        _dev(out, "out"), _dev(query, "query"), _dev(key_cache, "key_cache"),
+        _dev(value_cache, "value_cache"), _dev(k_scales, "k_scales", torch.float32),
+        _dev(v_scales, "v_scales", torch.float32),
+        _dev(block_tables, "block_tables", torch.int32),
+        _dev(context_lens, "context_lens", torch.int32), B, Hq, Hkv, D, BLOCK_SIZE, max_blocks,
+        NB, float(scale), int(partition_size), ws_ptr, ws_bytes, _status_ptr(status),
+        _stream(stream, query.device))
+    check(rc, "pa_decode_fp8")
+    return out
+
+
+def cache_write_fp8(key_cache, value_cache, key, value, slot_mapping, k_scales, v_scales, *,
+                    status=None, stream=None):
+    """Quantise new bf16 K/V rows to E4M3 and scatter them into their slots."""
+    torch = _torch()
+    NB, Hkv, BS, D = key_cache.shape
+    T = slot_mapping.shape[0]
+    if tuple(key.shape) != (T, Hkv, D) or tuple(value.shape) != (T, Hkv, D):
+        raise ValueError("key/value must be [num_tokens][num_kv_heads][head_dim]")
+    if not (_is_fp8(key_cache) and _is_fp8(value_cache)):
+        raise TypeError("pools must hold E4M3 codes")
+    rc = lib().pa_cache_write_fp8(
+        _dev(key_cache, "key_cache"), _dev(value_cache, "value_cache"),
+        _dev(key, "key", torch.bfloat16), _dev(value, "value", torch.bfloat16),
+        _dev(slot_mapping, "slot_mapping", torch.int64), _dev(k_scales, "k_scales", torch.float32),
+        _dev(v_scales, "v_scales", torch.float32), T, Hkv, D, BS, NB, _status_ptr(status),
+        _stream(stream, key_cache.device))
+    check(rc, "pa_cache_write_fp8")
 
 
 def cache_write(key_cache, value_cache, key, value, slot_mapping, *, status=None, stream=None):

@@ -38,6 +38,9 @@ SIGNATURES = {
                         vp, sz, vp, vp]),
     "pa_decode_static_scratch": (i32, [vp, vp, vp, vp, vp, vp, i32, i32, i32, i32, i32, i32, i32,
                                        f32, i32, i32, vp, vp]),
+    "pa_decode_fp8": (i32, [vp, vp, vp, vp, vp, vp, vp, vp, i32, i32, i32, i32, i32, i32, i32, f32,
+                            i32, vp, sz, vp, vp]),
+    "pa_cache_write_fp8": (i32, [vp, vp, vp, vp, vp, vp, vp, i32, i32, i32, i32, i32, vp, vp]),
     "pa_cache_write": (i32, [vp, vp, vp, vp, vp, i32, i32, i32, i32, i32, i32, vp, vp]),
     "pa_block_copy": (i32, [vp, vp, vp, i32, i32, i32, i32, i32, i32, vp, vp]),
     "pa_bm_create": (vp, [i32, i32]),
@@ -65,6 +68,7 @@ PA_ERR_NOT_FOUND = 6
 
 PA_DTYPE_F32 = 0
 PA_DTYPE_BF16 = 1
+PA_DTYPE_FP8_E4M3 = 2
 
 PA_DEV_BAD_BLOCK_ID = 1
 PA_DEV_BAD_CONTEXT_LEN = 2

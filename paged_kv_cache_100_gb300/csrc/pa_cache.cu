@@ -57,6 +57,60 @@ pa_cache_write_kernel(uint4 *__restrict__ kc, uint4 *__restrict__ vc,
     vc[dst] = value[idx];
 }
 
+// Quantising cache write into FP8 pools: one thread per 16 codes (16 bytes) of
+// one (token, KV head) row of K and of V.  Each element x of the bf16 row
+// becomes the E4M3 code of the float32 quotient x / scale[kv_head] (IEEE
+// division, round to nearest even, saturating at +-448).
+__global__ void __launch_bounds__(256)
+pa_cache_write_fp8_kernel(uint4 *__restrict__ kc, uint4 *__restrict__ vc,
+                          const uint4 *__restrict__ key, const uint4 *__restrict__ value,
+                          const int64_t *__restrict__ slot_mapping,
+                          const float *__restrict__ k_scales, const float *__restrict__ v_scales,
+                          int num_tokens, int num_kv_heads, int chunks_per_row, int num_blocks,
+                          int32_t *status) {
+    grid_dependency_wait();
+    grid_dependents_launch();
+    const int64_t idx = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+    const int64_t per_token = (int64_t)num_kv_heads * chunks_per_row;
+    if (idx >= (int64_t)num_tokens * per_token) return;
+    const int64_t i = idx / per_token;
+    const int64_t rem = idx - i * per_token;
+    const int64_t slot = slot_mapping[i];
+    if (slot < 0) return;
+    if (slot >= (int64_t)num_blocks * kBlockSize) {
+        if (rem == 0) report(status, PA_DEV_BAD_SLOT);
+        return;
+    }
+    const int64_t blk = slot / kBlockSize;
+    const int64_t off = slot - blk * kBlockSize;
+    const int64_t kvh = rem / chunks_per_row;
+    const int64_t ch = rem - kvh * chunks_per_row;
+    const int64_t dst = ((blk * num_kv_heads + kvh) * kBlockSize + off) * chunks_per_row + ch;
+    const float ks = k_scales[kvh], vs = v_scales[kvh];
+    // 16 bf16 inputs (two uint4) per 16 output codes
+    const uint4 *ksrc = key + 2 * idx;
+    const uint4 *vsrc = value + 2 * idx;
+    const uint4 k0 = ksrc[0], k1 = ksrc[1], v0 = vsrc[0], v1 = vsrc[1];
+    const uint32_t kw[8] = {k0.x, k0.y, k0.z, k0.w, k1.x, k1.y, k1.z, k1.w};
+    const uint32_t vw[8] = {v0.x, v0.y, v0.z, v0.w, v1.x, v1.y, v1.z, v1.w};
+    uint32_t ko[4], vo[4];
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+        const uint32_t klo = f32x2_to_e4m3x2(__fdiv_rn(bf16lo(kw[2 * j]), ks),
+                                             __fdiv_rn(bf16hi(kw[2 * j]), ks));
+        const uint32_t khi = f32x2_to_e4m3x2(__fdiv_rn(bf16lo(kw[2 * j + 1]), ks),
+                                             __fdiv_rn(bf16hi(kw[2 * j + 1]), ks));
+        const uint32_t vlo = f32x2_to_e4m3x2(__fdiv_rn(bf16lo(vw[2 * j]), vs),
+                                             __fdiv_rn(bf16hi(vw[2 * j]), vs));
+        const uint32_t vhi = f32x2_to_e4m3x2(__fdiv_rn(bf16lo(vw[2 * j + 1]), vs),
+                                             __fdiv_rn(bf16hi(vw[2 * j + 1]), vs));
+        ko[j] = klo | (khi << 16);
+        vo[j] = vlo | (vhi << 16);
+    }
+    kc[dst] = make_uint4(ko[0], ko[1], ko[2], ko[3]);
+    vc[dst] = make_uint4(vo[0], vo[1], vo[2], vo[3]);
+}
+
 // grid.x = pair, grid.y = slice of the block; every thread copies up to
 // kChunksPerThread 16-byte chunks of K and of V.
 constexpr int kCopyThreads = 256;
@@ -99,7 +153,9 @@ pa_block_copy_kernel(uint4 *__restrict__ kc, uint4 *__restrict__ vc,
     }
 }
 
-int elem_bytes(pa_dtype dtype) { return dtype == PA_DTYPE_F32 ? 4 : 2; }
+int elem_bytes(pa_dtype dtype) {
+    return dtype == PA_DTYPE_F32 ? 4 : (dtype == PA_DTYPE_BF16 ? 2 : 1);
+}
 
 }  // namespace
 
@@ -170,7 +226,8 @@ extern "C" pa_status pa_block_copy(void *key_cache, void *value_cache, const int
     if (num_pairs < 0 || num_kv_heads <= 0 || head_dim <= 0 || block_size != kBlockSize ||
         num_blocks <= 0)
         return PA_ERR_INVALID_ARG;
-    if (dtype != PA_DTYPE_F32 && dtype != PA_DTYPE_BF16) return PA_ERR_INVALID_ARG;
+    if (dtype != PA_DTYPE_F32 && dtype != PA_DTYPE_BF16 && dtype != PA_DTYPE_FP8_E4M3)
+        return PA_ERR_INVALID_ARG;
     const int64_t block_bytes = (int64_t)num_kv_heads * kBlockSize * head_dim * elem_bytes(dtype);
     if (block_bytes % 16 != 0) return PA_ERR_UNSUPPORTED;
     if (num_pairs == 0) return PA_OK;
@@ -188,6 +245,38 @@ extern "C" pa_status pa_block_copy(void *key_cache, void *value_cache, const int
         static_cast<uint4 *>(key_cache), static_cast<uint4 *>(value_cache), src_dst, chunks,
         num_blocks, device_status);
     if (e != cudaSuccess) return cuda_failure(e, "pa_block_copy_kernel launch");
+    count_launches(1);
+    return PA_OK;
+}
+
+extern "C" pa_status pa_cache_write_fp8(void *key_cache, void *value_cache, const void *key,
+                                        const void *value, const int64_t *slot_mapping,
+                                        const float *k_scales, const float *v_scales,
+                                        int num_tokens, int num_kv_heads, int head_dim,
+                                        int block_size, int num_blocks, int32_t *device_status,
+                                        void *stream) {
+    if (num_tokens < 0 || num_kv_heads <= 0 || head_dim <= 0 || block_size != kBlockSize ||
+        num_blocks <= 0)
+        return PA_ERR_INVALID_ARG;
+    if (head_dim % 16 != 0) return PA_ERR_UNSUPPORTED;
+    if (num_tokens == 0) return PA_OK;
+    if (!key_cache || !value_cache || !key || !value || !slot_mapping || !k_scales || !v_scales)
+        return PA_ERR_INVALID_ARG;
+    if (!aligned16(key_cache) || !aligned16(value_cache) || !aligned16(key) || !aligned16(value) ||
+        (reinterpret_cast<uintptr_t>(slot_mapping) & 7u) ||
+        (reinterpret_cast<uintptr_t>(k_scales) & 3u) || (reinterpret_cast<uintptr_t>(v_scales) & 3u))
+        return PA_ERR_INVALID_ARG;
+    const int chunks = head_dim / 16;
+    const int64_t total = (int64_t)num_tokens * num_kv_heads * chunks;
+    const int64_t grid = (total + 255) / 256;
+    if (grid >= ((int64_t)1 << 31)) return PA_ERR_UNSUPPORTED;
+    cudaError_t e = launch_chained(
+        pa_cache_write_fp8_kernel, dim3((unsigned)grid), dim3(256), 0,
+        static_cast<cudaStream_t>(stream), static_cast<uint4 *>(key_cache),
+        static_cast<uint4 *>(value_cache), static_cast<const uint4 *>(key),
+        static_cast<const uint4 *>(value), slot_mapping, k_scales, v_scales, num_tokens,
+        num_kv_heads, chunks, num_blocks, device_status);
+    if (e != cudaSuccess) return cuda_failure(e, "pa_cache_write_fp8_kernel launch");
     count_launches(1);
     return PA_OK;
 }

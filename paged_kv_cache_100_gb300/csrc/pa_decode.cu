@@ -60,6 +60,8 @@ struct DecodeArgs {
     float *part_o;      // [rows][head_dim], rows = (b * Hq + h) * max_parts + part
     float2 *part_ml;    // [rows] = (running max in log2 units, running sum)
     int32_t *status;
+    const float *k_scales;  // FP8 pools: per-KV-head scales (stored value = code * scale)
+    const float *v_scales;
     int num_seqs;
     int num_q_heads;
     int num_kv_heads;
@@ -196,6 +198,7 @@ struct MhaConsumer {
     static constexpr int RG = 32 / CH;
     static constexpr int RPL = 16 / RG;
     static constexpr int ROWS = 1;     // query heads per warp state
+    static constexpr int kElemBytes = 2;
     static_assert(RPL * 2 == CH, "lane layout");
 
     float q[8];
@@ -288,6 +291,7 @@ struct GqaConsumer {
     static constexpr int NT = D / 8;    // n-tiles of P.V
     static constexpr bool HI = G > 8;   // rows 8..15 hold real heads
     static constexpr int ROWS = G;
+    static constexpr int kElemBytes = 2;
 
     uint32_t qa[KS][4];
     float o[NT][4];
@@ -450,6 +454,7 @@ struct GqaTConsumer {
     static_assert(G >= 2 && G <= 8, "one n-tile of query heads");
     static constexpr int KS = D / 16;   // k-steps of S^T and m-tiles of O^T
     static constexpr int ROWS = G;
+    static constexpr int kElemBytes = 2;
 
     uint32_t qb[KS][2];
     float o[KS][4];
@@ -569,9 +574,320 @@ struct GqaTConsumer {
     }
 };
 
-template <int D, int NW, int STAGES>
+// ---------------------------------------------------------------------------
+// FP8 (E4M3) pools.  A tile is 16 rows x D codes (D bytes per row, one 128-byte
+// swizzle row at D = 128); the stored value of a code is code_value * scale of
+// its KV head, and the scales are applied once per score (K) and once per
+// output (V).  E4M3 values are exact in f16, so the kernels widen codes to f16
+// and keep fp32 accumulation.  The query is rounded to f16 once (exact for
+// |q| in [2^-14, 65504]).
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ uint32_t fp8_addr(uint32_t tile, int row, int byte) {
+    return tile + (uint32_t)(row * 128 + ((((byte >> 4) ^ (row & 7))) << 4) + (byte & 15));
+}
+
+__device__ __forceinline__ uint32_t lds32(uint32_t addr) {
+    uint32_t v;
+    asm volatile("ld.shared.u32 %0, [%1];" : "=r"(v) : "r"(addr));
+    return v;
+}
+
+__device__ __forceinline__ uint2 lds64(uint32_t addr) {
+    uint2 v;
+    asm volatile("ld.shared.v2.u32 {%0, %1}, [%2];" : "=r"(v.x), "=r"(v.y) : "r"(addr));
+    return v;
+}
+
+// Zeroes rows [nvalid, 16) of a 16 x 128-byte tile (values past the context may
+// be anything, NaN codes included, and must not reach a tensor-core sum).
+__device__ __forceinline__ void zero_tail_rows_128(uint32_t tile, int nvalid, int lane) {
+    const int zrows = 16 - nvalid;
+    for (int i = lane; i < zrows * 8; i += 32) {
+        const uint32_t addr = tile + (uint32_t)((nvalid + i / 8) * 128 + (i % 8) * 16);
+        asm volatile("st.shared.v4.u32 [%0], {%1, %1, %1, %1};" ::"r"(addr), "r"(0u) : "memory");
+    }
+    __syncwarp();
+}
+
+// One query head per KV head, FP8 pools, D = 128.  Lane layout: chunk c =
+// lane % 8 owns head-dim elements [16c, 16c+16) (one 16-byte chunk of codes);
+// row group rg = lane / 8 owns rows [4rg, 4rg+4).
+template <int D>
+struct MhaFp8Consumer {
+    static_assert(D == 128, "one 128-byte swizzle row per tile row");
+    static constexpr int CH = D / 16;
+    static constexpr int RG = 32 / CH;
+    static constexpr int RPL = 16 / RG;
+    static constexpr int ROWS = 1;
+    static constexpr int kElemBytes = 1;
+
+    uint32_t q[8];       // f16x2: elements 16c + 2i, 16c + 2i + 1
+    float acc[16];
+    float m, l;
+    float ck;            // softmax scale * log2(e) * k scale
+    float vs;
+    int lane, c, rg;
+
+    __device__ __forceinline__ void init(const DecodeArgs &a, const Work &w, int lane_) {
+        lane = lane_;
+        c = lane & (CH - 1);
+        rg = lane / CH;
+        const __nv_bfloat16 *qrow =
+            static_cast<const __nv_bfloat16 *>(a.query) + ((size_t)w.b * a.num_q_heads + w.head) * D;
+        const uint4 r0 = *reinterpret_cast<const uint4 *>(qrow + 16 * c);
+        const uint4 r1 = *reinterpret_cast<const uint4 *>(qrow + 16 * c + 8);
+        const uint32_t words[8] = {r0.x, r0.y, r0.z, r0.w, r1.x, r1.y, r1.z, r1.w};
+#pragma unroll
+        for (int i = 0; i < 8; ++i) q[i] = pack_f16x2(bf16lo(words[i]), bf16hi(words[i]));
+#pragma unroll
+        for (int e = 0; e < 16; ++e) acc[e] = 0.f;
+        m = -INFINITY;
+        l = 0.f;
+        ck = a.scale_log2 * a.k_scales[w.head];
+        vs = a.v_scales[w.head];
+    }
+
+    __device__ __forceinline__ void block(uint32_t ktile, uint32_t vtile, int nvalid) {
+        float v[RPL];
+#pragma unroll
+        for (int i = 0; i < RPL; ++i) {
+            const uint4 kw = lds128(swz(ktile, rg * RPL + i, c));
+            const uint32_t w4[4] = {kw.x, kw.y, kw.z, kw.w};
+            float dot = 0.f;
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                dot = dot2_f16_f32(q[2 * j], e4m3x2_to_f16x2(w4[j]), dot);
+                dot = dot2_f16_f32(q[2 * j + 1], e4m3x2_to_f16x2(w4[j] >> 16), dot);
+            }
+            v[i] = dot;
+        }
+#pragma unroll
+        for (int M = CH / 2, n = RPL; M >= 2; M >>= 1, n >>= 1) {
+            const bool upper = (lane & M) != 0;
+#pragma unroll
+            for (int k = 0; k < n / 2; ++k) {
+                const float send = upper ? v[k] : v[k + n / 2];
+                const float keep = upper ? v[k + n / 2] : v[k];
+                v[k] = keep + __shfl_xor_sync(kFull, send, M);
+            }
+        }
+        float s = (v[0] + __shfl_xor_sync(kFull, v[0], 1)) * ck;
+        const int row = rg * RPL + ((lane & (CH - 1)) >> 1);
+        s = row < nvalid ? s : -INFINITY;
+        float bmax = s;
+#pragma unroll
+        for (int M = 2; M < 32; M <<= 1) bmax = fmaxf(bmax, __shfl_xor_sync(kFull, bmax, M));
+        const float m_new = fmaxf(m, bmax);
+        const float alpha = exp2f(m - m_new);
+        const float p = exp2f(s - m_new);
+        l = l * alpha + ((lane & 1) ? 0.f : p);
+        m = m_new;
+#pragma unroll
+        for (int e = 0; e < 16; ++e) acc[e] *= alpha;
+#pragma unroll
+        for (int i = 0; i < RPL; ++i) {
+            const int r = rg * RPL + i;
+            const float pr = __shfl_sync(kFull, p, rg * CH + 2 * i);
+            const uint4 vw = lds128(swz(vtile, r, c));
+            if (r < nvalid) {
+                const uint32_t w4[4] = {vw.x, vw.y, vw.z, vw.w};
+#pragma unroll
+                for (int j = 0; j < 4; ++j) {
+                    const uint32_t h0 = e4m3x2_to_f16x2(w4[j]);
+                    const uint32_t h1 = e4m3x2_to_f16x2(w4[j] >> 16);
+                    acc[4 * j + 0] = fmaf(pr, f16lo(h0), acc[4 * j + 0]);
+                    acc[4 * j + 1] = fmaf(pr, f16hi(h0), acc[4 * j + 1]);
+                    acc[4 * j + 2] = fmaf(pr, f16lo(h1), acc[4 * j + 2]);
+                    acc[4 * j + 3] = fmaf(pr, f16hi(h1), acc[4 * j + 3]);
+                }
+            }
+        }
+    }
+
+    __device__ __forceinline__ void finish(float *acc_out, float *m_out, float *l_out) {
+#pragma unroll
+        for (int M = CH; M < 32; M <<= 1)
+#pragma unroll
+            for (int e = 0; e < 16; ++e) acc[e] += __shfl_xor_sync(kFull, acc[e], M);
+#pragma unroll
+        for (int M = 1; M < 32; M <<= 1) l += __shfl_xor_sync(kFull, l, M);
+        if (lane < CH) {
+            float4 *dst = reinterpret_cast<float4 *>(acc_out + 16 * c);
+#pragma unroll
+            for (int k = 0; k < 4; ++k)
+                dst[k] = make_float4(acc[4 * k] * vs, acc[4 * k + 1] * vs, acc[4 * k + 2] * vs,
+                                     acc[4 * k + 3] * vs);
+        }
+        if (lane == 0) {
+            m_out[0] = m;
+            l_out[0] = l;
+        }
+    }
+};
+
+// 2..8 query heads per KV head, FP8 pools, D = 128, on f16 tensor cores in the
+// transposed form of GqaTConsumer (tokens on M, heads on N).
+//  * S^T = K.Q^T: the contraction over the head dimension may visit it in any
+//    order as long as K and Q agree, so lane (g, t) loads 8 consecutive codes
+//    of rows g and g + 8 (bytes 32kk + 8t .. +8) and the Q fragments are laid
+//    out to match: k-step 2kk + hh covers head-dim elements
+//    32kk + 8t + 4hh + {0, 1} (k = 2t, 2t+1) and + {2, 3} (k = 2t+8, 2t+9).
+//  * O^T += V^T.P^T: the A operand needs two tokens of one head-dim element
+//    per register, so lane (g, t) loads 4 codes (bytes 32c + 4g ..) of token
+//    rows 2t, 2t+1, 2t+8, 2t+9 and pairs them with byte permutes; output rows
+//    are head-dim elements 32c + 4g + 2jp (row g) and + 1 (row g + 8) of m-tile
+//    2c + jp.
+template <int D, int G>
+struct GqaTFp8Consumer {
+    static_assert(D == 128, "one 128-byte swizzle row per tile row");
+    static_assert(G >= 2 && G <= 8, "one n-tile of query heads");
+    static constexpr int KS = D / 16;
+    static constexpr int ROWS = G;
+    static constexpr int kElemBytes = 1;
+
+    uint32_t qb[KS][2];
+    float o[KS][4];
+    float m0, m1, l0, l1;
+    float ck, vs;
+    int lane, g, t;
+
+    __device__ __forceinline__ void init(const DecodeArgs &a, const Work &w, int lane_) {
+        lane = lane_;
+        g = lane >> 2;
+        t = lane & 3;
+        ck = a.scale_log2 * a.k_scales[w.head];
+        vs = a.v_scales[w.head];
+        const __nv_bfloat16 *qg = static_cast<const __nv_bfloat16 *>(a.query) +
+                                  ((size_t)w.b * a.num_q_heads + (size_t)w.head * G) * D;
+        const uint32_t *qrow = reinterpret_cast<const uint32_t *>(qg + (size_t)g * D);
+#pragma unroll
+        for (int kk = 0; kk < D / 32; ++kk)
+#pragma unroll
+            for (int hh = 0; hh < 2; ++hh) {
+                const int d = 32 * kk + 8 * t + 4 * hh;
+                const uint32_t w0 = g < G ? qrow[d / 2] : 0u;
+                const uint32_t w1 = g < G ? qrow[d / 2 + 1] : 0u;
+                qb[2 * kk + hh][0] = pack_f16x2(bf16lo(w0), bf16hi(w0));
+                qb[2 * kk + hh][1] = pack_f16x2(bf16lo(w1), bf16hi(w1));
+            }
+#pragma unroll
+        for (int mt = 0; mt < KS; ++mt) o[mt][0] = o[mt][1] = o[mt][2] = o[mt][3] = 0.f;
+        m0 = m1 = -INFINITY;
+        l0 = l1 = 0.f;
+    }
+
+    __device__ __forceinline__ void block(uint32_t ktile, uint32_t vtile, int nvalid) {
+        float s[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+        for (int kk = 0; kk < D / 32; ++kk) {
+            const uint2 r0 = lds64(fp8_addr(ktile, g, 32 * kk + 8 * t));
+            const uint2 r1 = lds64(fp8_addr(ktile, g + 8, 32 * kk + 8 * t));
+            uint32_t a[4];
+            a[0] = e4m3x2_to_f16x2(r0.x);
+            a[1] = e4m3x2_to_f16x2(r1.x);
+            a[2] = e4m3x2_to_f16x2(r0.x >> 16);
+            a[3] = e4m3x2_to_f16x2(r1.x >> 16);
+            mma_f16_16816(s, a, qb[2 * kk][0], qb[2 * kk][1]);
+            a[0] = e4m3x2_to_f16x2(r0.y);
+            a[1] = e4m3x2_to_f16x2(r1.y);
+            a[2] = e4m3x2_to_f16x2(r0.y >> 16);
+            a[3] = e4m3x2_to_f16x2(r1.y >> 16);
+            mma_f16_16816(s, a, qb[2 * kk + 1][0], qb[2 * kk + 1][1]);
+        }
+        const bool v0 = g < nvalid, v1 = g + 8 < nvalid;
+        s[0] = v0 ? s[0] * ck : -INFINITY;
+        s[1] = v0 ? s[1] * ck : -INFINITY;
+        s[2] = v1 ? s[2] * ck : -INFINITY;
+        s[3] = v1 ? s[3] * ck : -INFINITY;
+        float mx0 = fmaxf(s[0], s[2]), mx1 = fmaxf(s[1], s[3]);
+#pragma unroll
+        for (int M = 4; M < 32; M <<= 1) {
+            mx0 = fmaxf(mx0, __shfl_xor_sync(kFull, mx0, M));
+            mx1 = fmaxf(mx1, __shfl_xor_sync(kFull, mx1, M));
+        }
+        const float mn0 = fmaxf(m0, mx0), mn1 = fmaxf(m1, mx1);
+        const float a0 = exp2f(m0 - mn0), a1 = exp2f(m1 - mn1);
+        m0 = mn0;
+        m1 = mn1;
+        const float p0 = exp2f(s[0] - mn0), p1 = exp2f(s[1] - mn1);
+        const float p2 = exp2f(s[2] - mn0), p3 = exp2f(s[3] - mn1);
+        l0 = l0 * a0 + (p0 + p2);
+        l1 = l1 * a1 + (p1 + p3);
+#pragma unroll
+        for (int mt = 0; mt < KS; ++mt) {
+            o[mt][0] *= a0;
+            o[mt][1] *= a1;
+            o[mt][2] *= a0;
+            o[mt][3] *= a1;
+        }
+        uint32_t top_hi, top_lo, bot_hi, bot_lo;
+        split_f16x2(p0, p1, top_hi, top_lo);
+        split_f16x2(p2, p3, bot_hi, bot_lo);
+        const uint32_t bh0 = movmatrix_trans(top_hi), bh1 = movmatrix_trans(bot_hi);
+        const uint32_t bl0 = movmatrix_trans(top_lo), bl1 = movmatrix_trans(bot_lo);
+        if (nvalid < 16) zero_tail_rows_128(vtile, nvalid, lane);
+#pragma unroll
+        for (int c = 0; c < D / 32; ++c) {
+            const int byte = 32 * c + 4 * g;
+            const uint32_t wa = lds32(fp8_addr(vtile, 2 * t, byte));
+            const uint32_t wb = lds32(fp8_addr(vtile, 2 * t + 1, byte));
+            const uint32_t wc = lds32(fp8_addr(vtile, 2 * t + 8, byte));
+            const uint32_t wd = lds32(fp8_addr(vtile, 2 * t + 9, byte));
+#pragma unroll
+            for (int jp = 0; jp < 2; ++jp) {
+                const uint32_t sel = jp == 0 ? 0x5140u : 0x7362u;
+                const uint32_t x0 = __byte_perm(wa, wb, sel);   // tokens 2t, 2t+1
+                const uint32_t x1 = __byte_perm(wc, wd, sel);   // tokens 2t+8, 2t+9
+                uint32_t a[4];
+                a[0] = e4m3x2_to_f16x2(x0);
+                a[1] = e4m3x2_to_f16x2(x0 >> 16);
+                a[2] = e4m3x2_to_f16x2(x1);
+                a[3] = e4m3x2_to_f16x2(x1 >> 16);
+                mma_f16_16816(o[2 * c + jp], a, bh0, bh1);
+                mma_f16_16816(o[2 * c + jp], a, bl0, bl1);
+            }
+        }
+    }
+
+    __device__ __forceinline__ void finish(float *acc_out, float *m_out, float *l_out) {
+#pragma unroll
+        for (int M = 4; M < 32; M <<= 1) {
+            l0 += __shfl_xor_sync(kFull, l0, M);
+            l1 += __shfl_xor_sync(kFull, l1, M);
+        }
+        const int h0 = 2 * t, h1 = 2 * t + 1;
+#pragma unroll
+        for (int c = 0; c < D / 32; ++c)
+#pragma unroll
+            for (int jp = 0; jp < 2; ++jp) {
+                const int d = 32 * c + 4 * g + 2 * jp;
+                const float *oo = o[2 * c + jp];
+                if (h0 < G) {
+                    acc_out[h0 * D + d] = oo[0] * vs;
+                    acc_out[h0 * D + d + 1] = oo[2] * vs;
+                }
+                if (h1 < G) {
+                    acc_out[h1 * D + d] = oo[1] * vs;
+                    acc_out[h1 * D + d + 1] = oo[3] * vs;
+                }
+            }
+        if (g == 0) {
+            if (h0 < G) {
+                m_out[h0] = m0;
+                l_out[h0] = l0;
+            }
+            if (h1 < G) {
+                m_out[h1] = m1;
+                l_out[h1] = l1;
+            }
+        }
+    }
+};
+
+template <int D, int ELEM, int NW, int STAGES>
 struct TmaLayout {
-    static constexpr int kTileBytes = 16 * D * 2;
+    static constexpr int kTileBytes = 16 * D * ELEM;
+    static constexpr int kBoxElems = 128 / ELEM;     // one 128-byte swizzle row per box row
     static constexpr int kStageBytes = 2 * kTileBytes;
     static constexpr int kStagesBytes = NW * STAGES * kStageBytes;
     static constexpr int kRowsMax = 16;   // rows of the merge state per warp
@@ -587,7 +903,7 @@ template <int D, class Consumer, int NW, int STAGES>
 __global__ void __launch_bounds__(NW * 32)
 pa_decode_bf16_kernel(const __grid_constant__ CUtensorMap kmap,
                       const __grid_constant__ CUtensorMap vmap, const DecodeArgs a) {
-    using Lay = TmaLayout<D, NW, STAGES>;
+    using Lay = TmaLayout<D, Consumer::kElemBytes, NW, STAGES>;
     grid_dependency_wait();
     grid_dependents_launch();
     Work w;
@@ -643,9 +959,9 @@ pa_decode_bf16_kernel(const __grid_constant__ CUtensorMap kmap,
         uint8_t *vt = kt + Lay::kTileBytes;
         mbar_arrive_expect_tx(&my_bars[s], Lay::kStageBytes);
 #pragma unroll
-        for (int x = 0; x < D; x += 64) {
-            tma_load_2d(kt + (x / 64) * 2048, &kmap, x, y, &my_bars[s]);
-            tma_load_2d(vt + (x / 64) * 2048, &vmap, x, y, &my_bars[s]);
+        for (int x = 0; x < D; x += Lay::kBoxElems) {
+            tma_load_2d(kt + (x / Lay::kBoxElems) * 2048, &kmap, x, y, &my_bars[s]);
+            tma_load_2d(vt + (x / Lay::kBoxElems) * 2048, &vmap, x, y, &my_bars[s]);
         }
     };
 
@@ -822,15 +1138,19 @@ PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
 
 // 2-D view of a pool as [num_blocks * num_kv_heads * 16 rows][head_dim] bf16,
 // loaded as boxes of 16 rows x 64 elements with 128-byte swizzle.
-bool encode_pool_map(CUtensorMap *map, const void *pool, int64_t rows, int D) {
+// 2-D view of a pool as [num_blocks * num_kv_heads * 16 rows][head_dim]
+// elements, loaded as boxes of 16 rows x 128 bytes with 128-byte swizzle.
+bool encode_pool_map(CUtensorMap *map, const void *pool, int64_t rows, int D, int elem_bytes) {
     auto enc = tensor_map_encoder();
     if (enc == nullptr) return false;
     cuuint64_t dims[2] = {(cuuint64_t)D, (cuuint64_t)rows};
-    cuuint64_t strides[1] = {(cuuint64_t)D * 2};
-    cuuint32_t box[2] = {64, 16};
+    cuuint64_t strides[1] = {(cuuint64_t)D * elem_bytes};
+    cuuint32_t box[2] = {(cuuint32_t)(128 / elem_bytes), 16};
     cuuint32_t estr[2] = {1, 1};
-    CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(pool), dims,
-                     strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+    const CUtensorMapDataType type =
+        elem_bytes == 2 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_UINT8;
+    CUresult r = enc(map, type, 2, const_cast<void *>(pool), dims, strides, box, estr,
+                     CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                      CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     return r == CUDA_SUCCESS;
 }
@@ -868,15 +1188,30 @@ cudaError_t allow_smem(K kernel, size_t bytes) {
 #ifndef PA_GQA16_STAGES
 #define PA_GQA16_STAGES 2
 #endif
+// FP8 pools (4 KiB per block): MHA 8 warps x 2 stages, GQA 4 warps x 4 stages
+// (64 KiB each, three CTAs per SM).
+#ifndef PA_MHA8_WARPS
+#define PA_MHA8_WARPS 8
+#endif
+#ifndef PA_MHA8_STAGES
+#define PA_MHA8_STAGES 2
+#endif
+#ifndef PA_GQA8_WARPS
+#define PA_GQA8_WARPS 4
+#endif
+#ifndef PA_GQA8_STAGES
+#define PA_GQA8_STAGES 4
+#endif
 constexpr int kNW = 4;   // fp32 kernel
 
 template <int D, class Consumer, int NW, int STAGES>
 pa_status launch_bf16(const DecodeArgs &a, const void *kc, const void *vc, int64_t rows,
                       cudaStream_t stream) {
     CUtensorMap kmap, vmap;
-    if (!encode_pool_map(&kmap, kc, rows, D) || !encode_pool_map(&vmap, vc, rows, D))
+    if (!encode_pool_map(&kmap, kc, rows, D, Consumer::kElemBytes) ||
+        !encode_pool_map(&vmap, vc, rows, D, Consumer::kElemBytes))
         return cuda_failure(cudaErrorInvalidValue, "cuTensorMapEncodeTiled");
-    const size_t smem = TmaLayout<D, NW, STAGES>::smem_bytes(a.part_blocks);
+    const size_t smem = TmaLayout<D, Consumer::kElemBytes, NW, STAGES>::smem_bytes(a.part_blocks);
     auto kernel = pa_decode_bf16_kernel<D, Consumer, NW, STAGES>;
     cudaError_t e = allow_smem(kernel, smem);
     if (e != cudaSuccess) return cuda_failure(e, "cudaFuncSetAttribute(decode)");
@@ -912,6 +1247,22 @@ pa_status dispatch_bf16(int group, const DecodeArgs &a, const void *kc, const vo
     case 8: return launch_gqa<D, 8>(a, kc, vc, rows, stream);
     case 12: return launch_gqa<D, 12>(a, kc, vc, rows, stream);
     case 16: return launch_gqa<D, 16>(a, kc, vc, rows, stream);
+    default: return PA_ERR_UNSUPPORTED;
+    }
+}
+
+pa_status dispatch_fp8(int group, const DecodeArgs &a, const void *kc, const void *vc,
+                       int64_t rows, cudaStream_t stream) {
+    constexpr int D = 128;
+    switch (group) {
+    case 1: return launch_bf16<D, MhaFp8Consumer<D>, PA_MHA8_WARPS, PA_MHA8_STAGES>(a, kc, vc, rows, stream);
+    case 2: return launch_bf16<D, GqaTFp8Consumer<D, 2>, PA_GQA8_WARPS, PA_GQA8_STAGES>(a, kc, vc, rows, stream);
+    case 3: return launch_bf16<D, GqaTFp8Consumer<D, 3>, PA_GQA8_WARPS, PA_GQA8_STAGES>(a, kc, vc, rows, stream);
+    case 4: return launch_bf16<D, GqaTFp8Consumer<D, 4>, PA_GQA8_WARPS, PA_GQA8_STAGES>(a, kc, vc, rows, stream);
+    case 5: return launch_bf16<D, GqaTFp8Consumer<D, 5>, PA_GQA8_WARPS, PA_GQA8_STAGES>(a, kc, vc, rows, stream);
+    case 6: return launch_bf16<D, GqaTFp8Consumer<D, 6>, PA_GQA8_WARPS, PA_GQA8_STAGES>(a, kc, vc, rows, stream);
+    case 7: return launch_bf16<D, GqaTFp8Consumer<D, 7>, PA_GQA8_WARPS, PA_GQA8_STAGES>(a, kc, vc, rows, stream);
+    case 8: return launch_bf16<D, GqaTFp8Consumer<D, 8>, PA_GQA8_WARPS, PA_GQA8_STAGES>(a, kc, vc, rows, stream);
     default: return PA_ERR_UNSUPPORTED;
     }
 }
@@ -994,9 +1345,9 @@ using namespace pa;
 extern "C" int pa_decode_partition_size(int num_seqs, int num_q_heads, int num_kv_heads,
                                         int max_blocks_per_seq, pa_dtype dtype) {
     if (num_seqs < 0 || num_q_heads <= 0 || num_kv_heads <= 0 || max_blocks_per_seq < 0 ||
-        (dtype != PA_DTYPE_F32 && dtype != PA_DTYPE_BF16))
+        (dtype != PA_DTYPE_F32 && dtype != PA_DTYPE_BF16 && dtype != PA_DTYPE_FP8_E4M3))
         return -1;
-    const int heads_axis = dtype == PA_DTYPE_BF16 ? num_kv_heads : num_q_heads;
+    const int heads_axis = dtype == PA_DTYPE_F32 ? num_q_heads : num_kv_heads;
     return auto_partition(num_seqs, heads_axis, max_blocks_per_seq);
 }
 
@@ -1005,9 +1356,9 @@ extern "C" size_t pa_decode_workspace_bytes(int num_seqs, int num_q_heads, int n
                                             int partition_size, pa_dtype dtype) {
     if (num_seqs < 0 || num_q_heads <= 0 || num_kv_heads <= 0 || head_dim <= 0 ||
         max_blocks_per_seq < 0 || block_size != kBlockSize ||
-        (dtype != PA_DTYPE_F32 && dtype != PA_DTYPE_BF16))
+        (dtype != PA_DTYPE_F32 && dtype != PA_DTYPE_BF16 && dtype != PA_DTYPE_FP8_E4M3))
         return (size_t)-1;
-    const int heads_axis = dtype == PA_DTYPE_BF16 ? num_kv_heads : num_q_heads;
+    const int heads_axis = dtype == PA_DTYPE_F32 ? num_q_heads : num_kv_heads;
     const int p = resolve_partition(partition_size, num_seqs, heads_axis, max_blocks_per_seq);
     if (p < 0) return (size_t)-1;
     const int part_blocks = p / kBlockSize;
@@ -1067,6 +1418,8 @@ extern "C" pa_status pa_decode(void *out, const void *query, const void *key_cac
                                  255) & ~size_t(255)))
                          : nullptr;
     a.status = device_status;
+    a.k_scales = nullptr;
+    a.v_scales = nullptr;
     a.num_seqs = num_seqs;
     a.num_q_heads = num_q_heads;
     a.num_kv_heads = num_kv_heads;
@@ -1092,4 +1445,67 @@ extern "C" pa_status pa_decode(void *out, const void *query, const void *key_cac
     if (s != PA_OK || max_parts <= 1) return s;
     return dtype == PA_DTYPE_BF16 ? launch_reduce<__nv_bfloat16>(a, head_dim, st)
                                   : launch_reduce<float>(a, head_dim, st);
+}
+
+extern "C" pa_status pa_decode_fp8(void *out, const void *query, const void *key_cache,
+                                   const void *value_cache, const float *k_scales,
+                                   const float *v_scales, const int32_t *block_tables,
+                                   const int32_t *context_lens, int num_seqs, int num_q_heads,
+                                   int num_kv_heads, int head_dim, int block_size,
+                                   int max_blocks_per_seq, int num_blocks, float scale,
+                                   int partition_size, void *workspace, size_t workspace_bytes,
+                                   int32_t *device_status, void *stream) {
+    if (num_seqs < 0 || num_q_heads <= 0 || num_kv_heads <= 0 || block_size != kBlockSize ||
+        max_blocks_per_seq < 0 || num_blocks <= 0 || num_q_heads % num_kv_heads != 0 ||
+        !(scale == scale))
+        return PA_ERR_INVALID_ARG;
+    if (partition_size != 0 &&
+        (partition_size < kBlockSize || partition_size > kMaxPartition || partition_size % kBlockSize))
+        return PA_ERR_INVALID_ARG;
+    if (num_seqs == 0) return PA_OK;
+    if (!out || !query || !key_cache || !value_cache || !k_scales || !v_scales || !block_tables ||
+        !context_lens)
+        return PA_ERR_INVALID_ARG;
+    if (!aligned16(out) || !aligned16(query) || !aligned16(key_cache) || !aligned16(value_cache) ||
+        (reinterpret_cast<uintptr_t>(k_scales) & 3u) || (reinterpret_cast<uintptr_t>(v_scales) & 3u))
+        return PA_ERR_INVALID_ARG;
+    const int group = num_q_heads / num_kv_heads;
+    if (head_dim != 128 || group > 8) return PA_ERR_UNSUPPORTED;
+    const int64_t rows = (int64_t)num_blocks * num_kv_heads * kBlockSize;
+    if (rows >= ((int64_t)1 << 31)) return PA_ERR_UNSUPPORTED;
+    const int p = resolve_partition(partition_size, num_seqs, num_kv_heads, max_blocks_per_seq);
+    if (p < 0) return PA_ERR_INVALID_ARG;
+    const int part_blocks = p / kBlockSize;
+    const int max_parts = max(1, (max_blocks_per_seq + part_blocks - 1) / part_blocks);
+    if ((int64_t)num_seqs * num_kv_heads * max_parts >= ((int64_t)1 << 31)) return PA_ERR_UNSUPPORTED;
+    const size_t need = workspace_for(num_seqs, num_q_heads, head_dim, max_parts);
+    if (need > 0 && (workspace == nullptr || workspace_bytes < need || !aligned16(workspace)))
+        return PA_ERR_WORKSPACE;
+
+    DecodeArgs a;
+    a.out = out;
+    a.query = query;
+    a.block_tables = block_tables;
+    a.context_lens = context_lens;
+    a.part_o = static_cast<float *>(workspace);
+    a.part_ml = need > 0 ? reinterpret_cast<float2 *>(
+                               static_cast<uint8_t *>(workspace) +
+                               (((size_t)num_seqs * num_q_heads * max_parts * head_dim * sizeof(float) +
+                                 255) & ~size_t(255)))
+                         : nullptr;
+    a.status = device_status;
+    a.k_scales = k_scales;
+    a.v_scales = v_scales;
+    a.num_seqs = num_seqs;
+    a.num_q_heads = num_q_heads;
+    a.num_kv_heads = num_kv_heads;
+    a.max_blocks = max_blocks_per_seq;
+    a.num_blocks = num_blocks;
+    a.part_blocks = part_blocks;
+    a.max_parts = max_parts;
+    a.scale_log2 = scale * kLog2e;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    pa_status s = dispatch_fp8(group, a, key_cache, value_cache, rows, st);
+    if (s != PA_OK || max_parts <= 1) return s;
+    return launch_reduce<__nv_bfloat16>(a, head_dim, st);
 }

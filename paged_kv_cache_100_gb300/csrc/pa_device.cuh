@@ -4,6 +4,7 @@
 
 #include <cuda.h>
 #include <cuda_bf16.h>
+#include <cuda_fp16.h>
 #include <stdint.h>
 
 #include "pa_internal.h"
@@ -130,6 +131,69 @@ __device__ __forceinline__ void mma_bf16_16816(float (&d)[4], const uint32_t (&a
         "{%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, {%0, %1, %2, %3};"
         : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
         : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+
+// D = A * B + D with f16 inputs, fp32 accumulation.
+__device__ __forceinline__ void mma_f16_16816(float (&d)[4], const uint32_t (&a)[4], uint32_t b0,
+                                              uint32_t b1) {
+    asm volatile(
+        "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 "
+        "{%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, {%0, %1, %2, %3};"
+        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+        : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+
+// ---------------------------------------------------------------------------
+// FP8 E4M3 helpers
+// ---------------------------------------------------------------------------
+// Two E4M3 codes (low byte = first element) to f16x2; exact (every E4M3 value,
+// subnormals included, is an f16 value).
+__device__ __forceinline__ uint32_t e4m3x2_to_f16x2(uint32_t two_codes) {
+    uint32_t r;
+    asm("{\n\t.reg .b16 lo, hi;\n\tmov.b32 {lo, hi}, %1;\n\t"
+        "cvt.rn.f16x2.e4m3x2 %0, lo;\n\t}"
+        : "=r"(r)
+        : "r"(two_codes));
+    return r;
+}
+
+// E4M3 codes of two floats, round to nearest even, saturating at +-448
+// (first element in the low byte).
+__device__ __forceinline__ uint32_t f32x2_to_e4m3x2(float first, float second) {
+    uint16_t r;
+    asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(r) : "f"(second), "f"(first));
+    return r;
+}
+
+// c + a.lo * b.lo + a.hi * b.hi with f16x2 a, b and fp32 accumulation
+// (each f16 product is exact in fp32).
+__device__ __forceinline__ float dot2_f16_f32(uint32_t a, uint32_t b, float c) {
+    float d;
+    asm("{\n\t.reg .b16 al, ah, bl, bh;\n\t"
+        "mov.b32 {al, ah}, %1;\n\tmov.b32 {bl, bh}, %2;\n\t"
+        "fma.rn.f32.f16 %0, al, bl, %3;\n\t"
+        "fma.rn.f32.f16 %0, ah, bh, %0;\n\t}"
+        : "=f"(d)
+        : "r"(a), "r"(b), "f"(c));
+    return d;
+}
+
+__device__ __forceinline__ float f16lo(uint32_t w) {
+    return __half2float(__ushort_as_half((unsigned short)(w & 0xffffu)));
+}
+__device__ __forceinline__ float f16hi(uint32_t w) {
+    return __half2float(__ushort_as_half((unsigned short)(w >> 16)));
+}
+
+__device__ __forceinline__ uint32_t pack_f16x2(float lo, float hi) {
+    __half2 v = __floats2half2_rn(lo, hi);
+    return *reinterpret_cast<uint32_t *>(&v);
+}
+
+// x = head + residual in f16 (relative error of the pair about 2^-22).
+__device__ __forceinline__ void split_f16x2(float x0, float x1, uint32_t &head, uint32_t &rest) {
+    head = pack_f16x2(x0, x1);
+    rest = pack_f16x2(x0 - f16lo(head), x1 - f16hi(head));
 }
 
 // ---------------------------------------------------------------------------

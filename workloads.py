@@ -262,3 +262,70 @@ def device_values(wl: Workload, device, seed: int | None = None):
 
     return (draw((B, Hq, D)), draw(wl.pool_shape()), draw(wl.pool_shape()),
             draw((B, Hkv, D)), draw((B, Hkv, D)))
+
+
+# ---------------------------------------------------------------------------
+# FP8 (E4M3) pools
+# ---------------------------------------------------------------------------
+FP8_RANGE_SIGMAS = 8.0      # +-8 standard deviations map to the largest code, 448
+
+
+def fp8_scales(wl: Workload) -> np.ndarray:
+    """Per-KV-head scales: a stored code stands for code_value * scale."""
+    return np.full(wl.num_kv_heads, FP8_RANGE_SIGMAS * wl.value_std / 448.0, dtype=np.float32)
+
+
+def to_e4m3_codes(x: np.ndarray, scale: np.ndarray) -> np.ndarray:
+    """E4M3 codes of x / scale (per KV head on axis 1), clamped to +-448 first."""
+    import torch
+    s = np.asarray(scale, np.float32).reshape((1, -1) + (1,) * (x.ndim - 2))
+    q = np.clip(np.asarray(x, np.float32) / s, -448.0, 448.0).astype(np.float32)
+    return torch.from_numpy(q).to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+
+
+@dataclass
+class Fp8HostValues:
+    query: np.ndarray        # [B][Hq][D] bf16 bits
+    key_cache: np.ndarray    # [NB][Hkv][16][D] E4M3 codes
+    value_cache: np.ndarray
+    key_new: np.ndarray      # [B][Hkv][D] bf16 bits (quantised by the cache write)
+    value_new: np.ndarray
+    k_scales: np.ndarray     # [Hkv] float32
+    v_scales: np.ndarray
+
+
+def fp8_host_values(wl: Workload, seed: int | None = None, poison_unused: bool = True):
+    """Host values for FP8 pools: normal values quantised to E4M3 per KV head; with
+    ``poison_unused`` the slots holding no context token get the NaN code 0x7F."""
+    hv = host_values(wl, seed=seed, poison_unused=False)
+    f = bf16_bits_to_f32 if hv.key_cache.dtype == np.uint16 else (lambda a: a)
+    ks = fp8_scales(wl)
+    vs = fp8_scales(wl)
+    kc = to_e4m3_codes(f(hv.key_cache), ks)
+    vc = to_e4m3_codes(f(hv.value_cache), vs)
+    if poison_unused:
+        mask = used_slot_mask(wl)
+        kc[~mask] = 0x7F
+        vc[~mask] = 0x7F
+    q, kn, vn = hv.query, hv.key_new, hv.value_new
+    if q.dtype != np.uint16:
+        q, kn, vn = to_bf16_bits(q), to_bf16_bits(kn), to_bf16_bits(vn)
+    return Fp8HostValues(q, kc, vc, kn, vn, ks, vs)
+
+
+def fp8_device_values(wl: Workload, device, seed: int | None = None):
+    """(query bf16, key_cache uint8, value_cache uint8, key_new bf16, value_new bf16,
+    k_scales, v_scales) drawn on a CUDA device with a seeded torch generator."""
+    import torch
+    q, kc, vc, kn, vn = device_values(wl, device, seed=seed)
+    ks = torch.from_numpy(fp8_scales(wl)).to(device)
+    vs = torch.from_numpy(fp8_scales(wl)).to(device)
+
+    def quant(pool, s):
+        out = torch.empty(pool.shape, dtype=torch.uint8, device=device)
+        for b0 in range(0, pool.shape[0], 4096):
+            x = pool[b0:b0 + 4096].float() / s.view(1, -1, 1, 1)
+            out[b0:b0 + 4096] = x.clamp_(-448, 448).to(torch.float8_e4m3fn).view(torch.uint8)
+        return out
+
+    return q, quant(kc, ks), quant(vc, vs), kn, vn, ks, vs
