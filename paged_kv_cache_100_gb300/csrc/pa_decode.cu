@@ -1188,8 +1188,10 @@ cudaError_t allow_smem(K kernel, size_t bytes) {
 #ifndef PA_GQA16_STAGES
 #define PA_GQA16_STAGES 2
 #endif
-// FP8 pools (4 KiB per block): MHA 8 warps x 2 stages, GQA 4 warps x 4 stages
-// (64 KiB each, three CTAs per SM).
+// FP8 pools (4 KiB per block): MHA 8 warps x 2 stages (64 KiB, three CTAs per
+// SM); GQA 8 warps x 2 stages (32 KiB; about 120 registers make it two CTAs
+// per SM).  Measured alternatives: MHA 8x1, 8x3, 8x4, 12x2, 16x2; GQA 4x2,
+// 4x4, 4x6, 6x2, 8x3.
 #ifndef PA_MHA8_WARPS
 #define PA_MHA8_WARPS 8
 #endif
@@ -1197,10 +1199,10 @@ cudaError_t allow_smem(K kernel, size_t bytes) {
 #define PA_MHA8_STAGES 2
 #endif
 #ifndef PA_GQA8_WARPS
-#define PA_GQA8_WARPS 4
+#define PA_GQA8_WARPS 8
 #endif
 #ifndef PA_GQA8_STAGES
-#define PA_GQA8_STAGES 4
+#define PA_GQA8_STAGES 2
 #endif
 constexpr int kNW = 4;   // fp32 kernel
 
