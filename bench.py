@@ -244,10 +244,11 @@ def measured_traffic(workload: str):
 class StepOps:
     """The library calls of one step for bf16 (or f32) pools or FP8 pools."""
 
-    def __init__(self, pkv, wl, kc, vc, ks, vs, P, ws):
+    def __init__(self, pkv, wl, kc, vc, ks, vs, P, ws, n_prefix=0):
         self.pkv, self.wl, self.kc, self.vc, self.ks, self.vs = pkv, wl, kc, vc, ks, vs
         self.P, self.ws = P, ws
         self.fp8 = ks is not None
+        self.n_prefix = n_prefix          # > 0: shared-prefix (cascade) decode
 
     def write(self, kn, vn, slots):
         if self.fp8:
@@ -256,7 +257,11 @@ class StepOps:
             self.pkv.cache_write(self.kc, self.vc, kn, vn, slots)
 
     def decode(self, q, bt, lens, out):
-        if self.fp8:
+        if self.n_prefix:
+            self.pkv.decode_shared_prefix(q, self.kc, self.vc, bt, lens, self.n_prefix,
+                                          self.wl.scale, out=out, partition_size=self.P,
+                                          workspace=self.ws)
+        elif self.fp8:
             self.pkv.decode_fp8(q, self.kc, self.vc, self.ks, self.vs, bt, lens, self.wl.scale,
                                 out=out, partition_size=self.P, workspace=self.ws)
         else:
@@ -297,7 +302,17 @@ def run_gpu(args):
                                                     wl.head_dim, wl.max_blocks, P, kv_dtype), 16),
                      dtype=torch.uint8, device=dev)
     stream = torch.cuda.current_stream(dev)
-    ops = StepOps(pkv, wl, kc, vc, ks, vs, P, ws)
+    n_prefix = 0
+    if args.decode != "plain" and not fp8:
+        n_prefix = pkv.shared_prefix_blocks(wl.block_tables)
+        if args.decode == "auto" and n_prefix < 4:
+            n_prefix = 0
+    if n_prefix:
+        P = args.partition_size or wl.partition_size
+        ws = torch.empty(max(pkv.lib().pa_decode_shared_prefix_workspace_bytes(
+            wl.num_seqs, wl.num_q_heads, wl.num_kv_heads, wl.head_dim, wl.max_blocks, n_prefix,
+            P), 16), dtype=torch.uint8, device=dev)
+    ops = StepOps(pkv, wl, kc, vc, ks, vs, P, ws, n_prefix)
 
     def step(ev_pre=None, ev_post=None):
         ops.write(kn, vn, slots)
@@ -382,9 +397,12 @@ def run_gpu(args):
         "context_tokens_per_s": float(wl.step_context_lens.sum()) * world / (ms_per_step * 1e-3),
         "hbm_frac_of_measured": achieved / peak if peak_kind == "measured" else None,
         "hbm_frac_of_nominal_7900": achieved / NOMINAL_HBM_GBS,
+        "decode_method": (f"shared-prefix cascade ({n_prefix} shared blocks read once per KV "
+                          "head; prefix, suffix and merge kernels)") if n_prefix else "paged decode",
         "roofline": {
-            "kernel": "pa_decode call (partition kernel, plus the merge kernel when a sequence "
-                      "spans several partitions)",
+            "kernel": ("pa_decode_shared_prefix call (prefix + suffix + merge kernels)" if n_prefix
+                       else "pa_decode call (partition kernel, plus the merge kernel when a "
+                            "sequence spans several partitions)"),
             "bound": "hbm",
             "achieved": achieved,
             "peak": peak,
@@ -620,6 +638,9 @@ def main(argv=None):
     ap.add_argument("--warmup", type=int, default=50)
     ap.add_argument("--workload", default="llama7b_mha", choices=W.WORKLOADS)
     ap.add_argument("--partition-size", type=int, default=0)
+    ap.add_argument("--decode", default="auto", choices=["auto", "plain", "shared-prefix"],
+                    help="auto: the shared-prefix cascade when every table shares >= 4 leading "
+                         "blocks (bf16 pools), else paged decode")
     ap.add_argument("--kv-dtype", default="bf16", choices=["bf16", "fp8"],
                     help="element type of the K/V pools (fp8 = E4M3 with per-head scales)")
     ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])

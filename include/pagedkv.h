@@ -71,6 +71,7 @@ typedef enum pa_dtype {
 #define PA_DEV_BAD_SLOT        4  /* slot >= num_blocks * block_size */
 #define PA_DEV_BAD_COPY_PAIR   8  /* a copy pair index outside [0, num_blocks) */
 #define PA_DEV_TIMEOUT        16  /* a bounded in-kernel wait gave up */
+#define PA_DEV_PREFIX_MISMATCH 32 /* pa_decode_shared_prefix: tables do not share the prefix */
 
 /* Human-readable name of a status. Never NULL. */
 const char *pa_status_string(pa_status status);
@@ -143,6 +144,37 @@ pa_status pa_decode(void *out, const void *query, const void *key_cache, const v
                     int max_blocks_per_seq, int num_blocks, float scale, pa_dtype dtype,
                     int partition_size, void *workspace, size_t workspace_bytes,
                     int32_t *device_status, void *stream);
+
+/*
+ * Paged decode attention for a batch whose block tables all begin with the same
+ * num_prefix_blocks physical blocks (a shared prefix: "PagedAttention por
+ * dentro", section "Copy-on-write para sampling paralelo" and "Prefix caching
+ * cross-session" - several sequences reading the same blocks).  Same result
+ * as pa_decode with the same arguments; the shared blocks are read once per
+ * KV head for all sequences instead of once per sequence.
+ *  num_prefix_blocks  length of the shared prefix in blocks; the blocks are
+ *                     taken from the first row of block_tables and every row
+ *                     must list the same ones (a row that does not is flagged
+ *                     PA_DEV_PREFIX_MISMATCH and its result is undefined).
+ *                     Contexts shorter than the prefix are handled (their
+ *                     positions past the context are masked).  0 = pa_decode.
+ *  partition_size     split-K partition of the part past the prefix (0 = the
+ *                     library's choice for max_blocks_per_seq - num_prefix_blocks)
+ *  workspace          at least pa_decode_shared_prefix_workspace_bytes(...)
+ * bf16 only; head_dim 64 or 128; group as in pa_decode.  Launches three kernels
+ * (prefix, suffix, merge).
+ */
+size_t pa_decode_shared_prefix_workspace_bytes(int num_seqs, int num_q_heads, int num_kv_heads,
+                                               int head_dim, int max_blocks_per_seq,
+                                               int num_prefix_blocks, int partition_size);
+pa_status pa_decode_shared_prefix(void *out, const void *query, const void *key_cache,
+                                  const void *value_cache, const int32_t *block_tables,
+                                  const int32_t *context_lens, int num_seqs, int num_q_heads,
+                                  int num_kv_heads, int head_dim, int block_size,
+                                  int max_blocks_per_seq, int num_blocks, float scale,
+                                  pa_dtype dtype, int num_prefix_blocks, int partition_size,
+                                  void *workspace, size_t workspace_bytes, int32_t *device_status,
+                                  void *stream);
 
 /*
  * Paged decode attention over FP8 pools.  The pages name quantising the KV

@@ -38,6 +38,9 @@ SIGNATURES = {
                         vp, sz, vp, vp]),
     "pa_decode_static_scratch": (i32, [vp, vp, vp, vp, vp, vp, i32, i32, i32, i32, i32, i32, i32,
                                        f32, i32, i32, vp, vp]),
+    "pa_decode_shared_prefix_workspace_bytes": (sz, [i32, i32, i32, i32, i32, i32, i32]),
+    "pa_decode_shared_prefix": (i32, [vp, vp, vp, vp, vp, vp, i32, i32, i32, i32, i32, i32, i32,
+                                      f32, i32, i32, i32, vp, sz, vp, vp]),
     "pa_decode_fp8": (i32, [vp, vp, vp, vp, vp, vp, vp, vp, i32, i32, i32, i32, i32, i32, i32, f32,
                             i32, vp, sz, vp, vp]),
     "pa_cache_write_fp8": (i32, [vp, vp, vp, vp, vp, vp, vp, i32, i32, i32, i32, i32, vp, vp]),
@@ -75,6 +78,7 @@ PA_DEV_BAD_CONTEXT_LEN = 2
 PA_DEV_BAD_SLOT = 4
 PA_DEV_BAD_COPY_PAIR = 8
 PA_DEV_TIMEOUT = 16
+PA_DEV_PREFIX_MISMATCH = 32
 
 
 class PagedKVError(RuntimeError):

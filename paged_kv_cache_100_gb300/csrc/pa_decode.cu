@@ -68,8 +68,15 @@ struct DecodeArgs {
     int max_blocks;     // block-table row length
     int num_blocks;     // pool size
     int part_blocks;    // partition size in blocks
-    int max_parts;      // partitions of the longest possible context
+    int max_parts;      // partition rows per (sequence, query head) in the workspace
     float scale_log2;   // softmax scale * log2(e)
+    // Shared-prefix (cascade) mode; all zero for plain decode.
+    int token_offset;   // tokens of every context handled elsewhere (a multiple of 16)
+    int part_base;      // workspace partition rows used before this kernel's partitions
+    int always_partial; // write (max, sum, output) partials even for one partition
+    int prefix_blocks;  // shared prefix length in blocks (prefix kernel)
+    int prefix_chunk_blocks;
+    int prefix_chunks;
 };
 
 // The (sequence, head, partition) a CTA works on, with its token range.
@@ -97,6 +104,7 @@ __device__ __forceinline__ bool cta_work(const DecodeArgs &a, int heads_axis, Wo
         if (threadIdx.x == 0 && w.part == 0 && w.head == 0) report(a.status, PA_DEV_BAD_CONTEXT_LEN);
         L = L < 0 ? 0 : lmax;
     }
+    L = max(L - a.token_offset, 0);   // the part of the context this kernel covers
     w.L = L;
     const int seq_blocks = (L + kBlockSize - 1) / kBlockSize;
     w.nparts = seq_blocks == 0 ? 1 : (seq_blocks + a.part_blocks - 1) / a.part_blocks;
@@ -139,11 +147,11 @@ __device__ __forceinline__ void merge_and_store(const DecodeArgs &a, const Work 
             O += wk * acc_base[k * acc_warp_stride + r * D + d];
         }
         const int h = first_head + r;
-        if (w.nparts == 1) {
+        if (w.nparts == 1 && !a.always_partial) {
             OutT *out = static_cast<OutT *>(a.out) + ((size_t)w.b * a.num_q_heads + h) * D + d;
             store_out<OutT>(out, Lsum > 0.f ? O / Lsum : 0.f);
         } else {
-            const size_t row = ((size_t)w.b * a.num_q_heads + h) * a.max_parts + w.part;
+            const size_t row = ((size_t)w.b * a.num_q_heads + h) * a.max_parts + a.part_base + w.part;
             a.part_o[row * D + d] = O;
             if (d == 0) a.part_ml[row] = make_float2(M, Lsum);
         }
@@ -927,7 +935,8 @@ pa_decode_bf16_kernel(const __grid_constant__ CUtensorMap kmap,
         tma_prefetch_desc(&kmap);
         tma_prefetch_desc(&vmap);
     }
-    const int32_t *trow = a.block_tables + (size_t)w.b * a.max_blocks + w.blk0;
+    const int32_t *trow =
+        a.block_tables + (size_t)w.b * a.max_blocks + a.token_offset / kBlockSize + w.blk0;
     for (int i = threadIdx.x; i < w.nblk; i += NW * 32) {
         int phys = trow[i];
         if ((unsigned)phys >= (unsigned)a.num_blocks) {
@@ -1013,6 +1022,284 @@ pa_decode_bf16_kernel(const __grid_constant__ CUtensorMap kmap,
                                        STAGES * Lay::kStageBytes / 4, s_m, s_l, Lay::kRowsMax);
 }
 
+// ---------------------------------------------------------------------------
+// Shared-prefix (cascade) attention.  When every block table of the batch
+// starts with the same physical blocks, those blocks' K/V are the same for all
+// sequences: instead of each sequence streaming them, one CTA streams a chunk
+// of the prefix once for 64 query rows (16 per warp) taken across sequences,
+// and the products become dense 16-row tensor-core tiles (query rows on M,
+// tokens and head-dim elements on N/K; P.V with P split into bf16 head and
+// residual).  Each (row, prefix chunk) leaves a partial (max, sum, output) in
+// the workspace; the suffix of every context runs through the decode kernel in
+// partial mode, and the merge kernel combines both.  The attention arithmetic
+// is unchanged: the softmax over the whole context is the merge of softmaxes
+// over its parts.
+// ---------------------------------------------------------------------------
+template <int D>
+struct PrefixWarp {
+    static constexpr int KS = D / 16;
+    static constexpr int NT = D / 8;
+
+    uint32_t qa[KS][4];
+    float o[NT][4];
+    float m0, m1, l0, l1;
+    int lim0, lim1;     // tokens of the rows' contexts (positions >= limit are masked)
+    float scale_log2;
+    int lane, g, t;
+
+    // rows r0 + g and r0 + g + 8 of this KV head's query rows (row = b * G + j)
+    __device__ __forceinline__ void init(const DecodeArgs &a, int kvh, int group, int rows_total,
+                                         int r0, int lane_) {
+        lane = lane_;
+        g = lane >> 2;
+        t = lane & 3;
+        scale_log2 = a.scale_log2;
+        const int lmax = a.max_blocks * kBlockSize;
+        int lims[2];
+        const uint32_t *qr[2];
+#pragma unroll
+        for (int k = 0; k < 2; ++k) {
+            const int r = r0 + g + 8 * k;
+            if (r < rows_total) {
+                const int b = r / group, j = r - b * group;
+                const int L = a.context_lens[b];
+                lims[k] = L < 0 ? 0 : (L > lmax ? lmax : L);
+                qr[k] = reinterpret_cast<const uint32_t *>(
+                    static_cast<const __nv_bfloat16 *>(a.query) +
+                    ((size_t)b * a.num_q_heads + (size_t)kvh * group + j) * D);
+            } else {
+                lims[k] = 0;
+                qr[k] = nullptr;
+            }
+        }
+        lim0 = lims[0];
+        lim1 = lims[1];
+#pragma unroll
+        for (int ks = 0; ks < KS; ++ks) {
+            qa[ks][0] = qr[0] ? qr[0][(16 * ks + 2 * t) / 2] : 0u;
+            qa[ks][2] = qr[0] ? qr[0][(16 * ks + 8 + 2 * t) / 2] : 0u;
+            qa[ks][1] = qr[1] ? qr[1][(16 * ks + 2 * t) / 2] : 0u;
+            qa[ks][3] = qr[1] ? qr[1][(16 * ks + 8 + 2 * t) / 2] : 0u;
+        }
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt) o[nt][0] = o[nt][1] = o[nt][2] = o[nt][3] = 0.f;
+        m0 = m1 = -INFINITY;
+        l0 = l1 = 0.f;
+    }
+
+    // One full 16-token block whose first token has context position tok0.
+    __device__ __forceinline__ void block(uint32_t ktile, uint32_t vtile, int tok0) {
+        // two independent accumulation chains per n-tile halve the dependent
+        // mma chain of Q.K^T
+        float s[2][4], u[2][4];
+#pragma unroll
+        for (int j = 0; j < 2; ++j)
+            s[j][0] = s[j][1] = s[j][2] = s[j][3] = u[j][0] = u[j][1] = u[j][2] = u[j][3] = 0.f;
+        const int mi = lane >> 3, rr = lane & 7;
+#pragma unroll
+        for (int kk = 0; kk < D / 32; ++kk) {
+#pragma unroll
+            for (int j = 0; j < 2; ++j) {
+                uint32_t b[4];
+                ldsm_x4(b, swz(ktile, 8 * j + rr, 4 * kk + mi));
+                mma_bf16_16816(s[j], qa[2 * kk], b[0], b[1]);
+                mma_bf16_16816(u[j], qa[2 * kk + 1], b[2], b[3]);
+            }
+        }
+#pragma unroll
+        for (int j = 0; j < 2; ++j)
+#pragma unroll
+            for (int e = 0; e < 4; ++e) s[j][e] += u[j][e];
+#pragma unroll
+        for (int j = 0; j < 2; ++j)
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                const int tok = tok0 + 8 * j + 2 * t + (e & 1);
+                const int lim = e < 2 ? lim0 : lim1;
+                s[j][e] = tok < lim ? s[j][e] * scale_log2 : -INFINITY;
+            }
+        float mx0 = fmaxf(fmaxf(s[0][0], s[0][1]), fmaxf(s[1][0], s[1][1]));
+        float mx1 = fmaxf(fmaxf(s[0][2], s[0][3]), fmaxf(s[1][2], s[1][3]));
+        mx0 = fmaxf(mx0, __shfl_xor_sync(kFull, mx0, 1));
+        mx0 = fmaxf(mx0, __shfl_xor_sync(kFull, mx0, 2));
+        mx1 = fmaxf(mx1, __shfl_xor_sync(kFull, mx1, 1));
+        mx1 = fmaxf(mx1, __shfl_xor_sync(kFull, mx1, 2));
+        // a row may have no valid token yet (all -inf): keep its state at zero
+        const float mn0 = fmaxf(m0, mx0), mn1 = fmaxf(m1, mx1);
+        const float ref0 = mn0 == -INFINITY ? 0.f : mn0, ref1 = mn1 == -INFINITY ? 0.f : mn1;
+        const float a0 = exp2f(m0 - ref0), a1 = exp2f(m1 - ref1);
+        m0 = mn0;
+        m1 = mn1;
+        float p[2][4];
+#pragma unroll
+        for (int j = 0; j < 2; ++j) {
+            p[j][0] = exp2f(s[j][0] - ref0);
+            p[j][1] = exp2f(s[j][1] - ref0);
+            p[j][2] = exp2f(s[j][2] - ref1);
+            p[j][3] = exp2f(s[j][3] - ref1);
+        }
+        l0 = l0 * a0 + (p[0][0] + p[0][1]) + (p[1][0] + p[1][1]);
+        l1 = l1 * a1 + (p[0][2] + p[0][3]) + (p[1][2] + p[1][3]);
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt) {
+            o[nt][0] *= a0;
+            o[nt][1] *= a0;
+            o[nt][2] *= a1;
+            o[nt][3] *= a1;
+        }
+        uint32_t pa[4], pl[4];
+        split_bf16x2(p[0][0], p[0][1], pa[0], pl[0]);
+        split_bf16x2(p[0][2], p[0][3], pa[1], pl[1]);
+        split_bf16x2(p[1][0], p[1][1], pa[2], pl[2]);
+        split_bf16x2(p[1][2], p[1][3], pa[3], pl[3]);
+#pragma unroll
+        for (int dd = 0; dd < D / 16; ++dd) {
+            uint32_t b[4];
+            ldsm_x4_trans(b, swz(vtile, (mi & 1) * 8 + rr, 2 * dd + (mi >> 1)));
+            mma_bf16_16816(o[2 * dd], pa, b[0], b[1]);
+            mma_bf16_16816(o[2 * dd + 1], pa, b[2], b[3]);
+            mma_bf16_16816(o[2 * dd], pl, b[0], b[1]);
+            mma_bf16_16816(o[2 * dd + 1], pl, b[2], b[3]);
+        }
+    }
+
+    // Partial state of rows r0 + g and r0 + g + 8 into workspace partition `part`.
+    __device__ __forceinline__ void store(const DecodeArgs &a, int kvh, int group, int rows_total,
+                                          int r0, int part) {
+        l0 += __shfl_xor_sync(kFull, l0, 1);
+        l0 += __shfl_xor_sync(kFull, l0, 2);
+        l1 += __shfl_xor_sync(kFull, l1, 1);
+        l1 += __shfl_xor_sync(kFull, l1, 2);
+#pragma unroll
+        for (int k = 0; k < 2; ++k) {
+            const int r = r0 + g + 8 * k;
+            if (r >= rows_total) continue;
+            const int b = r / group, j = r - b * group;
+            const size_t row =
+                ((size_t)b * a.num_q_heads + (size_t)kvh * group + j) * a.max_parts + part;
+            float *dst = a.part_o + row * D;
+#pragma unroll
+            for (int nt = 0; nt < NT; ++nt)
+                *reinterpret_cast<float2 *>(dst + 8 * nt + 2 * t) =
+                    k == 0 ? make_float2(o[nt][0], o[nt][1]) : make_float2(o[nt][2], o[nt][3]);
+            if (t == 0) a.part_ml[row] = k == 0 ? make_float2(m0, l0) : make_float2(m1, l1);
+        }
+    }
+};
+
+constexpr int kPrefixWarps = 4;     // consumer warps; one more warp issues the TMA loads
+constexpr int kPrefixRows = 16 * kPrefixWarps;
+
+template <int D, int STAGES>
+__global__ void __launch_bounds__((kPrefixWarps + 1) * 32)
+pa_prefix_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CUtensorMap vmap,
+                 const DecodeArgs a) {
+    constexpr int kTile = 16 * D * 2;
+    constexpr int kStage = 2 * kTile;
+    grid_dependency_wait();
+    grid_dependents_launch();
+    const int group = a.num_q_heads / a.num_kv_heads;
+    const int rows_total = a.num_seqs * group;
+    const int row_chunks = (rows_total + kPrefixRows - 1) / kPrefixRows;
+    int idx = blockIdx.x;
+    const int pc = idx % a.prefix_chunks;
+    idx /= a.prefix_chunks;
+    const int rc = idx % row_chunks;
+    const int kvh = idx / row_chunks;
+    const int blk0 = pc * a.prefix_chunk_blocks;
+    const int nblk = min(a.prefix_blocks - blk0, a.prefix_chunk_blocks);
+
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *stages = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                                  ~uintptr_t(1023));
+    uint64_t *full = reinterpret_cast<uint64_t *>(stages + STAGES * kStage);
+    uint64_t *empty = full + STAGES;
+    int32_t *s_table = reinterpret_cast<int32_t *>(empty + STAGES);
+    __shared__ int s_fail;
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    if (threadIdx.x == 0) {
+        s_fail = 0;
+        for (int s = 0; s < STAGES; ++s) {
+            mbar_init(&full[s], 1);
+            mbar_init(&empty[s], kPrefixWarps);
+        }
+        fence_mbar_init();
+        tma_prefetch_desc(&kmap);
+        tma_prefetch_desc(&vmap);
+    }
+    // the shared blocks, from the first sequence's table
+    for (int i = threadIdx.x; i < nblk; i += blockDim.x) {
+        int phys = a.block_tables[blk0 + i];
+        if ((unsigned)phys >= (unsigned)a.num_blocks) {
+            report(a.status, PA_DEV_BAD_BLOCK_ID);
+            phys = 0;
+        }
+        s_table[i] = phys;
+    }
+    // every sequence of this row chunk must list the same blocks (checked once,
+    // by the CTAs of KV head 0)
+    if (kvh == 0) {
+        const int b_first = rc * kPrefixRows / group;
+        const int b_last = min(a.num_seqs, ((rc + 1) * kPrefixRows + group - 1) / group);
+        for (int i = threadIdx.x; i < (b_last - b_first) * nblk; i += blockDim.x) {
+            const int b = b_first + i / nblk, j = blk0 + i % nblk;
+            if (a.block_tables[(size_t)b * a.max_blocks + j] != a.block_tables[j])
+                report(a.status, PA_DEV_PREFIX_MISMATCH);
+        }
+    }
+    __syncthreads();
+
+    if (warp == kPrefixWarps) {          // producer
+        if (lane == 0) {
+            for (int it = 0; it < nblk; ++it) {
+                const int s = it % STAGES;
+                if (it >= STAGES && !mbar_wait_bounded(&empty[s], ((it / STAGES) - 1) & 1)) {
+                    report(a.status, PA_DEV_TIMEOUT);
+                    s_fail = 1;
+                    break;
+                }
+                const int y = (s_table[it] * a.num_kv_heads + kvh) * kBlockSize;
+                uint8_t *kt = stages + s * kStage;
+                uint8_t *vt = kt + kTile;
+                mbar_arrive_expect_tx(&full[s], kStage);
+#pragma unroll
+                for (int x = 0; x < D; x += 64) {
+                    tma_load_2d(kt + (x / 64) * 2048, &kmap, x, y, &full[s]);
+                    tma_load_2d(vt + (x / 64) * 2048, &vmap, x, y, &full[s]);
+                }
+            }
+        }
+        return;
+    }
+
+    PrefixWarp<D> pw;
+    const int r0 = rc * kPrefixRows + warp * 16;
+    pw.init(a, kvh, group, rows_total, r0, lane);
+    bool ok = true;
+    int it = 0;
+    for (; it < nblk; ++it) {
+        const int s = it % STAGES;
+        const bool done = mbar_wait_bounded(&full[s], (it / STAGES) & 1);
+        if (!__all_sync(kFull, done)) {
+            ok = false;
+            break;
+        }
+        const uint32_t kt = smem_u32(stages + s * kStage);
+        pw.block(kt, kt + kTile, (blk0 + it) * kBlockSize);
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&empty[s]);
+    }
+    if (!ok) {
+        // give copies that may still be in flight a bounded chance to land first
+        for (int k = it; k < nblk && k < it + STAGES; ++k)
+            (void)mbar_wait_bounded(&full[k % STAGES], (k / STAGES) & 1);
+        if (lane == 0) report(a.status, PA_DEV_TIMEOUT);
+        return;
+    }
+    pw.store(a, kvh, group, rows_total, r0, pc);
+}
+
 // fp32 kernel: one CTA per (sequence, query head, partition); lane owns
 // head-dim elements lane + 32 e.  Plain loads; online softmax per token.
 template <int D, int NW>
@@ -1037,7 +1324,8 @@ __global__ void __launch_bounds__(NW * 32) pa_decode_f32_kernel(const float *__r
         acc[e] = 0.f;
     }
     float m = -INFINITY, l = 0.f;
-    const int32_t *trow = a.block_tables + (size_t)w.b * a.max_blocks + w.blk0;
+    const int32_t *trow =
+        a.block_tables + (size_t)w.b * a.max_blocks + a.token_offset / kBlockSize + w.blk0;
     for (int j = warp; j < w.nblk; j += NW) {
         int phys = trow[j];
         if ((unsigned)phys >= (unsigned)a.num_blocks) {
@@ -1084,9 +1372,11 @@ __global__ void __launch_bounds__(128) pa_reduce_kernel(const DecodeArgs a, int 
     int L = a.context_lens[b];
     const int lmax = a.max_blocks * kBlockSize;
     L = L < 0 ? 0 : (L > lmax ? lmax : L);
+    L = max(L - a.token_offset, 0);
     const int seq_blocks = (L + kBlockSize - 1) / kBlockSize;
-    const int nparts = seq_blocks == 0 ? 1 : (seq_blocks + a.part_blocks - 1) / a.part_blocks;
-    if (nparts <= 1) return;
+    const int nparts =
+        a.part_base + (seq_blocks == 0 ? 1 : (seq_blocks + a.part_blocks - 1) / a.part_blocks);
+    if (nparts <= 1 && !a.always_partial) return;
     const size_t row0 = ((size_t)b * a.num_q_heads + h) * a.max_parts;
     extern __shared__ float s_w[];   // [nparts] weights
     __shared__ float s_M, s_L;
@@ -1217,7 +1507,9 @@ pa_status launch_bf16(const DecodeArgs &a, const void *kc, const void *vc, int64
     auto kernel = pa_decode_bf16_kernel<D, Consumer, NW, STAGES>;
     cudaError_t e = allow_smem(kernel, smem);
     if (e != cudaSuccess) return cuda_failure(e, "cudaFuncSetAttribute(decode)");
-    const int64_t grid = (int64_t)a.num_seqs * a.num_kv_heads * a.max_parts;
+    // partitions this kernel owns (the workspace rows before part_base belong to
+    // the shared-prefix kernel)
+    const int64_t grid = (int64_t)a.num_seqs * a.num_kv_heads * (a.max_parts - a.part_base);
     e = launch_chained(kernel, dim3((unsigned)grid), dim3(NW * 32), smem, stream, kmap, vmap, a);
     if (e != cudaSuccess) return cuda_failure(e, "pa_decode_bf16_kernel launch");
     count_launches(1);
@@ -1430,6 +1722,8 @@ extern "C" pa_status pa_decode(void *out, const void *query, const void *key_cac
     a.part_blocks = part_blocks;
     a.max_parts = max_parts;
     a.scale_log2 = scale * kLog2e;
+    a.token_offset = a.part_base = a.always_partial = 0;
+    a.prefix_blocks = a.prefix_chunk_blocks = a.prefix_chunks = 0;
     cudaStream_t st = static_cast<cudaStream_t>(stream);
 
     pa_status s;
@@ -1506,8 +1800,219 @@ extern "C" pa_status pa_decode_fp8(void *out, const void *query, const void *key
     a.part_blocks = part_blocks;
     a.max_parts = max_parts;
     a.scale_log2 = scale * kLog2e;
+    a.token_offset = a.part_base = a.always_partial = 0;
+    a.prefix_blocks = a.prefix_chunk_blocks = a.prefix_chunks = 0;
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     pa_status s = dispatch_fp8(group, a, key_cache, value_cache, rows, st);
     if (s != PA_OK || max_parts <= 1) return s;
+    return launch_reduce<__nv_bfloat16>(a, head_dim, st);
+}
+
+namespace pa {
+namespace {
+
+constexpr int kPrefixStages = 4;
+
+// A library-owned side stream per device, with a fork and a join event, so
+// that the prefix kernel (tensor-core bound) runs alongside the suffix decode
+// (HBM bound).  The host sequence record / wait / launch / record / wait is
+// serialised by a mutex so concurrent callers cannot interleave the events.
+struct SideStream {
+    cudaStream_t stream = nullptr;
+    cudaEvent_t fork = nullptr, join = nullptr;
+};
+std::mutex g_side_mutex;
+SideStream g_side[64];
+
+pa_status side_stream_locked(SideStream **out) {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return cuda_failure(e, "cudaGetDevice");
+    if (dev < 0 || dev >= 64) return PA_ERR_UNSUPPORTED;
+    SideStream &ss = g_side[dev];
+    if (ss.stream == nullptr) {
+        e = cudaStreamCreateWithFlags(&ss.stream, cudaStreamNonBlocking);
+        if (e == cudaSuccess) e = cudaEventCreateWithFlags(&ss.fork, cudaEventDisableTiming);
+        if (e == cudaSuccess) e = cudaEventCreateWithFlags(&ss.join, cudaEventDisableTiming);
+        if (e != cudaSuccess) {
+            ss = SideStream();
+            return cuda_failure(e, "side stream set-up");
+        }
+    }
+    *out = &ss;
+    return PA_OK;
+}
+
+// Chunks of the shared prefix: about three CTAs per SM (each CTA works through
+// its chunk block after block, so short chunks finish sooner), at least 4
+// blocks per chunk.
+void prefix_chunking(int prefix_blocks, int kv_heads, int row_chunks, int *chunk_blocks,
+                     int *chunks) {
+    const int64_t per_chunk_ctas = (int64_t)kv_heads * row_chunks;
+    int want = (int)std::max<int64_t>(1, (3LL * sm_count() + per_chunk_ctas - 1) / per_chunk_ctas);
+    int cb = std::max(4, (prefix_blocks + want - 1) / std::max(1, want));
+    cb = std::min(cb, std::max(prefix_blocks, 1));
+    *chunk_blocks = cb;
+    *chunks = prefix_blocks == 0 ? 0 : (prefix_blocks + cb - 1) / cb;
+}
+
+struct SharedPlan {
+    int suffix_part_blocks, suffix_max_parts, prefix_chunk_blocks, prefix_chunks, max_parts;
+};
+
+bool plan_shared(int num_seqs, int num_q_heads, int num_kv_heads, int max_blocks_per_seq,
+                 int num_prefix_blocks, int partition_size, SharedPlan *p) {
+    if (num_prefix_blocks < 0 || num_prefix_blocks > max_blocks_per_seq) return false;
+    const int suffix_blocks = max_blocks_per_seq - num_prefix_blocks;
+    const int ps = resolve_partition(partition_size, num_seqs, num_kv_heads, suffix_blocks);
+    if (ps < 0) return false;
+    p->suffix_part_blocks = ps / kBlockSize;
+    p->suffix_max_parts = std::max(1, (suffix_blocks + p->suffix_part_blocks - 1) / p->suffix_part_blocks);
+    const int group = num_q_heads / num_kv_heads;
+    const int row_chunks = (num_seqs * group + kPrefixRows - 1) / kPrefixRows;
+    prefix_chunking(num_prefix_blocks, num_kv_heads, row_chunks, &p->prefix_chunk_blocks,
+                    &p->prefix_chunks);
+    p->max_parts = p->prefix_chunks + p->suffix_max_parts;
+    return true;
+}
+
+}  // namespace
+}  // namespace pa
+
+extern "C" size_t pa_decode_shared_prefix_workspace_bytes(int num_seqs, int num_q_heads,
+                                                          int num_kv_heads, int head_dim,
+                                                          int max_blocks_per_seq,
+                                                          int num_prefix_blocks,
+                                                          int partition_size) {
+    if (num_seqs < 0 || num_q_heads <= 0 || num_kv_heads <= 0 || head_dim <= 0 ||
+        num_q_heads % num_kv_heads != 0)
+        return (size_t)-1;
+    if (partition_size != 0 &&
+        (partition_size < kBlockSize || partition_size > kMaxPartition || partition_size % kBlockSize))
+        return (size_t)-1;
+    SharedPlan p;
+    if (!plan_shared(num_seqs, num_q_heads, num_kv_heads, max_blocks_per_seq, num_prefix_blocks,
+                     partition_size, &p))
+        return (size_t)-1;
+    const size_t rows = (size_t)num_seqs * num_q_heads * p.max_parts;
+    return ((rows * head_dim * sizeof(float) + 255) & ~size_t(255)) + rows * sizeof(float2);
+}
+
+extern "C" pa_status pa_decode_shared_prefix(
+    void *out, const void *query, const void *key_cache, const void *value_cache,
+    const int32_t *block_tables, const int32_t *context_lens, int num_seqs, int num_q_heads,
+    int num_kv_heads, int head_dim, int block_size, int max_blocks_per_seq, int num_blocks,
+    float scale, pa_dtype dtype, int num_prefix_blocks, int partition_size, void *workspace,
+    size_t workspace_bytes, int32_t *device_status, void *stream) {
+    if (num_seqs < 0 || num_q_heads <= 0 || num_kv_heads <= 0 || block_size != kBlockSize ||
+        max_blocks_per_seq < 0 || num_blocks <= 0 || num_q_heads % num_kv_heads != 0 ||
+        !(scale == scale) || num_prefix_blocks < 0 || num_prefix_blocks > max_blocks_per_seq)
+        return PA_ERR_INVALID_ARG;
+    if (dtype != PA_DTYPE_BF16) return PA_ERR_UNSUPPORTED;
+    if (partition_size != 0 &&
+        (partition_size < kBlockSize || partition_size > kMaxPartition || partition_size % kBlockSize))
+        return PA_ERR_INVALID_ARG;
+    if (num_seqs == 0) return PA_OK;
+    if (!out || !query || !key_cache || !value_cache || !block_tables || !context_lens)
+        return PA_ERR_INVALID_ARG;
+    if (!aligned16(out) || !aligned16(query) || !aligned16(key_cache) || !aligned16(value_cache))
+        return PA_ERR_INVALID_ARG;
+    const int group = num_q_heads / num_kv_heads;
+    if (head_dim != 64 && head_dim != 128) return PA_ERR_UNSUPPORTED;
+    if (group > 16) return PA_ERR_UNSUPPORTED;
+    if (num_prefix_blocks == 0)
+        return pa_decode(out, query, key_cache, value_cache, block_tables, context_lens, num_seqs,
+                         num_q_heads, num_kv_heads, head_dim, block_size, max_blocks_per_seq,
+                         num_blocks, scale, dtype, partition_size, workspace, workspace_bytes,
+                         device_status, stream);
+    const int64_t rows = (int64_t)num_blocks * num_kv_heads * kBlockSize;
+    if (rows >= ((int64_t)1 << 31)) return PA_ERR_UNSUPPORTED;
+    SharedPlan p;
+    if (!plan_shared(num_seqs, num_q_heads, num_kv_heads, max_blocks_per_seq, num_prefix_blocks,
+                     partition_size, &p))
+        return PA_ERR_INVALID_ARG;
+    const size_t need = pa_decode_shared_prefix_workspace_bytes(
+        num_seqs, num_q_heads, num_kv_heads, head_dim, max_blocks_per_seq, num_prefix_blocks,
+        partition_size);
+    if (workspace == nullptr || workspace_bytes < need || !aligned16(workspace))
+        return PA_ERR_WORKSPACE;
+    const int row_chunks = (num_seqs * group + kPrefixRows - 1) / kPrefixRows;
+    if ((int64_t)num_seqs * num_kv_heads * p.suffix_max_parts >= ((int64_t)1 << 31) ||
+        (int64_t)num_kv_heads * row_chunks * p.prefix_chunks >= ((int64_t)1 << 31))
+        return PA_ERR_UNSUPPORTED;
+
+    DecodeArgs a;
+    a.out = out;
+    a.query = query;
+    a.block_tables = block_tables;
+    a.context_lens = context_lens;
+    a.part_o = static_cast<float *>(workspace);
+    a.part_ml = reinterpret_cast<float2 *>(
+        static_cast<uint8_t *>(workspace) +
+        (((size_t)num_seqs * num_q_heads * p.max_parts * head_dim * sizeof(float) + 255) &
+         ~size_t(255)));
+    a.status = device_status;
+    a.k_scales = nullptr;
+    a.v_scales = nullptr;
+    a.num_seqs = num_seqs;
+    a.num_q_heads = num_q_heads;
+    a.num_kv_heads = num_kv_heads;
+    a.max_blocks = max_blocks_per_seq;
+    a.num_blocks = num_blocks;
+    a.part_blocks = p.suffix_part_blocks;
+    a.max_parts = p.max_parts;
+    a.scale_log2 = scale * kLog2e;
+    a.token_offset = num_prefix_blocks * kBlockSize;
+    a.part_base = p.prefix_chunks;
+    a.always_partial = 1;
+    a.prefix_blocks = num_prefix_blocks;
+    a.prefix_chunk_blocks = p.prefix_chunk_blocks;
+    a.prefix_chunks = p.prefix_chunks;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    std::lock_guard<std::mutex> lock(g_side_mutex);
+    SideStream *side = nullptr;
+    pa_status ss = side_stream_locked(&side);
+    if (ss != PA_OK) return ss;
+    cudaError_t fe = cudaEventRecord(side->fork, st);
+    if (fe == cudaSuccess) fe = cudaStreamWaitEvent(side->stream, side->fork, 0);
+    if (fe != cudaSuccess) return cuda_failure(fe, "side stream fork");
+
+    // 1. the shared prefix, once per KV head for 64 query rows at a time, on the
+    //    side stream
+    {
+        CUtensorMap kmap, vmap;
+        if (!encode_pool_map(&kmap, key_cache, rows, head_dim, 2) ||
+            !encode_pool_map(&vmap, value_cache, rows, head_dim, 2))
+            return cuda_failure(cudaErrorInvalidValue, "cuTensorMapEncodeTiled");
+        const size_t smem = 1024 + (size_t)kPrefixStages * 2 * 16 * head_dim * 2 +
+                            2 * kPrefixStages * sizeof(uint64_t) +
+                            (size_t)p.prefix_chunk_blocks * sizeof(int32_t) + 16;
+        const unsigned grid = (unsigned)((int64_t)num_kv_heads * row_chunks * p.prefix_chunks);
+        cudaError_t e;
+        if (head_dim == 128) {
+            auto kernel = pa_prefix_kernel<128, kPrefixStages>;
+            e = allow_smem(kernel, smem);
+            if (e == cudaSuccess)
+                e = launch_chained(kernel, dim3(grid), dim3((kPrefixWarps + 1) * 32), smem,
+                                   side->stream, kmap, vmap, a);
+        } else {
+            auto kernel = pa_prefix_kernel<64, kPrefixStages>;
+            e = allow_smem(kernel, smem);
+            if (e == cudaSuccess)
+                e = launch_chained(kernel, dim3(grid), dim3((kPrefixWarps + 1) * 32), smem,
+                                   side->stream, kmap, vmap, a);
+        }
+        if (e == cudaSuccess) e = cudaEventRecord(side->join, side->stream);
+        if (e != cudaSuccess) return cuda_failure(e, "pa_prefix_kernel launch");
+        count_launches(1);
+    }
+    // 2. every context past the prefix, as partials, on the caller's stream
+    pa_status s = head_dim == 64 ? dispatch_bf16<64>(group, a, key_cache, value_cache, rows, st)
+                                 : dispatch_bf16<128>(group, a, key_cache, value_cache, rows, st);
+    // join before anything else can fail, so the caller's stream always waits
+    cudaError_t je = cudaStreamWaitEvent(st, side->join, 0);
+    if (s != PA_OK) return s;
+    if (je != cudaSuccess) return cuda_failure(je, "side stream join");
+    // 3. merge prefix and suffix partials
     return launch_reduce<__nv_bfloat16>(a, head_dim, st);
 }

@@ -134,3 +134,19 @@ def test_python_binding_refuses_cpu_tensors():
     cl = torch.ones(1, dtype=torch.int32)
     with pytest.raises(ValueError):
         pkv.decode(q, kc, kc, bt, cl)
+
+
+def test_shared_prefix_blocks_helper():
+    import numpy as np
+    t = np.array([[5, 6, 7, 9], [5, 6, 7, 10], [5, 6, 8, -1]], np.int32)
+    assert pkv.shared_prefix_blocks(t) == 2
+    assert pkv.shared_prefix_blocks(t[:2]) == 3
+    assert pkv.shared_prefix_blocks(np.array([[1, -1], [1, -1]])) == 1
+
+
+def test_shared_prefix_workspace_rules(lib):
+    f = lib.pa_decode_shared_prefix_workspace_bytes
+    bad = ctypes.c_size_t(-1).value
+    assert f(128, 32, 8, 128, 129, 64, 0) > 0
+    assert f(128, 32, 8, 128, 129, 200, 0) == bad         # prefix longer than the tables
+    assert f(4, 6, 4, 128, 10, 2, 0) == bad               # heads not a multiple

@@ -1,0 +1,120 @@
+"""GPU parity: pa_decode_shared_prefix (prefix once per KV head, suffix per sequence,
+merged) against the oracle on the full tables, and against pa_decode."""
+import numpy as np
+import pytest
+
+import oracle
+import workloads as W
+from tests import helpers as H
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def pkv():
+    from paged_kv_cache_100_gb300.build import build
+    build()
+    import paged_kv_cache_100_gb300 as m
+    return m
+
+
+def _shared_workload(B, hq, hkv, D, prefix_blocks, suffix_lens, seed):
+    """Tables that all start with the same prefix_blocks blocks; context = prefix + suffix."""
+    rng = np.random.default_rng(seed)
+    lens = np.asarray([prefix_blocks * 16 + s for s in suffix_lens], np.int32)
+    own = [-(-(int(L) + 1) // 16) - prefix_blocks for L in lens]
+    own = [max(o, 0) for o in own]
+    NB = prefix_blocks + sum(own) + 3
+    perm = rng.permutation(NB).astype(np.int32)
+    width = prefix_blocks + max(own + [0])
+    tables = np.full((B, max(width, 1)), -1, np.int32)
+    tables[:, :prefix_blocks] = perm[:prefix_blocks]
+    pos = prefix_blocks
+    for b in range(B):
+        tables[b, prefix_blocks:prefix_blocks + own[b]] = perm[pos:pos + own[b]]
+        pos += own[b]
+    wl = W.Workload("shared_custom", B, hq, hkv, D, "bf16", 1.0, lens, tables, NB,
+                    np.zeros(B, np.int64), seed=seed)
+    return wl
+
+
+def _run(pkv, wl, hv, n_prefix, lens=None, status=None, partition_size=0):
+    import torch
+    q = H.host_to_device(hv.query, torch.bfloat16)
+    kc = H.host_to_device(hv.key_cache, torch.bfloat16)
+    vc = H.host_to_device(hv.value_cache, torch.bfloat16)
+    bt = torch.from_numpy(wl.block_tables).cuda()
+    cl = torch.from_numpy(np.asarray(wl.context_lens if lens is None else lens, np.int32)).cuda()
+    out = pkv.decode_shared_prefix(q, kc, vc, bt, cl, n_prefix, wl.scale, status=status,
+                                   partition_size=partition_size)
+    ref_gpu = pkv.decode(q, kc, vc, bt, cl, wl.scale)
+    torch.cuda.synchronize()
+    return out, ref_gpu
+
+
+@pytest.mark.parametrize("hq,hkv,D", [(8, 8, 128), (32, 8, 128), (16, 2, 128), (12, 4, 64),
+                                      (32, 2, 128), (4, 4, 64)])
+@pytest.mark.parametrize("prefix_blocks", [1, 7, 40])
+def test_shared_prefix_matches_oracle(pkv, hq, hkv, D, prefix_blocks):
+    suffix = [0, 1, 15, 16, 17, 200, 640, 3]
+    wl = _shared_workload(len(suffix), hq, hkv, D, prefix_blocks, suffix, seed=hq + D + prefix_blocks)
+    hv = W.host_values(wl)              # slots holding no context token are NaN
+    out, ref_gpu = _run(pkv, wl, hv, prefix_blocks)
+    ref = oracle.paged_decode(hv.query, hv.key_cache, hv.value_cache, wl.block_tables,
+                              wl.context_lens, wl.scale, threads=4)
+    H.assert_close(H.as_f64(out), ref, "bf16", f"shared prefix {hq}/{hkv}/{D} n={prefix_blocks}")
+    H.assert_close(H.as_f64(out), H.as_f64(ref_gpu), "bf16", "shared prefix vs pa_decode")
+
+
+def test_contexts_shorter_than_the_prefix_are_masked(pkv):
+    wl = _shared_workload(4, 16, 4, 128, 10, [5, 0, 30, 1], seed=9)
+    hv = W.host_values(wl, poison_unused=False)
+    lens = wl.context_lens.copy()
+    lens[1] = 37            # ends inside the prefix
+    lens[3] = 0             # empty
+    out, _ = _run(pkv, wl, hv, 10, lens=lens, partition_size=64)
+    ref = oracle.paged_decode(hv.query, hv.key_cache, hv.value_cache, wl.block_tables, lens,
+                              wl.scale)
+    got = H.as_f64(out)
+    assert np.all(got[3] == 0)
+    H.assert_close(got, ref, "bf16", "short contexts")
+
+
+def test_prefix_mismatch_is_flagged(pkv):
+    import torch
+    wl = _shared_workload(4, 8, 8, 128, 6, [10, 20, 30, 40], seed=4)
+    hv = W.host_values(wl, poison_unused=False)
+    wl.block_tables[2, 3] = wl.block_tables[2, 6]    # row 2 leaves the shared prefix
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    _run(pkv, wl, hv, 6, status=status)
+    assert int(status.item()) & pkv._lib.PA_DEV_PREFIX_MISMATCH
+
+
+@pytest.mark.parametrize("cow", [False, True])
+def test_shared_prefix_workload_full_size(pkv, cow):
+    """The 128-sequence mix: before copy-on-write all 64 prefix blocks are shared;
+    after it the first 16 sequences own block 63, so 63 blocks are shared."""
+    import torch
+    wl = W.make_workload("shared_prefix")
+    if not cow:
+        wl.block_tables[:wl.cow_pairs.shape[0], 63] = wl.cow_pairs[0, 0]
+    n_prefix = pkv.shared_prefix_blocks(wl.block_tables)
+    assert n_prefix == (63 if cow else 64)
+    q, kc, vc, kn, vn = W.device_values(wl, "cuda")
+    if cow:
+        pkv.block_copy(kc, vc, torch.from_numpy(wl.cow_pairs).cuda())
+    bt = torch.from_numpy(wl.block_tables).cuda()
+    lens = wl.step_context_lens
+    cl = torch.from_numpy(lens).cuda()
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    out = pkv.decode_shared_prefix(q, kc, vc, bt, cl, n_prefix, wl.scale, status=status)
+    plain = pkv.decode(q, kc, vc, bt, cl, wl.scale)
+    torch.cuda.synchronize()
+    assert int(status.item()) == 0
+    H.assert_close(H.as_f64(out), H.as_f64(plain), "bf16", "cascade vs plain decode")
+    seqs, pairs = H.sample_pairs(wl, lens, n_seqs=5, heads_per_seq=4, seed=4)
+    kch, vch, tabs, slens = H.compact_for_sequences(wl, seqs, kc, vc, lens)
+    qh = H.device_to_host_bits(q[torch.as_tensor(seqs, device="cuda")])
+    ref = oracle.paged_decode(qh, kch, vch, tabs, slens, wl.scale, sel=pairs, threads=8)
+    got = np.stack([H.as_f64(out[seqs[i], h]) for i, h in pairs])
+    H.assert_close(got, ref, "bf16", "shared-prefix workload")
