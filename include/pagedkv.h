@@ -316,6 +316,23 @@ pa_status pa_bm_make_private(pa_bm *bm, int seq, int logical_block, int32_t *cow
                              int32_t *cow_dst);
 pa_status pa_bm_free_seq(pa_bm *bm, int seq);
 int pa_bm_num_free(const pa_bm *bm);
+/* Released blocks kept for the prefix cache (handed out once the free list is empty). */
+int pa_bm_num_evictable(const pa_bm *bm);
+/* Prefix caching ("PagedAttention por dentro", section "Prefix caching
+ * cross-session"; "Cómo funciona realmente vLLM", section "Automatic Prefix
+ * Caching").  A full block whose K/V are written can be indexed by
+ *   key_j = FNV1a64(le64(key_{j-1}) || le32(tokens of block j)), key_{-1} = 0
+ * (a hash of its content and of everything before it).  A new sequence that
+ * begins with the same tokens reuses the indexed blocks (reference counts + 1;
+ * a lookup also compares the block's own tokens) and only the rest is newly
+ * allocated; *num_cached_tokens receives the number of leading tokens whose
+ * K/V are already in the pool (a multiple of block_size).  All or nothing. */
+pa_status pa_bm_alloc_seq_cached(pa_bm *bm, int seq, const int32_t *tokens, int num_tokens,
+                                 int *num_cached_tokens);
+/* Index seq's full blocks (over its first num_tokens tokens) once their K/V are
+ * written; returns how many blocks were newly indexed, -1 for an unknown seq.
+ * A key already indexed keeps its block; a block is indexed once. */
+int pa_bm_register_prefix(pa_bm *bm, int seq, const int32_t *tokens, int num_tokens);
 int pa_bm_num_tokens(const pa_bm *bm, int seq);       /* -1 if unknown */
 int pa_bm_ref_count(const pa_bm *bm, int block);      /* -1 if out of range */
 /* Copies up to cap entries of seq's table to out; returns its length, -1 if unknown. */

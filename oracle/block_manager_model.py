@@ -19,8 +19,50 @@ as well): the free list is a stack that initially pops 0, 1, 2, ...; a freed
 block is pushed back and is the next one handed out.  ``free_seq`` releases a
 table from its last entry to its first, so the first block of the freed table
 is reused first.
+
+Prefix caching ("PagedAttention por dentro", section "Prefix caching
+cross-session"; "Cómo funciona realmente vLLM", section "Automatic Prefix
+Caching": finished requests' blocks are indexed by a hash of their content and
+reused by a new request that begins the same way).  Reading: a full block's
+K/V depend on every token up to it, so its key chains over the whole prefix:
+    key_j = FNV1a64(le64(key_{j-1}) || le32(tokens[16j .. 16j+15])), key_{-1} = 0
+(FNV-1a, 64 bits: offset basis 0xcbf29ce484222325, prime 0x100000001b3).
+A lookup matches a cached block only if its key and its own 16 tokens agree.
+Released blocks that carry a key wait in an evictable list (least recently
+released first) and are reused only when the free list is empty; taking one
+drops its key.
 """
 from __future__ import annotations
+
+FNV_OFFSET = 0xCBF29CE484222325
+FNV_PRIME = 0x100000001B3
+MASK64 = (1 << 64) - 1
+
+
+def fnv1a64(data: bytes) -> int:
+    """64-bit FNV-1a of a byte string."""
+    h = FNV_OFFSET
+    for byte in data:
+        h ^= byte
+        h = (h * FNV_PRIME) & MASK64
+    return h
+
+
+def block_key(parent_key: int, tokens) -> int:
+    """Key of a full block given its parent's key (0 for the first block)."""
+    data = int(parent_key & MASK64).to_bytes(8, "little")
+    for t in tokens:
+        data += int(t & 0xFFFFFFFF).to_bytes(4, "little")
+    return fnv1a64(data)
+
+
+def block_keys(tokens, block_size: int = 16):
+    """Keys of the full blocks of a token sequence."""
+    keys, parent = [], 0
+    for j in range(len(tokens) // block_size):
+        parent = block_key(parent, tokens[j * block_size:(j + 1) * block_size])
+        keys.append(parent)
+    return keys
 
 
 class NoBlocks(Exception):
@@ -37,6 +79,11 @@ class BlockManagerModel:
         self.ref = [0] * num_blocks
         self.tables: dict[int, list[int]] = {}
         self.tokens: dict[int, int] = {}
+        # prefix cache
+        self.cached: dict[int, int] = {}          # key -> block
+        self.block_key: dict[int, int] = {}       # block -> key
+        self.block_tokens: dict[int, tuple] = {}  # block -> its 16 tokens
+        self.evictable: list[int] = []            # released keyed blocks, oldest first
 
     # -- queries ---------------------------------------------------------
     def num_free(self) -> int:
@@ -55,20 +102,84 @@ class BlockManagerModel:
         return -(-num_tokens // self.block_size)
 
     # -- mutations -------------------------------------------------------
+    def num_evictable(self) -> int:
+        return len(self.evictable)
+
     def _take(self) -> int:
-        if not self.free:
+        if self.free:
+            b = self.free.pop()
+        elif self.evictable:
+            b = self.evictable.pop(0)
+            key = self.block_key.pop(b)
+            del self.cached[key]
+            del self.block_tokens[b]
+        else:
             raise NoBlocks()
-        b = self.free.pop()
         assert self.ref[b] == 0
         self.ref[b] = 1
         return b
+
+    def _release(self, b: int) -> None:
+        self.ref[b] -= 1
+        assert self.ref[b] >= 0
+        if self.ref[b] == 0:
+            if b in self.block_key:
+                self.evictable.append(b)
+            else:
+                self.free.append(b)
+
+    def alloc_seq_cached(self, seq: int, tokens) -> int:
+        """New sequence holding ``tokens``: its leading full blocks are taken from the
+        prefix cache where they match; returns how many tokens were found cached."""
+        if seq in self.tables:
+            raise ValueError("sequence exists")
+        n = len(tokens)
+        hits = []
+        parent = 0
+        for j in range(n // self.block_size):
+            own = tuple(int(t) for t in tokens[j * self.block_size:(j + 1) * self.block_size])
+            parent = block_key(parent, own)
+            b = self.cached.get(parent)
+            if b is None or self.block_tokens[b] != own:
+                break
+            hits.append(b)
+        need = self.blocks_needed(n) - len(hits)
+        reusable = sum(1 for b in hits if self.ref[b] == 0)
+        if need > len(self.free) + len(self.evictable) - reusable:
+            raise NoBlocks()
+        for b in hits:
+            if self.ref[b] == 0:
+                self.evictable.remove(b)
+            self.ref[b] += 1
+        table = list(hits) + [self._take() for _ in range(need)]
+        self.tables[seq] = table
+        self.tokens[seq] = n
+        return len(hits) * self.block_size
+
+    def register_prefix(self, seq: int, tokens) -> int:
+        """Index the sequence's full blocks by key (their K/V are now written);
+        returns how many blocks were newly indexed."""
+        table = self.tables[seq]
+        n = min(len(tokens), self.tokens[seq])
+        added, parent = 0, 0
+        for j in range(n // self.block_size):
+            own = tuple(int(t) for t in tokens[j * self.block_size:(j + 1) * self.block_size])
+            parent = block_key(parent, own)
+            b = table[j]
+            if parent in self.cached or b in self.block_key:
+                continue
+            self.cached[parent] = b
+            self.block_key[b] = parent
+            self.block_tokens[b] = own
+            added += 1
+        return added
 
     def alloc_seq(self, seq: int, num_tokens: int) -> list[int]:
         """Give a new sequence room for ``num_tokens`` tokens (all or nothing)."""
         if seq in self.tables or num_tokens < 0:
             raise ValueError("sequence exists or bad length")
         need = self.blocks_needed(num_tokens)
-        if need > len(self.free):
+        if need > len(self.free) + len(self.evictable):
             raise NoBlocks()
         self.tables[seq] = [self._take() for _ in range(need)]
         self.tokens[seq] = num_tokens
@@ -90,7 +201,7 @@ class BlockManagerModel:
         if self.ref[old] <= 1:
             return None
         new = self._take()
-        self.ref[old] -= 1
+        self.ref[old] -= 1        # still held by another sequence: stays > 0
         table[logical_block] = new
         return (old, new)
 
@@ -111,10 +222,7 @@ class BlockManagerModel:
         table = self.tables.pop(seq)
         del self.tokens[seq]
         for b in reversed(table):
-            self.ref[b] -= 1
-            assert self.ref[b] >= 0
-            if self.ref[b] == 0:
-                self.free.append(b)
+            self._release(b)
 
     # -- invariants ------------------------------------------------------
     def check(self) -> None:
@@ -125,6 +233,11 @@ class BlockManagerModel:
                 counted[b] += 1
         assert counted == self.ref
         free = set(self.free)
-        assert len(free) == len(self.free)
+        ev = set(self.evictable)
+        assert len(free) == len(self.free) and len(ev) == len(self.evictable)
+        assert not (free & ev)
         for b in range(self.num_blocks):
-            assert (b in free) == (self.ref[b] == 0)
+            assert (b in free or b in ev) == (self.ref[b] == 0)
+            assert (b in ev) <= (b in self.block_key)
+        for key, b in self.cached.items():
+            assert self.block_key[b] == key

@@ -334,6 +334,27 @@ class BlockManager:
     def num_free(self) -> int:
         return int(lib().pa_bm_num_free(self._h))
 
+    def num_evictable(self) -> int:
+        return int(lib().pa_bm_num_evictable(self._h))
+
+    def alloc_seq_cached(self, seq: int, tokens) -> int:
+        """New sequence reusing the prefix cache; returns the number of cached tokens."""
+        import numpy as np
+        t = np.ascontiguousarray(tokens, dtype=np.int32)
+        n = ctypes.c_int()
+        check(lib().pa_bm_alloc_seq_cached(self._h, seq, t.ctypes.data, t.shape[0],
+                                           ctypes.byref(n)), "pa_bm_alloc_seq_cached")
+        return int(n.value)
+
+    def register_prefix(self, seq: int, tokens) -> int:
+        """Index the sequence's full blocks in the prefix cache; returns how many."""
+        import numpy as np
+        t = np.ascontiguousarray(tokens, dtype=np.int32)
+        n = lib().pa_bm_register_prefix(self._h, seq, t.ctypes.data, t.shape[0])
+        if n < 0:
+            raise KeyError(seq)
+        return int(n)
+
     def num_tokens(self, seq: int) -> int:
         n = lib().pa_bm_num_tokens(self._h, seq)
         if n < 0:

@@ -54,6 +54,9 @@ SIGNATURES = {
     "pa_bm_make_private": (i32, [vp, i32, i32, ptr_i32, ptr_i32]),
     "pa_bm_free_seq": (i32, [vp, i32]),
     "pa_bm_num_free": (i32, [vp]),
+    "pa_bm_num_evictable": (i32, [vp]),
+    "pa_bm_alloc_seq_cached": (i32, [vp, i32, vp, i32, ptr_int]),
+    "pa_bm_register_prefix": (i32, [vp, i32, vp, i32]),
     "pa_bm_num_tokens": (i32, [vp, i32]),
     "pa_bm_ref_count": (i32, [vp, i32]),
     "pa_bm_table": (i32, [vp, i32, vp, i32]),

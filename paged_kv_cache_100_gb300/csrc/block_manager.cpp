@@ -16,12 +16,50 @@
 // 0, 1, 2, ... first, a freed block is the next one handed out, and a table
 // is released from its last entry to its first.  Every failing operation
 // leaves the manager unchanged.
+//
+// Prefix caching ("PagedAttention por dentro", section "Prefix caching
+// cross-session"; "Cómo funciona realmente vLLM", section "Automatic Prefix
+// Caching"): full blocks whose K/V are written can be indexed by a key that
+// hashes their content and everything before it,
+//     key_j = FNV1a64(le64(key_{j-1}) || le32(tokens of block j)), key_{-1} = 0,
+// and a new sequence that begins with the same tokens reuses them.  A lookup
+// also compares the block's own tokens.  Released blocks that carry a key wait
+// in an evictable list (oldest release first) and are handed out only when the
+// free list is empty, losing their key then.
 #include <cstdint>
+#include <list>
 #include <new>
 #include <unordered_map>
 #include <vector>
 
 #include "pagedkv.h"
+
+namespace {
+
+constexpr uint64_t kFnvOffset = 0xcbf29ce484222325ull;
+constexpr uint64_t kFnvPrime = 0x100000001b3ull;
+
+uint64_t fnv1a_bytes(uint64_t h, const uint8_t *p, size_t n) {
+    for (size_t i = 0; i < n; ++i) {
+        h ^= p[i];
+        h *= kFnvPrime;
+    }
+    return h;
+}
+
+uint64_t block_key(uint64_t parent, const int32_t *tokens, int block_size) {
+    uint8_t buf[8];
+    for (int i = 0; i < 8; ++i) buf[i] = (uint8_t)(parent >> (8 * i));
+    uint64_t h = fnv1a_bytes(kFnvOffset, buf, 8);
+    for (int t = 0; t < block_size; ++t) {
+        const uint32_t v = (uint32_t)tokens[t];
+        uint8_t b4[4] = {(uint8_t)v, (uint8_t)(v >> 8), (uint8_t)(v >> 16), (uint8_t)(v >> 24)};
+        h = fnv1a_bytes(h, b4, 4);
+    }
+    return h;
+}
+
+}  // namespace
 
 struct pa_bm {
     int num_blocks;
@@ -33,12 +71,43 @@ struct pa_bm {
         int64_t tokens = 0;
     };
     std::unordered_map<int, Seq> seqs;
+    // prefix cache
+    std::unordered_map<uint64_t, int32_t> cached;       // key -> block
+    std::vector<uint8_t> has_key;
+    std::vector<uint64_t> key_of;
+    std::vector<std::vector<int32_t>> tokens_of;       // a keyed block's own tokens
+    std::list<int32_t> evictable;                       // front = oldest release
+    std::vector<std::list<int32_t>::iterator> ev_pos;
+    std::vector<uint8_t> in_ev;
+
+    size_t available() const { return free_stack.size() + evictable.size(); }
 
     int32_t take() {
-        const int32_t b = free_stack.back();
-        free_stack.pop_back();
+        int32_t b;
+        if (!free_stack.empty()) {
+            b = free_stack.back();
+            free_stack.pop_back();
+        } else {
+            b = evictable.front();
+            evictable.pop_front();
+            in_ev[b] = 0;
+            cached.erase(key_of[b]);
+            has_key[b] = 0;
+            tokens_of[b].clear();
+        }
         ref[b] = 1;
         return b;
+    }
+    void release(int32_t b) {
+        ref[b] -= 1;
+        if (ref[b] == 0) {
+            if (has_key[b]) {
+                ev_pos[b] = evictable.insert(evictable.end(), b);
+                in_ev[b] = 1;
+            } else {
+                free_stack.push_back(b);
+            }
+        }
     }
     int64_t blocks_for(int64_t tokens) const { return (tokens + block_size - 1) / block_size; }
 };
@@ -50,6 +119,11 @@ extern "C" pa_bm *pa_bm_create(int num_blocks, int block_size) {
     bm->num_blocks = num_blocks;
     bm->block_size = block_size;
     bm->ref.assign((size_t)num_blocks, 0);
+    bm->has_key.assign((size_t)num_blocks, 0);
+    bm->key_of.assign((size_t)num_blocks, 0);
+    bm->tokens_of.resize((size_t)num_blocks);
+    bm->ev_pos.resize((size_t)num_blocks);
+    bm->in_ev.assign((size_t)num_blocks, 0);
     bm->free_stack.reserve((size_t)num_blocks);
     for (int b = num_blocks - 1; b >= 0; --b) bm->free_stack.push_back(b);
     return bm;
@@ -61,7 +135,7 @@ extern "C" pa_status pa_bm_alloc_seq(pa_bm *bm, int seq, int num_tokens) {
     if (bm == nullptr || num_tokens < 0) return PA_ERR_INVALID_ARG;
     if (bm->seqs.count(seq)) return PA_ERR_NOT_FOUND;
     const int64_t need = bm->blocks_for(num_tokens);
-    if (need > (int64_t)bm->free_stack.size()) return PA_ERR_NO_BLOCKS;
+    if (need > (int64_t)bm->available()) return PA_ERR_NO_BLOCKS;
     pa_bm::Seq s;
     s.tokens = num_tokens;
     s.table.reserve((size_t)need);
@@ -87,7 +161,7 @@ static pa_status make_private(pa_bm *bm, pa_bm::Seq &s, int logical, int32_t *sr
         *dst = -1;
         return PA_OK;
     }
-    if (bm->free_stack.empty()) return PA_ERR_NO_BLOCKS;
+    if (bm->available() == 0) return PA_ERR_NO_BLOCKS;
     const int32_t fresh = bm->take();
     bm->ref[old] -= 1;
     s.table[(size_t)logical] = fresh;
@@ -116,7 +190,7 @@ extern "C" pa_status pa_bm_append_slot(pa_bm *bm, int seq, int64_t *slot, int32_
     const int64_t n = s.tokens;
     int32_t src = -1, dst = -1;
     if (n % bm->block_size == 0) {
-        if (bm->free_stack.empty()) return PA_ERR_NO_BLOCKS;
+        if (bm->available() == 0) return PA_ERR_NO_BLOCKS;
         s.table.push_back(bm->take());
     } else {
         pa_status st = make_private(bm, s, (int)s.table.size() - 1, &src, &dst);
@@ -134,13 +208,76 @@ extern "C" pa_status pa_bm_free_seq(pa_bm *bm, int seq) {
     auto it = bm->seqs.find(seq);
     if (it == bm->seqs.end()) return PA_ERR_NOT_FOUND;
     const std::vector<int32_t> &t = it->second.table;
-    for (size_t i = t.size(); i-- > 0;) {
-        const int32_t b = t[i];
-        bm->ref[b] -= 1;
-        if (bm->ref[b] == 0) bm->free_stack.push_back(b);
-    }
+    for (size_t i = t.size(); i-- > 0;) bm->release(t[i]);
     bm->seqs.erase(it);
     return PA_OK;
+}
+
+extern "C" int pa_bm_num_evictable(const pa_bm *bm) {
+    return bm == nullptr ? -1 : (int)bm->evictable.size();
+}
+
+extern "C" pa_status pa_bm_alloc_seq_cached(pa_bm *bm, int seq, const int32_t *tokens,
+                                            int num_tokens, int *num_cached_tokens) {
+    if (bm == nullptr || num_tokens < 0 || num_cached_tokens == nullptr ||
+        (num_tokens > 0 && tokens == nullptr))
+        return PA_ERR_INVALID_ARG;
+    if (bm->seqs.count(seq)) return PA_ERR_NOT_FOUND;
+    std::vector<int32_t> hits;
+    uint64_t parent = 0;
+    const int bs = bm->block_size;
+    for (int j = 0; j < num_tokens / bs; ++j) {
+        const int32_t *own = tokens + (size_t)j * bs;
+        parent = block_key(parent, own, bs);
+        auto f = bm->cached.find(parent);
+        if (f == bm->cached.end()) break;
+        const std::vector<int32_t> &stored = bm->tokens_of[f->second];
+        bool same = true;
+        for (int k = 0; k < bs && same; ++k) same = stored[k] == own[k];
+        if (!same) break;
+        hits.push_back(f->second);
+    }
+    const int64_t need = bm->blocks_for(num_tokens) - (int64_t)hits.size();
+    int64_t reusable = 0;
+    for (int32_t b : hits) reusable += bm->ref[b] == 0 ? 1 : 0;
+    if (need > (int64_t)bm->available() - reusable) return PA_ERR_NO_BLOCKS;
+    for (int32_t b : hits) {
+        if (bm->ref[b] == 0) {
+            bm->evictable.erase(bm->ev_pos[b]);
+            bm->in_ev[b] = 0;
+        }
+        bm->ref[b] += 1;
+    }
+    pa_bm::Seq s;
+    s.tokens = num_tokens;
+    s.table = hits;
+    for (int64_t i = 0; i < need; ++i) s.table.push_back(bm->take());
+    bm->seqs.emplace(seq, std::move(s));
+    *num_cached_tokens = (int)hits.size() * bs;
+    return PA_OK;
+}
+
+extern "C" int pa_bm_register_prefix(pa_bm *bm, int seq, const int32_t *tokens, int num_tokens) {
+    if (bm == nullptr || num_tokens < 0 || (num_tokens > 0 && tokens == nullptr)) return -1;
+    auto it = bm->seqs.find(seq);
+    if (it == bm->seqs.end()) return -1;
+    const std::vector<int32_t> &table = it->second.table;
+    const int bs = bm->block_size;
+    const int64_t n = num_tokens < it->second.tokens ? num_tokens : it->second.tokens;
+    int added = 0;
+    uint64_t parent = 0;
+    for (int64_t j = 0; j < n / bs; ++j) {
+        const int32_t *own = tokens + (size_t)j * bs;
+        parent = block_key(parent, own, bs);
+        const int32_t b = table[(size_t)j];
+        if (bm->cached.count(parent) || bm->has_key[b]) continue;
+        bm->cached.emplace(parent, b);
+        bm->has_key[b] = 1;
+        bm->key_of[b] = parent;
+        bm->tokens_of[b].assign(own, own + bs);
+        ++added;
+    }
+    return added;
 }
 
 extern "C" int pa_bm_num_free(const pa_bm *bm) {
