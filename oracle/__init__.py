@@ -59,7 +59,8 @@ def _load():
                                              i32, i32, i32, dbl, vp, i32, i32]
             lib.pao_paged_decode.restype = i32
             lib.pao_paged_decode_ex.argtypes = [vp, vp, i32, vp, vp, i32, vp, vp, vp, vp, i32,
-                                                i32, i32, i32, i32, i32, i32, dbl, vp, i32, i32]
+                                                i32, i32, i32, i32, i32, i32, dbl, vp, i32, i32,
+                                                i32]
             lib.pao_paged_decode_ex.restype = i32
             lib.pao_cache_write_fp8.argtypes = [vp, vp, vp, vp, vp, i32, i32, i32, i32, i32, vp,
                                                 vp]
@@ -98,14 +99,16 @@ def max_threads() -> int:
 
 
 def paged_decode(query, key_cache, value_cache, block_tables, context_lens, scale,
-                 sel=None, threads: int = 1, k_scales=None, v_scales=None) -> np.ndarray:
+                 sel=None, threads: int = 1, k_scales=None, v_scales=None,
+                 window: int = 0) -> np.ndarray:
     """fp64 paged decode attention.
 
     query [B][Hq][D] (float32 or bfloat16 bits); key_cache/value_cache
     [NB][Hkv][BS][D] of the same type, or E4M3 codes (uint8) with per-KV-head
     ``k_scales`` / ``v_scales``; block_tables int32 [B][max_blocks]; context_lens
-    int32 [B].  Returns float64 [B][Hq][D], or [n][D] for the (b, h) pairs of
-    ``sel`` (an int array of shape [n, 2]).
+    int32 [B].  ``window`` > 0 attends only to the last ``window`` tokens.
+    Returns float64 [B][Hq][D], or [n][D] for the (b, h) pairs of ``sel`` (an
+    int array of shape [n, 2]).
     """
     lib = _load()
     query = np.ascontiguousarray(query)
@@ -146,7 +149,7 @@ def paged_decode(query, key_cache, value_cache, block_tables, context_lens, scal
                                  block_tables.ctypes.data, context_lens.ctypes.data, B, Hq, Hkv,
                                  D, BS, block_tables.shape[1], NB, float(scale),
                                  None if sel_arr is None else sel_arr.ctypes.data, n_sel,
-                                 int(threads))
+                                 int(threads), int(window))
     if rc != 0:
         raise ValueError(f"oracle paged_decode failed with code {rc}")
     return out

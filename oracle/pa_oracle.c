@@ -23,6 +23,8 @@
  *    of its block (cache write).
  *  - same page, "Copy-on-write para sampling paralelo": on divergence only the
  *    last shared block is copied (block copy).
+ *  - "PagedAttention por dentro", "Sliding window attention": a model with a
+ *    window of W tokens attends only to the last W tokens of its context.
  *  - "KV cache: la memoria de trabajo que sostiene la inferencia LLM", "Trucos para que el cuaderno sea más fino":
  *    under GQA query heads share K/V in groups; query head h reads KV head
  *    floor(h / (Hq / Hkv)).
@@ -138,7 +140,7 @@ static int attend_one(double *out, const void *query, int q_dtype, const void *k
                       const float *v_scales, const int32_t *block_tables,
                       const int32_t *context_lens, int b, int h, int num_q_heads,
                       int num_kv_heads, int head_dim, int block_size, int max_blocks,
-                      int num_blocks, double scale)
+                      int num_blocks, double scale, int window)
 {
     const int group = num_q_heads / num_kv_heads;
     const int kvh = h / group;
@@ -151,6 +153,8 @@ static int attend_one(double *out, const void *query, int q_dtype, const void *k
         return PAO_OK;
     if (L < 0 || (int64_t)L > (int64_t)max_blocks * block_size)
         return PAO_ERR_INDEX;
+    /* With a window of W tokens only positions [L - W, L) take part. */
+    const int first = (window > 0 && L > window) ? L - window : 0;
 
     double *score = (double *)malloc(sizeof(double) * (size_t)L);
     int64_t *row = (int64_t *)malloc(sizeof(int64_t) * (size_t)L);
@@ -161,7 +165,7 @@ static int attend_one(double *out, const void *query, int q_dtype, const void *k
     }
 
     /* Gather: logical token t -> (physical block, offset inside it). */
-    for (t = 0; t < L; ++t) {
+    for (t = first; t < L; ++t) {
         int logical_block = t / block_size;
         int offset = t % block_size;
         int32_t phys = block_tables[(int64_t)b * max_blocks + logical_block];
@@ -179,7 +183,7 @@ static int attend_one(double *out, const void *query, int q_dtype, const void *k
 
     /* Scores s_t = scale * <q, k_t>. */
     const int64_t qbase = ((int64_t)b * num_q_heads + h) * head_dim;
-    for (t = 0; t < L; ++t) {
+    for (t = first; t < L; ++t) {
         double dot = 0.0;
         for (d = 0; d < head_dim; ++d)
             dot += widen(query, qbase + d, q_dtype) * (widen(key_cache, row[t] + d, kv_dtype) * ks);
@@ -187,16 +191,16 @@ static int attend_one(double *out, const void *query, int q_dtype, const void *k
     }
 
     /* Softmax: subtract the maximum, exponentiate, normalise. */
-    double mx = score[0];
-    for (t = 1; t < L; ++t)
+    double mx = score[first];
+    for (t = first + 1; t < L; ++t)
         if (score[t] > mx)
             mx = score[t];
     double denom = 0.0;
-    for (t = 0; t < L; ++t)
+    for (t = first; t < L; ++t)
         denom += exp(score[t] - mx);
 
     /* Output: the softmax-weighted sum of the value rows. */
-    for (t = 0; t < L; ++t) {
+    for (t = first; t < L; ++t) {
         double w = exp(score[t] - mx) / denom;
         for (d = 0; d < head_dim; ++d)
             out[d] += w * (widen(value_cache, row[t] + d, kv_dtype) * vs);
@@ -214,6 +218,7 @@ static int attend_one(double *out, const void *query, int q_dtype, const void *k
  *         (sel holds 2 * n_sel int32 values: b0, h0, b1, h1, ...).
  *   q_dtype, kv_dtype : element types of the query and of the pools; for
  *         FP8 pools k_scales / v_scales hold one scale per KV head (NULL = 1).
+ *   window : 0 = the whole context; W > 0 = only the last W tokens.
  *   num_threads : OpenMP threads over (b, h) pairs; 1 = serial.
  * Returns 0, or a nonzero code for bad arguments or an out-of-range table
  * entry (the oracle never reads outside the pools).
@@ -224,7 +229,7 @@ int pao_paged_decode_ex(double *out, const void *query, int q_dtype, const void 
                         const int32_t *context_lens, int num_seqs, int num_q_heads,
                         int num_kv_heads, int head_dim, int block_size, int max_blocks,
                         int num_blocks, double scale, const int32_t *sel, int n_sel,
-                        int num_threads)
+                        int num_threads, int window)
 {
     if (!out || !query || !key_cache || !value_cache || !block_tables || !context_lens)
         return PAO_ERR_ARG;
@@ -258,7 +263,8 @@ int pao_paged_decode_ex(double *out, const void *query, int q_dtype, const void 
         else
             rc = attend_one(out + i * head_dim, query, q_dtype, key_cache, value_cache, kv_dtype,
                             k_scales, v_scales, block_tables, context_lens, b, h, num_q_heads,
-                            num_kv_heads, head_dim, block_size, max_blocks, num_blocks, scale);
+                            num_kv_heads, head_dim, block_size, max_blocks, num_blocks, scale,
+                            window);
         if (rc != PAO_OK) {
 #ifdef _OPENMP
 #pragma omp critical
@@ -283,7 +289,7 @@ int pao_paged_decode(double *out, const void *query, const void *key_cache,
     return pao_paged_decode_ex(out, query, dtype, key_cache, value_cache, dtype, NULL, NULL,
                                block_tables, context_lens, num_seqs, num_q_heads, num_kv_heads,
                                head_dim, block_size, max_blocks, num_blocks, scale, sel, n_sel,
-                               num_threads);
+                               num_threads, 0);
 }
 
 /*

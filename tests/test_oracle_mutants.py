@@ -38,12 +38,15 @@ MUTANTS = {
     "fp8_k_scale_ignored": ("const double ks = k_scales ? (double)k_scales[kvh] : 1.0;",
                             "const double ks = 1.0;"),
     "fp8_write_multiplies": ("float kq = kx / k_scales[kvh];", "float kq = kx * k_scales[kvh];"),
+    "window_off_by_one": ("const int first = (window > 0 && L > window) ? L - window : 0;",
+                          "const int first = (window > 0 && L > window) ? L - window + 1 : 0;"),
     "copy_skips_v": ("memmove((char *)value_cache + dst * block_bytes,", "(void)(value_cache + dst * block_bytes,"),
 }
 
 from tests import test_oracle_fp8_pins as fp8pins  # noqa: E402
 
 PIN_FUNCS = [
+    lambda g: pins.test_window_matches_library_attention_on_the_last_tokens(17),
     lambda g: fp8pins.test_every_code_value_matches_torch(),
     lambda g: fp8pins.test_encode_matches_torch_below_overflow(),
     lambda g: fp8pins.test_encode_saturates_and_keeps_nan(),

@@ -315,3 +315,42 @@ def test_block_copy_applies_pairs_in_order():
     vc = -kc
     oracle.block_copy(kc, vc, [[0, 1], [1, 2]])              # chained: 2 gets the new 1 == 0
     assert np.array_equal(kc[2], kc[0]) and np.array_equal(vc[2], vc[0])
+
+
+# ---------------------------------------------------------------------------
+# sliding window ("PagedAttention por dentro", "Sliding window attention")
+# ---------------------------------------------------------------------------
+@pytest.mark.parametrize("window", [1, 5, 16, 17, 64])
+def test_window_matches_library_attention_on_the_last_tokens(window):
+    rng = np.random.default_rng(50 + window)
+    lens = [3, 16, 40, 130]
+    q, ck, cv, kc, vc, tables, L = _random_paged(rng, 4, 8, 2, 64, lens)
+    got = oracle.paged_decode(q, kc, vc, tables, L, 0.2, window=window)
+    for b, n in enumerate(lens):
+        lo = max(0, n - window)
+        want = _sdpa(q[b], ck[b][:, lo:], cv[b][:, lo:], 0.2, 4)
+        np.testing.assert_allclose(got[b], want, rtol=1e-11, atol=1e-12)
+
+
+def test_window_of_one_returns_the_last_value_and_wide_windows_change_nothing():
+    rng = np.random.default_rng(60)
+    lens = [7, 33]
+    q, ck, cv, kc, vc, tables, L = _random_paged(rng, 2, 4, 4, 32, lens)
+    one = oracle.paged_decode(q, kc, vc, tables, L, 0.5, window=1)
+    for b, n in enumerate(lens):
+        assert np.array_equal(one[b], cv[b][:, n - 1, :].astype(np.float64))
+    full = oracle.paged_decode(q, kc, vc, tables, L, 0.5)
+    assert np.array_equal(oracle.paged_decode(q, kc, vc, tables, L, 0.5, window=33), full)
+    assert np.array_equal(oracle.paged_decode(q, kc, vc, tables, L, 0.5, window=1000), full)
+
+
+def test_window_never_reads_released_blocks():
+    """Blocks wholly before the window may be gone (table entry -1)."""
+    rng = np.random.default_rng(61)
+    lens = [100]
+    q, ck, cv, kc, vc, tables, L = _random_paged(rng, 1, 2, 2, 16, lens)
+    want = oracle.paged_decode(q, kc, vc, tables, L, 0.3, window=40)
+    t2 = tables.copy()
+    t2[0, :3] = -1                       # positions 0..47 released; window starts at 60
+    got = oracle.paged_decode(q, kc, vc, t2, L, 0.3, window=40)
+    assert np.array_equal(got, want)
