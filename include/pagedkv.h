@@ -204,6 +204,37 @@ pa_status pa_decode_fp8(void *out, const void *query, const void *key_cache,
                         void *stream);
 
 /*
+ * Paged decode attention with a sliding window of `window` positions ("PagedAttention
+ * por dentro", section "Sliding window attention": a model with a window of W
+ * tokens attends only to the last W tokens of its context).  For a context of
+ * L = context_lens[b] tokens, the softmax and the weighted sum of pa_decode run
+ * over positions [max(L - window, 0), L) only; blocks wholly before the window
+ * are never read, so their table entries may be anything (a block manager may
+ * already have released them: pa_bm_trim_window).
+ *  k_scales, v_scales  FP8 pools only (dtype PA_DTYPE_FP8_E4M3, as in
+ *                      pa_decode_fp8); ignored otherwise (may be NULL)
+ *  dtype               PA_DTYPE_F32, PA_DTYPE_BF16 or PA_DTYPE_FP8_E4M3 with
+ *                      the limits of pa_decode / pa_decode_fp8
+ *  window              > 0 (PA_ERR_INVALID_ARG otherwise)
+ *  workspace           at least pa_decode_sliding_window_workspace_bytes(...)
+ *                      with the same window; the split-K partitions cover the
+ *                      window, at most ceil(window / 16) + 1 blocks
+ * Everything else, results for window >= L included, is as in pa_decode.
+ */
+size_t pa_decode_sliding_window_workspace_bytes(int num_seqs, int num_q_heads, int num_kv_heads,
+                                                int head_dim, int max_blocks_per_seq,
+                                                int block_size, int window, int partition_size,
+                                                pa_dtype dtype);
+pa_status pa_decode_sliding_window(void *out, const void *query, const void *key_cache,
+                                   const void *value_cache, const float *k_scales,
+                                   const float *v_scales, const int32_t *block_tables,
+                                   const int32_t *context_lens, int num_seqs, int num_q_heads,
+                                   int num_kv_heads, int head_dim, int block_size,
+                                   int max_blocks_per_seq, int num_blocks, float scale,
+                                   pa_dtype dtype, int window, int partition_size, void *workspace,
+                                   size_t workspace_bytes, int32_t *device_status, void *stream);
+
+/*
  * Cache write into FP8 pools: as pa_cache_write, but each element x of the
  * new bfloat16 rows is stored as the E4M3 code of the float32 quotient
  * x / scale[kv_head] (IEEE single-precision division, then rounding to the
@@ -333,6 +364,16 @@ pa_status pa_bm_alloc_seq_cached(pa_bm *bm, int seq, const int32_t *tokens, int 
  * written; returns how many blocks were newly indexed, -1 for an unknown seq.
  * A key already indexed keeps its block; a block is indexed once. */
 int pa_bm_register_prefix(pa_bm *bm, int seq, const int32_t *tokens, int num_tokens);
+/* Sliding window ("PagedAttention por dentro", section "Sliding window
+ * attention": only the blocks of the active window are kept, older ones are
+ * freed).  For a sequence of N tokens attending to its last `window` tokens,
+ * releases every block whose positions all lie before N - window (the last
+ * such entry first) and sets its table entry to -1; returns how many blocks
+ * were released (0 when none), -1 for an unknown seq or window <= 0.  Such a
+ * sequence is decoded with pa_decode_sliding_window with the same window or a
+ * smaller one; forks share only its remaining blocks, and pa_bm_make_private
+ * of a released entry returns PA_ERR_INVALID_ARG. */
+int pa_bm_trim_window(pa_bm *bm, int seq, int window);
 int pa_bm_num_tokens(const pa_bm *bm, int seq);       /* -1 if unknown */
 int pa_bm_ref_count(const pa_bm *bm, int block);      /* -1 if out of range */
 /* Copies up to cap entries of seq's table to out; returns its length, -1 if unknown. */

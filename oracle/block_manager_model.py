@@ -166,7 +166,7 @@ class BlockManagerModel:
             own = tuple(int(t) for t in tokens[j * self.block_size:(j + 1) * self.block_size])
             parent = block_key(parent, own)
             b = table[j]
-            if parent in self.cached or b in self.block_key:
+            if b < 0 or parent in self.cached or b in self.block_key:
                 continue
             self.cached[parent] = b
             self.block_key[b] = parent
@@ -192,12 +192,15 @@ class BlockManagerModel:
         self.tables[child] = list(self.tables[parent])
         self.tokens[child] = self.tokens[parent]
         for b in self.tables[child]:
-            self.ref[b] += 1
+            if b >= 0:
+                self.ref[b] += 1
 
     def make_private(self, seq: int, logical_block: int):
         """Copy-on-write of one logical block; returns (src, dst) or None if private."""
         table = self.tables[seq]
         old = table[logical_block]
+        if old < 0:
+            raise ValueError("block released by trim_window")
         if self.ref[old] <= 1:
             return None
         new = self._take()
@@ -222,7 +225,26 @@ class BlockManagerModel:
         table = self.tables.pop(seq)
         del self.tokens[seq]
         for b in reversed(table):
-            self._release(b)
+            if b >= 0:
+                self._release(b)
+
+    def trim_window(self, seq: int, window: int) -> int:
+        """Sliding window ("PagedAttention por dentro", section "Sliding window
+        attention": only the active window's blocks are kept).  Blocks whose
+        positions all precede N - window are released, last first, and their
+        entries become -1; returns how many were released."""
+        if window <= 0 or seq not in self.tables:
+            raise ValueError("bad trim")
+        table = self.tables[seq]
+        n = self.tokens[seq]
+        dead = (n - window) // self.block_size if n > window else 0
+        released = 0
+        for j in range(dead - 1, -1, -1):
+            if table[j] >= 0:
+                self._release(table[j])
+                table[j] = -1
+                released += 1
+        return released
 
     # -- invariants ------------------------------------------------------
     def check(self) -> None:
@@ -230,7 +252,8 @@ class BlockManagerModel:
         for seq, table in self.tables.items():
             assert len(table) == self.blocks_needed(self.tokens[seq])
             for b in table:
-                counted[b] += 1
+                if b >= 0:
+                    counted[b] += 1
         assert counted == self.ref
         free = set(self.free)
         ev = set(self.evictable)

@@ -25,7 +25,7 @@ from ._lib import PagedKVError, check, lib  # noqa: F401
 
 BLOCK_SIZE = 16
 
-__all__ = ["decode", "decode_fp8", "decode_shared_prefix", "shared_prefix_blocks", "decode_workspace_bytes", "decode_partition_size",
+__all__ = ["decode", "decode_fp8", "decode_sliding_window", "decode_shared_prefix", "shared_prefix_blocks", "decode_workspace_bytes", "decode_partition_size",
            "cache_write", "cache_write_fp8", "block_copy", "launch_count", "BlockManager",
            "PagedKVError", "BLOCK_SIZE", "library_path"]
 
@@ -238,6 +238,64 @@ def decode_fp8(query, key_cache, value_cache, k_scales, v_scales, block_tables, 
     return out
 
 
+def decode_sliding_window(query, key_cache, value_cache, block_tables, context_lens, window,
+                          scale=None, *, k_scales=None, v_scales=None, out=None,
+                          partition_size=0, workspace=None, status=None, stream=None):
+    """Decode over the last ``window`` positions of each context
+    (``pa_decode_sliding_window``); bf16/fp32 pools, or E4M3 pools with
+    ``k_scales``/``v_scales`` and a bf16 query.  Returns ``out``."""
+    torch = _torch()
+    B, Hq, D = query.shape
+    NB, Hkv, BS, D2 = key_cache.shape
+    if BS != BLOCK_SIZE or D2 != D or tuple(value_cache.shape) != tuple(key_cache.shape):
+        raise ValueError("pools must be [num_blocks][num_kv_heads][16][head_dim] like query")
+    if block_tables.dim() != 2 or block_tables.shape[0] != B or tuple(context_lens.shape) != (B,):
+        raise ValueError("block_tables must be [num_seqs][max_blocks], context_lens [num_seqs]")
+    if int(window) <= 0:
+        raise ValueError("window must be positive")
+    ks_ptr = vs_ptr = None
+    if _is_fp8(key_cache):
+        if not _is_fp8(value_cache) or query.dtype != torch.bfloat16:
+            raise TypeError("E4M3 pools take a bfloat16 query")
+        if k_scales is None or v_scales is None:
+            raise ValueError("E4M3 pools need k_scales and v_scales")
+        if tuple(k_scales.shape) != (Hkv,) or tuple(v_scales.shape) != (Hkv,):
+            raise ValueError("k_scales / v_scales must be [num_kv_heads]")
+        code = _lib.PA_DTYPE_FP8_E4M3
+        ks_ptr = _dev(k_scales, "k_scales", torch.float32)
+        vs_ptr = _dev(v_scales, "v_scales", torch.float32)
+    else:
+        code = _dtype_code(query)
+        if key_cache.dtype != query.dtype or value_cache.dtype != query.dtype:
+            raise TypeError("query and pools must share one element type")
+    if scale is None:
+        scale = 1.0 / math.sqrt(D)
+    if out is None:
+        out = torch.empty_like(query)
+    elif out.shape != query.shape or out.dtype != query.dtype:
+        raise ValueError("out must match query")
+    max_blocks = block_tables.shape[1]
+    need = lib().pa_decode_sliding_window_workspace_bytes(B, Hq, Hkv, D, max_blocks, BLOCK_SIZE,
+                                                          int(window), int(partition_size), code)
+    if need == ctypes.c_size_t(-1).value:
+        raise ValueError("invalid arguments for pa_decode_sliding_window_workspace_bytes")
+    ws_ptr, ws_bytes = None, 0
+    if need > 0:
+        if workspace is None:
+            workspace = torch.empty(need, dtype=torch.uint8, device=query.device)
+        ws_ptr = _dev(workspace, "workspace")
+        ws_bytes = workspace.numel() * workspace.element_size()
+    rc = lib().pa_decode_sliding_window(
+        _dev(out, "out"), _dev(query, "query"), _dev(key_cache, "key_cache"),
+        _dev(value_cache, "value_cache"), ks_ptr, vs_ptr,
+        _dev(block_tables, "block_tables", torch.int32),
+        _dev(context_lens, "context_lens", torch.int32), B, Hq, Hkv, D, BLOCK_SIZE, max_blocks,
+        NB, float(scale), code, int(window), int(partition_size), ws_ptr, ws_bytes,
+        _status_ptr(status), _stream(stream, query.device))
+    check(rc, "pa_decode_sliding_window")
+    return out
+
+
 def cache_write_fp8(key_cache, value_cache, key, value, slot_mapping, k_scales, v_scales, *,
                     status=None, stream=None):
     """Quantise new bf16 K/V rows to E4M3 and scatter them into their slots."""
@@ -351,6 +409,16 @@ class BlockManager:
         import numpy as np
         t = np.ascontiguousarray(tokens, dtype=np.int32)
         n = lib().pa_bm_register_prefix(self._h, seq, t.ctypes.data, t.shape[0])
+        if n < 0:
+            raise KeyError(seq)
+        return int(n)
+
+    def trim_window(self, seq: int, window: int) -> int:
+        """Release the blocks wholly before the last ``window`` tokens (their table
+        entries become -1); returns how many were released."""
+        if int(window) <= 0:
+            raise ValueError("window must be positive")
+        n = lib().pa_bm_trim_window(self._h, seq, int(window))
         if n < 0:
             raise KeyError(seq)
         return int(n)

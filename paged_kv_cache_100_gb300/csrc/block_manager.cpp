@@ -149,13 +149,15 @@ extern "C" pa_status pa_bm_fork(pa_bm *bm, int parent, int child) {
     auto it = bm->seqs.find(parent);
     if (it == bm->seqs.end() || bm->seqs.count(child)) return PA_ERR_NOT_FOUND;
     pa_bm::Seq s = it->second;
-    for (int32_t b : s.table) bm->ref[b] += 1;
+    for (int32_t b : s.table)
+        if (b >= 0) bm->ref[b] += 1;   // -1: released by pa_bm_trim_window
     bm->seqs.emplace(child, std::move(s));
     return PA_OK;
 }
 
 static pa_status make_private(pa_bm *bm, pa_bm::Seq &s, int logical, int32_t *src, int32_t *dst) {
     const int32_t old = s.table[(size_t)logical];
+    if (old < 0) return PA_ERR_INVALID_ARG;   // released by pa_bm_trim_window
     if (bm->ref[old] <= 1) {
         *src = -1;
         *dst = -1;
@@ -208,9 +210,32 @@ extern "C" pa_status pa_bm_free_seq(pa_bm *bm, int seq) {
     auto it = bm->seqs.find(seq);
     if (it == bm->seqs.end()) return PA_ERR_NOT_FOUND;
     const std::vector<int32_t> &t = it->second.table;
-    for (size_t i = t.size(); i-- > 0;) bm->release(t[i]);
+    for (size_t i = t.size(); i-- > 0;)
+        if (t[i] >= 0) bm->release(t[i]);
     bm->seqs.erase(it);
     return PA_OK;
+}
+
+// Sliding window ("PagedAttention por dentro", section "Sliding window
+// attention": the engine keeps only the blocks of the active window and frees
+// the older ones).  A sequence of N tokens that attends to its last `window`
+// tokens never reads a block whose positions all lie before N - window: those
+// are released (last such entry first) and their table entries become -1.
+extern "C" int pa_bm_trim_window(pa_bm *bm, int seq, int window) {
+    if (bm == nullptr || window <= 0) return -1;
+    auto it = bm->seqs.find(seq);
+    if (it == bm->seqs.end()) return -1;
+    pa_bm::Seq &s = it->second;
+    const int64_t dead = s.tokens > window ? (s.tokens - window) / bm->block_size : 0;
+    int released = 0;
+    for (int64_t j = dead; j-- > 0;) {
+        const int32_t b = s.table[(size_t)j];
+        if (b < 0) continue;
+        bm->release(b);
+        s.table[(size_t)j] = -1;
+        ++released;
+    }
+    return released;
 }
 
 extern "C" int pa_bm_num_evictable(const pa_bm *bm) {
@@ -270,7 +295,7 @@ extern "C" int pa_bm_register_prefix(pa_bm *bm, int seq, const int32_t *tokens, 
         const int32_t *own = tokens + (size_t)j * bs;
         parent = block_key(parent, own, bs);
         const int32_t b = table[(size_t)j];
-        if (bm->cached.count(parent) || bm->has_key[b]) continue;
+        if (b < 0 || bm->cached.count(parent) || bm->has_key[b]) continue;
         bm->cached.emplace(parent, b);
         bm->has_key[b] = 1;
         bm->key_of[b] = parent;

@@ -77,12 +77,14 @@ struct DecodeArgs {
     int prefix_blocks;  // shared prefix length in blocks (prefix kernel)
     int prefix_chunk_blocks;
     int prefix_chunks;
+    int window;         // > 0: attend only to the last `window` positions
 };
 
 // The (sequence, head, partition) a CTA works on, with its token range.
 struct Work {
     int b, head, part;
     int L;          // context length (clamped)
+    int start;      // first position attended (sliding window), else 0
     int nparts;     // partitions of this sequence (1 when L == 0)
     int blk0;       // first logical block of the partition
     int nblk;       // blocks in the partition
@@ -106,10 +108,14 @@ __device__ __forceinline__ bool cta_work(const DecodeArgs &a, int heads_axis, Wo
     }
     L = max(L - a.token_offset, 0);   // the part of the context this kernel covers
     w.L = L;
+    // sliding window: positions [L - window, L); whole blocks before it are skipped
+    w.start = (a.window > 0 && L > a.window) ? L - a.window : 0;
+    const int first_blk = w.start / kBlockSize;
     const int seq_blocks = (L + kBlockSize - 1) / kBlockSize;
-    w.nparts = seq_blocks == 0 ? 1 : (seq_blocks + a.part_blocks - 1) / a.part_blocks;
+    const int range = seq_blocks - first_blk;
+    w.nparts = range <= 0 ? 1 : (range + a.part_blocks - 1) / a.part_blocks;
     if (w.part >= w.nparts) return false;
-    w.blk0 = w.part * a.part_blocks;
+    w.blk0 = first_blk + w.part * a.part_blocks;
     const int end = min(w.blk0 + a.part_blocks, seq_blocks);
     w.nblk = max(end - w.blk0, 0);
     return true;
@@ -165,6 +171,22 @@ __device__ __forceinline__ void merge_and_store(const DecodeArgs &a, const Work 
 // ---------------------------------------------------------------------------
 __device__ __forceinline__ uint32_t swz(uint32_t tile, int row, int chunk) {
     return tile + (uint32_t)((chunk >> 3) * 2048 + row * 128 + (((chunk & 7) ^ (row & 7)) << 4));
+}
+
+// Zeroes the rows outside [nlo, nvalid) of a 16-row bf16 tile of D/64 swizzled
+// sub-tiles (whole rows, so the swizzle does not matter).
+template <int D>
+__device__ __forceinline__ void zero_rows_outside(uint32_t tile, int nlo, int nvalid, int lane) {
+    constexpr int kChunks = D / 8;          // 16-byte chunks per row
+    const int zrows = 16 - (nvalid - nlo);
+    for (int i = lane; i < zrows * kChunks; i += 32) {
+        int r = i / kChunks;
+        r = r < nlo ? r : r - nlo + nvalid;
+        const int ch = i % kChunks;
+        asm volatile("st.shared.v4.u32 [%0], {%1, %1, %1, %1};" ::"r"(swz(tile, r, ch)), "r"(0u)
+                     : "memory");
+    }
+    __syncwarp();
 }
 
 __device__ __forceinline__ uint4 lds128(uint32_t addr) {
@@ -233,7 +255,7 @@ struct MhaConsumer {
         l = 0.f;
     }
 
-    __device__ __forceinline__ void block(uint32_t ktile, uint32_t vtile, int nvalid) {
+    __device__ __forceinline__ void block(uint32_t ktile, uint32_t vtile, int nlo, int nvalid) {
         float v[RPL];
 #pragma unroll
         for (int i = 0; i < RPL; ++i) v[i] = dot8(q, lds128(swz(ktile, rg * RPL + i, c)));
@@ -251,7 +273,7 @@ struct MhaConsumer {
         }
         float s = v[0] + __shfl_xor_sync(kFull, v[0], 1);
         const int row = rg * RPL + ((lane & (CH - 1)) >> 1);
-        s = row < nvalid ? s : -INFINITY;
+        s = (row >= nlo && row < nvalid) ? s : -INFINITY;
         float bmax = s;
 #pragma unroll
         for (int M = 2; M < 32; M <<= 1) bmax = fmaxf(bmax, __shfl_xor_sync(kFull, bmax, M));
@@ -267,7 +289,7 @@ struct MhaConsumer {
             const int r = rg * RPL + i;
             const float pr = __shfl_sync(kFull, p, rg * CH + 2 * i);
             const uint4 vv = lds128(swz(vtile, r, c));
-            if (r < nvalid) axpy8(acc, pr, vv);
+            if (r >= nlo && r < nvalid) axpy8(acc, pr, vv);
         }
     }
 
@@ -330,7 +352,7 @@ struct GqaConsumer {
         l0 = l1 = 0.f;
     }
 
-    __device__ __forceinline__ void block(uint32_t ktile, uint32_t vtile, int nvalid) {
+    __device__ __forceinline__ void block(uint32_t ktile, uint32_t vtile, int nlo, int nvalid) {
         float s[2][4];
 #pragma unroll
         for (int j = 0; j < 2; ++j) s[j][0] = s[j][1] = s[j][2] = s[j][3] = 0.f;
@@ -350,7 +372,7 @@ struct GqaConsumer {
 #pragma unroll
             for (int e = 0; e < 4; ++e) {
                 const int tok = 8 * j + 2 * t + (e & 1);
-                s[j][e] = tok < nvalid ? s[j][e] * scale_log2 : -INFINITY;
+                s[j][e] = (tok >= nlo && tok < nvalid) ? s[j][e] * scale_log2 : -INFINITY;
             }
         float mx0 = fmaxf(fmaxf(s[0][0], s[0][1]), fmaxf(s[1][0], s[1][1]));
         mx0 = fmaxf(mx0, __shfl_xor_sync(kFull, mx0, 1));
@@ -398,19 +420,9 @@ struct GqaConsumer {
         } else {
             pa[1] = pa[3] = pl[1] = pl[3] = 0u;
         }
-        if (nvalid < 16) {
-            // Rows past the context may hold anything (even NaN): zero them so
-            // that 0 * row stays 0 in the tensor-core sum.
-            const int zrows = 16 - nvalid;
-            for (int i = lane; i < zrows * (D / 8); i += 32) {
-                const int r = nvalid + i / (D / 8);
-                const int ch = i % (D / 8);
-                asm volatile("st.shared.v4.u32 [%0], {%1, %1, %1, %1};" ::"r"(swz(vtile, r, ch)),
-                             "r"(0u)
-                             : "memory");
-            }
-            __syncwarp();
-        }
+        // Rows outside the context may hold anything (even NaN): zero them so
+        // that 0 * row stays 0 in the tensor-core sum.
+        if (nlo > 0 || nvalid < 16) zero_rows_outside<D>(vtile, nlo, nvalid, lane);
 #pragma unroll
         for (int dd = 0; dd < D / 16; ++dd) {
             uint32_t b[4];
@@ -489,7 +501,7 @@ struct GqaTConsumer {
         l0 = l1 = 0.f;
     }
 
-    __device__ __forceinline__ void block(uint32_t ktile, uint32_t vtile, int nvalid) {
+    __device__ __forceinline__ void block(uint32_t ktile, uint32_t vtile, int nlo, int nvalid) {
         const int mi = lane >> 3, rr = lane & 7;
         float s[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
@@ -498,7 +510,7 @@ struct GqaTConsumer {
             ldsm_x4(a, swz(ktile, (mi & 1) * 8 + rr, 2 * ks + (mi >> 1)));
             mma_bf16_16816(s, a, qb[ks][0], qb[ks][1]);
         }
-        const bool v0 = g < nvalid, v1 = g + 8 < nvalid;
+        const bool v0 = g >= nlo && g < nvalid, v1 = g + 8 >= nlo && g + 8 < nvalid;
         s[0] = v0 ? s[0] * scale_log2 : -INFINITY;
         s[1] = v0 ? s[1] * scale_log2 : -INFINITY;
         s[2] = v1 ? s[2] * scale_log2 : -INFINITY;
@@ -530,17 +542,7 @@ struct GqaTConsumer {
         split_bf16x2(p2, p3, bot_hi, bot_lo);   // token g + 8
         const uint32_t bh0 = movmatrix_trans(top_hi), bh1 = movmatrix_trans(bot_hi);
         const uint32_t bl0 = movmatrix_trans(top_lo), bl1 = movmatrix_trans(bot_lo);
-        if (nvalid < 16) {
-            const int zrows = 16 - nvalid;
-            for (int i = lane; i < zrows * (D / 8); i += 32) {
-                const int r = nvalid + i / (D / 8);
-                const int ch = i % (D / 8);
-                asm volatile("st.shared.v4.u32 [%0], {%1, %1, %1, %1};" ::"r"(swz(vtile, r, ch)),
-                             "r"(0u)
-                             : "memory");
-            }
-            __syncwarp();
-        }
+        if (nlo > 0 || nvalid < 16) zero_rows_outside<D>(vtile, nlo, nvalid, lane);
 #pragma unroll
         for (int mt = 0; mt < KS; ++mt) {
             uint32_t a[4];
@@ -606,12 +608,15 @@ __device__ __forceinline__ uint2 lds64(uint32_t addr) {
     return v;
 }
 
-// Zeroes rows [nvalid, 16) of a 16 x 128-byte tile (values past the context may
-// be anything, NaN codes included, and must not reach a tensor-core sum).
-__device__ __forceinline__ void zero_tail_rows_128(uint32_t tile, int nvalid, int lane) {
-    const int zrows = 16 - nvalid;
+// Zeroes the rows outside [nlo, nvalid) of a 16 x 128-byte tile (values
+// outside the context may be anything, NaN codes included, and must not reach
+// a tensor-core sum).
+__device__ __forceinline__ void zero_rows_outside_128(uint32_t tile, int nlo, int nvalid, int lane) {
+    const int zrows = 16 - (nvalid - nlo);
     for (int i = lane; i < zrows * 8; i += 32) {
-        const uint32_t addr = tile + (uint32_t)((nvalid + i / 8) * 128 + (i % 8) * 16);
+        int r = i / 8;
+        r = r < nlo ? r : r - nlo + nvalid;
+        const uint32_t addr = tile + (uint32_t)(r * 128 + (i % 8) * 16);
         asm volatile("st.shared.v4.u32 [%0], {%1, %1, %1, %1};" ::"r"(addr), "r"(0u) : "memory");
     }
     __syncwarp();
@@ -655,7 +660,7 @@ struct MhaFp8Consumer {
         vs = a.v_scales[w.head];
     }
 
-    __device__ __forceinline__ void block(uint32_t ktile, uint32_t vtile, int nvalid) {
+    __device__ __forceinline__ void block(uint32_t ktile, uint32_t vtile, int nlo, int nvalid) {
         float v[RPL];
 #pragma unroll
         for (int i = 0; i < RPL; ++i) {
@@ -681,7 +686,7 @@ struct MhaFp8Consumer {
         }
         float s = (v[0] + __shfl_xor_sync(kFull, v[0], 1)) * ck;
         const int row = rg * RPL + ((lane & (CH - 1)) >> 1);
-        s = row < nvalid ? s : -INFINITY;
+        s = (row >= nlo && row < nvalid) ? s : -INFINITY;
         float bmax = s;
 #pragma unroll
         for (int M = 2; M < 32; M <<= 1) bmax = fmaxf(bmax, __shfl_xor_sync(kFull, bmax, M));
@@ -697,7 +702,7 @@ struct MhaFp8Consumer {
             const int r = rg * RPL + i;
             const float pr = __shfl_sync(kFull, p, rg * CH + 2 * i);
             const uint4 vw = lds128(swz(vtile, r, c));
-            if (r < nvalid) {
+            if (r >= nlo && r < nvalid) {
                 const uint32_t w4[4] = {vw.x, vw.y, vw.z, vw.w};
 #pragma unroll
                 for (int j = 0; j < 4; ++j) {
@@ -784,7 +789,7 @@ struct GqaTFp8Consumer {
         l0 = l1 = 0.f;
     }
 
-    __device__ __forceinline__ void block(uint32_t ktile, uint32_t vtile, int nvalid) {
+    __device__ __forceinline__ void block(uint32_t ktile, uint32_t vtile, int nlo, int nvalid) {
         float s[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
         for (int kk = 0; kk < D / 32; ++kk) {
@@ -802,7 +807,7 @@ struct GqaTFp8Consumer {
             a[3] = e4m3x2_to_f16x2(r1.y >> 16);
             mma_f16_16816(s, a, qb[2 * kk + 1][0], qb[2 * kk + 1][1]);
         }
-        const bool v0 = g < nvalid, v1 = g + 8 < nvalid;
+        const bool v0 = g >= nlo && g < nvalid, v1 = g + 8 >= nlo && g + 8 < nvalid;
         s[0] = v0 ? s[0] * ck : -INFINITY;
         s[1] = v0 ? s[1] * ck : -INFINITY;
         s[2] = v1 ? s[2] * ck : -INFINITY;
@@ -833,7 +838,7 @@ struct GqaTFp8Consumer {
         split_f16x2(p2, p3, bot_hi, bot_lo);
         const uint32_t bh0 = movmatrix_trans(top_hi), bh1 = movmatrix_trans(bot_hi);
         const uint32_t bl0 = movmatrix_trans(top_lo), bl1 = movmatrix_trans(bot_lo);
-        if (nvalid < 16) zero_tail_rows_128(vtile, nvalid, lane);
+        if (nlo > 0 || nvalid < 16) zero_rows_outside_128(vtile, nlo, nvalid, lane);
 #pragma unroll
         for (int c = 0; c < D / 32; ++c) {
             const int byte = 32 * c + 4 * g;
@@ -988,8 +993,9 @@ pa_decode_bf16_kernel(const __grid_constant__ CUtensorMap kmap,
         }
         const int tok0 = (w.blk0 + warp + it * NW) * kBlockSize;
         const int nvalid = min(kBlockSize, w.L - tok0);
+        const int nlo = max(0, w.start - tok0);
         const uint32_t kt = smem_u32(my_stages + s * Lay::kStageBytes);
-        cons.block(kt, kt + Lay::kTileBytes, nvalid);
+        cons.block(kt, kt + Lay::kTileBytes, nlo, nvalid);
         __syncwarp();
         if (lane == 0 && it + STAGES < my_count) {
             fence_proxy_async_smem();
@@ -1334,8 +1340,9 @@ __global__ void __launch_bounds__(NW * 32) pa_decode_f32_kernel(const float *__r
         }
         const int tok0 = (w.blk0 + j) * kBlockSize;
         const int nvalid = min(kBlockSize, w.L - tok0);
+        const int nlo = max(0, w.start - tok0);
         const size_t base = (((size_t)phys * a.num_kv_heads + kvh) * kBlockSize) * D;
-        for (int r = 0; r < nvalid; ++r) {
+        for (int r = nlo; r < nvalid; ++r) {
             const float *krow = kc + base + (size_t)r * D;
             const float *vrow = vc + base + (size_t)r * D;
             float s = 0.f;
@@ -1373,9 +1380,10 @@ __global__ void __launch_bounds__(128) pa_reduce_kernel(const DecodeArgs a, int 
     const int lmax = a.max_blocks * kBlockSize;
     L = L < 0 ? 0 : (L > lmax ? lmax : L);
     L = max(L - a.token_offset, 0);
-    const int seq_blocks = (L + kBlockSize - 1) / kBlockSize;
+    const int start = (a.window > 0 && L > a.window) ? L - a.window : 0;
+    const int range = (L + kBlockSize - 1) / kBlockSize - start / kBlockSize;
     const int nparts =
-        a.part_base + (seq_blocks == 0 ? 1 : (seq_blocks + a.part_blocks - 1) / a.part_blocks);
+        a.part_base + (range <= 0 ? 1 : (range + a.part_blocks - 1) / a.part_blocks);
     if (nparts <= 1 && !a.always_partial) return;
     const size_t row0 = ((size_t)b * a.num_q_heads + h) * a.max_parts;
     extern __shared__ float s_w[];   // [nparts] weights
@@ -1645,56 +1653,89 @@ extern "C" int pa_decode_partition_size(int num_seqs, int num_q_heads, int num_k
     return auto_partition(num_seqs, heads_axis, max_blocks_per_seq);
 }
 
-extern "C" size_t pa_decode_workspace_bytes(int num_seqs, int num_q_heads, int num_kv_heads,
-                                            int head_dim, int max_blocks_per_seq, int block_size,
-                                            int partition_size, pa_dtype dtype) {
-    if (num_seqs < 0 || num_q_heads <= 0 || num_kv_heads <= 0 || head_dim <= 0 ||
-        max_blocks_per_seq < 0 || block_size != kBlockSize ||
-        (dtype != PA_DTYPE_F32 && dtype != PA_DTYPE_BF16 && dtype != PA_DTYPE_FP8_E4M3))
-        return (size_t)-1;
+namespace pa {
+namespace {
+
+bool kv_dtype_ok(pa_dtype d) {
+    return d == PA_DTYPE_F32 || d == PA_DTYPE_BF16 || d == PA_DTYPE_FP8_E4M3;
+}
+
+// Blocks one sequence's decode can touch: the whole table, or for a sliding
+// window of W positions at most ceil(W / 16) + 1 blocks (the window's first
+// position need not start a block).
+int span_blocks(int max_blocks, int window) {
+    if (window <= 0) return max_blocks;
+    return std::min(max_blocks, (window + kBlockSize - 1) / kBlockSize + 1);
+}
+
+// Partition size and partition count of a decode call; false on a bad size.
+bool plan_decode(int num_seqs, int num_q_heads, int num_kv_heads, int max_blocks, pa_dtype dtype,
+                 int window, int partition_size, int *part_blocks, int *max_parts) {
     const int heads_axis = dtype == PA_DTYPE_F32 ? num_q_heads : num_kv_heads;
-    const int p = resolve_partition(partition_size, num_seqs, heads_axis, max_blocks_per_seq);
-    if (p < 0) return (size_t)-1;
-    const int part_blocks = p / kBlockSize;
-    const int max_parts = max(1, (max_blocks_per_seq + part_blocks - 1) / part_blocks);
+    const int span = span_blocks(max_blocks, window);
+    const int p = resolve_partition(partition_size, num_seqs, heads_axis, span);
+    if (p < 0) return false;
+    *part_blocks = p / kBlockSize;
+    *max_parts = std::max(1, (span + *part_blocks - 1) / *part_blocks);
+    return true;
+}
+
+size_t decode_workspace(int num_seqs, int num_q_heads, int num_kv_heads, int head_dim,
+                        int max_blocks, int block_size, int window, int partition_size,
+                        pa_dtype dtype) {
+    if (num_seqs < 0 || num_q_heads <= 0 || num_kv_heads <= 0 || head_dim <= 0 ||
+        max_blocks < 0 || block_size != kBlockSize || window < 0 || !kv_dtype_ok(dtype))
+        return (size_t)-1;
+    int part_blocks, max_parts;
+    if (!plan_decode(num_seqs, num_q_heads, num_kv_heads, max_blocks, dtype, window,
+                     partition_size, &part_blocks, &max_parts))
+        return (size_t)-1;
     return workspace_for(num_seqs, num_q_heads, head_dim, max_parts);
 }
 
-extern "C" pa_status pa_decode(void *out, const void *query, const void *key_cache,
-                               const void *value_cache, const int32_t *block_tables,
-                               const int32_t *context_lens, int num_seqs, int num_q_heads,
-                               int num_kv_heads, int head_dim, int block_size,
-                               int max_blocks_per_seq, int num_blocks, float scale, pa_dtype dtype,
-                               int partition_size, void *workspace, size_t workspace_bytes,
-                               int32_t *device_status, void *stream) {
+// The one decode path behind pa_decode, pa_decode_fp8 and
+// pa_decode_sliding_window: validation, planning, kernel and merge launches.
+pa_status decode_common(void *out, const void *query, const void *key_cache,
+                        const void *value_cache, const float *k_scales, const float *v_scales,
+                        const int32_t *block_tables, const int32_t *context_lens, int num_seqs,
+                        int num_q_heads, int num_kv_heads, int head_dim, int block_size,
+                        int max_blocks_per_seq, int num_blocks, float scale, pa_dtype dtype,
+                        int window, int partition_size, void *workspace, size_t workspace_bytes,
+                        int32_t *device_status, void *stream) {
     if (num_seqs < 0 || num_q_heads <= 0 || num_kv_heads <= 0 || block_size != kBlockSize ||
         max_blocks_per_seq < 0 || num_blocks <= 0 || num_q_heads % num_kv_heads != 0 ||
-        !(scale == scale))
+        !(scale == scale) || window < 0 || !kv_dtype_ok(dtype))
         return PA_ERR_INVALID_ARG;
-    if (dtype != PA_DTYPE_F32 && dtype != PA_DTYPE_BF16) return PA_ERR_INVALID_ARG;
-    const int heads_axis = dtype == PA_DTYPE_BF16 ? num_kv_heads : num_q_heads;
     if (partition_size != 0 &&
         (partition_size < kBlockSize || partition_size > kMaxPartition || partition_size % kBlockSize))
         return PA_ERR_INVALID_ARG;
     if (num_seqs == 0) return PA_OK;
-    const int p = resolve_partition(partition_size, num_seqs, heads_axis, max_blocks_per_seq);
-    if (p < 0) return PA_ERR_INVALID_ARG;
+    const bool fp8 = dtype == PA_DTYPE_FP8_E4M3;
     if (!out || !query || !key_cache || !value_cache || !block_tables || !context_lens)
         return PA_ERR_INVALID_ARG;
+    if (fp8 && (!k_scales || !v_scales)) return PA_ERR_INVALID_ARG;
     if (!aligned16(out) || !aligned16(query) || !aligned16(key_cache) || !aligned16(value_cache))
+        return PA_ERR_INVALID_ARG;
+    if (fp8 && ((reinterpret_cast<uintptr_t>(k_scales) & 3u) ||
+                (reinterpret_cast<uintptr_t>(v_scales) & 3u)))
         return PA_ERR_INVALID_ARG;
     const int group = num_q_heads / num_kv_heads;
     if (dtype == PA_DTYPE_BF16) {
         if (head_dim != 64 && head_dim != 128) return PA_ERR_UNSUPPORTED;
         if (group > 16) return PA_ERR_UNSUPPORTED;
+    } else if (fp8) {
+        if (head_dim != 128 || group > 8) return PA_ERR_UNSUPPORTED;
     } else {
         if (head_dim != 32 && head_dim != 64 && head_dim != 128 && head_dim != 256)
             return PA_ERR_UNSUPPORTED;
     }
     const int64_t rows = (int64_t)num_blocks * num_kv_heads * kBlockSize;
     if (rows >= ((int64_t)1 << 31)) return PA_ERR_UNSUPPORTED;
-    const int part_blocks = p / kBlockSize;
-    const int max_parts = max(1, (max_blocks_per_seq + part_blocks - 1) / part_blocks);
+    int part_blocks, max_parts;
+    if (!plan_decode(num_seqs, num_q_heads, num_kv_heads, max_blocks_per_seq, dtype, window,
+                     partition_size, &part_blocks, &max_parts))
+        return PA_ERR_INVALID_ARG;
+    const int heads_axis = dtype == PA_DTYPE_F32 ? num_q_heads : num_kv_heads;
     if ((int64_t)num_seqs * heads_axis * max_parts >= ((int64_t)1 << 31)) return PA_ERR_UNSUPPORTED;
     const size_t need = workspace_for(num_seqs, num_q_heads, head_dim, max_parts);
     if (need > 0 && (workspace == nullptr || workspace_bytes < need || !aligned16(workspace)))
@@ -1712,8 +1753,8 @@ extern "C" pa_status pa_decode(void *out, const void *query, const void *key_cac
                                  255) & ~size_t(255)))
                          : nullptr;
     a.status = device_status;
-    a.k_scales = nullptr;
-    a.v_scales = nullptr;
+    a.k_scales = fp8 ? k_scales : nullptr;
+    a.v_scales = fp8 ? v_scales : nullptr;
     a.num_seqs = num_seqs;
     a.num_q_heads = num_q_heads;
     a.num_kv_heads = num_kv_heads;
@@ -1724,10 +1765,13 @@ extern "C" pa_status pa_decode(void *out, const void *query, const void *key_cac
     a.scale_log2 = scale * kLog2e;
     a.token_offset = a.part_base = a.always_partial = 0;
     a.prefix_blocks = a.prefix_chunk_blocks = a.prefix_chunks = 0;
+    a.window = window;
     cudaStream_t st = static_cast<cudaStream_t>(stream);
 
     pa_status s;
-    if (dtype == PA_DTYPE_BF16) {
+    if (fp8) {
+        s = dispatch_fp8(group, a, key_cache, value_cache, rows, st);
+    } else if (dtype == PA_DTYPE_BF16) {
         s = head_dim == 64 ? dispatch_bf16<64>(group, a, key_cache, value_cache, rows, st)
                            : dispatch_bf16<128>(group, a, key_cache, value_cache, rows, st);
     } else {
@@ -1739,8 +1783,32 @@ extern "C" pa_status pa_decode(void *out, const void *query, const void *key_cac
         }
     }
     if (s != PA_OK || max_parts <= 1) return s;
-    return dtype == PA_DTYPE_BF16 ? launch_reduce<__nv_bfloat16>(a, head_dim, st)
-                                  : launch_reduce<float>(a, head_dim, st);
+    return dtype == PA_DTYPE_F32 ? launch_reduce<float>(a, head_dim, st)
+                                 : launch_reduce<__nv_bfloat16>(a, head_dim, st);
+}
+
+}  // namespace
+}  // namespace pa
+
+extern "C" size_t pa_decode_workspace_bytes(int num_seqs, int num_q_heads, int num_kv_heads,
+                                            int head_dim, int max_blocks_per_seq, int block_size,
+                                            int partition_size, pa_dtype dtype) {
+    return decode_workspace(num_seqs, num_q_heads, num_kv_heads, head_dim, max_blocks_per_seq,
+                            block_size, 0, partition_size, dtype);
+}
+
+extern "C" pa_status pa_decode(void *out, const void *query, const void *key_cache,
+                               const void *value_cache, const int32_t *block_tables,
+                               const int32_t *context_lens, int num_seqs, int num_q_heads,
+                               int num_kv_heads, int head_dim, int block_size,
+                               int max_blocks_per_seq, int num_blocks, float scale, pa_dtype dtype,
+                               int partition_size, void *workspace, size_t workspace_bytes,
+                               int32_t *device_status, void *stream) {
+    if (dtype != PA_DTYPE_F32 && dtype != PA_DTYPE_BF16) return PA_ERR_INVALID_ARG;
+    return decode_common(out, query, key_cache, value_cache, nullptr, nullptr, block_tables,
+                         context_lens, num_seqs, num_q_heads, num_kv_heads, head_dim, block_size,
+                         max_blocks_per_seq, num_blocks, scale, dtype, 0, partition_size,
+                         workspace, workspace_bytes, device_status, stream);
 }
 
 extern "C" pa_status pa_decode_fp8(void *out, const void *query, const void *key_cache,
@@ -1751,61 +1819,34 @@ extern "C" pa_status pa_decode_fp8(void *out, const void *query, const void *key
                                    int max_blocks_per_seq, int num_blocks, float scale,
                                    int partition_size, void *workspace, size_t workspace_bytes,
                                    int32_t *device_status, void *stream) {
-    if (num_seqs < 0 || num_q_heads <= 0 || num_kv_heads <= 0 || block_size != kBlockSize ||
-        max_blocks_per_seq < 0 || num_blocks <= 0 || num_q_heads % num_kv_heads != 0 ||
-        !(scale == scale))
-        return PA_ERR_INVALID_ARG;
-    if (partition_size != 0 &&
-        (partition_size < kBlockSize || partition_size > kMaxPartition || partition_size % kBlockSize))
-        return PA_ERR_INVALID_ARG;
-    if (num_seqs == 0) return PA_OK;
-    if (!out || !query || !key_cache || !value_cache || !k_scales || !v_scales || !block_tables ||
-        !context_lens)
-        return PA_ERR_INVALID_ARG;
-    if (!aligned16(out) || !aligned16(query) || !aligned16(key_cache) || !aligned16(value_cache) ||
-        (reinterpret_cast<uintptr_t>(k_scales) & 3u) || (reinterpret_cast<uintptr_t>(v_scales) & 3u))
-        return PA_ERR_INVALID_ARG;
-    const int group = num_q_heads / num_kv_heads;
-    if (head_dim != 128 || group > 8) return PA_ERR_UNSUPPORTED;
-    const int64_t rows = (int64_t)num_blocks * num_kv_heads * kBlockSize;
-    if (rows >= ((int64_t)1 << 31)) return PA_ERR_UNSUPPORTED;
-    const int p = resolve_partition(partition_size, num_seqs, num_kv_heads, max_blocks_per_seq);
-    if (p < 0) return PA_ERR_INVALID_ARG;
-    const int part_blocks = p / kBlockSize;
-    const int max_parts = max(1, (max_blocks_per_seq + part_blocks - 1) / part_blocks);
-    if ((int64_t)num_seqs * num_kv_heads * max_parts >= ((int64_t)1 << 31)) return PA_ERR_UNSUPPORTED;
-    const size_t need = workspace_for(num_seqs, num_q_heads, head_dim, max_parts);
-    if (need > 0 && (workspace == nullptr || workspace_bytes < need || !aligned16(workspace)))
-        return PA_ERR_WORKSPACE;
+    return decode_common(out, query, key_cache, value_cache, k_scales, v_scales, block_tables,
+                         context_lens, num_seqs, num_q_heads, num_kv_heads, head_dim, block_size,
+                         max_blocks_per_seq, num_blocks, scale, PA_DTYPE_FP8_E4M3, 0,
+                         partition_size, workspace, workspace_bytes, device_status, stream);
+}
 
-    DecodeArgs a;
-    a.out = out;
-    a.query = query;
-    a.block_tables = block_tables;
-    a.context_lens = context_lens;
-    a.part_o = static_cast<float *>(workspace);
-    a.part_ml = need > 0 ? reinterpret_cast<float2 *>(
-                               static_cast<uint8_t *>(workspace) +
-                               (((size_t)num_seqs * num_q_heads * max_parts * head_dim * sizeof(float) +
-                                 255) & ~size_t(255)))
-                         : nullptr;
-    a.status = device_status;
-    a.k_scales = k_scales;
-    a.v_scales = v_scales;
-    a.num_seqs = num_seqs;
-    a.num_q_heads = num_q_heads;
-    a.num_kv_heads = num_kv_heads;
-    a.max_blocks = max_blocks_per_seq;
-    a.num_blocks = num_blocks;
-    a.part_blocks = part_blocks;
-    a.max_parts = max_parts;
-    a.scale_log2 = scale * kLog2e;
-    a.token_offset = a.part_base = a.always_partial = 0;
-    a.prefix_blocks = a.prefix_chunk_blocks = a.prefix_chunks = 0;
-    cudaStream_t st = static_cast<cudaStream_t>(stream);
-    pa_status s = dispatch_fp8(group, a, key_cache, value_cache, rows, st);
-    if (s != PA_OK || max_parts <= 1) return s;
-    return launch_reduce<__nv_bfloat16>(a, head_dim, st);
+extern "C" size_t pa_decode_sliding_window_workspace_bytes(int num_seqs, int num_q_heads,
+                                                           int num_kv_heads, int head_dim,
+                                                           int max_blocks_per_seq, int block_size,
+                                                           int window, int partition_size,
+                                                           pa_dtype dtype) {
+    if (window <= 0) return (size_t)-1;
+    return decode_workspace(num_seqs, num_q_heads, num_kv_heads, head_dim, max_blocks_per_seq,
+                            block_size, window, partition_size, dtype);
+}
+
+extern "C" pa_status pa_decode_sliding_window(
+    void *out, const void *query, const void *key_cache, const void *value_cache,
+    const float *k_scales, const float *v_scales, const int32_t *block_tables,
+    const int32_t *context_lens, int num_seqs, int num_q_heads, int num_kv_heads, int head_dim,
+    int block_size, int max_blocks_per_seq, int num_blocks, float scale, pa_dtype dtype, int window,
+    int partition_size, void *workspace, size_t workspace_bytes, int32_t *device_status,
+    void *stream) {
+    if (window <= 0) return PA_ERR_INVALID_ARG;
+    return decode_common(out, query, key_cache, value_cache, k_scales, v_scales, block_tables,
+                         context_lens, num_seqs, num_q_heads, num_kv_heads, head_dim, block_size,
+                         max_blocks_per_seq, num_blocks, scale, dtype, window, partition_size,
+                         workspace, workspace_bytes, device_status, stream);
 }
 
 namespace pa {
@@ -1968,6 +2009,7 @@ extern "C" pa_status pa_decode_shared_prefix(
     a.prefix_blocks = num_prefix_blocks;
     a.prefix_chunk_blocks = p.prefix_chunk_blocks;
     a.prefix_chunks = p.prefix_chunks;
+    a.window = 0;
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     std::lock_guard<std::mutex> lock(g_side_mutex);
     SideStream *side = nullptr;

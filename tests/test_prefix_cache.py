@@ -128,3 +128,80 @@ def test_native_prefix_cache_matches_the_model():
                 assert bm.table(s) == model.table(s)
             for b in range(60):
                 assert bm.ref_count(b) == model.ref_count(b)
+
+
+def test_trim_window_releases_blocks_before_the_window():
+    """Only blocks wholly before the last W tokens go back to the pool."""
+    bm = BlockManagerModel(16)
+    bm.alloc_seq(0, 70)                                   # blocks 0..4, positions 0..69
+    assert bm.trim_window(0, 40) == 1                     # window [30, 70): block 0 ends at 15
+    assert bm.table(0) == [-1, 1, 2, 3, 4]
+    assert bm.trim_window(0, 40) == 0                     # idempotent
+    assert bm.trim_window(0, 16) == 2                     # window [54, 70): blocks 1, 2 die
+    assert bm.table(0) == [-1, -1, -1, 3, 4]
+    assert bm.num_free() == 11 + 3
+    assert bm.trim_window(0, 1000) == 0                   # window longer than the context
+    slot, cow = bm.append_slot(0)                         # growth is unaffected
+    assert slot == 4 * 16 + 6 and cow is None
+    bm.fork(0, 1)
+    assert [bm.ref_count(b) for b in (3, 4)] == [2, 2]
+    with pytest.raises(ValueError):
+        bm.make_private(1, 0)
+    bm.free_seq(0)
+    bm.free_seq(1)
+    assert bm.num_free() == 16
+    bm.check()
+
+
+def test_native_sliding_window_matches_the_model():
+    rng = random.Random(5)
+    bm, model = pkv.BlockManager(48), BlockManagerModel(48)
+    live, nxt = [], 0
+    for step in range(3000):
+        op = rng.random()
+        if op < 0.15 or not live:
+            n = rng.randrange(0, 120)
+            try:
+                model.alloc_seq(nxt, n)
+                ok = True
+            except NoBlocks:
+                ok = False
+            if ok:
+                bm.alloc_seq(nxt, n)
+                live.append(nxt)
+            else:
+                with pytest.raises(pkv.PagedKVError):
+                    bm.alloc_seq(nxt, n)
+            nxt += 1
+        elif op < 0.35:
+            s, w = rng.choice(live), rng.randrange(1, 80)
+            assert bm.trim_window(s, w) == model.trim_window(s, w)
+        elif op < 0.45:
+            s = rng.choice(live)
+            model.fork(s, nxt)
+            bm.fork(s, nxt)
+            live.append(nxt)
+            nxt += 1
+        elif op < 0.8:
+            s = rng.choice(live)
+            try:
+                want = model.append_slot(s)
+            except NoBlocks:
+                want = None
+            if want is None:
+                with pytest.raises(pkv.PagedKVError):
+                    bm.append_slot(s)
+            else:
+                assert bm.append_slot(s) == want
+        else:
+            s = rng.choice(live)
+            model.free_seq(s)
+            bm.free_seq(s)
+            live.remove(s)
+        if step % 25 == 0:
+            model.check()
+            assert bm.num_free() == model.num_free()
+            for s in live:
+                assert bm.table(s) == model.table(s)
+            for b in range(48):
+                assert bm.ref_count(b) == model.ref_count(b)
