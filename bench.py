@@ -46,29 +46,36 @@ def kv_bytes_per_token(n_layers, n_kv_heads, head_dim, bytes_per_elem=2) -> int:
     return 2 * n_layers * n_kv_heads * head_dim * bytes_per_elem
 
 
-def decode_algorithmic_bytes(wl: W.Workload, lens=None, kv_elem_bytes=None) -> dict:
-    """Least bytes one decode call moves: K/V of every context token, Q, O, tables, lengths."""
+def _window_range(L, window):
+    """Positions [start, L) a decode attends to (all of them when window is 0)."""
+    return (L - window if (window and L > window) else 0), L
+
+
+def decode_algorithmic_bytes(wl: W.Workload, lens=None, kv_elem_bytes=None, window=0) -> dict:
+    """Least bytes one decode call moves: K/V of every attended context token, Q, O,
+    the table entries of the attended blocks, lengths."""
     lens = wl.step_context_lens if lens is None else np.asarray(lens)
     lens = lens.astype(np.int64)
     e = wl.elem_bytes
-    kv = int(lens.sum()) * kv_bytes_per_token(1, wl.num_kv_heads, wl.head_dim,
-                                              kv_elem_bytes or e)
+    rows = sum(L - _window_range(int(L), window)[0] for L in lens)
+    blocks = sum(-(-int(L) // 16) - _window_range(int(L), window)[0] // 16 for L in lens)
+    kv = int(rows) * kv_bytes_per_token(1, wl.num_kv_heads, wl.head_dim, kv_elem_bytes or e)
     q = wl.num_seqs * wl.num_q_heads * wl.head_dim * e
-    tables = int((-(-lens // 16)).sum()) * 4 + 4 * wl.num_seqs
+    tables = int(blocks) * 4 + 4 * wl.num_seqs
     return {"kv": kv, "q": q, "o": q, "tables": tables, "total": kv + 2 * q + tables}
 
 
-def unique_kv_bytes(wl: W.Workload, lens=None, kv_elem_bytes=None) -> int:
+def unique_kv_bytes(wl: W.Workload, lens=None, kv_elem_bytes=None, window=0) -> int:
     """K/V bytes of distinct (block, slot) pairs read: shared prefix blocks count once."""
     lens = wl.step_context_lens if lens is None else np.asarray(lens)
-    seen = {}
+    slots = []
     for b in range(wl.num_seqs):
-        L = int(lens[b])
-        for j in range(-(-L // 16)):
-            phys = int(wl.block_tables[b, j])
-            seen[phys] = max(seen.get(phys, 0), min(16, L - 16 * j))
-    return sum(seen.values()) * kv_bytes_per_token(1, wl.num_kv_heads, wl.head_dim,
-                                                   kv_elem_bytes or wl.elem_bytes)
+        start, L = _window_range(int(lens[b]), window)
+        t = np.arange(start, L, dtype=np.int64)
+        slots.append(wl.block_tables[b, t // 16].astype(np.int64) * 16 + t % 16)
+    n = np.unique(np.concatenate(slots)).size if slots else 0
+    return n * kv_bytes_per_token(1, wl.num_kv_heads, wl.head_dim,
+                                          kv_elem_bytes or wl.elem_bytes)
 
 
 def step_write_bytes(wl: W.Workload) -> int:
@@ -244,11 +251,12 @@ def measured_traffic(workload: str):
 class StepOps:
     """The library calls of one step for bf16 (or f32) pools or FP8 pools."""
 
-    def __init__(self, pkv, wl, kc, vc, ks, vs, P, ws, n_prefix=0):
+    def __init__(self, pkv, wl, kc, vc, ks, vs, P, ws, n_prefix=0, window=0):
         self.pkv, self.wl, self.kc, self.vc, self.ks, self.vs = pkv, wl, kc, vc, ks, vs
         self.P, self.ws = P, ws
         self.fp8 = ks is not None
         self.n_prefix = n_prefix          # > 0: shared-prefix (cascade) decode
+        self.window = window              # > 0: sliding-window decode
 
     def write(self, kn, vn, slots):
         if self.fp8:
@@ -257,7 +265,11 @@ class StepOps:
             self.pkv.cache_write(self.kc, self.vc, kn, vn, slots)
 
     def decode(self, q, bt, lens, out):
-        if self.n_prefix:
+        if self.window:
+            self.pkv.decode_sliding_window(q, self.kc, self.vc, bt, lens, self.window,
+                                           self.wl.scale, k_scales=self.ks, v_scales=self.vs,
+                                           out=out, partition_size=self.P, workspace=self.ws)
+        elif self.n_prefix:
             self.pkv.decode_shared_prefix(q, self.kc, self.vc, bt, lens, self.n_prefix,
                                           self.wl.scale, out=out, partition_size=self.P,
                                           workspace=self.ws)
@@ -303,7 +315,13 @@ def run_gpu(args):
                      dtype=torch.uint8, device=dev)
     stream = torch.cuda.current_stream(dev)
     n_prefix = 0
-    if args.decode != "plain" and not fp8:
+    window = args.window
+    if window:
+        P = args.partition_size
+        ws = torch.empty(max(pkv.lib().pa_decode_sliding_window_workspace_bytes(
+            wl.num_seqs, wl.num_q_heads, wl.num_kv_heads, wl.head_dim, wl.max_blocks, 16, window,
+            P, 2 if fp8 else (1 if wl.dtype == "bf16" else 0)), 16), dtype=torch.uint8, device=dev)
+    elif args.decode != "plain" and not fp8:
         n_prefix = pkv.shared_prefix_blocks(wl.block_tables)
         if args.decode == "auto" and n_prefix < 4:
             n_prefix = 0
@@ -312,7 +330,7 @@ def run_gpu(args):
         ws = torch.empty(max(pkv.lib().pa_decode_shared_prefix_workspace_bytes(
             wl.num_seqs, wl.num_q_heads, wl.num_kv_heads, wl.head_dim, wl.max_blocks, n_prefix,
             P), 16), dtype=torch.uint8, device=dev)
-    ops = StepOps(pkv, wl, kc, vc, ks, vs, P, ws, n_prefix)
+    ops = StepOps(pkv, wl, kc, vc, ks, vs, P, ws, n_prefix, window)
 
     def step(ev_pre=None, ev_post=None):
         ops.write(kn, vn, slots)
@@ -369,8 +387,8 @@ def run_gpu(args):
     if rank != 0:
         return None
     kv_e = 1 if fp8 else None
-    logical = decode_algorithmic_bytes(wl, kv_elem_bytes=kv_e)
-    unique_kv = unique_kv_bytes(wl, kv_elem_bytes=kv_e)
+    logical = decode_algorithmic_bytes(wl, kv_elem_bytes=kv_e, window=window)
+    unique_kv = unique_kv_bytes(wl, kv_elem_bytes=kv_e, window=window)
     hbm_bytes = logical["total"] - logical["kv"] + unique_kv
     peak, peak_kind = load_peaks()
     achieved = hbm_bytes / (decode_ms * 1e-3) / 1e9
@@ -389,7 +407,7 @@ def run_gpu(args):
         "vs_baseline": None,
         "dtype": "fp8_e4m3 K/V, bf16 Q/O" if fp8 else wl.dtype,
         "data": "synthetic (seeded; N(0, %g) values, shuffled block pool)" % wl.value_std,
-        "config": workload_config(wl, P, world, kv_dtype),
+        "config": workload_config(wl, P, world, kv_dtype, window),
         "decode_ms": decode_ms,
         "ms_per_step_with_call_events": ms_step_with_events,
         "kv_gbs": unique_kv / (decode_ms * 1e-3) / 1e9,
@@ -397,10 +415,14 @@ def run_gpu(args):
         "context_tokens_per_s": float(wl.step_context_lens.sum()) * world / (ms_per_step * 1e-3),
         "hbm_frac_of_measured": achieved / peak if peak_kind == "measured" else None,
         "hbm_frac_of_nominal_7900": achieved / NOMINAL_HBM_GBS,
-        "decode_method": (f"shared-prefix cascade ({n_prefix} shared blocks read once per KV "
-                          "head; prefix, suffix and merge kernels)") if n_prefix else "paged decode",
+        "decode_method": (f"sliding window of the last {window} positions" if window else
+                          (f"shared-prefix cascade ({n_prefix} shared blocks read once per KV "
+                           "head; prefix, suffix and merge kernels)") if n_prefix
+                          else "paged decode"),
         "roofline": {
-            "kernel": ("pa_decode_shared_prefix call (prefix + suffix + merge kernels)" if n_prefix
+            "kernel": ("pa_decode_sliding_window call (partition kernel, plus the merge kernel "
+                       "when a window spans several partitions)" if window else
+                       "pa_decode_shared_prefix call (prefix + suffix + merge kernels)" if n_prefix
                        else "pa_decode call (partition kernel, plus the merge kernel when a "
                             "sequence spans several partitions)"),
             "bound": "hbm",
@@ -424,15 +446,16 @@ def run_gpu(args):
         line["unique_kv_bytes"] = unique_kv
     if not args.no_cpu_baseline and world == 1:
         line["cpu_baseline"] = cpu_baseline(args, wl, q, kc, vc, budget_s=args.cpu_seconds,
-                                            ks=ks, vs=vs)
+                                            ks=ks, vs=vs, window=window)
     return line
 
 
-def workload_config(wl, P, world, kv_dtype=None):
+def workload_config(wl, P, world, kv_dtype=None, window=0):
     lens = wl.step_context_lens
     kv_e = 1 if kv_dtype == "fp8" else None
-    return {
-        "workload": wl.name + ("+fp8_kv" if kv_dtype == "fp8" else ""),
+    cfg = {
+        "workload": wl.name + ("+fp8_kv" if kv_dtype == "fp8" else "") +
+                    (f"+window{window}" if window else ""),
         "kv_dtype": kv_dtype or wl.dtype,
         "num_seqs_per_gpu": wl.num_seqs,
         "global_batch": wl.num_seqs * world,
@@ -446,8 +469,11 @@ def workload_config(wl, P, world, kv_dtype=None):
         "cow_pairs_per_step": int(wl.cow_pairs.shape[0]),
         "parallelism": f"weak scaling, {world} independent replica(s)",
         "l2": "inputs larger than L2: %.2f GB of K/V read per step vs 129 MB L2"
-              % (decode_algorithmic_bytes(wl, kv_elem_bytes=kv_e)["kv"] / 1e9),
+              % (decode_algorithmic_bytes(wl, kv_elem_bytes=kv_e, window=window)["kv"] / 1e9),
     }
+    if window:
+        cfg["window"] = window
+    return cfg
 
 
 def run_e2e(args, pkv, wl, q, kc, vc, kn, vn, dev, stream, ops):
@@ -522,7 +548,7 @@ def _bits(t):
     return t.contiguous().cpu().numpy()
 
 
-def cpu_baseline(args, wl, q, kc, vc, budget_s=10.0, ks=None, vs=None):
+def cpu_baseline(args, wl, q, kc, vc, budget_s=10.0, ks=None, vs=None, window=0):
     import torch
     import oracle
     threads = oracle.max_threads()
@@ -537,13 +563,15 @@ def cpu_baseline(args, wl, q, kc, vc, budget_s=10.0, ks=None, vs=None):
     reps = 0
     scales = {} if ks is None else {"k_scales": ks.cpu().numpy(), "v_scales": vs.cpu().numpy()}
     while True:
-        oracle.paged_decode(qh, kch, vch, tabs, lens, wl.scale, threads=threads, **scales)
+        oracle.paged_decode(qh, kch, vch, tabs, lens, wl.scale, threads=threads, window=window,
+                            **scales)
         reps += 1
         if time.perf_counter() - t0 >= budget_s:
             break
     dt = time.perf_counter() - t0
-    # scale the sample's time to the whole batch by context tokens
-    frac = float(lens.sum()) / float(wl.step_context_lens.sum())
+    # scale the sample's time to the whole batch by attended context tokens
+    att = lambda ls: float(sum(min(int(L), window) if window else int(L) for L in ls))
+    frac = att(lens) / att(wl.step_context_lens)
     t_batch = dt / reps / frac
     return {"value": wl.num_seqs / t_batch, "unit": "tokens/s", "cores": threads, "kind": "oracle",
             "sample": f"{n_seq} of {wl.num_seqs} sequences (all {wl.num_q_heads} heads, "
@@ -585,7 +613,7 @@ def run_reference(args):
         scales = {"k_scales": s8, "v_scales": s8}
     for _ in range(args.warmup):
         oracle.paged_decode(qh[:1], kch, vch, tabs[:1], lens[:1], wl.scale, threads=threads,
-                            **scales)
+                            window=args.window, **scales)
     steps = args.steps
     tokens = 0
     ctx = 0
@@ -595,15 +623,16 @@ def run_reference(args):
     for i in range(steps):
         j = i % n_seq
         oracle.paged_decode(qh[j:j + 1], kch, vch, tabs[j:j + 1], lens[j:j + 1], wl.scale,
-                            threads=threads, **scales)
+                            threads=threads, window=args.window, **scales)
         tokens += 1
-        ctx += int(lens[j])
+        ctx += min(int(lens[j]), args.window) if args.window else int(lens[j])
         done += 1
         if time.perf_counter() > deadline:
             break
     dt = time.perf_counter() - t0
     # tokens/s of the whole batch at this rate of context tokens per second
-    batch_ctx = float(wl.step_context_lens.sum())
+    batch_ctx = float(sum(min(int(L), args.window) if args.window else int(L)
+                          for L in wl.step_context_lens))
     value = wl.num_seqs / (batch_ctx / (ctx / dt))
     sample = (f"{done} steps, each one sequence of {n_seq} sampled ({int(lens.sum())} context "
               f"tokens in the sample), all {wl.num_q_heads} heads; rate scaled to the "
@@ -623,7 +652,7 @@ def run_reference(args):
         "dtype": "f64",
         "data": "synthetic (seeded)",
         "config": workload_config(wl, args.partition_size or wl.partition_size or "library choice",
-                                  world, getattr(args, "kv_dtype", "bf16")),
+                                  world, getattr(args, "kv_dtype", "bf16"), args.window),
         "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": threads, "kind": "oracle",
                          "sample": sample},
         "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0,
@@ -638,6 +667,8 @@ def main(argv=None):
     ap.add_argument("--warmup", type=int, default=50)
     ap.add_argument("--workload", default="llama7b_mha", choices=W.WORKLOADS)
     ap.add_argument("--partition-size", type=int, default=0)
+    ap.add_argument("--window", type=int, default=0,
+                    help="> 0: sliding-window decode over the last WINDOW positions")
     ap.add_argument("--decode", default="auto", choices=["auto", "plain", "shared-prefix"],
                     help="auto: the shared-prefix cascade when every table shares >= 4 leading "
                          "blocks (bf16 pools), else paged decode")
