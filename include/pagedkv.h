@@ -317,6 +317,37 @@ pa_status pa_block_copy(void *key_cache, void *value_cache, const int32_t *src_d
                         pa_dtype dtype, int32_t *device_status, void *stream);
 
 /*
+ * Swap of blocks between the pools and a staging buffer ("PagedAttention por
+ * dentro", section "Evicción y preemption", strategy 2 "swap": the blocks of
+ * a preempted sequence move to CPU memory, freeing device memory, and come
+ * back when it is scheduled again).
+ *  block_ids    device int32 [num_ids]: physical blocks, in staging order
+ *  staging      [num_ids][2][num_kv_heads][16][head_dim] elements of dtype:
+ *               entry i holds block_ids[i]'s K tile, then its V tile (all KV
+ *               heads), pa_swap_bytes(num_ids, ...) bytes in all.  Any
+ *               device-accessible address, 16-byte aligned: device memory of
+ *               the current device, managed memory, or page-locked host memory
+ *               (cudaHostAlloc / cudaMallocHost / cudaHostRegister; the host
+ *               pointer is passed and the library uses its device mapping),
+ *               which the kernel reads or writes directly over the CPU-GPU
+ *               link.  Other addresses (pageable host memory, another device's
+ *               memory) return PA_ERR_INVALID_ARG.
+ * pa_swap_out copies the listed blocks (both pools) into staging; pa_swap_in
+ * copies staging into the listed blocks.  Bit copies.  For pa_swap_in the ids
+ * must be distinct.  An id outside [0, num_blocks) is skipped and flagged
+ * PA_DEV_BAD_BLOCK_ID.  One kernel launch each; the caller owns both sides and
+ * orders them with the stream (the staging buffer is complete once the stream
+ * reaches the point after pa_swap_out).
+ */
+size_t pa_swap_bytes(int num_ids, int num_kv_heads, int head_dim, pa_dtype dtype);
+pa_status pa_swap_out(const void *key_cache, const void *value_cache, const int32_t *block_ids,
+                      int num_ids, void *staging, int num_kv_heads, int head_dim, int block_size,
+                      int num_blocks, pa_dtype dtype, int32_t *device_status, void *stream);
+pa_status pa_swap_in(void *key_cache, void *value_cache, const int32_t *block_ids, int num_ids,
+                     const void *staging, int num_kv_heads, int head_dim, int block_size,
+                     int num_blocks, pa_dtype dtype, int32_t *device_status, void *stream);
+
+/*
  * Host block manager: one pool of num_blocks blocks of block_size tokens,
  * per-sequence block tables, reference counts and copy-on-write.
  * Source: "PagedAttention por dentro", sections "La tabla de páginas (block
@@ -374,6 +405,19 @@ int pa_bm_register_prefix(pa_bm *bm, int seq, const int32_t *tokens, int num_tok
  * smaller one; forks share only its remaining blocks, and pa_bm_make_private
  * of a released entry returns PA_ERR_INVALID_ARG. */
 int pa_bm_trim_window(pa_bm *bm, int seq, int window);
+/* Swap bookkeeping ("PagedAttention por dentro", section "Evicción y
+ * preemption", strategy "swap").  pa_bm_swap_out lists seq's blocks in table
+ * order (skipping entries released by pa_bm_trim_window) into block_ids (cap
+ * entries; *num_ids receives the count), releases them (last entry first) and
+ * marks seq swapped: its live entries read -2.  A swapped sequence can only be
+ * swapped in, freed or queried.  pa_bm_swap_in takes fresh blocks for its -2
+ * entries in table order (all or nothing: PA_ERR_NO_BLOCKS) and writes them,
+ * in that order, to block_ids - the order pa_swap_out's staging holds them
+ * in.  Sharing with other sequences is not restored: every block swapped in
+ * is private.  PA_ERR_INVALID_ARG for a sequence in the wrong state or a cap
+ * that is too small (nothing changes then). */
+pa_status pa_bm_swap_out(pa_bm *bm, int seq, int32_t *block_ids, int cap, int *num_ids);
+pa_status pa_bm_swap_in(pa_bm *bm, int seq, int32_t *block_ids, int cap, int *num_ids);
 int pa_bm_num_tokens(const pa_bm *bm, int seq);       /* -1 if unknown */
 int pa_bm_ref_count(const pa_bm *bm, int block);      /* -1 if out of range */
 /* Copies up to cap entries of seq's table to out; returns its length, -1 if unknown. */

@@ -225,3 +225,32 @@ def block_copy(key_cache, value_cache, pairs) -> None:
                             Hkv, D, BS, NB, key_cache.itemsize)
     if rc != 0:
         raise ValueError(f"oracle block_copy failed with code {rc}")
+
+
+def swap_out(key_cache, value_cache, block_ids) -> np.ndarray:
+    """Preemption by swap ("PagedAttention por dentro", section "Evicción y
+    preemption", strategy "swap"): the listed blocks copied out, in order, as
+    staging[i] = (K tile of block_ids[i], V tile of block_ids[i]) over all KV
+    heads; shape [n][2][Hkv][16][D] of the pools' element type."""
+    ids = [int(b) for b in block_ids]
+    NB, Hkv, BS, D = key_cache.shape
+    staging = np.empty((len(ids), 2, Hkv, BS, D), dtype=key_cache.dtype)
+    for i, b in enumerate(ids):
+        if not 0 <= b < NB:
+            raise IndexError(f"block id {b} outside the pool")
+        staging[i, 0] = key_cache[b]
+        staging[i, 1] = value_cache[b]
+    return staging
+
+
+def swap_in(key_cache, value_cache, block_ids, staging) -> None:
+    """Inverse of ``swap_out``: staging[i] goes back into block block_ids[i] (in place)."""
+    ids = [int(b) for b in block_ids]
+    NB = key_cache.shape[0]
+    if len(set(ids)) != len(ids):
+        raise ValueError("swap-in block ids must be distinct")
+    for i, b in enumerate(ids):
+        if not 0 <= b < NB:
+            raise IndexError(f"block id {b} outside the pool")
+        key_cache[b] = staging[i, 0]
+        value_cache[b] = staging[i, 1]

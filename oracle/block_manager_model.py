@@ -84,6 +84,7 @@ class BlockManagerModel:
         self.block_key: dict[int, int] = {}       # block -> key
         self.block_tokens: dict[int, tuple] = {}  # block -> its 16 tokens
         self.evictable: list[int] = []            # released keyed blocks, oldest first
+        self.swapped: set[int] = set()            # sequences whose blocks are swapped out
 
     # -- queries ---------------------------------------------------------
     def num_free(self) -> int:
@@ -128,6 +129,10 @@ class BlockManagerModel:
             else:
                 self.free.append(b)
 
+    def _live(self, seq: int) -> None:
+        if seq in self.swapped:
+            raise ValueError("sequence is swapped out")
+
     def alloc_seq_cached(self, seq: int, tokens) -> int:
         """New sequence holding ``tokens``: its leading full blocks are taken from the
         prefix cache where they match; returns how many tokens were found cached."""
@@ -160,6 +165,7 @@ class BlockManagerModel:
         """Index the sequence's full blocks by key (their K/V are now written);
         returns how many blocks were newly indexed."""
         table = self.tables[seq]
+        self._live(seq)
         n = min(len(tokens), self.tokens[seq])
         added, parent = 0, 0
         for j in range(n // self.block_size):
@@ -189,6 +195,7 @@ class BlockManagerModel:
         """The child shares every block of the parent (reference counts + 1)."""
         if parent not in self.tables or child in self.tables:
             raise ValueError("bad fork")
+        self._live(parent)
         self.tables[child] = list(self.tables[parent])
         self.tokens[child] = self.tokens[parent]
         for b in self.tables[child]:
@@ -198,6 +205,7 @@ class BlockManagerModel:
     def make_private(self, seq: int, logical_block: int):
         """Copy-on-write of one logical block; returns (src, dst) or None if private."""
         table = self.tables[seq]
+        self._live(seq)
         old = table[logical_block]
         if old < 0:
             raise ValueError("block released by trim_window")
@@ -211,6 +219,7 @@ class BlockManagerModel:
     def append_slot(self, seq: int):
         """Room for one more token.  Returns (slot, cow) where cow is (src, dst) or None."""
         table = self.tables[seq]
+        self._live(seq)
         n = self.tokens[seq]
         cow = None
         if n % self.block_size == 0:
@@ -224,6 +233,7 @@ class BlockManagerModel:
     def free_seq(self, seq: int) -> None:
         table = self.tables.pop(seq)
         del self.tokens[seq]
+        self.swapped.discard(seq)
         for b in reversed(table):
             if b >= 0:
                 self._release(b)
@@ -236,6 +246,7 @@ class BlockManagerModel:
         if window <= 0 or seq not in self.tables:
             raise ValueError("bad trim")
         table = self.tables[seq]
+        self._live(seq)
         n = self.tokens[seq]
         dead = (n - window) // self.block_size if n > window else 0
         released = 0
@@ -245,6 +256,36 @@ class BlockManagerModel:
                 table[j] = -1
                 released += 1
         return released
+
+    def swap_out(self, seq: int) -> list[int]:
+        """Preemption by swap ("PagedAttention por dentro", section "Evicción y
+        preemption"): returns the sequence's blocks in table order, releases them
+        (last entry first) and marks their entries -2."""
+        table = self.tables[seq]
+        self._live(seq)
+        ids = [b for b in table if b >= 0]
+        for j in range(len(table) - 1, -1, -1):
+            if table[j] >= 0:
+                self._release(table[j])
+                table[j] = -2
+        self.swapped.add(seq)
+        return ids
+
+    def swap_in(self, seq: int) -> list[int]:
+        """Fresh private blocks for the -2 entries, in table order (all or nothing)."""
+        if seq not in self.swapped:
+            raise ValueError("sequence is not swapped out")
+        table = self.tables[seq]
+        need = sum(1 for b in table if b == -2)
+        if need > len(self.free) + len(self.evictable):
+            raise NoBlocks()
+        ids = []
+        for j, b in enumerate(table):
+            if b == -2:
+                table[j] = self._take()
+                ids.append(table[j])
+        self.swapped.discard(seq)
+        return ids
 
     # -- invariants ------------------------------------------------------
     def check(self) -> None:

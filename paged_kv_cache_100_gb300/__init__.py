@@ -25,7 +25,7 @@ from ._lib import PagedKVError, check, lib  # noqa: F401
 
 BLOCK_SIZE = 16
 
-__all__ = ["decode", "decode_fp8", "decode_sliding_window", "decode_shared_prefix", "shared_prefix_blocks", "decode_workspace_bytes", "decode_partition_size",
+__all__ = ["swap_out", "swap_in", "decode", "decode_fp8", "decode_sliding_window", "decode_shared_prefix", "shared_prefix_blocks", "decode_workspace_bytes", "decode_partition_size",
            "cache_write", "cache_write_fp8", "block_copy", "launch_count", "BlockManager",
            "PagedKVError", "BLOCK_SIZE", "library_path"]
 
@@ -347,6 +347,53 @@ def block_copy(key_cache, value_cache, src_dst, *, status=None, stream=None):
     check(rc, "pa_block_copy")
 
 
+def _staging_ptr(t, nbytes):
+    """Device-accessible staging: a CUDA tensor or a page-locked host tensor."""
+    if not (t.is_cuda or t.is_pinned()):
+        raise ValueError("staging must be a CUDA tensor or page-locked host memory")
+    if not t.is_contiguous():
+        raise ValueError("staging must be contiguous")
+    if t.numel() * t.element_size() < nbytes:
+        raise ValueError("staging is too small")
+    return t.data_ptr()
+
+
+def _swap_geometry(key_cache, block_ids):
+    torch = _torch()
+    NB, Hkv, BS, D = key_cache.shape
+    if block_ids.dim() != 1:
+        raise ValueError("block_ids must be [num_ids]")
+    code = _lib.PA_DTYPE_FP8_E4M3 if _is_fp8(key_cache) else _dtype_code(key_cache)
+    n = block_ids.shape[0]
+    nbytes = lib().pa_swap_bytes(n, Hkv, D, code)
+    return NB, Hkv, BS, D, code, n, nbytes, _dev(block_ids, "block_ids", torch.int32)
+
+
+def swap_out(key_cache, value_cache, block_ids, staging=None, *, status=None, stream=None):
+    """Copy the listed blocks (both pools) into ``staging`` ``[n][2][Hkv][16][D]``
+    (``pa_swap_out``).  By default the staging is new page-locked host memory,
+    written by the kernel over the CPU-GPU link; returns it (complete once the
+    stream reaches this point)."""
+    torch = _torch()
+    NB, Hkv, BS, D, code, n, nbytes, ids = _swap_geometry(key_cache, block_ids)
+    if staging is None:
+        staging = torch.empty((n, 2, Hkv, BS, D), dtype=key_cache.dtype, pin_memory=True)
+    rc = lib().pa_swap_out(_dev(key_cache, "key_cache"), _dev(value_cache, "value_cache"), ids,
+                           n, _staging_ptr(staging, nbytes), Hkv, D, BS, NB, code,
+                           _status_ptr(status), _stream(stream, key_cache.device))
+    check(rc, "pa_swap_out")
+    return staging
+
+
+def swap_in(key_cache, value_cache, block_ids, staging, *, status=None, stream=None):
+    """Copy ``staging`` back into the listed blocks (``pa_swap_in``); ids distinct."""
+    NB, Hkv, BS, D, code, n, nbytes, ids = _swap_geometry(key_cache, block_ids)
+    rc = lib().pa_swap_in(_dev(key_cache, "key_cache"), _dev(value_cache, "value_cache"), ids,
+                          n, _staging_ptr(staging, nbytes), Hkv, D, BS, NB, code,
+                          _status_ptr(status), _stream(stream, key_cache.device))
+    check(rc, "pa_swap_in")
+
+
 class BlockManager:
     """Host block manager (``pa_bm_*``): pool, block tables, ref counts, copy-on-write."""
 
@@ -422,6 +469,26 @@ class BlockManager:
         if n < 0:
             raise KeyError(seq)
         return int(n)
+
+    def swap_out(self, seq: int) -> list:
+        """Release the sequence's blocks for a swap; returns them in staging order."""
+        import numpy as np
+        cap = max(1, len(self.table(seq)))
+        ids = np.empty(cap, dtype=np.int32)
+        n = ctypes.c_int()
+        check(lib().pa_bm_swap_out(self._h, seq, ids.ctypes.data, cap, ctypes.byref(n)),
+              "pa_bm_swap_out")
+        return ids[:n.value].tolist()
+
+    def swap_in(self, seq: int) -> list:
+        """Fresh blocks for a swapped-out sequence, in staging order."""
+        import numpy as np
+        cap = max(1, len(self.table(seq)))
+        ids = np.empty(cap, dtype=np.int32)
+        n = ctypes.c_int()
+        check(lib().pa_bm_swap_in(self._h, seq, ids.ctypes.data, cap, ctypes.byref(n)),
+              "pa_bm_swap_in")
+        return ids[:n.value].tolist()
 
     def num_tokens(self, seq: int) -> int:
         n = lib().pa_bm_num_tokens(self._h, seq)

@@ -48,6 +48,9 @@ SIGNATURES = {
     "pa_decode_sliding_window": (i32, [vp, vp, vp, vp, vp, vp, vp, vp, i32, i32, i32, i32, i32,
                                        i32, i32, f32, i32, i32, i32, vp, sz, vp, vp]),
     "pa_cache_write_fp8": (i32, [vp, vp, vp, vp, vp, vp, vp, i32, i32, i32, i32, i32, vp, vp]),
+    "pa_swap_bytes": (sz, [i32, i32, i32, i32]),
+    "pa_swap_out": (i32, [vp, vp, vp, i32, vp, i32, i32, i32, i32, i32, vp, vp]),
+    "pa_swap_in": (i32, [vp, vp, vp, i32, vp, i32, i32, i32, i32, i32, vp, vp]),
     "pa_cache_write": (i32, [vp, vp, vp, vp, vp, i32, i32, i32, i32, i32, i32, vp, vp]),
     "pa_block_copy": (i32, [vp, vp, vp, i32, i32, i32, i32, i32, i32, vp, vp]),
     "pa_bm_create": (vp, [i32, i32]),
@@ -62,6 +65,8 @@ SIGNATURES = {
     "pa_bm_alloc_seq_cached": (i32, [vp, i32, vp, i32, ptr_int]),
     "pa_bm_register_prefix": (i32, [vp, i32, vp, i32]),
     "pa_bm_trim_window": (i32, [vp, i32, i32]),
+    "pa_bm_swap_out": (i32, [vp, i32, vp, i32, ptr_int]),
+    "pa_bm_swap_in": (i32, [vp, i32, vp, i32, ptr_int]),
     "pa_bm_num_tokens": (i32, [vp, i32]),
     "pa_bm_ref_count": (i32, [vp, i32]),
     "pa_bm_table": (i32, [vp, i32, vp, i32]),

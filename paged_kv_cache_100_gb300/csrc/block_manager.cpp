@@ -67,8 +67,9 @@ struct pa_bm {
     std::vector<int32_t> free_stack;   // back() is handed out next
     std::vector<int32_t> ref;
     struct Seq {
-        std::vector<int32_t> table;
+        std::vector<int32_t> table;   // -1: released by a window trim; -2: swapped out
         int64_t tokens = 0;
+        bool swapped = false;
     };
     std::unordered_map<int, Seq> seqs;
     // prefix cache
@@ -148,6 +149,7 @@ extern "C" pa_status pa_bm_fork(pa_bm *bm, int parent, int child) {
     if (bm == nullptr) return PA_ERR_INVALID_ARG;
     auto it = bm->seqs.find(parent);
     if (it == bm->seqs.end() || bm->seqs.count(child)) return PA_ERR_NOT_FOUND;
+    if (it->second.swapped) return PA_ERR_INVALID_ARG;
     pa_bm::Seq s = it->second;
     for (int32_t b : s.table)
         if (b >= 0) bm->ref[b] += 1;   // -1: released by pa_bm_trim_window
@@ -177,7 +179,8 @@ extern "C" pa_status pa_bm_make_private(pa_bm *bm, int seq, int logical_block, i
     if (bm == nullptr || cow_src == nullptr || cow_dst == nullptr) return PA_ERR_INVALID_ARG;
     auto it = bm->seqs.find(seq);
     if (it == bm->seqs.end()) return PA_ERR_NOT_FOUND;
-    if (logical_block < 0 || (size_t)logical_block >= it->second.table.size())
+    if (logical_block < 0 || (size_t)logical_block >= it->second.table.size() ||
+        it->second.swapped)
         return PA_ERR_INVALID_ARG;
     return make_private(bm, it->second, logical_block, cow_src, cow_dst);
 }
@@ -189,6 +192,7 @@ extern "C" pa_status pa_bm_append_slot(pa_bm *bm, int seq, int64_t *slot, int32_
     auto it = bm->seqs.find(seq);
     if (it == bm->seqs.end()) return PA_ERR_NOT_FOUND;
     pa_bm::Seq &s = it->second;
+    if (s.swapped) return PA_ERR_INVALID_ARG;
     const int64_t n = s.tokens;
     int32_t src = -1, dst = -1;
     if (n % bm->block_size == 0) {
@@ -226,6 +230,7 @@ extern "C" int pa_bm_trim_window(pa_bm *bm, int seq, int window) {
     auto it = bm->seqs.find(seq);
     if (it == bm->seqs.end()) return -1;
     pa_bm::Seq &s = it->second;
+    if (s.swapped) return -1;
     const int64_t dead = s.tokens > window ? (s.tokens - window) / bm->block_size : 0;
     int released = 0;
     for (int64_t j = dead; j-- > 0;) {
@@ -285,7 +290,7 @@ extern "C" pa_status pa_bm_alloc_seq_cached(pa_bm *bm, int seq, const int32_t *t
 extern "C" int pa_bm_register_prefix(pa_bm *bm, int seq, const int32_t *tokens, int num_tokens) {
     if (bm == nullptr || num_tokens < 0 || (num_tokens > 0 && tokens == nullptr)) return -1;
     auto it = bm->seqs.find(seq);
-    if (it == bm->seqs.end()) return -1;
+    if (it == bm->seqs.end() || it->second.swapped) return -1;
     const std::vector<int32_t> &table = it->second.table;
     const int bs = bm->block_size;
     const int64_t n = num_tokens < it->second.tokens ? num_tokens : it->second.tokens;
@@ -358,7 +363,8 @@ extern "C" pa_status pa_bm_fill_tables(const pa_bm *bm, const int32_t *seqs, int
     for (int i = 0; i < n; ++i) {
         auto it = bm->seqs.find(seqs[i]);
         if (it == bm->seqs.end()) return PA_ERR_NOT_FOUND;
-        if (it->second.table.size() > (size_t)max_blocks) return PA_ERR_INVALID_ARG;
+        if (it->second.table.size() > (size_t)max_blocks || it->second.swapped)
+            return PA_ERR_INVALID_ARG;
     }
     for (int i = 0; i < n; ++i) {
         const pa_bm::Seq &s = bm->seqs.find(seqs[i])->second;
@@ -368,5 +374,51 @@ extern "C" pa_status pa_bm_fill_tables(const pa_bm *bm, const int32_t *seqs, int
         for (; j < (size_t)max_blocks; ++j) row[j] = -1;
         context_lens[i] = (int32_t)s.tokens;
     }
+    return PA_OK;
+}
+
+extern "C" pa_status pa_bm_swap_out(pa_bm *bm, int seq, int32_t *block_ids, int cap,
+                                    int *num_ids) {
+    if (bm == nullptr || num_ids == nullptr || cap < 0 || (cap > 0 && block_ids == nullptr))
+        return PA_ERR_INVALID_ARG;
+    auto it = bm->seqs.find(seq);
+    if (it == bm->seqs.end()) return PA_ERR_NOT_FOUND;
+    pa_bm::Seq &s = it->second;
+    if (s.swapped) return PA_ERR_INVALID_ARG;
+    int n = 0;
+    for (int32_t b : s.table) n += b >= 0;
+    if (n > cap) return PA_ERR_INVALID_ARG;
+    int k = 0;
+    for (int32_t b : s.table)
+        if (b >= 0) block_ids[k++] = b;
+    for (size_t i = s.table.size(); i-- > 0;) {
+        if (s.table[i] < 0) continue;
+        bm->release(s.table[i]);
+        s.table[i] = -2;
+    }
+    s.swapped = true;
+    *num_ids = n;
+    return PA_OK;
+}
+
+extern "C" pa_status pa_bm_swap_in(pa_bm *bm, int seq, int32_t *block_ids, int cap, int *num_ids) {
+    if (bm == nullptr || num_ids == nullptr || cap < 0 || (cap > 0 && block_ids == nullptr))
+        return PA_ERR_INVALID_ARG;
+    auto it = bm->seqs.find(seq);
+    if (it == bm->seqs.end()) return PA_ERR_NOT_FOUND;
+    pa_bm::Seq &s = it->second;
+    if (!s.swapped) return PA_ERR_INVALID_ARG;
+    int n = 0;
+    for (int32_t b : s.table) n += b == -2;
+    if (n > cap) return PA_ERR_INVALID_ARG;
+    if ((size_t)n > bm->available()) return PA_ERR_NO_BLOCKS;
+    int k = 0;
+    for (int32_t &b : s.table)
+        if (b == -2) {
+            b = bm->take();
+            block_ids[k++] = b;
+        }
+    s.swapped = false;
+    *num_ids = n;
     return PA_OK;
 }

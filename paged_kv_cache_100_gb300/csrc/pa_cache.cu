@@ -153,6 +153,42 @@ pa_block_copy_kernel(uint4 *__restrict__ kc, uint4 *__restrict__ vc,
     }
 }
 
+// Swap between the pools and a staging buffer laid out [id][K, V][block
+// bytes]: CTA (i, slice, kv) moves one slice of block_ids[i]'s K or V tile.
+// The staging side may be page-locked host memory reached over the
+// CPU-GPU link, so each thread keeps kChunksPerThread 16-byte loads in
+// flight before it stores.
+template <bool kOut>
+__global__ void __launch_bounds__(kCopyThreads)
+pa_swap_kernel(uint4 *__restrict__ kc, uint4 *__restrict__ vc, uint4 *__restrict__ stage,
+               const int32_t *__restrict__ block_ids, int64_t chunks_per_block, int num_blocks,
+               int32_t *status) {
+    grid_dependency_wait();
+    grid_dependents_launch();
+    const int32_t id = block_ids[blockIdx.x];
+    if ((unsigned)id >= (unsigned)num_blocks) {
+        if (blockIdx.y == 0 && blockIdx.z == 0 && threadIdx.x == 0)
+            report(status, PA_DEV_BAD_BLOCK_ID);
+        return;
+    }
+    uint4 *pool = (blockIdx.z == 0 ? kc : vc) + (int64_t)id * chunks_per_block;
+    uint4 *st = stage + ((int64_t)blockIdx.x * 2 + blockIdx.z) * chunks_per_block;
+    const uint4 *from = kOut ? pool : st;
+    uint4 *to = kOut ? st : pool;
+    const int64_t first = (int64_t)blockIdx.y * kCopyThreads * kChunksPerThread + threadIdx.x;
+    uint4 buf[kChunksPerThread];
+#pragma unroll
+    for (int u = 0; u < kChunksPerThread; ++u) {
+        const int64_t c = first + (int64_t)u * kCopyThreads;
+        if (c < chunks_per_block) buf[u] = from[c];
+    }
+#pragma unroll
+    for (int u = 0; u < kChunksPerThread; ++u) {
+        const int64_t c = first + (int64_t)u * kCopyThreads;
+        if (c < chunks_per_block) to[c] = buf[u];
+    }
+}
+
 int elem_bytes(pa_dtype dtype) {
     return dtype == PA_DTYPE_F32 ? 4 : (dtype == PA_DTYPE_BF16 ? 2 : 1);
 }
@@ -279,4 +315,99 @@ extern "C" pa_status pa_cache_write_fp8(void *key_cache, void *value_cache, cons
     if (e != cudaSuccess) return cuda_failure(e, "pa_cache_write_fp8_kernel launch");
     count_launches(1);
     return PA_OK;
+}
+
+namespace {
+
+// The address a kernel on the current device uses for p: device memory of this
+// device and managed memory as they are, page-locked host memory through its
+// mapping.  Anything else (pageable host memory, another device's memory) is
+// refused, so that no kernel dereferences an address it cannot reach.
+pa_status device_address(const void *p, void **dev) {
+    cudaPointerAttributes at;
+    cudaError_t e = cudaPointerGetAttributes(&at, p);
+    if (e != cudaSuccess) {
+        (void)cudaGetLastError();
+        return PA_ERR_INVALID_ARG;
+    }
+    int cur = 0;
+    e = cudaGetDevice(&cur);
+    if (e != cudaSuccess) return cuda_failure(e, "cudaGetDevice");
+    switch (at.type) {
+    case cudaMemoryTypeDevice:
+        if (at.device != cur) return PA_ERR_INVALID_ARG;
+        *dev = const_cast<void *>(p);
+        return PA_OK;
+    case cudaMemoryTypeManaged:
+        *dev = const_cast<void *>(p);
+        return PA_OK;
+    case cudaMemoryTypeHost:
+        if (at.devicePointer == nullptr) return PA_ERR_INVALID_ARG;
+        *dev = at.devicePointer;
+        return PA_OK;
+    default:
+        return PA_ERR_INVALID_ARG;
+    }
+}
+
+pa_status swap_common(bool out, void *key_cache, void *value_cache, const int32_t *block_ids,
+                      int num_ids, void *staging, int num_kv_heads, int head_dim, int block_size,
+                      int num_blocks, pa_dtype dtype, int32_t *device_status, void *stream) {
+    if (num_ids < 0 || num_kv_heads <= 0 || head_dim <= 0 || block_size != kBlockSize ||
+        num_blocks <= 0)
+        return PA_ERR_INVALID_ARG;
+    if (dtype != PA_DTYPE_F32 && dtype != PA_DTYPE_BF16 && dtype != PA_DTYPE_FP8_E4M3)
+        return PA_ERR_INVALID_ARG;
+    const int64_t block_bytes = (int64_t)num_kv_heads * kBlockSize * head_dim * elem_bytes(dtype);
+    if (block_bytes % 16 != 0) return PA_ERR_UNSUPPORTED;
+    if (num_ids == 0) return PA_OK;
+    if (!key_cache || !value_cache || !block_ids || !staging) return PA_ERR_INVALID_ARG;
+    if (!aligned16(key_cache) || !aligned16(value_cache) || !aligned16(staging) ||
+        (reinterpret_cast<uintptr_t>(block_ids) & 3u))
+        return PA_ERR_INVALID_ARG;
+    void *stage = nullptr;
+    pa_status st = device_address(staging, &stage);
+    if (st != PA_OK) return st;
+    if (!aligned16(stage)) return PA_ERR_INVALID_ARG;
+    const int64_t chunks = block_bytes / 16;
+    const int64_t per_cta = (int64_t)kCopyThreads * kChunksPerThread;
+    const int64_t slices = (chunks + per_cta - 1) / per_cta;
+    if (slices > 65535) return PA_ERR_UNSUPPORTED;
+    dim3 grid((unsigned)num_ids, (unsigned)slices, 2);
+    auto kernel = out ? pa_swap_kernel<true> : pa_swap_kernel<false>;
+    cudaError_t e = launch_chained(kernel, grid, dim3(kCopyThreads), 0,
+                                   static_cast<cudaStream_t>(stream),
+                                   static_cast<uint4 *>(key_cache), static_cast<uint4 *>(value_cache),
+                                   static_cast<uint4 *>(stage), block_ids, chunks, num_blocks,
+                                   device_status);
+    if (e != cudaSuccess) return cuda_failure(e, "pa_swap_kernel launch");
+    count_launches(1);
+    return PA_OK;
+}
+
+}  // namespace
+
+extern "C" size_t pa_swap_bytes(int num_ids, int num_kv_heads, int head_dim, pa_dtype dtype) {
+    if (num_ids < 0 || num_kv_heads <= 0 || head_dim <= 0 ||
+        (dtype != PA_DTYPE_F32 && dtype != PA_DTYPE_BF16 && dtype != PA_DTYPE_FP8_E4M3))
+        return (size_t)-1;
+    return (size_t)num_ids * 2 * num_kv_heads * kBlockSize * head_dim * elem_bytes(dtype);
+}
+
+extern "C" pa_status pa_swap_out(const void *key_cache, const void *value_cache,
+                                 const int32_t *block_ids, int num_ids, void *staging,
+                                 int num_kv_heads, int head_dim, int block_size, int num_blocks,
+                                 pa_dtype dtype, int32_t *device_status, void *stream) {
+    return swap_common(true, const_cast<void *>(key_cache), const_cast<void *>(value_cache),
+                       block_ids, num_ids, staging, num_kv_heads, head_dim, block_size,
+                       num_blocks, dtype, device_status, stream);
+}
+
+extern "C" pa_status pa_swap_in(void *key_cache, void *value_cache, const int32_t *block_ids,
+                                int num_ids, const void *staging, int num_kv_heads, int head_dim,
+                                int block_size, int num_blocks, pa_dtype dtype,
+                                int32_t *device_status, void *stream) {
+    return swap_common(false, key_cache, value_cache, block_ids, num_ids,
+                       const_cast<void *>(staging), num_kv_heads, head_dim, block_size,
+                       num_blocks, dtype, device_status, stream);
 }

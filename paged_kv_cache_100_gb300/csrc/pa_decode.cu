@@ -1677,6 +1677,11 @@ bool plan_decode(int num_seqs, int num_q_heads, int num_kv_heads, int max_blocks
     if (p < 0) return false;
     *part_blocks = p / kBlockSize;
     *max_parts = std::max(1, (span + *part_blocks - 1) / *part_blocks);
+    // Every sequence longer than a window covers the same number of blocks
+    // (span or span - 1): spread them evenly over the partitions instead of
+    // leaving a last partition of a block or two.
+    if (window > 0 && partition_size == 0 && *max_parts > 1)
+        *part_blocks = (span + *max_parts - 1) / *max_parts;
     return true;
 }
 
