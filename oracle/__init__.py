@@ -1,4 +1,5 @@
-"""Oracle for paged decode attention, cache write, block copy and the block manager.
+"""Oracle for paged decode attention, chunked prefill, cache write, block copy, swap
+and the block manager.
 
 TEST INFRASTRUCTURE ONLY.  Only ``tests/``, ``__graft_entry__.smoke()`` and the
 CPU-baseline / reference legs of ``bench.py`` may import this package.  The
@@ -73,6 +74,9 @@ def _load():
             lib.pao_cache_write.restype = i32
             lib.pao_block_copy.argtypes = [vp, vp, vp, i32, i32, i32, i32, i32, i32]
             lib.pao_block_copy.restype = i32
+            lib.pao_paged_prefill.argtypes = [vp, vp, i32, vp, vp, i32, vp, vp, vp, vp, vp, i32,
+                                              i32, i32, i32, i32, i32, i32, dbl, i32, i32]
+            lib.pao_paged_prefill.restype = i32
             lib.pao_max_threads.argtypes = []
             lib.pao_max_threads.restype = i32
             _lib = lib
@@ -152,6 +156,59 @@ def paged_decode(query, key_cache, value_cache, block_tables, context_lens, scal
                                  int(threads), int(window))
     if rc != 0:
         raise ValueError(f"oracle paged_decode failed with code {rc}")
+    return out
+
+
+def paged_prefill(query, key_cache, value_cache, block_tables, context_lens, query_start,
+                  scale, threads: int = 1, k_scales=None, v_scales=None,
+                  window: int = 0) -> np.ndarray:
+    """fp64 chunked prefill over paged K/V (see ``pao_paged_prefill``).
+
+    query [total_tokens][Hq][D]; sequence b's chunk is rows
+    query_start[b] .. query_start[b+1]-1, the last T_b of its context_lens[b]
+    positions (their K/V already in the pools).  Each row attends causally to
+    the positions up to its own (the last ``window`` of them when ``window`` > 0).
+    Returns float64 [total_tokens][Hq][D].
+    """
+    lib = _load()
+    query = np.ascontiguousarray(query)
+    key_cache = np.ascontiguousarray(key_cache)
+    value_cache = np.ascontiguousarray(value_cache)
+    q_code = _dtype_code(query)
+    kv_code = _dtype_code(key_cache)
+    if _dtype_code(value_cache) != kv_code:
+        raise TypeError("key_cache and value_cache must share one element type")
+    if kv_code == FP8_E4M3:
+        if k_scales is None or v_scales is None:
+            raise ValueError("E4M3 pools need k_scales and v_scales")
+    elif q_code != kv_code:
+        raise TypeError("query and unquantised pools must share one element type")
+    block_tables = np.ascontiguousarray(block_tables, dtype=np.int32)
+    context_lens = np.ascontiguousarray(context_lens, dtype=np.int32)
+    query_start = np.ascontiguousarray(query_start, dtype=np.int32)
+    N, Hq, D = query.shape
+    NB, Hkv, BS, D2 = key_cache.shape
+    B = context_lens.shape[0]
+    if D2 != D or value_cache.shape != key_cache.shape:
+        raise ValueError("shape mismatch between query and caches")
+    if block_tables.ndim != 2 or block_tables.shape[0] != B or query_start.shape != (B + 1,):
+        raise ValueError("block_tables must be [B][max_blocks] and query_start [B + 1]")
+    if int(query_start[-1]) != N:
+        raise ValueError("query_start[B] must equal the number of query rows")
+    ks = vs = None
+    if kv_code == FP8_E4M3:
+        ks = np.ascontiguousarray(k_scales, dtype=np.float32).reshape(Hkv)
+        vs = np.ascontiguousarray(v_scales, dtype=np.float32).reshape(Hkv)
+    out = np.zeros((N, Hq, D), dtype=np.float64)
+    rc = lib.pao_paged_prefill(out.ctypes.data, query.ctypes.data, q_code, key_cache.ctypes.data,
+                               value_cache.ctypes.data, kv_code,
+                               None if ks is None else ks.ctypes.data,
+                               None if vs is None else vs.ctypes.data,
+                               block_tables.ctypes.data, context_lens.ctypes.data,
+                               query_start.ctypes.data, B, Hq, Hkv, D, BS, block_tables.shape[1],
+                               NB, float(scale), int(window), int(threads))
+    if rc != 0:
+        raise ValueError(f"oracle paged_prefill failed with code {rc}")
     return out
 
 

@@ -131,33 +131,29 @@ static double widen(const void *base, int64_t idx, int dtype)
     }
 }
 
-/* Attention of one query head of one sequence over its paged context.
- * Two passes over the scores (maximum, then normalised weights), exactly the
- * textbook softmax(q K^T * scale) V with the K/V rows gathered through the
- * block table in logical token order. */
-static int attend_one(double *out, const void *query, int q_dtype, const void *key_cache,
-                      const void *value_cache, int kv_dtype, const float *k_scales,
-                      const float *v_scales, const int32_t *block_tables,
-                      const int32_t *context_lens, int b, int h, int num_q_heads,
-                      int num_kv_heads, int head_dim, int block_size, int max_blocks,
-                      int num_blocks, double scale, int window)
+/* Attention of one query row over positions [first, last) of sequence b's
+ * paged context (KV head kvh).  Two passes over the scores (maximum, then
+ * normalised weights), exactly the textbook softmax(q K^T * scale) V with the
+ * K/V rows gathered through the block table in logical token order.  The
+ * query row starts at element qbase of `query`. */
+static int attend_span(double *out, const void *query, int64_t qbase, int q_dtype,
+                       const void *key_cache, const void *value_cache, int kv_dtype,
+                       const float *k_scales, const float *v_scales,
+                       const int32_t *block_tables, int b, int kvh, int first, int last,
+                       int num_kv_heads, int head_dim, int block_size, int max_blocks,
+                       int num_blocks, double scale)
 {
-    const int group = num_q_heads / num_kv_heads;
-    const int kvh = h / group;
-    const int L = context_lens[b];
     int d, t;
 
     for (d = 0; d < head_dim; ++d)
         out[d] = 0.0;
-    if (L == 0)
+    if (last <= first)
         return PAO_OK;
-    if (L < 0 || (int64_t)L > (int64_t)max_blocks * block_size)
+    if (first < 0 || (int64_t)last > (int64_t)max_blocks * block_size)
         return PAO_ERR_INDEX;
-    /* With a window of W tokens only positions [L - W, L) take part. */
-    const int first = (window > 0 && L > window) ? L - window : 0;
 
-    double *score = (double *)malloc(sizeof(double) * (size_t)L);
-    int64_t *row = (int64_t *)malloc(sizeof(int64_t) * (size_t)L);
+    double *score = (double *)malloc(sizeof(double) * (size_t)last);
+    int64_t *row = (int64_t *)malloc(sizeof(int64_t) * (size_t)last);
     if (!score || !row) {
         free(score);
         free(row);
@@ -165,7 +161,7 @@ static int attend_one(double *out, const void *query, int q_dtype, const void *k
     }
 
     /* Gather: logical token t -> (physical block, offset inside it). */
-    for (t = first; t < L; ++t) {
+    for (t = first; t < last; ++t) {
         int logical_block = t / block_size;
         int offset = t % block_size;
         int32_t phys = block_tables[(int64_t)b * max_blocks + logical_block];
@@ -182,8 +178,7 @@ static int attend_one(double *out, const void *query, int q_dtype, const void *k
     const double vs = v_scales ? (double)v_scales[kvh] : 1.0;
 
     /* Scores s_t = scale * <q, k_t>. */
-    const int64_t qbase = ((int64_t)b * num_q_heads + h) * head_dim;
-    for (t = first; t < L; ++t) {
+    for (t = first; t < last; ++t) {
         double dot = 0.0;
         for (d = 0; d < head_dim; ++d)
             dot += widen(query, qbase + d, q_dtype) * (widen(key_cache, row[t] + d, kv_dtype) * ks);
@@ -192,15 +187,15 @@ static int attend_one(double *out, const void *query, int q_dtype, const void *k
 
     /* Softmax: subtract the maximum, exponentiate, normalise. */
     double mx = score[first];
-    for (t = first + 1; t < L; ++t)
+    for (t = first + 1; t < last; ++t)
         if (score[t] > mx)
             mx = score[t];
     double denom = 0.0;
-    for (t = first; t < L; ++t)
+    for (t = first; t < last; ++t)
         denom += exp(score[t] - mx);
 
     /* Output: the softmax-weighted sum of the value rows. */
-    for (t = first; t < L; ++t) {
+    for (t = first; t < last; ++t) {
         double w = exp(score[t] - mx) / denom;
         for (d = 0; d < head_dim; ++d)
             out[d] += w * (widen(value_cache, row[t] + d, kv_dtype) * vs);
@@ -209,6 +204,27 @@ static int attend_one(double *out, const void *query, int q_dtype, const void *k
     free(score);
     free(row);
     return PAO_OK;
+}
+
+/* Decode: query head h of sequence b attends to its whole context [0, L), or
+ * with a window of W tokens to [L - W, L). */
+static int attend_one(double *out, const void *query, int q_dtype, const void *key_cache,
+                      const void *value_cache, int kv_dtype, const float *k_scales,
+                      const float *v_scales, const int32_t *block_tables,
+                      const int32_t *context_lens, int b, int h, int num_q_heads,
+                      int num_kv_heads, int head_dim, int block_size, int max_blocks,
+                      int num_blocks, double scale, int window)
+{
+    const int group = num_q_heads / num_kv_heads;
+    const int L = context_lens[b];
+    if (L < 0 || (int64_t)L > (int64_t)max_blocks * block_size)
+        return PAO_ERR_INDEX;
+    /* With a window of W tokens only positions [L - W, L) take part. */
+    const int first = (window > 0 && L > window) ? L - window : 0;
+    const int64_t qbase = ((int64_t)b * num_q_heads + h) * head_dim;
+    return attend_span(out, query, qbase, q_dtype, key_cache, value_cache, kv_dtype, k_scales,
+                       v_scales, block_tables, b, h / group, first, L, num_kv_heads, head_dim,
+                       block_size, max_blocks, num_blocks, scale);
 }
 
 /*
@@ -397,4 +413,74 @@ int pao_max_threads(void)
 #else
     return 1;
 #endif
+}
+
+/*
+ * Chunked (paged) prefill ("PagedAttention por dentro", section "Chunked
+ * prefill integrado con paged KV": prefill is cut into chunks that run over
+ * the same paged KV cache as decode).  Sequence b brings a chunk of
+ * T_b = query_start[b+1] - query_start[b] new tokens whose K/V are already in
+ * the pools; its context then holds L_b = context_lens[b] tokens, the chunk
+ * being the last T_b of them.  Query row i of the chunk sits at position
+ * p = L_b - T_b + i and attends causally ("KV cache: la memoria de trabajo",
+ * "El mecanismo en sí (en cristiano)": a token looks at itself and the tokens
+ * before it) to positions [0, p], or with a window of W tokens to
+ * [p + 1 - W, p].
+ *   query : [total_tokens][num_q_heads][head_dim], row query_start[b] + i for
+ *           token i of sequence b; out likewise, in double.
+ *   query_start : int32 [num_seqs + 1], non-decreasing, query_start[0] = 0.
+ */
+int pao_paged_prefill(double *out, const void *query, int q_dtype, const void *key_cache,
+                      const void *value_cache, int kv_dtype, const float *k_scales,
+                      const float *v_scales, const int32_t *block_tables,
+                      const int32_t *context_lens, const int32_t *query_start, int num_seqs,
+                      int num_q_heads, int num_kv_heads, int head_dim, int block_size,
+                      int max_blocks, int num_blocks, double scale, int window, int num_threads)
+{
+    if (!out || !query || !key_cache || !value_cache || !block_tables || !context_lens ||
+        !query_start)
+        return PAO_ERR_ARG;
+    if (q_dtype < 0 || q_dtype > 1 || kv_dtype < 0 || kv_dtype > 2)
+        return PAO_ERR_ARG;
+    if (num_seqs < 0 || num_q_heads <= 0 || num_kv_heads <= 0 || head_dim <= 0 ||
+        block_size <= 0 || max_blocks < 0 || num_blocks < 0 || window < 0)
+        return PAO_ERR_ARG;
+    if (num_q_heads % num_kv_heads != 0 || query_start[0] != 0)
+        return PAO_ERR_ARG;
+    int b;
+    for (b = 0; b < num_seqs; ++b) {
+        const int T = query_start[b + 1] - query_start[b];
+        if (T < 0 || T > context_lens[b])
+            return PAO_ERR_ARG;
+    }
+    const int group = num_q_heads / num_kv_heads;
+    const int64_t rows = (int64_t)query_start[num_seqs] * num_q_heads;
+    int status = PAO_OK;
+    int64_t r;
+    (void)num_threads;
+#ifdef _OPENMP
+#pragma omp parallel for schedule(dynamic, 16) num_threads(num_threads > 0 ? num_threads : 1)
+#endif
+    for (r = 0; r < rows; ++r) {
+        const int64_t tok = r / num_q_heads;
+        const int h = (int)(r % num_q_heads);
+        int sb = 0;
+        while (query_start[sb + 1] <= tok)   /* the sequence that owns this token */
+            ++sb;
+        const int T = query_start[sb + 1] - query_start[sb];
+        const int L = context_lens[sb];
+        const int p = L - T + (int)(tok - query_start[sb]);
+        const int first = (window > 0 && p + 1 > window) ? p + 1 - window : 0;
+        int rc = attend_span(out + r * head_dim, query, r * head_dim, q_dtype, key_cache,
+                             value_cache, kv_dtype, k_scales, v_scales, block_tables, sb,
+                             h / group, first, p + 1, num_kv_heads, head_dim, block_size,
+                             max_blocks, num_blocks, scale);
+        if (rc != PAO_OK) {
+#ifdef _OPENMP
+#pragma omp critical
+#endif
+            status = rc;
+        }
+    }
+    return status;
 }

@@ -18,7 +18,16 @@ SRC = os.path.join(os.path.dirname(oracle.__file__), "pa_oracle.c")
 
 MUTANTS = {
     "drop_scale": ("score[t] = scale * dot;", "score[t] = dot;"),
-    "kv_head_modulo": ("const int kvh = h / group;", "const int kvh = h % num_kv_heads;"),
+    "kv_head_modulo": ("v_scales, block_tables, b, h / group, first, L,",
+                       "v_scales, block_tables, b, h % num_kv_heads, first, L,"),
+    "prefill_excludes_self": ("h / group, first, p + 1, num_kv_heads",
+                              "h / group, first, p, num_kv_heads"),
+    "prefill_ignores_cached_context": ("const int p = L - T + (int)(tok - query_start[sb]);",
+                                       "const int p = (int)(tok - query_start[sb]);"),
+    "prefill_window_off_by_one": ("(window > 0 && p + 1 > window) ? p + 1 - window : 0;",
+                                  "(window > 0 && p + 1 > window) ? p - window : 0;"),
+    "prefill_kv_head": ("h / group, first, p + 1, num_kv_heads",
+                        "h % num_kv_heads, first, p + 1, num_kv_heads"),
     "offset_shift": ("int offset = t % block_size;", "int offset = (t + 1) % block_size;"),
     "block_index": ("int logical_block = t / block_size;",
                     "int logical_block = (t / block_size) % 2;"),
@@ -46,6 +55,8 @@ MUTANTS = {
 from tests import test_oracle_fp8_pins as fp8pins  # noqa: E402
 
 PIN_FUNCS = [
+    lambda g: pins.test_prefill_matches_library_causal_attention(2, 8, 2, 64, [(0, 21), (37, 19), (100, 1)]),
+    lambda g: pins.test_prefill_window_matches_library_attention(9),
     lambda g: pins.test_window_matches_library_attention_on_the_last_tokens(17),
     lambda g: fp8pins.test_every_code_value_matches_torch(),
     lambda g: fp8pins.test_encode_matches_torch_below_overflow(),
@@ -86,7 +97,7 @@ def test_pins_catch_planted_mistake(name, tmp_path, golden_dir, monkeypatch):
     mutant = ctypes.CDLL(so)
     for fn in ("pao_paged_decode", "pao_paged_decode_ex", "pao_cache_write",
                "pao_cache_write_fp8", "pao_e4m3_value", "pao_e4m3_encode", "pao_block_copy",
-               "pao_max_threads"):
+               "pao_max_threads", "pao_paged_prefill"):
         getattr(mutant, fn).argtypes = getattr(real, fn).argtypes
         getattr(mutant, fn).restype = getattr(real, fn).restype
     monkeypatch.setattr(oracle, "_lib", mutant)

@@ -354,3 +354,85 @@ def test_window_never_reads_released_blocks():
     t2[0, :3] = -1                       # positions 0..47 released; window starts at 60
     got = oracle.paged_decode(q, kc, vc, t2, L, 0.3, window=40)
     assert np.array_equal(got, want)
+
+
+# ---------------------------------------------------------------------------
+# Chunked prefill
+# ---------------------------------------------------------------------------
+def _random_chunks(rng, Hq, Hkv, D, specs, spare=3):
+    """specs: (cached tokens C, chunk tokens T) per sequence; context L = C + T."""
+    lens = [c + t for c, t in specs]
+    _, ck, cv, kc, vc, tables, L = _random_paged(rng, len(specs), Hq, Hkv, D, lens, spare)
+    qs = np.zeros(len(specs) + 1, dtype=np.int32)
+    qs[1:] = np.cumsum([t for _, t in specs])
+    q = rng.standard_normal((int(qs[-1]), Hq, D)).astype(np.float32)
+    return q, ck, cv, kc, vc, tables, L, qs
+
+
+def _sdpa_causal(q, ck, cv, scale, group, cached, window=0):
+    """Library attention of T query rows at positions cached .. cached+T-1 over
+    contiguous K/V [Hkv][L][D], with an explicit causal (and window) mask."""
+    T, L = q.shape[0], ck.shape[1]
+    i = np.arange(T)[:, None] + cached
+    j = np.arange(L)[None, :]
+    allowed = j <= i
+    if window:
+        allowed &= j > i - window
+    qt = torch.from_numpy(q.astype(np.float64)).permute(1, 0, 2)[None]   # [1,Hq,T,D]
+    kt = torch.from_numpy(ck.astype(np.float64))[None]
+    vt = torch.from_numpy(cv.astype(np.float64))[None]
+    o = torch.nn.functional.scaled_dot_product_attention(
+        qt, kt, vt, attn_mask=torch.from_numpy(allowed), scale=scale, enable_gqa=group > 1)
+    return o[0].permute(1, 0, 2).numpy()
+
+
+@pytest.mark.parametrize("B,Hq,Hkv,D,specs", [
+    (2, 8, 2, 64, [(0, 21), (37, 19), (100, 1)]),
+    (1, 4, 4, 32, [(0, 50)]),
+    (2, 16, 2, 128, [(15, 17), (48, 33)]),
+])
+def test_prefill_matches_library_causal_attention(B, Hq, Hkv, D, specs):
+    rng = np.random.default_rng(70 + Hq + D)
+    q, ck, cv, kc, vc, tables, L, qs = _random_chunks(rng, Hq, Hkv, D, specs)
+    got = oracle.paged_prefill(q, kc, vc, tables, L, qs, 0.15)
+    for b, (c, t) in enumerate(specs):
+        want = _sdpa_causal(q[qs[b]:qs[b + 1]], ck[b], cv[b], 0.15, Hq // Hkv, c)
+        np.testing.assert_allclose(got[qs[b]:qs[b + 1]], want, rtol=1e-11, atol=1e-12)
+
+
+@pytest.mark.parametrize("window", [1, 9, 40])
+def test_prefill_window_matches_library_attention(window):
+    rng = np.random.default_rng(80 + window)
+    specs = [(0, 30), (25, 20), (64, 3)]
+    q, ck, cv, kc, vc, tables, L, qs = _random_chunks(rng, 8, 4, 64, specs)
+    got = oracle.paged_prefill(q, kc, vc, tables, L, qs, 0.3, window=window)
+    for b, (c, t) in enumerate(specs):
+        want = _sdpa_causal(q[qs[b]:qs[b + 1]], ck[b], cv[b], 0.3, 2, c, window)
+        np.testing.assert_allclose(got[qs[b]:qs[b + 1]], want, rtol=1e-11, atol=1e-12)
+
+
+def test_prefill_first_row_of_a_fresh_sequence_is_its_own_value():
+    """Position 0 attends to itself alone: softmax weight 1."""
+    rng = np.random.default_rng(90)
+    q, ck, cv, kc, vc, tables, L, qs = _random_chunks(rng, 4, 2, 32, [(0, 5), (0, 1)])
+    got = oracle.paged_prefill(q, kc, vc, tables, L, qs, 0.5)
+    for b in range(2):
+        for h in range(4):
+            assert np.array_equal(got[qs[b], h], cv[b][h // 2, 0].astype(np.float64))
+
+
+def test_prefill_rows_equal_decode_and_chunking_changes_nothing():
+    """Row i of a chunk is the decode of that query over the first C + i + 1
+    positions, and splitting one prompt into chunks gives the same rows."""
+    rng = np.random.default_rng(91)
+    q, ck, cv, kc, vc, tables, L, qs = _random_chunks(rng, 8, 2, 64, [(0, 70)])
+    whole = oracle.paged_prefill(q, kc, vc, tables, L, qs, 0.2)
+    for i in (0, 15, 16, 69):
+        dec = oracle.paged_decode(q[i:i + 1], kc, vc, tables, np.array([i + 1], np.int32), 0.2)
+        assert np.array_equal(dec[0], whole[i])
+    for cut in (1, 16, 33):
+        a = oracle.paged_prefill(q[:cut], kc, vc, tables, np.array([cut], np.int32),
+                                 np.array([0, cut], np.int32), 0.2)
+        b = oracle.paged_prefill(q[cut:], kc, vc, tables, L, np.array([0, 70 - cut], np.int32),
+                                 0.2)
+        assert np.array_equal(np.concatenate([a, b]), whole)
