@@ -72,6 +72,7 @@ typedef enum pa_dtype {
 #define PA_DEV_BAD_COPY_PAIR   8  /* a copy pair index outside [0, num_blocks) */
 #define PA_DEV_TIMEOUT        16  /* a bounded in-kernel wait gave up */
 #define PA_DEV_PREFIX_MISMATCH 32 /* pa_decode_shared_prefix: tables do not share the prefix */
+#define PA_DEV_BAD_QUERY_LEN  64  /* pa_prefill: a chunk longer than max_query_len */
 
 /* Human-readable name of a status. Never NULL. */
 const char *pa_status_string(pa_status status);
@@ -315,6 +316,40 @@ pa_status pa_cache_write(void *key_cache, void *value_cache, const void *key, co
 pa_status pa_block_copy(void *key_cache, void *value_cache, const int32_t *src_dst, int num_pairs,
                         int num_kv_heads, int head_dim, int block_size, int num_blocks,
                         pa_dtype dtype, int32_t *device_status, void *stream);
+
+/*
+ * Chunked (paged) prefill attention ("PagedAttention por dentro", section
+ * "Chunked prefill integrado con paged KV": prefill is cut into chunks that run
+ * over the same paged KV cache as decode).  Sequence b brings a chunk of
+ * T_b = query_start[b+1] - query_start[b] new tokens whose K/V are already in
+ * the pools (pa_cache_write); its context then holds L_b = context_lens[b]
+ * tokens, the chunk being the last T_b of them.  Query row i of the chunk sits
+ * at position p = L_b - T_b + i and attends causally to positions [0, p]
+ * ("KV cache: la memoria de trabajo que sostiene la inferencia LLM", "El
+ * mecanismo en sí (en cristiano)"); with window > 0, to [p + 1 - window, p]
+ * ("PagedAttention por dentro", "Sliding window attention").
+ *  out, query        device bfloat16 [num_query_tokens][num_q_heads][head_dim];
+ *                    rows query_start[b] .. query_start[b+1]-1 are sequence b's
+ *  query_start       device int32 [num_seqs + 1], non-decreasing, [0] = 0,
+ *                    [num_seqs] = num_query_tokens
+ *  context_lens      device int32 [num_seqs], L_b >= T_b
+ *  max_query_len     host int, at least every T_b (sizes the grid); rows of a
+ *                    longer chunk past max_query_len are not computed and the
+ *                    call flags PA_DEV_BAD_QUERY_LEN
+ *  window            0 = causal over the whole context
+ * Pools, block tables, scale, device_status and stream as in pa_decode; table
+ * entries of blocks wholly before every row's window are not read.
+ * Supported: bf16, head_dim 128, group (num_q_heads / num_kv_heads) 1, 2, 4, 8
+ * or 16.  Arithmetic: S = QK^T and O = PV on tcgen05 tensor cores with fp32
+ * accumulation in tensor memory; P goes to the second product as a bf16 head
+ * plus a bf16 residual (about 2^-17 relative).  One kernel launch; no workspace.
+ */
+pa_status pa_prefill(void *out, const void *query, const void *key_cache, const void *value_cache,
+                     const int32_t *block_tables, const int32_t *context_lens,
+                     const int32_t *query_start, int num_seqs, int num_q_heads, int num_kv_heads,
+                     int head_dim, int block_size, int max_blocks_per_seq, int num_blocks,
+                     int num_query_tokens, int max_query_len, float scale, pa_dtype dtype,
+                     int window, int32_t *device_status, void *stream);
 
 /*
  * Swap of blocks between the pools and a staging buffer ("PagedAttention por

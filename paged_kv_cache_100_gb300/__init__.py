@@ -25,7 +25,7 @@ from ._lib import PagedKVError, check, lib  # noqa: F401
 
 BLOCK_SIZE = 16
 
-__all__ = ["swap_out", "swap_in", "decode", "decode_fp8", "decode_sliding_window", "decode_shared_prefix", "shared_prefix_blocks", "decode_workspace_bytes", "decode_partition_size",
+__all__ = ["prefill", "swap_out", "swap_in", "decode", "decode_fp8", "decode_sliding_window", "decode_shared_prefix", "shared_prefix_blocks", "decode_workspace_bytes", "decode_partition_size",
            "cache_write", "cache_write_fp8", "block_copy", "launch_count", "BlockManager",
            "PagedKVError", "BLOCK_SIZE", "library_path"]
 
@@ -345,6 +345,44 @@ def block_copy(key_cache, value_cache, src_dst, *, status=None, stream=None):
         _dev(src_dst, "src_dst", torch.int32), P, Hkv, D, BS, NB, _dtype_code(key_cache),
         _status_ptr(status), _stream(stream, key_cache.device))
     check(rc, "pa_block_copy")
+
+
+def prefill(query, key_cache, value_cache, block_tables, context_lens, query_start,
+            max_query_len=None, scale=None, *, window=0, out=None, status=None, stream=None):
+    """Chunked prefill over the paged pools (``pa_prefill``); returns ``out``.
+
+    ``query`` [tokens][Hq][D] bf16 holds every sequence's chunk back to back,
+    ``query_start`` (int32 [B+1]) where each begins; ``context_lens`` counts
+    each context with its chunk.  ``max_query_len`` bounds the chunk lengths
+    (read from ``query_start`` when omitted, which synchronises the stream)."""
+    torch = _torch()
+    N, Hq, D = query.shape
+    NB, Hkv, BS, D2 = key_cache.shape
+    B = context_lens.shape[0]
+    if BS != BLOCK_SIZE or D2 != D or tuple(value_cache.shape) != tuple(key_cache.shape):
+        raise ValueError("pools must be [num_blocks][num_kv_heads][16][head_dim] like query")
+    if block_tables.dim() != 2 or block_tables.shape[0] != B or tuple(query_start.shape) != (B + 1,):
+        raise ValueError("block_tables must be [num_seqs][max_blocks], query_start [num_seqs + 1]")
+    if query.dtype != torch.bfloat16 or key_cache.dtype != torch.bfloat16 or \
+            value_cache.dtype != torch.bfloat16:
+        raise TypeError("pa_prefill takes bfloat16 query and pools")
+    if max_query_len is None:
+        max_query_len = int((query_start[1:] - query_start[:-1]).max().item()) if B else 0
+    if scale is None:
+        scale = 1.0 / math.sqrt(D)
+    if out is None:
+        out = torch.empty_like(query)
+    elif out.shape != query.shape or out.dtype != query.dtype:
+        raise ValueError("out must match query")
+    rc = lib().pa_prefill(
+        _dev(out, "out"), _dev(query, "query"), _dev(key_cache, "key_cache"),
+        _dev(value_cache, "value_cache"), _dev(block_tables, "block_tables", torch.int32),
+        _dev(context_lens, "context_lens", torch.int32),
+        _dev(query_start, "query_start", torch.int32), B, Hq, Hkv, D, BLOCK_SIZE,
+        block_tables.shape[1], NB, N, int(max_query_len), float(scale), _lib.PA_DTYPE_BF16,
+        int(window), _status_ptr(status), _stream(stream, query.device))
+    check(rc, "pa_prefill")
+    return out
 
 
 def _staging_ptr(t, nbytes):

@@ -48,6 +48,8 @@ SIGNATURES = {
     "pa_decode_sliding_window": (i32, [vp, vp, vp, vp, vp, vp, vp, vp, i32, i32, i32, i32, i32,
                                        i32, i32, f32, i32, i32, i32, vp, sz, vp, vp]),
     "pa_cache_write_fp8": (i32, [vp, vp, vp, vp, vp, vp, vp, i32, i32, i32, i32, i32, vp, vp]),
+    "pa_prefill": (i32, [vp, vp, vp, vp, vp, vp, vp, i32, i32, i32, i32, i32, i32, i32, i32, i32,
+                         f32, i32, i32, vp, vp]),
     "pa_swap_bytes": (sz, [i32, i32, i32, i32]),
     "pa_swap_out": (i32, [vp, vp, vp, i32, vp, i32, i32, i32, i32, i32, vp, vp]),
     "pa_swap_in": (i32, [vp, vp, vp, i32, vp, i32, i32, i32, i32, i32, vp, vp]),
@@ -92,6 +94,7 @@ PA_DEV_BAD_SLOT = 4
 PA_DEV_BAD_COPY_PAIR = 8
 PA_DEV_TIMEOUT = 16
 PA_DEV_PREFIX_MISMATCH = 32
+PA_DEV_BAD_QUERY_LEN = 64
 
 
 class PagedKVError(RuntimeError):

@@ -1,0 +1,521 @@
+// Chunked (paged) prefill attention on 5th-generation tensor cores.
+//
+// "PagedAttention por dentro: bloques, tabla de páginas, evicción y el estado
+// del arte del KV cache en 2026", section "Chunked prefill integrado con paged
+// KV": prefill is cut into chunks that run over the same paged KV cache as
+// decode.  Sequence b brings T_b new tokens (their K/V already written into the
+// pools); its context then holds L_b tokens, the chunk being the last T_b.  Row
+// i of the chunk (position p = L_b - T_b + i) attends causally to positions
+// [0, p] ("KV cache: la memoria de trabajo que sostiene la inferencia LLM",
+// "El mecanismo en sí (en cristiano)"), or to its last W positions with a
+// sliding window ("PagedAttention por dentro", "Sliding window attention").
+//
+// One CTA computes a 128-row tile of (token, query head of the group) rows of
+// one sequence and one KV head, flash-attention style over 128-position K/V
+// tiles gathered block by block through the block table:
+//   warp 0      TMA producer: Q tile once, then K and V tiles (eight 16-row
+//               blocks each) into two-stage rings;
+//   warp 1      MMA issuer: S = Q K^T into tensor memory (two S buffers), then
+//               O += P V into a tensor-memory accumulator; owns the TMEM
+//               allocation;
+//   warps 2..5  softmax: one thread per row (= TMEM lane) reads its S row,
+//               keeps the running maximum and sum, writes P (bf16 head and bf16
+//               residual) to shared memory, rescales O in tensor memory only
+//               when the maximum grew by more than 2^8, and writes the output.
+// Every wait is bounded (about a second); a wait that gives up sets
+// PA_DEV_TIMEOUT and the CTA drains its tensor-core work and returns.
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <cudaTypedefs.h>
+#include <math.h>
+
+#include <climits>
+#include <mutex>
+
+#include "pa_device.cuh"
+#include "pa_internal.h"
+
+namespace pa {
+namespace {
+
+constexpr int kRows = 128;               // M: query rows per CTA
+constexpr int kKv = 128;                 // N: K/V positions per step (8 blocks)
+constexpr int kD = 128;                  // head_dim
+constexpr int kHalf = 16384;             // one 64-column swizzled region of a tile
+constexpr int kTile = 2 * kHalf;         // 128 rows x 256 bytes
+constexpr int kThreads = 192;
+constexpr float kRescaleLog2 = 8.0f;     // lazy rescale threshold (factor 256)
+
+// shared memory map (offsets from a 1024-byte aligned base)
+constexpr int kOffQ = 0;
+constexpr int kOffK = kOffQ + kTile;            // two stages
+constexpr int kOffV = kOffK + 2 * kTile;        // two stages
+constexpr int kOffP = kOffV + 2 * kTile;        // P head, then P residual
+constexpr int kOffBar = kOffP + 2 * kTile;
+constexpr int kNumBars = 16;
+constexpr int kSmemBytes = kOffBar + kNumBars * 8 + 16 + 1024;   // + slot, flag, alignment
+
+// barrier indices
+constexpr int kQFull = 0, kKFull = 1, kKEmpty = 3, kVFull = 5, kVEmpty = 7, kSFull = 9,
+              kSFree = 11, kPFull = 13, kPvDone = 14, kDrain = 15;
+
+// TMEM columns: S buffers at 0 and 128, O at 256.
+constexpr uint32_t kTmemCols = 512;
+constexpr uint32_t kColO = 256;
+
+struct PrefillArgs {
+    void *out;
+    const int32_t *block_tables;
+    const int32_t *context_lens;
+    const int32_t *query_start;
+    int32_t *status;
+    int num_q_heads;
+    int num_kv_heads;
+    int group;
+    int max_blocks;
+    int num_blocks;
+    int max_query_len;
+    int window;
+    float scale_log2;
+};
+
+__device__ __forceinline__ bool wait_or_fail(uint64_t *bar, uint32_t parity, volatile int *fail,
+                                             int32_t *status) {
+    if (*fail) return false;
+    if (mbar_wait_bounded(bar, parity)) return true;
+    *fail = 1;
+    report(status, PA_DEV_TIMEOUT);
+    return false;
+}
+
+__device__ __forceinline__ uint32_t pack2_bf16(float lo, float hi) {
+    __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
+    return *reinterpret_cast<uint32_t *>(&v);
+}
+
+__global__ void __launch_bounds__(kThreads, 1)
+    pa_prefill_kernel(const __grid_constant__ CUtensorMap qmap,
+                      const __grid_constant__ CUtensorMap kmap,
+                      const __grid_constant__ CUtensorMap vmap, const PrefillArgs a) {
+    grid_dependency_wait();
+    grid_dependents_launch();
+    const int b = blockIdx.z;
+    const int kvh = blockIdx.y;
+    const int g = a.group;
+    const int tok_per_tile = kRows / g;
+    const int mt = gridDim.x - 1 - blockIdx.x;   // later (longer) tiles first
+    const int q0 = a.query_start[b];
+    const int T = a.query_start[b + 1] - q0;
+    const int L = a.context_lens[b];
+    if (T < 0 || T > L || L > a.max_blocks * kBlockSize) {
+        if (blockIdx.x == 0 && kvh == 0 && threadIdx.x == 0) report(a.status, PA_DEV_BAD_CONTEXT_LEN);
+        return;
+    }
+    if (T > a.max_query_len && blockIdx.x == 0 && kvh == 0 && threadIdx.x == 0)
+        report(a.status, PA_DEV_BAD_QUERY_LEN);
+    const int t0 = mt * tok_per_tile;
+    if (t0 >= T) return;
+    const int ntok = min(tok_per_tile, T - t0);
+    const int C = L - T;
+    const int qpos_lo = C + t0, qpos_hi = C + t0 + ntok - 1;
+    const int kv_hi = qpos_hi + 1;
+    const int kv_lo = a.window > 0 ? max(0, qpos_lo + 1 - a.window) : 0;
+    const int blk_lo = kv_lo / kBlockSize;
+    const int blk_hi = (kv_hi + kBlockSize - 1) / kBlockSize;
+    const int n_tiles = (blk_hi - blk_lo + 7) / 8;
+
+    extern __shared__ uint8_t smem_raw[];
+    const uint32_t raw_u = smem_u32(smem_raw);
+    uint8_t *base = smem_raw + (((raw_u + 1023u) & ~1023u) - raw_u);
+    uint8_t *sQ = base + kOffQ;
+    uint8_t *sK = base + kOffK;
+    uint8_t *sV = base + kOffV;
+    uint8_t *sP = base + kOffP;
+    uint64_t *bars = reinterpret_cast<uint64_t *>(base + kOffBar);
+    uint32_t *tslot = reinterpret_cast<uint32_t *>(base + kOffBar + kNumBars * 8);
+    volatile int *fail = reinterpret_cast<volatile int *>(base + kOffBar + kNumBars * 8 + 4);
+
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+    if (threadIdx.x == 0) {
+        mbar_init(&bars[kQFull], 1);
+        for (int s = 0; s < 2; ++s) {
+            mbar_init(&bars[kKFull + s], 1);
+            mbar_init(&bars[kKEmpty + s], 1);
+            mbar_init(&bars[kVFull + s], 1);
+            mbar_init(&bars[kVEmpty + s], 1);
+            mbar_init(&bars[kSFull + s], 1);
+            mbar_init(&bars[kSFree + s], 128);
+        }
+        mbar_init(&bars[kPFull], 128);
+        mbar_init(&bars[kPvDone], 1);
+        mbar_init(&bars[kDrain], 1);
+        *fail = 0;
+        fence_mbar_init();
+        tma_prefetch_desc(&qmap);
+        tma_prefetch_desc(&kmap);
+        tma_prefetch_desc(&vmap);
+    }
+    if (warp == 1) tmem_alloc(tslot, kTmemCols);
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tslot;
+
+    if (warp == 0) {
+        // ---------------- TMA producer ----------------
+        if (lane == 0) {
+            mbar_arrive_expect_tx(&bars[kQFull], kTile);
+            tma_load_4d(sQ, &qmap, 0, 0, kvh, q0 + t0, &bars[kQFull]);
+            tma_load_4d(sQ + kHalf, &qmap, 64, 0, kvh, q0 + t0, &bars[kQFull]);
+            const int32_t *trow = a.block_tables + (size_t)b * a.max_blocks;
+            int issued_k = 0, issued_v = 0;
+            for (int j = 0; j < n_tiles; ++j) {
+                const int s = j & 1;
+                const int blk0 = blk_lo + 8 * j;
+                const int nb = min(8, blk_hi - blk0);
+                int rows[8];
+                for (int i = 0; i < nb; ++i) {
+                    int phys = trow[blk0 + i];
+                    if ((unsigned)phys >= (unsigned)a.num_blocks) {
+                        report(a.status, PA_DEV_BAD_BLOCK_ID);
+                        phys = 0;
+                    }
+                    rows[i] = (phys * a.num_kv_heads + kvh) * kBlockSize;
+                }
+                if (j >= 2 && !wait_or_fail(&bars[kKEmpty + s], ((j >> 1) - 1) & 1, fail, a.status))
+                    break;
+                uint8_t *kd = sK + s * kTile;
+                mbar_arrive_expect_tx(&bars[kKFull + s], nb * 4096);
+                for (int i = 0; i < nb; ++i) {
+                    tma_load_2d(kd + i * 2048, &kmap, 0, rows[i], &bars[kKFull + s]);
+                    tma_load_2d(kd + kHalf + i * 2048, &kmap, 64, rows[i], &bars[kKFull + s]);
+                }
+                issued_k = j + 1;
+                if (j >= 2 && !wait_or_fail(&bars[kVEmpty + s], ((j >> 1) - 1) & 1, fail, a.status))
+                    break;
+                uint8_t *vd = sV + s * kTile;
+                mbar_arrive_expect_tx(&bars[kVFull + s], nb * 4096);
+                for (int i = 0; i < nb; ++i) {
+                    tma_load_2d(vd + i * 2048, &vmap, 0, rows[i], &bars[kVFull + s]);
+                    tma_load_2d(vd + kHalf + i * 2048, &vmap, 64, rows[i], &bars[kVFull + s]);
+                }
+                issued_v = j + 1;
+            }
+            // drain: no copy of ours may still be landing when the CTA leaves
+            (void)mbar_wait_bounded(&bars[kQFull], 0);
+            for (int j = max(0, issued_k - 2); j < issued_k; ++j)
+                (void)mbar_wait_bounded(&bars[kKFull + (j & 1)], (j >> 1) & 1);
+            for (int j = max(0, issued_v - 2); j < issued_v; ++j)
+                (void)mbar_wait_bounded(&bars[kVFull + (j & 1)], (j >> 1) & 1);
+        }
+    } else if (warp == 1) {
+        // ---------------- MMA issuer ----------------
+        if (lane == 0) {
+            constexpr uint32_t idS = idesc_bf16_f32(kRows, kKv, false);
+            constexpr uint32_t idPV = idesc_bf16_f32(kRows, kD, true);
+            const uint32_t q_u = smem_u32(sQ), k_u = smem_u32(sK), v_u = smem_u32(sV),
+                           p_u = smem_u32(sP);
+            bool ok = wait_or_fail(&bars[kQFull], 0, fail, a.status);
+            auto issue_pv = [&](int i) -> bool {
+                const int s = i & 1;
+                if (!wait_or_fail(&bars[kPFull], i & 1, fail, a.status)) return false;
+                if (!wait_or_fail(&bars[kVFull + s], (i >> 1) & 1, fail, a.status)) return false;
+                tc_fence_after();
+                const uint32_t vb = v_u + s * kTile;
+#pragma unroll
+                for (int k = 0; k < 8; ++k) {
+                    const uint32_t po = (k >> 2) * kHalf + (k & 3) * 32;
+                    const uint64_t vdesc = sw128_desc(vb + k * 2048, kHalf, 1024);
+                    umma_bf16(tmem + kColO, sw128_desc(p_u + po, 16, 1024), vdesc, idPV,
+                              (i > 0 || k > 0) ? 1u : 0u);
+                    umma_bf16(tmem + kColO, sw128_desc(p_u + kTile + po, 16, 1024), vdesc, idPV, 1u);
+                }
+                umma_commit(&bars[kPvDone]);
+                umma_commit(&bars[kVEmpty + s]);
+                return true;
+            };
+            for (int j = 0; ok && j < n_tiles; ++j) {
+                const int s = j & 1;
+                if (!wait_or_fail(&bars[kKFull + s], (j >> 1) & 1, fail, a.status)) break;
+                if (j >= 2 && !wait_or_fail(&bars[kSFree + s], ((j >> 1) - 1) & 1, fail, a.status))
+                    break;
+                tc_fence_after();
+                const uint32_t kb = k_u + s * kTile;
+#pragma unroll
+                for (int k = 0; k < 8; ++k) {
+                    const uint32_t o = (k >> 2) * kHalf + (k & 3) * 32;
+                    umma_bf16(tmem + s * kKv, sw128_desc(q_u + o, 16, 1024),
+                              sw128_desc(kb + o, 16, 1024), idS, k > 0 ? 1u : 0u);
+                }
+                umma_commit(&bars[kSFull + s]);
+                umma_commit(&bars[kKEmpty + s]);
+                if (j >= 1 && !issue_pv(j - 1)) {
+                    ok = false;
+                    break;
+                }
+                if (j == n_tiles - 1 && !issue_pv(j)) ok = false;
+            }
+            // every MMA issued above has completed once kDrain flips
+            umma_commit(&bars[kDrain]);
+            if (!mbar_wait_bounded(&bars[kDrain], 0)) {
+                *fail = 1;
+                report(a.status, PA_DEV_TIMEOUT);
+            }
+        }
+    } else {
+        // ---------------- softmax warpgroup ----------------
+        const int quarter = warp & 3;
+        const int r = quarter * 32 + lane;            // tile row = TMEM lane
+        const int tr = r / g;
+        const bool real = tr < ntok;
+        const int qpos = C + t0 + min(tr, ntok - 1);
+        const int wlo = a.window > 0 ? qpos + 1 - a.window : INT_MIN;   // first allowed position
+        const uint32_t lane_base = tmem + ((uint32_t)(quarter * 32) << 16);
+        uint8_t *prow_hi = sP + (r >> 3) * 1024 + (r & 7) * 128;
+        const float sl2 = a.scale_log2;
+        float m_used = -INFINITY, l = 0.f;
+        bool ok = true;
+        for (int j = 0; j < n_tiles; ++j) {
+            const int s = j & 1;
+            if (!wait_or_fail(&bars[kSFull + s], (j >> 1) & 1, fail, a.status)) {
+                ok = false;
+                break;
+            }
+            tc_fence_after();
+            const int k0 = (blk_lo + 8 * j) * kBlockSize;
+            const bool masked = (k0 + kKv - 1 > qpos_lo) ||
+                                (a.window > 0 && k0 < qpos_hi + 1 - a.window);
+            const uint32_t srow = lane_base + s * kKv;
+            // pass 1: row maximum of the valid scores
+            float mx = -INFINITY;
+#pragma unroll 1
+            for (int c = 0; c < kKv; c += 32) {
+                uint32_t v[32];
+                tmem_ld32(srow + c, v);
+                tmem_wait_ld();
+#pragma unroll
+                for (int i = 0; i < 32; ++i) {
+                    const int kp = k0 + c + i;
+                    const bool valid = !masked || (kp <= qpos && kp >= wlo);
+                    mx = fmaxf(mx, valid ? __uint_as_float(v[i]) : -INFINITY);
+                }
+            }
+            const float m_tile = mx * sl2;
+            const float m_new = fmaxf(m_used, m_tile);
+            // P of the previous tile must have been consumed (and O updated)
+            // before P is overwritten or O rescaled.
+            if (j >= 1 && !wait_or_fail(&bars[kPvDone], (j - 1) & 1, fail, a.status)) {
+                ok = false;
+                break;
+            }
+            if (m_new > m_used + kRescaleLog2) {
+                const float alpha = exp2f(m_used - m_new);   // 0 while m_used is -inf
+                if (j >= 1) {
+                    tc_fence_after();
+#pragma unroll 1
+                    for (int c = 0; c < kD; c += 32) {
+                        uint32_t o[32];
+                        tmem_ld32(lane_base + kColO + c, o);
+                        tmem_wait_ld();
+#pragma unroll
+                        for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * alpha);
+                        tmem_st32(lane_base + kColO + c, o);
+                    }
+                    tmem_wait_st();
+                }
+                l *= alpha;
+                m_used = m_new;
+            }
+            const float m_ref = m_used == -INFINITY ? 0.f : m_used;
+            // pass 2: P = 2^(s * scale_log2 - m_ref), bf16 head + bf16 residual
+            float psum = 0.f;
+#pragma unroll 1
+            for (int c = 0; c < kKv; c += 32) {
+                uint32_t v[32];
+                tmem_ld32(srow + c, v);
+                tmem_wait_ld();
+                uint32_t hi[16], lo[16];
+#pragma unroll
+                for (int i = 0; i < 32; i += 2) {
+                    float p2[2];
+#pragma unroll
+                    for (int e = 0; e < 2; ++e) {
+                        const int kp = k0 + c + i + e;
+                        const bool valid = !masked || (kp <= qpos && kp >= wlo);
+                        p2[e] = valid ? exp2f(fmaf(__uint_as_float(v[i + e]), sl2, -m_ref)) : 0.f;
+                        psum += p2[e];
+                    }
+                    const uint32_t h = pack2_bf16(p2[0], p2[1]);
+                    hi[i >> 1] = h;
+                    lo[i >> 1] = pack2_bf16(p2[0] - __uint_as_float(h << 16),
+                                            p2[1] - __uint_as_float(h & 0xffff0000u));
+                }
+                // 32 columns = four 16-byte chunks of this row, in region c / 64
+                const int region = c >> 6;
+#pragma unroll
+                for (int q4 = 0; q4 < 4; ++q4) {
+                    const int chunk = ((c & 63) >> 3) + q4;
+                    const uint32_t off = region * kHalf + ((chunk ^ (r & 7)) << 4);
+                    *reinterpret_cast<uint4 *>(prow_hi + off) =
+                        make_uint4(hi[4 * q4], hi[4 * q4 + 1], hi[4 * q4 + 2], hi[4 * q4 + 3]);
+                    *reinterpret_cast<uint4 *>(prow_hi + kTile + off) =
+                        make_uint4(lo[4 * q4], lo[4 * q4 + 1], lo[4 * q4 + 2], lo[4 * q4 + 3]);
+                }
+            }
+            l += psum;
+            tc_fence_before();
+            mbar_arrive(&bars[kSFree + s]);
+            // V rows of positions outside [kv_lo, kv_hi) may hold anything
+            // (NaN included): zero them so that 0 * row stays 0.
+            if (k0 < kv_lo || k0 + kKv > kv_hi) {
+                if (!wait_or_fail(&bars[kVFull + s], (j >> 1) & 1, fail, a.status)) {
+                    ok = false;
+                    break;
+                }
+                const int kp = k0 + r;
+                if (kp < kv_lo || kp >= kv_hi) {
+                    uint8_t *vrow = sV + s * kTile + (r >> 3) * 1024 + (r & 7) * 128;
+#pragma unroll
+                    for (int q = 0; q < 8; ++q) {
+                        *reinterpret_cast<uint4 *>(vrow + q * 16) = make_uint4(0, 0, 0, 0);
+                        *reinterpret_cast<uint4 *>(vrow + kHalf + q * 16) = make_uint4(0, 0, 0, 0);
+                    }
+                }
+            }
+            fence_proxy_async_smem();
+            tc_fence_before();
+            mbar_arrive(&bars[kPFull]);
+        }
+        if (ok && wait_or_fail(&bars[kDrain], 0, fail, a.status)) {
+            tc_fence_after();
+            const float inv = l > 0.f ? 1.f / l : 0.f;
+            __nv_bfloat16 *orow = static_cast<__nv_bfloat16 *>(a.out) +
+                                  ((size_t)(q0 + t0 + tr) * a.num_q_heads + kvh * g + (r % g)) * kD;
+#pragma unroll 1
+            for (int c = 0; c < kD; c += 32) {
+                uint32_t o[32];
+                tmem_ld32(lane_base + kColO + c, o);
+                tmem_wait_ld();
+                if (real) {
+#pragma unroll
+                    for (int q = 0; q < 4; ++q) {
+                        uint4 w;
+                        w.x = pack2_bf16(__uint_as_float(o[8 * q + 0]) * inv, __uint_as_float(o[8 * q + 1]) * inv);
+                        w.y = pack2_bf16(__uint_as_float(o[8 * q + 2]) * inv, __uint_as_float(o[8 * q + 3]) * inv);
+                        w.z = pack2_bf16(__uint_as_float(o[8 * q + 4]) * inv, __uint_as_float(o[8 * q + 5]) * inv);
+                        w.w = pack2_bf16(__uint_as_float(o[8 * q + 6]) * inv, __uint_as_float(o[8 * q + 7]) * inv);
+                        *reinterpret_cast<uint4 *>(orow + c + 8 * q) = w;
+                    }
+                }
+            }
+        }
+    }
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 1) {
+        tc_fence_after();
+        tmem_dealloc(tmem, kTmemCols);
+    }
+}
+
+PFN_cuTensorMapEncodeTiled_v12000 encoder() {
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void *p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                             &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+    });
+    return fn;
+}
+
+}  // namespace
+}  // namespace pa
+
+using namespace pa;
+
+extern "C" pa_status pa_prefill(void *out, const void *query, const void *key_cache,
+                                const void *value_cache, const int32_t *block_tables,
+                                const int32_t *context_lens, const int32_t *query_start,
+                                int num_seqs, int num_q_heads, int num_kv_heads, int head_dim,
+                                int block_size, int max_blocks_per_seq, int num_blocks,
+                                int num_query_tokens, int max_query_len, float scale,
+                                pa_dtype dtype, int window, int32_t *device_status, void *stream) {
+    if (num_seqs < 0 || num_q_heads <= 0 || num_kv_heads <= 0 || block_size != kBlockSize ||
+        max_blocks_per_seq < 0 || num_blocks <= 0 || num_q_heads % num_kv_heads != 0 ||
+        num_query_tokens < 0 || max_query_len < 0 || window < 0 || !(scale == scale))
+        return PA_ERR_INVALID_ARG;
+    if (dtype != PA_DTYPE_BF16) return PA_ERR_UNSUPPORTED;
+    const int group = num_q_heads / num_kv_heads;
+    if (head_dim != kD || (group != 1 && group != 2 && group != 4 && group != 8 && group != 16))
+        return PA_ERR_UNSUPPORTED;
+    if (num_seqs == 0 || num_query_tokens == 0 || max_query_len == 0) return PA_OK;
+    if (!out || !query || !key_cache || !value_cache || !block_tables || !context_lens ||
+        !query_start)
+        return PA_ERR_INVALID_ARG;
+    if (!aligned16(out) || !aligned16(query) || !aligned16(key_cache) || !aligned16(value_cache))
+        return PA_ERR_INVALID_ARG;
+    const int64_t rows = (int64_t)num_blocks * num_kv_heads * kBlockSize;
+    if (rows >= ((int64_t)1 << 31)) return PA_ERR_UNSUPPORTED;
+    const int64_t tiles = ((int64_t)max_query_len * group + kRows - 1) / kRows;
+    if (tiles > 0x7fffffff || num_kv_heads > 65535 || num_seqs > 65535) return PA_ERR_UNSUPPORTED;
+    auto enc = encoder();
+    if (enc == nullptr) return cuda_failure(cudaErrorInvalidValue, "cuTensorMapEncodeTiled lookup");
+
+    CUtensorMap qmap, kmap, vmap;
+    {
+        // query as [tokens][kv head][head of the group][head_dim]: a box of
+        // (128 / group) tokens x group heads x 64 elements is one 128-row tile
+        cuuint64_t dims[4] = {(cuuint64_t)kD, (cuuint64_t)group, (cuuint64_t)num_kv_heads,
+                              (cuuint64_t)num_query_tokens};
+        cuuint64_t strides[3] = {(cuuint64_t)kD * 2, (cuuint64_t)group * kD * 2,
+                                 (cuuint64_t)num_q_heads * kD * 2};
+        cuuint32_t box[4] = {64, (cuuint32_t)group, 1, (cuuint32_t)(kRows / group)};
+        cuuint32_t estr[4] = {1, 1, 1, 1};
+        if (enc(&qmap, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void *>(query), dims, strides,
+                box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+            return cuda_failure(cudaErrorInvalidValue, "cuTensorMapEncodeTiled(query)");
+    }
+    for (int which = 0; which < 2; ++which) {
+        // pool as [num_blocks * num_kv_heads * 16 rows][head_dim], 16-row boxes
+        cuuint64_t dims[2] = {(cuuint64_t)kD, (cuuint64_t)rows};
+        cuuint64_t strides[1] = {(cuuint64_t)kD * 2};
+        cuuint32_t box[2] = {64, (cuuint32_t)kBlockSize};
+        cuuint32_t estr[2] = {1, 1};
+        CUtensorMap *m = which == 0 ? &kmap : &vmap;
+        const void *pool = which == 0 ? key_cache : value_cache;
+        if (enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(pool), dims, strides,
+                box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+            return cuda_failure(cudaErrorInvalidValue, "cuTensorMapEncodeTiled(pool)");
+    }
+    PrefillArgs a;
+    a.out = out;
+    a.block_tables = block_tables;
+    a.context_lens = context_lens;
+    a.query_start = query_start;
+    a.status = device_status;
+    a.num_q_heads = num_q_heads;
+    a.num_kv_heads = num_kv_heads;
+    a.group = group;
+    a.max_blocks = max_blocks_per_seq;
+    a.num_blocks = num_blocks;
+    a.max_query_len = max_query_len;
+    a.window = window;
+    a.scale_log2 = scale * 1.4426950408889634f;
+    cudaError_t e = cudaFuncSetAttribute(pa_prefill_kernel,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+    if (e != cudaSuccess) return cuda_failure(e, "cudaFuncSetAttribute(prefill)");
+    dim3 grid((unsigned)tiles, (unsigned)num_kv_heads, (unsigned)num_seqs);
+    e = launch_chained(pa_prefill_kernel, grid, dim3(kThreads), (size_t)kSmemBytes,
+                       static_cast<cudaStream_t>(stream), qmap, kmap, vmap, a);
+    if (e != cudaSuccess) return cuda_failure(e, "pa_prefill_kernel launch");
+    count_launches(1);
+    return PA_OK;
+}

@@ -1,0 +1,137 @@
+"""GPU parity for chunked prefill: pa_prefill (tcgen05 tensor cores) through the C ABI
+against the fp64 oracle.
+
+Slots that hold no context token are NaN-poisoned, so a kernel that reads past a
+context (or, with a window, before every row's window) shows it as NaN."""
+import numpy as np
+import pytest
+
+import oracle
+import workloads as W
+from tests import helpers as H
+
+pytestmark = pytest.mark.gpu
+
+D = 128
+
+
+@pytest.fixture(scope="module")
+def pkv():
+    from paged_kv_cache_100_gb300.build import build
+    build()
+    import paged_kv_cache_100_gb300 as m
+    return m
+
+
+def _case(hq, hkv, specs, seed, window=0):
+    """specs: (cached C, chunk T) per sequence.  Returns host inputs for both sides."""
+    lens = [c + t for c, t in specs]
+    wl = W.custom_workload(len(specs), hq, hkv, D, lens, dtype="bf16", seed=seed)
+    hv = W.host_values(wl)
+    qs = np.zeros(len(specs) + 1, np.int32)
+    qs[1:] = np.cumsum([t for _, t in specs])
+    rng = np.random.default_rng(seed + 1000)
+    q = W.to_bf16_bits(rng.standard_normal((int(qs[-1]), hq, D), dtype=np.float32))
+    tables = wl.block_tables.copy()
+    if window:
+        # nothing before the first chunk row's window is needed: poison it and
+        # drop the blocks wholly before it, as a block manager's trim would
+        for b, (c, t) in enumerate(specs):
+            lo = max(0, c + 1 - window)
+            for pos in range(lo):
+                phys = int(tables[b, pos // 16])
+                hv.key_cache[phys, :, pos % 16] = 0x7FC0
+                hv.value_cache[phys, :, pos % 16] = 0x7FC0
+            tables[b, :lo // 16] = -1
+    return wl, hv, q, qs, tables, np.asarray(lens, np.int32)
+
+
+def _run(pkv, wl, hv, q, qs, tables, lens, window=0, max_query_len=None):
+    import torch
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    out = pkv.prefill(H.host_to_device(q, torch.bfloat16),
+                      H.host_to_device(hv.key_cache, torch.bfloat16),
+                      H.host_to_device(hv.value_cache, torch.bfloat16),
+                      torch.from_numpy(tables).cuda(), torch.from_numpy(lens).cuda(),
+                      torch.from_numpy(qs).cuda(), max_query_len, wl.scale, window=window,
+                      status=status)
+    torch.cuda.synchronize()
+    return out, int(status.item())
+
+
+def _oracle(wl, hv, q, qs, tables, lens, window=0):
+    return oracle.paged_prefill(q, hv.key_cache, hv.value_cache, tables, lens, qs, wl.scale,
+                                threads=8, window=window)
+
+
+SPECS = [(0, 1), (0, 5), (0, 127), (0, 128), (0, 129), (17, 50), (300, 200), (1000, 31)]
+
+
+@pytest.mark.parametrize("hq,hkv", [(4, 4), (8, 4), (8, 2), (16, 2), (16, 1)])
+def test_prefill_matches_oracle(pkv, hq, hkv):
+    wl, hv, q, qs, tables, lens = _case(hq, hkv, SPECS, seed=hq * 10 + hkv)
+    got, st = _run(pkv, wl, hv, q, qs, tables, lens)
+    assert st == 0
+    H.assert_close(H.as_f64(got), _oracle(wl, hv, q, qs, tables, lens), "bf16",
+                   f"prefill {hq}/{hkv}")
+
+
+def test_long_fresh_prompt_spans_many_tiles(pkv):
+    specs = [(0, 700), (0, 260)]
+    wl, hv, q, qs, tables, lens = _case(8, 8, specs, seed=5)
+    got, st = _run(pkv, wl, hv, q, qs, tables, lens)
+    assert st == 0
+    H.assert_close(H.as_f64(got), _oracle(wl, hv, q, qs, tables, lens), "bf16", "long prompt")
+
+
+@pytest.mark.parametrize("window", [1, 16, 100, 300])
+def test_prefill_sliding_window_matches_oracle(pkv, window):
+    specs = [(0, 64), (40, 90), (500, 140), (33, 1)]
+    wl, hv, q, qs, tables, lens = _case(8, 2, specs, seed=window, window=window)
+    got, st = _run(pkv, wl, hv, q, qs, tables, lens, window=window)
+    assert st == 0
+    H.assert_close(H.as_f64(got), _oracle(wl, hv, q, qs, tables, lens, window), "bf16",
+                   f"prefill window {window}")
+
+
+def test_first_row_of_a_fresh_prompt_is_its_own_value(pkv):
+    """Position 0 attends to itself alone: the output is that V row, rounded to bf16."""
+    specs = [(0, 3), (0, 200)]
+    wl, hv, q, qs, tables, lens = _case(8, 2, specs, seed=21)
+    got, st = _run(pkv, wl, hv, q, qs, tables, lens)
+    bits = H.device_to_host_bits(got)
+    for b in range(2):
+        phys = int(tables[b, 0])
+        for h in range(8):
+            assert np.array_equal(bits[qs[b], h], hv.value_cache[phys, h // 4, 0])
+
+
+def test_chunked_equals_whole_prompt(pkv):
+    """A prompt prefilled in two chunks gives the rows of the one-chunk prefill."""
+    import torch
+    wl, hv, q, qs, tables, lens = _case(8, 2, [(0, 300)], seed=31)
+    whole, _ = _run(pkv, wl, hv, q, qs, tables, lens)
+    cut = 137
+    first, _ = _run(pkv, wl, hv, q[:cut], np.array([0, cut], np.int32), tables,
+                    np.array([cut], np.int32))
+    second, _ = _run(pkv, wl, hv, q[cut:], np.array([0, 300 - cut], np.int32), tables, lens)
+    both = torch.cat([first, second])
+    ref = _oracle(wl, hv, q, qs, tables, lens)
+    H.assert_close(H.as_f64(both), ref, "bf16", "two chunks")
+    H.assert_close(H.as_f64(whole), ref, "bf16", "one chunk")
+
+
+def test_too_long_chunk_is_flagged(pkv):
+    wl, hv, q, qs, tables, lens = _case(4, 4, [(0, 300)], seed=41)
+    _, st = _run(pkv, wl, hv, q, qs, tables, lens, max_query_len=100)
+    assert st & 64                                   # PA_DEV_BAD_QUERY_LEN
+
+
+def test_unsupported_shapes_fail_loudly(pkv):
+    import torch
+    q = torch.zeros(4, 6, D, dtype=torch.bfloat16, device="cuda")
+    kc = torch.zeros(4, 2, 16, D, dtype=torch.bfloat16, device="cuda")      # group 3
+    qs = torch.tensor([0, 4], dtype=torch.int32, device="cuda")
+    with pytest.raises(pkv.PagedKVError):
+        pkv.prefill(q, kc, kc, torch.zeros(1, 1, dtype=torch.int32, device="cuda"),
+                    torch.tensor([4], dtype=torch.int32, device="cuda"), qs, 4)
