@@ -32,6 +32,8 @@ if ROOT not in sys.path:
 import workloads as W  # noqa: E402
 
 METRIC = "paged decode attention tokens/s and KV GB/s (% of GB300 HBM peak), 1 GPU"
+PREFILL_METRIC = ("chunked paged prefill attention query tokens/s and TFLOP/s "
+                  "(% of GB300 bf16 tensor peak), 1 GPU")
 NOMINAL_HBM_GBS = 7900.0     # GB300 HBM3e nominal
 FALLBACK_HBM_GBS = 6800.0    # earlier GB300 measurement, used only without MEASURED_PEAKS.json
 L2_BYTES = 129 * 10**6
@@ -660,12 +662,298 @@ def run_reference(args):
     }
 
 
+# ---------------------------------------------------------------------------
+# Chunked prefill ("PagedAttention por dentro", "Chunked prefill integrado con
+# paged KV"): a step is the cache write of every chunk token's K/V followed by
+# causal attention of the chunk rows over their paged contexts.
+# ---------------------------------------------------------------------------
+def prefill_pairs(pw, window=0) -> int:
+    """(query row, attended position) pairs of one query head over the batch."""
+    total = 0
+    for b in range(pw.num_seqs):
+        p = np.arange(int(pw.cached[b]), int(pw.cached[b] + pw.chunk[b]), dtype=np.int64)
+        n = p + 1
+        if window:
+            n = np.minimum(n, window)
+        total += int(n.sum())
+    return total
+
+
+def prefill_flops(pw, window=0) -> int:
+    """QK^T and PV over the attended pairs: 2 * 2 * head_dim flops per pair and head."""
+    return 4 * pw.head_dim * pw.num_q_heads * prefill_pairs(pw, window)
+
+
+def load_tensor_peak():
+    """Measured cuBLAS bf16 throughput, sustained (the prefill loop runs for seconds)."""
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            p = json.load(f)
+        return float(p["bf16_tflops_sustained"]), "measured sustained"
+    except Exception:
+        return 1700.0, "fallback sustained"
+
+
+def prefill_config(pw, world, window):
+    cfg = {
+        "workload": pw.name + (f"+window{window}" if window else ""),
+        "num_seqs_per_gpu": pw.num_seqs,
+        "global_batch": pw.num_seqs * world,
+        "query_tokens_per_gpu": pw.num_tokens,
+        "num_q_heads": pw.num_q_heads,
+        "num_kv_heads": pw.num_kv_heads,
+        "head_dim": pw.head_dim,
+        "block_size": pw.block_size,
+        "cached_min_max_mean": [int(pw.cached.min()), int(pw.cached.max()), float(pw.cached.mean())],
+        "chunk_min_max": [int(pw.chunk.min()), int(pw.chunk.max())],
+        "num_blocks": pw.num_blocks,
+        "parallelism": f"weak scaling, {world} independent replica(s)",
+        "l2": "inputs larger than L2: %.2f GB of K/V pools vs 129 MB L2"
+              % (2 * np.prod(pw.pool_shape()) * 2 / 1e9),
+    }
+    if window:
+        cfg["window"] = window
+    return cfg
+
+
+def run_prefill_gpu(args):
+    import torch
+    rank, world, local = dist_env()
+    if world > 1:
+        torch.cuda.set_device(local)
+        init_dist("nccl")
+    dev = torch.device("cuda", local if world > 1 else 0)
+    torch.cuda.set_device(dev)
+    from paged_kv_cache_100_gb300.build import build
+    if rank == 0 or world == 1:
+        build()
+    barrier()
+    import paged_kv_cache_100_gb300 as pkv
+
+    pw = W.make_prefill_workload(args.workload, seed=args.seed)
+    q, kc, vc, kn, vn = W.prefill_device_values(pw, dev, seed=args.seed + 17 + rank)
+    bt = torch.from_numpy(pw.block_tables).to(dev)
+    lens = torch.from_numpy(pw.context_lens).to(dev)
+    qs = torch.from_numpy(pw.query_start).to(dev)
+    slots = torch.from_numpy(pw.slot_mapping).to(dev)
+    maxq = int(pw.chunk.max())
+    out = torch.empty_like(q)
+    stream = torch.cuda.current_stream(dev)
+    window = args.window
+
+    def step(ev_pre=None, ev_post=None, q_=q, kn_=kn, vn_=vn, slots_=slots, bt_=bt, lens_=lens,
+             qs_=qs):
+        pkv.cache_write(kc, vc, kn_, vn_, slots_)
+        if ev_pre is not None:
+            ev_pre.record(stream)
+        pkv.prefill(q_, kc, vc, bt_, lens_, qs_, maxq, pw.scale, window=window, out=out)
+        if ev_post is not None:
+            ev_post.record(stream)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize(dev)
+    K = args.steps
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    sampler = ClockSampler(dev.index or 0, pci_bus_id(dev)) if rank == 0 else None
+    barrier()
+    torch.cuda.synchronize(dev)
+    launches0 = pkv.launch_count()
+    if sampler:
+        sampler.start()
+    e0.record(stream)
+    for _ in range(K):
+        step()
+    e1.record(stream)
+    torch.cuda.synchronize(dev)
+    barrier()
+    launches = pkv.launch_count() - launches0
+    pre = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
+    post = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
+    for i in range(K):
+        step(pre[i], post[i])
+    torch.cuda.synchronize(dev)
+    barrier()
+    clocks = sampler.stop() if sampler else None
+    ms_per_step = max_over_ranks(e0.elapsed_time(e1), dev) / K
+    prefill_ms = max_over_ranks(sum(a_.elapsed_time(b_) for a_, b_ in zip(pre, post)) / K, dev)
+
+    # end to end: chunk inputs from pinned host memory, output back, every step
+    host = {"q": q.cpu().pin_memory(), "kn": kn.cpu().pin_memory(), "vn": vn.cpu().pin_memory(),
+            "slots": torch.from_numpy(pw.slot_mapping).pin_memory(),
+            "bt": torch.from_numpy(pw.block_tables).pin_memory(),
+            "lens": torch.from_numpy(pw.context_lens).pin_memory(),
+            "qs": torch.from_numpy(pw.query_start).pin_memory()}
+    devb = {k: torch.empty_like(v, device=dev) for k, v in host.items()}
+    out_host = torch.empty(out.shape, dtype=out.dtype).pin_memory()
+
+    def e2e_step():
+        for k, v in host.items():
+            devb[k].copy_(v, non_blocking=True)
+        step(q_=devb["q"], kn_=devb["kn"], vn_=devb["vn"], slots_=devb["slots"], bt_=devb["bt"],
+             lens_=devb["lens"], qs_=devb["qs"])
+        out_host.copy_(out, non_blocking=True)
+
+    for _ in range(3):
+        e2e_step()
+    torch.cuda.synchronize(dev)
+    KE = max(1, min(K, args.e2e_steps))
+    barrier()
+    e2 = torch.cuda.Event(enable_timing=True)
+    e3 = torch.cuda.Event(enable_timing=True)
+    e2.record(stream)
+    for _ in range(KE):
+        e2e_step()
+    e3.record(stream)
+    torch.cuda.synchronize(dev)
+    barrier()
+    e2e_ms = max_over_ranks(e2.elapsed_time(e3) / KE, dev)
+    if rank != 0:
+        return None
+    flops = prefill_flops(pw, window)
+    peak, peak_kind = load_tensor_peak()
+    achieved = flops / (prefill_ms * 1e-3) / 1e12
+    line = {
+        "metric": PREFILL_METRIC,
+        "value": pw.num_tokens * world / (ms_per_step * 1e-3),
+        "unit": "tokens/s",
+        "n_gpus": world,
+        "steps": K,
+        "warmup": args.warmup,
+        "ms_per_step": ms_per_step,
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "bf16",
+        "data": "synthetic (seeded; N(0, %g) values, shuffled block pool)" % pw.value_std,
+        "config": prefill_config(pw, world, window),
+        "prefill_ms": prefill_ms,
+        "roofline": {
+            "kernel": "pa_prefill_kernel (tcgen05 S = QK^T and O = PV, TMEM accumulators)",
+            "bound": "tensor",
+            "achieved": achieved,
+            "peak": peak,
+            "peak_source": f"{peak_kind} (MEASURED_PEAKS.json bf16_tflops_sustained)",
+            "unit": "TFLOP/s",
+            "frac": achieved / peak,
+            "traffic": None,
+            "algorithmic_flops_per_call": flops,
+            "flops_rule": "4 * head_dim flops per (query row, query head, attended position): "
+                          "causal pairs only, masked tile halves not counted",
+        },
+        "gpu_launches": int(launches),
+        "clocks": clocks,
+        "e2e": {"value": pw.num_tokens * world / (e2e_ms * 1e-3), "unit": "tokens/s",
+                "ms_per_step": e2e_ms, "steps": KE,
+                "h2d_bytes_per_step": int(sum(v.numel() * v.element_size() for v in host.values())),
+                "d2h_bytes_per_step": int(out.numel() * out.element_size())},
+    }
+    if not args.no_cpu_baseline and world == 1:
+        line["cpu_baseline"] = prefill_cpu_baseline(pw, q, kc, vc, args.cpu_seconds, window)
+    return line
+
+
+def _prefill_sample(pw, rows=16):
+    """The last ``rows`` chunk rows of the sequence with the longest context."""
+    b = int(np.argmax(pw.context_lens))
+    L = int(pw.context_lens[b])
+    rows = min(rows, int(pw.chunk[b]))
+    r0 = int(pw.query_start[b] + pw.chunk[b]) - rows
+    return b, L, rows, r0
+
+
+def prefill_cpu_baseline(pw, q, kc, vc, budget_s, window):
+    import torch
+    import oracle
+    threads = oracle.max_threads()
+    b, L, rows, r0 = _prefill_sample(pw)
+    need = -(-L // 16)
+    used = pw.block_tables[b, :need]
+    idx = torch.from_numpy(used.astype(np.int64)).to(kc.device)
+    kch, vch = _bits(kc.index_select(0, idx)), _bits(vc.index_select(0, idx))
+    qh = _bits(q[r0:r0 + rows])
+    tab = np.arange(need, dtype=np.int32)[None]
+    t0 = time.perf_counter()
+    reps = 0
+    while True:
+        oracle.paged_prefill(qh, kch, vch, tab, np.array([L], np.int32),
+                             np.array([0, rows], np.int32), pw.scale, threads=threads,
+                             window=window)
+        reps += 1
+        if time.perf_counter() - t0 >= budget_s:
+            break
+    dt = time.perf_counter() - t0
+    pos = np.arange(L - rows, L, dtype=np.int64) + 1
+    sample_pairs = int((np.minimum(pos, window) if window else pos).sum())
+    t_batch = dt / reps * prefill_pairs(pw, window) / sample_pairs
+    return {"value": pw.num_tokens / t_batch, "unit": "tokens/s", "cores": threads,
+            "kind": "oracle",
+            "sample": f"last {rows} chunk rows of the longest sequence (context {L}, all "
+                      f"{pw.num_q_heads} heads) x {reps} repetitions in {dt:.1f} s; time scaled "
+                      "to the batch by attended (row, position) pairs"}
+
+
+def run_prefill_reference(args):
+    rank, world, _ = dist_env()
+    if world > 1 and rank != 0:
+        return None
+    import oracle
+    oracle.build()
+    pw = W.make_prefill_workload(args.workload, seed=args.seed)
+    threads = oracle.max_threads()
+    b, L, rows, r0 = _prefill_sample(pw)
+    need = -(-L // 16)
+    vrng = np.random.Generator(np.random.PCG64(args.seed + 99))
+
+    def draw(shape):
+        return W.to_bf16_bits(vrng.standard_normal(shape, dtype=np.float32) * np.float32(pw.value_std))
+
+    kch = draw((need, pw.num_kv_heads, 16, pw.head_dim))
+    vch = draw((need, pw.num_kv_heads, 16, pw.head_dim))
+    qh = draw((rows, pw.num_q_heads, pw.head_dim))
+    tab = np.arange(need, dtype=np.int32)[None]
+    lens, qs = np.array([L], np.int32), np.array([0, rows], np.int32)
+    for _ in range(args.warmup):
+        oracle.paged_prefill(qh[:1], kch, vch, tab, np.array([L - rows + 1], np.int32),
+                             np.array([0, 1], np.int32), pw.scale, threads=threads,
+                             window=args.window)
+    t0 = time.perf_counter()
+    deadline = t0 + args.reference_seconds
+    done = 0
+    for _ in range(args.steps):
+        oracle.paged_prefill(qh, kch, vch, tab, lens, qs, pw.scale, threads=threads,
+                             window=args.window)
+        done += 1
+        if time.perf_counter() > deadline:
+            break
+    dt = time.perf_counter() - t0
+    pos = np.arange(L - rows, L, dtype=np.int64) + 1
+    sample_pairs = int((np.minimum(pos, args.window) if args.window else pos).sum())
+    value = pw.num_tokens / (dt / done * prefill_pairs(pw, args.window) / sample_pairs)
+    return {
+        "impl": "reference", "metric": PREFILL_METRIC, "value": value, "unit": "tokens/s",
+        "n_gpus": world, "steps": done, "warmup": args.warmup,
+        "ms_per_step": dt / max(done, 1) * 1e3, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f64", "data": "synthetic (seeded)",
+        "config": prefill_config(pw, world, args.window),
+        "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": threads, "kind": "oracle",
+                         "sample": f"{done} steps, each the last {rows} chunk rows of the longest "
+                                   f"sequence (context {L}); rate scaled to the batch by "
+                                   "attended (row, position) pairs"},
+        "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+
+
 def main(argv=None):
     ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=3000)
     ap.add_argument("--warmup", type=int, default=50)
-    ap.add_argument("--workload", default="llama7b_mha", choices=W.WORKLOADS)
+    ap.add_argument("--op", default="decode", choices=["decode", "prefill"],
+                    help="decode (default) or chunked prefill (--workload prefill_*)")
+    ap.add_argument("--workload", default=None, choices=W.WORKLOADS + W.PREFILL_WORKLOADS)
     ap.add_argument("--partition-size", type=int, default=0)
     ap.add_argument("--window", type=int, default=0,
                     help="> 0: sliding-window decode over the last WINDOW positions")
@@ -683,7 +971,16 @@ def main(argv=None):
     args = ap.parse_args(argv)
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")
-    line = run_reference(args) if args.impl == "reference" else run_gpu(args)
+    if args.op == "prefill":
+        args.workload = args.workload or "prefill_llama70b_chunked"
+        if args.workload not in W.PREFILL_WORKLOADS:
+            ap.error("--op prefill takes a prefill_* workload")
+        line = run_prefill_reference(args) if args.impl == "reference" else run_prefill_gpu(args)
+    else:
+        args.workload = args.workload or "llama7b_mha"
+        if args.workload not in W.WORKLOADS:
+            ap.error("--op decode takes a decode workload")
+        line = run_reference(args) if args.impl == "reference" else run_gpu(args)
     if line is not None:
         print(json.dumps(line), flush=True)
     try:

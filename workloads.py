@@ -160,6 +160,122 @@ def make_workload(name: str, seed: int = 0) -> Workload:
 WORKLOADS = ("tiny", "llama7b_mha", "llama70b_gqa", "long_splitk", "shared_prefix")
 
 
+# ---------------------------------------------------------------------------
+# Chunked prefill ("PagedAttention por dentro", section "Chunked prefill
+# integrado con paged KV")
+# ---------------------------------------------------------------------------
+@dataclass
+class PrefillWorkload:
+    """Sequences that each bring a chunk of new tokens on top of a cached context."""
+    name: str
+    num_seqs: int
+    num_q_heads: int
+    num_kv_heads: int
+    head_dim: int
+    value_std: float
+    cached: np.ndarray              # int32 [B]: tokens already in the cache
+    chunk: np.ndarray               # int32 [B]: new tokens of this step
+    block_tables: np.ndarray        # int32 [B][max_blocks]
+    num_blocks: int
+    seed: int = 0
+    dtype: str = "bf16"
+    block_size: int = BLOCK_SIZE
+
+    @property
+    def scale(self) -> float:
+        return 1.0 / math.sqrt(self.head_dim)
+
+    @property
+    def group(self) -> int:
+        return self.num_q_heads // self.num_kv_heads
+
+    @property
+    def max_blocks(self) -> int:
+        return self.block_tables.shape[1]
+
+    @property
+    def elem_bytes(self) -> int:
+        return 2
+
+    @property
+    def context_lens(self) -> np.ndarray:
+        return (self.cached + self.chunk).astype(np.int32)
+
+    @property
+    def query_start(self) -> np.ndarray:
+        qs = np.zeros(self.num_seqs + 1, dtype=np.int32)
+        qs[1:] = np.cumsum(self.chunk)
+        return qs
+
+    @property
+    def num_tokens(self) -> int:
+        return int(self.chunk.sum())
+
+    @property
+    def slot_mapping(self) -> np.ndarray:
+        """int64 [num_tokens]: slot of every chunk token (positions C .. C+T-1)."""
+        out = []
+        for b in range(self.num_seqs):
+            pos = np.arange(int(self.cached[b]), int(self.cached[b] + self.chunk[b]), dtype=np.int64)
+            out.append(self.block_tables[b, pos // BLOCK_SIZE].astype(np.int64) * BLOCK_SIZE
+                       + pos % BLOCK_SIZE)
+        return np.concatenate(out) if out else np.zeros(0, np.int64)
+
+    def pool_shape(self):
+        return (self.num_blocks, self.num_kv_heads, self.block_size, self.head_dim)
+
+
+def make_prefill_workload(name: str, seed: int = 0) -> PrefillWorkload:
+    """prefill_llama7b: 8 fresh 2048-token prompts, 32 heads MHA, head_dim 128;
+    prefill_llama70b_chunked: 16 sequences of 64 query / 8 KV heads, each bringing a
+    512-token chunk on top of a cached context uniform in [0, 8192] (multiples of
+    16).  bf16, N(0, 1) values, tables are slices of a shuffled pool 1.1x the blocks
+    in use."""
+    rng = np.random.Generator(np.random.PCG64(seed))
+    if name == "prefill_llama7b":
+        B, Hq, Hkv, std = 8, 32, 32, 1.0
+        cached = np.zeros(B, dtype=np.int32)
+        chunk = np.full(B, 2048, dtype=np.int32)
+    elif name == "prefill_llama70b_chunked":
+        B, Hq, Hkv, std = 16, 64, 8, 1.0
+        cached = (rng.integers(0, 512, size=B, endpoint=True) * 16).astype(np.int32)
+        chunk = np.full(B, 512, dtype=np.int32)
+    elif name == "prefill_tiny":
+        B, Hq, Hkv, std = 3, 8, 2, 1.0
+        cached = np.array([0, 37, 200], dtype=np.int32)
+        chunk = np.array([70, 19, 130], dtype=np.int32)
+    else:
+        raise KeyError(f"unknown prefill workload {name!r}")
+    need = _blocks(cached.astype(np.int64) + chunk)
+    num_blocks = int(math.ceil(1.1 * int(need.sum()))) + 1
+    order = rng.permutation(num_blocks).astype(np.int32)
+    tables = _tables_from_slices(order, need)
+    return PrefillWorkload(name, B, Hq, Hkv, 128, std, cached, chunk, tables, num_blocks, seed)
+
+
+PREFILL_WORKLOADS = ("prefill_llama7b", "prefill_llama70b_chunked", "prefill_tiny")
+
+
+def prefill_device_values(pw: PrefillWorkload, device, seed: int | None = None):
+    """(query, key_cache, value_cache, key_new, value_new) in bf16 on a CUDA device,
+    drawn with a seeded torch generator (values N(0, value_std))."""
+    import torch
+    g = torch.Generator(device=device)
+    g.manual_seed(pw.seed + 7 if seed is None else seed)
+
+    def draw(shape):
+        x = torch.randn(shape, generator=g, device=device, dtype=torch.float32)
+        return (x * pw.value_std).to(torch.bfloat16)
+
+    N = pw.num_tokens
+    q = draw((N, pw.num_q_heads, pw.head_dim))
+    kc = draw(pw.pool_shape())
+    vc = draw(pw.pool_shape())
+    kn = draw((N, pw.num_kv_heads, pw.head_dim))
+    vn = draw((N, pw.num_kv_heads, pw.head_dim))
+    return q, kc, vc, kn, vn
+
+
 def custom_workload(num_seqs, num_q_heads, num_kv_heads, head_dim, context_lens, dtype="bf16",
                     value_std=1.0, spare_blocks=4, seed=0, name="custom") -> Workload:
     """A workload with given lengths; block tables are slices of a shuffled pool."""
