@@ -73,6 +73,7 @@ typedef enum pa_dtype {
 #define PA_DEV_TIMEOUT        16  /* a bounded in-kernel wait gave up */
 #define PA_DEV_PREFIX_MISMATCH 32 /* pa_decode_shared_prefix: tables do not share the prefix */
 #define PA_DEV_BAD_QUERY_LEN  64  /* pa_prefill: a chunk longer than max_query_len */
+#define PA_DEV_SMEM_ALIGN    128  /* pa_prefill: shared memory not 1024-byte aligned (nothing computed) */
 
 /* Human-readable name of a status. Never NULL. */
 const char *pa_status_string(pa_status status);

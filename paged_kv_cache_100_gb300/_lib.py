@@ -95,6 +95,7 @@ PA_DEV_BAD_COPY_PAIR = 8
 PA_DEV_TIMEOUT = 16
 PA_DEV_PREFIX_MISMATCH = 32
 PA_DEV_BAD_QUERY_LEN = 64
+PA_DEV_SMEM_ALIGN = 128
 
 
 class PagedKVError(RuntimeError):

@@ -18,10 +18,13 @@
 //   warp 1      MMA issuer: S = Q K^T into tensor memory (two S buffers), then
 //               O += P V into a tensor-memory accumulator; owns the TMEM
 //               allocation;
-//   warps 2..5  softmax: one thread per row (= TMEM lane) reads its S row,
-//               keeps the running maximum and sum, writes P (bf16 head and bf16
-//               residual) to shared memory, rescales O in tensor memory only
-//               when the maximum grew by more than 2^8, and writes the output.
+//   warps 2..9  softmax: two threads per row (= TMEM lane), each owning 64 of
+//               the 128 columns of S and of O.  They agree on the row maximum
+//               through shared memory once per tile, keep their part of the
+//               running sum, write P (bf16 head and bf16 residual) to shared
+//               memory, rescale their half of O in tensor memory only when the
+//               maximum grew by more than 2^8, and write their half of the
+//               output row.
 // Every wait is bounded (about a second); a wait that gives up sets
 // PA_DEV_TIMEOUT and the CTA drains its tensor-core work and returns.
 #include <cuda.h>
@@ -44,7 +47,8 @@ constexpr int kKv = 128;                 // N: K/V positions per step (8 blocks)
 constexpr int kD = 128;                  // head_dim
 constexpr int kHalf = 16384;             // one 64-column swizzled region of a tile
 constexpr int kTile = 2 * kHalf;         // 128 rows x 256 bytes
-constexpr int kThreads = 192;
+constexpr int kThreads = 320;            // 2 + 8 warps
+constexpr int kSoftmaxThreads = 256;
 constexpr float kRescaleLog2 = 8.0f;     // lazy rescale threshold (factor 256)
 
 // shared memory map (offsets from a 1024-byte aligned base)
@@ -54,7 +58,11 @@ constexpr int kOffV = kOffK + 2 * kTile;        // two stages
 constexpr int kOffP = kOffV + 2 * kTile;        // P head, then P residual
 constexpr int kOffBar = kOffP + 2 * kTile;
 constexpr int kNumBars = 16;
-constexpr int kSmemBytes = kOffBar + kNumBars * 8 + 16 + 1024;   // + slot, flag, alignment
+constexpr int kOffRed = kOffBar + 256;          // row-maximum exchange [2 tiles][2 halves][128]
+constexpr int kSmemBytes = kOffRed + 2 * 2 * kRows * 4;
+// The tiles need 1024-byte alignment; the dynamic shared memory of a kernel
+// without static shared memory starts on such a boundary, and the kernel
+// checks it (PA_DEV_SMEM_ALIGN) instead of reserving slack it has no room for.
 
 // barrier indices
 constexpr int kQFull = 0, kKFull = 1, kKEmpty = 3, kVFull = 5, kVEmpty = 7, kSFull = 9,
@@ -87,6 +95,20 @@ __device__ __forceinline__ bool wait_or_fail(uint64_t *bar, uint32_t parity, vol
     *fail = 1;
     report(status, PA_DEV_TIMEOUT);
     return false;
+}
+
+// A bounded wait whose outcome is the same for every lane of the warp, so
+// that the .sync.aligned tensor-memory instructions after it stay convergent.
+__device__ __forceinline__ bool warp_wait(uint64_t *bar, uint32_t parity, volatile int *fail,
+                                          int32_t *status) {
+    return __all_sync(0xffffffffu, wait_or_fail(bar, parity, fail, status));
+}
+
+// 2^x (ex2.approx.ftz: about 2 ulp; 2^-inf = +0)
+__device__ __forceinline__ float ex2_approx(float x) {
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
 }
 
 __device__ __forceinline__ uint32_t pack2_bf16(float lo, float hi) {
@@ -125,9 +147,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int blk_hi = (kv_hi + kBlockSize - 1) / kBlockSize;
     const int n_tiles = (blk_hi - blk_lo + 7) / 8;
 
-    extern __shared__ uint8_t smem_raw[];
-    const uint32_t raw_u = smem_u32(smem_raw);
-    uint8_t *base = smem_raw + (((raw_u + 1023u) & ~1023u) - raw_u);
+    extern __shared__ __align__(1024) uint8_t smem_raw[];
+    if (smem_u32(smem_raw) & 1023u) {
+        if (threadIdx.x == 0) report(a.status, PA_DEV_SMEM_ALIGN);
+        return;
+    }
+    uint8_t *base = smem_raw;
     uint8_t *sQ = base + kOffQ;
     uint8_t *sK = base + kOffK;
     uint8_t *sV = base + kOffV;
@@ -146,9 +171,9 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_init(&bars[kVFull + s], 1);
             mbar_init(&bars[kVEmpty + s], 1);
             mbar_init(&bars[kSFull + s], 1);
-            mbar_init(&bars[kSFree + s], 128);
+            mbar_init(&bars[kSFree + s], kSoftmaxThreads);
         }
-        mbar_init(&bars[kPFull], 128);
+        mbar_init(&bars[kPFull], kSoftmaxThreads);
         mbar_init(&bars[kPvDone], 1);
         mbar_init(&bars[kDrain], 1);
         *fail = 0;
@@ -265,136 +290,148 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
         }
     } else {
-        // ---------------- softmax warpgroup ----------------
+        // ---------------- softmax warps ----------------
         const int quarter = warp & 3;
+        const int half = (warp - 2) >> 2;             // columns [64 * half, 64 * half + 64)
         const int r = quarter * 32 + lane;            // tile row = TMEM lane
         const int tr = r / g;
         const bool real = tr < ntok;
         const int qpos = C + t0 + min(tr, ntok - 1);
         const int wlo = a.window > 0 ? qpos + 1 - a.window : INT_MIN;   // first allowed position
-        const uint32_t lane_base = tmem + ((uint32_t)(quarter * 32) << 16);
-        uint8_t *prow_hi = sP + (r >> 3) * 1024 + (r & 7) * 128;
+        const uint32_t lane_base = tmem + ((uint32_t)(quarter * 32) << 16) + half * 64;
+        float *red = reinterpret_cast<float *>(base + kOffRed);
+        uint8_t *prow = sP + half * kHalf + (r >> 3) * 1024 + (r & 7) * 128;
         const float sl2 = a.scale_log2;
         float m_used = -INFINITY, l = 0.f;
+        // Every softmax thread runs every iteration and reaches the named
+        // barrier the same number of times, even after a wait gave up (then it
+        // only skips the work), so that no barrier can wait forever.
         bool ok = true;
         for (int j = 0; j < n_tiles; ++j) {
             const int s = j & 1;
-            if (!wait_or_fail(&bars[kSFull + s], (j >> 1) & 1, fail, a.status)) {
-                ok = false;
-                break;
-            }
-            tc_fence_after();
-            const int k0 = (blk_lo + 8 * j) * kBlockSize;
-            const bool masked = (k0 + kKv - 1 > qpos_lo) ||
-                                (a.window > 0 && k0 < qpos_hi + 1 - a.window);
-            const uint32_t srow = lane_base + s * kKv;
-            // pass 1: row maximum of the valid scores
-            float mx = -INFINITY;
-#pragma unroll 1
-            for (int c = 0; c < kKv; c += 32) {
-                uint32_t v[32];
-                tmem_ld32(srow + c, v);
-                tmem_wait_ld();
+            const bool got = ok && warp_wait(&bars[kSFull + s], (j >> 1) & 1, fail, a.status);
+            const int k0 = (blk_lo + 8 * j) * kBlockSize + half * 64;   // position of column 0
+            const bool masked = (k0 + 63 > qpos_lo) || (a.window > 0 && k0 < qpos_hi + 1 - a.window);
+            uint32_t v[64];
+            if (!got) {
 #pragma unroll
-                for (int i = 0; i < 32; ++i) {
-                    const int kp = k0 + c + i;
-                    const bool valid = !masked || (kp <= qpos && kp >= wlo);
-                    mx = fmaxf(mx, valid ? __uint_as_float(v[i]) : -INFINITY);
+                for (int i = 0; i < 64; ++i) v[i] = __float_as_uint(-INFINITY);
+            } else {
+                tc_fence_after();
+                uint32_t (&v0)[32] = *reinterpret_cast<uint32_t (*)[32]>(&v[0]);
+                uint32_t (&v1)[32] = *reinterpret_cast<uint32_t (*)[32]>(&v[32]);
+                tmem_ld32(lane_base + s * kKv, v0);
+                tmem_ld32(lane_base + s * kKv + 32, v1);
+                tmem_wait_ld();
+                // S is in registers: the buffer can take the next product
+                tc_fence_before();
+                mbar_arrive(&bars[kSFree + s]);
+            }
+            if (masked) {
+#pragma unroll
+                for (int i = 0; i < 64; ++i) {
+                    const int kp = k0 + i;
+                    if (!(kp <= qpos && kp >= wlo)) v[i] = __float_as_uint(-INFINITY);
                 }
             }
-            const float m_tile = mx * sl2;
+            // row maximum: four independent chains, then the partner's half
+            float mx4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+#pragma unroll
+            for (int i = 0; i < 64; ++i) mx4[i & 3] = fmaxf(mx4[i & 3], __uint_as_float(v[i]));
+            const float mine = fmaxf(fmaxf(mx4[0], mx4[1]), fmaxf(mx4[2], mx4[3]));
+            red[(s * 2 + half) * kRows + r] = mine;
+            asm volatile("bar.sync 1, %0;" ::"n"(kSoftmaxThreads) : "memory");
+            const float other = red[(s * 2 + (half ^ 1)) * kRows + r];
+            if (!got) {
+                ok = false;
+                continue;
+            }
+            const float m_tile = fmaxf(mine, other) * sl2;
             const float m_new = fmaxf(m_used, m_tile);
             // P of the previous tile must have been consumed (and O updated)
             // before P is overwritten or O rescaled.
-            if (j >= 1 && !wait_or_fail(&bars[kPvDone], (j - 1) & 1, fail, a.status)) {
+            if (j >= 1 && !warp_wait(&bars[kPvDone], (j - 1) & 1, fail, a.status)) {
                 ok = false;
-                break;
+                continue;
             }
-            if (m_new > m_used + kRescaleLog2) {
-                const float alpha = exp2f(m_used - m_new);   // 0 while m_used is -inf
-                if (j >= 1) {
-                    tc_fence_after();
+            // Lazy rescale: only rows whose maximum grew by more than 2^8 move
+            // their reference; the warp rescales O together (tensor-memory
+            // access is warp-wide), with factor 1 on the other rows.
+            const bool need = m_new > m_used + kRescaleLog2;
+            const float alpha = need ? exp2f(m_used - m_new) : 1.f;   // 0 while m_used is -inf
+            if (j >= 1 && __any_sync(0xffffffffu, need)) {
+                tc_fence_after();
 #pragma unroll 1
-                    for (int c = 0; c < kD; c += 32) {
-                        uint32_t o[32];
-                        tmem_ld32(lane_base + kColO + c, o);
-                        tmem_wait_ld();
+                for (int c = 0; c < 64; c += 32) {
+                    uint32_t o[32];
+                    tmem_ld32(lane_base + kColO + c, o);
+                    tmem_wait_ld();
 #pragma unroll
-                        for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * alpha);
-                        tmem_st32(lane_base + kColO + c, o);
-                    }
-                    tmem_wait_st();
+                    for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * alpha);
+                    tmem_st32(lane_base + kColO + c, o);
                 }
+                tmem_wait_st();
+            }
+            if (need) {
                 l *= alpha;
                 m_used = m_new;
             }
             const float m_ref = m_used == -INFINITY ? 0.f : m_used;
-            // pass 2: P = 2^(s * scale_log2 - m_ref), bf16 head + bf16 residual
-            float psum = 0.f;
-#pragma unroll 1
-            for (int c = 0; c < kKv; c += 32) {
-                uint32_t v[32];
-                tmem_ld32(srow + c, v);
-                tmem_wait_ld();
-                uint32_t hi[16], lo[16];
+            // P = 2^(s * scale_log2 - m_ref) as a bf16 head + bf16 residual
+            float ps4[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-                for (int i = 0; i < 32; i += 2) {
-                    float p2[2];
+            for (int c = 0; c < 64; c += 8) {
+                uint32_t hi[4], lo[4];
 #pragma unroll
-                    for (int e = 0; e < 2; ++e) {
-                        const int kp = k0 + c + i + e;
-                        const bool valid = !masked || (kp <= qpos && kp >= wlo);
-                        p2[e] = valid ? exp2f(fmaf(__uint_as_float(v[i + e]), sl2, -m_ref)) : 0.f;
-                        psum += p2[e];
-                    }
-                    const uint32_t h = pack2_bf16(p2[0], p2[1]);
+                for (int i = 0; i < 8; i += 2) {
+                    const float p0 = ex2_approx(fmaf(__uint_as_float(v[c + i]), sl2, -m_ref));
+                    const float p1 = ex2_approx(fmaf(__uint_as_float(v[c + i + 1]), sl2, -m_ref));
+                    ps4[(i >> 1) & 3] += p0 + p1;
+                    const uint32_t h = pack2_bf16(p0, p1);
                     hi[i >> 1] = h;
-                    lo[i >> 1] = pack2_bf16(p2[0] - __uint_as_float(h << 16),
-                                            p2[1] - __uint_as_float(h & 0xffff0000u));
+                    lo[i >> 1] = pack2_bf16(p0 - __uint_as_float(h << 16),
+                                            p1 - __uint_as_float(h & 0xffff0000u));
                 }
-                // 32 columns = four 16-byte chunks of this row, in region c / 64
-                const int region = c >> 6;
-#pragma unroll
-                for (int q4 = 0; q4 < 4; ++q4) {
-                    const int chunk = ((c & 63) >> 3) + q4;
-                    const uint32_t off = region * kHalf + ((chunk ^ (r & 7)) << 4);
-                    *reinterpret_cast<uint4 *>(prow_hi + off) =
-                        make_uint4(hi[4 * q4], hi[4 * q4 + 1], hi[4 * q4 + 2], hi[4 * q4 + 3]);
-                    *reinterpret_cast<uint4 *>(prow_hi + kTile + off) =
-                        make_uint4(lo[4 * q4], lo[4 * q4 + 1], lo[4 * q4 + 2], lo[4 * q4 + 3]);
-                }
+                const uint32_t off = ((uint32_t)((c >> 3) ^ (r & 7))) << 4;
+                *reinterpret_cast<uint4 *>(prow + off) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
+                *reinterpret_cast<uint4 *>(prow + kTile + off) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
             }
-            l += psum;
-            tc_fence_before();
-            mbar_arrive(&bars[kSFree + s]);
+            l += (ps4[0] + ps4[1]) + (ps4[2] + ps4[3]);
             // V rows of positions outside [kv_lo, kv_hi) may hold anything
             // (NaN included): zero them so that 0 * row stays 0.
-            if (k0 < kv_lo || k0 + kKv > kv_hi) {
-                if (!wait_or_fail(&bars[kVFull + s], (j >> 1) & 1, fail, a.status)) {
+            const int k0_tile = (blk_lo + 8 * j) * kBlockSize;
+            if (k0_tile < kv_lo || k0_tile + kKv > kv_hi) {
+                if (!warp_wait(&bars[kVFull + s], (j >> 1) & 1, fail, a.status)) {
                     ok = false;
-                    break;
+                    continue;
                 }
-                const int kp = k0 + r;
+                const int kp = k0_tile + r;
                 if (kp < kv_lo || kp >= kv_hi) {
-                    uint8_t *vrow = sV + s * kTile + (r >> 3) * 1024 + (r & 7) * 128;
+                    uint8_t *vrow = sV + s * kTile + half * kHalf + (r >> 3) * 1024 + (r & 7) * 128;
 #pragma unroll
-                    for (int q = 0; q < 8; ++q) {
+                    for (int q = 0; q < 8; ++q)
                         *reinterpret_cast<uint4 *>(vrow + q * 16) = make_uint4(0, 0, 0, 0);
-                        *reinterpret_cast<uint4 *>(vrow + kHalf + q * 16) = make_uint4(0, 0, 0, 0);
-                    }
                 }
             }
             fence_proxy_async_smem();
             tc_fence_before();
             mbar_arrive(&bars[kPFull]);
         }
-        if (ok && wait_or_fail(&bars[kDrain], 0, fail, a.status)) {
+        // the row sum is the two halves' sums (both kept against the same
+        // maximum); exchanged in the slots of the parity the last tile did not
+        // use, whose reads all finished before the last tile's barrier
+        const int sx = n_tiles & 1;
+        red[(sx * 2 + half) * kRows + r] = l;
+        asm volatile("bar.sync 1, %0;" ::"n"(kSoftmaxThreads) : "memory");
+        const float l_row = l + red[(sx * 2 + (half ^ 1)) * kRows + r];
+        if (__all_sync(0xffffffffu, ok) && warp_wait(&bars[kDrain], 0, fail, a.status)) {
             tc_fence_after();
-            const float inv = l > 0.f ? 1.f / l : 0.f;
+            const float inv = l_row > 0.f ? 1.f / l_row : 0.f;
             __nv_bfloat16 *orow = static_cast<__nv_bfloat16 *>(a.out) +
-                                  ((size_t)(q0 + t0 + tr) * a.num_q_heads + kvh * g + (r % g)) * kD;
+                                  ((size_t)(q0 + t0 + tr) * a.num_q_heads + kvh * g + (r % g)) * kD +
+                                  half * 64;
 #pragma unroll 1
-            for (int c = 0; c < kD; c += 32) {
+            for (int c = 0; c < 64; c += 32) {
                 uint32_t o[32];
                 tmem_ld32(lane_base + kColO + c, o);
                 tmem_wait_ld();
