@@ -14,17 +14,22 @@
 // one sequence and one KV head, flash-attention style over 128-position K/V
 // tiles gathered block by block through the block table:
 //   warp 0      TMA producer: Q tile once, then K and V tiles (eight 16-row
-//               blocks each) into two-stage rings;
+//               blocks each) into kStages-deep rings;
 //   warp 1      MMA issuer: S = Q K^T into tensor memory (two S buffers), then
-//               O += P V into a tensor-memory accumulator; owns the TMEM
+//               O += P V into a tensor-memory accumulator with P read from
+//               tensor memory (written over its own S); owns the TMEM
 //               allocation;
-//   warps 2..9  softmax: two threads per row (= TMEM lane), each owning 64 of
-//               the 128 columns of S and of O.  They agree on the row maximum
+//   warps 2..   softmax: kSplit threads per row (= TMEM lane), each owning
+//               128 / kSplit of the columns of S and of O.  They agree on the row maximum
 //               through shared memory once per tile, keep their part of the
-//               running sum, write P (bf16 head and bf16 residual) to shared
-//               memory, rescale their half of O in tensor memory only when the
-//               maximum grew by more than 2^8, and write their half of the
-//               output row.
+//               running sum, write P (bf16 head and bf16 residual) over the
+//               S columns they read, rescale their half of O in tensor memory
+//               only when the maximum grew by more than 2^8, and write their
+//               half of the output row.
+// The MMAs of one thread execute in issue order, so S_{j+2} (issued after
+// PV_j) cannot overwrite the P that PV_j reads, and the commit that signals
+// S_{j+1} also covers PV_{j-1}: the softmax of tile j+1 may write its P while
+// PV_j still runs.
 // Every wait is bounded (about a second); a wait that gives up sets
 // PA_DEV_TIMEOUT and the CTA drains its tensor-core work and returns.
 #include <cuda.h>
@@ -47,30 +52,43 @@ constexpr int kKv = 128;                 // N: K/V positions per step (8 blocks)
 constexpr int kD = 128;                  // head_dim
 constexpr int kHalf = 16384;             // one 64-column swizzled region of a tile
 constexpr int kTile = 2 * kHalf;         // 128 rows x 256 bytes
-constexpr int kThreads = 320;            // 2 + 8 warps
-constexpr int kSoftmaxThreads = 256;
+#ifndef PA_PREFILL_SPLIT
+#define PA_PREFILL_SPLIT 2
+#endif
+#ifndef PA_PREFILL_STAGES
+#define PA_PREFILL_STAGES 3
+#endif
+constexpr int kSplit = PA_PREFILL_SPLIT;     // softmax threads per row
+constexpr int kStages = PA_PREFILL_STAGES;   // depth of the K and V rings
+constexpr int kCols = kKv / kSplit;      // S / O columns per softmax thread
+constexpr int kSoftmaxThreads = kRows * kSplit;
+constexpr int kThreads = 64 + kSoftmaxThreads;   // producer warp, MMA warp, softmax warps
 constexpr float kRescaleLog2 = 8.0f;     // lazy rescale threshold (factor 256)
 
 // shared memory map (offsets from a 1024-byte aligned base)
 constexpr int kOffQ = 0;
-constexpr int kOffK = kOffQ + kTile;            // two stages
-constexpr int kOffV = kOffK + 2 * kTile;        // two stages
-constexpr int kOffP = kOffV + 2 * kTile;        // P head, then P residual
-constexpr int kOffBar = kOffP + 2 * kTile;
-constexpr int kNumBars = 16;
-constexpr int kOffRed = kOffBar + 256;          // row-maximum exchange [2 tiles][2 halves][128]
-constexpr int kSmemBytes = kOffRed + 2 * 2 * kRows * 4;
+constexpr int kOffK = kOffQ + kTile;
+constexpr int kOffV = kOffK + kStages * kTile;
+constexpr int kOffBar = kOffV + kStages * kTile;
+constexpr int kNumBars = 4 * kStages + 9;
+constexpr int kOffRed = kOffBar + 256;          // row-maximum exchange [2 tiles][kSplit][128]
+constexpr int kSmemBytes = kOffRed + 2 * kSplit * kRows * 4;
 // The tiles need 1024-byte alignment; the dynamic shared memory of a kernel
 // without static shared memory starts on such a boundary, and the kernel
 // checks it (PA_DEV_SMEM_ALIGN) instead of reserving slack it has no room for.
 
 // barrier indices
-constexpr int kQFull = 0, kKFull = 1, kKEmpty = 3, kVFull = 5, kVEmpty = 7, kSFull = 9,
-              kSFree = 11, kPFull = 13, kPvDone = 14, kDrain = 15;
+constexpr int kQFull = 0, kKFull = 1, kKEmpty = kKFull + kStages, kVFull = kKEmpty + kStages,
+              kVEmpty = kVFull + kStages, kSFull = kVEmpty + kStages, kPFull = kSFull + 3,
+              kPvDone = kPFull + 3, kDrain = kPvDone + 1;
+static_assert(kNumBars * 8 + 8 <= 256, "barrier block");
+static_assert(kSmemBytes <= 227 * 1024, "shared memory");
 
-// TMEM columns: S buffers at 0 and 128, O at 256.
+// TMEM columns: three S / P buffers at 0, 128 and 256, O at 384.  With three
+// buffers the MMA issuer runs two S products ahead of the softmax.
+constexpr int kSBufs = 3;
 constexpr uint32_t kTmemCols = 512;
-constexpr uint32_t kColO = 256;
+constexpr uint32_t kColO = kSBufs * kKv;
 
 struct PrefillArgs {
     void *out;
@@ -156,7 +174,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint8_t *sQ = base + kOffQ;
     uint8_t *sK = base + kOffK;
     uint8_t *sV = base + kOffV;
-    uint8_t *sP = base + kOffP;
     uint64_t *bars = reinterpret_cast<uint64_t *>(base + kOffBar);
     uint32_t *tslot = reinterpret_cast<uint32_t *>(base + kOffBar + kNumBars * 8);
     volatile int *fail = reinterpret_cast<volatile int *>(base + kOffBar + kNumBars * 8 + 4);
@@ -165,15 +182,16 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int lane = threadIdx.x & 31;
     if (threadIdx.x == 0) {
         mbar_init(&bars[kQFull], 1);
-        for (int s = 0; s < 2; ++s) {
+        for (int s = 0; s < kStages; ++s) {
             mbar_init(&bars[kKFull + s], 1);
             mbar_init(&bars[kKEmpty + s], 1);
             mbar_init(&bars[kVFull + s], 1);
             mbar_init(&bars[kVEmpty + s], 1);
-            mbar_init(&bars[kSFull + s], 1);
-            mbar_init(&bars[kSFree + s], kSoftmaxThreads);
         }
-        mbar_init(&bars[kPFull], kSoftmaxThreads);
+        for (int s = 0; s < kSBufs; ++s) {
+            mbar_init(&bars[kSFull + s], 1);
+            mbar_init(&bars[kPFull + s], kSoftmaxThreads);
+        }
         mbar_init(&bars[kPvDone], 1);
         mbar_init(&bars[kDrain], 1);
         *fail = 0;
@@ -197,7 +215,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             const int32_t *trow = a.block_tables + (size_t)b * a.max_blocks;
             int issued_k = 0, issued_v = 0;
             for (int j = 0; j < n_tiles; ++j) {
-                const int s = j & 1;
+                const int s = j % kStages;
+                const uint32_t ph = (uint32_t)(j / kStages) & 1u;   // this use of stage s
                 const int blk0 = blk_lo + 8 * j;
                 const int nb = min(8, blk_hi - blk0);
                 int rows[8];
@@ -209,7 +228,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     }
                     rows[i] = (phys * a.num_kv_heads + kvh) * kBlockSize;
                 }
-                if (j >= 2 && !wait_or_fail(&bars[kKEmpty + s], ((j >> 1) - 1) & 1, fail, a.status))
+                if (j >= kStages && !wait_or_fail(&bars[kKEmpty + s], ph ^ 1u, fail, a.status))
                     break;
                 uint8_t *kd = sK + s * kTile;
                 mbar_arrive_expect_tx(&bars[kKFull + s], nb * 4096);
@@ -218,7 +237,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     tma_load_2d(kd + kHalf + i * 2048, &kmap, 64, rows[i], &bars[kKFull + s]);
                 }
                 issued_k = j + 1;
-                if (j >= 2 && !wait_or_fail(&bars[kVEmpty + s], ((j >> 1) - 1) & 1, fail, a.status))
+                if (j >= kStages && !wait_or_fail(&bars[kVEmpty + s], ph ^ 1u, fail, a.status))
                     break;
                 uint8_t *vd = sV + s * kTile;
                 mbar_arrive_expect_tx(&bars[kVFull + s], nb * 4096);
@@ -230,44 +249,47 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             // drain: no copy of ours may still be landing when the CTA leaves
             (void)mbar_wait_bounded(&bars[kQFull], 0);
-            for (int j = max(0, issued_k - 2); j < issued_k; ++j)
-                (void)mbar_wait_bounded(&bars[kKFull + (j & 1)], (j >> 1) & 1);
-            for (int j = max(0, issued_v - 2); j < issued_v; ++j)
-                (void)mbar_wait_bounded(&bars[kVFull + (j & 1)], (j >> 1) & 1);
+            for (int j = max(0, issued_k - kStages); j < issued_k; ++j)
+                (void)mbar_wait_bounded(&bars[kKFull + j % kStages], (j / kStages) & 1);
+            for (int j = max(0, issued_v - kStages); j < issued_v; ++j)
+                (void)mbar_wait_bounded(&bars[kVFull + j % kStages], (j / kStages) & 1);
         }
     } else if (warp == 1) {
         // ---------------- MMA issuer ----------------
         if (lane == 0) {
             constexpr uint32_t idS = idesc_bf16_f32(kRows, kKv, false);
             constexpr uint32_t idPV = idesc_bf16_f32(kRows, kD, true);
-            const uint32_t q_u = smem_u32(sQ), k_u = smem_u32(sK), v_u = smem_u32(sV),
-                           p_u = smem_u32(sP);
+            const uint32_t q_u = smem_u32(sQ), k_u = smem_u32(sK), v_u = smem_u32(sV);
             bool ok = wait_or_fail(&bars[kQFull], 0, fail, a.status);
             auto issue_pv = [&](int i) -> bool {
-                const int s = i & 1;
-                if (!wait_or_fail(&bars[kPFull], i & 1, fail, a.status)) return false;
-                if (!wait_or_fail(&bars[kVFull + s], (i >> 1) & 1, fail, a.status)) return false;
+                const int s = i % kSBufs;            // S / P buffer
+                const int sv = i % kStages;          // V stage
+                if (!wait_or_fail(&bars[kPFull + s], (i / kSBufs) & 1, fail, a.status)) return false;
+                if (!wait_or_fail(&bars[kVFull + sv], (i / kStages) & 1, fail, a.status)) return false;
                 tc_fence_after();
-                const uint32_t vb = v_u + s * kTile;
+                const uint32_t vb = v_u + sv * kTile;
+                // P of tokens [16k, 16k + 16) (owned by the softmax thread of
+                // part 16k / kCols): head pairs from column kCols * part +
+                // (16k mod kCols) / 2 of the S buffer, residual kCols / 2 further
 #pragma unroll
                 for (int k = 0; k < 8; ++k) {
-                    const uint32_t po = (k >> 2) * kHalf + (k & 3) * 32;
+                    const uint32_t pc = tmem + s * kKv + (16 * k / kCols) * kCols + (16 * k % kCols) / 2;
                     const uint64_t vdesc = sw128_desc(vb + k * 2048, kHalf, 1024);
-                    umma_bf16(tmem + kColO, sw128_desc(p_u + po, 16, 1024), vdesc, idPV,
-                              (i > 0 || k > 0) ? 1u : 0u);
-                    umma_bf16(tmem + kColO, sw128_desc(p_u + kTile + po, 16, 1024), vdesc, idPV, 1u);
+                    umma_bf16_tmem_a(tmem + kColO, pc, vdesc, idPV, (i > 0 || k > 0) ? 1u : 0u);
+                    umma_bf16_tmem_a(tmem + kColO, pc + kCols / 2, vdesc, idPV, 1u);
                 }
                 umma_commit(&bars[kPvDone]);
-                umma_commit(&bars[kVEmpty + s]);
+                umma_commit(&bars[kVEmpty + sv]);
                 return true;
             };
+            // order: S_0, S_1, S_2, PV_0, S_3, PV_1, ...: S_j overwrites the P
+            // of tile j - 3, whose PV was issued one iteration earlier
             for (int j = 0; ok && j < n_tiles; ++j) {
-                const int s = j & 1;
-                if (!wait_or_fail(&bars[kKFull + s], (j >> 1) & 1, fail, a.status)) break;
-                if (j >= 2 && !wait_or_fail(&bars[kSFree + s], ((j >> 1) - 1) & 1, fail, a.status))
-                    break;
+                const int s = j % kSBufs;
+                const int sk = j % kStages;
+                if (!wait_or_fail(&bars[kKFull + sk], (j / kStages) & 1, fail, a.status)) break;
                 tc_fence_after();
-                const uint32_t kb = k_u + s * kTile;
+                const uint32_t kb = k_u + sk * kTile;
 #pragma unroll
                 for (int k = 0; k < 8; ++k) {
                     const uint32_t o = (k >> 2) * kHalf + (k & 3) * 32;
@@ -275,13 +297,14 @@ __global__ void __launch_bounds__(kThreads, 1)
                               sw128_desc(kb + o, 16, 1024), idS, k > 0 ? 1u : 0u);
                 }
                 umma_commit(&bars[kSFull + s]);
-                umma_commit(&bars[kKEmpty + s]);
-                if (j >= 1 && !issue_pv(j - 1)) {
+                umma_commit(&bars[kKEmpty + sk]);
+                if (j >= 2 && !issue_pv(j - 2)) {
                     ok = false;
                     break;
                 }
-                if (j == n_tiles - 1 && !issue_pv(j)) ok = false;
             }
+            for (int i = max(0, n_tiles - 2); ok && i < n_tiles; ++i)
+                if (!issue_pv(i)) ok = false;
             // every MMA issued above has completed once kDrain flips
             umma_commit(&bars[kDrain]);
             if (!mbar_wait_bounded(&bars[kDrain], 0)) {
@@ -292,15 +315,14 @@ __global__ void __launch_bounds__(kThreads, 1)
     } else {
         // ---------------- softmax warps ----------------
         const int quarter = warp & 3;
-        const int half = (warp - 2) >> 2;             // columns [64 * half, 64 * half + 64)
+        const int part = (warp - 2) >> 2;             // columns [kCols * part, kCols * part + kCols)
         const int r = quarter * 32 + lane;            // tile row = TMEM lane
         const int tr = r / g;
         const bool real = tr < ntok;
         const int qpos = C + t0 + min(tr, ntok - 1);
         const int wlo = a.window > 0 ? qpos + 1 - a.window : INT_MIN;   // first allowed position
-        const uint32_t lane_base = tmem + ((uint32_t)(quarter * 32) << 16) + half * 64;
+        const uint32_t lane_base = tmem + ((uint32_t)(quarter * 32) << 16) + part * kCols;
         float *red = reinterpret_cast<float *>(base + kOffRed);
-        uint8_t *prow = sP + half * kHalf + (r >> 3) * 1024 + (r & 7) * 128;
         const float sl2 = a.scale_log2;
         float m_used = -INFINITY, l = 0.f;
         // Every softmax thread runs every iteration and reaches the named
@@ -308,61 +330,60 @@ __global__ void __launch_bounds__(kThreads, 1)
         // only skips the work), so that no barrier can wait forever.
         bool ok = true;
         for (int j = 0; j < n_tiles; ++j) {
-            const int s = j & 1;
-            const bool got = ok && warp_wait(&bars[kSFull + s], (j >> 1) & 1, fail, a.status);
-            const int k0 = (blk_lo + 8 * j) * kBlockSize + half * 64;   // position of column 0
-            const bool masked = (k0 + 63 > qpos_lo) || (a.window > 0 && k0 < qpos_hi + 1 - a.window);
-            uint32_t v[64];
+            const int s = j % kSBufs;
+            const bool got = ok && warp_wait(&bars[kSFull + s], (j / kSBufs) & 1, fail, a.status);
+            const int k0 = (blk_lo + 8 * j) * kBlockSize + part * kCols;   // position of column 0
+            const bool masked = (k0 + kCols - 1 > qpos_lo) ||
+                                (a.window > 0 && k0 < qpos_hi + 1 - a.window);
+            uint32_t v[kCols];
             if (!got) {
 #pragma unroll
-                for (int i = 0; i < 64; ++i) v[i] = __float_as_uint(-INFINITY);
+                for (int i = 0; i < kCols; ++i) v[i] = __float_as_uint(-INFINITY);
             } else {
                 tc_fence_after();
-                uint32_t (&v0)[32] = *reinterpret_cast<uint32_t (*)[32]>(&v[0]);
-                uint32_t (&v1)[32] = *reinterpret_cast<uint32_t (*)[32]>(&v[32]);
-                tmem_ld32(lane_base + s * kKv, v0);
-                tmem_ld32(lane_base + s * kKv + 32, v1);
+#pragma unroll
+                for (int c = 0; c < kCols; c += 32)
+                    tmem_ld32(lane_base + s * kKv + c, *reinterpret_cast<uint32_t (*)[32]>(&v[c]));
                 tmem_wait_ld();
-                // S is in registers: the buffer can take the next product
-                tc_fence_before();
-                mbar_arrive(&bars[kSFree + s]);
             }
             if (masked) {
 #pragma unroll
-                for (int i = 0; i < 64; ++i) {
+                for (int i = 0; i < kCols; ++i) {
                     const int kp = k0 + i;
                     if (!(kp <= qpos && kp >= wlo)) v[i] = __float_as_uint(-INFINITY);
                 }
             }
-            // row maximum: four independent chains, then the partner's half
+            // row maximum: four independent chains, then the other parts'
             float mx4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
 #pragma unroll
-            for (int i = 0; i < 64; ++i) mx4[i & 3] = fmaxf(mx4[i & 3], __uint_as_float(v[i]));
-            const float mine = fmaxf(fmaxf(mx4[0], mx4[1]), fmaxf(mx4[2], mx4[3]));
-            red[(s * 2 + half) * kRows + r] = mine;
+            for (int i = 0; i < kCols; ++i) mx4[i & 3] = fmaxf(mx4[i & 3], __uint_as_float(v[i]));
+            float mrow = fmaxf(fmaxf(mx4[0], mx4[1]), fmaxf(mx4[2], mx4[3]));
+            const int rp = j & 1;                     // exchange slots of this tile
+            red[(rp * kSplit + part) * kRows + r] = mrow;
             asm volatile("bar.sync 1, %0;" ::"n"(kSoftmaxThreads) : "memory");
-            const float other = red[(s * 2 + (half ^ 1)) * kRows + r];
+#pragma unroll
+            for (int o = 1; o < kSplit; ++o)
+                mrow = fmaxf(mrow, red[(rp * kSplit + ((part + o) % kSplit)) * kRows + r]);
             if (!got) {
                 ok = false;
                 continue;
             }
-            const float m_tile = fmaxf(mine, other) * sl2;
+            const float m_tile = mrow * sl2;
             const float m_new = fmaxf(m_used, m_tile);
-            // P of the previous tile must have been consumed (and O updated)
-            // before P is overwritten or O rescaled.
-            if (j >= 1 && !warp_wait(&bars[kPvDone], (j - 1) & 1, fail, a.status)) {
-                ok = false;
-                continue;
-            }
             // Lazy rescale: only rows whose maximum grew by more than 2^8 move
             // their reference; the warp rescales O together (tensor-memory
-            // access is warp-wide), with factor 1 on the other rows.
+            // access is warp-wide), with factor 1 on the other rows, once every
+            // PV issued so far has landed in O.
             const bool need = m_new > m_used + kRescaleLog2;
             const float alpha = need ? exp2f(m_used - m_new) : 1.f;   // 0 while m_used is -inf
             if (j >= 1 && __any_sync(0xffffffffu, need)) {
+                if (!warp_wait(&bars[kPvDone], (j - 1) & 1, fail, a.status)) {
+                    ok = false;
+                    continue;
+                }
                 tc_fence_after();
 #pragma unroll 1
-                for (int c = 0; c < 64; c += 32) {
+                for (int c = 0; c < kCols; c += 32) {
                     uint32_t o[32];
                     tmem_ld32(lane_base + kColO + c, o);
                     tmem_wait_ld();
@@ -377,61 +398,71 @@ __global__ void __launch_bounds__(kThreads, 1)
                 m_used = m_new;
             }
             const float m_ref = m_used == -INFINITY ? 0.f : m_used;
-            // P = 2^(s * scale_log2 - m_ref) as a bf16 head + bf16 residual
+            // P = 2^(s * scale_log2 - m_ref) as a bf16 head + bf16 residual,
+            // written over this thread's own S columns: head pairs in the
+            // first half, residual pairs in the second
             float ps4[4] = {0.f, 0.f, 0.f, 0.f};
+            uint32_t hi[kCols / 2], lo[kCols / 2];
 #pragma unroll
-            for (int c = 0; c < 64; c += 8) {
-                uint32_t hi[4], lo[4];
-#pragma unroll
-                for (int i = 0; i < 8; i += 2) {
-                    const float p0 = ex2_approx(fmaf(__uint_as_float(v[c + i]), sl2, -m_ref));
-                    const float p1 = ex2_approx(fmaf(__uint_as_float(v[c + i + 1]), sl2, -m_ref));
-                    ps4[(i >> 1) & 3] += p0 + p1;
-                    const uint32_t h = pack2_bf16(p0, p1);
-                    hi[i >> 1] = h;
-                    lo[i >> 1] = pack2_bf16(p0 - __uint_as_float(h << 16),
-                                            p1 - __uint_as_float(h & 0xffff0000u));
-                }
-                const uint32_t off = ((uint32_t)((c >> 3) ^ (r & 7))) << 4;
-                *reinterpret_cast<uint4 *>(prow + off) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
-                *reinterpret_cast<uint4 *>(prow + kTile + off) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
+            for (int i = 0; i < kCols; i += 2) {
+                const float p0 = ex2_approx(fmaf(__uint_as_float(v[i]), sl2, -m_ref));
+                const float p1 = ex2_approx(fmaf(__uint_as_float(v[i + 1]), sl2, -m_ref));
+                ps4[(i >> 1) & 3] += p0 + p1;
+                const uint32_t h = pack2_bf16(p0, p1);
+                hi[i >> 1] = h;
+                lo[i >> 1] = pack2_bf16(p0 - __uint_as_float(h << 16),
+                                        p1 - __uint_as_float(h & 0xffff0000u));
             }
+#pragma unroll
+            for (int c = 0; c < kCols / 2; c += 16) {
+                tmem_st16(lane_base + s * kKv + c, *reinterpret_cast<const uint32_t (*)[16]>(&hi[c]));
+                tmem_st16(lane_base + s * kKv + kCols / 2 + c,
+                          *reinterpret_cast<const uint32_t (*)[16]>(&lo[c]));
+            }
+            tmem_wait_st();
             l += (ps4[0] + ps4[1]) + (ps4[2] + ps4[3]);
             // V rows of positions outside [kv_lo, kv_hi) may hold anything
-            // (NaN included): zero them so that 0 * row stays 0.
+            // (NaN included): zero them so that 0 * row stays 0 (the kSplit
+            // threads of a row clear a share of it each).
             const int k0_tile = (blk_lo + 8 * j) * kBlockSize;
             if (k0_tile < kv_lo || k0_tile + kKv > kv_hi) {
-                if (!warp_wait(&bars[kVFull + s], (j >> 1) & 1, fail, a.status)) {
+                if (!warp_wait(&bars[kVFull + j % kStages], (j / kStages) & 1, fail, a.status)) {
                     ok = false;
                     continue;
                 }
                 const int kp = k0_tile + r;
                 if (kp < kv_lo || kp >= kv_hi) {
-                    uint8_t *vrow = sV + s * kTile + half * kHalf + (r >> 3) * 1024 + (r & 7) * 128;
+                    // this thread's share of the row's 256 bytes (two 128-byte regions)
+                    constexpr int kBytes = 256 / kSplit;
+                    const int b0 = part * kBytes;
+                    uint8_t *vrow = sV + (j % kStages) * kTile + (b0 >> 7) * kHalf + (r >> 3) * 1024 +
+                                    (r & 7) * 128 + (b0 & 127);
 #pragma unroll
-                    for (int q = 0; q < 8; ++q)
+                    for (int q = 0; q < kBytes / 16; ++q)
                         *reinterpret_cast<uint4 *>(vrow + q * 16) = make_uint4(0, 0, 0, 0);
                 }
             }
             fence_proxy_async_smem();
             tc_fence_before();
-            mbar_arrive(&bars[kPFull]);
+            mbar_arrive(&bars[kPFull + s]);
         }
-        // the row sum is the two halves' sums (both kept against the same
-        // maximum); exchanged in the slots of the parity the last tile did not
-        // use, whose reads all finished before the last tile's barrier
+        // the row sum is the parts' sums (all kept against the same maximum);
+        // exchanged in the slots of the parity the last tile did not use,
+        // whose reads all finished before the last tile's barrier
         const int sx = n_tiles & 1;
-        red[(sx * 2 + half) * kRows + r] = l;
+        red[(sx * kSplit + part) * kRows + r] = l;
         asm volatile("bar.sync 1, %0;" ::"n"(kSoftmaxThreads) : "memory");
-        const float l_row = l + red[(sx * 2 + (half ^ 1)) * kRows + r];
+        float l_row = l;
+#pragma unroll
+        for (int o = 1; o < kSplit; ++o) l_row += red[(sx * kSplit + ((part + o) % kSplit)) * kRows + r];
         if (__all_sync(0xffffffffu, ok) && warp_wait(&bars[kDrain], 0, fail, a.status)) {
             tc_fence_after();
             const float inv = l_row > 0.f ? 1.f / l_row : 0.f;
             __nv_bfloat16 *orow = static_cast<__nv_bfloat16 *>(a.out) +
                                   ((size_t)(q0 + t0 + tr) * a.num_q_heads + kvh * g + (r % g)) * kD +
-                                  half * 64;
+                                  part * kCols;
 #pragma unroll 1
-            for (int c = 0; c < 64; c += 32) {
+            for (int c = 0; c < kCols; c += 32) {
                 uint32_t o[32];
                 tmem_ld32(lane_base + kColO + c, o);
                 tmem_wait_ld();
