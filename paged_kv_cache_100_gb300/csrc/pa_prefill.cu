@@ -10,26 +10,27 @@
 // "El mecanismo en sí (en cristiano)"), or to its last W positions with a
 // sliding window ("PagedAttention por dentro", "Sliding window attention").
 //
-// One CTA computes a 128-row tile of (token, query head of the group) rows of
-// one sequence and one KV head, flash-attention style over 128-position K/V
-// tiles gathered block by block through the block table:
-//   warp 0      TMA producer: Q tile once, then K and V tiles (eight 16-row
-//               blocks each) into kStages-deep rings;
-//   warp 1      MMA issuer: S = Q K^T into tensor memory (two S buffers), then
-//               O += P V into a tensor-memory accumulator with P read from
-//               tensor memory (written over its own S); owns the TMEM
-//               allocation;
-//   warps 2..   softmax: kSplit threads per row (= TMEM lane), each owning
-//               128 / kSplit of the columns of S and of O.  They agree on the row maximum
-//               through shared memory once per tile, keep their part of the
-//               running sum, write P (bf16 head and bf16 residual) over the
-//               S columns they read, rescale their half of O in tensor memory
-//               only when the maximum grew by more than 2^8, and write their
-//               half of the output row.
-// The MMAs of one thread execute in issue order, so S_{j+2} (issued after
-// PV_j) cannot overwrite the P that PV_j reads, and the commit that signals
-// S_{j+1} also covers PV_{j-1}: the softmax of tile j+1 may write its P while
-// PV_j still runs.
+// One CTA computes two 128-row tiles (A, then B) of (token, query head of the
+// group) rows of one sequence and one KV head, flash-attention style over
+// 128-position K/V tiles gathered block by block through the block table.
+// Each K/V tile loaded serves 256 rows.
+//   warp 0       TMA producer: both Q tiles once, then K and V tiles (eight
+//                16-row blocks each) into kStages-deep rings;
+//   warp 1       MMA issuer, ping-pong between the tiles:
+//                  S_A(0) S_B(0) | PV_A(j) S_A(j+1) PV_B(j) S_B(j+1) | ...
+//                S = Q K^T lands in tensor memory; O += P V reads P from tensor
+//                memory (written over its own S) and accumulates in tensor
+//                memory; owns the TMEM allocation (S_A, S_B, O_A, O_B);
+//   warps 2..9   softmax of tile A, warps 10..17 softmax of tile B: two threads
+//                per row (= TMEM lane), each owning 64 of the 128 columns of S
+//                and of O.  They agree on the row maximum through shared memory
+//                once per K/V tile, keep their part of the running sum, write P
+//                (bf16 head and bf16 residual) over the S columns they read,
+//                rescale their part of O only when the maximum grew by more than
+//                2^8, and write their part of the output row.
+// While one tile's softmax runs, the tensor cores work on the other tile.  The
+// MMAs of one thread execute in issue order: S_X(j+1), issued after PV_X(j),
+// cannot overwrite the P that PV_X(j) reads.
 // Every wait is bounded (about a second); a wait that gives up sets
 // PA_DEV_TIMEOUT and the CTA drains its tensor-core work and returns.
 #include <cuda.h>
@@ -47,48 +48,46 @@
 namespace pa {
 namespace {
 
-constexpr int kRows = 128;               // M: query rows per CTA
+constexpr int kRows = 128;               // rows per Q tile (M of every MMA)
+constexpr int kQT = 2;                   // Q tiles per CTA
 constexpr int kKv = 128;                 // N: K/V positions per step (8 blocks)
 constexpr int kD = 128;                  // head_dim
 constexpr int kHalf = 16384;             // one 64-column swizzled region of a tile
 constexpr int kTile = 2 * kHalf;         // 128 rows x 256 bytes
-#ifndef PA_PREFILL_SPLIT
-#define PA_PREFILL_SPLIT 2
-#endif
-#ifndef PA_PREFILL_STAGES
-#define PA_PREFILL_STAGES 3
-#endif
-constexpr int kSplit = PA_PREFILL_SPLIT;     // softmax threads per row
-constexpr int kStages = PA_PREFILL_STAGES;   // depth of the K and V rings
+constexpr int kSplit = 2;                // softmax threads per row
 constexpr int kCols = kKv / kSplit;      // S / O columns per softmax thread
-constexpr int kSoftmaxThreads = kRows * kSplit;
-constexpr int kThreads = 64 + kSoftmaxThreads;   // producer warp, MMA warp, softmax warps
+constexpr int kGroup = kRows * kSplit;   // softmax threads per Q tile
+constexpr int kThreads = 64 + kQT * kGroup;
+#ifndef PA_PREFILL_STAGES
+#define PA_PREFILL_STAGES 2
+#endif
+constexpr int kStages = PA_PREFILL_STAGES;   // depth of the K and V rings
 constexpr float kRescaleLog2 = 8.0f;     // lazy rescale threshold (factor 256)
 
-// shared memory map (offsets from a 1024-byte aligned base)
-constexpr int kOffQ = 0;
-constexpr int kOffK = kOffQ + kTile;
-constexpr int kOffV = kOffK + kStages * kTile;
+// shared memory map (offsets from the 1024-byte aligned dynamic base)
+constexpr int kOffQ = 0;                          // kQT tiles
+constexpr int kOffK = kOffQ + kQT * kTile;        // kStages tiles
+constexpr int kOffV = kOffK + kStages * kTile;    // kStages tiles
 constexpr int kOffBar = kOffV + kStages * kTile;
-constexpr int kNumBars = 4 * kStages + 9;
-constexpr int kOffRed = kOffBar + 256;          // row-maximum exchange [2 tiles][kSplit][128]
-constexpr int kSmemBytes = kOffRed + 2 * kSplit * kRows * 4;
+constexpr int kNumBars = 4 * kStages + 8;
+constexpr int kOffRed = kOffBar + 256;            // [kQT][2 parities][kSplit][128] floats
+constexpr int kSmemBytes = kOffRed + kQT * 2 * kSplit * kRows * 4;
 // The tiles need 1024-byte alignment; the dynamic shared memory of a kernel
 // without static shared memory starts on such a boundary, and the kernel
-// checks it (PA_DEV_SMEM_ALIGN) instead of reserving slack it has no room for.
+// checks it (PA_DEV_SMEM_ALIGN) instead of reserving slack.
 
 // barrier indices
 constexpr int kQFull = 0, kKFull = 1, kKEmpty = kKFull + kStages, kVFull = kKEmpty + kStages,
-              kVEmpty = kVFull + kStages, kSFull = kVEmpty + kStages, kPFull = kSFull + 3,
-              kPvDone = kPFull + 3, kDrain = kPvDone + 1;
+              kVEmpty = kVFull + kStages, kSFull = kVEmpty + kStages, kPFull = kSFull + kQT,
+              kPvDone = kPFull + kQT, kDrain = kPvDone + kQT;
+static_assert(kDrain + 1 == kNumBars, "barrier count");
 static_assert(kNumBars * 8 + 8 <= 256, "barrier block");
 static_assert(kSmemBytes <= 227 * 1024, "shared memory");
 
-// TMEM columns: three S / P buffers at 0, 128 and 256, O at 384.  With three
-// buffers the MMA issuer runs two S products ahead of the softmax.
-constexpr int kSBufs = 3;
+// TMEM columns: S_A, S_B, then O_A, O_B.
 constexpr uint32_t kTmemCols = 512;
-constexpr uint32_t kColO = kSBufs * kKv;
+__device__ __forceinline__ uint32_t col_s(int x) { return (uint32_t)(x * kKv); }
+__device__ __forceinline__ uint32_t col_o(int x) { return (uint32_t)(kQT * kKv + x * kD); }
 
 struct PrefillArgs {
     void *out;
@@ -134,6 +133,10 @@ __device__ __forceinline__ uint32_t pack2_bf16(float lo, float hi) {
     return *reinterpret_cast<uint32_t *>(&v);
 }
 
+__device__ __forceinline__ void named_sync(int id) {
+    asm volatile("bar.sync %0, %1;" ::"r"(id), "n"(kGroup) : "memory");
+}
+
 __global__ void __launch_bounds__(kThreads, 1)
     pa_prefill_kernel(const __grid_constant__ CUtensorMap qmap,
                       const __grid_constant__ CUtensorMap kmap,
@@ -154,13 +157,13 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     if (T > a.max_query_len && blockIdx.x == 0 && kvh == 0 && threadIdx.x == 0)
         report(a.status, PA_DEV_BAD_QUERY_LEN);
-    const int t0 = mt * tok_per_tile;
+    const int t0 = mt * kQT * tok_per_tile;       // first token of tile A
     if (t0 >= T) return;
-    const int ntok = min(tok_per_tile, T - t0);
+    const bool has_b = t0 + tok_per_tile < T;
     const int C = L - T;
-    const int qpos_lo = C + t0, qpos_hi = C + t0 + ntok - 1;
-    const int kv_hi = qpos_hi + 1;
-    const int kv_lo = a.window > 0 ? max(0, qpos_lo + 1 - a.window) : 0;
+    const int last_tok = min(T, t0 + kQT * tok_per_tile) - 1;
+    const int kv_hi = C + last_tok + 1;
+    const int kv_lo = a.window > 0 ? max(0, C + t0 + 1 - a.window) : 0;
     const int blk_lo = kv_lo / kBlockSize;
     const int blk_hi = (kv_hi + kBlockSize - 1) / kBlockSize;
     const int n_tiles = (blk_hi - blk_lo + 7) / 8;
@@ -188,11 +191,11 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_init(&bars[kVFull + s], 1);
             mbar_init(&bars[kVEmpty + s], 1);
         }
-        for (int s = 0; s < kSBufs; ++s) {
-            mbar_init(&bars[kSFull + s], 1);
-            mbar_init(&bars[kPFull + s], kSoftmaxThreads);
+        for (int x = 0; x < kQT; ++x) {
+            mbar_init(&bars[kSFull + x], 1);
+            mbar_init(&bars[kPFull + x], kGroup);
+            mbar_init(&bars[kPvDone + x], 1);
         }
-        mbar_init(&bars[kPvDone], 1);
         mbar_init(&bars[kDrain], 1);
         *fail = 0;
         fence_mbar_init();
@@ -209,9 +212,13 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (warp == 0) {
         // ---------------- TMA producer ----------------
         if (lane == 0) {
-            mbar_arrive_expect_tx(&bars[kQFull], kTile);
-            tma_load_4d(sQ, &qmap, 0, 0, kvh, q0 + t0, &bars[kQFull]);
-            tma_load_4d(sQ + kHalf, &qmap, 64, 0, kvh, q0 + t0, &bars[kQFull]);
+            const int nq = has_b ? kQT : 1;
+            mbar_arrive_expect_tx(&bars[kQFull], nq * kTile);
+            for (int x = 0; x < nq; ++x) {
+                const int row0 = q0 + t0 + x * tok_per_tile;
+                tma_load_4d(sQ + x * kTile, &qmap, 0, 0, kvh, row0, &bars[kQFull]);
+                tma_load_4d(sQ + x * kTile + kHalf, &qmap, 64, 0, kvh, row0, &bars[kQFull]);
+            }
             const int32_t *trow = a.block_tables + (size_t)b * a.max_blocks;
             int issued_k = 0, issued_v = 0;
             for (int j = 0; j < n_tiles; ++j) {
@@ -261,50 +268,61 @@ __global__ void __launch_bounds__(kThreads, 1)
             constexpr uint32_t idPV = idesc_bf16_f32(kRows, kD, true);
             const uint32_t q_u = smem_u32(sQ), k_u = smem_u32(sK), v_u = smem_u32(sV);
             bool ok = wait_or_fail(&bars[kQFull], 0, fail, a.status);
-            auto issue_pv = [&](int i) -> bool {
-                const int s = i % kSBufs;            // S / P buffer
-                const int sv = i % kStages;          // V stage
-                if (!wait_or_fail(&bars[kPFull + s], (i / kSBufs) & 1, fail, a.status)) return false;
-                if (!wait_or_fail(&bars[kVFull + sv], (i / kStages) & 1, fail, a.status)) return false;
-                tc_fence_after();
-                const uint32_t vb = v_u + sv * kTile;
-                // P of tokens [16k, 16k + 16) (owned by the softmax thread of
-                // part 16k / kCols): head pairs from column kCols * part +
-                // (16k mod kCols) / 2 of the S buffer, residual kCols / 2 further
-#pragma unroll
-                for (int k = 0; k < 8; ++k) {
-                    const uint32_t pc = tmem + s * kKv + (16 * k / kCols) * kCols + (16 * k % kCols) / 2;
-                    const uint64_t vdesc = sw128_desc(vb + k * 2048, kHalf, 1024);
-                    umma_bf16_tmem_a(tmem + kColO, pc, vdesc, idPV, (i > 0 || k > 0) ? 1u : 0u);
-                    umma_bf16_tmem_a(tmem + kColO, pc + kCols / 2, vdesc, idPV, 1u);
-                }
-                umma_commit(&bars[kPvDone]);
-                umma_commit(&bars[kVEmpty + sv]);
-                return true;
-            };
-            // order: S_0, S_1, S_2, PV_0, S_3, PV_1, ...: S_j overwrites the P
-            // of tile j - 3, whose PV was issued one iteration earlier
-            for (int j = 0; ok && j < n_tiles; ++j) {
-                const int s = j % kSBufs;
-                const int sk = j % kStages;
-                if (!wait_or_fail(&bars[kKFull + sk], (j / kStages) & 1, fail, a.status)) break;
-                tc_fence_after();
-                const uint32_t kb = k_u + sk * kTile;
+            auto issue_s = [&](int x, int j) {
+                const uint32_t qb = q_u + x * kTile;
+                const uint32_t kb = k_u + (j % kStages) * kTile;
 #pragma unroll
                 for (int k = 0; k < 8; ++k) {
                     const uint32_t o = (k >> 2) * kHalf + (k & 3) * 32;
-                    umma_bf16(tmem + s * kKv, sw128_desc(q_u + o, 16, 1024),
+                    umma_bf16(tmem + col_s(x), sw128_desc(qb + o, 16, 1024),
                               sw128_desc(kb + o, 16, 1024), idS, k > 0 ? 1u : 0u);
                 }
-                umma_commit(&bars[kSFull + s]);
-                umma_commit(&bars[kKEmpty + sk]);
-                if (j >= 2 && !issue_pv(j - 2)) {
-                    ok = false;
-                    break;
+                umma_commit(&bars[kSFull + x]);
+            };
+            // P of tokens [16k, 16k + 16) sits in the 32-column chunk k / 2 of
+            // the S buffer: head pairs from column 32 (k / 2) + 8 (k % 2),
+            // residual pairs 16 columns further
+            auto issue_pv = [&](int x, int j) -> bool {
+                if (!wait_or_fail(&bars[kPFull + x], j & 1, fail, a.status)) return false;
+                tc_fence_after();
+                const uint32_t vb = v_u + (j % kStages) * kTile;
+#pragma unroll
+                for (int k = 0; k < 8; ++k) {
+                    const uint32_t pc = tmem + col_s(x) + 32 * (k >> 1) + 8 * (k & 1);
+                    const uint64_t vdesc = sw128_desc(vb + k * 2048, kHalf, 1024);
+                    umma_bf16_tmem_a(tmem + col_o(x), pc, vdesc, idPV, (j > 0 || k > 0) ? 1u : 0u);
+                    umma_bf16_tmem_a(tmem + col_o(x), pc + 16, vdesc, idPV, 1u);
+                }
+                umma_commit(&bars[kPvDone + x]);
+                return true;
+            };
+            if (ok && wait_or_fail(&bars[kKFull], 0, fail, a.status)) {
+                tc_fence_after();
+                issue_s(0, 0);
+                if (has_b) issue_s(1, 0);
+                umma_commit(&bars[kKEmpty]);
+            } else {
+                ok = false;
+            }
+            for (int j = 0; ok && j < n_tiles; ++j) {
+                const int sv = j % kStages;
+                const bool more = j + 1 < n_tiles;
+                const int sk = (j + 1) % kStages;
+                if (!wait_or_fail(&bars[kVFull + sv], (j / kStages) & 1, fail, a.status)) break;
+                if (!issue_pv(0, j)) break;
+                if (more) {
+                    if (!wait_or_fail(&bars[kKFull + sk], ((j + 1) / kStages) & 1, fail, a.status))
+                        break;
+                    tc_fence_after();
+                    issue_s(0, j + 1);
+                }
+                if (has_b && !issue_pv(1, j)) break;
+                umma_commit(&bars[kVEmpty + sv]);
+                if (more) {
+                    if (has_b) issue_s(1, j + 1);
+                    umma_commit(&bars[kKEmpty + sk]);
                 }
             }
-            for (int i = max(0, n_tiles - 2); ok && i < n_tiles; ++i)
-                if (!issue_pv(i)) ok = false;
             // every MMA issued above has completed once kDrain flips
             umma_commit(&bars[kDrain]);
             if (!mbar_wait_bounded(&bars[kDrain], 0)) {
@@ -313,168 +331,177 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
         }
     } else {
-        // ---------------- softmax warps ----------------
-        const int quarter = warp & 3;
-        const int part = (warp - 2) >> 2;             // columns [kCols * part, kCols * part + kCols)
-        const int r = quarter * 32 + lane;            // tile row = TMEM lane
-        const int tr = r / g;
-        const bool real = tr < ntok;
-        const int qpos = C + t0 + min(tr, ntok - 1);
-        const int wlo = a.window > 0 ? qpos + 1 - a.window : INT_MIN;   // first allowed position
-        const uint32_t lane_base = tmem + ((uint32_t)(quarter * 32) << 16) + part * kCols;
-        float *red = reinterpret_cast<float *>(base + kOffRed);
-        const float sl2 = a.scale_log2;
-        float m_used = -INFINITY, l = 0.f;
-        // Every softmax thread runs every iteration and reaches the named
-        // barrier the same number of times, even after a wait gave up (then it
-        // only skips the work), so that no barrier can wait forever.
-        bool ok = true;
-        for (int j = 0; j < n_tiles; ++j) {
-            const int s = j % kSBufs;
-            const bool got = ok && warp_wait(&bars[kSFull + s], (j / kSBufs) & 1, fail, a.status);
-            const int k0 = (blk_lo + 8 * j) * kBlockSize + part * kCols;   // position of column 0
-            const bool masked = (k0 + kCols - 1 > qpos_lo) ||
-                                (a.window > 0 && k0 < qpos_hi + 1 - a.window);
-            uint32_t v[kCols];
-            if (!got) {
+        // ---------------- softmax groups ----------------
+        const int x = (warp - 2) / (kGroup / 32);     // Q tile of this group
+        const int gw = (warp - 2) % (kGroup / 32);    // warp within the group
+        if (x == 0 || has_b) {
+            const int quarter = warp & 3;
+            const int part = gw >> 2;                     // columns [kCols * part, + kCols)
+            const int r = quarter * 32 + lane;            // tile row = TMEM lane
+            const int tx0 = t0 + x * tok_per_tile;        // first token of this tile
+            const int ntok = max(0, min(tok_per_tile, T - tx0));
+            const int tr = r / g;
+            const bool real = tr < ntok;
+            const int qpos = C + tx0 + min(tr, max(ntok, 1) - 1);
+            const int qpos_lo = C + tx0, qpos_hi = C + tx0 + max(ntok, 1) - 1;
+            const int wlo = a.window > 0 ? qpos + 1 - a.window : INT_MIN;
+            const uint32_t lane_off = ((uint32_t)(quarter * 32) << 16) + part * kCols;
+            const uint32_t s_base = tmem + col_s(x) + lane_off;
+            const uint32_t o_base = tmem + col_o(x) + lane_off;
+            float *red = reinterpret_cast<float *>(base + kOffRed) + x * 2 * kSplit * kRows;
+            const float sl2 = a.scale_log2;
+            float m_used = -INFINITY, l = 0.f;
+            // Every thread of the group runs every iteration and reaches the
+            // named barrier the same number of times, even after a wait gave up
+            // (then it only skips the work), so that no barrier waits forever.
+            bool ok = true;
+            for (int j = 0; j < n_tiles; ++j) {
+                const bool got = ok && warp_wait(&bars[kSFull + x], j & 1, fail, a.status);
+                const int k0 = (blk_lo + 8 * j) * kBlockSize + part * kCols;   // column 0's position
+                // pass 1: row maximum over this thread's columns
+                float mx4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+                if (got) {
+                    tc_fence_after();
+#pragma unroll 1
+                    for (int c = 0; c < kCols; c += 32) {
+                        uint32_t v[32];
+                        tmem_ld32(s_base + c, v);
+                        tmem_wait_ld();
+                        const int kc = k0 + c;
+                        if ((kc + 31 > qpos_lo) || (a.window > 0 && kc < qpos_hi + 1 - a.window)) {
 #pragma unroll
-                for (int i = 0; i < kCols; ++i) v[i] = __float_as_uint(-INFINITY);
-            } else {
-                tc_fence_after();
+                            for (int i = 0; i < 32; ++i)
+                                if (!(kc + i <= qpos && kc + i >= wlo)) v[i] = __float_as_uint(-INFINITY);
+                        }
 #pragma unroll
-                for (int c = 0; c < kCols; c += 32)
-                    tmem_ld32(lane_base + s * kKv + c, *reinterpret_cast<uint32_t (*)[32]>(&v[c]));
-                tmem_wait_ld();
-            }
-            if (masked) {
-#pragma unroll
-                for (int i = 0; i < kCols; ++i) {
-                    const int kp = k0 + i;
-                    if (!(kp <= qpos && kp >= wlo)) v[i] = __float_as_uint(-INFINITY);
+                        for (int i = 0; i < 32; ++i) mx4[i & 3] = fmaxf(mx4[i & 3], __uint_as_float(v[i]));
+                    }
                 }
-            }
-            // row maximum: four independent chains, then the other parts'
-            float mx4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+                float mrow = fmaxf(fmaxf(mx4[0], mx4[1]), fmaxf(mx4[2], mx4[3]));
+                const int rp = j & 1;
+                red[(rp * kSplit + part) * kRows + r] = mrow;
+                named_sync(1 + x);
 #pragma unroll
-            for (int i = 0; i < kCols; ++i) mx4[i & 3] = fmaxf(mx4[i & 3], __uint_as_float(v[i]));
-            float mrow = fmaxf(fmaxf(mx4[0], mx4[1]), fmaxf(mx4[2], mx4[3]));
-            const int rp = j & 1;                     // exchange slots of this tile
-            red[(rp * kSplit + part) * kRows + r] = mrow;
-            asm volatile("bar.sync 1, %0;" ::"n"(kSoftmaxThreads) : "memory");
-#pragma unroll
-            for (int o = 1; o < kSplit; ++o)
-                mrow = fmaxf(mrow, red[(rp * kSplit + ((part + o) % kSplit)) * kRows + r]);
-            if (!got) {
-                ok = false;
-                continue;
-            }
-            const float m_tile = mrow * sl2;
-            const float m_new = fmaxf(m_used, m_tile);
-            // Lazy rescale: only rows whose maximum grew by more than 2^8 move
-            // their reference; the warp rescales O together (tensor-memory
-            // access is warp-wide), with factor 1 on the other rows, once every
-            // PV issued so far has landed in O.
-            const bool need = m_new > m_used + kRescaleLog2;
-            const float alpha = need ? exp2f(m_used - m_new) : 1.f;   // 0 while m_used is -inf
-            if (j >= 1 && __any_sync(0xffffffffu, need)) {
-                if (!warp_wait(&bars[kPvDone], (j - 1) & 1, fail, a.status)) {
+                for (int o = 1; o < kSplit; ++o)
+                    mrow = fmaxf(mrow, red[(rp * kSplit + ((part + o) % kSplit)) * kRows + r]);
+                if (!got) {
                     ok = false;
                     continue;
                 }
+                const float m_new = fmaxf(m_used, mrow * sl2);
+                // Lazy rescale: only rows whose maximum grew by more than 2^8
+                // move their reference; the warp rescales O together (warp-wide
+                // tensor-memory access, factor 1 on the other rows) once every
+                // PV of this tile issued so far has landed.
+                const bool need = m_new > m_used + kRescaleLog2;
+                const float alpha = need ? exp2f(m_used - m_new) : 1.f;   // 0 while m_used is -inf
+                if (j >= 1 && __any_sync(0xffffffffu, need)) {
+                    if (!warp_wait(&bars[kPvDone + x], (j - 1) & 1, fail, a.status)) {
+                        ok = false;
+                        continue;
+                    }
+                    tc_fence_after();
+#pragma unroll 1
+                    for (int c = 0; c < kCols; c += 32) {
+                        uint32_t o[32];
+                        tmem_ld32(o_base + c, o);
+                        tmem_wait_ld();
+#pragma unroll
+                        for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * alpha);
+                        tmem_st32(o_base + c, o);
+                    }
+                    tmem_wait_st();
+                }
+                if (need) {
+                    l *= alpha;
+                    m_used = m_new;
+                }
+                const float m_ref = m_used == -INFINITY ? 0.f : m_used;
+                // pass 2: P = 2^(s * scale_log2 - m_ref) as a bf16 head + bf16
+                // residual, written over the same 32 columns it was read from
+                // (head pairs in the first 16, residual pairs in the next 16)
+                float ps4[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll 1
+                for (int c = 0; c < kCols; c += 32) {
+                    uint32_t v[32];
+                    tmem_ld32(s_base + c, v);
+                    tmem_wait_ld();
+                    const int kc = k0 + c;
+                    const bool masked =
+                        (kc + 31 > qpos_lo) || (a.window > 0 && kc < qpos_hi + 1 - a.window);
+                    uint32_t hi[16], lo[16];
+#pragma unroll
+                    for (int i = 0; i < 32; i += 2) {
+                        float p0 = ex2_approx(fmaf(__uint_as_float(v[i]), sl2, -m_ref));
+                        float p1 = ex2_approx(fmaf(__uint_as_float(v[i + 1]), sl2, -m_ref));
+                        if (masked) {
+                            if (!(kc + i <= qpos && kc + i >= wlo)) p0 = 0.f;
+                            if (!(kc + i + 1 <= qpos && kc + i + 1 >= wlo)) p1 = 0.f;
+                        }
+                        ps4[(i >> 1) & 3] += p0 + p1;
+                        const uint32_t h = pack2_bf16(p0, p1);
+                        hi[i >> 1] = h;
+                        lo[i >> 1] = pack2_bf16(p0 - __uint_as_float(h << 16),
+                                                p1 - __uint_as_float(h & 0xffff0000u));
+                    }
+                    tmem_st16(s_base + c, hi);
+                    tmem_st16(s_base + c + 16, lo);
+                }
+                tmem_wait_st();
+                l += (ps4[0] + ps4[1]) + (ps4[2] + ps4[3]);
+                // V rows of positions outside [kv_lo, kv_hi) may hold anything
+                // (NaN included): tile A's group zeroes them (PV_B runs after
+                // PV_A) so that 0 * row stays 0; each thread clears its share.
+                const int k0_tile = (blk_lo + 8 * j) * kBlockSize;
+                if (x == 0 && (k0_tile < kv_lo || k0_tile + kKv > kv_hi)) {
+                    if (!warp_wait(&bars[kVFull + j % kStages], (j / kStages) & 1, fail, a.status)) {
+                        ok = false;
+                        continue;
+                    }
+                    const int kp = k0_tile + r;
+                    if (kp < kv_lo || kp >= kv_hi) {
+                        constexpr int kBytes = 256 / kSplit;
+                        const int b0 = part * kBytes;
+                        uint8_t *vrow = sV + (j % kStages) * kTile + (b0 >> 7) * kHalf +
+                                        (r >> 3) * 1024 + (r & 7) * 128 + (b0 & 127);
+#pragma unroll
+                        for (int q = 0; q < kBytes / 16; ++q)
+                            *reinterpret_cast<uint4 *>(vrow + q * 16) = make_uint4(0, 0, 0, 0);
+                    }
+                }
+                fence_proxy_async_smem();
+                tc_fence_before();
+                mbar_arrive(&bars[kPFull + x]);
+            }
+            // the row sum is the parts' sums (all against the same maximum),
+            // exchanged in the slots of the parity the last tile did not use
+            const int sx = n_tiles & 1;
+            red[(sx * kSplit + part) * kRows + r] = l;
+            named_sync(1 + x);
+            float l_row = l;
+#pragma unroll
+            for (int o = 1; o < kSplit; ++o) l_row += red[(sx * kSplit + ((part + o) % kSplit)) * kRows + r];
+            if (__all_sync(0xffffffffu, ok) && warp_wait(&bars[kDrain], 0, fail, a.status)) {
                 tc_fence_after();
+                const float inv = l_row > 0.f ? 1.f / l_row : 0.f;
+                __nv_bfloat16 *orow = static_cast<__nv_bfloat16 *>(a.out) +
+                                      ((size_t)(q0 + tx0 + tr) * a.num_q_heads + kvh * g + (r % g)) * kD +
+                                      part * kCols;
 #pragma unroll 1
                 for (int c = 0; c < kCols; c += 32) {
                     uint32_t o[32];
-                    tmem_ld32(lane_base + kColO + c, o);
+                    tmem_ld32(o_base + c, o);
                     tmem_wait_ld();
+                    if (real) {
 #pragma unroll
-                    for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * alpha);
-                    tmem_st32(lane_base + kColO + c, o);
-                }
-                tmem_wait_st();
-            }
-            if (need) {
-                l *= alpha;
-                m_used = m_new;
-            }
-            const float m_ref = m_used == -INFINITY ? 0.f : m_used;
-            // P = 2^(s * scale_log2 - m_ref) as a bf16 head + bf16 residual,
-            // written over this thread's own S columns: head pairs in the
-            // first half, residual pairs in the second
-            float ps4[4] = {0.f, 0.f, 0.f, 0.f};
-            uint32_t hi[kCols / 2], lo[kCols / 2];
-#pragma unroll
-            for (int i = 0; i < kCols; i += 2) {
-                const float p0 = ex2_approx(fmaf(__uint_as_float(v[i]), sl2, -m_ref));
-                const float p1 = ex2_approx(fmaf(__uint_as_float(v[i + 1]), sl2, -m_ref));
-                ps4[(i >> 1) & 3] += p0 + p1;
-                const uint32_t h = pack2_bf16(p0, p1);
-                hi[i >> 1] = h;
-                lo[i >> 1] = pack2_bf16(p0 - __uint_as_float(h << 16),
-                                        p1 - __uint_as_float(h & 0xffff0000u));
-            }
-#pragma unroll
-            for (int c = 0; c < kCols / 2; c += 16) {
-                tmem_st16(lane_base + s * kKv + c, *reinterpret_cast<const uint32_t (*)[16]>(&hi[c]));
-                tmem_st16(lane_base + s * kKv + kCols / 2 + c,
-                          *reinterpret_cast<const uint32_t (*)[16]>(&lo[c]));
-            }
-            tmem_wait_st();
-            l += (ps4[0] + ps4[1]) + (ps4[2] + ps4[3]);
-            // V rows of positions outside [kv_lo, kv_hi) may hold anything
-            // (NaN included): zero them so that 0 * row stays 0 (the kSplit
-            // threads of a row clear a share of it each).
-            const int k0_tile = (blk_lo + 8 * j) * kBlockSize;
-            if (k0_tile < kv_lo || k0_tile + kKv > kv_hi) {
-                if (!warp_wait(&bars[kVFull + j % kStages], (j / kStages) & 1, fail, a.status)) {
-                    ok = false;
-                    continue;
-                }
-                const int kp = k0_tile + r;
-                if (kp < kv_lo || kp >= kv_hi) {
-                    // this thread's share of the row's 256 bytes (two 128-byte regions)
-                    constexpr int kBytes = 256 / kSplit;
-                    const int b0 = part * kBytes;
-                    uint8_t *vrow = sV + (j % kStages) * kTile + (b0 >> 7) * kHalf + (r >> 3) * 1024 +
-                                    (r & 7) * 128 + (b0 & 127);
-#pragma unroll
-                    for (int q = 0; q < kBytes / 16; ++q)
-                        *reinterpret_cast<uint4 *>(vrow + q * 16) = make_uint4(0, 0, 0, 0);
-                }
-            }
-            fence_proxy_async_smem();
-            tc_fence_before();
-            mbar_arrive(&bars[kPFull + s]);
-        }
-        // the row sum is the parts' sums (all kept against the same maximum);
-        // exchanged in the slots of the parity the last tile did not use,
-        // whose reads all finished before the last tile's barrier
-        const int sx = n_tiles & 1;
-        red[(sx * kSplit + part) * kRows + r] = l;
-        asm volatile("bar.sync 1, %0;" ::"n"(kSoftmaxThreads) : "memory");
-        float l_row = l;
-#pragma unroll
-        for (int o = 1; o < kSplit; ++o) l_row += red[(sx * kSplit + ((part + o) % kSplit)) * kRows + r];
-        if (__all_sync(0xffffffffu, ok) && warp_wait(&bars[kDrain], 0, fail, a.status)) {
-            tc_fence_after();
-            const float inv = l_row > 0.f ? 1.f / l_row : 0.f;
-            __nv_bfloat16 *orow = static_cast<__nv_bfloat16 *>(a.out) +
-                                  ((size_t)(q0 + t0 + tr) * a.num_q_heads + kvh * g + (r % g)) * kD +
-                                  part * kCols;
-#pragma unroll 1
-            for (int c = 0; c < kCols; c += 32) {
-                uint32_t o[32];
-                tmem_ld32(lane_base + kColO + c, o);
-                tmem_wait_ld();
-                if (real) {
-#pragma unroll
-                    for (int q = 0; q < 4; ++q) {
-                        uint4 w;
-                        w.x = pack2_bf16(__uint_as_float(o[8 * q + 0]) * inv, __uint_as_float(o[8 * q + 1]) * inv);
-                        w.y = pack2_bf16(__uint_as_float(o[8 * q + 2]) * inv, __uint_as_float(o[8 * q + 3]) * inv);
-                        w.z = pack2_bf16(__uint_as_float(o[8 * q + 4]) * inv, __uint_as_float(o[8 * q + 5]) * inv);
-                        w.w = pack2_bf16(__uint_as_float(o[8 * q + 6]) * inv, __uint_as_float(o[8 * q + 7]) * inv);
-                        *reinterpret_cast<uint4 *>(orow + c + 8 * q) = w;
+                        for (int q = 0; q < 4; ++q) {
+                            uint4 w;
+                            w.x = pack2_bf16(__uint_as_float(o[8 * q + 0]) * inv, __uint_as_float(o[8 * q + 1]) * inv);
+                            w.y = pack2_bf16(__uint_as_float(o[8 * q + 2]) * inv, __uint_as_float(o[8 * q + 3]) * inv);
+                            w.z = pack2_bf16(__uint_as_float(o[8 * q + 4]) * inv, __uint_as_float(o[8 * q + 5]) * inv);
+                            w.w = pack2_bf16(__uint_as_float(o[8 * q + 6]) * inv, __uint_as_float(o[8 * q + 7]) * inv);
+                            *reinterpret_cast<uint4 *>(orow + c + 8 * q) = w;
+                        }
                     }
                 }
             }
@@ -530,7 +557,7 @@ extern "C" pa_status pa_prefill(void *out, const void *query, const void *key_ca
         return PA_ERR_INVALID_ARG;
     const int64_t rows = (int64_t)num_blocks * num_kv_heads * kBlockSize;
     if (rows >= ((int64_t)1 << 31)) return PA_ERR_UNSUPPORTED;
-    const int64_t tiles = ((int64_t)max_query_len * group + kRows - 1) / kRows;
+    const int64_t tiles = ((int64_t)max_query_len * group + kQT * kRows - 1) / (kQT * kRows);
     if (tiles > 0x7fffffff || num_kv_heads > 65535 || num_seqs > 65535) return PA_ERR_UNSUPPORTED;
     auto enc = encoder();
     if (enc == nullptr) return cuda_failure(cudaErrorInvalidValue, "cuTensorMapEncodeTiled lookup");
