@@ -18,7 +18,7 @@ LIB = os.path.join(BUILD, "libpagedkv.so")
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 CU_SOURCES = ["pa_decode.cu", "pa_cache.cu", "pa_decode_noalloc.cu", "pa_prefill.cu"]
 CPP_SOURCES = ["block_manager.cpp"]
-HEADERS = ["pa_device.cuh", "pa_internal.h"]
+HEADERS = ["pa_device.cuh", "pa_internal.h", "pa_tc.cuh"]
 
 
 def _nvcc() -> str:

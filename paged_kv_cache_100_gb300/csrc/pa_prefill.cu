@@ -44,6 +44,7 @@
 
 #include "pa_device.cuh"
 #include "pa_internal.h"
+#include "pa_tc.cuh"
 
 namespace pa {
 namespace {
