@@ -1370,12 +1370,20 @@ __global__ void __launch_bounds__(NW * 32) pa_decode_f32_kernel(const float *__r
 }
 
 // Merges the partitions of every (sequence, query head) that has more than one.
+// Merge of the split-K partials: one warp per (sequence, query head) row, four
+// rows per CTA.  Every lane owns D/128 float4 columns of the output; the
+// partials' (max, sum) pairs are read by the lanes in parallel, and the
+// partial rows are loaded eight at a time so that their L2 latencies overlap.
+constexpr int kReduceRows = 4;
+
 template <typename OutT>
-__global__ void __launch_bounds__(128) pa_reduce_kernel(const DecodeArgs a, int D) {
+__global__ void __launch_bounds__(32 * kReduceRows) pa_reduce_kernel(const DecodeArgs a, int D) {
     grid_dependency_wait();
     grid_dependents_launch();
-    const int b = blockIdx.x / a.num_q_heads;
-    const int h = blockIdx.x - b * a.num_q_heads;
+    const int lane = threadIdx.x & 31;
+    const int row = blockIdx.x * kReduceRows + (threadIdx.x >> 5);
+    if (row >= a.num_seqs * a.num_q_heads) return;
+    const int b = row / a.num_q_heads;
     int L = a.context_lens[b];
     const int lmax = a.max_blocks * kBlockSize;
     L = L < 0 ? 0 : (L > lmax ? lmax : L);
@@ -1385,35 +1393,51 @@ __global__ void __launch_bounds__(128) pa_reduce_kernel(const DecodeArgs a, int 
     const int nparts =
         a.part_base + (range <= 0 ? 1 : (range + a.part_blocks - 1) / a.part_blocks);
     if (nparts <= 1 && !a.always_partial) return;
-    const size_t row0 = ((size_t)b * a.num_q_heads + h) * a.max_parts;
-    extern __shared__ float s_w[];   // [nparts] weights
-    __shared__ float s_M, s_L;
-    if (threadIdx.x < 32) {
-        float M = -INFINITY;
-        for (int p = threadIdx.x; p < nparts; p += 32) M = fmaxf(M, a.part_ml[row0 + p].x);
+    const size_t row0 = (size_t)row * a.max_parts;
+    const float2 *ml = a.part_ml + row0;
+    float M = -INFINITY;
+    for (int p = lane; p < nparts; p += 32) M = fmaxf(M, ml[p].x);
 #pragma unroll
-        for (int k = 16; k >= 1; k >>= 1) M = fmaxf(M, __shfl_xor_sync(kFull, M, k));
-        float Lsum = 0.f;
-        for (int p = threadIdx.x; p < nparts; p += 32) {
-            const float2 ml = a.part_ml[row0 + p];
-            const float wgt = ml.x == -INFINITY ? 0.f : exp2f(ml.x - M);
-            s_w[p] = wgt;
-            Lsum += wgt * ml.y;
-        }
-#pragma unroll
-        for (int k = 16; k >= 1; k >>= 1) Lsum += __shfl_xor_sync(kFull, Lsum, k);
-        if (threadIdx.x == 0) {
-            s_M = M;
-            s_L = Lsum;
-        }
+    for (int k = 16; k >= 1; k >>= 1) M = fmaxf(M, __shfl_xor_sync(kFull, M, k));
+    float Lsum = 0.f;
+    for (int p = lane; p < nparts; p += 32) {
+        const float2 v = ml[p];
+        Lsum += v.x == -INFINITY ? 0.f : exp2f(v.x - M) * v.y;
     }
-    __syncthreads();
-    const float inv = s_L > 0.f ? 1.f / s_L : 0.f;
-    OutT *out = static_cast<OutT *>(a.out) + ((size_t)b * a.num_q_heads + h) * D;
-    for (int d = threadIdx.x; d < D; d += blockDim.x) {
-        float O = 0.f;
-        for (int p = 0; p < nparts; ++p) O = fmaf(s_w[p], a.part_o[(row0 + p) * D + d], O);
-        store_out<OutT>(out + d, s_L > 0.f ? O * inv : 0.f);
+#pragma unroll
+    for (int k = 16; k >= 1; k >>= 1) Lsum += __shfl_xor_sync(kFull, Lsum, k);
+    const float inv = Lsum > 0.f ? 1.f / Lsum : 0.f;
+    const int q4 = D >> 2;                         // float4 columns per row
+    const float4 *po = reinterpret_cast<const float4 *>(a.part_o + row0 * D);
+    OutT *out = static_cast<OutT *>(a.out) + (size_t)row * D;
+    for (int q = lane; q < q4; q += 32) {
+        float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+        for (int p0 = 0; p0 < nparts; p0 += 8) {
+            float4 v[8];
+            float w[8];
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+                if (p0 + i < nparts) {
+                    v[i] = po[(size_t)(p0 + i) * q4 + q];
+                    const float mi = ml[p0 + i].x;
+                    w[i] = mi == -INFINITY ? 0.f : exp2f(mi - M);
+                } else {
+                    v[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+                    w[i] = 0.f;
+                }
+            }
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+                acc.x = fmaf(w[i], v[i].x, acc.x);
+                acc.y = fmaf(w[i], v[i].y, acc.y);
+                acc.z = fmaf(w[i], v[i].z, acc.z);
+                acc.w = fmaf(w[i], v[i].w, acc.w);
+            }
+        }
+        store_out<OutT>(out + 4 * q + 0, acc.x * inv);
+        store_out<OutT>(out + 4 * q + 1, acc.y * inv);
+        store_out<OutT>(out + 4 * q + 2, acc.z * inv);
+        store_out<OutT>(out + 4 * q + 3, acc.w * inv);
     }
 }
 
@@ -1582,14 +1606,10 @@ pa_status launch_f32(const DecodeArgs &a, const void *kc, const void *vc, cudaSt
 
 template <typename OutT>
 pa_status launch_reduce(const DecodeArgs &a, int D, cudaStream_t stream) {
-    const size_t smem = (size_t)a.max_parts * sizeof(float);
     auto kernel = pa_reduce_kernel<OutT>;
-    if (smem > 48 * 1024) {
-        cudaError_t e = allow_smem(kernel, smem);
-        if (e != cudaSuccess) return cuda_failure(e, "cudaFuncSetAttribute(reduce)");
-    }
-    cudaError_t e = launch_chained(kernel, dim3((unsigned)(a.num_seqs * a.num_q_heads)), dim3(128),
-                                   smem, stream, a, D);
+    const int64_t rows = (int64_t)a.num_seqs * a.num_q_heads;
+    const unsigned grid = (unsigned)((rows + kReduceRows - 1) / kReduceRows);
+    cudaError_t e = launch_chained(kernel, dim3(grid), dim3(32 * kReduceRows), 0, stream, a, D);
     if (e != cudaSuccess) return cuda_failure(e, "pa_reduce_kernel launch");
     count_launches(1);
     return PA_OK;
