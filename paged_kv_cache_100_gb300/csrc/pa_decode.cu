@@ -1926,8 +1926,9 @@ struct SharedPlan {
     int suffix_part_blocks, suffix_max_parts, prefix_chunk_blocks, prefix_chunks, max_parts;
 };
 
-bool plan_shared(int num_seqs, int num_q_heads, int num_kv_heads, int max_blocks_per_seq,
-                 int num_prefix_blocks, int partition_size, SharedPlan *p) {
+bool plan_shared(int num_seqs, int num_q_heads, int num_kv_heads, int head_dim,
+                 int max_blocks_per_seq, int num_prefix_blocks, int partition_size,
+                 SharedPlan *p) {
     if (num_prefix_blocks < 0 || num_prefix_blocks > max_blocks_per_seq) return false;
     const int suffix_blocks = max_blocks_per_seq - num_prefix_blocks;
     const int ps = resolve_partition(partition_size, num_seqs, num_kv_heads, suffix_blocks);
@@ -1935,9 +1936,18 @@ bool plan_shared(int num_seqs, int num_q_heads, int num_kv_heads, int max_blocks
     p->suffix_part_blocks = ps / kBlockSize;
     p->suffix_max_parts = std::max(1, (suffix_blocks + p->suffix_part_blocks - 1) / p->suffix_part_blocks);
     const int group = num_q_heads / num_kv_heads;
-    const int row_chunks = (num_seqs * group + kPrefixRows - 1) / kPrefixRows;
-    prefix_chunking(num_prefix_blocks, num_kv_heads, row_chunks, &p->prefix_chunk_blocks,
-                    &p->prefix_chunks);
+    if (prefix_tc_supported(head_dim, num_q_heads, num_kv_heads)) {
+        // tensor-core prefix: whole 8-block K/V tiles, about one CTA per SM
+        p->prefix_chunk_blocks =
+            prefix_tc_chunk_blocks(num_seqs, num_q_heads, num_kv_heads, num_prefix_blocks, sm_count());
+        p->prefix_chunks = num_prefix_blocks == 0
+                               ? 0
+                               : (num_prefix_blocks + p->prefix_chunk_blocks - 1) / p->prefix_chunk_blocks;
+    } else {
+        const int row_chunks = (num_seqs * group + kPrefixRows - 1) / kPrefixRows;
+        prefix_chunking(num_prefix_blocks, num_kv_heads, row_chunks, &p->prefix_chunk_blocks,
+                        &p->prefix_chunks);
+    }
     p->max_parts = p->prefix_chunks + p->suffix_max_parts;
     return true;
 }
@@ -1957,8 +1967,8 @@ extern "C" size_t pa_decode_shared_prefix_workspace_bytes(int num_seqs, int num_
         (partition_size < kBlockSize || partition_size > kMaxPartition || partition_size % kBlockSize))
         return (size_t)-1;
     SharedPlan p;
-    if (!plan_shared(num_seqs, num_q_heads, num_kv_heads, max_blocks_per_seq, num_prefix_blocks,
-                     partition_size, &p))
+    if (!plan_shared(num_seqs, num_q_heads, num_kv_heads, head_dim, max_blocks_per_seq,
+                     num_prefix_blocks, partition_size, &p))
         return (size_t)-1;
     const size_t rows = (size_t)num_seqs * num_q_heads * p.max_parts;
     return ((rows * head_dim * sizeof(float) + 255) & ~size_t(255)) + rows * sizeof(float2);
@@ -1994,8 +2004,8 @@ extern "C" pa_status pa_decode_shared_prefix(
     const int64_t rows = (int64_t)num_blocks * num_kv_heads * kBlockSize;
     if (rows >= ((int64_t)1 << 31)) return PA_ERR_UNSUPPORTED;
     SharedPlan p;
-    if (!plan_shared(num_seqs, num_q_heads, num_kv_heads, max_blocks_per_seq, num_prefix_blocks,
-                     partition_size, &p))
+    if (!plan_shared(num_seqs, num_q_heads, num_kv_heads, head_dim, max_blocks_per_seq,
+                     num_prefix_blocks, partition_size, &p))
         return PA_ERR_INVALID_ARG;
     const size_t need = pa_decode_shared_prefix_workspace_bytes(
         num_seqs, num_q_heads, num_kv_heads, head_dim, max_blocks_per_seq, num_prefix_blocks,
@@ -2044,9 +2054,19 @@ extern "C" pa_status pa_decode_shared_prefix(
     if (fe == cudaSuccess) fe = cudaStreamWaitEvent(side->stream, side->fork, 0);
     if (fe != cudaSuccess) return cuda_failure(fe, "side stream fork");
 
-    // 1. the shared prefix, once per KV head for 64 query rows at a time, on the
-    //    side stream
-    {
+    // 1. the shared prefix, once per KV head for all sequences, on the side
+    //    stream: on the tensor cores (256 rows per K/V tile) where the shape
+    //    allows, else 64 query rows at a time on mma.sync tiles
+    if (prefix_tc_supported(head_dim, num_q_heads, num_kv_heads)) {
+        pa_status ps = launch_prefix_tc(query, key_cache, value_cache, block_tables, context_lens,
+                                        num_seqs, num_q_heads, num_kv_heads, max_blocks_per_seq,
+                                        num_blocks, a.scale_log2, num_prefix_blocks,
+                                        p.prefix_chunk_blocks, p.prefix_chunks, a.part_o,
+                                        a.part_ml, p.max_parts, device_status, side->stream);
+        cudaError_t e = cudaEventRecord(side->join, side->stream);
+        if (ps != PA_OK) return ps;
+        if (e != cudaSuccess) return cuda_failure(e, "side stream join record");
+    } else {
         CUtensorMap kmap, vmap;
         if (!encode_pool_map(&kmap, key_cache, rows, head_dim, 2) ||
             !encode_pool_map(&vmap, value_cache, rows, head_dim, 2))

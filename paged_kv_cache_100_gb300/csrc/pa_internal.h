@@ -42,4 +42,17 @@ cudaError_t launch_chained(void (*kernel)(KArgs...), dim3 grid, dim3 block, size
     return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
 }
 
+// Shared prefix of a decode batch on the tensor cores (pa_prefill.cu): split-K
+// partials (max, sum, unnormalised output) of every (sequence, query head) row
+// against each chunk of the prefix blocks, written to partial index = chunk.
+bool prefix_tc_supported(int head_dim, int num_q_heads, int num_kv_heads);
+int prefix_tc_chunk_blocks(int num_seqs, int num_q_heads, int num_kv_heads, int prefix_blocks,
+                           int sm_count);
+pa_status launch_prefix_tc(const void *query, const void *key_cache, const void *value_cache,
+                           const int32_t *block_tables, const int32_t *context_lens, int num_seqs,
+                           int num_q_heads, int num_kv_heads, int max_blocks, int num_blocks,
+                           float scale_log2, int prefix_blocks, int chunk_blocks, int chunks,
+                           float *part_o, float2 *part_ml, int max_parts, int32_t *status,
+                           cudaStream_t stream);
+
 }  // namespace pa

@@ -39,6 +39,7 @@
 #include <cudaTypedefs.h>
 #include <math.h>
 
+#include <algorithm>
 #include <climits>
 #include <mutex>
 
@@ -82,7 +83,7 @@ constexpr int kQFull = 0, kKFull = 1, kKEmpty = kKFull + kStages, kVFull = kKEmp
               kVEmpty = kVFull + kStages, kSFull = kVEmpty + kStages, kPFull = kSFull + kQT,
               kPvDone = kPFull + kQT, kDrain = kPvDone + kQT;
 static_assert(kDrain + 1 == kNumBars, "barrier count");
-static_assert(kNumBars * 8 + 8 <= 256, "barrier block");
+static_assert(kNumBars * 8 + 16 <= 256, "barrier block");
 static_assert(kSmemBytes <= 227 * 1024, "shared memory");
 
 // TMEM columns: S_A, S_B, then O_A, O_B.
@@ -90,21 +91,32 @@ constexpr uint32_t kTmemCols = 512;
 __device__ __forceinline__ uint32_t col_s(int x) { return (uint32_t)(x * kKv); }
 __device__ __forceinline__ uint32_t col_o(int x) { return (uint32_t)(kQT * kKv + x * kD); }
 
+}  // namespace
+
 struct PrefillArgs {
-    void *out;
+    void *out;                    // prefill: bf16 [tokens][Hq][D]
     const int32_t *block_tables;
     const int32_t *context_lens;
-    const int32_t *query_start;
+    const int32_t *query_start;   // prefill only
     int32_t *status;
+    int num_seqs;
     int num_q_heads;
     int num_kv_heads;
     int group;
     int max_blocks;
     int num_blocks;
-    int max_query_len;
-    int window;
+    int max_query_len;            // prefill only
+    int window;                   // prefill only
     float scale_log2;
+    // shared-prefix mode: split-K partials of the prefix, one per chunk
+    float *part_o;                // [rows * max_parts][D], rows = (b * Hq + h)
+    float2 *part_ml;              // [rows * max_parts]: (max, sum), log2 domain
+    int max_parts;
+    int prefix_blocks;
+    int chunk_blocks;
 };
+
+namespace {
 
 __device__ __forceinline__ bool wait_or_fail(uint64_t *bar, uint32_t parity, volatile int *fail,
                                              int32_t *status) {
@@ -138,35 +150,59 @@ __device__ __forceinline__ void named_sync(int id) {
     asm volatile("bar.sync %0, %1;" ::"r"(id), "n"(kGroup) : "memory");
 }
 
+// kPrefix = false: chunked prefill.  CTA (pair tile, KV head, sequence): 256
+// (token, head) rows of one sequence's chunk, causal over its own table.
+// kPrefix = true: the shared prefix of a decode batch.  CTA (pair tile, KV
+// head, prefix chunk): 256 (sequence, head) rows across sequences against one
+// chunk of the blocks every table starts with (read from the first table);
+// each row sees the chunk's positions below its own context length, and the
+// CTA writes split-K partials instead of outputs.
+template <bool kPrefix>
 __global__ void __launch_bounds__(kThreads, 1)
-    pa_prefill_kernel(const __grid_constant__ CUtensorMap qmap,
+    pa_attn_tc_kernel(const __grid_constant__ CUtensorMap qmap,
                       const __grid_constant__ CUtensorMap kmap,
                       const __grid_constant__ CUtensorMap vmap, const PrefillArgs a) {
     grid_dependency_wait();
     grid_dependents_launch();
-    const int b = blockIdx.z;
     const int kvh = blockIdx.y;
     const int g = a.group;
     const int tok_per_tile = kRows / g;
-    const int mt = gridDim.x - 1 - blockIdx.x;   // later (longer) tiles first
-    const int q0 = a.query_start[b];
-    const int T = a.query_start[b + 1] - q0;
-    const int L = a.context_lens[b];
-    if (T < 0 || T > L || L > a.max_blocks * kBlockSize) {
-        if (blockIdx.x == 0 && kvh == 0 && threadIdx.x == 0) report(a.status, PA_DEV_BAD_CONTEXT_LEN);
-        return;
+    const int lmax = a.max_blocks * kBlockSize;
+    // b: sequence whose table and chunk (prefill) this CTA serves; q0 + t0:
+    // query row (token, or sequence in prefix mode) of tile A's first group
+    int b, q0, T, C, t0, kv_lo, kv_hi, blk_lo, blk_hi;
+    if constexpr (!kPrefix) {
+        b = blockIdx.z;
+        const int mt = gridDim.x - 1 - blockIdx.x;   // later (longer) tiles first
+        q0 = a.query_start[b];
+        T = a.query_start[b + 1] - q0;
+        const int L = a.context_lens[b];
+        if (T < 0 || T > L || L > lmax) {
+            if (blockIdx.x == 0 && kvh == 0 && threadIdx.x == 0) report(a.status, PA_DEV_BAD_CONTEXT_LEN);
+            return;
+        }
+        if (T > a.max_query_len && blockIdx.x == 0 && kvh == 0 && threadIdx.x == 0)
+            report(a.status, PA_DEV_BAD_QUERY_LEN);
+        t0 = mt * kQT * tok_per_tile;                 // first token of tile A
+        if (t0 >= T) return;
+        C = L - T;
+        const int last_tok = min(T, t0 + kQT * tok_per_tile) - 1;
+        kv_hi = C + last_tok + 1;
+        kv_lo = a.window > 0 ? max(0, C + t0 + 1 - a.window) : 0;
+        blk_lo = kv_lo / kBlockSize;
+        blk_hi = (kv_hi + kBlockSize - 1) / kBlockSize;
+    } else {
+        b = 0;                                         // the shared blocks: first table
+        q0 = 0;
+        T = a.num_seqs;                                // "tokens" are the sequences
+        C = 0;
+        t0 = blockIdx.x * kQT * tok_per_tile;
+        blk_lo = blockIdx.z * a.chunk_blocks;
+        blk_hi = min(a.prefix_blocks, blk_lo + a.chunk_blocks);
+        kv_lo = blk_lo * kBlockSize;
+        kv_hi = blk_hi * kBlockSize;                   // lowered below to the rows' longest context
     }
-    if (T > a.max_query_len && blockIdx.x == 0 && kvh == 0 && threadIdx.x == 0)
-        report(a.status, PA_DEV_BAD_QUERY_LEN);
-    const int t0 = mt * kQT * tok_per_tile;       // first token of tile A
-    if (t0 >= T) return;
     const bool has_b = t0 + tok_per_tile < T;
-    const int C = L - T;
-    const int last_tok = min(T, t0 + kQT * tok_per_tile) - 1;
-    const int kv_hi = C + last_tok + 1;
-    const int kv_lo = a.window > 0 ? max(0, C + t0 + 1 - a.window) : 0;
-    const int blk_lo = kv_lo / kBlockSize;
-    const int blk_hi = (kv_hi + kBlockSize - 1) / kBlockSize;
     const int n_tiles = (blk_hi - blk_lo + 7) / 8;
 
     extern __shared__ __align__(1024) uint8_t smem_raw[];
@@ -203,6 +239,31 @@ __global__ void __launch_bounds__(kThreads, 1)
         tma_prefetch_desc(&qmap);
         tma_prefetch_desc(&kmap);
         tma_prefetch_desc(&vmap);
+    }
+    if constexpr (kPrefix) {
+        // positions past every row's context are never attended: their V rows
+        // are zeroed like a context's tail (kv_hi = longest context, clipped)
+        int *s_maxl = reinterpret_cast<int *>(base + kOffBar + kNumBars * 8 + 8);
+        if (threadIdx.x == 0) *s_maxl = 0;
+        __syncthreads();
+        const int nseq = min(T - t0, kQT * tok_per_tile);
+        for (int i = threadIdx.x; i < nseq; i += kThreads) {
+            int L = a.context_lens[t0 + i];
+            L = L < 0 ? 0 : (L > lmax ? lmax : L);
+            atomicMax(s_maxl, L);
+        }
+        // every sequence of these rows must list the chunk's blocks (checked
+        // by the CTAs of KV head 0)
+        if (kvh == 0) {
+            const int nblk = blk_hi - blk_lo;
+            for (int i = threadIdx.x; i < nseq * nblk; i += kThreads) {
+                const int sq = t0 + i / nblk, jb = blk_lo + i % nblk;
+                if (a.block_tables[(size_t)sq * a.max_blocks + jb] != a.block_tables[jb])
+                    report(a.status, PA_DEV_PREFIX_MISMATCH);
+            }
+        }
+        __syncthreads();
+        kv_hi = max(kv_lo, min(kv_hi, *s_maxl));
     }
     if (warp == 1) tmem_alloc(tslot, kTmemCols);
     tc_fence_before();
@@ -339,13 +400,27 @@ __global__ void __launch_bounds__(kThreads, 1)
             const int quarter = warp & 3;
             const int part = gw >> 2;                     // columns [kCols * part, + kCols)
             const int r = quarter * 32 + lane;            // tile row = TMEM lane
-            const int tx0 = t0 + x * tok_per_tile;        // first token of this tile
+            const int tx0 = t0 + x * tok_per_tile;        // first token (sequence) of this tile
             const int ntok = max(0, min(tok_per_tile, T - tx0));
             const int tr = r / g;
             const bool real = tr < ntok;
-            const int qpos = C + tx0 + min(tr, max(ntok, 1) - 1);
-            const int qpos_lo = C + tx0, qpos_hi = C + tx0 + max(ntok, 1) - 1;
-            const int wlo = a.window > 0 ? qpos + 1 - a.window : INT_MIN;
+            // this row attends to positions [wlo, qpos]; a 32-column chunk
+            // needs no mask when it lies inside [qpos_lo_win, qpos_lo] for
+            // every row of the tile
+            int qpos, qpos_lo, qpos_hi, wlo;
+            if constexpr (!kPrefix) {
+                qpos = C + tx0 + min(tr, max(ntok, 1) - 1);
+                qpos_lo = C + tx0;
+                qpos_hi = C + tx0 + max(ntok, 1) - 1;
+                wlo = a.window > 0 ? qpos + 1 - a.window : INT_MIN;
+            } else {
+                int L = real ? a.context_lens[tx0 + tr] : 0;
+                L = L < 0 ? 0 : (L > lmax ? lmax : L);
+                qpos = min(L, blk_hi * kBlockSize) - 1;   // last attended position
+                qpos_lo = -1;                              // always mask (short kernel)
+                qpos_hi = 0;
+                wlo = INT_MIN;
+            }
             const uint32_t lane_off = ((uint32_t)(quarter * 32) << 16) + part * kCols;
             const uint32_t s_base = tmem + col_s(x) + lane_off;
             const uint32_t o_base = tmem + col_o(x) + lane_off;
@@ -369,7 +444,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                         tmem_ld32(s_base + c, v);
                         tmem_wait_ld();
                         const int kc = k0 + c;
-                        if ((kc + 31 > qpos_lo) || (a.window > 0 && kc < qpos_hi + 1 - a.window)) {
+                        if ((kc + 31 > qpos_lo) || (!kPrefix && a.window > 0 && kc < qpos_hi + 1 - a.window)) {
 #pragma unroll
                             for (int i = 0; i < 32; ++i)
                                 if (!(kc + i <= qpos && kc + i >= wlo)) v[i] = __float_as_uint(-INFINITY);
@@ -429,7 +504,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     tmem_wait_ld();
                     const int kc = k0 + c;
                     const bool masked =
-                        (kc + 31 > qpos_lo) || (a.window > 0 && kc < qpos_hi + 1 - a.window);
+                        (kc + 31 > qpos_lo) || (!kPrefix && a.window > 0 && kc < qpos_hi + 1 - a.window);
                     uint32_t hi[16], lo[16];
 #pragma unroll
                     for (int i = 0; i < 32; i += 2) {
@@ -482,7 +557,29 @@ __global__ void __launch_bounds__(kThreads, 1)
             float l_row = l;
 #pragma unroll
             for (int o = 1; o < kSplit; ++o) l_row += red[(sx * kSplit + ((part + o) % kSplit)) * kRows + r];
-            if (__all_sync(0xffffffffu, ok) && warp_wait(&bars[kDrain], 0, fail, a.status)) {
+            if (kPrefix && __all_sync(0xffffffffu, ok) && warp_wait(&bars[kDrain], 0, fail, a.status)) {
+                // split-K partial of this chunk: (max, sum) and the unnormalised
+                // output, in the partial row of (sequence, head, chunk)
+                tc_fence_after();
+                const size_t prow = ((size_t)(tx0 + tr) * a.num_q_heads + kvh * g + (r % g)) * a.max_parts +
+                                    blockIdx.z;
+#pragma unroll 1
+                for (int c = 0; c < kCols; c += 32) {
+                    uint32_t o[32];
+                    tmem_ld32(o_base + c, o);
+                    tmem_wait_ld();
+                    if (real) {
+                        float4 *dst = reinterpret_cast<float4 *>(a.part_o + prow * kD + part * kCols + c);
+#pragma unroll
+                        for (int q = 0; q < 8; ++q)
+                            dst[q] = make_float4(__uint_as_float(o[4 * q]), __uint_as_float(o[4 * q + 1]),
+                                                 __uint_as_float(o[4 * q + 2]), __uint_as_float(o[4 * q + 3]));
+                    }
+                }
+                if (real && part == 0)
+                    a.part_ml[prow] = make_float2(l_row > 0.f ? m_used : -INFINITY, l_row);
+            } else if (!kPrefix && __all_sync(0xffffffffu, ok) &&
+                       warp_wait(&bars[kDrain], 0, fail, a.status)) {
                 tc_fence_after();
                 const float inv = l_row > 0.f ? 1.f / l_row : 0.f;
                 __nv_bfloat16 *orow = static_cast<__nv_bfloat16 *>(a.out) +
@@ -530,7 +627,121 @@ PFN_cuTensorMapEncodeTiled_v12000 encoder() {
     return fn;
 }
 
+// Tensor maps of one call: the query as [rows][KV head][head of the group]
+// [head_dim] (a box of 128 / group rows x group heads x 64 elements is one
+// 128-row tile), and each pool as [num_blocks * num_kv_heads * 16 rows]
+// [head_dim] with 16-row boxes.
+pa_status encode_maps(const void *query, int query_rows, int num_q_heads, int num_kv_heads,
+                      const void *key_cache, const void *value_cache, int64_t pool_rows,
+                      CUtensorMap *qmap, CUtensorMap *kmap, CUtensorMap *vmap) {
+    auto enc = encoder();
+    if (enc == nullptr) return cuda_failure(cudaErrorInvalidValue, "cuTensorMapEncodeTiled lookup");
+    const int group = num_q_heads / num_kv_heads;
+    {
+        cuuint64_t dims[4] = {(cuuint64_t)kD, (cuuint64_t)group, (cuuint64_t)num_kv_heads,
+                              (cuuint64_t)query_rows};
+        cuuint64_t strides[3] = {(cuuint64_t)kD * 2, (cuuint64_t)group * kD * 2,
+                                 (cuuint64_t)num_q_heads * kD * 2};
+        cuuint32_t box[4] = {64, (cuuint32_t)group, 1, (cuuint32_t)(kRows / group)};
+        cuuint32_t estr[4] = {1, 1, 1, 1};
+        if (enc(qmap, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void *>(query), dims, strides,
+                box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+            return cuda_failure(cudaErrorInvalidValue, "cuTensorMapEncodeTiled(query)");
+    }
+    for (int which = 0; which < 2; ++which) {
+        cuuint64_t dims[2] = {(cuuint64_t)kD, (cuuint64_t)pool_rows};
+        cuuint64_t strides[1] = {(cuuint64_t)kD * 2};
+        cuuint32_t box[2] = {64, (cuuint32_t)kBlockSize};
+        cuuint32_t estr[2] = {1, 1};
+        CUtensorMap *m = which == 0 ? kmap : vmap;
+        const void *pool = which == 0 ? key_cache : value_cache;
+        if (enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(pool), dims, strides,
+                box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+            return cuda_failure(cudaErrorInvalidValue, "cuTensorMapEncodeTiled(pool)");
+    }
+    return PA_OK;
+}
+
+template <bool kPrefix>
+pa_status launch_tc(const CUtensorMap &qmap, const CUtensorMap &kmap, const CUtensorMap &vmap,
+                    const PrefillArgs &a, dim3 grid, cudaStream_t stream) {
+    auto kernel = pa_attn_tc_kernel<kPrefix>;
+    cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         kSmemBytes);
+    if (e != cudaSuccess) return cuda_failure(e, "cudaFuncSetAttribute(tensor-core attention)");
+    e = launch_chained(kernel, grid, dim3(kThreads), (size_t)kSmemBytes, stream, qmap, kmap, vmap, a);
+    if (e != cudaSuccess) return cuda_failure(e, "pa_attn_tc_kernel launch");
+    count_launches(1);
+    return PA_OK;
+}
+
+bool group_ok(int group) {
+    return group == 1 || group == 2 || group == 4 || group == 8 || group == 16;
+}
+
 }  // namespace
+
+bool prefix_tc_supported(int head_dim, int num_q_heads, int num_kv_heads) {
+    return head_dim == kD && num_kv_heads > 0 && num_q_heads % num_kv_heads == 0 &&
+           group_ok(num_q_heads / num_kv_heads);
+}
+
+// Prefix chunk (in blocks, whole 8-block K/V tiles) that gives about
+// PA_PREFIX_TC_CTAS_PER_100_SM / 100 CTAs per SM over (256-row tiles x KV heads
+// x chunks).  The prefix runs beside the suffix decode, so it takes only part
+// of the GPU.
+#ifndef PA_PREFIX_TC_CTAS_PER_100_SM
+#define PA_PREFIX_TC_CTAS_PER_100_SM 50
+#endif
+int prefix_tc_chunk_blocks(int num_seqs, int num_q_heads, int num_kv_heads, int prefix_blocks,
+                           int sm_count) {
+    const int group = num_q_heads / num_kv_heads;
+    const int64_t tiles = ((int64_t)num_seqs * group + kQT * kRows - 1) / (kQT * kRows);
+    const int64_t per_chunk = std::max<int64_t>(1, tiles * num_kv_heads);
+    const int64_t target = std::max<int64_t>(1, (int64_t)sm_count * PA_PREFIX_TC_CTAS_PER_100_SM / 100);
+    const int64_t want = std::max<int64_t>(1, (target + per_chunk - 1) / per_chunk);
+    int cb = (int)((prefix_blocks + want - 1) / want);
+    cb = ((cb + 7) / 8) * 8;
+    return std::max(8, std::min(cb, ((prefix_blocks + 7) / 8) * 8));
+}
+
+pa_status launch_prefix_tc(const void *query, const void *key_cache, const void *value_cache,
+                           const int32_t *block_tables, const int32_t *context_lens, int num_seqs,
+                           int num_q_heads, int num_kv_heads, int max_blocks, int num_blocks,
+                           float scale_log2, int prefix_blocks, int chunk_blocks, int chunks,
+                           float *part_o, float2 *part_ml, int max_parts, int32_t *status,
+                           cudaStream_t stream) {
+    const int group = num_q_heads / num_kv_heads;
+    const int64_t pool_rows = (int64_t)num_blocks * num_kv_heads * kBlockSize;
+    const int64_t tiles = ((int64_t)num_seqs * group + kQT * kRows - 1) / (kQT * kRows);
+    if (tiles > 0x7fffffff || num_kv_heads > 65535 || chunks > 65535) return PA_ERR_UNSUPPORTED;
+    CUtensorMap qmap, kmap, vmap;
+    pa_status st = encode_maps(query, num_seqs, num_q_heads, num_kv_heads, key_cache, value_cache,
+                               pool_rows, &qmap, &kmap, &vmap);
+    if (st != PA_OK) return st;
+    PrefillArgs a = {};
+    a.block_tables = block_tables;
+    a.context_lens = context_lens;
+    a.status = status;
+    a.num_seqs = num_seqs;
+    a.num_q_heads = num_q_heads;
+    a.num_kv_heads = num_kv_heads;
+    a.group = group;
+    a.max_blocks = max_blocks;
+    a.num_blocks = num_blocks;
+    a.scale_log2 = scale_log2;
+    a.part_o = part_o;
+    a.part_ml = part_ml;
+    a.max_parts = max_parts;
+    a.prefix_blocks = prefix_blocks;
+    a.chunk_blocks = chunk_blocks;
+    return launch_tc<true>(qmap, kmap, vmap, a, dim3((unsigned)tiles, (unsigned)num_kv_heads,
+                                                      (unsigned)chunks),
+                           stream);
+}
+
 }  // namespace pa
 
 using namespace pa;
@@ -547,9 +758,8 @@ extern "C" pa_status pa_prefill(void *out, const void *query, const void *key_ca
         num_query_tokens < 0 || max_query_len < 0 || window < 0 || !(scale == scale))
         return PA_ERR_INVALID_ARG;
     if (dtype != PA_DTYPE_BF16) return PA_ERR_UNSUPPORTED;
+    if (!prefix_tc_supported(head_dim, num_q_heads, num_kv_heads)) return PA_ERR_UNSUPPORTED;
     const int group = num_q_heads / num_kv_heads;
-    if (head_dim != kD || (group != 1 && group != 2 && group != 4 && group != 8 && group != 16))
-        return PA_ERR_UNSUPPORTED;
     if (num_seqs == 0 || num_query_tokens == 0 || max_query_len == 0) return PA_OK;
     if (!out || !query || !key_cache || !value_cache || !block_tables || !context_lens ||
         !query_start)
@@ -560,43 +770,17 @@ extern "C" pa_status pa_prefill(void *out, const void *query, const void *key_ca
     if (rows >= ((int64_t)1 << 31)) return PA_ERR_UNSUPPORTED;
     const int64_t tiles = ((int64_t)max_query_len * group + kQT * kRows - 1) / (kQT * kRows);
     if (tiles > 0x7fffffff || num_kv_heads > 65535 || num_seqs > 65535) return PA_ERR_UNSUPPORTED;
-    auto enc = encoder();
-    if (enc == nullptr) return cuda_failure(cudaErrorInvalidValue, "cuTensorMapEncodeTiled lookup");
-
     CUtensorMap qmap, kmap, vmap;
-    {
-        // query as [tokens][kv head][head of the group][head_dim]: a box of
-        // (128 / group) tokens x group heads x 64 elements is one 128-row tile
-        cuuint64_t dims[4] = {(cuuint64_t)kD, (cuuint64_t)group, (cuuint64_t)num_kv_heads,
-                              (cuuint64_t)num_query_tokens};
-        cuuint64_t strides[3] = {(cuuint64_t)kD * 2, (cuuint64_t)group * kD * 2,
-                                 (cuuint64_t)num_q_heads * kD * 2};
-        cuuint32_t box[4] = {64, (cuuint32_t)group, 1, (cuuint32_t)(kRows / group)};
-        cuuint32_t estr[4] = {1, 1, 1, 1};
-        if (enc(&qmap, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void *>(query), dims, strides,
-                box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-                CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
-            return cuda_failure(cudaErrorInvalidValue, "cuTensorMapEncodeTiled(query)");
-    }
-    for (int which = 0; which < 2; ++which) {
-        // pool as [num_blocks * num_kv_heads * 16 rows][head_dim], 16-row boxes
-        cuuint64_t dims[2] = {(cuuint64_t)kD, (cuuint64_t)rows};
-        cuuint64_t strides[1] = {(cuuint64_t)kD * 2};
-        cuuint32_t box[2] = {64, (cuuint32_t)kBlockSize};
-        cuuint32_t estr[2] = {1, 1};
-        CUtensorMap *m = which == 0 ? &kmap : &vmap;
-        const void *pool = which == 0 ? key_cache : value_cache;
-        if (enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(pool), dims, strides,
-                box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-                CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
-            return cuda_failure(cudaErrorInvalidValue, "cuTensorMapEncodeTiled(pool)");
-    }
-    PrefillArgs a;
+    pa_status st = encode_maps(query, num_query_tokens, num_q_heads, num_kv_heads, key_cache,
+                               value_cache, rows, &qmap, &kmap, &vmap);
+    if (st != PA_OK) return st;
+    PrefillArgs a = {};
     a.out = out;
     a.block_tables = block_tables;
     a.context_lens = context_lens;
     a.query_start = query_start;
     a.status = device_status;
+    a.num_seqs = num_seqs;
     a.num_q_heads = num_q_heads;
     a.num_kv_heads = num_kv_heads;
     a.group = group;
@@ -605,13 +789,7 @@ extern "C" pa_status pa_prefill(void *out, const void *query, const void *key_ca
     a.max_query_len = max_query_len;
     a.window = window;
     a.scale_log2 = scale * 1.4426950408889634f;
-    cudaError_t e = cudaFuncSetAttribute(pa_prefill_kernel,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
-    if (e != cudaSuccess) return cuda_failure(e, "cudaFuncSetAttribute(prefill)");
-    dim3 grid((unsigned)tiles, (unsigned)num_kv_heads, (unsigned)num_seqs);
-    e = launch_chained(pa_prefill_kernel, grid, dim3(kThreads), (size_t)kSmemBytes,
-                       static_cast<cudaStream_t>(stream), qmap, kmap, vmap, a);
-    if (e != cudaSuccess) return cuda_failure(e, "pa_prefill_kernel launch");
-    count_launches(1);
-    return PA_OK;
+    return launch_tc<false>(qmap, kmap, vmap, a,
+                            dim3((unsigned)tiles, (unsigned)num_kv_heads, (unsigned)num_seqs),
+                            static_cast<cudaStream_t>(stream));
 }
