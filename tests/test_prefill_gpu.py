@@ -121,6 +121,15 @@ def test_chunked_equals_whole_prompt(pkv):
     H.assert_close(H.as_f64(whole), ref, "bf16", "one chunk")
 
 
+def test_sequences_without_new_tokens_are_skipped(pkv):
+    """A batch may hold sequences whose chunk is empty this step."""
+    specs = [(40, 0), (0, 33), (100, 0), (20, 70), (5, 0)]
+    wl, hv, q, qs, tables, lens = _case(8, 2, specs, seed=51)
+    got, st = _run(pkv, wl, hv, q, qs, tables, lens)
+    assert st == 0
+    H.assert_close(H.as_f64(got), _oracle(wl, hv, q, qs, tables, lens), "bf16", "empty chunks")
+
+
 def test_too_long_chunk_is_flagged(pkv):
     wl, hv, q, qs, tables, lens = _case(4, 4, [(0, 300)], seed=41)
     _, st = _run(pkv, wl, hv, q, qs, tables, lens, max_query_len=100)

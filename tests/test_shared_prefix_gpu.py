@@ -53,7 +53,7 @@ def _run(pkv, wl, hv, n_prefix, lens=None, status=None, partition_size=0):
 
 
 @pytest.mark.parametrize("hq,hkv,D", [(8, 8, 128), (32, 8, 128), (16, 2, 128), (12, 4, 64),
-                                      (32, 2, 128), (4, 4, 64)])
+                                      (32, 2, 128), (4, 4, 64), (16, 8, 128)])
 @pytest.mark.parametrize("prefix_blocks", [1, 7, 40])
 def test_shared_prefix_matches_oracle(pkv, hq, hkv, D, prefix_blocks):
     suffix = [0, 1, 15, 16, 17, 200, 640, 3]
@@ -64,6 +64,19 @@ def test_shared_prefix_matches_oracle(pkv, hq, hkv, D, prefix_blocks):
                               wl.context_lens, wl.scale, threads=4)
     H.assert_close(H.as_f64(out), ref, "bf16", f"shared prefix {hq}/{hkv}/{D} n={prefix_blocks}")
     H.assert_close(H.as_f64(out), H.as_f64(ref_gpu), "bf16", "shared prefix vs pa_decode")
+
+
+def test_many_sequences_span_several_row_tiles(pkv):
+    """70 sequences x 4 heads of a group = 280 rows per KV head: two 256-row
+    tiles on the tensor-core prefix path, the second one partly empty."""
+    rng = np.random.default_rng(12)
+    suffix = rng.integers(0, 300, 70).tolist()
+    wl = _shared_workload(70, 8, 2, 128, 19, suffix, seed=13)
+    hv = W.host_values(wl)
+    out, ref_gpu = _run(pkv, wl, hv, 19)
+    ref = oracle.paged_decode(hv.query, hv.key_cache, hv.value_cache, wl.block_tables,
+                              wl.context_lens, wl.scale, threads=8)
+    H.assert_close(H.as_f64(out), ref, "bf16", "70 sequences")
 
 
 def test_contexts_shorter_than_the_prefix_are_masked(pkv):
