@@ -1458,8 +1458,6 @@ PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
     return fn;
 }
 
-// 2-D view of a pool as [num_blocks * num_kv_heads * 16 rows][head_dim] bf16,
-// loaded as boxes of 16 rows x 64 elements with 128-byte swizzle.
 // 2-D view of a pool as [num_blocks * num_kv_heads * 16 rows][head_dim]
 // elements, loaded as boxes of 16 rows x 128 bytes with 128-byte swizzle.
 bool encode_pool_map(CUtensorMap *map, const void *pool, int64_t rows, int D, int elem_bytes) {

@@ -31,6 +31,12 @@
 // While one tile's softmax runs, the tensor cores work on the other tile.  The
 // MMAs of one thread execute in issue order: S_X(j+1), issued after PV_X(j),
 // cannot overwrite the P that PV_X(j) reads.
+// The same kernel, in prefix mode, computes the shared prefix of a decode
+// batch whose tables all start with the same blocks ("PagedAttention por
+// dentro", "Copy-on-write para sampling paralelo" and "Prefix caching
+// cross-session"): its rows are (sequence, query head) pairs across the batch,
+// its K/V the shared blocks, and it leaves split-K partials that the decode's
+// merge combines with the rest of each context.
 // Every wait is bounded (about a second); a wait that gives up sets
 // PA_DEV_TIMEOUT and the CTA drains its tensor-core work and returns.
 #include <cuda.h>
