@@ -19,6 +19,7 @@ import argparse
 import hashlib
 import json
 import os
+import re
 import statistics
 import sys
 import time
@@ -224,11 +225,19 @@ def pci_bus_id(dev):
         return None
 
 
+def _code_only(src: str) -> str:
+    """C/CUDA source without comments, blank lines and indentation, so that an
+    edit of comments alone keeps the hash (the compiled kernel is the same)."""
+    src = re.sub(r"/\*.*?\*/", " ", src, flags=re.S)
+    src = re.sub(r"//[^\n]*", "", src)
+    return "\n".join(line.strip() for line in src.splitlines() if line.strip())
+
+
 def kernel_source_hash() -> str:
     h = hashlib.sha256()
     for f in ("pa_decode.cu", "pa_device.cuh", "pa_internal.h"):
-        with open(os.path.join(ROOT, "paged_kv_cache_100_gb300", "csrc", f), "rb") as fh:
-            h.update(fh.read())
+        with open(os.path.join(ROOT, "paged_kv_cache_100_gb300", "csrc", f)) as fh:
+            h.update(_code_only(fh.read()).encode())
     return h.hexdigest()[:16]
 
 
