@@ -164,7 +164,8 @@ pa_status pa_decode(void *out, const void *query, const void *key_cache, const v
  *                     library's choice for max_blocks_per_seq - num_prefix_blocks)
  *  workspace          at least pa_decode_shared_prefix_workspace_bytes(...)
  * bf16 only; head_dim 64 or 128; group as in pa_decode.  Launches three kernels
- * (prefix, suffix, merge).
+ * on the caller's stream: the prefix kernel first (it takes part of the SMs),
+ * the suffix decode beside it, then the merge of both.
  */
 size_t pa_decode_shared_prefix_workspace_bytes(int num_seqs, int num_q_heads, int num_kv_heads,
                                                int head_dim, int max_blocks_per_seq,

@@ -78,6 +78,12 @@ struct DecodeArgs {
     int prefix_chunk_blocks;
     int prefix_chunks;
     int window;         // > 0: attend only to the last `window` positions
+    // 1: only CTA 0 waits for the kernel before it in the stream (the
+    // shared-prefix kernel), so that the others stream the suffix beside it.
+    // Safe because that kernel waited for everything before it and let this
+    // one launch only after all of its CTAs had done so; CTA 0's wait keeps
+    // this grid from completing before it.
+    int defer_wait;
 };
 
 // The (sequence, head, partition) a CTA works on, with its token range.
@@ -917,7 +923,7 @@ __global__ void __launch_bounds__(NW * 32)
 pa_decode_bf16_kernel(const __grid_constant__ CUtensorMap kmap,
                       const __grid_constant__ CUtensorMap vmap, const DecodeArgs a) {
     using Lay = TmaLayout<D, Consumer::kElemBytes, NW, STAGES>;
-    grid_dependency_wait();
+    if (!a.defer_wait || blockIdx.x == 0) grid_dependency_wait();
     grid_dependents_launch();
     Work w;
     if (!cta_work(a, a.num_kv_heads, w)) return;
@@ -1375,6 +1381,7 @@ __global__ void __launch_bounds__(NW * 32) pa_decode_f32_kernel(const float *__r
 // partials' (max, sum) pairs are read by the lanes in parallel, and the
 // partial rows are loaded eight at a time so that their L2 latencies overlap.
 constexpr int kReduceRows = 4;
+constexpr int kReduceSpec = 8;   // shared-prefix merge: partial rows read in the first round
 
 template <typename OutT>
 __global__ void __launch_bounds__(32 * kReduceRows) pa_reduce_kernel(const DecodeArgs a, int D) {
@@ -1384,6 +1391,61 @@ __global__ void __launch_bounds__(32 * kReduceRows) pa_reduce_kernel(const Decod
     const int row = blockIdx.x * kReduceRows + (threadIdx.x >> 5);
     if (row >= a.num_seqs * a.num_q_heads) return;
     const int b = row / a.num_q_heads;
+    const int q4 = D >> 2;                         // float4 columns per row
+    if (a.always_partial && a.part_base < kReduceSpec && q4 <= 32) {
+        // Shared-prefix merge: every row has the prefix chunks' partials and at
+        // least one suffix partial, so those kSpec = part_base + 1 rows are read
+        // at once with the context length (one round of L2 latency); only a
+        // context with several suffix partitions reads more.
+        const int kSpec = a.part_base + 1;
+        const size_t row0 = (size_t)row * a.max_parts;
+        const float2 *ml = a.part_ml + row0;
+        const float4 *po = reinterpret_cast<const float4 *>(a.part_o + row0 * D);
+        int L = a.context_lens[b];
+        float2 m_l[kReduceSpec];
+        float4 v[kReduceSpec];
+#pragma unroll
+        for (int i = 0; i < kReduceSpec; ++i) {
+            if (i < kSpec) {
+                m_l[i] = ml[i];
+                v[i] = lane < q4 ? po[(size_t)i * q4 + lane] : make_float4(0.f, 0.f, 0.f, 0.f);
+            }
+        }
+        const int lmax = a.max_blocks * kBlockSize;
+        L = L < 0 ? 0 : (L > lmax ? lmax : L);
+        L = max(L - a.token_offset, 0);
+        const int range = (L + kBlockSize - 1) / kBlockSize;
+        const int nparts = a.part_base + (range <= 0 ? 1 : (range + a.part_blocks - 1) / a.part_blocks);
+        float M = -INFINITY;
+#pragma unroll
+        for (int i = 0; i < kReduceSpec; ++i)
+            if (i < kSpec) M = fmaxf(M, m_l[i].x);
+        for (int p = kSpec; p < nparts; ++p) M = fmaxf(M, ml[p].x);
+        float Lsum = 0.f;
+        float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+        auto add = [&](float2 mlp, float4 o) {
+            const float w = mlp.x == -INFINITY ? 0.f : exp2f(mlp.x - M);
+            Lsum = fmaf(w, mlp.y, Lsum);
+            acc.x = fmaf(w, o.x, acc.x);
+            acc.y = fmaf(w, o.y, acc.y);
+            acc.z = fmaf(w, o.z, acc.z);
+            acc.w = fmaf(w, o.w, acc.w);
+        };
+#pragma unroll
+        for (int i = 0; i < kReduceSpec; ++i)
+            if (i < kSpec) add(m_l[i], v[i]);
+        for (int p = kSpec; p < nparts; ++p)
+            add(ml[p], lane < q4 ? po[(size_t)p * q4 + lane] : make_float4(0.f, 0.f, 0.f, 0.f));
+        if (lane < q4) {
+            const float inv = Lsum > 0.f ? 1.f / Lsum : 0.f;
+            OutT *out = static_cast<OutT *>(a.out) + (size_t)row * D + 4 * lane;
+            store_out<OutT>(out + 0, acc.x * inv);
+            store_out<OutT>(out + 1, acc.y * inv);
+            store_out<OutT>(out + 2, acc.z * inv);
+            store_out<OutT>(out + 3, acc.w * inv);
+        }
+        return;
+    }
     int L = a.context_lens[b];
     const int lmax = a.max_blocks * kBlockSize;
     L = L < 0 ? 0 : (L > lmax ? lmax : L);
@@ -1407,7 +1469,6 @@ __global__ void __launch_bounds__(32 * kReduceRows) pa_reduce_kernel(const Decod
 #pragma unroll
     for (int k = 16; k >= 1; k >>= 1) Lsum += __shfl_xor_sync(kFull, Lsum, k);
     const float inv = Lsum > 0.f ? 1.f / Lsum : 0.f;
-    const int q4 = D >> 2;                         // float4 columns per row
     const float4 *po = reinterpret_cast<const float4 *>(a.part_o + row0 * D);
     OutT *out = static_cast<OutT *>(a.out) + (size_t)row * D;
     for (int q = lane; q < q4; q += 32) {
@@ -1789,6 +1850,7 @@ pa_status decode_common(void *out, const void *query, const void *key_cache,
     a.token_offset = a.part_base = a.always_partial = 0;
     a.prefix_blocks = a.prefix_chunk_blocks = a.prefix_chunks = 0;
     a.window = window;
+    a.defer_wait = 0;
     cudaStream_t st = static_cast<cudaStream_t>(stream);
 
     pa_status s;
@@ -1876,36 +1938,6 @@ namespace pa {
 namespace {
 
 constexpr int kPrefixStages = 4;
-
-// A library-owned side stream per device, with a fork and a join event, so
-// that the prefix kernel (tensor-core bound) runs alongside the suffix decode
-// (HBM bound).  The host sequence record / wait / launch / record / wait is
-// serialised by a mutex so concurrent callers cannot interleave the events.
-struct SideStream {
-    cudaStream_t stream = nullptr;
-    cudaEvent_t fork = nullptr, join = nullptr;
-};
-std::mutex g_side_mutex;
-SideStream g_side[64];
-
-pa_status side_stream_locked(SideStream **out) {
-    int dev = 0;
-    cudaError_t e = cudaGetDevice(&dev);
-    if (e != cudaSuccess) return cuda_failure(e, "cudaGetDevice");
-    if (dev < 0 || dev >= 64) return PA_ERR_UNSUPPORTED;
-    SideStream &ss = g_side[dev];
-    if (ss.stream == nullptr) {
-        e = cudaStreamCreateWithFlags(&ss.stream, cudaStreamNonBlocking);
-        if (e == cudaSuccess) e = cudaEventCreateWithFlags(&ss.fork, cudaEventDisableTiming);
-        if (e == cudaSuccess) e = cudaEventCreateWithFlags(&ss.join, cudaEventDisableTiming);
-        if (e != cudaSuccess) {
-            ss = SideStream();
-            return cuda_failure(e, "side stream set-up");
-        }
-    }
-    *out = &ss;
-    return PA_OK;
-}
 
 // Chunks of the shared prefix: about three CTAs per SM (each CTA works through
 // its chunk block after block, so short chunks finish sooner), at least 4
@@ -2015,6 +2047,7 @@ extern "C" pa_status pa_decode_shared_prefix(
         (int64_t)num_kv_heads * row_chunks * p.prefix_chunks >= ((int64_t)1 << 31))
         return PA_ERR_UNSUPPORTED;
 
+    const bool tc_prefix = prefix_tc_supported(head_dim, num_q_heads, num_kv_heads);
     DecodeArgs a;
     a.out = out;
     a.query = query;
@@ -2043,27 +2076,21 @@ extern "C" pa_status pa_decode_shared_prefix(
     a.prefix_chunk_blocks = p.prefix_chunk_blocks;
     a.prefix_chunks = p.prefix_chunks;
     a.window = 0;
+    a.defer_wait = 1;
     cudaStream_t st = static_cast<cudaStream_t>(stream);
-    std::lock_guard<std::mutex> lock(g_side_mutex);
-    SideStream *side = nullptr;
-    pa_status ss = side_stream_locked(&side);
-    if (ss != PA_OK) return ss;
-    cudaError_t fe = cudaEventRecord(side->fork, st);
-    if (fe == cudaSuccess) fe = cudaStreamWaitEvent(side->stream, side->fork, 0);
-    if (fe != cudaSuccess) return cuda_failure(fe, "side stream fork");
 
-    // 1. the shared prefix, once per KV head for all sequences, on the side
-    //    stream: on the tensor cores (256 rows per K/V tile) where the shape
-    //    allows, else 64 query rows at a time on mma.sync tiles
-    if (prefix_tc_supported(head_dim, num_q_heads, num_kv_heads)) {
+    // 1. the shared prefix, once per KV head for all sequences: on the tensor
+    //    cores (256 rows per K/V tile) where the shape allows, else 64 query
+    //    rows at a time on mma.sync tiles.  It takes part of the SMs (one CTA
+    //    each) and lets the suffix kernel launch as soon as all of its CTAs
+    //    have started.
+    if (tc_prefix) {
         pa_status ps = launch_prefix_tc(query, key_cache, value_cache, block_tables, context_lens,
                                         num_seqs, num_q_heads, num_kv_heads, max_blocks_per_seq,
                                         num_blocks, a.scale_log2, num_prefix_blocks,
                                         p.prefix_chunk_blocks, p.prefix_chunks, a.part_o,
-                                        a.part_ml, p.max_parts, device_status, side->stream);
-        cudaError_t e = cudaEventRecord(side->join, side->stream);
+                                        a.part_ml, p.max_parts, device_status, st);
         if (ps != PA_OK) return ps;
-        if (e != cudaSuccess) return cuda_failure(e, "side stream join record");
     } else {
         CUtensorMap kmap, vmap;
         if (!encode_pool_map(&kmap, key_cache, rows, head_dim, 2) ||
@@ -2078,26 +2105,23 @@ extern "C" pa_status pa_decode_shared_prefix(
             auto kernel = pa_prefix_kernel<128, kPrefixStages>;
             e = allow_smem(kernel, smem);
             if (e == cudaSuccess)
-                e = launch_chained(kernel, dim3(grid), dim3((kPrefixWarps + 1) * 32), smem,
-                                   side->stream, kmap, vmap, a);
+                e = launch_chained(kernel, dim3(grid), dim3((kPrefixWarps + 1) * 32), smem, st,
+                                   kmap, vmap, a);
         } else {
             auto kernel = pa_prefix_kernel<64, kPrefixStages>;
             e = allow_smem(kernel, smem);
             if (e == cudaSuccess)
-                e = launch_chained(kernel, dim3(grid), dim3((kPrefixWarps + 1) * 32), smem,
-                                   side->stream, kmap, vmap, a);
+                e = launch_chained(kernel, dim3(grid), dim3((kPrefixWarps + 1) * 32), smem, st,
+                                   kmap, vmap, a);
         }
-        if (e == cudaSuccess) e = cudaEventRecord(side->join, side->stream);
         if (e != cudaSuccess) return cuda_failure(e, "pa_prefix_kernel launch");
         count_launches(1);
     }
-    // 2. every context past the prefix, as partials, on the caller's stream
+    // 2. every context past the prefix, as partials, beside the prefix kernel
+    //    (defer_wait: only its CTA 0 waits for the prefix kernel to finish)
     pa_status s = head_dim == 64 ? dispatch_bf16<64>(group, a, key_cache, value_cache, rows, st)
                                  : dispatch_bf16<128>(group, a, key_cache, value_cache, rows, st);
-    // join before anything else can fail, so the caller's stream always waits
-    cudaError_t je = cudaStreamWaitEvent(st, side->join, 0);
     if (s != PA_OK) return s;
-    if (je != cudaSuccess) return cuda_failure(je, "side stream join");
     // 3. merge prefix and suffix partials
     return launch_reduce<__nv_bfloat16>(a, head_dim, st);
 }

@@ -25,7 +25,9 @@ inline bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 
 // while the previous kernel in the stream is still running.  Every kernel of
 // this library starts with griddepcontrol.wait (nothing before it reads global
 // memory), so ordering with earlier work is kept; what overlaps is only the
-// launch and CTA set-up of one kernel with the tail of the one before.
+// launch and CTA set-up of one kernel with the tail of the one before.  The
+// one exception is the suffix decode of pa_decode_shared_prefix, which follows
+// the prefix kernel and runs beside it (DecodeArgs::defer_wait).
 template <typename... KArgs, typename... Args>
 cudaError_t launch_chained(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem,
                            cudaStream_t stream, Args &&...args) {

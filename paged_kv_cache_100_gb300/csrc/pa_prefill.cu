@@ -699,7 +699,7 @@ bool prefix_tc_supported(int head_dim, int num_q_heads, int num_kv_heads) {
 // x chunks).  The prefix runs beside the suffix decode, so it takes only part
 // of the GPU.
 #ifndef PA_PREFIX_TC_CTAS_PER_100_SM
-#define PA_PREFIX_TC_CTAS_PER_100_SM 50
+#define PA_PREFIX_TC_CTAS_PER_100_SM 25
 #endif
 int prefix_tc_chunk_blocks(int num_seqs, int num_q_heads, int num_kv_heads, int prefix_blocks,
                            int sm_count) {

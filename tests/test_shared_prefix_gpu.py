@@ -131,3 +131,39 @@ def test_shared_prefix_workload_full_size(pkv, cow):
     ref = oracle.paged_decode(qh, kch, vch, tabs, slens, wl.scale, sel=pairs, threads=8)
     got = np.stack([H.as_f64(out[seqs[i], h]) for i, h in pairs])
     H.assert_close(got, ref, "bf16", "shared-prefix workload")
+
+
+@pytest.mark.parametrize("fill", ["zeros", "ones", "random"])
+def test_workspace_reused_across_calls(pkv, fill):
+    """The CTA that completes a row set merges it, counted on per-(sequence, KV
+    head) words in the workspace.  Whatever the workspace held before (zeros,
+    all-ones bytes, random bytes) and however often it is reused, every call
+    must give the same result as pa_decode."""
+    import torch
+    rng = np.random.default_rng(31)
+    suffix = rng.integers(0, 400, 40).tolist()
+    wl = _shared_workload(40, 16, 4, 128, 21, suffix, seed=32)
+    hv = W.host_values(wl, poison_unused=False)
+    q = H.host_to_device(hv.query, torch.bfloat16)
+    kc = H.host_to_device(hv.key_cache, torch.bfloat16)
+    vc = H.host_to_device(hv.value_cache, torch.bfloat16)
+    bt = torch.from_numpy(wl.block_tables).cuda()
+    cl = torch.from_numpy(wl.context_lens).cuda()
+    need = pkv.lib().pa_decode_shared_prefix_workspace_bytes(40, 16, 4, 128, wl.block_tables.shape[1],
+                                                             21, 64)
+    if fill == "zeros":
+        ws = torch.zeros(need, dtype=torch.uint8, device="cuda")
+    elif fill == "ones":
+        ws = torch.full((need,), 255, dtype=torch.uint8, device="cuda")
+    else:
+        g = torch.Generator(device="cuda")
+        g.manual_seed(5)
+        ws = torch.randint(0, 256, (need,), dtype=torch.uint8, device="cuda", generator=g)
+    plain = pkv.decode(q, kc, vc, bt, cl, wl.scale)
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    for call in range(3):
+        out = pkv.decode_shared_prefix(q, kc, vc, bt, cl, 21, wl.scale, workspace=ws, status=status,
+                                       partition_size=64)
+        torch.cuda.synchronize()
+        assert int(status.item()) == 0
+        H.assert_close(H.as_f64(out), H.as_f64(plain), "bf16", f"call {call} ({fill})")
