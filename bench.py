@@ -280,6 +280,10 @@ class StepOps:
             self.pkv.decode_sliding_window(q, self.kc, self.vc, bt, lens, self.window,
                                            self.wl.scale, k_scales=self.ks, v_scales=self.vs,
                                            out=out, partition_size=self.P, workspace=self.ws)
+        elif self.n_prefix and self.fp8:
+            self.pkv.decode_shared_prefix_fp8(q, self.kc, self.vc, self.ks, self.vs, bt, lens,
+                                              self.n_prefix, self.wl.scale, out=out,
+                                              partition_size=self.P, workspace=self.ws)
         elif self.n_prefix:
             self.pkv.decode_shared_prefix(q, self.kc, self.vc, bt, lens, self.n_prefix,
                                           self.wl.scale, out=out, partition_size=self.P,
@@ -332,15 +336,17 @@ def run_gpu(args):
         ws = torch.empty(max(pkv.lib().pa_decode_sliding_window_workspace_bytes(
             wl.num_seqs, wl.num_q_heads, wl.num_kv_heads, wl.head_dim, wl.max_blocks, 16, window,
             P, 2 if fp8 else (1 if wl.dtype == "bf16" else 0)), 16), dtype=torch.uint8, device=dev)
-    elif args.decode != "plain" and not fp8:
+    elif args.decode != "plain":
         n_prefix = pkv.shared_prefix_blocks(wl.block_tables)
         if args.decode == "auto" and n_prefix < 4:
             n_prefix = 0
     if n_prefix:
         P = args.partition_size or wl.partition_size
-        ws = torch.empty(max(pkv.lib().pa_decode_shared_prefix_workspace_bytes(
-            wl.num_seqs, wl.num_q_heads, wl.num_kv_heads, wl.head_dim, wl.max_blocks, n_prefix,
-            P), 16), dtype=torch.uint8, device=dev)
+        ws_bytes = (pkv.lib().pa_decode_shared_prefix_fp8_workspace_bytes if fp8 else
+                    pkv.lib().pa_decode_shared_prefix_workspace_bytes)
+        ws = torch.empty(max(ws_bytes(wl.num_seqs, wl.num_q_heads, wl.num_kv_heads, wl.head_dim,
+                                      wl.max_blocks, n_prefix, P), 16),
+                         dtype=torch.uint8, device=dev)
     ops = StepOps(pkv, wl, kc, vc, ks, vs, P, ws, n_prefix, window)
 
     def step(ev_pre=None, ev_post=None):
@@ -428,12 +434,15 @@ def run_gpu(args):
         "hbm_frac_of_nominal_7900": achieved / NOMINAL_HBM_GBS,
         "decode_method": (f"sliding window of the last {window} positions" if window else
                           (f"shared-prefix cascade ({n_prefix} shared blocks read once per KV "
-                           "head; prefix, suffix and merge kernels)") if n_prefix
+                           "head; " + ("widen, " if fp8 else "") + "prefix, suffix and merge "
+                           "kernels)") if n_prefix
                           else "paged decode"),
         "roofline": {
             "kernel": ("pa_decode_sliding_window call (partition kernel, plus the merge kernel "
                        "when a window spans several partitions)" if window else
-                       "pa_decode_shared_prefix call (prefix + suffix + merge kernels)" if n_prefix
+                       ("pa_decode_shared_prefix_fp8 call (widen + prefix + suffix + merge "
+                        "kernels)" if fp8 else
+                        "pa_decode_shared_prefix call (prefix + suffix + merge kernels)") if n_prefix
                        else "pa_decode call (partition kernel, plus the merge kernel when a "
                             "sequence spans several partitions)"),
             "bound": "hbm",
@@ -968,7 +977,7 @@ def main(argv=None):
                     help="> 0: sliding-window decode over the last WINDOW positions")
     ap.add_argument("--decode", default="auto", choices=["auto", "plain", "shared-prefix"],
                     help="auto: the shared-prefix cascade when every table shares >= 4 leading "
-                         "blocks (bf16 pools), else paged decode")
+                         "blocks, else paged decode")
     ap.add_argument("--kv-dtype", default="bf16", choices=["bf16", "fp8"],
                     help="element type of the K/V pools (fp8 = E4M3 with per-head scales)")
     ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])

@@ -180,6 +180,32 @@ pa_status pa_decode_shared_prefix(void *out, const void *query, const void *key_
                                   void *stream);
 
 /*
+ * The shared-prefix decode over FP8 (E4M3) pools with per-KV-head scales, as
+ * pa_decode_fp8 computes it: same arguments as pa_decode_fp8 plus
+ * num_prefix_blocks.  The prefix blocks' codes are first widened to bf16 code
+ * values (exact) in the workspace, then the tensor-core prefix kernel reads
+ * that copy once per KV head for all sequences, with the K scale folded into
+ * the softmax scale and the V scale into its partial outputs; the rest of every
+ * context runs through the FP8 decode kernel.  head_dim 128; groups 1, 2, 4, 8
+ * take this path, and with num_prefix_blocks 0 the call is pa_decode_fp8.
+ *  workspace  at least pa_decode_shared_prefix_fp8_workspace_bytes(...) bytes
+ * Launches four kernels on the caller's stream (widen, prefix, suffix, merge).
+ */
+size_t pa_decode_shared_prefix_fp8_workspace_bytes(int num_seqs, int num_q_heads,
+                                                   int num_kv_heads, int head_dim,
+                                                   int max_blocks_per_seq, int num_prefix_blocks,
+                                                   int partition_size);
+pa_status pa_decode_shared_prefix_fp8(void *out, const void *query, const void *key_cache,
+                                      const void *value_cache, const float *k_scales,
+                                      const float *v_scales, const int32_t *block_tables,
+                                      const int32_t *context_lens, int num_seqs, int num_q_heads,
+                                      int num_kv_heads, int head_dim, int block_size,
+                                      int max_blocks_per_seq, int num_blocks, float scale,
+                                      int num_prefix_blocks, int partition_size, void *workspace,
+                                      size_t workspace_bytes, int32_t *device_status,
+                                      void *stream);
+
+/*
  * Paged decode attention over FP8 pools.  The pages name quantising the KV
  * cache to FP8 as halving it ("KV cache: la memoria de trabajo que sostiene la
  * inferencia LLM", section "Trucos para que el cuaderno sea más fino"); the

@@ -25,7 +25,7 @@ from ._lib import PagedKVError, check, lib  # noqa: F401
 
 BLOCK_SIZE = 16
 
-__all__ = ["prefill", "swap_out", "swap_in", "decode", "decode_fp8", "decode_sliding_window", "decode_shared_prefix", "shared_prefix_blocks", "decode_workspace_bytes", "decode_partition_size",
+__all__ = ["prefill", "swap_out", "swap_in", "decode", "decode_fp8", "decode_sliding_window", "decode_shared_prefix", "decode_shared_prefix_fp8", "shared_prefix_blocks", "decode_workspace_bytes", "decode_partition_size",
            "cache_write", "cache_write_fp8", "block_copy", "launch_count", "BlockManager",
            "PagedKVError", "BLOCK_SIZE", "library_path"]
 
@@ -187,6 +187,47 @@ def decode_shared_prefix(query, key_cache, value_cache, block_tables, context_le
     check(rc, "pa_decode_shared_prefix")
     return out
 
+
+
+def decode_shared_prefix_fp8(query, key_cache, value_cache, k_scales, v_scales, block_tables,
+                             context_lens, num_prefix_blocks, scale=None, *, out=None,
+                             partition_size=0, workspace=None, status=None, stream=None):
+    """Shared-prefix decode over E4M3 pools (``pa_decode_shared_prefix_fp8``); returns
+    ``out`` (bf16)."""
+    torch = _torch()
+    B, Hq, D = query.shape
+    NB, Hkv, BS, D2 = key_cache.shape
+    if BS != BLOCK_SIZE or D2 != D or tuple(value_cache.shape) != tuple(key_cache.shape):
+        raise ValueError("pools must be [num_blocks][num_kv_heads][16][head_dim] like query")
+    if not (_is_fp8(key_cache) and _is_fp8(value_cache)) or query.dtype != torch.bfloat16:
+        raise TypeError("pa_decode_shared_prefix_fp8 takes E4M3 pools and a bfloat16 query")
+    if tuple(k_scales.shape) != (Hkv,) or tuple(v_scales.shape) != (Hkv,):
+        raise ValueError("k_scales / v_scales must be [num_kv_heads]")
+    if block_tables.dim() != 2 or block_tables.shape[0] != B or tuple(context_lens.shape) != (B,):
+        raise ValueError("block_tables must be [num_seqs][max_blocks], context_lens [num_seqs]")
+    if scale is None:
+        scale = 1.0 / math.sqrt(D)
+    if out is None:
+        out = torch.empty_like(query)
+    max_blocks = block_tables.shape[1]
+    need = lib().pa_decode_shared_prefix_fp8_workspace_bytes(B, Hq, Hkv, D, max_blocks,
+                                                             int(num_prefix_blocks),
+                                                             int(partition_size))
+    if need == ctypes.c_size_t(-1).value:
+        raise ValueError("invalid arguments for pa_decode_shared_prefix_fp8_workspace_bytes")
+    if workspace is None:
+        workspace = torch.empty(max(int(need), 16), dtype=torch.uint8, device=query.device)
+    rc = lib().pa_decode_shared_prefix_fp8(
+        _dev(out, "out"), _dev(query, "query"), _dev(key_cache, "key_cache"),
+        _dev(value_cache, "value_cache"), _dev(k_scales, "k_scales", torch.float32),
+        _dev(v_scales, "v_scales", torch.float32),
+        _dev(block_tables, "block_tables", torch.int32),
+        _dev(context_lens, "context_lens", torch.int32), B, Hq, Hkv, D, BLOCK_SIZE, max_blocks,
+        NB, float(scale), int(num_prefix_blocks), int(partition_size),
+        _dev(workspace, "workspace"), workspace.numel() * workspace.element_size(),
+        _status_ptr(status), _stream(stream, query.device))
+    check(rc, "pa_decode_shared_prefix_fp8")
+    return out
 
 def shared_prefix_blocks(block_tables) -> int:
     """Length (in blocks) of the physical prefix every row of host block tables shares."""

@@ -43,6 +43,9 @@ SIGNATURES = {
                                       f32, i32, i32, i32, vp, sz, vp, vp]),
     "pa_decode_fp8": (i32, [vp, vp, vp, vp, vp, vp, vp, vp, i32, i32, i32, i32, i32, i32, i32, f32,
                             i32, vp, sz, vp, vp]),
+    "pa_decode_shared_prefix_fp8_workspace_bytes": (sz, [i32, i32, i32, i32, i32, i32, i32]),
+    "pa_decode_shared_prefix_fp8": (i32, [vp, vp, vp, vp, vp, vp, vp, vp, i32, i32, i32, i32, i32,
+                                          i32, i32, f32, i32, i32, vp, sz, vp, vp]),
     "pa_decode_sliding_window_workspace_bytes": (sz, [i32, i32, i32, i32, i32, i32, i32, i32,
                                                       i32]),
     "pa_decode_sliding_window": (i32, [vp, vp, vp, vp, vp, vp, vp, vp, i32, i32, i32, i32, i32,

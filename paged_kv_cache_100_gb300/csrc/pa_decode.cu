@@ -1585,6 +1585,20 @@ cudaError_t allow_smem(K kernel, size_t bytes) {
 #ifndef PA_GQA8_STAGES
 #define PA_GQA8_STAGES 2
 #endif
+// FP8 GQA CTAs that stream at most PA_GQA8S_MAX_BLOCKS blocks (short contexts,
+// e.g. the part of a context past a shared prefix): 4 warps x 2 stages.  Each
+// warp then gets twice as many blocks, so its ring fills; on the 128-sequence
+// shared-prefix mix (suffixes of 1..64 blocks) the FP8 suffix took 50.0 us
+// against 55.2 us with 8 warps.
+#ifndef PA_GQA8S_WARPS
+#define PA_GQA8S_WARPS 4
+#endif
+#ifndef PA_GQA8S_STAGES
+#define PA_GQA8S_STAGES 2
+#endif
+#ifndef PA_GQA8S_MAX_BLOCKS
+#define PA_GQA8S_MAX_BLOCKS 128
+#endif
 constexpr int kNW = 4;   // fp32 kernel
 
 template <int D, class Consumer, int NW, int STAGES>
@@ -1636,18 +1650,32 @@ pa_status dispatch_bf16(int group, const DecodeArgs &a, const void *kc, const vo
     }
 }
 
+template <int G>
+pa_status launch_gqa_fp8(bool short_span, const DecodeArgs &a, const void *kc, const void *vc,
+                         int64_t rows, cudaStream_t stream) {
+    constexpr int D = 128;
+    if (short_span)
+        return launch_bf16<D, GqaTFp8Consumer<D, G>, PA_GQA8S_WARPS, PA_GQA8S_STAGES>(a, kc, vc, rows,
+                                                                                    stream);
+    return launch_bf16<D, GqaTFp8Consumer<D, G>, PA_GQA8_WARPS, PA_GQA8_STAGES>(a, kc, vc, rows,
+                                                                              stream);
+}
+
 pa_status dispatch_fp8(int group, const DecodeArgs &a, const void *kc, const void *vc,
                        int64_t rows, cudaStream_t stream) {
     constexpr int D = 128;
+    // blocks one CTA streams at most: short spans take the narrower GQA CTA
+    const int span = std::min(a.part_blocks, std::max(0, a.max_blocks - a.token_offset / kBlockSize));
+    const bool short_span = span <= PA_GQA8S_MAX_BLOCKS;
     switch (group) {
     case 1: return launch_bf16<D, MhaFp8Consumer<D>, PA_MHA8_WARPS, PA_MHA8_STAGES>(a, kc, vc, rows, stream);
-    case 2: return launch_bf16<D, GqaTFp8Consumer<D, 2>, PA_GQA8_WARPS, PA_GQA8_STAGES>(a, kc, vc, rows, stream);
-    case 3: return launch_bf16<D, GqaTFp8Consumer<D, 3>, PA_GQA8_WARPS, PA_GQA8_STAGES>(a, kc, vc, rows, stream);
-    case 4: return launch_bf16<D, GqaTFp8Consumer<D, 4>, PA_GQA8_WARPS, PA_GQA8_STAGES>(a, kc, vc, rows, stream);
-    case 5: return launch_bf16<D, GqaTFp8Consumer<D, 5>, PA_GQA8_WARPS, PA_GQA8_STAGES>(a, kc, vc, rows, stream);
-    case 6: return launch_bf16<D, GqaTFp8Consumer<D, 6>, PA_GQA8_WARPS, PA_GQA8_STAGES>(a, kc, vc, rows, stream);
-    case 7: return launch_bf16<D, GqaTFp8Consumer<D, 7>, PA_GQA8_WARPS, PA_GQA8_STAGES>(a, kc, vc, rows, stream);
-    case 8: return launch_bf16<D, GqaTFp8Consumer<D, 8>, PA_GQA8_WARPS, PA_GQA8_STAGES>(a, kc, vc, rows, stream);
+    case 2: return launch_gqa_fp8<2>(short_span, a, kc, vc, rows, stream);
+    case 3: return launch_gqa_fp8<3>(short_span, a, kc, vc, rows, stream);
+    case 4: return launch_gqa_fp8<4>(short_span, a, kc, vc, rows, stream);
+    case 5: return launch_gqa_fp8<5>(short_span, a, kc, vc, rows, stream);
+    case 6: return launch_gqa_fp8<6>(short_span, a, kc, vc, rows, stream);
+    case 7: return launch_gqa_fp8<7>(short_span, a, kc, vc, rows, stream);
+    case 8: return launch_gqa_fp8<8>(short_span, a, kc, vc, rows, stream);
     default: return PA_ERR_UNSUPPORTED;
     }
 }
@@ -1985,82 +2013,167 @@ bool plan_shared(int num_seqs, int num_q_heads, int num_kv_heads, int head_dim,
 }  // namespace
 }  // namespace pa
 
-extern "C" size_t pa_decode_shared_prefix_workspace_bytes(int num_seqs, int num_q_heads,
-                                                          int num_kv_heads, int head_dim,
-                                                          int max_blocks_per_seq,
-                                                          int num_prefix_blocks,
-                                                          int partition_size) {
+namespace pa {
+namespace {
+
+// Widens the E4M3 codes of the shared prefix (the first prefix_blocks entries
+// of the first block table, every KV head, K and V) to their bf16 code values
+// (exact: every E4M3 value is a bf16 value) in a staging pool
+// [prefix_blocks][Hkv][16][D], block j of the prefix at index j.  The
+// tensor-core prefix kernel reads it and applies the per-head scales.  CTA
+// (prefix block, KV head, K or V): 128 threads, 16 codes each per step.
+__global__ void __launch_bounds__(128)
+    pa_widen_prefix_kernel(const uint8_t *__restrict__ kc, const uint8_t *__restrict__ vc,
+                           const int32_t *__restrict__ table0, int num_kv_heads, int num_blocks,
+                           int D, __nv_bfloat16 *__restrict__ sk, __nv_bfloat16 *__restrict__ sv,
+                           int32_t *status) {
+    grid_dependency_wait();
+    grid_dependents_launch();
+    const int j = blockIdx.x / num_kv_heads;
+    const int kvh = blockIdx.x - j * num_kv_heads;
+    int phys = table0[j];
+    if ((unsigned)phys >= (unsigned)num_blocks) {
+        if (threadIdx.x == 0) report(status, PA_DEV_BAD_BLOCK_ID);
+        phys = 0;
+    }
+    const size_t tile = (size_t)kBlockSize * D;
+    const uint4 *src = reinterpret_cast<const uint4 *>((blockIdx.y ? vc : kc) +
+                                                       ((size_t)phys * num_kv_heads + kvh) * tile);
+    uint4 *dst = reinterpret_cast<uint4 *>((blockIdx.y ? sv : sk) +
+                                           ((size_t)j * num_kv_heads + kvh) * tile);
+    for (int i = threadIdx.x; i < (int)(tile / 16); i += 128) {
+        const uint4 c = src[i];
+        const uint32_t words[4] = {c.x, c.y, c.z, c.w};
+        uint32_t o[8];
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+            const uint32_t lo = e4m3x2_to_f16x2(words[k] & 0xffffu);
+            const uint32_t hi = e4m3x2_to_f16x2(words[k] >> 16);
+            o[2 * k] = pack_bf16x2(f16lo(lo), f16hi(lo));
+            o[2 * k + 1] = pack_bf16x2(f16lo(hi), f16hi(hi));
+        }
+        dst[2 * i] = make_uint4(o[0], o[1], o[2], o[3]);
+        dst[2 * i + 1] = make_uint4(o[4], o[5], o[6], o[7]);
+    }
+}
+
+bool partition_ok(int partition_size) {
+    return partition_size == 0 || (partition_size >= kBlockSize && partition_size <= kMaxPartition &&
+                                   partition_size % kBlockSize == 0);
+}
+
+// FP8 pools take the cascade where the tensor-core prefix kernel takes the
+// shape (head_dim 128, groups 1, 2, 4, 8); elsewhere the call is pa_decode_fp8.
+bool fp8_cascade(int head_dim, int num_q_heads, int num_kv_heads, int num_prefix_blocks) {
+    return num_prefix_blocks > 0 && prefix_tc_supported(head_dim, num_q_heads, num_kv_heads) &&
+           num_q_heads / num_kv_heads <= 8;
+}
+
+// Workspace of the shared-prefix decode: partial outputs and (max, sum) pairs,
+// then (FP8 pools) the staging copies of the prefix's K and V; every part
+// 256-byte aligned.
+struct SharedLayout {
+    size_t ml_offset, staged_k_offset, staged_v_offset, total;
+};
+SharedLayout shared_layout(int num_seqs, int num_q_heads, int num_kv_heads, int head_dim,
+                           int max_parts, int staged_blocks) {
+    auto up = [](size_t x) { return (x + 255) & ~size_t(255); };
+    const size_t rows = (size_t)num_seqs * num_q_heads * max_parts;
+    const size_t staged = (size_t)staged_blocks * num_kv_heads * kBlockSize * head_dim * 2;
+    SharedLayout l;
+    l.ml_offset = up(rows * head_dim * sizeof(float));
+    l.staged_k_offset = l.ml_offset + up(rows * sizeof(float2));
+    l.staged_v_offset = l.staged_k_offset + up(staged);
+    l.total = staged_blocks > 0 ? l.staged_v_offset + staged : l.ml_offset + rows * sizeof(float2);
+    return l;
+}
+
+size_t shared_workspace(int num_seqs, int num_q_heads, int num_kv_heads, int head_dim,
+                        int max_blocks_per_seq, int num_prefix_blocks, int partition_size,
+                        bool fp8) {
     if (num_seqs < 0 || num_q_heads <= 0 || num_kv_heads <= 0 || head_dim <= 0 ||
-        num_q_heads % num_kv_heads != 0)
+        num_q_heads % num_kv_heads != 0 || !partition_ok(partition_size))
         return (size_t)-1;
-    if (partition_size != 0 &&
-        (partition_size < kBlockSize || partition_size > kMaxPartition || partition_size % kBlockSize))
-        return (size_t)-1;
+    if (fp8 && !fp8_cascade(head_dim, num_q_heads, num_kv_heads, num_prefix_blocks))
+        return decode_workspace(num_seqs, num_q_heads, num_kv_heads, head_dim, max_blocks_per_seq,
+                                kBlockSize, 0, partition_size, PA_DTYPE_FP8_E4M3);
     SharedPlan p;
     if (!plan_shared(num_seqs, num_q_heads, num_kv_heads, head_dim, max_blocks_per_seq,
                      num_prefix_blocks, partition_size, &p))
         return (size_t)-1;
-    const size_t rows = (size_t)num_seqs * num_q_heads * p.max_parts;
-    return ((rows * head_dim * sizeof(float) + 255) & ~size_t(255)) + rows * sizeof(float2);
+    return shared_layout(num_seqs, num_q_heads, num_kv_heads, head_dim, p.max_parts,
+                         fp8 ? num_prefix_blocks : 0)
+        .total;
 }
 
-extern "C" pa_status pa_decode_shared_prefix(
-    void *out, const void *query, const void *key_cache, const void *value_cache,
-    const int32_t *block_tables, const int32_t *context_lens, int num_seqs, int num_q_heads,
-    int num_kv_heads, int head_dim, int block_size, int max_blocks_per_seq, int num_blocks,
-    float scale, pa_dtype dtype, int num_prefix_blocks, int partition_size, void *workspace,
-    size_t workspace_bytes, int32_t *device_status, void *stream) {
+// The path behind pa_decode_shared_prefix (bf16 pools) and
+// pa_decode_shared_prefix_fp8 (E4M3 pools with per-head scales).
+pa_status shared_prefix_common(void *out, const void *query, const void *key_cache,
+                               const void *value_cache, const float *k_scales,
+                               const float *v_scales, const int32_t *block_tables,
+                               const int32_t *context_lens, int num_seqs, int num_q_heads,
+                               int num_kv_heads, int head_dim, int block_size,
+                               int max_blocks_per_seq, int num_blocks, float scale, pa_dtype dtype,
+                               int num_prefix_blocks, int partition_size, void *workspace,
+                               size_t workspace_bytes, int32_t *device_status, void *stream) {
+    const bool fp8 = dtype == PA_DTYPE_FP8_E4M3;
     if (num_seqs < 0 || num_q_heads <= 0 || num_kv_heads <= 0 || block_size != kBlockSize ||
         max_blocks_per_seq < 0 || num_blocks <= 0 || num_q_heads % num_kv_heads != 0 ||
         !(scale == scale) || num_prefix_blocks < 0 || num_prefix_blocks > max_blocks_per_seq)
         return PA_ERR_INVALID_ARG;
-    if (dtype != PA_DTYPE_BF16) return PA_ERR_UNSUPPORTED;
-    if (partition_size != 0 &&
-        (partition_size < kBlockSize || partition_size > kMaxPartition || partition_size % kBlockSize))
-        return PA_ERR_INVALID_ARG;
+    if (!partition_ok(partition_size)) return PA_ERR_INVALID_ARG;
     if (num_seqs == 0) return PA_OK;
     if (!out || !query || !key_cache || !value_cache || !block_tables || !context_lens)
         return PA_ERR_INVALID_ARG;
     if (!aligned16(out) || !aligned16(query) || !aligned16(key_cache) || !aligned16(value_cache))
         return PA_ERR_INVALID_ARG;
     const int group = num_q_heads / num_kv_heads;
-    if (head_dim != 64 && head_dim != 128) return PA_ERR_UNSUPPORTED;
-    if (group > 16) return PA_ERR_UNSUPPORTED;
-    if (num_prefix_blocks == 0)
-        return pa_decode(out, query, key_cache, value_cache, block_tables, context_lens, num_seqs,
-                         num_q_heads, num_kv_heads, head_dim, block_size, max_blocks_per_seq,
-                         num_blocks, scale, dtype, partition_size, workspace, workspace_bytes,
-                         device_status, stream);
+    if (fp8) {
+        if (!k_scales || !v_scales) return PA_ERR_INVALID_ARG;
+        if (head_dim != 128 || group > 8) return PA_ERR_UNSUPPORTED;
+        if (!fp8_cascade(head_dim, num_q_heads, num_kv_heads, num_prefix_blocks))
+            return decode_common(out, query, key_cache, value_cache, k_scales, v_scales,
+                                 block_tables, context_lens, num_seqs, num_q_heads, num_kv_heads,
+                                 head_dim, block_size, max_blocks_per_seq, num_blocks, scale, dtype,
+                                 0, partition_size, workspace, workspace_bytes, device_status,
+                                 stream);
+    } else {
+        if (head_dim != 64 && head_dim != 128) return PA_ERR_UNSUPPORTED;
+        if (group > 16) return PA_ERR_UNSUPPORTED;
+        if (num_prefix_blocks == 0)
+            return decode_common(out, query, key_cache, value_cache, nullptr, nullptr, block_tables,
+                                 context_lens, num_seqs, num_q_heads, num_kv_heads, head_dim,
+                                 block_size, max_blocks_per_seq, num_blocks, scale, dtype, 0,
+                                 partition_size, workspace, workspace_bytes, device_status, stream);
+    }
     const int64_t rows = (int64_t)num_blocks * num_kv_heads * kBlockSize;
     if (rows >= ((int64_t)1 << 31)) return PA_ERR_UNSUPPORTED;
     SharedPlan p;
     if (!plan_shared(num_seqs, num_q_heads, num_kv_heads, head_dim, max_blocks_per_seq,
                      num_prefix_blocks, partition_size, &p))
         return PA_ERR_INVALID_ARG;
-    const size_t need = pa_decode_shared_prefix_workspace_bytes(
-        num_seqs, num_q_heads, num_kv_heads, head_dim, max_blocks_per_seq, num_prefix_blocks,
-        partition_size);
-    if (workspace == nullptr || workspace_bytes < need || !aligned16(workspace))
+    const SharedLayout lay = shared_layout(num_seqs, num_q_heads, num_kv_heads, head_dim,
+                                           p.max_parts, fp8 ? num_prefix_blocks : 0);
+    if (workspace == nullptr || workspace_bytes < lay.total || !aligned16(workspace))
         return PA_ERR_WORKSPACE;
     const int row_chunks = (num_seqs * group + kPrefixRows - 1) / kPrefixRows;
     if ((int64_t)num_seqs * num_kv_heads * p.suffix_max_parts >= ((int64_t)1 << 31) ||
-        (int64_t)num_kv_heads * row_chunks * p.prefix_chunks >= ((int64_t)1 << 31))
+        (int64_t)num_kv_heads * row_chunks * p.prefix_chunks >= ((int64_t)1 << 31) ||
+        (int64_t)num_prefix_blocks * num_kv_heads >= ((int64_t)1 << 31))
         return PA_ERR_UNSUPPORTED;
 
     const bool tc_prefix = prefix_tc_supported(head_dim, num_q_heads, num_kv_heads);
+    uint8_t *ws = static_cast<uint8_t *>(workspace);
     DecodeArgs a;
     a.out = out;
     a.query = query;
     a.block_tables = block_tables;
     a.context_lens = context_lens;
-    a.part_o = static_cast<float *>(workspace);
-    a.part_ml = reinterpret_cast<float2 *>(
-        static_cast<uint8_t *>(workspace) +
-        (((size_t)num_seqs * num_q_heads * p.max_parts * head_dim * sizeof(float) + 255) &
-         ~size_t(255)));
+    a.part_o = reinterpret_cast<float *>(ws);
+    a.part_ml = reinterpret_cast<float2 *>(ws + lay.ml_offset);
     a.status = device_status;
-    a.k_scales = nullptr;
-    a.v_scales = nullptr;
+    a.k_scales = fp8 ? k_scales : nullptr;
+    a.v_scales = fp8 ? v_scales : nullptr;
     a.num_seqs = num_seqs;
     a.num_q_heads = num_q_heads;
     a.num_kv_heads = num_kv_heads;
@@ -2079,17 +2192,35 @@ extern "C" pa_status pa_decode_shared_prefix(
     a.defer_wait = 1;
     cudaStream_t st = static_cast<cudaStream_t>(stream);
 
+    // 0. FP8 pools: the prefix blocks' codes widened to bf16 for the tensor cores
+    if (fp8) {
+        cudaError_t e = launch_chained(
+            pa_widen_prefix_kernel, dim3((unsigned)(num_prefix_blocks * num_kv_heads), 2), dim3(128),
+            0, st, static_cast<const uint8_t *>(key_cache), static_cast<const uint8_t *>(value_cache),
+            block_tables, num_kv_heads, num_blocks, head_dim,
+            reinterpret_cast<__nv_bfloat16 *>(ws + lay.staged_k_offset),
+            reinterpret_cast<__nv_bfloat16 *>(ws + lay.staged_v_offset), device_status);
+        if (e != cudaSuccess) return cuda_failure(e, "pa_widen_prefix_kernel launch");
+        count_launches(1);
+    }
     // 1. the shared prefix, once per KV head for all sequences: on the tensor
     //    cores (256 rows per K/V tile) where the shape allows, else 64 query
     //    rows at a time on mma.sync tiles.  It takes part of the SMs (one CTA
     //    each) and lets the suffix kernel launch as soon as all of its CTAs
     //    have started.
     if (tc_prefix) {
-        pa_status ps = launch_prefix_tc(query, key_cache, value_cache, block_tables, context_lens,
-                                        num_seqs, num_q_heads, num_kv_heads, max_blocks_per_seq,
-                                        num_blocks, a.scale_log2, num_prefix_blocks,
-                                        p.prefix_chunk_blocks, p.prefix_chunks, a.part_o,
-                                        a.part_ml, p.max_parts, device_status, st);
+        pa_status ps =
+            fp8 ? launch_prefix_tc(query, ws + lay.staged_k_offset, ws + lay.staged_v_offset,
+                                   block_tables, context_lens, num_seqs, num_q_heads, num_kv_heads,
+                                   max_blocks_per_seq, num_prefix_blocks, a.scale_log2,
+                                   num_prefix_blocks, p.prefix_chunk_blocks, p.prefix_chunks,
+                                   a.part_o, a.part_ml, p.max_parts, true, k_scales, v_scales,
+                                   device_status, st)
+                : launch_prefix_tc(query, key_cache, value_cache, block_tables, context_lens,
+                                   num_seqs, num_q_heads, num_kv_heads, max_blocks_per_seq,
+                                   num_blocks, a.scale_log2, num_prefix_blocks,
+                                   p.prefix_chunk_blocks, p.prefix_chunks, a.part_o, a.part_ml,
+                                   p.max_parts, false, nullptr, nullptr, device_status, st);
         if (ps != PA_OK) return ps;
     } else {
         CUtensorMap kmap, vmap;
@@ -2119,9 +2250,61 @@ extern "C" pa_status pa_decode_shared_prefix(
     }
     // 2. every context past the prefix, as partials, beside the prefix kernel
     //    (defer_wait: only its CTA 0 waits for the prefix kernel to finish)
-    pa_status s = head_dim == 64 ? dispatch_bf16<64>(group, a, key_cache, value_cache, rows, st)
+    pa_status s = fp8 ? dispatch_fp8(group, a, key_cache, value_cache, rows, st)
+                : head_dim == 64 ? dispatch_bf16<64>(group, a, key_cache, value_cache, rows, st)
                                  : dispatch_bf16<128>(group, a, key_cache, value_cache, rows, st);
     if (s != PA_OK) return s;
     // 3. merge prefix and suffix partials
     return launch_reduce<__nv_bfloat16>(a, head_dim, st);
+}
+
+}  // namespace
+}  // namespace pa
+
+extern "C" size_t pa_decode_shared_prefix_workspace_bytes(int num_seqs, int num_q_heads,
+                                                          int num_kv_heads, int head_dim,
+                                                          int max_blocks_per_seq,
+                                                          int num_prefix_blocks,
+                                                          int partition_size) {
+    return shared_workspace(num_seqs, num_q_heads, num_kv_heads, head_dim, max_blocks_per_seq,
+                            num_prefix_blocks, partition_size, false);
+}
+
+extern "C" pa_status pa_decode_shared_prefix(
+    void *out, const void *query, const void *key_cache, const void *value_cache,
+    const int32_t *block_tables, const int32_t *context_lens, int num_seqs, int num_q_heads,
+    int num_kv_heads, int head_dim, int block_size, int max_blocks_per_seq, int num_blocks,
+    float scale, pa_dtype dtype, int num_prefix_blocks, int partition_size, void *workspace,
+    size_t workspace_bytes, int32_t *device_status, void *stream) {
+    if (dtype != PA_DTYPE_BF16) return PA_ERR_UNSUPPORTED;
+    return shared_prefix_common(out, query, key_cache, value_cache, nullptr, nullptr, block_tables,
+                                context_lens, num_seqs, num_q_heads, num_kv_heads, head_dim,
+                                block_size, max_blocks_per_seq, num_blocks, scale, dtype,
+                                num_prefix_blocks, partition_size, workspace, workspace_bytes,
+                                device_status, stream);
+}
+
+extern "C" size_t pa_decode_shared_prefix_fp8_workspace_bytes(int num_seqs, int num_q_heads,
+                                                              int num_kv_heads, int head_dim,
+                                                              int max_blocks_per_seq,
+                                                              int num_prefix_blocks,
+                                                              int partition_size) {
+    return shared_workspace(num_seqs, num_q_heads, num_kv_heads, head_dim, max_blocks_per_seq,
+                            num_prefix_blocks, partition_size, true);
+}
+
+extern "C" pa_status pa_decode_shared_prefix_fp8(
+    void *out, const void *query, const void *key_cache, const void *value_cache,
+    const float *k_scales, const float *v_scales, const int32_t *block_tables,
+    const int32_t *context_lens, int num_seqs, int num_q_heads, int num_kv_heads, int head_dim,
+    int block_size, int max_blocks_per_seq, int num_blocks, float scale, int num_prefix_blocks,
+    int partition_size, void *workspace, size_t workspace_bytes, int32_t *device_status,
+    void *stream) {
+    if ((reinterpret_cast<uintptr_t>(k_scales) & 3u) || (reinterpret_cast<uintptr_t>(v_scales) & 3u))
+        return PA_ERR_INVALID_ARG;
+    return shared_prefix_common(out, query, key_cache, value_cache, k_scales, v_scales,
+                                block_tables, context_lens, num_seqs, num_q_heads, num_kv_heads,
+                                head_dim, block_size, max_blocks_per_seq, num_blocks, scale,
+                                PA_DTYPE_FP8_E4M3, num_prefix_blocks, partition_size, workspace,
+                                workspace_bytes, device_status, stream);
 }

@@ -47,6 +47,9 @@ cudaError_t launch_chained(void (*kernel)(KArgs...), dim3 grid, dim3 block, size
 // Shared prefix of a decode batch on the tensor cores (pa_prefill.cu): split-K
 // partials (max, sum, unnormalised output) of every (sequence, query head) row
 // against each chunk of the prefix blocks, written to partial index = chunk.
+// staged: key_cache / value_cache are a bf16 copy of the prefix blocks' E4M3
+// code values, block j of the prefix at index j (num_blocks = prefix_blocks),
+// with per-KV-head scales k_scales / v_scales (else both nullptr).
 bool prefix_tc_supported(int head_dim, int num_q_heads, int num_kv_heads);
 int prefix_tc_chunk_blocks(int num_seqs, int num_q_heads, int num_kv_heads, int prefix_blocks,
                            int sm_count);
@@ -54,7 +57,8 @@ pa_status launch_prefix_tc(const void *query, const void *key_cache, const void 
                            const int32_t *block_tables, const int32_t *context_lens, int num_seqs,
                            int num_q_heads, int num_kv_heads, int max_blocks, int num_blocks,
                            float scale_log2, int prefix_blocks, int chunk_blocks, int chunks,
-                           float *part_o, float2 *part_ml, int max_parts, int32_t *status,
+                           float *part_o, float2 *part_ml, int max_parts, bool staged,
+                           const float *k_scales, const float *v_scales, int32_t *status,
                            cudaStream_t stream);
 
 }  // namespace pa

@@ -120,6 +120,12 @@ struct PrefillArgs {
     int max_parts;
     int prefix_blocks;
     int chunk_blocks;
+    // shared prefix of FP8 pools: the K/V tensors are a staging copy of the
+    // prefix blocks' code values in bf16, block j at index j (no table), and
+    // the stored values are code * scale of the KV head (nullptr: bf16 pools)
+    int staged;
+    const float *k_scales;
+    const float *v_scales;
 };
 
 namespace {
@@ -296,7 +302,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const int nb = min(8, blk_hi - blk0);
                 int rows[8];
                 for (int i = 0; i < nb; ++i) {
-                    int phys = trow[blk0 + i];
+                    int phys = a.staged ? blk0 + i : trow[blk0 + i];
                     if ((unsigned)phys >= (unsigned)a.num_blocks) {
                         report(a.status, PA_DEV_BAD_BLOCK_ID);
                         phys = 0;
@@ -431,7 +437,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             const uint32_t s_base = tmem + col_s(x) + lane_off;
             const uint32_t o_base = tmem + col_o(x) + lane_off;
             float *red = reinterpret_cast<float *>(base + kOffRed) + x * 2 * kSplit * kRows;
-            const float sl2 = a.scale_log2;
+            const float sl2 = a.k_scales != nullptr ? a.scale_log2 * a.k_scales[kvh] : a.scale_log2;
             float m_used = -INFINITY, l = 0.f;
             // Every thread of the group runs every iteration and reaches the
             // named barrier the same number of times, even after a wait gave up
@@ -569,6 +575,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 tc_fence_after();
                 const size_t prow = ((size_t)(tx0 + tr) * a.num_q_heads + kvh * g + (r % g)) * a.max_parts +
                                     blockIdx.z;
+                const float vs = a.v_scales != nullptr ? a.v_scales[kvh] : 1.f;
 #pragma unroll 1
                 for (int c = 0; c < kCols; c += 32) {
                     uint32_t o[32];
@@ -578,8 +585,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                         float4 *dst = reinterpret_cast<float4 *>(a.part_o + prow * kD + part * kCols + c);
 #pragma unroll
                         for (int q = 0; q < 8; ++q)
-                            dst[q] = make_float4(__uint_as_float(o[4 * q]), __uint_as_float(o[4 * q + 1]),
-                                                 __uint_as_float(o[4 * q + 2]), __uint_as_float(o[4 * q + 3]));
+                            dst[q] = make_float4(__uint_as_float(o[4 * q]) * vs, __uint_as_float(o[4 * q + 1]) * vs,
+                                                 __uint_as_float(o[4 * q + 2]) * vs,
+                                                 __uint_as_float(o[4 * q + 3]) * vs);
                     }
                 }
                 if (real && part == 0)
@@ -697,9 +705,11 @@ bool prefix_tc_supported(int head_dim, int num_q_heads, int num_kv_heads) {
 // Prefix chunk (in blocks, whole 8-block K/V tiles) that gives about
 // PA_PREFIX_TC_CTAS_PER_100_SM / 100 CTAs per SM over (256-row tiles x KV heads
 // x chunks).  The prefix runs beside the suffix decode, so it takes only part
-// of the GPU.
+// of the GPU: on the 128-sequence mix (63 shared blocks, 8 KV heads) a sixth
+// of the SMs (two chunks, 32 CTAs) gave the shortest call; 16 CTAs made the
+// prefix the longer of the two, 48 or more slowed the suffix.
 #ifndef PA_PREFIX_TC_CTAS_PER_100_SM
-#define PA_PREFIX_TC_CTAS_PER_100_SM 25
+#define PA_PREFIX_TC_CTAS_PER_100_SM 15
 #endif
 int prefix_tc_chunk_blocks(int num_seqs, int num_q_heads, int num_kv_heads, int prefix_blocks,
                            int sm_count) {
@@ -717,7 +727,8 @@ pa_status launch_prefix_tc(const void *query, const void *key_cache, const void 
                            const int32_t *block_tables, const int32_t *context_lens, int num_seqs,
                            int num_q_heads, int num_kv_heads, int max_blocks, int num_blocks,
                            float scale_log2, int prefix_blocks, int chunk_blocks, int chunks,
-                           float *part_o, float2 *part_ml, int max_parts, int32_t *status,
+                           float *part_o, float2 *part_ml, int max_parts, bool staged,
+                           const float *k_scales, const float *v_scales, int32_t *status,
                            cudaStream_t stream) {
     const int group = num_q_heads / num_kv_heads;
     const int64_t pool_rows = (int64_t)num_blocks * num_kv_heads * kBlockSize;
@@ -743,6 +754,9 @@ pa_status launch_prefix_tc(const void *query, const void *key_cache, const void 
     a.max_parts = max_parts;
     a.prefix_blocks = prefix_blocks;
     a.chunk_blocks = chunk_blocks;
+    a.staged = staged ? 1 : 0;
+    a.k_scales = k_scales;
+    a.v_scales = v_scales;
     return launch_tc<true>(qmap, kmap, vmap, a, dim3((unsigned)tiles, (unsigned)num_kv_heads,
                                                       (unsigned)chunks),
                            stream);

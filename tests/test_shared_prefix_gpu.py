@@ -167,3 +167,68 @@ def test_workspace_reused_across_calls(pkv, fill):
         torch.cuda.synchronize()
         assert int(status.item()) == 0
         H.assert_close(H.as_f64(out), H.as_f64(plain), "bf16", f"call {call} ({fill})")
+
+
+def _fp8_run(pkv, wl, hv, n_prefix, lens=None, status=None, partition_size=0, workspace=None):
+    import torch
+    q = H.host_to_device(hv.query, torch.bfloat16)
+    kc = torch.from_numpy(np.ascontiguousarray(hv.key_cache)).cuda()
+    vc = torch.from_numpy(np.ascontiguousarray(hv.value_cache)).cuda()
+    ks = torch.from_numpy(np.ascontiguousarray(hv.k_scales)).cuda()
+    vs = torch.from_numpy(np.ascontiguousarray(hv.v_scales)).cuda()
+    bt = torch.from_numpy(wl.block_tables).cuda()
+    cl = torch.from_numpy(np.asarray(wl.context_lens if lens is None else lens, np.int32)).cuda()
+    out = pkv.decode_shared_prefix_fp8(q, kc, vc, ks, vs, bt, cl, n_prefix, wl.scale, status=status,
+                                       partition_size=partition_size, workspace=workspace)
+    ref_gpu = pkv.decode_fp8(q, kc, vc, ks, vs, bt, cl, wl.scale)
+    torch.cuda.synchronize()
+    return out, ref_gpu
+
+
+@pytest.mark.parametrize("hq,hkv", [(8, 8), (32, 8), (16, 2), (16, 8), (6, 2)])
+@pytest.mark.parametrize("prefix_blocks", [1, 9, 40])
+def test_shared_prefix_fp8_matches_oracle(pkv, hq, hkv, prefix_blocks):
+    """E4M3 pools: the prefix widened to bf16 code values on the tensor cores with
+    the per-head scales folded in, the suffix on the FP8 decode kernel (group 3
+    takes plain FP8 decode)."""
+    suffix = [0, 1, 15, 16, 17, 200, 640, 3]
+    wl = _shared_workload(len(suffix), hq, hkv, 128, prefix_blocks, suffix, seed=hq + hkv + prefix_blocks)
+    hv = W.fp8_host_values(wl)          # slots holding no context token carry the NaN code
+    out, ref_gpu = _fp8_run(pkv, wl, hv, prefix_blocks)
+    ref = oracle.paged_decode(hv.query, hv.key_cache, hv.value_cache, wl.block_tables,
+                              wl.context_lens, wl.scale, threads=4, k_scales=hv.k_scales,
+                              v_scales=hv.v_scales)
+    H.assert_close(H.as_f64(out), ref, "bf16", f"fp8 shared prefix {hq}/{hkv} n={prefix_blocks}")
+    H.assert_close(H.as_f64(out), H.as_f64(ref_gpu), "bf16", "fp8 shared prefix vs pa_decode_fp8")
+
+
+def test_shared_prefix_fp8_short_contexts_and_split_suffix(pkv):
+    wl = _shared_workload(6, 16, 4, 128, 12, [5, 0, 30, 1, 900, 333], seed=19)
+    hv = W.fp8_host_values(wl, poison_unused=False)
+    lens = wl.context_lens.copy()
+    lens[1] = 37            # ends inside the prefix
+    lens[3] = 0             # empty
+    out, _ = _fp8_run(pkv, wl, hv, 12, lens=lens, partition_size=64)
+    ref = oracle.paged_decode(hv.query, hv.key_cache, hv.value_cache, wl.block_tables, lens,
+                              wl.scale, k_scales=hv.k_scales, v_scales=hv.v_scales)
+    got = H.as_f64(out)
+    assert np.all(got[3] == 0)
+    H.assert_close(got, ref, "bf16", "fp8 short contexts")
+
+
+def test_shared_prefix_fp8_workload_full_size(pkv):
+    """The 128-sequence mix on E4M3 pools, after copy-on-write (63 shared blocks)."""
+    import torch
+    wl = W.make_workload("shared_prefix")
+    n_prefix = pkv.shared_prefix_blocks(wl.block_tables)
+    q, kc, vc, _, _, ks, vs = W.fp8_device_values(wl, "cuda")
+    pkv.block_copy(kc, vc, torch.from_numpy(wl.cow_pairs).cuda())
+    bt = torch.from_numpy(wl.block_tables).cuda()
+    lens = wl.step_context_lens
+    cl = torch.from_numpy(lens).cuda()
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    out = pkv.decode_shared_prefix_fp8(q, kc, vc, ks, vs, bt, cl, n_prefix, wl.scale, status=status)
+    plain = pkv.decode_fp8(q, kc, vc, ks, vs, bt, cl, wl.scale)
+    torch.cuda.synchronize()
+    assert int(status.item()) == 0
+    H.assert_close(H.as_f64(out), H.as_f64(plain), "bf16", "fp8 cascade vs plain FP8 decode")
