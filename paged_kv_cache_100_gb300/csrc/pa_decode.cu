@@ -51,6 +51,7 @@ namespace {
 
 constexpr uint32_t kFull = 0xffffffffu;
 constexpr float kLog2e = 1.4426950408889634f;
+constexpr float kLazyRescaleLog2 = 8.f;   // FP8 consumers: rescale when the maximum grows by > 2^8
 
 struct DecodeArgs {
     void *out;
@@ -675,8 +676,10 @@ struct MhaFp8Consumer {
             float dot = 0.f;
 #pragma unroll
             for (int j = 0; j < 4; ++j) {
-                dot = dot2_f16_f32(q[2 * j], e4m3x2_to_f16x2(w4[j]), dot);
-                dot = dot2_f16_f32(q[2 * j + 1], e4m3x2_to_f16x2(w4[j] >> 16), dot);
+                uint32_t k01, k23;
+                e4m3x4_to_f16x2x2(w4[j], k01, k23);
+                dot = dot2_f16_f32(q[2 * j], k01, dot);
+                dot = dot2_f16_f32(q[2 * j + 1], k23, dot);
             }
             v[i] = dot;
         }
@@ -696,28 +699,32 @@ struct MhaFp8Consumer {
         float bmax = s;
 #pragma unroll
         for (int M = 2; M < 32; M <<= 1) bmax = fmaxf(bmax, __shfl_xor_sync(kFull, bmax, M));
-        const float m_new = fmaxf(m, bmax);
-        const float alpha = exp2f(m - m_new);
-        const float p = exp2f(s - m_new);
-        l = l * alpha + ((lane & 1) ? 0.f : p);
-        m = m_new;
+        // Lazy rescale: the reference maximum m moves (and acc, l are rescaled)
+        // only when the block's maximum exceeds it by more than 2^8, so the
+        // weights stay in [0, 256].  The decision is warp-uniform.
+        if (bmax > m + kLazyRescaleLog2) {
+            const float alpha = exp2f(m - bmax);   // 0 while m is -inf
+            l *= alpha;
 #pragma unroll
-        for (int e = 0; e < 16; ++e) acc[e] *= alpha;
+            for (int e = 0; e < 16; ++e) acc[e] *= alpha;
+            m = bmax;
+        }
+        const float p = exp2f(s - m);
+        l += (lane & 1) ? 0.f : p;
 #pragma unroll
         for (int i = 0; i < RPL; ++i) {
             const int r = rg * RPL + i;
-            const float pr = __shfl_sync(kFull, p, rg * CH + 2 * i);
+            // the weight enters the products as f16 (relative error <= 2^-11)
+            const uint32_t p16 = pack_f16x2(__shfl_sync(kFull, p, rg * CH + 2 * i), 0.f);
             const uint4 vw = lds128(swz(vtile, r, c));
             if (r >= nlo && r < nvalid) {
                 const uint32_t w4[4] = {vw.x, vw.y, vw.z, vw.w};
 #pragma unroll
                 for (int j = 0; j < 4; ++j) {
-                    const uint32_t h0 = e4m3x2_to_f16x2(w4[j]);
-                    const uint32_t h1 = e4m3x2_to_f16x2(w4[j] >> 16);
-                    acc[4 * j + 0] = fmaf(pr, f16lo(h0), acc[4 * j + 0]);
-                    acc[4 * j + 1] = fmaf(pr, f16hi(h0), acc[4 * j + 1]);
-                    acc[4 * j + 2] = fmaf(pr, f16lo(h1), acc[4 * j + 2]);
-                    acc[4 * j + 3] = fmaf(pr, f16hi(h1), acc[4 * j + 3]);
+                    uint32_t v01, v23;
+                    e4m3x4_to_f16x2x2(w4[j], v01, v23);
+                    fma2_f16_f32(p16, v01, acc[4 * j + 0], acc[4 * j + 1]);
+                    fma2_f16_f32(p16, v23, acc[4 * j + 2], acc[4 * j + 3]);
                 }
             }
         }
@@ -802,15 +809,11 @@ struct GqaTFp8Consumer {
             const uint2 r0 = lds64(fp8_addr(ktile, g, 32 * kk + 8 * t));
             const uint2 r1 = lds64(fp8_addr(ktile, g + 8, 32 * kk + 8 * t));
             uint32_t a[4];
-            a[0] = e4m3x2_to_f16x2(r0.x);
-            a[1] = e4m3x2_to_f16x2(r1.x);
-            a[2] = e4m3x2_to_f16x2(r0.x >> 16);
-            a[3] = e4m3x2_to_f16x2(r1.x >> 16);
+            e4m3x4_to_f16x2x2(r0.x, a[0], a[2]);
+            e4m3x4_to_f16x2x2(r1.x, a[1], a[3]);
             mma_f16_16816(s, a, qb[2 * kk][0], qb[2 * kk][1]);
-            a[0] = e4m3x2_to_f16x2(r0.y);
-            a[1] = e4m3x2_to_f16x2(r1.y);
-            a[2] = e4m3x2_to_f16x2(r0.y >> 16);
-            a[3] = e4m3x2_to_f16x2(r1.y >> 16);
+            e4m3x4_to_f16x2x2(r0.y, a[0], a[2]);
+            e4m3x4_to_f16x2x2(r1.y, a[1], a[3]);
             mma_f16_16816(s, a, qb[2 * kk + 1][0], qb[2 * kk + 1][1]);
         }
         const bool v0 = g >= nlo && g < nvalid, v1 = g + 8 >= nlo && g + 8 < nvalid;
@@ -824,21 +827,30 @@ struct GqaTFp8Consumer {
             mx0 = fmaxf(mx0, __shfl_xor_sync(kFull, mx0, M));
             mx1 = fmaxf(mx1, __shfl_xor_sync(kFull, mx1, M));
         }
-        const float mn0 = fmaxf(m0, mx0), mn1 = fmaxf(m1, mx1);
-        const float a0 = exp2f(m0 - mn0), a1 = exp2f(m1 - mn1);
-        m0 = mn0;
-        m1 = mn1;
-        const float p0 = exp2f(s[0] - mn0), p1 = exp2f(s[1] - mn1);
-        const float p2 = exp2f(s[2] - mn0), p3 = exp2f(s[3] - mn1);
-        l0 = l0 * a0 + (p0 + p2);
-        l1 = l1 * a1 + (p1 + p3);
+        // Lazy rescale: a head's reference maximum moves (and its O and sum
+        // are rescaled) only when the block's maximum exceeds it by more than
+        // 2^8, so the weights stay in [0, 256] (f16 holds them); the warp skips
+        // the rescale when no head of it needs one.
+        const bool need0 = mx0 > m0 + kLazyRescaleLog2, need1 = mx1 > m1 + kLazyRescaleLog2;
+        if (__any_sync(kFull, need0 || need1)) {
+            const float a0 = need0 ? exp2f(m0 - mx0) : 1.f;   // 0 while m0 is -inf
+            const float a1 = need1 ? exp2f(m1 - mx1) : 1.f;
+            m0 = need0 ? mx0 : m0;
+            m1 = need1 ? mx1 : m1;
+            l0 *= a0;
+            l1 *= a1;
 #pragma unroll
-        for (int mt = 0; mt < KS; ++mt) {
-            o[mt][0] *= a0;
-            o[mt][1] *= a1;
-            o[mt][2] *= a0;
-            o[mt][3] *= a1;
+            for (int mt = 0; mt < KS; ++mt) {
+                o[mt][0] *= a0;
+                o[mt][1] *= a1;
+                o[mt][2] *= a0;
+                o[mt][3] *= a1;
+            }
         }
+        const float p0 = exp2f(s[0] - m0), p1 = exp2f(s[1] - m1);
+        const float p2 = exp2f(s[2] - m0), p3 = exp2f(s[3] - m1);
+        l0 += p0 + p2;
+        l1 += p1 + p3;
         uint32_t top_hi, top_lo, bot_hi, bot_lo;
         split_f16x2(p0, p1, top_hi, top_lo);
         split_f16x2(p2, p3, bot_hi, bot_lo);
@@ -858,10 +870,8 @@ struct GqaTFp8Consumer {
                 const uint32_t x0 = __byte_perm(wa, wb, sel);   // tokens 2t, 2t+1
                 const uint32_t x1 = __byte_perm(wc, wd, sel);   // tokens 2t+8, 2t+9
                 uint32_t a[4];
-                a[0] = e4m3x2_to_f16x2(x0);
-                a[1] = e4m3x2_to_f16x2(x0 >> 16);
-                a[2] = e4m3x2_to_f16x2(x1);
-                a[3] = e4m3x2_to_f16x2(x1 >> 16);
+                e4m3x4_to_f16x2x2(x0, a[0], a[1]);
+                e4m3x4_to_f16x2x2(x1, a[2], a[3]);
                 mma_f16_16816(o[2 * c + jp], a, bh0, bh1);
                 mma_f16_16816(o[2 * c + jp], a, bl0, bl1);
             }

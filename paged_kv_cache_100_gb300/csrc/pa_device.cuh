@@ -161,6 +161,28 @@ __device__ __forceinline__ uint32_t e4m3x2_to_f16x2(uint32_t two_codes) {
     return r;
 }
 
+// Four E4M3 codes (byte k = element k) to two f16x2 words: elements 0, 1 in
+// *lo and 2, 3 in *hi; exact.  Both halves come straight from the 32-bit
+// word's 16-bit halves (no shift).
+__device__ __forceinline__ void e4m3x4_to_f16x2x2(uint32_t four_codes, uint32_t &lo, uint32_t &hi) {
+    asm("{\n\t.reg .b16 l, h;\n\tmov.b32 {l, h}, %2;\n\t"
+        "cvt.rn.f16x2.e4m3x2 %0, l;\n\tcvt.rn.f16x2.e4m3x2 %1, h;\n\t}"
+        : "=r"(lo), "=r"(hi)
+        : "r"(four_codes));
+}
+
+// acc0 += p * v.lo, acc1 += p * v.hi with an f16 weight p (low half of the
+// 32-bit p16), an f16x2 pair v and fp32 accumulators (each product is exact in
+// fp32).
+__device__ __forceinline__ void fma2_f16_f32(uint32_t p16, uint32_t v, float &acc0, float &acc1) {
+    asm("{\n\t.reg .b16 pl, ph, vl, vh;\n\t"
+        "mov.b32 {pl, ph}, %2;\n\tmov.b32 {vl, vh}, %3;\n\t"
+        "fma.rn.f32.f16 %0, pl, vl, %0;\n\t"
+        "fma.rn.f32.f16 %1, pl, vh, %1;\n\t}"
+        : "+f"(acc0), "+f"(acc1)
+        : "r"(p16), "r"(v));
+}
+
 // E4M3 codes of two floats, round to nearest even, saturating at +-448
 // (first element in the low byte).
 __device__ __forceinline__ uint32_t f32x2_to_e4m3x2(float first, float second) {
