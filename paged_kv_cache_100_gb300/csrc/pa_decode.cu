@@ -776,11 +776,22 @@ struct GqaTFp8Consumer {
     float m0, m1, l0, l1;
     float ck, vs;
     int lane, g, t;
+    // This lane's swizzled byte offsets in a tile (fp8_addr with the lane's
+    // rows and columns folded in): K rows g (+ 1024 for row g + 8) at column
+    // 32kk + 8t; V rows 2t (+ 1024: 2t + 8) and 2t + 1 (+ 1024: 2t + 9) at
+    // column 32c + 4g.
+    uint32_t koff[D / 32], voff_a[D / 32], voff_b[D / 32];
 
     __device__ __forceinline__ void init(const DecodeArgs &a, const Work &w, int lane_) {
         lane = lane_;
         g = lane >> 2;
         t = lane & 3;
+#pragma unroll
+        for (int c = 0; c < D / 32; ++c) {
+            koff[c] = fp8_addr(0u, g, 32 * c + 8 * t);
+            voff_a[c] = fp8_addr(0u, 2 * t, 32 * c + 4 * g);
+            voff_b[c] = fp8_addr(0u, 2 * t + 1, 32 * c + 4 * g);
+        }
         ck = a.scale_log2 * a.k_scales[w.head];
         vs = a.v_scales[w.head];
         const __nv_bfloat16 *qg = static_cast<const __nv_bfloat16 *>(a.query) +
@@ -806,8 +817,9 @@ struct GqaTFp8Consumer {
         float s[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
         for (int kk = 0; kk < D / 32; ++kk) {
-            const uint2 r0 = lds64(fp8_addr(ktile, g, 32 * kk + 8 * t));
-            const uint2 r1 = lds64(fp8_addr(ktile, g + 8, 32 * kk + 8 * t));
+            const uint32_t ka = ktile + koff[kk];
+            const uint2 r0 = lds64(ka);
+            const uint2 r1 = lds64(ka + 1024);   // row g + 8: same swizzle phase
             uint32_t a[4];
             e4m3x4_to_f16x2x2(r0.x, a[0], a[2]);
             e4m3x4_to_f16x2x2(r1.x, a[1], a[3]);
@@ -859,11 +871,11 @@ struct GqaTFp8Consumer {
         if (nlo > 0 || nvalid < 16) zero_rows_outside_128(vtile, nlo, nvalid, lane);
 #pragma unroll
         for (int c = 0; c < D / 32; ++c) {
-            const int byte = 32 * c + 4 * g;
-            const uint32_t wa = lds32(fp8_addr(vtile, 2 * t, byte));
-            const uint32_t wb = lds32(fp8_addr(vtile, 2 * t + 1, byte));
-            const uint32_t wc = lds32(fp8_addr(vtile, 2 * t + 8, byte));
-            const uint32_t wd = lds32(fp8_addr(vtile, 2 * t + 9, byte));
+            const uint32_t va = vtile + voff_a[c], vb = vtile + voff_b[c];
+            const uint32_t wa = lds32(va);
+            const uint32_t wb = lds32(vb);
+            const uint32_t wc = lds32(va + 1024);   // rows + 8: same swizzle phase
+            const uint32_t wd = lds32(vb + 1024);
 #pragma unroll
             for (int jp = 0; jp < 2; ++jp) {
                 const uint32_t sel = jp == 0 ? 0x5140u : 0x7362u;
@@ -1580,9 +1592,10 @@ cudaError_t allow_smem(K kernel, size_t bytes) {
 #define PA_GQA16_STAGES 2
 #endif
 // FP8 pools (4 KiB per block): MHA 8 warps x 2 stages (64 KiB, three CTAs per
-// SM); GQA 8 warps x 2 stages (32 KiB; about 120 registers make it two CTAs
-// per SM).  Measured alternatives: MHA 8x1, 8x3, 8x4, 12x2, 16x2; GQA 4x2,
-// 4x4, 4x6, 6x2, 8x3.
+// SM); GQA 4 warps x 3 stages (48 KiB).  Measured alternatives with the
+// current consumers: MHA 8x3, 12x2, 4x4 (7B-shaped batch 89.4 us at 8x2
+// against 92.5-99.2 us); GQA 8x2, 8x3, 6x2 (70B-shaped batch 208.4 us at 4x3
+// against 210.6-217.5 us).
 #ifndef PA_MHA8_WARPS
 #define PA_MHA8_WARPS 8
 #endif
@@ -1590,16 +1603,15 @@ cudaError_t allow_smem(K kernel, size_t bytes) {
 #define PA_MHA8_STAGES 2
 #endif
 #ifndef PA_GQA8_WARPS
-#define PA_GQA8_WARPS 8
+#define PA_GQA8_WARPS 4
 #endif
 #ifndef PA_GQA8_STAGES
-#define PA_GQA8_STAGES 2
+#define PA_GQA8_STAGES 3
 #endif
 // FP8 GQA CTAs that stream at most PA_GQA8S_MAX_BLOCKS blocks (short contexts,
-// e.g. the part of a context past a shared prefix): 4 warps x 2 stages.  Each
-// warp then gets twice as many blocks, so its ring fills; on the 128-sequence
-// shared-prefix mix (suffixes of 1..64 blocks) the FP8 suffix took 50.0 us
-// against 55.2 us with 8 warps.
+// e.g. the part of a context past a shared prefix): 4 warps x 2 stages.  On
+// the 128-sequence shared-prefix mix (suffixes of 1..64 blocks) the FP8
+// suffix took 50.0 us against 55.2 us with 8 warps x 2 stages.
 #ifndef PA_GQA8S_WARPS
 #define PA_GQA8S_WARPS 4
 #endif
