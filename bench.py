@@ -756,6 +756,7 @@ def run_prefill_gpu(args):
     slots = torch.from_numpy(pw.slot_mapping).to(dev)
     maxq = int(pw.chunk.max())
     out = torch.empty_like(q)
+    ws = torch.empty(int(pkv.lib().pa_prefill_workspace_bytes()), dtype=torch.uint8, device=dev)
     stream = torch.cuda.current_stream(dev)
     window = args.window
 
@@ -764,7 +765,8 @@ def run_prefill_gpu(args):
         pkv.cache_write(kc, vc, kn_, vn_, slots_)
         if ev_pre is not None:
             ev_pre.record(stream)
-        pkv.prefill(q_, kc, vc, bt_, lens_, qs_, maxq, pw.scale, window=window, out=out)
+        pkv.prefill(q_, kc, vc, bt_, lens_, qs_, maxq, pw.scale, window=window, out=out,
+                    workspace=ws)
         if ev_post is not None:
             ev_post.record(stream)
 

@@ -367,17 +367,25 @@ pa_status pa_block_copy(void *key_cache, void *value_cache, const int32_t *src_d
  *  window            0 = causal over the whole context
  * Pools, block tables, scale, device_status and stream as in pa_decode; table
  * entries of blocks wholly before every row's window are not read.
+ *  workspace         device scratch of at least pa_prefill_workspace_bytes()
+ *                    bytes, 16-byte aligned: the work counter of the CTAs
+ *                    (set to zero on the stream by each call; calls that run
+ *                    at the same time need their own)
  * Supported: bf16, head_dim 128, group (num_q_heads / num_kv_heads) 1, 2, 4, 8
  * or 16.  Arithmetic: S = QK^T and O = PV on tcgen05 tensor cores with fp32
  * accumulation in tensor memory; P goes to the second product as a bf16 head
- * plus a bf16 residual (about 2^-17 relative).  One kernel launch; no workspace.
+ * plus a bf16 residual (about 2^-17 relative).  A memset of the work counter,
+ * then one kernel launch: one CTA per SM, each taking (256-row tile, KV head,
+ * sequence) items in turn.
  */
+size_t pa_prefill_workspace_bytes(void);
 pa_status pa_prefill(void *out, const void *query, const void *key_cache, const void *value_cache,
                      const int32_t *block_tables, const int32_t *context_lens,
                      const int32_t *query_start, int num_seqs, int num_q_heads, int num_kv_heads,
                      int head_dim, int block_size, int max_blocks_per_seq, int num_blocks,
                      int num_query_tokens, int max_query_len, float scale, pa_dtype dtype,
-                     int window, int32_t *device_status, void *stream);
+                     int window, void *workspace, size_t workspace_bytes, int32_t *device_status,
+                     void *stream);
 
 /*
  * Swap of blocks between the pools and a staging buffer ("PagedAttention por

@@ -389,7 +389,8 @@ def block_copy(key_cache, value_cache, src_dst, *, status=None, stream=None):
 
 
 def prefill(query, key_cache, value_cache, block_tables, context_lens, query_start,
-            max_query_len=None, scale=None, *, window=0, out=None, status=None, stream=None):
+            max_query_len=None, scale=None, *, window=0, out=None, workspace=None, status=None,
+            stream=None):
     """Chunked prefill over the paged pools (``pa_prefill``); returns ``out``.
 
     ``query`` [tokens][Hq][D] bf16 holds every sequence's chunk back to back,
@@ -415,13 +416,17 @@ def prefill(query, key_cache, value_cache, block_tables, context_lens, query_sta
         out = torch.empty_like(query)
     elif out.shape != query.shape or out.dtype != query.dtype:
         raise ValueError("out must match query")
+    need = int(lib().pa_prefill_workspace_bytes())
+    if workspace is None:
+        workspace = torch.empty(need, dtype=torch.uint8, device=query.device)
     rc = lib().pa_prefill(
         _dev(out, "out"), _dev(query, "query"), _dev(key_cache, "key_cache"),
         _dev(value_cache, "value_cache"), _dev(block_tables, "block_tables", torch.int32),
         _dev(context_lens, "context_lens", torch.int32),
         _dev(query_start, "query_start", torch.int32), B, Hq, Hkv, D, BLOCK_SIZE,
         block_tables.shape[1], NB, N, int(max_query_len), float(scale), _lib.PA_DTYPE_BF16,
-        int(window), _status_ptr(status), _stream(stream, query.device))
+        int(window), _dev(workspace, "workspace"), workspace.numel() * workspace.element_size(),
+        _status_ptr(status), _stream(stream, query.device))
     check(rc, "pa_prefill")
     return out
 

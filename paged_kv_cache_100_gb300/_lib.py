@@ -51,8 +51,9 @@ SIGNATURES = {
     "pa_decode_sliding_window": (i32, [vp, vp, vp, vp, vp, vp, vp, vp, i32, i32, i32, i32, i32,
                                        i32, i32, f32, i32, i32, i32, vp, sz, vp, vp]),
     "pa_cache_write_fp8": (i32, [vp, vp, vp, vp, vp, vp, vp, i32, i32, i32, i32, i32, vp, vp]),
+    "pa_prefill_workspace_bytes": (sz, []),
     "pa_prefill": (i32, [vp, vp, vp, vp, vp, vp, vp, i32, i32, i32, i32, i32, i32, i32, i32, i32,
-                         f32, i32, i32, vp, vp]),
+                         f32, i32, i32, vp, sz, vp, vp]),
     "pa_swap_bytes": (sz, [i32, i32, i32, i32]),
     "pa_swap_out": (i32, [vp, vp, vp, i32, vp, i32, i32, i32, i32, i32, vp, vp]),
     "pa_swap_in": (i32, [vp, vp, vp, i32, vp, i32, i32, i32, i32, i32, vp, vp]),

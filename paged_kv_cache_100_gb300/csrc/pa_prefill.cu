@@ -71,13 +71,14 @@ constexpr int kThreads = 64 + kQT * kGroup;
 #endif
 constexpr int kStages = PA_PREFILL_STAGES;   // depth of the K and V rings
 constexpr float kRescaleLog2 = 8.0f;     // lazy rescale threshold (factor 256)
+constexpr size_t kPrefillWorkspaceBytes = 256;   // the ticket counter (rounded up)
 
 // shared memory map (offsets from the 1024-byte aligned dynamic base)
 constexpr int kOffQ = 0;                          // kQT tiles
 constexpr int kOffK = kOffQ + kQT * kTile;        // kStages tiles
 constexpr int kOffV = kOffK + kStages * kTile;    // kStages tiles
 constexpr int kOffBar = kOffV + kStages * kTile;
-constexpr int kNumBars = 4 * kStages + 8;
+constexpr int kNumBars = 4 * kStages + 15;
 constexpr int kOffRed = kOffBar + 256;            // [kQT][2 parities][kSplit][128] floats
 constexpr int kSmemBytes = kOffRed + kQT * 2 * kSplit * kRows * 4;
 // The tiles need 1024-byte alignment; the dynamic shared memory of a kernel
@@ -87,9 +88,12 @@ constexpr int kSmemBytes = kOffRed + kQT * 2 * kSplit * kRows * 4;
 // barrier indices
 constexpr int kQFull = 0, kKFull = 1, kKEmpty = kKFull + kStages, kVFull = kKEmpty + kStages,
               kVEmpty = kVFull + kStages, kSFull = kVEmpty + kStages, kPFull = kSFull + kQT,
-              kPvDone = kPFull + kQT, kDrain = kPvDone + kQT;
+              kPvDone = kPFull + kQT, kOFree = kPvDone + kQT, kItemFull = kOFree + kQT,
+              kItemEmpty = kItemFull + 2, kQFree = kItemEmpty + 2, kDrain = kQFree + 1;
 static_assert(kDrain + 1 == kNumBars, "barrier count");
-static_assert(kNumBars * 8 + 16 <= 256, "barrier block");
+// barriers, then the TMEM slot, the failure flag, the prefix-mode context bound
+// and the two-entry item queue
+static_assert(kNumBars * 8 + 20 <= 256, "barrier block");
 static_assert(kSmemBytes <= 227 * 1024, "shared memory");
 
 // TMEM columns: S_A, S_B, then O_A, O_B.
@@ -126,6 +130,11 @@ struct PrefillArgs {
     int staged;
     const float *k_scales;
     const float *v_scales;
+    // items: n_mt pair tiles per (sequence or prefix chunk, KV head); prefill
+    // CTAs take them from *work_counter (zero at launch) up to num_items
+    int n_mt;
+    int num_items;
+    unsigned int *work_counter;
 };
 
 namespace {
@@ -162,13 +171,100 @@ __device__ __forceinline__ void named_sync(int id) {
     asm volatile("bar.sync %0, %1;" ::"r"(id), "n"(kGroup) : "memory");
 }
 
-// kPrefix = false: chunked prefill.  CTA (pair tile, KV head, sequence): 256
+// The work of one CTA step ("item"): two 128-row Q tiles of one KV head
+// against a range of positions.
+struct Item {
+    int b;          // sequence whose table (and chunk, prefill) the item reads
+    int kvh;
+    int q0, T, C;   // first query row of the chunk, its tokens, context before it
+    int t0;         // first token (prefix mode: sequence) of tile A
+    int kv_lo, kv_hi, blk_lo, blk_hi, n_tiles;
+    int zidx;       // prefix mode: chunk index (partial row)
+    bool has_b;
+};
+
+// kPrefix = false: chunked prefill.  Item (pair tile, KV head, sequence): 256
 // (token, head) rows of one sequence's chunk, causal over its own table.
-// kPrefix = true: the shared prefix of a decode batch.  CTA (pair tile, KV
+// Items are numbered pair-tile fastest (the last, longest tile of a (sequence,
+// KV head) first), so that CTAs working at the same time share K/V in L2.
+// kPrefix = true: the shared prefix of a decode batch.  Item (pair tile, KV
 // head, prefix chunk): 256 (sequence, head) rows across sequences against one
 // chunk of the blocks every table starts with (read from the first table);
 // each row sees the chunk's positions below its own context length, and the
 // CTA writes split-K partials instead of outputs.
+template <bool kPrefix>
+__device__ __forceinline__ bool describe_item(const PrefillArgs &a, int item, int kv_hi_cap,
+                                              bool report_errors, Item &d) {
+    const int g = a.group;
+    const int tok_per_tile = kRows / g;
+    const int lmax = a.max_blocks * kBlockSize;
+    if constexpr (!kPrefix) {
+        const int x = item % a.n_mt;
+        const int rest = item / a.n_mt;
+        d.kvh = rest % a.num_kv_heads;
+        d.b = rest / a.num_kv_heads;
+        const int mt = a.n_mt - 1 - x;
+        d.q0 = a.query_start[d.b];
+        d.T = a.query_start[d.b + 1] - d.q0;
+        const int L = a.context_lens[d.b];
+        if (d.T < 0 || d.T > L || L > lmax) {
+            if (report_errors && x == 0 && d.kvh == 0) report(a.status, PA_DEV_BAD_CONTEXT_LEN);
+            return false;
+        }
+        if (report_errors && d.T > a.max_query_len && x == 0 && d.kvh == 0)
+            report(a.status, PA_DEV_BAD_QUERY_LEN);
+        d.t0 = mt * kQT * tok_per_tile;
+        if (d.t0 >= d.T) return false;
+        d.C = L - d.T;
+        const int last_tok = min(d.T, d.t0 + kQT * tok_per_tile) - 1;
+        d.kv_hi = d.C + last_tok + 1;
+        d.kv_lo = a.window > 0 ? max(0, d.C + d.t0 + 1 - a.window) : 0;
+        d.blk_lo = d.kv_lo / kBlockSize;
+        d.blk_hi = (d.kv_hi + kBlockSize - 1) / kBlockSize;
+        d.zidx = 0;
+    } else {
+        const int x = item % a.n_mt;
+        const int rest = item / a.n_mt;
+        d.kvh = rest % a.num_kv_heads;
+        d.zidx = rest / a.num_kv_heads;
+        d.b = 0;                                          // the shared blocks: first table
+        d.q0 = 0;
+        d.T = a.num_seqs;                                 // "tokens" are the sequences
+        d.C = 0;
+        d.t0 = x * kQT * tok_per_tile;
+        d.blk_lo = d.zidx * a.chunk_blocks;
+        d.blk_hi = min(a.prefix_blocks, d.blk_lo + a.chunk_blocks);
+        d.kv_lo = d.blk_lo * kBlockSize;
+        // positions past every row's context are never attended: their V rows
+        // are zeroed like a context's tail
+        d.kv_hi = max(d.kv_lo, min(d.blk_hi * kBlockSize, kv_hi_cap));
+    }
+    d.has_b = d.t0 + tok_per_tile < d.T;
+    d.n_tiles = (d.blk_hi - d.blk_lo + 7) / 8;
+    return true;
+}
+
+// AND of `v` over the kGroup threads of softmax group x (named barrier 3 + x).
+__device__ __forceinline__ bool group_all(int x, bool v) {
+    uint32_t r;
+    asm volatile(
+        "{\n\t.reg .pred p, q;\n\tsetp.ne.u32 p, %1, 0;\n\t"
+        "bar.red.and.pred q, %2, %3, p;\n\tselp.u32 %0, 1, 0, q;\n\t}"
+        : "=r"(r)
+        : "r"((uint32_t)v), "r"(3 + x), "n"(kGroup)
+        : "memory");
+    return r != 0;
+}
+
+// A persistent CTA (one per SM) works through items.  Prefill takes them in
+// order from a ticket counter (a.work_counter, zero at launch), so CTAs that
+// finish early take more; prefix mode has one item per CTA (its block index,
+// known to every warp).  In prefill the producer warp fetches the next item
+// while the current one runs and passes it to the other warps through a
+// two-entry queue in shared memory;
+// every barrier phase is counted across items, so the next item's Q and K/V
+// loads and its first QK^T products start while the last P.V products and the
+// output of the item before are still in flight.
 template <bool kPrefix>
 __global__ void __launch_bounds__(kThreads, 1)
     pa_attn_tc_kernel(const __grid_constant__ CUtensorMap qmap,
@@ -176,46 +272,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                       const __grid_constant__ CUtensorMap vmap, const PrefillArgs a) {
     grid_dependency_wait();
     grid_dependents_launch();
-    const int kvh = blockIdx.y;
     const int g = a.group;
     const int tok_per_tile = kRows / g;
     const int lmax = a.max_blocks * kBlockSize;
-    // b: sequence whose table and chunk (prefill) this CTA serves; q0 + t0:
-    // query row (token, or sequence in prefix mode) of tile A's first group
-    int b, q0, T, C, t0, kv_lo, kv_hi, blk_lo, blk_hi;
-    if constexpr (!kPrefix) {
-        b = blockIdx.z;
-        const int mt = gridDim.x - 1 - blockIdx.x;   // later (longer) tiles first
-        q0 = a.query_start[b];
-        T = a.query_start[b + 1] - q0;
-        const int L = a.context_lens[b];
-        if (T < 0 || T > L || L > lmax) {
-            if (blockIdx.x == 0 && kvh == 0 && threadIdx.x == 0) report(a.status, PA_DEV_BAD_CONTEXT_LEN);
-            return;
-        }
-        if (T > a.max_query_len && blockIdx.x == 0 && kvh == 0 && threadIdx.x == 0)
-            report(a.status, PA_DEV_BAD_QUERY_LEN);
-        t0 = mt * kQT * tok_per_tile;                 // first token of tile A
-        if (t0 >= T) return;
-        C = L - T;
-        const int last_tok = min(T, t0 + kQT * tok_per_tile) - 1;
-        kv_hi = C + last_tok + 1;
-        kv_lo = a.window > 0 ? max(0, C + t0 + 1 - a.window) : 0;
-        blk_lo = kv_lo / kBlockSize;
-        blk_hi = (kv_hi + kBlockSize - 1) / kBlockSize;
-    } else {
-        b = 0;                                         // the shared blocks: first table
-        q0 = 0;
-        T = a.num_seqs;                                // "tokens" are the sequences
-        C = 0;
-        t0 = blockIdx.x * kQT * tok_per_tile;
-        blk_lo = blockIdx.z * a.chunk_blocks;
-        blk_hi = min(a.prefix_blocks, blk_lo + a.chunk_blocks);
-        kv_lo = blk_lo * kBlockSize;
-        kv_hi = blk_hi * kBlockSize;                   // lowered below to the rows' longest context
-    }
-    const bool has_b = t0 + tok_per_tile < T;
-    const int n_tiles = (blk_hi - blk_lo + 7) / 8;
 
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     if (smem_u32(smem_raw) & 1023u) {
@@ -229,11 +288,14 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint64_t *bars = reinterpret_cast<uint64_t *>(base + kOffBar);
     uint32_t *tslot = reinterpret_cast<uint32_t *>(base + kOffBar + kNumBars * 8);
     volatile int *fail = reinterpret_cast<volatile int *>(base + kOffBar + kNumBars * 8 + 4);
+    int *s_maxl = reinterpret_cast<int *>(base + kOffBar + kNumBars * 8 + 8);
+    volatile int *s_item = reinterpret_cast<volatile int *>(base + kOffBar + kNumBars * 8 + 12);  // [2]
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
     if (threadIdx.x == 0) {
         mbar_init(&bars[kQFull], 1);
+        mbar_init(&bars[kQFree], 1);
         for (int s = 0; s < kStages; ++s) {
             mbar_init(&bars[kKFull + s], 1);
             mbar_init(&bars[kKEmpty + s], 1);
@@ -244,95 +306,147 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_init(&bars[kSFull + x], 1);
             mbar_init(&bars[kPFull + x], kGroup);
             mbar_init(&bars[kPvDone + x], 1);
+            mbar_init(&bars[kOFree + x], kGroup);
+        }
+        for (int q = 0; q < 2; ++q) {
+            mbar_init(&bars[kItemFull + q], 1);
+            mbar_init(&bars[kItemEmpty + q], 1 + kQT * kGroup);
         }
         mbar_init(&bars[kDrain], 1);
         *fail = 0;
+        *s_maxl = 0;
         fence_mbar_init();
         tma_prefetch_desc(&qmap);
         tma_prefetch_desc(&kmap);
         tma_prefetch_desc(&vmap);
     }
     if constexpr (kPrefix) {
-        // positions past every row's context are never attended: their V rows
-        // are zeroed like a context's tail (kv_hi = longest context, clipped)
-        int *s_maxl = reinterpret_cast<int *>(base + kOffBar + kNumBars * 8 + 8);
-        if (threadIdx.x == 0) *s_maxl = 0;
+        // this CTA's one item: the longest context among its rows bounds the
+        // positions attended, and (KV head 0) every sequence of these rows
+        // must list the chunk's blocks
         __syncthreads();
-        const int nseq = min(T - t0, kQT * tok_per_tile);
+        const int kvh = blockIdx.y;
+        const int t0 = blockIdx.x * kQT * tok_per_tile;
+        const int nseq = min(a.num_seqs - t0, kQT * tok_per_tile);
         for (int i = threadIdx.x; i < nseq; i += kThreads) {
             int L = a.context_lens[t0 + i];
             L = L < 0 ? 0 : (L > lmax ? lmax : L);
             atomicMax(s_maxl, L);
         }
-        // every sequence of these rows must list the chunk's blocks (checked
-        // by the CTAs of KV head 0)
         if (kvh == 0) {
-            const int nblk = blk_hi - blk_lo;
+            const int blk_lo = blockIdx.z * a.chunk_blocks;
+            const int nblk = min(a.prefix_blocks, blk_lo + a.chunk_blocks) - blk_lo;
             for (int i = threadIdx.x; i < nseq * nblk; i += kThreads) {
                 const int sq = t0 + i / nblk, jb = blk_lo + i % nblk;
                 if (a.block_tables[(size_t)sq * a.max_blocks + jb] != a.block_tables[jb])
                     report(a.status, PA_DEV_PREFIX_MISMATCH);
             }
         }
-        __syncthreads();
-        kv_hi = max(kv_lo, min(kv_hi, *s_maxl));
     }
     if (warp == 1) tmem_alloc(tslot, kTmemCols);
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = *tslot;
+    const int kv_hi_cap = kPrefix ? *s_maxl : 0;
 
     if (warp == 0) {
-        // ---------------- TMA producer ----------------
+        // ---------------- TMA producer (and item fetch) ----------------
         if (lane == 0) {
-            const int nq = has_b ? kQT : 1;
-            mbar_arrive_expect_tx(&bars[kQFull], nq * kTile);
-            for (int x = 0; x < nq; ++x) {
-                const int row0 = q0 + t0 + x * tok_per_tile;
-                tma_load_4d(sQ + x * kTile, &qmap, 0, 0, kvh, row0, &bars[kQFull]);
-                tma_load_4d(sQ + x * kTile + kHalf, &qmap, 64, 0, kvh, row0, &bars[kQFull]);
-            }
-            const int32_t *trow = a.block_tables + (size_t)b * a.max_blocks;
-            int issued_k = 0, issued_v = 0;
-            for (int j = 0; j < n_tiles; ++j) {
-                const int s = j % kStages;
-                const uint32_t ph = (uint32_t)(j / kStages) & 1u;   // this use of stage s
-                const int blk0 = blk_lo + 8 * j;
-                const int nb = min(8, blk_hi - blk0);
-                int rows[8];
-                for (int i = 0; i < nb; ++i) {
-                    int phys = a.staged ? blk0 + i : trow[blk0 + i];
-                    if ((unsigned)phys >= (unsigned)a.num_blocks) {
-                        report(a.status, PA_DEV_BAD_BLOCK_ID);
-                        phys = 0;
+            int item_issued = -1;                   // items whose Q load was issued
+            uint32_t issued_k = 0, issued_v = 0;    // K/V steps issued (global count)
+            uint32_t gstep = 0;                     // K/V steps of earlier items
+            bool ok = true;
+            bool first = true;
+            for (int it = 0;; ++it) {
+                // next non-empty item, or -1
+                int item = -1;
+                Item d;
+                if constexpr (kPrefix) {
+                    if (first) {
+                        item = blockIdx.x + gridDim.x * (blockIdx.y + gridDim.y * blockIdx.z);
+                        describe_item<true>(a, item, kv_hi_cap, true, d);
                     }
-                    rows[i] = (phys * a.num_kv_heads + kvh) * kBlockSize;
+                } else {
+                    for (;;) {
+                        const int t = (int)atomicAdd(a.work_counter, 1u);
+                        if (t >= a.num_items) break;
+                        if (describe_item<false>(a, t, 0, true, d)) {
+                            item = t;
+                            break;
+                        }
+                    }
                 }
-                if (j >= kStages && !wait_or_fail(&bars[kKEmpty + s], ph ^ 1u, fail, a.status))
-                    break;
-                uint8_t *kd = sK + s * kTile;
-                mbar_arrive_expect_tx(&bars[kKFull + s], nb * 4096);
-                for (int i = 0; i < nb; ++i) {
-                    tma_load_2d(kd + i * 2048, &kmap, 0, rows[i], &bars[kKFull + s]);
-                    tma_load_2d(kd + kHalf + i * 2048, &kmap, 64, rows[i], &bars[kKFull + s]);
+                first = false;
+                if (!ok) item = -1;
+                if constexpr (!kPrefix) {
+                    // prefix mode has no queue: every warp knows its one item
+                    const int slot = it & 1;
+                    if (it >= 2 && !wait_or_fail(&bars[kItemEmpty + slot], ((it >> 1) - 1) & 1, fail, a.status))
+                        item = -1;
+                    s_item[slot] = item;
+                    mbar_arrive(&bars[kItemFull + slot]);
                 }
-                issued_k = j + 1;
-                if (j >= kStages && !wait_or_fail(&bars[kVEmpty + s], ph ^ 1u, fail, a.status))
-                    break;
-                uint8_t *vd = sV + s * kTile;
-                mbar_arrive_expect_tx(&bars[kVFull + s], nb * 4096);
-                for (int i = 0; i < nb; ++i) {
-                    tma_load_2d(vd + i * 2048, &vmap, 0, rows[i], &bars[kVFull + s]);
-                    tma_load_2d(vd + kHalf + i * 2048, &vmap, 64, rows[i], &bars[kVFull + s]);
+                if (item < 0) break;
+                // Q (both tiles) once the last QK^T of the item before has run
+                if (it >= 1 && !wait_or_fail(&bars[kQFree], (it - 1) & 1, fail, a.status)) {
+                    ok = false;
+                    continue;
                 }
-                issued_v = j + 1;
+                const int nq = d.has_b ? kQT : 1;
+                mbar_arrive_expect_tx(&bars[kQFull], nq * kTile);
+                for (int x = 0; x < nq; ++x) {
+                    const int row0 = d.q0 + d.t0 + x * tok_per_tile;
+                    tma_load_4d(sQ + x * kTile, &qmap, 0, 0, d.kvh, row0, &bars[kQFull]);
+                    tma_load_4d(sQ + x * kTile + kHalf, &qmap, 64, 0, d.kvh, row0, &bars[kQFull]);
+                }
+                item_issued = it;
+                const int32_t *trow = a.block_tables + (size_t)d.b * a.max_blocks;
+                for (int j = 0; ok && j < d.n_tiles; ++j) {
+                    const uint32_t gs = gstep + j;
+                    const int s = gs % kStages;
+                    const uint32_t ph = (gs / kStages) & 1u;   // this use of stage s
+                    const int blk0 = d.blk_lo + 8 * j;
+                    const int nb = min(8, d.blk_hi - blk0);
+                    int rows[8];
+                    for (int i = 0; i < nb; ++i) {
+                        int phys = a.staged ? blk0 + i : trow[blk0 + i];
+                        if ((unsigned)phys >= (unsigned)a.num_blocks) {
+                            report(a.status, PA_DEV_BAD_BLOCK_ID);
+                            phys = 0;
+                        }
+                        rows[i] = (phys * a.num_kv_heads + d.kvh) * kBlockSize;
+                    }
+                    if (gs >= kStages && !wait_or_fail(&bars[kKEmpty + s], ph ^ 1u, fail, a.status)) {
+                        ok = false;
+                        break;
+                    }
+                    uint8_t *kd = sK + s * kTile;
+                    mbar_arrive_expect_tx(&bars[kKFull + s], nb * 4096);
+                    for (int i = 0; i < nb; ++i) {
+                        tma_load_2d(kd + i * 2048, &kmap, 0, rows[i], &bars[kKFull + s]);
+                        tma_load_2d(kd + kHalf + i * 2048, &kmap, 64, rows[i], &bars[kKFull + s]);
+                    }
+                    issued_k = gs + 1;
+                    if (gs >= kStages && !wait_or_fail(&bars[kVEmpty + s], ph ^ 1u, fail, a.status)) {
+                        ok = false;
+                        break;
+                    }
+                    uint8_t *vd = sV + s * kTile;
+                    mbar_arrive_expect_tx(&bars[kVFull + s], nb * 4096);
+                    for (int i = 0; i < nb; ++i) {
+                        tma_load_2d(vd + i * 2048, &vmap, 0, rows[i], &bars[kVFull + s]);
+                        tma_load_2d(vd + kHalf + i * 2048, &vmap, 64, rows[i], &bars[kVFull + s]);
+                    }
+                    issued_v = gs + 1;
+                }
+                gstep += d.n_tiles;
             }
             // drain: no copy of ours may still be landing when the CTA leaves
-            (void)mbar_wait_bounded(&bars[kQFull], 0);
-            for (int j = max(0, issued_k - kStages); j < issued_k; ++j)
+            if (item_issued >= 0) (void)mbar_wait_bounded(&bars[kQFull], item_issued & 1);
+            for (uint32_t j = issued_k > kStages ? issued_k - kStages : 0; j < issued_k; ++j)
                 (void)mbar_wait_bounded(&bars[kKFull + j % kStages], (j / kStages) & 1);
-            for (int j = max(0, issued_v - kStages); j < issued_v; ++j)
+            for (uint32_t j = issued_v > kStages ? issued_v - kStages : 0; j < issued_v; ++j)
                 (void)mbar_wait_bounded(&bars[kVFull + j % kStages], (j / kStages) & 1);
         }
     } else if (warp == 1) {
@@ -341,10 +455,12 @@ __global__ void __launch_bounds__(kThreads, 1)
             constexpr uint32_t idS = idesc_bf16_f32(kRows, kKv, false);
             constexpr uint32_t idPV = idesc_bf16_f32(kRows, kD, true);
             const uint32_t q_u = smem_u32(sQ), k_u = smem_u32(sK), v_u = smem_u32(sV);
-            bool ok = wait_or_fail(&bars[kQFull], 0, fail, a.status);
-            auto issue_s = [&](int x, int j) {
+            uint32_t gstep = 0;
+            uint32_t pcount[kQT] = {0, 0};   // P phases per Q tile (global)
+            bool ok = true;
+            auto issue_s = [&](int x, uint32_t gs) {
                 const uint32_t qb = q_u + x * kTile;
-                const uint32_t kb = k_u + (j % kStages) * kTile;
+                const uint32_t kb = k_u + (gs % kStages) * kTile;
 #pragma unroll
                 for (int k = 0; k < 8; ++k) {
                     const uint32_t o = (k >> 2) * kHalf + (k & 3) * 32;
@@ -356,10 +472,15 @@ __global__ void __launch_bounds__(kThreads, 1)
             // P of tokens [16k, 16k + 16) sits in the 32-column chunk k / 2 of
             // the S buffer: head pairs from column 32 (k / 2) + 8 (k % 2),
             // residual pairs 16 columns further
-            auto issue_pv = [&](int x, int j) -> bool {
-                if (!wait_or_fail(&bars[kPFull + x], j & 1, fail, a.status)) return false;
+            auto issue_pv = [&](int x, uint32_t gs, int j, int it) -> bool {
+                if (!wait_or_fail(&bars[kPFull + x], pcount[x] & 1, fail, a.status)) return false;
+                ++pcount[x];
+                // the first P.V of an item overwrites O: the item before must
+                // have read it out
+                if (j == 0 && it >= 1 && !wait_or_fail(&bars[kOFree + x], (it - 1) & 1, fail, a.status))
+                    return false;
                 tc_fence_after();
-                const uint32_t vb = v_u + (j % kStages) * kTile;
+                const uint32_t vb = v_u + (gs % kStages) * kTile;
 #pragma unroll
                 for (int k = 0; k < 8; ++k) {
                     const uint32_t pc = tmem + col_s(x) + 32 * (k >> 1) + 8 * (k & 1);
@@ -370,253 +491,305 @@ __global__ void __launch_bounds__(kThreads, 1)
                 umma_commit(&bars[kPvDone + x]);
                 return true;
             };
-            if (ok && wait_or_fail(&bars[kKFull], 0, fail, a.status)) {
+            for (int it = 0; ok; ++it) {
+                int item;
+                if constexpr (kPrefix) {
+                    item = it == 0 ? (int)(blockIdx.x + gridDim.x * (blockIdx.y + gridDim.y * blockIdx.z)) : -1;
+                } else {
+                    const int slot = it & 1;
+                    if (!wait_or_fail(&bars[kItemFull + slot], (it >> 1) & 1, fail, a.status)) break;
+                    item = s_item[slot];
+                    mbar_arrive(&bars[kItemEmpty + slot]);
+                }
+                if (item < 0) break;
+                Item d;
+                describe_item<kPrefix>(a, item, kv_hi_cap, false, d);
+                const int n = d.n_tiles;
+                if (!wait_or_fail(&bars[kQFull], it & 1, fail, a.status) ||
+                    !wait_or_fail(&bars[kKFull + gstep % kStages], (gstep / kStages) & 1, fail, a.status))
+                    break;
                 tc_fence_after();
-                issue_s(0, 0);
-                if (has_b) issue_s(1, 0);
-                umma_commit(&bars[kKEmpty]);
-            } else {
-                ok = false;
-            }
-            for (int j = 0; ok && j < n_tiles; ++j) {
-                const int sv = j % kStages;
-                const bool more = j + 1 < n_tiles;
-                const int sk = (j + 1) % kStages;
-                if (!wait_or_fail(&bars[kVFull + sv], (j / kStages) & 1, fail, a.status)) break;
-                if (!issue_pv(0, j)) break;
-                if (more) {
-                    if (!wait_or_fail(&bars[kKFull + sk], ((j + 1) / kStages) & 1, fail, a.status))
+                issue_s(0, gstep);
+                if (d.has_b) issue_s(1, gstep);
+                umma_commit(&bars[kKEmpty + gstep % kStages]);
+                if (n == 1) umma_commit(&bars[kQFree]);
+                for (int j = 0; ok && j < n; ++j) {
+                    const uint32_t gs = gstep + j, gk = gs + 1;
+                    const bool more = j + 1 < n;
+                    if (!wait_or_fail(&bars[kVFull + gs % kStages], (gs / kStages) & 1, fail, a.status) ||
+                        !issue_pv(0, gs, j, it)) {
+                        ok = false;
                         break;
-                    tc_fence_after();
-                    issue_s(0, j + 1);
+                    }
+                    if (more) {
+                        if (!wait_or_fail(&bars[kKFull + gk % kStages], (gk / kStages) & 1, fail, a.status)) {
+                            ok = false;
+                            break;
+                        }
+                        tc_fence_after();
+                        issue_s(0, gk);
+                    }
+                    if (d.has_b && !issue_pv(1, gs, j, it)) {
+                        ok = false;
+                        break;
+                    }
+                    umma_commit(&bars[kVEmpty + gs % kStages]);
+                    if (more) {
+                        if (d.has_b) issue_s(1, gk);
+                        umma_commit(&bars[kKEmpty + gk % kStages]);
+                        if (j + 2 == n) umma_commit(&bars[kQFree]);   // the item's last QK^T is issued
+                    }
                 }
-                if (has_b && !issue_pv(1, j)) break;
-                umma_commit(&bars[kVEmpty + sv]);
-                if (more) {
-                    if (has_b) issue_s(1, j + 1);
-                    umma_commit(&bars[kKEmpty + sk]);
-                }
-            }
-            // every MMA issued above has completed once kDrain flips
-            umma_commit(&bars[kDrain]);
-            if (!mbar_wait_bounded(&bars[kDrain], 0)) {
-                *fail = 1;
-                report(a.status, PA_DEV_TIMEOUT);
+                // every MMA of this item has completed once kDrain flips
+                umma_commit(&bars[kDrain]);
+                gstep += n;
             }
         }
     } else {
         // ---------------- softmax groups ----------------
         const int x = (warp - 2) / (kGroup / 32);     // Q tile of this group
         const int gw = (warp - 2) % (kGroup / 32);    // warp within the group
-        if (x == 0 || has_b) {
-            const int quarter = warp & 3;
-            const int part = gw >> 2;                     // columns [kCols * part, + kCols)
-            const int r = quarter * 32 + lane;            // tile row = TMEM lane
-            const int tx0 = t0 + x * tok_per_tile;        // first token (sequence) of this tile
-            const int ntok = max(0, min(tok_per_tile, T - tx0));
-            const int tr = r / g;
-            const bool real = tr < ntok;
-            // this row attends to positions [wlo, qpos]; a 32-column chunk
-            // needs no mask when it lies inside [qpos_lo_win, qpos_lo] for
-            // every row of the tile
-            int qpos, qpos_lo, qpos_hi, wlo;
-            if constexpr (!kPrefix) {
-                qpos = C + tx0 + min(tr, max(ntok, 1) - 1);
-                qpos_lo = C + tx0;
-                qpos_hi = C + tx0 + max(ntok, 1) - 1;
-                wlo = a.window > 0 ? qpos + 1 - a.window : INT_MIN;
+        const int quarter = warp & 3;
+        const int part = gw >> 2;                     // columns [kCols * part, + kCols)
+        const int r = quarter * 32 + lane;            // tile row = TMEM lane
+        const int tr = r / g;
+        const uint32_t lane_off = ((uint32_t)(quarter * 32) << 16) + part * kCols;
+        const uint32_t s_base = tmem + col_s(x) + lane_off;
+        const uint32_t o_base = tmem + col_o(x) + lane_off;
+        float *red = reinterpret_cast<float *>(base + kOffRed) + x * 2 * kSplit * kRows;
+        uint32_t sc = 0;      // S / P / P.V phases of this group (global)
+        uint32_t ex = 0;      // exchanges through `red` (their slot alternates)
+        uint32_t gstep = 0;   // K/V steps of earlier items
+        bool ok = true;
+        for (int it = 0;; ++it) {
+            int item;
+            if constexpr (kPrefix) {
+                item = it == 0 ? (int)(blockIdx.x + gridDim.x * (blockIdx.y + gridDim.y * blockIdx.z)) : -1;
             } else {
-                int L = real ? a.context_lens[tx0 + tr] : 0;
-                L = L < 0 ? 0 : (L > lmax ? lmax : L);
-                qpos = min(L, blk_hi * kBlockSize) - 1;   // last attended position
-                qpos_lo = -1;                              // always mask (short kernel)
-                qpos_hi = 0;
-                wlo = INT_MIN;
+                const int slot = it & 1;
+                const bool got_item = warp_wait(&bars[kItemFull + slot], (it >> 1) & 1, fail, a.status);
+                item = got_item ? s_item[slot] : -1;
+                mbar_arrive(&bars[kItemEmpty + slot]);
             }
-            const uint32_t lane_off = ((uint32_t)(quarter * 32) << 16) + part * kCols;
-            const uint32_t s_base = tmem + col_s(x) + lane_off;
-            const uint32_t o_base = tmem + col_o(x) + lane_off;
-            float *red = reinterpret_cast<float *>(base + kOffRed) + x * 2 * kSplit * kRows;
-            const float sl2 = a.k_scales != nullptr ? a.scale_log2 * a.k_scales[kvh] : a.scale_log2;
-            float m_used = -INFINITY, l = 0.f;
-            // Every thread of the group runs every iteration and reaches the
-            // named barrier the same number of times, even after a wait gave up
-            // (then it only skips the work), so that no barrier waits forever.
-            bool ok = true;
-            for (int j = 0; j < n_tiles; ++j) {
-                const bool got = ok && warp_wait(&bars[kSFull + x], j & 1, fail, a.status);
-                const int k0 = (blk_lo + 8 * j) * kBlockSize + part * kCols;   // column 0's position
-                // pass 1: row maximum over this thread's columns
-                float mx4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
-                if (got) {
-                    tc_fence_after();
+            // every thread of the group takes the same decision, so that all of
+            // them reach the group's named barriers equally often
+            if (!group_all(x, item >= 0 && ok && !*fail)) break;
+            Item d;
+            describe_item<kPrefix>(a, item, kv_hi_cap, false, d);
+            const int n_tiles = d.n_tiles;
+            if (x == 0 || d.has_b) {
+                const float sl2k = a.k_scales != nullptr ? a.scale_log2 * a.k_scales[d.kvh] : a.scale_log2;
+                const int tx0 = d.t0 + x * tok_per_tile;      // first token (sequence) of this tile
+                const int ntok = max(0, min(tok_per_tile, d.T - tx0));
+                const bool real = tr < ntok;
+                // this row attends to positions [wlo, qpos]; a 32-column chunk
+                // needs no mask when it lies inside [qpos_lo_win, qpos_lo] for
+                // every row of the tile
+                int qpos, qpos_lo, qpos_hi, wlo;
+                if constexpr (!kPrefix) {
+                    qpos = d.C + tx0 + min(tr, max(ntok, 1) - 1);
+                    qpos_lo = d.C + tx0;
+                    qpos_hi = d.C + tx0 + max(ntok, 1) - 1;
+                    wlo = a.window > 0 ? qpos + 1 - a.window : INT_MIN;
+                } else {
+                    int L = real ? a.context_lens[tx0 + tr] : 0;
+                    L = L < 0 ? 0 : (L > lmax ? lmax : L);
+                    qpos = min(L, d.blk_hi * kBlockSize) - 1;   // last attended position
+                    qpos_lo = -1;                                // always mask (short kernel)
+                    qpos_hi = 0;
+                    wlo = INT_MIN;
+                }
+                float m_used = -INFINITY, l = 0.f;
+                // Every thread of the group runs every iteration and reaches the
+                // named barrier the same number of times, even after a wait gave
+                // up (then it only skips the work), so that no barrier waits forever.
+                for (int j = 0; j < n_tiles; ++j) {
+                    const bool got = ok && warp_wait(&bars[kSFull + x], sc & 1, fail, a.status);
+                    const int k0 = (d.blk_lo + 8 * j) * kBlockSize + part * kCols;   // column 0's position
+                    // pass 1: row maximum over this thread's columns
+                    float mx4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+                    if (got) {
+                        tc_fence_after();
+#pragma unroll 1
+                        for (int c = 0; c < kCols; c += 32) {
+                            uint32_t v[32];
+                            tmem_ld32(s_base + c, v);
+                            tmem_wait_ld();
+                            const int kc = k0 + c;
+                            if ((kc + 31 > qpos_lo) || (!kPrefix && a.window > 0 && kc < qpos_hi + 1 - a.window)) {
+#pragma unroll
+                                for (int i = 0; i < 32; ++i)
+                                    if (!(kc + i <= qpos && kc + i >= wlo)) v[i] = __float_as_uint(-INFINITY);
+                            }
+#pragma unroll
+                            for (int i = 0; i < 32; ++i) mx4[i & 3] = fmaxf(mx4[i & 3], __uint_as_float(v[i]));
+                        }
+                    }
+                    float mrow = fmaxf(fmaxf(mx4[0], mx4[1]), fmaxf(mx4[2], mx4[3]));
+                    const int rp = ex & 1;
+                    ++ex;
+                    red[(rp * kSplit + part) * kRows + r] = mrow;
+                    named_sync(1 + x);
+#pragma unroll
+                    for (int o = 1; o < kSplit; ++o)
+                        mrow = fmaxf(mrow, red[(rp * kSplit + ((part + o) % kSplit)) * kRows + r]);
+                    const uint32_t my_sc = sc++;
+                    if (!got) {
+                        ok = false;
+                        continue;
+                    }
+                    const float m_new = fmaxf(m_used, mrow * sl2k);
+                    // Lazy rescale: only rows whose maximum grew by more than 2^8
+                    // move their reference; the warp rescales O together (warp-wide
+                    // tensor-memory access, factor 1 on the other rows) once every
+                    // PV of this tile issued so far has landed.
+                    const bool need = m_new > m_used + kRescaleLog2;
+                    const float alpha = need ? exp2f(m_used - m_new) : 1.f;   // 0 while m_used is -inf
+                    if (j >= 1 && __any_sync(0xffffffffu, need)) {
+                        if (!warp_wait(&bars[kPvDone + x], (my_sc - 1) & 1, fail, a.status)) {
+                            ok = false;
+                            continue;
+                        }
+                        tc_fence_after();
+#pragma unroll 1
+                        for (int c = 0; c < kCols; c += 32) {
+                            uint32_t o[32];
+                            tmem_ld32(o_base + c, o);
+                            tmem_wait_ld();
+#pragma unroll
+                            for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * alpha);
+                            tmem_st32(o_base + c, o);
+                        }
+                        tmem_wait_st();
+                    }
+                    if (need) {
+                        l *= alpha;
+                        m_used = m_new;
+                    }
+                    const float m_ref = m_used == -INFINITY ? 0.f : m_used;
+                    // pass 2: P = 2^(s * scale_log2 - m_ref) as a bf16 head + bf16
+                    // residual, written over the same 32 columns it was read from
+                    // (head pairs in the first 16, residual pairs in the next 16)
+                    float ps4[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll 1
                     for (int c = 0; c < kCols; c += 32) {
                         uint32_t v[32];
                         tmem_ld32(s_base + c, v);
                         tmem_wait_ld();
                         const int kc = k0 + c;
-                        if ((kc + 31 > qpos_lo) || (!kPrefix && a.window > 0 && kc < qpos_hi + 1 - a.window)) {
+                        const bool masked =
+                            (kc + 31 > qpos_lo) || (!kPrefix && a.window > 0 && kc < qpos_hi + 1 - a.window);
+                        uint32_t hi[16], lo[16];
 #pragma unroll
-                            for (int i = 0; i < 32; ++i)
-                                if (!(kc + i <= qpos && kc + i >= wlo)) v[i] = __float_as_uint(-INFINITY);
+                        for (int i = 0; i < 32; i += 2) {
+                            float p0 = ex2_approx(fmaf(__uint_as_float(v[i]), sl2k, -m_ref));
+                            float p1 = ex2_approx(fmaf(__uint_as_float(v[i + 1]), sl2k, -m_ref));
+                            if (masked) {
+                                if (!(kc + i <= qpos && kc + i >= wlo)) p0 = 0.f;
+                                if (!(kc + i + 1 <= qpos && kc + i + 1 >= wlo)) p1 = 0.f;
+                            }
+                            ps4[(i >> 1) & 3] += p0 + p1;
+                            const uint32_t h = pack2_bf16(p0, p1);
+                            hi[i >> 1] = h;
+                            lo[i >> 1] = pack2_bf16(p0 - __uint_as_float(h << 16),
+                                                    p1 - __uint_as_float(h & 0xffff0000u));
                         }
-#pragma unroll
-                        for (int i = 0; i < 32; ++i) mx4[i & 3] = fmaxf(mx4[i & 3], __uint_as_float(v[i]));
+                        tmem_st16(s_base + c, hi);
+                        tmem_st16(s_base + c + 16, lo);
                     }
+                    tmem_wait_st();
+                    l += (ps4[0] + ps4[1]) + (ps4[2] + ps4[3]);
+                    // V rows of positions outside [kv_lo, kv_hi) may hold anything
+                    // (NaN included): tile A's group zeroes them (PV_B runs after
+                    // PV_A) so that 0 * row stays 0; each thread clears its share.
+                    const int k0_tile = (d.blk_lo + 8 * j) * kBlockSize;
+                    if (x == 0 && (k0_tile < d.kv_lo || k0_tile + kKv > d.kv_hi)) {
+                        const uint32_t gs = gstep + j;
+                        if (!warp_wait(&bars[kVFull + gs % kStages], (gs / kStages) & 1, fail, a.status)) {
+                            ok = false;
+                            continue;
+                        }
+                        const int kp = k0_tile + r;
+                        if (kp < d.kv_lo || kp >= d.kv_hi) {
+                            constexpr int kBytes = 256 / kSplit;
+                            const int b0 = part * kBytes;
+                            uint8_t *vrow = sV + (gs % kStages) * kTile + (b0 >> 7) * kHalf +
+                                            (r >> 3) * 1024 + (r & 7) * 128 + (b0 & 127);
+#pragma unroll
+                            for (int q = 0; q < kBytes / 16; ++q)
+                                *reinterpret_cast<uint4 *>(vrow + q * 16) = make_uint4(0, 0, 0, 0);
+                        }
+                    }
+                    fence_proxy_async_smem();
+                    tc_fence_before();
+                    mbar_arrive(&bars[kPFull + x]);
                 }
-                float mrow = fmaxf(fmaxf(mx4[0], mx4[1]), fmaxf(mx4[2], mx4[3]));
-                const int rp = j & 1;
-                red[(rp * kSplit + part) * kRows + r] = mrow;
+                // the row sum is the parts' sums (all against the same maximum),
+                // exchanged in the slots of the other parity
+                const int sx = ex & 1;
+                ++ex;
+                red[(sx * kSplit + part) * kRows + r] = l;
                 named_sync(1 + x);
+                float l_row = l;
 #pragma unroll
-                for (int o = 1; o < kSplit; ++o)
-                    mrow = fmaxf(mrow, red[(rp * kSplit + ((part + o) % kSplit)) * kRows + r]);
-                if (!got) {
-                    ok = false;
-                    continue;
-                }
-                const float m_new = fmaxf(m_used, mrow * sl2);
-                // Lazy rescale: only rows whose maximum grew by more than 2^8
-                // move their reference; the warp rescales O together (warp-wide
-                // tensor-memory access, factor 1 on the other rows) once every
-                // PV of this tile issued so far has landed.
-                const bool need = m_new > m_used + kRescaleLog2;
-                const float alpha = need ? exp2f(m_used - m_new) : 1.f;   // 0 while m_used is -inf
-                if (j >= 1 && __any_sync(0xffffffffu, need)) {
-                    if (!warp_wait(&bars[kPvDone + x], (j - 1) & 1, fail, a.status)) {
-                        ok = false;
-                        continue;
-                    }
+                for (int o = 1; o < kSplit; ++o) l_row += red[(sx * kSplit + ((part + o) % kSplit)) * kRows + r];
+                const bool drained = warp_wait(&bars[kDrain], it & 1, fail, a.status);
+                if (kPrefix && __all_sync(0xffffffffu, ok) && drained) {
+                    // split-K partial of this chunk: (max, sum) and the unnormalised
+                    // output, in the partial row of (sequence, head, chunk)
                     tc_fence_after();
+                    const size_t prow = ((size_t)(tx0 + tr) * a.num_q_heads + d.kvh * g + (r % g)) * a.max_parts +
+                                        d.zidx;
+                    const float vs = a.v_scales != nullptr ? a.v_scales[d.kvh] : 1.f;
 #pragma unroll 1
                     for (int c = 0; c < kCols; c += 32) {
                         uint32_t o[32];
                         tmem_ld32(o_base + c, o);
                         tmem_wait_ld();
+                        if (real) {
+                            float4 *dst = reinterpret_cast<float4 *>(a.part_o + prow * kD + part * kCols + c);
 #pragma unroll
-                        for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * alpha);
-                        tmem_st32(o_base + c, o);
-                    }
-                    tmem_wait_st();
-                }
-                if (need) {
-                    l *= alpha;
-                    m_used = m_new;
-                }
-                const float m_ref = m_used == -INFINITY ? 0.f : m_used;
-                // pass 2: P = 2^(s * scale_log2 - m_ref) as a bf16 head + bf16
-                // residual, written over the same 32 columns it was read from
-                // (head pairs in the first 16, residual pairs in the next 16)
-                float ps4[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll 1
-                for (int c = 0; c < kCols; c += 32) {
-                    uint32_t v[32];
-                    tmem_ld32(s_base + c, v);
-                    tmem_wait_ld();
-                    const int kc = k0 + c;
-                    const bool masked =
-                        (kc + 31 > qpos_lo) || (!kPrefix && a.window > 0 && kc < qpos_hi + 1 - a.window);
-                    uint32_t hi[16], lo[16];
-#pragma unroll
-                    for (int i = 0; i < 32; i += 2) {
-                        float p0 = ex2_approx(fmaf(__uint_as_float(v[i]), sl2, -m_ref));
-                        float p1 = ex2_approx(fmaf(__uint_as_float(v[i + 1]), sl2, -m_ref));
-                        if (masked) {
-                            if (!(kc + i <= qpos && kc + i >= wlo)) p0 = 0.f;
-                            if (!(kc + i + 1 <= qpos && kc + i + 1 >= wlo)) p1 = 0.f;
+                            for (int q = 0; q < 8; ++q)
+                                dst[q] = make_float4(__uint_as_float(o[4 * q]) * vs, __uint_as_float(o[4 * q + 1]) * vs,
+                                                     __uint_as_float(o[4 * q + 2]) * vs,
+                                                     __uint_as_float(o[4 * q + 3]) * vs);
                         }
-                        ps4[(i >> 1) & 3] += p0 + p1;
-                        const uint32_t h = pack2_bf16(p0, p1);
-                        hi[i >> 1] = h;
-                        lo[i >> 1] = pack2_bf16(p0 - __uint_as_float(h << 16),
-                                                p1 - __uint_as_float(h & 0xffff0000u));
                     }
-                    tmem_st16(s_base + c, hi);
-                    tmem_st16(s_base + c + 16, lo);
-                }
-                tmem_wait_st();
-                l += (ps4[0] + ps4[1]) + (ps4[2] + ps4[3]);
-                // V rows of positions outside [kv_lo, kv_hi) may hold anything
-                // (NaN included): tile A's group zeroes them (PV_B runs after
-                // PV_A) so that 0 * row stays 0; each thread clears its share.
-                const int k0_tile = (blk_lo + 8 * j) * kBlockSize;
-                if (x == 0 && (k0_tile < kv_lo || k0_tile + kKv > kv_hi)) {
-                    if (!warp_wait(&bars[kVFull + j % kStages], (j / kStages) & 1, fail, a.status)) {
-                        ok = false;
-                        continue;
-                    }
-                    const int kp = k0_tile + r;
-                    if (kp < kv_lo || kp >= kv_hi) {
-                        constexpr int kBytes = 256 / kSplit;
-                        const int b0 = part * kBytes;
-                        uint8_t *vrow = sV + (j % kStages) * kTile + (b0 >> 7) * kHalf +
-                                        (r >> 3) * 1024 + (r & 7) * 128 + (b0 & 127);
-#pragma unroll
-                        for (int q = 0; q < kBytes / 16; ++q)
-                            *reinterpret_cast<uint4 *>(vrow + q * 16) = make_uint4(0, 0, 0, 0);
-                    }
-                }
-                fence_proxy_async_smem();
-                tc_fence_before();
-                mbar_arrive(&bars[kPFull + x]);
-            }
-            // the row sum is the parts' sums (all against the same maximum),
-            // exchanged in the slots of the parity the last tile did not use
-            const int sx = n_tiles & 1;
-            red[(sx * kSplit + part) * kRows + r] = l;
-            named_sync(1 + x);
-            float l_row = l;
-#pragma unroll
-            for (int o = 1; o < kSplit; ++o) l_row += red[(sx * kSplit + ((part + o) % kSplit)) * kRows + r];
-            if (kPrefix && __all_sync(0xffffffffu, ok) && warp_wait(&bars[kDrain], 0, fail, a.status)) {
-                // split-K partial of this chunk: (max, sum) and the unnormalised
-                // output, in the partial row of (sequence, head, chunk)
-                tc_fence_after();
-                const size_t prow = ((size_t)(tx0 + tr) * a.num_q_heads + kvh * g + (r % g)) * a.max_parts +
-                                    blockIdx.z;
-                const float vs = a.v_scales != nullptr ? a.v_scales[kvh] : 1.f;
+                    if (real && part == 0)
+                        a.part_ml[prow] = make_float2(l_row > 0.f ? m_used : -INFINITY, l_row);
+                } else if (!kPrefix && __all_sync(0xffffffffu, ok) && drained) {
+                    tc_fence_after();
+                    const float inv = l_row > 0.f ? 1.f / l_row : 0.f;
+                    __nv_bfloat16 *orow = static_cast<__nv_bfloat16 *>(a.out) +
+                                          ((size_t)(d.q0 + tx0 + tr) * a.num_q_heads + d.kvh * g + (r % g)) * kD +
+                                          part * kCols;
 #pragma unroll 1
-                for (int c = 0; c < kCols; c += 32) {
-                    uint32_t o[32];
-                    tmem_ld32(o_base + c, o);
-                    tmem_wait_ld();
-                    if (real) {
-                        float4 *dst = reinterpret_cast<float4 *>(a.part_o + prow * kD + part * kCols + c);
+                    for (int c = 0; c < kCols; c += 32) {
+                        uint32_t o[32];
+                        tmem_ld32(o_base + c, o);
+                        tmem_wait_ld();
+                        if (real) {
 #pragma unroll
-                        for (int q = 0; q < 8; ++q)
-                            dst[q] = make_float4(__uint_as_float(o[4 * q]) * vs, __uint_as_float(o[4 * q + 1]) * vs,
-                                                 __uint_as_float(o[4 * q + 2]) * vs,
-                                                 __uint_as_float(o[4 * q + 3]) * vs);
-                    }
-                }
-                if (real && part == 0)
-                    a.part_ml[prow] = make_float2(l_row > 0.f ? m_used : -INFINITY, l_row);
-            } else if (!kPrefix && __all_sync(0xffffffffu, ok) &&
-                       warp_wait(&bars[kDrain], 0, fail, a.status)) {
-                tc_fence_after();
-                const float inv = l_row > 0.f ? 1.f / l_row : 0.f;
-                __nv_bfloat16 *orow = static_cast<__nv_bfloat16 *>(a.out) +
-                                      ((size_t)(q0 + tx0 + tr) * a.num_q_heads + kvh * g + (r % g)) * kD +
-                                      part * kCols;
-#pragma unroll 1
-                for (int c = 0; c < kCols; c += 32) {
-                    uint32_t o[32];
-                    tmem_ld32(o_base + c, o);
-                    tmem_wait_ld();
-                    if (real) {
-#pragma unroll
-                        for (int q = 0; q < 4; ++q) {
-                            uint4 w;
-                            w.x = pack2_bf16(__uint_as_float(o[8 * q + 0]) * inv, __uint_as_float(o[8 * q + 1]) * inv);
-                            w.y = pack2_bf16(__uint_as_float(o[8 * q + 2]) * inv, __uint_as_float(o[8 * q + 3]) * inv);
-                            w.z = pack2_bf16(__uint_as_float(o[8 * q + 4]) * inv, __uint_as_float(o[8 * q + 5]) * inv);
-                            w.w = pack2_bf16(__uint_as_float(o[8 * q + 6]) * inv, __uint_as_float(o[8 * q + 7]) * inv);
-                            *reinterpret_cast<uint4 *>(orow + c + 8 * q) = w;
+                            for (int q = 0; q < 4; ++q) {
+                                uint4 w;
+                                w.x = pack2_bf16(__uint_as_float(o[8 * q + 0]) * inv, __uint_as_float(o[8 * q + 1]) * inv);
+                                w.y = pack2_bf16(__uint_as_float(o[8 * q + 2]) * inv, __uint_as_float(o[8 * q + 3]) * inv);
+                                w.z = pack2_bf16(__uint_as_float(o[8 * q + 4]) * inv, __uint_as_float(o[8 * q + 5]) * inv);
+                                w.w = pack2_bf16(__uint_as_float(o[8 * q + 6]) * inv, __uint_as_float(o[8 * q + 7]) * inv);
+                                *reinterpret_cast<uint4 *>(orow + c + 8 * q) = w;
+                            }
                         }
                     }
                 }
+                if (!drained) ok = false;
+            } else {
+                // tile B has no rows in this item: keep the drain phase in step
+                if (!warp_wait(&bars[kDrain], it & 1, fail, a.status)) ok = false;
             }
+            // O of this tile has been read: the next item's first P.V may overwrite it
+            tc_fence_before();
+            mbar_arrive(&bars[kOFree + x]);
+            gstep += n_tiles;
         }
     }
     tc_fence_before();
@@ -691,6 +864,18 @@ pa_status launch_tc(const CUtensorMap &qmap, const CUtensorMap &kmap, const CUte
     return PA_OK;
 }
 
+// Streaming multiprocessors of the current device (152 when the runtime
+// cannot tell).
+int prefill_sm_count() {
+    int dev = 0, n = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0) {
+        (void)cudaGetLastError();
+        return 152;
+    }
+    return n;
+}
+
 bool group_ok(int group) {
     return group == 1 || group == 2 || group == 4 || group == 8 || group == 16;
 }
@@ -757,6 +942,8 @@ pa_status launch_prefix_tc(const void *query, const void *key_cache, const void 
     a.staged = staged ? 1 : 0;
     a.k_scales = k_scales;
     a.v_scales = v_scales;
+    a.n_mt = (int)tiles;                 // one item per CTA: its block index
+    a.num_items = (int)(tiles * num_kv_heads * chunks);
     return launch_tc<true>(qmap, kmap, vmap, a, dim3((unsigned)tiles, (unsigned)num_kv_heads,
                                                       (unsigned)chunks),
                            stream);
@@ -766,13 +953,16 @@ pa_status launch_prefix_tc(const void *query, const void *key_cache, const void 
 
 using namespace pa;
 
+extern "C" size_t pa_prefill_workspace_bytes(void) { return kPrefillWorkspaceBytes; }
+
 extern "C" pa_status pa_prefill(void *out, const void *query, const void *key_cache,
                                 const void *value_cache, const int32_t *block_tables,
                                 const int32_t *context_lens, const int32_t *query_start,
                                 int num_seqs, int num_q_heads, int num_kv_heads, int head_dim,
                                 int block_size, int max_blocks_per_seq, int num_blocks,
                                 int num_query_tokens, int max_query_len, float scale,
-                                pa_dtype dtype, int window, int32_t *device_status, void *stream) {
+                                pa_dtype dtype, int window, void *workspace, size_t workspace_bytes,
+                                int32_t *device_status, void *stream) {
     if (num_seqs < 0 || num_q_heads <= 0 || num_kv_heads <= 0 || block_size != kBlockSize ||
         max_blocks_per_seq < 0 || num_blocks <= 0 || num_q_heads % num_kv_heads != 0 ||
         num_query_tokens < 0 || max_query_len < 0 || window < 0 || !(scale == scale))
@@ -786,10 +976,13 @@ extern "C" pa_status pa_prefill(void *out, const void *query, const void *key_ca
         return PA_ERR_INVALID_ARG;
     if (!aligned16(out) || !aligned16(query) || !aligned16(key_cache) || !aligned16(value_cache))
         return PA_ERR_INVALID_ARG;
+    if (workspace == nullptr || workspace_bytes < kPrefillWorkspaceBytes || !aligned16(workspace))
+        return PA_ERR_WORKSPACE;
     const int64_t rows = (int64_t)num_blocks * num_kv_heads * kBlockSize;
     if (rows >= ((int64_t)1 << 31)) return PA_ERR_UNSUPPORTED;
     const int64_t tiles = ((int64_t)max_query_len * group + kQT * kRows - 1) / (kQT * kRows);
-    if (tiles > 0x7fffffff || num_kv_heads > 65535 || num_seqs > 65535) return PA_ERR_UNSUPPORTED;
+    const int64_t items = tiles * num_kv_heads * num_seqs;
+    if (items >= ((int64_t)1 << 31) - kThreads) return PA_ERR_UNSUPPORTED;
     CUtensorMap qmap, kmap, vmap;
     pa_status st = encode_maps(query, num_query_tokens, num_q_heads, num_kv_heads, key_cache,
                                value_cache, rows, &qmap, &kmap, &vmap);
@@ -809,7 +1002,14 @@ extern "C" pa_status pa_prefill(void *out, const void *query, const void *key_ca
     a.max_query_len = max_query_len;
     a.window = window;
     a.scale_log2 = scale * 1.4426950408889634f;
-    return launch_tc<false>(qmap, kmap, vmap, a,
-                            dim3((unsigned)tiles, (unsigned)num_kv_heads, (unsigned)num_seqs),
-                            static_cast<cudaStream_t>(stream));
+    a.n_mt = (int)tiles;
+    a.num_items = (int)items;
+    a.work_counter = static_cast<unsigned int *>(workspace);
+    cudaStream_t cs = static_cast<cudaStream_t>(stream);
+    // the ticket counter starts at zero on every call
+    cudaError_t e = cudaMemsetAsync(workspace, 0, sizeof(unsigned int), cs);
+    if (e != cudaSuccess) return cuda_failure(e, "cudaMemsetAsync(prefill ticket)");
+    // persistent: one CTA per SM (each holds a whole SM), at most one per item
+    const int64_t grid = std::min<int64_t>(items, prefill_sm_count());
+    return launch_tc<false>(qmap, kmap, vmap, a, dim3((unsigned)grid), cs);
 }

@@ -144,3 +144,27 @@ def test_unsupported_shapes_fail_loudly(pkv):
     with pytest.raises(pkv.PagedKVError):
         pkv.prefill(q, kc, kc, torch.zeros(1, 1, dtype=torch.int32, device="cuda"),
                     torch.tensor([4], dtype=torch.int32, device="cuda"), qs, 4)
+
+
+def test_more_items_than_ctas(pkv):
+    """The kernel keeps one CTA per SM and hands out (tile, KV head, sequence)
+    items from a counter: 20 sequences x 16 KV heads x up to 3 tiles is several
+    items per CTA, of very different lengths, some of them empty.  Every item
+    must be done exactly once, on every call (the counter restarts)."""
+    import torch
+    rng = np.random.default_rng(77)
+    specs = [(int(rng.integers(0, 40)) * 16, int(rng.integers(1, 700))) for _ in range(20)]
+    wl, hv, q, qs, tables, lens = _case(16, 16, specs, seed=78)
+    ref = _oracle(wl, hv, q, qs, tables, lens)
+    args = (H.host_to_device(q, torch.bfloat16), H.host_to_device(hv.key_cache, torch.bfloat16),
+            H.host_to_device(hv.value_cache, torch.bfloat16), torch.from_numpy(tables).cuda(),
+            torch.from_numpy(lens).cuda(), torch.from_numpy(qs).cuda(), None, wl.scale)
+    ws = torch.full((int(pkv.lib().pa_prefill_workspace_bytes()),), 255, dtype=torch.uint8,
+                    device="cuda")
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    for call in range(3):
+        out = torch.full_like(args[0], float("nan"))
+        pkv.prefill(*args, out=out, workspace=ws, status=status)
+        torch.cuda.synchronize()
+        assert int(status.item()) == 0
+        H.assert_close(H.as_f64(out), ref, "bf16", f"persistent prefill, call {call}")
