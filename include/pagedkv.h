@@ -373,8 +373,11 @@ pa_status pa_block_copy(void *key_cache, void *value_cache, const int32_t *src_d
  *                    at the same time need their own)
  * Supported: bf16, head_dim 128, group (num_q_heads / num_kv_heads) 1, 2, 4, 8
  * or 16.  Arithmetic: S = QK^T and O = PV on tcgen05 tensor cores with fp32
- * accumulation in tensor memory; P goes to the second product as a bf16 head
- * plus a bf16 residual (about 2^-17 relative).  A memset of the work counter,
+ * accumulation in tensor memory.  The second product runs on f16 operands: P
+ * rounded to f16 (2^-11 relative), each V tile converted to f16 in shared
+ * memory, which is exact for |v| in [2^-14, 65504]; smaller magnitudes lose
+ * at most 2^-25 absolute, larger ones saturate to +-65504 (V beyond f16's
+ * range is not supported).  A memset of the work counter,
  * then one kernel launch: one CTA per SM, each taking (256-row tile, KV head,
  * sequence) items in turn.
  */

@@ -25,9 +25,13 @@
 //                per row (= TMEM lane), each owning 64 of the 128 columns of S
 //                and of O.  They agree on the row maximum through shared memory
 //                once per K/V tile, keep their part of the running sum, write P
-//                (bf16 head and bf16 residual) over the S columns they read,
-//                rescale their part of O only when the maximum grew by more than
-//                2^8, and write their part of the output row.
+//                (f16) over the S columns they read, rescale their part of O
+//                only when the maximum grew by more than 2^8, and write their
+//                part of the output row;
+//   warps 18..19 convert each landed V tile to f16 in place (P.V runs on f16
+//                operands: bf16 weights would be too coarse for the output
+//                tolerance) and zero the rows of positions outside the tile's
+//                range.
 // While one tile's softmax runs, the tensor cores work on the other tile.  The
 // MMAs of one thread execute in issue order: S_X(j+1), issued after PV_X(j),
 // cannot overwrite the P that PV_X(j) reads.
@@ -65,7 +69,9 @@ constexpr int kTile = 2 * kHalf;         // 128 rows x 256 bytes
 constexpr int kSplit = 2;                // softmax threads per row
 constexpr int kCols = kKv / kSplit;      // S / O columns per softmax thread
 constexpr int kGroup = kRows * kSplit;   // softmax threads per Q tile
-constexpr int kThreads = 64 + kQT * kGroup;
+constexpr int kConvWarp0 = 2 + kQT * kGroup / 32;   // first V-conversion warp
+constexpr int kConvThreads = 64;                     // V-conversion threads
+constexpr int kThreads = 64 + kQT * kGroup + kConvThreads;
 #ifndef PA_PREFILL_STAGES
 #define PA_PREFILL_STAGES 2
 #endif
@@ -78,7 +84,7 @@ constexpr int kOffQ = 0;                          // kQT tiles
 constexpr int kOffK = kOffQ + kQT * kTile;        // kStages tiles
 constexpr int kOffV = kOffK + kStages * kTile;    // kStages tiles
 constexpr int kOffBar = kOffV + kStages * kTile;
-constexpr int kNumBars = 4 * kStages + 15;
+constexpr int kNumBars = 5 * kStages + 15;
 constexpr int kOffRed = kOffBar + 256;            // [kQT][2 parities][kSplit][128] floats
 constexpr int kSmemBytes = kOffRed + kQT * 2 * kSplit * kRows * 4;
 // The tiles need 1024-byte alignment; the dynamic shared memory of a kernel
@@ -87,7 +93,8 @@ constexpr int kSmemBytes = kOffRed + kQT * 2 * kSplit * kRows * 4;
 
 // barrier indices
 constexpr int kQFull = 0, kKFull = 1, kKEmpty = kKFull + kStages, kVFull = kKEmpty + kStages,
-              kVEmpty = kVFull + kStages, kSFull = kVEmpty + kStages, kPFull = kSFull + kQT,
+              kVEmpty = kVFull + kStages, kVConv = kVEmpty + kStages, kSFull = kVConv + kStages,
+              kPFull = kSFull + kQT,
               kPvDone = kPFull + kQT, kOFree = kPvDone + kQT, kItemFull = kOFree + kQT,
               kItemEmpty = kItemFull + 2, kQFree = kItemEmpty + 2, kDrain = kQFree + 1;
 static_assert(kDrain + 1 == kNumBars, "barrier count");
@@ -165,6 +172,27 @@ __device__ __forceinline__ float ex2_approx(float x) {
 __device__ __forceinline__ uint32_t pack2_bf16(float lo, float hi) {
     __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
     return *reinterpret_cast<uint32_t *>(&v);
+}
+
+// two floats as an f16 pair, `lo` in the low half (round to nearest even)
+__device__ __forceinline__ uint32_t pack2_f16(float lo, float hi) {
+    uint32_t r;
+    asm("cvt.rn.f16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
+    return r;
+}
+
+// Eight bf16 values (a 16-byte chunk) as eight f16 values in place order:
+// exact for magnitudes in [2^-14, 65504], smaller ones become f16 subnormals
+// (absolute error below 2^-25), larger ones saturate to +-65504.
+__device__ __forceinline__ uint4 bf16x8_to_f16x8(uint4 w) {
+    uint32_t o[4];
+    const uint32_t in[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+    for (int i = 0; i < 4; ++i)
+        asm("cvt.rn.satfinite.f16x2.f32 %0, %1, %2;"
+            : "=r"(o[i])
+            : "f"(__uint_as_float(in[i] & 0xffff0000u)), "f"(__uint_as_float(in[i] << 16)));
+    return make_uint4(o[0], o[1], o[2], o[3]);
 }
 
 __device__ __forceinline__ void named_sync(int id) {
@@ -301,6 +329,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_init(&bars[kKEmpty + s], 1);
             mbar_init(&bars[kVFull + s], 1);
             mbar_init(&bars[kVEmpty + s], 1);
+            mbar_init(&bars[kVConv + s], kConvThreads);
         }
         for (int x = 0; x < kQT; ++x) {
             mbar_init(&bars[kSFull + x], 1);
@@ -310,7 +339,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         for (int q = 0; q < 2; ++q) {
             mbar_init(&bars[kItemFull + q], 1);
-            mbar_init(&bars[kItemEmpty + q], 1 + kQT * kGroup);
+            mbar_init(&bars[kItemEmpty + q], 1 + kQT * kGroup + kConvThreads);
         }
         mbar_init(&bars[kDrain], 1);
         *fail = 0;
@@ -453,7 +482,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         // ---------------- MMA issuer ----------------
         if (lane == 0) {
             constexpr uint32_t idS = idesc_bf16_f32(kRows, kKv, false);
-            constexpr uint32_t idPV = idesc_bf16_f32(kRows, kD, true);
+            constexpr uint32_t idPV = idesc_f16_f32(kRows, kD, true);
             const uint32_t q_u = smem_u32(sQ), k_u = smem_u32(sK), v_u = smem_u32(sV);
             uint32_t gstep = 0;
             uint32_t pcount[kQT] = {0, 0};   // P phases per Q tile (global)
@@ -469,9 +498,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
                 umma_commit(&bars[kSFull + x]);
             };
-            // P of tokens [16k, 16k + 16) sits in the 32-column chunk k / 2 of
-            // the S buffer: head pairs from column 32 (k / 2) + 8 (k % 2),
-            // residual pairs 16 columns further
+            // P (f16 pairs) of tokens [16k, 16k + 16) sits in the 32-column
+            // chunk k / 2 of the S buffer, from column 32 (k / 2) + 8 (k % 2)
             auto issue_pv = [&](int x, uint32_t gs, int j, int it) -> bool {
                 if (!wait_or_fail(&bars[kPFull + x], pcount[x] & 1, fail, a.status)) return false;
                 ++pcount[x];
@@ -486,7 +514,6 @@ __global__ void __launch_bounds__(kThreads, 1)
                     const uint32_t pc = tmem + col_s(x) + 32 * (k >> 1) + 8 * (k & 1);
                     const uint64_t vdesc = sw128_desc(vb + k * 2048, kHalf, 1024);
                     umma_bf16_tmem_a(tmem + col_o(x), pc, vdesc, idPV, (j > 0 || k > 0) ? 1u : 0u);
-                    umma_bf16_tmem_a(tmem + col_o(x), pc + 16, vdesc, idPV, 1u);
                 }
                 umma_commit(&bars[kPvDone + x]);
                 return true;
@@ -516,7 +543,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 for (int j = 0; ok && j < n; ++j) {
                     const uint32_t gs = gstep + j, gk = gs + 1;
                     const bool more = j + 1 < n;
-                    if (!wait_or_fail(&bars[kVFull + gs % kStages], (gs / kStages) & 1, fail, a.status) ||
+                    if (!wait_or_fail(&bars[kVConv + gs % kStages], (gs / kStages) & 1, fail, a.status) ||
                         !issue_pv(0, gs, j, it)) {
                         ok = false;
                         break;
@@ -544,6 +571,52 @@ __global__ void __launch_bounds__(kThreads, 1)
                 umma_commit(&bars[kDrain]);
                 gstep += n;
             }
+        }
+    } else if (warp >= kConvWarp0) {
+        // ---------------- V conversion ----------------
+        // Each landed V tile becomes f16 in place before its P.V products:
+        // rows of positions outside [kv_lo, kv_hi) may hold anything (NaN
+        // included) and are zeroed instead, so that 0 * row stays 0.  Thread t
+        // takes the 16-byte chunks t, t + kConvThreads, ... (a chunk's row is
+        // its offset within the 64-column half over 128 bytes; the swizzle only
+        // permutes chunks within a row).
+        const int ct = threadIdx.x - kConvWarp0 * 32;
+        uint32_t gstep = 0;
+        bool ok = true;
+        for (int it = 0;; ++it) {
+            int item;
+            if constexpr (kPrefix) {
+                item = it == 0 ? (int)(blockIdx.x + gridDim.x * (blockIdx.y + gridDim.y * blockIdx.z)) : -1;
+            } else {
+                const int slot = it & 1;
+                const bool got_item = wait_or_fail(&bars[kItemFull + slot], (it >> 1) & 1, fail, a.status);
+                item = got_item ? s_item[slot] : -1;
+                mbar_arrive(&bars[kItemEmpty + slot]);
+            }
+            if (item < 0) break;
+            Item d;
+            describe_item<kPrefix>(a, item, kv_hi_cap, false, d);
+            for (int j = 0; ok && j < d.n_tiles; ++j) {
+                const uint32_t gs = gstep + j;
+                const int st = gs % kStages;
+                if (!wait_or_fail(&bars[kVFull + st], (gs / kStages) & 1, fail, a.status)) {
+                    ok = false;
+                    break;
+                }
+                const int k0_tile = (d.blk_lo + 8 * j) * kBlockSize;
+                const bool edge = k0_tile < d.kv_lo || k0_tile + kKv > d.kv_hi;
+                uint4 *vt = reinterpret_cast<uint4 *>(sV + st * kTile);
+#pragma unroll 8
+                for (int i = 0; i < kTile / 16 / kConvThreads; ++i) {
+                    const int c = ct + i * kConvThreads;
+                    const int kp = k0_tile + (c % (kHalf / 16)) / 8;
+                    const uint4 w = vt[c];
+                    vt[c] = (edge && (kp < d.kv_lo || kp >= d.kv_hi)) ? make_uint4(0, 0, 0, 0) : bf16x8_to_f16x8(w);
+                }
+                fence_proxy_async_smem();
+                mbar_arrive(&bars[kVConv + st]);
+            }
+            gstep += d.n_tiles;
         }
     } else {
         // ---------------- softmax groups ----------------
@@ -667,9 +740,11 @@ __global__ void __launch_bounds__(kThreads, 1)
                         m_used = m_new;
                     }
                     const float m_ref = m_used == -INFINITY ? 0.f : m_used;
-                    // pass 2: P = 2^(s * scale_log2 - m_ref) as a bf16 head + bf16
-                    // residual, written over the same 32 columns it was read from
-                    // (head pairs in the first 16, residual pairs in the next 16)
+                    // pass 2: P = 2^(s * scale_log2 - m_ref) in f16 (at most 2^8, so
+                    // always finite; 11 significant bits keep the weights within
+                    // the output tolerance, where bf16's 8 bits do not), written as
+                    // 16 columns of pairs over the first half of the 32 columns it
+                    // was read from
                     float ps4[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll 1
                     for (int c = 0; c < kCols; c += 32) {
@@ -679,7 +754,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                         const int kc = k0 + c;
                         const bool masked =
                             (kc + 31 > qpos_lo) || (!kPrefix && a.window > 0 && kc < qpos_hi + 1 - a.window);
-                        uint32_t hi[16], lo[16];
+                        uint32_t pp[16];
 #pragma unroll
                         for (int i = 0; i < 32; i += 2) {
                             float p0 = ex2_approx(fmaf(__uint_as_float(v[i]), sl2k, -m_ref));
@@ -689,38 +764,12 @@ __global__ void __launch_bounds__(kThreads, 1)
                                 if (!(kc + i + 1 <= qpos && kc + i + 1 >= wlo)) p1 = 0.f;
                             }
                             ps4[(i >> 1) & 3] += p0 + p1;
-                            const uint32_t h = pack2_bf16(p0, p1);
-                            hi[i >> 1] = h;
-                            lo[i >> 1] = pack2_bf16(p0 - __uint_as_float(h << 16),
-                                                    p1 - __uint_as_float(h & 0xffff0000u));
+                            pp[i >> 1] = pack2_f16(p0, p1);
                         }
-                        tmem_st16(s_base + c, hi);
-                        tmem_st16(s_base + c + 16, lo);
+                        tmem_st16(s_base + c, pp);
                     }
                     tmem_wait_st();
                     l += (ps4[0] + ps4[1]) + (ps4[2] + ps4[3]);
-                    // V rows of positions outside [kv_lo, kv_hi) may hold anything
-                    // (NaN included): tile A's group zeroes them (PV_B runs after
-                    // PV_A) so that 0 * row stays 0; each thread clears its share.
-                    const int k0_tile = (d.blk_lo + 8 * j) * kBlockSize;
-                    if (x == 0 && (k0_tile < d.kv_lo || k0_tile + kKv > d.kv_hi)) {
-                        const uint32_t gs = gstep + j;
-                        if (!warp_wait(&bars[kVFull + gs % kStages], (gs / kStages) & 1, fail, a.status)) {
-                            ok = false;
-                            continue;
-                        }
-                        const int kp = k0_tile + r;
-                        if (kp < d.kv_lo || kp >= d.kv_hi) {
-                            constexpr int kBytes = 256 / kSplit;
-                            const int b0 = part * kBytes;
-                            uint8_t *vrow = sV + (gs % kStages) * kTile + (b0 >> 7) * kHalf +
-                                            (r >> 3) * 1024 + (r & 7) * 128 + (b0 & 127);
-#pragma unroll
-                            for (int q = 0; q < kBytes / 16; ++q)
-                                *reinterpret_cast<uint4 *>(vrow + q * 16) = make_uint4(0, 0, 0, 0);
-                        }
-                    }
-                    fence_proxy_async_smem();
                     tc_fence_before();
                     mbar_arrive(&bars[kPFull + x]);
                 }

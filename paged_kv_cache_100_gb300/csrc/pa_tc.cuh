@@ -54,6 +54,12 @@ __host__ __device__ constexpr uint32_t idesc_bf16_f32(int M, int N, bool b_mn_ma
            ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
 }
 
+// The same with f16 operands (A and B of one MMA always share their type).
+__host__ __device__ constexpr uint32_t idesc_f16_f32(int M, int N, bool b_mn_major) {
+    return (1u << 4) | ((b_mn_major ? 1u : 0u) << 16) | ((uint32_t)(N >> 3) << 17) |
+           ((uint32_t)(M >> 4) << 24);
+}
+
 // D[tmem] (+)= A[smem] * B[smem]; issued by one thread.
 __device__ __forceinline__ void umma_bf16(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
                                           uint32_t idesc, uint32_t accumulate) {
@@ -65,7 +71,8 @@ __device__ __forceinline__ void umma_bf16(uint32_t d_tmem, uint64_t a_desc, uint
 }
 
 // D[tmem] (+)= A[tmem] * B[smem]: A (M rows = TMEM lanes) packs two 16-bit
-// elements per 32-bit column, K index 2c and 2c+1 in column c.
+// elements per 32-bit column, K index 2c and 2c+1 in column c; the operand
+// types (bf16 or f16) are the instruction descriptor's.
 __device__ __forceinline__ void umma_bf16_tmem_a(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc,
                                                  uint32_t idesc, uint32_t accumulate) {
     asm volatile(
