@@ -233,23 +233,39 @@ def _code_only(src: str) -> str:
     return "\n".join(line.strip() for line in src.splitlines() if line.strip())
 
 
-def kernel_source_hash() -> str:
+DECODE_SOURCES = ("pa_decode.cu", "pa_device.cuh", "pa_internal.h")
+# the shared-prefix cascade also runs the tensor-core kernel in prefix mode
+CASCADE_SOURCES = DECODE_SOURCES + ("pa_prefill.cu", "pa_tc.cuh")
+
+
+def kernel_source_hash(files=DECODE_SOURCES) -> str:
     h = hashlib.sha256()
-    for f in ("pa_decode.cu", "pa_device.cuh", "pa_internal.h"):
+    for f in files:
         with open(os.path.join(ROOT, "paged_kv_cache_100_gb300", "csrc", f)) as fh:
             h.update(_code_only(fh.read()).encode())
     return h.hexdigest()[:16]
 
 
-def measured_traffic(workload: str):
-    """DRAM bytes per pa_decode call from the committed ncu summary, if it still
-    describes the current kernel source (else None)."""
+def traffic_key(workload: str, kv_dtype: str = "bf16", window: int = 0, partition_size: int = 0,
+                decode: str = "auto") -> str:
+    """Key of a decode configuration in the traffic record: the workload name
+    alone for its default line (bf16 pools, whole context, library-chosen
+    partition), else every setting that changes the kernel or its bytes."""
+    if kv_dtype == "bf16" and window == 0 and partition_size == 0 and decode == "auto":
+        return workload
+    return f"{workload}|{kv_dtype}|window={window}|partition={partition_size}|decode={decode}"
+
+
+def measured_traffic(key: str):
+    """DRAM bytes per decode call from the committed ncu summary for exactly
+    this configuration, if it still describes the current kernel source (else
+    None)."""
     path = os.path.join(ROOT, "profiles", "decode_traffic.json")
     try:
         with open(path) as f:
             rec = json.load(f)
-        entry = rec[workload]
-        if entry.get("kernel_source_hash") != kernel_source_hash():
+        entry = rec[key]
+        if entry.get("kernel_source_hash") != kernel_source_hash(tuple(entry.get("sources", DECODE_SOURCES))):
             return None
         return float(entry["dram_bytes_per_call"])
     except Exception:
@@ -410,7 +426,8 @@ def run_gpu(args):
     peak, peak_kind = load_peaks()
     achieved = hbm_bytes / (decode_ms * 1e-3) / 1e9
     tokens_per_s = wl.num_seqs * world / (ms_per_step * 1e-3)
-    traffic = measured_traffic(args.workload)
+    traffic = measured_traffic(traffic_key(args.workload, args.kv_dtype, window, args.partition_size,
+                                           args.decode))
     line = {
         "metric": METRIC,
         "value": tokens_per_s,
