@@ -652,6 +652,10 @@ __global__ void __launch_bounds__(kThreads, 1)
             const int n_tiles = d.n_tiles;
             if (x == 0 || d.has_b) {
                 const float sl2k = a.k_scales != nullptr ? a.scale_log2 * a.k_scales[d.kvh] : a.scale_log2;
+                // a negative scale reverses the order of the scores; masked
+                // positions take the raw value that never wins
+                const bool neg = sl2k < 0.f;
+                const float fill = neg ? INFINITY : -INFINITY;
                 const int tx0 = d.t0 + x * tok_per_tile;      // first token (sequence) of this tile
                 const int ntok = max(0, min(tok_per_tile, d.T - tx0));
                 const bool real = tr < ntok;
@@ -679,8 +683,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                 for (int j = 0; j < n_tiles; ++j) {
                     const bool got = ok && warp_wait(&bars[kSFull + x], sc & 1, fail, a.status);
                     const int k0 = (d.blk_lo + 8 * j) * kBlockSize + part * kCols;   // column 0's position
-                    // pass 1: row maximum over this thread's columns
-                    float mx4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+                    // pass 1: the raw score whose scaled value is the row maximum
+                    // over this thread's columns (the largest raw score, or the
+                    // smallest when the scale is negative)
+                    float mx4[4] = {fill, fill, fill, fill};
                     if (got) {
                         tc_fence_after();
 #pragma unroll 1
@@ -692,20 +698,28 @@ __global__ void __launch_bounds__(kThreads, 1)
                             if ((kc + 31 > qpos_lo) || (!kPrefix && a.window > 0 && kc < qpos_hi + 1 - a.window)) {
 #pragma unroll
                                 for (int i = 0; i < 32; ++i)
-                                    if (!(kc + i <= qpos && kc + i >= wlo)) v[i] = __float_as_uint(-INFINITY);
+                                    if (!(kc + i <= qpos && kc + i >= wlo)) v[i] = __float_as_uint(fill);
                             }
+                            if (!neg) {
 #pragma unroll
-                            for (int i = 0; i < 32; ++i) mx4[i & 3] = fmaxf(mx4[i & 3], __uint_as_float(v[i]));
+                                for (int i = 0; i < 32; ++i) mx4[i & 3] = fmaxf(mx4[i & 3], __uint_as_float(v[i]));
+                            } else {
+#pragma unroll
+                                for (int i = 0; i < 32; ++i) mx4[i & 3] = fminf(mx4[i & 3], __uint_as_float(v[i]));
+                            }
                         }
                     }
-                    float mrow = fmaxf(fmaxf(mx4[0], mx4[1]), fmaxf(mx4[2], mx4[3]));
+                    float mrow = neg ? fminf(fminf(mx4[0], mx4[1]), fminf(mx4[2], mx4[3]))
+                                     : fmaxf(fmaxf(mx4[0], mx4[1]), fmaxf(mx4[2], mx4[3]));
                     const int rp = ex & 1;
                     ++ex;
                     red[(rp * kSplit + part) * kRows + r] = mrow;
                     named_sync(1 + x);
 #pragma unroll
-                    for (int o = 1; o < kSplit; ++o)
-                        mrow = fmaxf(mrow, red[(rp * kSplit + ((part + o) % kSplit)) * kRows + r]);
+                    for (int o = 1; o < kSplit; ++o) {
+                        const float other = red[(rp * kSplit + ((part + o) % kSplit)) * kRows + r];
+                        mrow = neg ? fminf(mrow, other) : fmaxf(mrow, other);
+                    }
                     const uint32_t my_sc = sc++;
                     if (!got) {
                         ok = false;

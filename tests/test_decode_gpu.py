@@ -28,18 +28,33 @@ def _device_inputs(wl, hv, lens=None):
     return q, kc, vc, bt, cl
 
 
-def _run(pkv, wl, hv, lens=None, partition_size=0, status=None):
+def _run(pkv, wl, hv, lens=None, partition_size=0, status=None, scale=None):
     import torch
     q, kc, vc, bt, cl = _device_inputs(wl, hv, lens)
-    out = pkv.decode(q, kc, vc, bt, cl, wl.scale, partition_size=partition_size, status=status)
+    out = pkv.decode(q, kc, vc, bt, cl, wl.scale if scale is None else scale,
+                     partition_size=partition_size, status=status)
     torch.cuda.synchronize()
     return out
 
 
-def _oracle(wl, hv, lens=None):
+def _oracle(wl, hv, lens=None, scale=None):
     lens = wl.context_lens if lens is None else lens
     return oracle.paged_decode(hv.query, hv.key_cache, hv.value_cache, wl.block_tables,
-                               np.asarray(lens, np.int32), wl.scale, threads=4)
+                               np.asarray(lens, np.int32), wl.scale if scale is None else scale,
+                               threads=4)
+
+
+@pytest.mark.parametrize("hq,hkv", [(4, 4), (8, 2), (16, 2)])
+@pytest.mark.parametrize("scale", [-0.0883883, 0.0])
+def test_nonpositive_scale(pkv, hq, hkv, scale):
+    """A negative scale reverses the order of the scores; scale 0 weighs every
+    position equally (MHA and GQA consumers, split and unsplit)."""
+    lens = [1, 17, 300, 1100]
+    wl = W.custom_workload(len(lens), hq, hkv, 128, lens, dtype="bf16", seed=hq + hkv)
+    hv = W.host_values(wl)
+    for ps in (0, 64):
+        got = H.as_f64(_run(pkv, wl, hv, partition_size=ps, scale=scale))
+        H.assert_close(got, _oracle(wl, hv, scale=scale), "bf16", f"decode scale {scale} P {ps}")
 
 
 def test_tiny_fp32_workload(pkv):

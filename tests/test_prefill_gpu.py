@@ -46,22 +46,22 @@ def _case(hq, hkv, specs, seed, window=0):
     return wl, hv, q, qs, tables, np.asarray(lens, np.int32)
 
 
-def _run(pkv, wl, hv, q, qs, tables, lens, window=0, max_query_len=None):
+def _run(pkv, wl, hv, q, qs, tables, lens, window=0, max_query_len=None, scale=None):
     import torch
     status = torch.zeros(1, dtype=torch.int32, device="cuda")
     out = pkv.prefill(H.host_to_device(q, torch.bfloat16),
                       H.host_to_device(hv.key_cache, torch.bfloat16),
                       H.host_to_device(hv.value_cache, torch.bfloat16),
                       torch.from_numpy(tables).cuda(), torch.from_numpy(lens).cuda(),
-                      torch.from_numpy(qs).cuda(), max_query_len, wl.scale, window=window,
-                      status=status)
+                      torch.from_numpy(qs).cuda(), max_query_len,
+                      wl.scale if scale is None else scale, window=window, status=status)
     torch.cuda.synchronize()
     return out, int(status.item())
 
 
-def _oracle(wl, hv, q, qs, tables, lens, window=0):
-    return oracle.paged_prefill(q, hv.key_cache, hv.value_cache, tables, lens, qs, wl.scale,
-                                threads=8, window=window)
+def _oracle(wl, hv, q, qs, tables, lens, window=0, scale=None):
+    return oracle.paged_prefill(q, hv.key_cache, hv.value_cache, tables, lens, qs,
+                                wl.scale if scale is None else scale, threads=8, window=window)
 
 
 SPECS = [(0, 1), (0, 5), (0, 127), (0, 128), (0, 129), (17, 50), (300, 200), (1000, 31)]
@@ -74,6 +74,19 @@ def test_prefill_matches_oracle(pkv, hq, hkv):
     assert st == 0
     H.assert_close(H.as_f64(got), _oracle(wl, hv, q, qs, tables, lens), "bf16",
                    f"prefill {hq}/{hkv}")
+
+
+@pytest.mark.parametrize("scale", [-0.0883883, -0.5, 0.0])
+def test_prefill_nonpositive_scale(pkv, scale):
+    """A negative scale reverses the order of the scores (the row maximum of
+    scale * s sits at the smallest s); scale 0 weighs every attended position
+    equally."""
+    specs = [(0, 5), (0, 130), (300, 200), (17, 1)]
+    wl, hv, q, qs, tables, lens = _case(8, 2, specs, seed=31)
+    got, st = _run(pkv, wl, hv, q, qs, tables, lens, scale=scale)
+    assert st == 0
+    H.assert_close(H.as_f64(got), _oracle(wl, hv, q, qs, tables, lens, scale=scale), "bf16",
+                   f"prefill scale {scale}")
 
 
 def test_long_fresh_prompt_spans_many_tiles(pkv):
