@@ -79,6 +79,24 @@ def test_many_sequences_span_several_row_tiles(pkv):
     H.assert_close(H.as_f64(out), ref, "bf16", "70 sequences")
 
 
+@pytest.mark.parametrize("hq,hkv,partition_size", [(16, 2, 0), (16, 4, 0), (8, 4, 32), (16, 8, 16)])
+def test_many_short_suffixes(pkv, hq, hkv, partition_size):
+    """Hundreds of short suffixes (some empty) and, with small partitions,
+    several partitions per sequence: more suffix CTAs than fit on the GPU at
+    once, and empty trailing partitions."""
+    rng = np.random.default_rng(hq * 100 + hkv + partition_size)
+    B = 600
+    suffix = rng.integers(0, 90, B)
+    suffix[::7] = 0
+    wl = _shared_workload(B, hq, hkv, 128, 3, suffix.tolist(), seed=hq + hkv + partition_size)
+    hv = W.host_values(wl)
+    out, ref_gpu = _run(pkv, wl, hv, 3, partition_size=partition_size)
+    ref = oracle.paged_decode(hv.query, hv.key_cache, hv.value_cache, wl.block_tables,
+                              wl.context_lens, wl.scale, threads=8)
+    H.assert_close(H.as_f64(out), ref, "bf16", f"{B} suffixes {hq}/{hkv} P={partition_size}")
+    H.assert_close(H.as_f64(out), H.as_f64(ref_gpu), "bf16", "many suffixes vs pa_decode")
+
+
 def test_contexts_shorter_than_the_prefix_are_masked(pkv):
     wl = _shared_workload(4, 16, 4, 128, 10, [5, 0, 30, 1], seed=9)
     hv = W.host_values(wl, poison_unused=False)
@@ -200,6 +218,23 @@ def test_shared_prefix_fp8_matches_oracle(pkv, hq, hkv, prefix_blocks):
                               v_scales=hv.v_scales)
     H.assert_close(H.as_f64(out), ref, "bf16", f"fp8 shared prefix {hq}/{hkv} n={prefix_blocks}")
     H.assert_close(H.as_f64(out), H.as_f64(ref_gpu), "bf16", "fp8 shared prefix vs pa_decode_fp8")
+
+
+@pytest.mark.parametrize("hq,hkv,partition_size", [(16, 4, 0), (16, 2, 32)])
+def test_shared_prefix_fp8_many_short_suffixes(pkv, hq, hkv, partition_size):
+    """E4M3 pools with hundreds of short suffixes (more CTAs than fit at once)."""
+    rng = np.random.default_rng(7 * hq + hkv + partition_size)
+    B = 500
+    suffix = rng.integers(0, 90, B)
+    suffix[::5] = 0
+    wl = _shared_workload(B, hq, hkv, 128, 2, suffix.tolist(), seed=3 * hq + hkv)
+    hv = W.fp8_host_values(wl)
+    out, ref_gpu = _fp8_run(pkv, wl, hv, 2, partition_size=partition_size)
+    ref = oracle.paged_decode(hv.query, hv.key_cache, hv.value_cache, wl.block_tables,
+                              wl.context_lens, wl.scale, threads=8, k_scales=hv.k_scales,
+                              v_scales=hv.v_scales)
+    H.assert_close(H.as_f64(out), ref, "bf16", f"fp8 {B} suffixes {hq}/{hkv} P={partition_size}")
+    H.assert_close(H.as_f64(out), H.as_f64(ref_gpu), "bf16", "fp8 many suffixes vs pa_decode_fp8")
 
 
 def test_shared_prefix_fp8_short_contexts_and_split_suffix(pkv):
