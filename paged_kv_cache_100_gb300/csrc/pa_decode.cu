@@ -863,11 +863,11 @@ struct GqaTFp8Consumer {
         const float p2 = exp2f(s[2] - m0), p3 = exp2f(s[3] - m1);
         l0 += p0 + p2;
         l1 += p1 + p3;
-        uint32_t top_hi, top_lo, bot_hi, bot_lo;
-        split_f16x2(p0, p1, top_hi, top_lo);
-        split_f16x2(p2, p3, bot_hi, bot_lo);
-        const uint32_t bh0 = movmatrix_trans(top_hi), bh1 = movmatrix_trans(bot_hi);
-        const uint32_t bl0 = movmatrix_trans(top_lo), bl1 = movmatrix_trans(bot_lo);
+        // P in f16, rounded once: 11 significant bits move an output by at most
+        // 2^-11 of the largest |v| it weighs (no residual product needed, unlike
+        // bf16 weights)
+        const uint32_t bh0 = movmatrix_trans(pack_f16x2(p0, p1));
+        const uint32_t bh1 = movmatrix_trans(pack_f16x2(p2, p3));
         if (nlo > 0 || nvalid < 16) zero_rows_outside_128(vtile, nlo, nvalid, lane);
 #pragma unroll
         for (int c = 0; c < D / 32; ++c) {
@@ -885,7 +885,6 @@ struct GqaTFp8Consumer {
                 e4m3x4_to_f16x2x2(x0, a[0], a[1]);
                 e4m3x4_to_f16x2x2(x1, a[2], a[3]);
                 mma_f16_16816(o[2 * c + jp], a, bh0, bh1);
-                mma_f16_16816(o[2 * c + jp], a, bl0, bl1);
             }
         }
     }
@@ -1592,10 +1591,10 @@ cudaError_t allow_smem(K kernel, size_t bytes) {
 #define PA_GQA16_STAGES 2
 #endif
 // FP8 pools (4 KiB per block): MHA 8 warps x 2 stages (64 KiB, three CTAs per
-// SM); GQA 4 warps x 3 stages (48 KiB).  Measured alternatives with the
-// current consumers: MHA 8x3, 12x2, 4x4 (7B-shaped batch 89.4 us at 8x2
-// against 92.5-99.2 us); GQA 8x2, 8x3, 6x2 (70B-shaped batch 208.4 us at 4x3
-// against 210.6-217.5 us).
+// SM); GQA 8 warps x 3 stages (96 KiB, two CTAs per SM).  Measured
+// alternatives: MHA 8x3, 12x2, 4x4 (7B-shaped batch 89.4 us at 8x2 against
+// 92.5-99.2 us); GQA, with P.V on single f16 weights, 4x2, 4x3, 4x4, 6x2, 8x2
+// (70B-shaped batch 206.0 us at 8x3 against 208.3-210.6 us).
 #ifndef PA_MHA8_WARPS
 #define PA_MHA8_WARPS 8
 #endif
@@ -1603,7 +1602,7 @@ cudaError_t allow_smem(K kernel, size_t bytes) {
 #define PA_MHA8_STAGES 2
 #endif
 #ifndef PA_GQA8_WARPS
-#define PA_GQA8_WARPS 4
+#define PA_GQA8_WARPS 8
 #endif
 #ifndef PA_GQA8_STAGES
 #define PA_GQA8_STAGES 3
@@ -1687,7 +1686,8 @@ pa_status dispatch_fp8(int group, const DecodeArgs &a, const void *kc, const voi
                        int64_t rows, cudaStream_t stream) {
     constexpr int D = 128;
     // blocks one CTA streams at most: short spans take the narrower GQA CTA
-    const int span = std::min(a.part_blocks, std::max(0, a.max_blocks - a.token_offset / kBlockSize));
+    int span = std::min(a.part_blocks, std::max(0, a.max_blocks - a.token_offset / kBlockSize));
+    if (a.window > 0) span = std::min(span, a.window / kBlockSize + 1);
     const bool short_span = span <= PA_GQA8S_MAX_BLOCKS;
     switch (group) {
     case 1: return launch_bf16<D, MhaFp8Consumer<D>, PA_MHA8_WARPS, PA_MHA8_STAGES>(a, kc, vc, rows, stream);
