@@ -513,30 +513,55 @@ def workload_config(wl, P, world, kv_dtype=None, window=0):
     return cfg
 
 
+class PackedInputs:
+    """A step's host inputs packed into one pinned buffer (256-byte aligned
+    pieces) with a device twin: one host-to-device copy per step instead of one
+    per tensor.  `dev[name]` are views of the device buffer with each input's
+    dtype and shape."""
+
+    def __init__(self, tensors: dict, dev):
+        import torch
+        offs, off = {}, 0
+        for k, t in tensors.items():
+            offs[k] = off
+            off += (t.numel() * t.element_size() + 255) // 256 * 256
+        self.nbytes = off
+        self.host = torch.empty(max(off, 1), dtype=torch.uint8).pin_memory()
+        self.device = torch.empty(max(off, 1), dtype=torch.uint8, device=dev)
+        self.dev = {}
+        for k, t in tensors.items():
+            n = t.numel() * t.element_size()
+            self.host[offs[k]:offs[k] + n].copy_(t.contiguous().view(-1).view(torch.uint8))
+            self.dev[k] = self.device[offs[k]:offs[k] + n].view(t.dtype).view(t.shape)
+        self.used = sum(t.numel() * t.element_size() for t in tensors.values())
+
+    def upload(self):
+        self.device.copy_(self.host, non_blocking=True)
+
+
 def run_e2e(args, pkv, wl, q, kc, vc, kn, vn, dev, stream, ops):
     """Same step through the public API with host inputs: H2D of the step's inputs
-    (query, new K/V rows, slots, tables, lengths, copy pairs) and D2H of the output
-    inside the timed region."""
+    (query, new K/V rows, slots, tables, lengths, copy pairs; packed in one pinned
+    buffer, one copy) and D2H of the output inside the timed region."""
     import torch
-    host = {
-        "q": q.cpu().pin_memory(), "kn": kn.cpu().pin_memory(), "vn": vn.cpu().pin_memory(),
-        "slots": torch.from_numpy(wl.slot_mapping).pin_memory(),
-        "bt": torch.from_numpy(wl.block_tables).pin_memory(),
-        "lens": torch.from_numpy(wl.step_context_lens).pin_memory(),
-        "pairs": torch.from_numpy(wl.cow_pairs).pin_memory(),
+    has_cow = wl.cow_pairs.shape[0] > 0
+    inputs = {
+        "q": q.cpu(), "kn": kn.cpu(), "vn": vn.cpu(),
+        "slots": torch.from_numpy(wl.slot_mapping),
+        "bt": torch.from_numpy(wl.block_tables),
+        "lens": torch.from_numpy(wl.step_context_lens),
     }
-    devb = {k: torch.empty_like(v, device=dev) for k, v in host.items()}
+    if has_cow:
+        inputs["pairs"] = torch.from_numpy(wl.cow_pairs)
+    packed = PackedInputs(inputs, dev)
+    devb = packed.dev
     out = torch.empty_like(q)
     out_host = torch.empty(out.shape, dtype=out.dtype).pin_memory()
-    has_cow = wl.cow_pairs.shape[0] > 0
-    h2d = sum(v.numel() * v.element_size() for k, v in host.items() if k != "pairs" or has_cow)
+    h2d = packed.nbytes
     d2h = out.numel() * out.element_size()
 
     def step():
-        for k, v in host.items():
-            if k == "pairs" and not has_cow:
-                continue
-            devb[k].copy_(v, non_blocking=True)
+        packed.upload()
         ops.write(devb["kn"], devb["vn"], devb["slots"])
         if has_cow:
             pkv.block_copy(kc, vc, devb["pairs"])
@@ -816,18 +841,18 @@ def run_prefill_gpu(args):
     ms_per_step = max_over_ranks(e0.elapsed_time(e1), dev) / K
     prefill_ms = max_over_ranks(sum(a_.elapsed_time(b_) for a_, b_ in zip(pre, post)) / K, dev)
 
-    # end to end: chunk inputs from pinned host memory, output back, every step
-    host = {"q": q.cpu().pin_memory(), "kn": kn.cpu().pin_memory(), "vn": vn.cpu().pin_memory(),
-            "slots": torch.from_numpy(pw.slot_mapping).pin_memory(),
-            "bt": torch.from_numpy(pw.block_tables).pin_memory(),
-            "lens": torch.from_numpy(pw.context_lens).pin_memory(),
-            "qs": torch.from_numpy(pw.query_start).pin_memory()}
-    devb = {k: torch.empty_like(v, device=dev) for k, v in host.items()}
+    # end to end: chunk inputs from pinned host memory (one packed copy), output
+    # back, every step
+    packed = PackedInputs({"q": q.cpu(), "kn": kn.cpu(), "vn": vn.cpu(),
+                           "slots": torch.from_numpy(pw.slot_mapping),
+                           "bt": torch.from_numpy(pw.block_tables),
+                           "lens": torch.from_numpy(pw.context_lens),
+                           "qs": torch.from_numpy(pw.query_start)}, dev)
+    devb = packed.dev
     out_host = torch.empty(out.shape, dtype=out.dtype).pin_memory()
 
     def e2e_step():
-        for k, v in host.items():
-            devb[k].copy_(v, non_blocking=True)
+        packed.upload()
         step(q_=devb["q"], kn_=devb["kn"], vn_=devb["vn"], slots_=devb["slots"], bt_=devb["bt"],
              lens_=devb["lens"], qs_=devb["qs"])
         out_host.copy_(out, non_blocking=True)
@@ -883,7 +908,7 @@ def run_prefill_gpu(args):
         "clocks": clocks,
         "e2e": {"value": pw.num_tokens * world / (e2e_ms * 1e-3), "unit": "tokens/s",
                 "ms_per_step": e2e_ms, "steps": KE,
-                "h2d_bytes_per_step": int(sum(v.numel() * v.element_size() for v in host.values())),
+                "h2d_bytes_per_step": int(packed.nbytes),
                 "d2h_bytes_per_step": int(out.numel() * out.element_size())},
     }
     if not args.no_cpu_baseline and world == 1:
