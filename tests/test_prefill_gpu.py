@@ -181,3 +181,40 @@ def test_more_items_than_ctas(pkv):
         torch.cuda.synchronize()
         assert int(status.item()) == 0
         H.assert_close(H.as_f64(out), ref, "bf16", f"persistent prefill, call {call}")
+
+
+@pytest.mark.parametrize("name", ["prefill_llama70b_chunked", "prefill_llama7b"])
+def test_full_size_workload_sampled(pkv, name):
+    """The bench's prefill workloads at full size, in the bench's launch
+    configuration (cache write of the chunk, then pa_prefill).  Sampled rows are
+    checked one by one: query row i of sequence b sits at position p = C_b + i
+    and attends to positions [0, p], which is the decode of that row's query
+    over a context of p + 1 tokens."""
+    import torch
+    pw = W.make_prefill_workload(name)
+    dev = torch.device("cuda")
+    q, kc, vc, kn, vn = W.prefill_device_values(pw, dev)
+    tables = torch.from_numpy(pw.block_tables).to(dev)
+    lens = torch.from_numpy(pw.context_lens).to(dev)
+    qs = torch.from_numpy(pw.query_start).to(dev)
+    pkv.cache_write(kc, vc, kn, vn, torch.from_numpy(pw.slot_mapping).to(dev))
+    status = torch.zeros(1, dtype=torch.int32, device=dev)
+    out = pkv.prefill(q, kc, vc, tables, lens, qs, int(pw.chunk.max()), 1.0 / np.sqrt(pw.head_dim),
+                      status=status)
+    torch.cuda.synchronize()
+    assert int(status.item()) == 0
+    rng = np.random.default_rng(5)
+    seqs = rng.choice(pw.num_seqs, size=3, replace=False)
+    rows, ctx, tabs = [], [], []
+    for b in seqs:
+        for i in rng.choice(int(pw.chunk[b]), size=4, replace=False):
+            rows.append(int(pw.query_start[b]) + int(i))
+            ctx.append(int(pw.cached[b]) + int(i) + 1)
+            tabs.append(pw.block_tables[b])
+    idx = torch.tensor(rows, device=dev)
+    qh = H.device_to_host_bits(q.index_select(0, idx))
+    kch, vch = H.device_to_host_bits(kc), H.device_to_host_bits(vc)
+    ref = oracle.paged_decode(qh, kch, vch, np.stack(tabs).astype(np.int32),
+                              np.asarray(ctx, np.int32), 1.0 / np.sqrt(pw.head_dim), threads=8)
+    got = H.as_f64(out.index_select(0, idx))
+    H.assert_close(got, ref, "bf16", f"{name} sampled rows")
