@@ -216,12 +216,6 @@ __device__ __forceinline__ uint32_t pack_f16x2(float lo, float hi) {
     return *reinterpret_cast<uint32_t *>(&v);
 }
 
-// x = head + residual in f16 (relative error of the pair about 2^-22).
-__device__ __forceinline__ void split_f16x2(float x0, float x1, uint32_t &head, uint32_t &rest) {
-    head = pack_f16x2(x0, x1);
-    rest = pack_f16x2(x0 - f16lo(head), x1 - f16hi(head));
-}
-
 // ---------------------------------------------------------------------------
 // bf16 helpers (bfloat16 is the upper half of a binary32, so widening is exact)
 // ---------------------------------------------------------------------------
