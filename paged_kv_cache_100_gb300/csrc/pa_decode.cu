@@ -1058,15 +1058,17 @@ pa_decode_bf16_kernel(const __grid_constant__ CUtensorMap kmap,
 // ---------------------------------------------------------------------------
 // Shared-prefix (cascade) attention.  When every block table of the batch
 // starts with the same physical blocks, those blocks' K/V are the same for all
-// sequences: instead of each sequence streaming them, one CTA streams a chunk
-// of the prefix once for 64 query rows (16 per warp) taken across sequences,
-// and the products become dense 16-row tensor-core tiles (query rows on M,
-// tokens and head-dim elements on N/K; P.V with P split into bf16 head and
-// residual).  Each (row, prefix chunk) leaves a partial (max, sum, output) in
-// the workspace; the suffix of every context runs through the decode kernel in
-// partial mode, and the merge kernel combines both.  The attention arithmetic
-// is unchanged: the softmax over the whole context is the merge of softmaxes
-// over its parts.
+// sequences: instead of each sequence streaming them, the prefix is streamed
+// once per KV head for query rows taken across sequences.  Head dimension 128
+// with groups the tcgen05 kernel supports runs it there (pa_prefill.cu, prefix
+// mode: 256 rows per K/V tile); other shapes use the kernel below, where one
+// CTA streams a chunk of the prefix for 64 query rows (16 per warp) as dense
+// 16-row mma.sync tiles (query rows on M, tokens and head-dim elements on N/K;
+// P.V with P split into bf16 head and residual).  Each (row, prefix chunk)
+// leaves a partial (max, sum, output) in the workspace; the suffix of every
+// context runs through the decode kernel in partial mode, and the merge kernel
+// combines both.  The attention arithmetic is unchanged: the softmax over the
+// whole context is the merge of softmaxes over its parts.
 // ---------------------------------------------------------------------------
 template <int D>
 struct PrefixWarp {
