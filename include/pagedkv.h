@@ -52,7 +52,7 @@ extern "C" {
 typedef enum pa_status {
     PA_OK = 0,
     PA_ERR_INVALID_ARG = 1,  /* null pointer, bad size, misaligned pointer, ... */
-    PA_ERR_UNSUPPORTED = 2,  /* valid arguments this build has no kernel for */
+    PA_ERR_UNSUPPORTED = 2,  /* valid arguments the library has no kernel for */
     PA_ERR_CUDA = 3,         /* a CUDA call failed; see pa_last_error() */
     PA_ERR_NO_BLOCKS = 4,    /* block manager: the pool has no free block */
     PA_ERR_WORKSPACE = 5,    /* workspace missing or smaller than required */
