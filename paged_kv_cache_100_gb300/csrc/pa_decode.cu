@@ -766,7 +766,7 @@ struct MhaFp8Consumer {
 template <int D, int G>
 struct GqaTFp8Consumer {
     static_assert(D == 128, "one 128-byte swizzle row per tile row");
-    static_assert(G >= 2 && G <= 8, "one n-tile of query heads");
+    static_assert(G >= 1 && G <= 8, "one n-tile of query heads");
     static constexpr int KS = D / 16;
     static constexpr int ROWS = G;
     static constexpr int kElemBytes = 1;
@@ -1622,6 +1622,9 @@ cudaError_t allow_smem(K kernel, size_t bytes) {
 #ifndef PA_GQA8S_MAX_BLOCKS
 #define PA_GQA8S_MAX_BLOCKS 128
 #endif
+#ifndef PA_MHA8T_MAX_BLOCKS
+#define PA_MHA8T_MAX_BLOCKS 64
+#endif
 constexpr int kNW = 4;   // fp32 kernel
 
 template <int D, class Consumer, int NW, int STAGES>
@@ -1692,7 +1695,17 @@ pa_status dispatch_fp8(int group, const DecodeArgs &a, const void *kc, const voi
     if (a.window > 0) span = std::min(span, a.window / kBlockSize + 1);
     const bool short_span = span <= PA_GQA8S_MAX_BLOCKS;
     switch (group) {
-    case 1: return launch_bf16<D, MhaFp8Consumer<D>, PA_MHA8_WARPS, PA_MHA8_STAGES>(a, kc, vc, rows, stream);
+    case 1:
+        // CTAs of at most PA_MHA8T_MAX_BLOCKS blocks (e.g. 512-token partitions
+        // of long contexts) take the tensor-core consumer with one real query
+        // head of its eight n-tile columns: fewer instructions per block than
+        // the CUDA-core consumer (long_splitk 32k contexts: 327.8 against
+        // 337.0 us); longer spans keep the CUDA-core consumer (7B-shaped batch:
+        // 93.3 against 96.7 us).
+        if (span <= PA_MHA8T_MAX_BLOCKS)
+            return launch_bf16<D, GqaTFp8Consumer<D, 1>, PA_GQA8S_WARPS, PA_GQA8S_STAGES>(a, kc, vc, rows,
+                                                                                        stream);
+        return launch_bf16<D, MhaFp8Consumer<D>, PA_MHA8_WARPS, PA_MHA8_STAGES>(a, kc, vc, rows, stream);
     case 2: return launch_gqa_fp8<2>(short_span, a, kc, vc, rows, stream);
     case 3: return launch_gqa_fp8<3>(short_span, a, kc, vc, rows, stream);
     case 4: return launch_gqa_fp8<4>(short_span, a, kc, vc, rows, stream);
