@@ -114,14 +114,15 @@ def test_block_copy_fp8_bit_exact(pkv):
     assert np.array_equal(kc.cpu().numpy(), kref) and np.array_equal(vc.cpu().numpy(), vref)
 
 
-@pytest.mark.parametrize("name", ["llama7b_mha", "llama70b_gqa", "shared_prefix"])
+@pytest.mark.parametrize("name", ["llama7b_mha", "llama70b_gqa", "long_splitk", "shared_prefix"])
 def test_fp8_full_size_workload_sampled(pkv, name):
     import torch
     wl = W.make_workload(name)
     q, kc, vc, kn, vn, ks, vs = W.fp8_device_values(wl, "cuda")
     bt = torch.from_numpy(wl.block_tables).cuda()
     lens = wl.context_lens
-    out = pkv.decode_fp8(q, kc, vc, ks, vs, bt, torch.from_numpy(lens).cuda(), wl.scale)
+    out = pkv.decode_fp8(q, kc, vc, ks, vs, bt, torch.from_numpy(lens).cuda(), wl.scale,
+                         partition_size=wl.partition_size)
     torch.cuda.synchronize()
     seqs, pairs = H.sample_pairs(wl, lens, n_seqs=5, heads_per_seq=4, seed=3)
     kch, vch, tabs, slens = H.compact_for_sequences(wl, seqs, kc, vc, lens)
