@@ -222,7 +222,9 @@ pa_status pa_decode_shared_prefix_fp8(void *out, const void *query, const void *
  * pa_decode_workspace_bytes(..., PA_DTYPE_FP8_E4M3), device_status, stream).
  * Supported: head_dim 128, group (num_q_heads / num_kv_heads) 1..8.
  * Arithmetic: codes are widened exactly; the query is rounded to f16 once
- * (exact for |q| in [2^-14, 65504]); accumulation is fp32.
+ * (exact for |q| in [2^-14, 65504]); the softmax weights enter P.V as f16
+ * (an output moves by at most 2^-11 of the largest |v| it weighs);
+ * accumulation is fp32.
  */
 pa_status pa_decode_fp8(void *out, const void *query, const void *key_cache,
                         const void *value_cache, const float *k_scales, const float *v_scales,
@@ -374,10 +376,11 @@ pa_status pa_block_copy(void *key_cache, void *value_cache, const int32_t *src_d
  * Supported: bf16, head_dim 128, group (num_q_heads / num_kv_heads) 1, 2, 4, 8
  * or 16.  Arithmetic: S = QK^T and O = PV on tcgen05 tensor cores with fp32
  * accumulation in tensor memory.  The second product runs on f16 operands: P
- * rounded to f16 (2^-11 relative), each V tile converted to f16 in shared
- * memory, which is exact for |v| in [2^-14, 65504]; smaller magnitudes lose
- * at most 2^-25 absolute, larger ones saturate to +-65504 (V beyond f16's
- * range is not supported).  A memset of the work counter,
+ * rounded to f16 (2^-11 relative, so an output moves by at most 2^-11 of the
+ * largest |v| it weighs), each V tile converted to f16 in shared memory, which
+ * is exact for |v| in [2^-14, 65504]; smaller magnitudes lose at most 2^-25
+ * absolute, larger ones saturate to +-65504 (V beyond f16's range is not
+ * supported).  A memset of the work counter,
  * then one kernel launch: one CTA per SM, each taking (256-row tile, KV head,
  * sequence) items in turn.
  */

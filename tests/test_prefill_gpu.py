@@ -218,3 +218,21 @@ def test_full_size_workload_sampled(pkv, name):
                               np.asarray(ctx, np.int32), 1.0 / np.sqrt(pw.head_dim), threads=8)
     got = H.as_f64(out.index_select(0, idx))
     H.assert_close(got, ref, "bf16", f"{name} sampled rows")
+
+
+def test_large_values_within_f16_range(pkv):
+    """P.V runs on f16 operands: V is converted from bf16 in shared memory, exact
+    for magnitudes up to 65504.  Values of a few thousand to 40000 must come
+    through within the tolerance.  (They are positive: a weight's f16 rounding
+    moves an output by up to 2^-11 of the largest |v| it weighs, which a
+    cancelling mix of such values would not keep within 1e-2 of the result.)"""
+    specs = [(0, 40), (100, 130)]
+    wl, hv, q, qs, tables, lens = _case(8, 2, specs, seed=61)
+    rng = np.random.default_rng(62)
+    v = W.bf16_bits_to_f32(hv.value_cache)
+    big = rng.choice([30000.0, 3000.0, 2500.0, 40000.0], size=v.shape).astype(np.float32)
+    keep = np.isnan(v)                                  # slots outside every context stay NaN
+    hv.value_cache = np.where(keep, hv.value_cache, W.to_bf16_bits(big))
+    got, st = _run(pkv, wl, hv, q, qs, tables, lens)
+    assert st == 0
+    H.assert_close(H.as_f64(got), _oracle(wl, hv, q, qs, tables, lens), "bf16", "large V")
