@@ -227,8 +227,12 @@ __device__ __forceinline__ bool describe_item(const PrefillArgs &a, int item, in
     const int tok_per_tile = kRows / g;
     const int lmax = a.max_blocks * kBlockSize;
     if constexpr (!kPrefix) {
-        const int x = item % a.n_mt;
-        const int rest = item / a.n_mt;
+        // kv_hi_cap (prefill): 0 = a (sequence, KV head) group's tiles
+        // together, longest first; 1 = every group's longest tile, then every
+        // group's next one, ...
+        const int groups = a.num_seqs * a.num_kv_heads;
+        const int x = kv_hi_cap ? item / groups : item % a.n_mt;
+        const int rest = kv_hi_cap ? item - x * groups : item / a.n_mt;
         d.kvh = rest % a.num_kv_heads;
         d.b = rest / a.num_kv_heads;
         const int mt = a.n_mt - 1 - x;
@@ -349,11 +353,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         tma_prefetch_desc(&kmap);
         tma_prefetch_desc(&vmap);
     }
+    __syncthreads();   // s_maxl is zero
     if constexpr (kPrefix) {
         // this CTA's one item: the longest context among its rows bounds the
         // positions attended, and (KV head 0) every sequence of these rows
         // must list the chunk's blocks
-        __syncthreads();
         const int kvh = blockIdx.y;
         const int t0 = blockIdx.x * kQT * tok_per_tile;
         const int nseq = min(a.num_seqs - t0, kQT * tok_per_tile);
@@ -371,13 +375,33 @@ __global__ void __launch_bounds__(kThreads, 1)
                     report(a.status, PA_DEV_PREFIX_MISMATCH);
             }
         }
+    } else if (warp == 2) {
+        // Item order for this call: when the chunks bring more tokens than the
+        // contexts held before them (fresh prompts), a group's causal tiles
+        // range from short to long and the tiles go longest first across all
+        // groups; otherwise a group's tiles stay together (their K/V shared in
+        // L2 by the CTAs working at the same time).
+        long long cached = 0, fresh = 0;
+        for (int i = lane; i < a.num_seqs; i += 32) {
+            const int T = a.query_start[i + 1] - a.query_start[i];
+            const int L = a.context_lens[i];
+            fresh += T > 0 ? T : 0;
+            cached += L - T > 0 ? L - T : 0;
+        }
+#pragma unroll
+        for (int o = 16; o >= 1; o >>= 1) {
+            cached += __shfl_xor_sync(0xffffffffu, cached, o);
+            fresh += __shfl_xor_sync(0xffffffffu, fresh, o);
+        }
+        if (lane == 0) *s_maxl = cached < fresh ? 1 : 0;
     }
     if (warp == 1) tmem_alloc(tslot, kTmemCols);
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = *tslot;
-    const int kv_hi_cap = kPrefix ? *s_maxl : 0;
+    // prefix mode: the longest context of the CTA's rows; prefill: the item order
+    const int kv_hi_cap = *s_maxl;
 
     if (warp == 0) {
         // ---------------- TMA producer (and item fetch) ----------------
@@ -400,7 +424,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     for (;;) {
                         const int t = (int)atomicAdd(a.work_counter, 1u);
                         if (t >= a.num_items) break;
-                        if (describe_item<false>(a, t, 0, true, d)) {
+                        if (describe_item<false>(a, t, kv_hi_cap, true, d)) {
                             item = t;
                             break;
                         }
