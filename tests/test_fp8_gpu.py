@@ -57,6 +57,20 @@ def test_decode_fp8_matches_oracle(pkv, hq, hkv, partition_size):
     H.assert_close(got, _oracle(wl, hv), "bf16", f"fp8 {hq}/{hkv} P={partition_size}")
 
 
+@pytest.mark.parametrize("hq,hkv", [(8, 8), (16, 2)])
+@pytest.mark.parametrize("partition_size", [0, 16384])
+def test_decode_fp8_empty_and_one_token_contexts(pkv, hq, hkv, partition_size):
+    """An empty context gives zeros; a one-token context gives that token's value
+    (code times its head's scale, rounded to bf16), on the tensor-core and the
+    CUDA-core MHA consumers alike."""
+    lens = [0, 1, 40, 0, 1]
+    wl = W.custom_workload(len(lens), hq, hkv, 128, lens, dtype="bf16", seed=hq + hkv + 5)
+    hv = W.fp8_host_values(wl)
+    got = H.as_f64(_decode(pkv, wl, hv, partition_size=partition_size))
+    assert np.all(got[0] == 0) and np.all(got[3] == 0)
+    H.assert_close(got, _oracle(wl, hv), "bf16", f"fp8 short contexts {hq}/{hkv} P={partition_size}")
+
+
 def test_cache_write_fp8_bit_exact_including_saturation_and_tiny_values(pkv):
     import torch
     wl = W.custom_workload(6, 8, 4, 128, [0, 15, 16, 31, 300, 7], dtype="bf16", seed=2)
