@@ -86,7 +86,9 @@ constexpr int kOffV = kOffK + kStages * kTile;    // kStages tiles
 constexpr int kOffBar = kOffV + kStages * kTile;
 constexpr int kNumBars = 5 * kStages + 15;
 constexpr int kOffRed = kOffBar + 256;            // [kQT][2 parities][kSplit][128] floats
-constexpr int kSmemBytes = kOffRed + kQT * 2 * kSplit * kRows * 4;
+constexpr int kPermMax = 64;                      // prefill: sequences ordered by length (at most)
+constexpr int kOffPerm = kOffRed + kQT * 2 * kSplit * kRows * 4;   // int [kPermMax]
+constexpr int kSmemBytes = kOffPerm + kPermMax * 4;
 // The tiles need 1024-byte alignment; the dynamic shared memory of a kernel
 // without static shared memory starts on such a boundary, and the kernel
 // checks it (PA_DEV_SMEM_ALIGN) instead of reserving slack.
@@ -222,7 +224,8 @@ struct Item {
 // CTA writes split-K partials instead of outputs.
 template <bool kPrefix>
 __device__ __forceinline__ bool describe_item(const PrefillArgs &a, int item, int kv_hi_cap,
-                                              bool report_errors, Item &d) {
+                                              bool report_errors, Item &d,
+                                              const int *perm = nullptr) {
     const int g = a.group;
     const int tok_per_tile = kRows / g;
     const int lmax = a.max_blocks * kBlockSize;
@@ -235,6 +238,7 @@ __device__ __forceinline__ bool describe_item(const PrefillArgs &a, int item, in
         const int rest = kv_hi_cap ? item - x * groups : item / a.n_mt;
         d.kvh = rest % a.num_kv_heads;
         d.b = rest / a.num_kv_heads;
+        if (perm != nullptr) d.b = perm[d.b];   // sequences longest first
         const int mt = a.n_mt - 1 - x;
         d.q0 = a.query_start[d.b];
         d.T = a.query_start[d.b + 1] - d.q0;
@@ -394,6 +398,20 @@ __global__ void __launch_bounds__(kThreads, 1)
             fresh += __shfl_xor_sync(0xffffffffu, fresh, o);
         }
         if (lane == 0) *s_maxl = cached < fresh ? 1 : 0;
+        // sequences longest context first (ties by index), so that the call
+        // ends on the shortest ones
+        if (a.num_seqs <= kPermMax) {
+            int *perm = reinterpret_cast<int *>(base + kOffPerm);
+            for (int i = lane; i < a.num_seqs; i += 32) {
+                const int li = a.context_lens[i];
+                int r = 0;
+                for (int j = 0; j < a.num_seqs; ++j) {
+                    const int lj = a.context_lens[j];
+                    r += (lj > li) | ((lj == li) & (j < i));
+                }
+                perm[r] = i;
+            }
+        }
     }
     if (warp == 1) tmem_alloc(tslot, kTmemCols);
     tc_fence_before();
@@ -402,6 +420,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t tmem = *tslot;
     // prefix mode: the longest context of the CTA's rows; prefill: the item order
     const int kv_hi_cap = *s_maxl;
+    const int *perm = (!kPrefix && a.num_seqs <= kPermMax) ? reinterpret_cast<const int *>(base + kOffPerm)
+                                                           : nullptr;
 
     if (warp == 0) {
         // ---------------- TMA producer (and item fetch) ----------------
@@ -424,7 +444,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     for (;;) {
                         const int t = (int)atomicAdd(a.work_counter, 1u);
                         if (t >= a.num_items) break;
-                        if (describe_item<false>(a, t, kv_hi_cap, true, d)) {
+                        if (describe_item<false>(a, t, kv_hi_cap, true, d, perm)) {
                             item = t;
                             break;
                         }
@@ -554,7 +574,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
                 if (item < 0) break;
                 Item d;
-                describe_item<kPrefix>(a, item, kv_hi_cap, false, d);
+                describe_item<kPrefix>(a, item, kv_hi_cap, false, d, perm);
                 const int n = d.n_tiles;
                 if (!wait_or_fail(&bars[kQFull], it & 1, fail, a.status) ||
                     !wait_or_fail(&bars[kKFull + gstep % kStages], (gstep / kStages) & 1, fail, a.status))
@@ -619,7 +639,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             if (item < 0) break;
             Item d;
-            describe_item<kPrefix>(a, item, kv_hi_cap, false, d);
+            describe_item<kPrefix>(a, item, kv_hi_cap, false, d, perm);
             for (int j = 0; ok && j < d.n_tiles; ++j) {
                 const uint32_t gs = gstep + j;
                 const int st = gs % kStages;
@@ -672,7 +692,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             // them reach the group's named barriers equally often
             if (!group_all(x, item >= 0 && ok && !*fail)) break;
             Item d;
-            describe_item<kPrefix>(a, item, kv_hi_cap, false, d);
+            describe_item<kPrefix>(a, item, kv_hi_cap, false, d, perm);
             const int n_tiles = d.n_tiles;
             if (x == 0 || d.has_b) {
                 const float sl2k = a.k_scales != nullptr ? a.scale_log2 * a.k_scales[d.kvh] : a.scale_log2;
