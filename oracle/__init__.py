@@ -72,7 +72,8 @@ def _load():
             lib.pao_e4m3_encode.restype = ctypes.c_uint8
             lib.pao_cache_write.argtypes = [vp, vp, vp, vp, vp, i32, i32, i32, i32, i32, i32]
             lib.pao_cache_write.restype = i32
-            lib.pao_block_copy.argtypes = [vp, vp, vp, i32, i32, i32, i32, i32, i32]
+            lib.pao_block_copy.argtypes = [vp, vp, vp, i32, i32, i32, i32, i32, i32,
+                                           ctypes.POINTER(ctypes.c_int)]
             lib.pao_block_copy.restype = i32
             lib.pao_paged_prefill.argtypes = [vp, vp, i32, vp, vp, i32, vp, vp, vp, vp, vp, i32,
                                               i32, i32, i32, i32, i32, i32, dbl, i32, i32]
@@ -270,18 +271,25 @@ def cache_write(key_cache, value_cache, key, value, slot_mapping) -> None:
         raise ValueError(f"oracle cache_write failed with code {rc}")
 
 
-def block_copy(key_cache, value_cache, pairs) -> None:
-    """In-place block copy; ``pairs`` is an int array [P][2] of (src, dst)."""
+def block_copy(key_cache, value_cache, pairs) -> bool:
+    """In-place block copy; ``pairs`` is an int array [P][2] of (src, dst).
+
+    Pairs are independent copies into fresh blocks (see ``pao_block_copy``):
+    a pair with an index outside the pool, or whose dst is the src or dst of
+    another pair (src != dst for both), is skipped.  Returns True when some
+    pair was skipped."""
     lib = _load()
     for a in (key_cache, value_cache):
         if not a.flags.c_contiguous:
             raise ValueError("pools must be C-contiguous (written in place)")
     pairs = np.ascontiguousarray(np.asarray(pairs, dtype=np.int32).reshape(-1, 2))
     NB, Hkv, BS, D = key_cache.shape
+    skipped = ctypes.c_int(0)
     rc = lib.pao_block_copy(_ptr(key_cache), _ptr(value_cache), _ptr(pairs), pairs.shape[0],
-                            Hkv, D, BS, NB, key_cache.itemsize)
+                            Hkv, D, BS, NB, key_cache.itemsize, ctypes.byref(skipped))
     if rc != 0:
         raise ValueError(f"oracle block_copy failed with code {rc}")
+    return bool(skipped.value)
 
 
 def swap_out(key_cache, value_cache, block_ids) -> np.ndarray:

@@ -381,27 +381,63 @@ int pao_cache_write_fp8(uint8_t *key_cache, uint8_t *value_cache, const uint16_t
 }
 
 /*
- * Block copy (copy-on-write): for each pair (src, dst), in list order, the
- * whole physical block dst of both pools becomes a copy of block src.
+ * Block copy (copy-on-write), "PagedAttention por dentro", "Copy-on-write para
+ * sampling paralelo": a sequence about to write into a block it shares gets a
+ * copy of that one block in a block taken from the pool, and only the copy
+ * changes.  Each pair (src, dst) of the list is one such copy: the whole
+ * physical block dst of both pools becomes block src as it was before the
+ * call.  Since every copy on the pages goes into a freshly taken block, no copy
+ * of a list writes a block that another copy of the same list reads or
+ * writes; a list is read that way, pair by pair:
+ *   - a pair with an index outside [0, num_blocks) is skipped;
+ *   - a pair with src == dst changes nothing (it is not "live");
+ *   - a live pair whose dst is the src or the dst of another live pair is
+ *     skipped (it would overwrite what the other reads, or what it writes);
+ *   - every other live pair is copied.
+ * The copied pairs then touch disjoint destinations that no copied pair
+ * reads, so copying them one after another in list order gives the same
+ * pools as copying them all at once from the pools before the call.
+ * *skipped receives 1 when some pair was skipped, else 0.
  * pairs holds 2 * num_pairs int32 values: src0, dst0, src1, dst1, ...
  */
 int pao_block_copy(void *key_cache, void *value_cache, const int32_t *pairs,
                    int num_pairs, int num_kv_heads, int head_dim,
-                   int block_size, int num_blocks, int elem_bytes)
+                   int block_size, int num_blocks, int elem_bytes, int *skipped)
 {
-    if (!key_cache || !value_cache || (!pairs && num_pairs > 0))
+    if (!key_cache || !value_cache || !skipped || (!pairs && num_pairs > 0) || num_pairs < 0)
         return PAO_ERR_ARG;
     const int64_t block_bytes = (int64_t)num_kv_heads * block_size * head_dim * elem_bytes;
-    int p;
+    char *live = (char *)calloc((size_t)num_pairs + 1, 1);
+    if (!live)
+        return PAO_ERR_NOMEM;
+    *skipped = 0;
+    int p, q;
     for (p = 0; p < num_pairs; ++p) {
         int32_t src = pairs[2 * p], dst = pairs[2 * p + 1];
-        if (src < 0 || src >= num_blocks || dst < 0 || dst >= num_blocks)
-            return PAO_ERR_INDEX;
-        memmove((char *)key_cache + dst * block_bytes, (const char *)key_cache + src * block_bytes,
-                (size_t)block_bytes);
-        memmove((char *)value_cache + dst * block_bytes,
-                (const char *)value_cache + src * block_bytes, (size_t)block_bytes);
+        if (src < 0 || src >= num_blocks || dst < 0 || dst >= num_blocks) {
+            *skipped = 1;
+            continue;
+        }
+        live[p] = src != dst;
     }
+    for (p = 0; p < num_pairs; ++p) {
+        if (!live[p])
+            continue;
+        int32_t src = pairs[2 * p], dst = pairs[2 * p + 1];
+        int clash = 0;
+        for (q = 0; q < num_pairs; ++q)
+            if (q != p && live[q] && (pairs[2 * q] == dst || pairs[2 * q + 1] == dst))
+                clash = 1;
+        if (clash) {
+            *skipped = 1;
+            continue;
+        }
+        memcpy((char *)key_cache + dst * block_bytes, (const char *)key_cache + src * block_bytes,
+               (size_t)block_bytes);
+        memcpy((char *)value_cache + dst * block_bytes,
+               (const char *)value_cache + src * block_bytes, (size_t)block_bytes);
+    }
+    free(live);
     return PAO_OK;
 }
 

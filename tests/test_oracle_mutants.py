@@ -49,7 +49,10 @@ MUTANTS = {
     "fp8_write_multiplies": ("float kq = kx / k_scales[kvh];", "float kq = kx * k_scales[kvh];"),
     "window_off_by_one": ("const int first = (window > 0 && L > window) ? L - window : 0;",
                           "const int first = (window > 0 && L > window) ? L - window + 1 : 0;"),
-    "copy_skips_v": ("memmove((char *)value_cache + dst * block_bytes,", "(void)(value_cache + dst * block_bytes,"),
+    "copy_skips_v": ("memcpy((char *)value_cache + dst * block_bytes,", "(void)(value_cache + dst * block_bytes,"),
+    "copy_ignores_clashes": ("        if (clash) {\n            *skipped = 1;", "        if (0) {\n            *skipped = 1;"),
+    "copy_checks_dst_only": ("(pairs[2 * q] == dst || pairs[2 * q + 1] == dst)", "(pairs[2 * q + 1] == dst)"),
+    "copy_self_pair_live": ("live[p] = src != dst;", "live[p] = 1;"),
 }
 
 from tests import test_oracle_fp8_pins as fp8pins  # noqa: E402
@@ -75,6 +78,9 @@ PIN_FUNCS = [
     lambda g: pins.test_cache_write_places_each_row_in_its_slot_and_nothing_else(),
     lambda g: pins.test_cache_write_then_decode_sees_the_new_token(),
     lambda g: pins.test_block_copy_duplicates_whole_blocks_and_cow_is_invisible_to_decode(),
+    lambda g: pins.test_block_copy_chained_list_skips_the_pair_that_overwrites_a_source(),
+    lambda g: pins.test_block_copy_duplicate_destination_skips_both_pairs(),
+    lambda g: pins.test_block_copy_self_pair_is_a_no_op_that_blocks_nothing(),
 ]
 
 

@@ -347,11 +347,54 @@ def test_block_copy_duplicates_whole_blocks_and_cow_is_invisible_to_decode():
     assert np.array_equal(before, after)
 
 
-def test_block_copy_applies_pairs_in_order():
-    kc = np.arange(4 * 2 * 16 * 2, dtype=np.float32).reshape(4, 2, 16, 2)
-    vc = -kc
-    oracle.block_copy(kc, vc, [[0, 1], [1, 2]])              # chained: 2 gets the new 1 == 0
-    assert np.array_equal(kc[2], kc[0]) and np.array_equal(vc[2], vc[0])
+# Block copy lists ("PagedAttention por dentro", "Copy-on-write para sampling
+# paralelo"): every copy on the pages goes into a freshly taken block, so the
+# pairs of one list are independent copies.  A pair whose destination another
+# pair reads or writes is not such a copy and is skipped; the expectations
+# below are written from the pools before the call.
+def _numbered_pools(nb=6):
+    kc = np.arange(nb * 2 * 16 * 2, dtype=np.float32).reshape(nb, 2, 16, 2)
+    return kc, -kc - 1.0
+
+
+def test_block_copy_chained_list_skips_the_pair_that_overwrites_a_source():
+    kc, vc = _numbered_pools()
+    k0, v0 = kc.copy(), vc.copy()
+    skipped = oracle.block_copy(kc, vc, [[0, 1], [1, 2], [3, 4]])
+    assert skipped
+    # (0, 1) would overwrite the source of (1, 2): skipped; (1, 2) copies the old block 1
+    assert np.array_equal(kc[1], k0[1]) and np.array_equal(vc[1], v0[1])
+    assert np.array_equal(kc[2], k0[1]) and np.array_equal(vc[2], v0[1])
+    assert np.array_equal(kc[4], k0[3]) and np.array_equal(vc[4], v0[3])
+    for b in (0, 3, 5):
+        assert np.array_equal(kc[b], k0[b]) and np.array_equal(vc[b], v0[b])
+
+
+def test_block_copy_duplicate_destination_skips_both_pairs():
+    kc, vc = _numbered_pools()
+    k0, v0 = kc.copy(), vc.copy()
+    assert oracle.block_copy(kc, vc, [[0, 2], [1, 2], [0, 5]])
+    assert np.array_equal(kc[2], k0[2]) and np.array_equal(vc[2], v0[2])
+    assert np.array_equal(kc[5], k0[0]) and np.array_equal(vc[5], v0[0])
+    # two copies of one source into distinct fresh blocks are independent
+    kc, vc = _numbered_pools()
+    assert not oracle.block_copy(kc, vc, [[0, 1], [0, 2]])
+    assert np.array_equal(kc[1], k0[0]) and np.array_equal(kc[2], k0[0])
+
+
+def test_block_copy_self_pair_is_a_no_op_that_blocks_nothing():
+    kc, vc = _numbered_pools()
+    k0, v0 = kc.copy(), vc.copy()
+    assert not oracle.block_copy(kc, vc, [[3, 3], [3, 1]])
+    assert np.array_equal(kc[3], k0[3]) and np.array_equal(kc[1], k0[3])
+    assert np.array_equal(vc[1], v0[3])
+
+
+def test_block_copy_skips_pairs_outside_the_pool():
+    kc, vc = _numbered_pools()
+    k0 = kc.copy()
+    assert oracle.block_copy(kc, vc, [[0, 6], [-1, 2], [4, 5]])
+    assert np.array_equal(kc[:5], k0[:5]) and np.array_equal(kc[5], k0[4])
 
 
 # ---------------------------------------------------------------------------
