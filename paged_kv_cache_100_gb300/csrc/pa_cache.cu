@@ -113,13 +113,21 @@ pa_cache_write_fp8_kernel(uint4 *__restrict__ kc, uint4 *__restrict__ vc,
 
 // grid.x = pair, grid.y = slice of the block; every thread copies up to
 // kChunksPerThread 16-byte chunks of K and of V.
+//
+// The pairs of one list are independent copies into fresh blocks (every
+// copy-on-write takes its destination from the pool), so they run
+// concurrently.  A pair is "live" when both indices are in the pool and
+// src != dst; a live pair whose dst is the src or the dst of another live
+// pair would race with it and is skipped and flagged.  Each CTA checks its
+// own pair against the whole list (num_pairs reads of 8 bytes, spread over the
+// CTA's threads).
 constexpr int kCopyThreads = 256;
 constexpr int kChunksPerThread = 4;
 
 __global__ void __launch_bounds__(kCopyThreads)
 pa_block_copy_kernel(uint4 *__restrict__ kc, uint4 *__restrict__ vc,
-                     const int32_t *__restrict__ src_dst, int64_t chunks_per_block, int num_blocks,
-                     int32_t *status) {
+                     const int32_t *__restrict__ src_dst, int num_pairs, int64_t chunks_per_block,
+                     int num_blocks, int32_t *status) {
     grid_dependency_wait();
     grid_dependents_launch();
     const int32_t src = src_dst[2 * blockIdx.x];
@@ -129,6 +137,18 @@ pa_block_copy_kernel(uint4 *__restrict__ kc, uint4 *__restrict__ vc,
         return;
     }
     if (src == dst) return;
+    bool clash = false;
+    for (int q = threadIdx.x; q < num_pairs; q += kCopyThreads) {
+        if (q == (int)blockIdx.x) continue;
+        const int2 o = reinterpret_cast<const int2 *>(src_dst)[q];
+        const bool live = (unsigned)o.x < (unsigned)num_blocks &&
+                          (unsigned)o.y < (unsigned)num_blocks && o.x != o.y;
+        clash |= live && (o.x == dst || o.y == dst);
+    }
+    if (__syncthreads_or(clash)) {
+        if (blockIdx.y == 0 && threadIdx.x == 0) report(status, PA_DEV_BAD_COPY_PAIR);
+        return;
+    }
     const int64_t first = (int64_t)blockIdx.y * kCopyThreads * kChunksPerThread + threadIdx.x;
     const uint4 *ks = kc + (int64_t)src * chunks_per_block;
     const uint4 *vs = vc + (int64_t)src * chunks_per_block;
@@ -269,7 +289,7 @@ extern "C" pa_status pa_block_copy(void *key_cache, void *value_cache, const int
     if (num_pairs == 0) return PA_OK;
     if (!key_cache || !value_cache || !src_dst) return PA_ERR_INVALID_ARG;
     if (!aligned16(key_cache) || !aligned16(value_cache) ||
-        (reinterpret_cast<uintptr_t>(src_dst) & 3u))
+        (reinterpret_cast<uintptr_t>(src_dst) & 7u))
         return PA_ERR_INVALID_ARG;
     const int64_t chunks = block_bytes / 16;
     const int64_t per_cta = (int64_t)kCopyThreads * kChunksPerThread;
@@ -278,8 +298,8 @@ extern "C" pa_status pa_block_copy(void *key_cache, void *value_cache, const int
     dim3 grid((unsigned)num_pairs, (unsigned)slices);
     cudaError_t e = launch_chained(
         pa_block_copy_kernel, grid, dim3(kCopyThreads), 0, static_cast<cudaStream_t>(stream),
-        static_cast<uint4 *>(key_cache), static_cast<uint4 *>(value_cache), src_dst, chunks,
-        num_blocks, device_status);
+        static_cast<uint4 *>(key_cache), static_cast<uint4 *>(value_cache), src_dst, num_pairs,
+        chunks, num_blocks, device_status);
     if (e != cudaSuccess) return cuda_failure(e, "pa_block_copy_kernel launch");
     count_launches(1);
     return PA_OK;

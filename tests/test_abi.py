@@ -123,6 +123,7 @@ def test_cache_write_and_block_copy_argument_checks(lib):
     bc = lib.pa_block_copy
     assert bc(16, 16, 16, 1, 8, 128, 16, 0, 1, None, None) == _lib.PA_ERR_INVALID_ARG
     assert bc(16, 16, None, 1, 8, 128, 16, 4, 1, None, None) == _lib.PA_ERR_INVALID_ARG
+    assert bc(16, 16, 20, 1, 8, 128, 16, 4, 1, None, None) == _lib.PA_ERR_INVALID_ARG  # pairs not 8-byte aligned
     assert bc(None, None, None, 0, 8, 128, 16, 4, 1, None, None) == _lib.PA_OK
 
 

@@ -79,6 +79,44 @@ def test_block_copy_bit_exact_small(pkv):
     assert H.device_to_host_bits(vc).tobytes() == vref.tobytes()
 
 
+LISTS = {
+    "chained": [[0, 1], [1, 2], [3, 4]],
+    "duplicate_dst": [[0, 2], [1, 2], [0, 5]],
+    "shared_src": [[0, 1], [0, 2], [3, 4]],
+    "self_pair": [[3, 3], [3, 1]],
+    "out_of_range": [[0, 99], [-1, 2], [4, 5]],
+    "cycle": [[0, 1], [1, 0], [2, 3]],
+}
+
+
+@pytest.mark.parametrize("name", sorted(LISTS) + ["random"])
+def test_block_copy_lists_match_oracle_and_flag(pkv, name):
+    """Chained, duplicate-destination, self and out-of-range pair lists: the
+    pools equal the oracle's byte for byte and the flag is raised exactly when
+    the oracle skipped a pair."""
+    import torch
+    nb = 64 if name == "random" else 12
+    rng = np.random.default_rng(7)
+    kc_h = W.to_bf16_bits(rng.standard_normal((nb, 2, 16, 64), dtype=np.float32))
+    vc_h = W.to_bf16_bits(rng.standard_normal((nb, 2, 16, 64), dtype=np.float32))
+    if name == "random":
+        pairs = rng.integers(0, nb, size=(40, 2)).astype(np.int32)
+        pairs[::7, 1] = nb + 3                      # a few out of range
+    else:
+        pairs = np.asarray(LISTS[name], dtype=np.int32)
+    kc = H.host_to_device(kc_h, torch.bfloat16)
+    vc = H.host_to_device(vc_h, torch.bfloat16)
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    pkv.block_copy(kc, vc, torch.from_numpy(pairs).cuda(), status=status)
+    torch.cuda.synchronize()
+    kref, vref = kc_h.copy(), vc_h.copy()
+    skipped = oracle.block_copy(kref, vref, pairs)
+    assert H.device_to_host_bits(kc).tobytes() == kref.tobytes()
+    assert H.device_to_host_bits(vc).tobytes() == vref.tobytes()
+    assert bool(int(status.item()) & pkv._lib.PA_DEV_BAD_COPY_PAIR) == skipped
+    assert int(status.item()) & ~pkv._lib.PA_DEV_BAD_COPY_PAIR == 0
+
+
 def test_bad_slots_and_pairs_are_flagged_not_followed(pkv):
     import torch
     wl = W.custom_workload(2, 4, 4, 64, [3, 9], dtype="bf16", seed=4)
@@ -101,30 +139,69 @@ def test_bad_slots_and_pairs_are_flagged_not_followed(pkv):
     assert torch.equal(kc.view(torch.int16), before_k.view(torch.int16))
 
 
-@pytest.mark.parametrize("name", ["llama7b_mha", "llama70b_gqa", "shared_prefix"])
-def test_full_size_cache_write_and_copy_bit_exact(pkv, name):
-    """Every appended row lands in its slot, the copies equal their sources, nothing else moves."""
+def _checked_blocks(wl, n_canary=64, seed=0):
+    """The blocks the step writes (slots and copy-on-write destinations), their
+    copy sources, and a seeded sample of other blocks (canaries), sorted."""
+    slots = wl.slot_mapping[wl.slot_mapping >= 0]
+    touched = set((slots // 16).tolist())
+    for s, d in wl.cow_pairs.tolist():
+        touched |= {int(s), int(d)}
+    touched = np.asarray(sorted(touched), dtype=np.int64)
+    rest = np.setdiff1d(np.arange(wl.num_blocks, dtype=np.int64), touched)
+    canary = np.random.default_rng(seed).choice(rest, size=min(n_canary, rest.size), replace=False)
+    return touched, np.sort(np.concatenate([touched, canary]))
+
+
+@pytest.mark.parametrize("kv", ["bf16", "fp8"])
+@pytest.mark.parametrize("name", W.WORKLOADS)
+def test_full_size_step_writes_match_oracle(pkv, name, kv):
+    """The step's cache write (and copy-on-write copies) at the bench's full sizes,
+    byte for byte against the oracle: the written blocks, their copy sources and
+    64 canary blocks are replayed through oracle.cache_write(_fp8) and
+    oracle.block_copy on host copies taken before the step; every other block
+    of both pools must be unchanged."""
     import torch
     wl = W.make_workload(name)
-    q, kc, vc, kn, vn = W.device_values(wl, "cuda")
+    fp8 = kv == "fp8"
+    if fp8 and wl.dtype != "bf16":
+        pytest.skip("FP8 pools take bf16 rows; the f32 workload has none")
+    if fp8:
+        q, kc, vc, kn, vn, ks, vs = W.fp8_device_values(wl, "cuda")
+    else:
+        q, kc, vc, kn, vn = W.device_values(wl, "cuda")
+    del q
+    touched, blocks = _checked_blocks(wl)
+    idx = torch.from_numpy(blocks).cuda()
+    kref, vref = H.device_to_host_bits(kc.index_select(0, idx)), H.device_to_host_bits(vc.index_select(0, idx))
     k0, v0 = kc.clone(), vc.clone()
     slots = torch.from_numpy(wl.slot_mapping).cuda()
-    pkv.cache_write(kc, vc, kn, vn, slots)
-    pairs = torch.from_numpy(wl.cow_pairs).cuda()
+    if fp8:
+        pkv.cache_write_fp8(kc, vc, kn, vn, slots, ks, vs)
+    else:
+        pkv.cache_write(kc, vc, kn, vn, slots)
     if wl.cow_pairs.shape[0]:
-        pkv.block_copy(kc, vc, pairs)
+        pkv.block_copy(kc, vc, torch.from_numpy(wl.cow_pairs).cuda())
     torch.cuda.synchronize()
-    # expected pools, built with plain indexing on the device (no library kernel)
-    ke, ve = k0.clone(), v0.clone()
-    blk = slots // 16
-    off = slots % 16
-    ke[blk, :, off, :] = kn
-    ve[blk, :, off, :] = vn
-    for s, d in wl.cow_pairs.tolist():
-        ke[d] = ke[s]
-        ve[d] = ve[s]
-    assert torch.equal(kc.view(torch.int16), ke.view(torch.int16))
-    assert torch.equal(vc.view(torch.int16), ve.view(torch.int16))
+    kgot, vgot = H.device_to_host_bits(kc.index_select(0, idx)), H.device_to_host_bits(vc.index_select(0, idx))
+    # the oracle on the checked blocks, renumbered 0 .. len(blocks) - 1
+    pos = np.searchsorted(blocks, wl.slot_mapping // 16)
+    local_slots = pos * 16 + wl.slot_mapping % 16
+    kn_h, vn_h = H.device_to_host_bits(kn), H.device_to_host_bits(vn)
+    if fp8:
+        oracle.cache_write_fp8(kref, vref, kn_h, vn_h, local_slots, ks.cpu().numpy(), vs.cpu().numpy())
+    else:
+        oracle.cache_write(kref, vref, kn_h, vn_h, local_slots)
+    if wl.cow_pairs.shape[0]:
+        assert not oracle.block_copy(kref, vref, np.searchsorted(blocks, wl.cow_pairs))
+    assert kgot.tobytes() == kref.tobytes()
+    assert vgot.tobytes() == vref.tobytes()
+    # nothing outside the written blocks moved: put their old contents back and
+    # compare the whole pools with the copies taken before the step
+    tidx = torch.from_numpy(touched).cuda()
+    kc.index_copy_(0, tidx, k0.index_select(0, tidx))
+    vc.index_copy_(0, tidx, v0.index_select(0, tidx))
+    assert torch.equal(kc.view(torch.uint8), k0.view(torch.uint8))
+    assert torch.equal(vc.view(torch.uint8), v0.view(torch.uint8))
 
 
 def test_shared_prefix_step_matches_oracle_and_cow_is_invisible(pkv):
