@@ -74,6 +74,8 @@ typedef enum pa_dtype {
 #define PA_DEV_PREFIX_MISMATCH 32 /* pa_decode_shared_prefix: tables do not share the prefix */
 #define PA_DEV_BAD_QUERY_LEN  64  /* pa_prefill: a chunk longer than max_query_len */
 #define PA_DEV_SMEM_ALIGN    128  /* pa_prefill: shared memory not 1024-byte aligned (nothing computed) */
+#define PA_DEV_RANGE         256  /* a value outside f16's finite range (|x| >= 65536, or infinite)
+                                     reached an f16 operand; see the entry points that stage in f16 */
 
 /* Human-readable name of a status. Never NULL. */
 const char *pa_status_string(pa_status status);
@@ -151,9 +153,17 @@ pa_status pa_decode(void *out, const void *query, const void *key_cache, const v
  * Paged decode attention for a batch whose block tables all begin with the same
  * num_prefix_blocks physical blocks (a shared prefix: "PagedAttention por
  * dentro", section "Copy-on-write para sampling paralelo" and "Prefix caching
- * cross-session" - several sequences reading the same blocks).  Same result
- * as pa_decode with the same arguments; the shared blocks are read once per
- * KV head for all sequences instead of once per sequence.
+ * cross-session" - several sequences reading the same blocks).  The result of
+ * pa_decode with the same arguments, within pa_decode's tolerance; the shared
+ * blocks are read once per KV head for all sequences instead of once per
+ * sequence.
+ * Precision: at head_dim 128 and groups 1, 2, 4, 8 or 16 the prefix runs on
+ * the tensor-core kernel of pa_prefill, whose P.V takes f16 operands (see
+ * pa_prefill): the softmax weights are rounded to f16 and each prefix V value
+ * is converted to f16, exact for |v| in [2^-14, 65504].  A prefix V value of
+ * magnitude 65536 or more (or infinite) saturates to +-65504 and the call
+ * flags PA_DEV_RANGE; such results are not those of pa_decode.  Other shapes
+ * run the prefix on bf16 tensor-core tiles without that limit.
  *  num_prefix_blocks  length of the shared prefix in blocks; the blocks are
  *                     taken from the first row of block_tables and every row
  *                     must list the same ones (a row that does not is flagged
@@ -222,9 +232,10 @@ pa_status pa_decode_shared_prefix_fp8(void *out, const void *query, const void *
  * pa_decode_workspace_bytes(..., PA_DTYPE_FP8_E4M3), device_status, stream).
  * Supported: head_dim 128, group (num_q_heads / num_kv_heads) 1..8.
  * Arithmetic: codes are widened exactly; the query is rounded to f16 once
- * (exact for |q| in [2^-14, 65504]); the softmax weights enter P.V as f16
- * (an output moves by at most 2^-11 of the largest |v| it weighs);
- * accumulation is fp32.
+ * (exact for |q| in [2^-14, 65504]; a query element of magnitude 65536 or
+ * more, or infinite, becomes infinite and the call flags PA_DEV_RANGE); the
+ * softmax weights enter P.V as f16 (an output moves by at most 2^-11 of the
+ * largest |v| it weighs); accumulation is fp32.
  */
 pa_status pa_decode_fp8(void *out, const void *query, const void *key_cache,
                         const void *value_cache, const float *k_scales, const float *v_scales,
@@ -338,10 +349,20 @@ pa_status pa_cache_write(void *key_cache, void *value_cache, const void *key, co
  * bit-exact copy of block src in both pools (all KV heads, all 16 slots).
  * Source: "PagedAttention por dentro", section "Copy-on-write para sampling
  * paralelo" (on divergence only the last shared block is copied).
- *  src_dst     device int32 [num_pairs][2] = (src, dst)
- * Pairs run concurrently: no dst may appear twice or equal another pair's src
- * (the host block manager never emits such lists); src == dst is a no-op.
- * A pair with an index out of range is skipped and flagged.
+ *  src_dst     device int32 [num_pairs][2] = (src, dst), 8-byte aligned
+ * The pairs are independent copies into fresh blocks (on the pages every copy
+ * goes into a block just taken from the pool), so they run concurrently and
+ * each copies block src as it was before the call:
+ *  - a pair with an index outside [0, num_blocks) is skipped and flagged
+ *    PA_DEV_BAD_COPY_PAIR;
+ *  - a pair with src == dst changes nothing;
+ *  - a pair (src != dst) whose dst is the src or the dst of another pair
+ *    (both indices in range, src != dst) is skipped and flagged
+ *    PA_DEV_BAD_COPY_PAIR: a chained list such as (a, b), (b, c) copies only
+ *    (b, c), and two pairs with one dst both stay undone.
+ * Every other pair is copied.  The host block manager never emits a skipped
+ * pair.  Each CTA checks its pair against the whole list, so the kernel reads
+ * the list num_pairs times (from L2).
  */
 pa_status pa_block_copy(void *key_cache, void *value_cache, const int32_t *src_dst, int num_pairs,
                         int num_kv_heads, int head_dim, int block_size, int num_blocks,
@@ -379,8 +400,10 @@ pa_status pa_block_copy(void *key_cache, void *value_cache, const int32_t *src_d
  * rounded to f16 (2^-11 relative, so an output moves by at most 2^-11 of the
  * largest |v| it weighs), each V tile converted to f16 in shared memory, which
  * is exact for |v| in [2^-14, 65504]; smaller magnitudes lose at most 2^-25
- * absolute, larger ones saturate to +-65504 (V beyond f16's range is not
- * supported).  A memset of the work counter,
+ * absolute, larger ones (|v| >= 65536, or infinite) saturate to +-65504 and
+ * the call flags PA_DEV_RANGE (V beyond f16's range is not supported; the
+ * flag says the result is not the attention of the given values).  A memset
+ * of the work counter,
  * then one kernel launch: one CTA per SM, each taking (256-row tile, KV head,
  * sequence) items in turn.
  */
@@ -508,6 +531,26 @@ pa_status pa_bm_append_slots(pa_bm *bm, const int32_t *seqs, int n, int64_t *slo
  * context lengths [n] for the listed sequences. */
 pa_status pa_bm_fill_tables(const pa_bm *bm, const int32_t *seqs, int n, int32_t *tables,
                             int max_blocks, int32_t *context_lens);
+/* Occupancy of the pool and its internal fragmentation ("Cómo funciona
+ * realmente vLLM", section "La sobre-reserva estática y los tres tipos de
+ * desperdicio": slots reserved for a sequence that never receive a token;
+ * "PagedAttention por dentro", opening section: paging keeps that waste under
+ * 4 %, since only a sequence's last block can be partly empty).  A block's
+ * filled slots are the most tokens any table entry pointing at it holds (an
+ * entry fills its block from offset 0 up, and shared entries fill it alike). */
+typedef struct pa_bm_stats_t {
+    int64_t num_blocks;        /* pool size */
+    int64_t free_blocks;       /* on the free list */
+    int64_t evictable_blocks;  /* released but kept for the prefix cache */
+    int64_t used_blocks;       /* reference count >= 1 */
+    int64_t shared_blocks;     /* reference count >= 2 */
+    int64_t reserved_slots;    /* used_blocks * block_size */
+    int64_t filled_slots;      /* slots of used blocks holding a token */
+    int64_t logical_tokens;    /* tokens of all sequences held in blocks, a shared
+                                  block counted once per sequence */
+    double internal_fragmentation; /* (reserved - filled) / reserved; 0 if nothing is used */
+} pa_bm_stats_t;
+pa_status pa_bm_stats(const pa_bm *bm, pa_bm_stats_t *out);
 
 #ifdef __cplusplus
 }

@@ -78,7 +78,17 @@ SIGNATURES = {
     "pa_bm_table": (i32, [vp, i32, vp, i32]),
     "pa_bm_append_slots": (i32, [vp, vp, i32, vp, vp, ptr_int, ptr_int]),
     "pa_bm_fill_tables": (i32, [vp, vp, i32, vp, i32, vp]),
+    "pa_bm_stats": (i32, [vp, vp]),
 }
+
+
+class BmStats(ctypes.Structure):
+    """pa_bm_stats_t"""
+    _fields_ = [("num_blocks", ctypes.c_int64), ("free_blocks", ctypes.c_int64),
+                ("evictable_blocks", ctypes.c_int64), ("used_blocks", ctypes.c_int64),
+                ("shared_blocks", ctypes.c_int64), ("reserved_slots", ctypes.c_int64),
+                ("filled_slots", ctypes.c_int64), ("logical_tokens", ctypes.c_int64),
+                ("internal_fragmentation", ctypes.c_double)]
 
 PA_OK = 0
 PA_ERR_INVALID_ARG = 1
@@ -100,6 +110,7 @@ PA_DEV_TIMEOUT = 16
 PA_DEV_PREFIX_MISMATCH = 32
 PA_DEV_BAD_QUERY_LEN = 64
 PA_DEV_SMEM_ALIGN = 128
+PA_DEV_RANGE = 256
 
 
 class PagedKVError(RuntimeError):

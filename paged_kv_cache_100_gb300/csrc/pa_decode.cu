@@ -657,8 +657,13 @@ struct MhaFp8Consumer {
         const uint4 r0 = *reinterpret_cast<const uint4 *>(qrow + 16 * c);
         const uint4 r1 = *reinterpret_cast<const uint4 *>(qrow + 16 * c + 8);
         const uint32_t words[8] = {r0.x, r0.y, r0.z, r0.w, r1.x, r1.y, r1.z, r1.w};
+        bool beyond = false;
 #pragma unroll
-        for (int i = 0; i < 8; ++i) q[i] = pack_f16x2(bf16lo(words[i]), bf16hi(words[i]));
+        for (int i = 0; i < 8; ++i) {
+            q[i] = pack_f16x2(bf16lo(words[i]), bf16hi(words[i]));
+            beyond |= bf16x2_beyond_f16(words[i]);
+        }
+        if (beyond) report(a.status, PA_DEV_RANGE);   // the f16 query is not q
 #pragma unroll
         for (int e = 0; e < 16; ++e) acc[e] = 0.f;
         m = -INFINITY;
@@ -797,6 +802,7 @@ struct GqaTFp8Consumer {
         const __nv_bfloat16 *qg = static_cast<const __nv_bfloat16 *>(a.query) +
                                   ((size_t)w.b * a.num_q_heads + (size_t)w.head * G) * D;
         const uint32_t *qrow = reinterpret_cast<const uint32_t *>(qg + (size_t)g * D);
+        bool beyond = false;
 #pragma unroll
         for (int kk = 0; kk < D / 32; ++kk)
 #pragma unroll
@@ -806,7 +812,9 @@ struct GqaTFp8Consumer {
                 const uint32_t w1 = g < G ? qrow[d / 2 + 1] : 0u;
                 qb[2 * kk + hh][0] = pack_f16x2(bf16lo(w0), bf16hi(w0));
                 qb[2 * kk + hh][1] = pack_f16x2(bf16lo(w1), bf16hi(w1));
+                beyond |= bf16x2_beyond_f16(w0) | bf16x2_beyond_f16(w1);
             }
+        if (beyond) report(a.status, PA_DEV_RANGE);   // the f16 query is not q
 #pragma unroll
         for (int mt = 0; mt < KS; ++mt) o[mt][0] = o[mt][1] = o[mt][2] = o[mt][3] = 0.f;
         m0 = m1 = -INFINITY;

@@ -211,6 +211,14 @@ __device__ __forceinline__ float f16hi(uint32_t w) {
     return __half2float(__ushort_as_half((unsigned short)(w >> 16)));
 }
 
+// True when either bfloat16 of the pair lies outside f16's finite range:
+// |x| >= 65536 (the largest bf16 below that, 65280, is an f16 value) or
+// infinite; NaN is not counted.
+__device__ __forceinline__ bool bf16x2_beyond_f16(uint32_t w) {
+    const uint32_t lo = w & 0x7fffu, hi = (w >> 16) & 0x7fffu;
+    return (lo - 0x4780u <= 0x7f80u - 0x4780u) | (hi - 0x4780u <= 0x7f80u - 0x4780u);
+}
+
 __device__ __forceinline__ uint32_t pack_f16x2(float lo, float hi) {
     __half2 v = __floats2half2_rn(lo, hi);
     return *reinterpret_cast<uint32_t *>(&v);

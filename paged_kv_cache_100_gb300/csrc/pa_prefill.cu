@@ -626,6 +626,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         // permutes chunks within a row).
         const int ct = threadIdx.x - kConvWarp0 * 32;
         uint32_t gstep = 0;
+        uint32_t saturated = 0;   // halves that became +-65504: only out-of-range inputs do
         bool ok = true;
         for (int it = 0;; ++it) {
             int item;
@@ -655,13 +656,21 @@ __global__ void __launch_bounds__(kThreads, 1)
                     const int c = ct + i * kConvThreads;
                     const int kp = k0_tile + (c % (kHalf / 16)) / 8;
                     const uint4 w = vt[c];
-                    vt[c] = (edge && (kp < d.kv_lo || kp >= d.kv_hi)) ? make_uint4(0, 0, 0, 0) : bf16x8_to_f16x8(w);
+                    const uint4 h = (edge && (kp < d.kv_lo || kp >= d.kv_hi)) ? make_uint4(0, 0, 0, 0)
+                                                                              : bf16x8_to_f16x8(w);
+                    vt[c] = h;
+                    // 65504 is no bf16 value, so an f16 of magnitude 65504 is a saturated one
+                    saturated |= __vcmpeq2(h.x & 0x7fff7fffu, 0x7bff7bffu) |
+                                 __vcmpeq2(h.y & 0x7fff7fffu, 0x7bff7bffu) |
+                                 __vcmpeq2(h.z & 0x7fff7fffu, 0x7bff7bffu) |
+                                 __vcmpeq2(h.w & 0x7fff7fffu, 0x7bff7bffu);
                 }
                 fence_proxy_async_smem();
                 mbar_arrive(&bars[kVConv + st]);
             }
             gstep += d.n_tiles;
         }
+        if (saturated) report(a.status, PA_DEV_RANGE);
     } else {
         // ---------------- softmax groups ----------------
         const int x = (warp - 2) / (kGroup / 32);     // Q tile of this group
