@@ -210,6 +210,11 @@ class BlockManagerModel:
         if old < 0:
             raise ValueError("block released by trim_window")
         if self.ref[old] <= 1:
+            # private already; a block the prefix cache indexes is about to be
+            # written in place, so its content stops matching its key: drop it
+            if old in self.block_key:
+                del self.cached[self.block_key.pop(old)]
+                del self.block_tokens[old]
             return None
         new = self._take()
         self.ref[old] -= 1        # still held by another sequence: stays > 0
@@ -286,6 +291,40 @@ class BlockManagerModel:
                 ids.append(table[j])
         self.swapped.discard(seq)
         return ids
+
+    # -- occupancy -------------------------------------------------------
+    def stats(self) -> dict:
+        """Pool occupancy and internal fragmentation ("Cómo funciona realmente
+        vLLM", section "La sobre-reserva estática y los tres tipos de
+        desperdicio": slots reserved for a sequence that never get a token).
+        Sequence s with N tokens holds min(16, N - 16 j) tokens in the block of
+        its table entry j; a block shared by several entries holds the most of
+        them (each fills it from offset 0)."""
+        bs = self.block_size
+        held = {}
+        logical = 0
+        for seq, table in self.tables.items():
+            n = self.tokens[seq]
+            for j, b in enumerate(table):
+                if b < 0:
+                    continue
+                k = min(bs, n - j * bs)
+                logical += k
+                held[b] = max(held.get(b, 0), k)
+        used = sum(1 for r in self.ref if r >= 1)
+        reserved = used * bs
+        filled = sum(held.values())
+        return {
+            "num_blocks": self.num_blocks,
+            "free_blocks": len(self.free),
+            "evictable_blocks": len(self.evictable),
+            "used_blocks": used,
+            "shared_blocks": sum(1 for r in self.ref if r >= 2),
+            "reserved_slots": reserved,
+            "filled_slots": filled,
+            "logical_tokens": logical,
+            "internal_fragmentation": (reserved - filled) / reserved if reserved else 0.0,
+        }
 
     # -- invariants ------------------------------------------------------
     def check(self) -> None:

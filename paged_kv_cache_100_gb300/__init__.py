@@ -604,6 +604,12 @@ class BlockManager:
         check(rc, f"pa_bm_append_slots (done {ndone.value} of {n})")
         return slots, pairs[:ncow.value].copy()
 
+    def stats(self) -> dict:
+        """Pool occupancy and internal fragmentation (``pa_bm_stats``)."""
+        st = _lib.BmStats()
+        check(lib().pa_bm_stats(self._h, ctypes.byref(st)), "pa_bm_stats")
+        return {name: getattr(st, name) for name, _ in _lib.BmStats._fields_}
+
     def fill_tables(self, seqs, max_blocks: int):
         """Dense block tables [n][max_blocks] (-1 padded) and context lengths [n] (numpy)."""
         import numpy as np

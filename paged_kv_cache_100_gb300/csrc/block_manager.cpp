@@ -161,6 +161,14 @@ static pa_status make_private(pa_bm *bm, pa_bm::Seq &s, int logical, int32_t *sr
     const int32_t old = s.table[(size_t)logical];
     if (old < 0) return PA_ERR_INVALID_ARG;   // released by pa_bm_trim_window
     if (bm->ref[old] <= 1) {
+        // Already private.  A block indexed by the prefix cache is about to be
+        // written in place, so its content will no longer match its key: the
+        // key is dropped and a later lookup cannot hand the block out.
+        if (bm->has_key[old]) {
+            bm->cached.erase(bm->key_of[old]);
+            bm->has_key[old] = 0;
+            bm->tokens_of[old].clear();
+        }
         *src = -1;
         *dst = -1;
         return PA_OK;
@@ -420,5 +428,46 @@ extern "C" pa_status pa_bm_swap_in(pa_bm *bm, int seq, int32_t *block_ids, int c
         }
     s.swapped = false;
     *num_ids = n;
+    return PA_OK;
+}
+
+// Occupancy and internal fragmentation of the pool ("Cómo funciona realmente
+// vLLM", section "La sobre-reserva estática y los tres tipos de desperdicio":
+// internal fragmentation is reserved slots that never receive a token; with
+// 16-token blocks only each sequence's last block can hold such slots).  A
+// block's filled slots are the longest run any table entry pointing at it has
+// written: every entry fills a block from offset 0 up.
+extern "C" pa_status pa_bm_stats(const pa_bm *bm, pa_bm_stats_t *out) {
+    if (bm == nullptr || out == nullptr) return PA_ERR_INVALID_ARG;
+    const int64_t bs = bm->block_size;
+    std::vector<int32_t> fill((size_t)bm->num_blocks, 0);
+    int64_t logical = 0;
+    for (const auto &kv : bm->seqs) {
+        const pa_bm::Seq &s = kv.second;
+        for (size_t j = 0; j < s.table.size(); ++j) {
+            const int32_t b = s.table[j];
+            if (b < 0) continue;   // released by a window trim, or swapped out
+            const int64_t left = s.tokens - (int64_t)j * bs;
+            const int32_t f = (int32_t)(left < bs ? left : bs);
+            logical += f;
+            if (f > fill[(size_t)b]) fill[(size_t)b] = f;
+        }
+    }
+    int64_t used = 0, shared = 0, filled = 0;
+    for (int b = 0; b < bm->num_blocks; ++b) {
+        used += bm->ref[(size_t)b] >= 1;
+        shared += bm->ref[(size_t)b] >= 2;
+        filled += fill[(size_t)b];
+    }
+    out->num_blocks = bm->num_blocks;
+    out->free_blocks = (int64_t)bm->free_stack.size();
+    out->evictable_blocks = (int64_t)bm->evictable.size();
+    out->used_blocks = used;
+    out->shared_blocks = shared;
+    out->reserved_slots = used * bs;
+    out->filled_slots = filled;
+    out->logical_tokens = logical;
+    out->internal_fragmentation =
+        used == 0 ? 0.0 : (double)(used * bs - filled) / (double)(used * bs);
     return PA_OK;
 }

@@ -20,6 +20,52 @@ def test_273_tokens_take_18_blocks(golden_dir):
     bm.check()
 
 
+def test_273_token_session_wastes_15_of_288_slots(golden_dir):
+    """Internal fragmentation of the pages' 273-token session: 18 blocks of 16
+    reserve 288 slots, 273 hold a token, so 15 / 288 (5.2 %) of the reservation is
+    waste ("Cómo funciona realmente vLLM", "La sobre-reserva estática y los tres
+    tipos de desperdicio": internal fragmentation is reserved slots that are never
+    written)."""
+    g = _golden(golden_dir)["tokens_to_blocks"]
+    bm = BlockManagerModel(64)
+    bm.alloc_seq(0, g["tokens"])
+    st = bm.stats()
+    assert st["used_blocks"] == g["blocks"] and st["reserved_slots"] == 288
+    assert st["filled_slots"] == g["tokens"] and st["logical_tokens"] == g["tokens"]
+    assert st["internal_fragmentation"] == pytest.approx(15 / 288, abs=0, rel=1e-15)
+    assert st["free_blocks"] == 64 - 18 and st["shared_blocks"] == 0
+
+
+def test_forked_sessions_share_slots_until_they_diverge():
+    """A fork shares every block: logical tokens double, filled slots do not.
+    Its first new token copies the shared last block (8 tokens) into a fresh one."""
+    bm = BlockManagerModel(16)
+    bm.alloc_seq(0, 40)                                # 3 blocks: 16 + 16 + 8
+    bm.fork(0, 1)
+    st = bm.stats()
+    assert (st["used_blocks"], st["shared_blocks"], st["filled_slots"], st["logical_tokens"]) == (3, 3, 40, 80)
+    _, cow = bm.append_slot(1)                         # token 40 of the child
+    assert cow is not None
+    st = bm.stats()
+    assert (st["used_blocks"], st["shared_blocks"]) == (4, 2)
+    assert st["filled_slots"] == 16 + 16 + 8 + 9 and st["logical_tokens"] == 81
+    assert st["internal_fragmentation"] == pytest.approx((64 - 49) / 64, rel=1e-15)
+
+
+def test_waste_of_the_7b_shaped_batch_is_under_four_percent():
+    """The pages' figure for paging ("PagedAttention por dentro", opening section:
+    under 4 % waste) holds for the 64 contexts of the 7B-shaped decode batch
+    (lengths uniform in [128, 2048]): only each last block can be partly empty."""
+    import workloads as W
+    wl = W.make_workload("llama7b_mha")
+    bm = BlockManagerModel(wl.num_blocks)
+    for b, L in enumerate(wl.context_lens):
+        bm.alloc_seq(b, int(L))
+    st = bm.stats()
+    assert st["filled_slots"] == int(wl.context_lens.sum())
+    assert 0 < st["internal_fragmentation"] < 0.04
+
+
 def test_128_tokens_on_32_layers_take_256_blocks(golden_dir):
     """One pool per layer: a session holds blocks in each of the 32 layers' pools."""
     g = _golden(golden_dir)["blocks_per_session_all_layers"]

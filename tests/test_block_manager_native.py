@@ -15,6 +15,7 @@ def _built():
 
 
 def _same(bm, model, live):
+    assert bm.stats() == model.stats()
     assert bm.num_free() == model.num_free()
     for s in live:
         assert bm.table(s) == model.table(s)

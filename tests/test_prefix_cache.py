@@ -103,7 +103,7 @@ def test_native_prefix_cache_matches_the_model():
             live.append(nxt)
             toks[nxt] = list(toks[s])
             nxt += 1
-        elif op < 0.8:
+        elif op < 0.75:
             s = rng.choice(live)
             try:
                 want = model.append_slot(s)
@@ -115,6 +115,19 @@ def test_native_prefix_cache_matches_the_model():
             else:
                 assert bm.append_slot(s) == want
                 toks[s].append(rng.randrange(0, 8))
+        elif op < 0.8:
+            s = rng.choice(live)
+            if model.table(s):
+                j = rng.randrange(len(model.table(s)))
+                try:
+                    want = model.make_private(s, j)
+                except NoBlocks:
+                    want = "full"
+                if want == "full":
+                    with pytest.raises(pkv.PagedKVError):
+                        bm.make_private(s, j)
+                else:
+                    assert bm.make_private(s, j) == want
         else:
             s = rng.choice(live)
             model.free_seq(s)
@@ -122,12 +135,27 @@ def test_native_prefix_cache_matches_the_model():
             live.remove(s)
         if step % 25 == 0:
             model.check()
+            assert bm.stats() == model.stats()
             assert bm.num_free() == model.num_free()
             assert bm.num_evictable() == model.num_evictable()
             for s in live:
                 assert bm.table(s) == model.table(s)
             for b in range(60):
                 assert bm.ref_count(b) == model.ref_count(b)
+
+
+def test_making_a_cached_block_private_drops_its_key():
+    """A registered block about to be written in place (make_private on a block
+    only its own sequence holds) must leave the prefix cache: a later sequence
+    with the same tokens may not reuse it."""
+    toks = list(range(40))
+    for make in (BlockManagerModel, pkv.BlockManager):
+        bm = make(16)
+        assert bm.alloc_seq_cached(0, toks) == 0
+        assert bm.register_prefix(0, toks) == 2
+        assert bm.make_private(0, 1) is None          # private: written in place
+        assert bm.alloc_seq_cached(1, toks) == 16     # block 0 reused, block 1 not
+        assert bm.table(1)[0] == bm.table(0)[0] and bm.table(1)[1] != bm.table(0)[1]
 
 
 def test_trim_window_releases_blocks_before_the_window():
@@ -200,6 +228,7 @@ def test_native_sliding_window_matches_the_model():
             live.remove(s)
         if step % 25 == 0:
             model.check()
+            assert bm.stats() == model.stats()
             assert bm.num_free() == model.num_free()
             for s in live:
                 assert bm.table(s) == model.table(s)

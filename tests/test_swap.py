@@ -163,6 +163,7 @@ def test_native_swap_matches_the_model():
             live.remove(s)
         if step % 25 == 0:
             model.check()
+            assert bm.stats() == model.stats()
             assert bm.num_free() == model.num_free()
             for s in live + out:
                 assert bm.table(s) == model.table(s)
