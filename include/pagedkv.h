@@ -311,10 +311,14 @@ pa_status pa_cache_write_fp8(void *key_cache, void *value_cache, const void *key
  *  - Size limit: when pa_decode_workspace_bytes(...) for these arguments
  *    exceeds PA_STATIC_SCRATCH_BYTES the call returns PA_ERR_WORKSPACE and
  *    enqueues nothing (use pa_decode with a workspace, or a larger
- *    partition_size, then).
+ *    partition_size, then).  Invalid arguments are reported first, with the
+ *    status pa_decode gives them.
  *  - Set-up: the first call on a device that needs scratch looks up the
  *    array's device address (cudaGetSymbolAddress) with that device current;
- *    make that first call before any stream capture.
+ *    make that first call before any stream capture.  The address is kept
+ *    with the context it belongs to; a call in a new context of the device
+ *    (after cudaDeviceReset) looks it up again, so make the first call after
+ *    a reset before any stream capture too.
  *  - Sharing: every call on a device uses the same array and leaves its last
  *    contents there.  No part of it has to start at zero.  Calls that overlap
  *    on the GPU (other streams, other host threads) race on it; serialise them.
