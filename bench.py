@@ -311,6 +311,271 @@ class StepOps:
             self.pkv.decode(q, self.kc, self.vc, bt, lens, self.wl.scale, out=out,
                             partition_size=self.P, workspace=self.ws)
 
+def rotation_copies(unique_kv_bytes: int) -> int:
+    """Pool copies used in turn, step after step, so that no step finds K/V of the
+    step before it in L2: between two reads of one copy at least twice the L2
+    size of other K/V streams through.  K/V of four times the L2 size or more
+    (and parity-sized pools too small to measure) need no rotation."""
+    if unique_kv_bytes >= 4 * L2_BYTES or unique_kv_bytes < 16 * 10**6:
+        return 1
+    return min(8, 1 + -(-2 * L2_BYTES // unique_kv_bytes))
+
+
+def l2_note(unique_kv: int, copies: int) -> str:
+    if copies > 1:
+        return ("%.0f MB of distinct K/V per step vs 129 MB L2: %d pool copies used in turn, "
+                "%.0f MB of other K/V between two reads of a copy"
+                % (unique_kv / 1e6, copies, (copies - 1) * unique_kv / 1e6))
+    if unique_kv >= 4 * L2_BYTES:
+        return "inputs larger than L2: %.2f GB of distinct K/V per step vs 129 MB L2" % (unique_kv / 1e9)
+    return ("%.2f MB of distinct K/V per step fits in the 129 MB L2 (a parity-sized "
+            "configuration; its timing is not an HBM figure)" % (unique_kv / 1e6))
+
+
+def cpu_model() -> str:
+    """The host CPU's model name (lscpu), else the machine type."""
+    import platform
+    import subprocess
+    try:
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+        for line in out.splitlines():
+            if line.strip().startswith("Model name:"):
+                return line.split(":", 1)[1].strip()
+    except Exception:
+        pass
+    return platform.machine() or "unknown"
+
+
+def measure_decode(pkv, dev, stream, args, workload, kv_dtype="bf16", window=0, decode="auto",
+                   partition_size=0, soak_s=0.5, rank=0, world=1, sample_clocks=True):
+    """One decode configuration: W warm-up steps, K timed steps back to back, K
+    steps with every decode call bracketed by events, a loop of the same step for
+    at least ``soak_s`` seconds (NVML clock samples over it and the timed steps),
+    and the end-to-end run through the public API with host inputs.  Returns the
+    measurements and the workload description."""
+    import torch
+    wl = W.make_workload(workload, seed=args.seed)
+    fp8 = kv_dtype == "fp8"
+    if fp8:
+        q, kc, vc, kn, vn, ks, vs = W.fp8_device_values(wl, dev, seed=args.seed + 17 + rank)
+    else:
+        q, kc, vc, kn, vn = W.device_values(wl, dev, seed=args.seed + 17 + rank)
+        ks = vs = None
+    kv_e = 1 if fp8 else None
+    logical = decode_algorithmic_bytes(wl, kv_elem_bytes=kv_e, window=window)
+    unique_kv = unique_kv_bytes(wl, kv_elem_bytes=kv_e, window=window)
+    copies = rotation_copies(unique_kv)
+    pools = [(kc, vc)] + [(kc.clone(), vc.clone()) for _ in range(copies - 1)]
+    bt = torch.from_numpy(wl.block_tables).to(dev)
+    lens = torch.from_numpy(wl.step_context_lens).to(dev)
+    slots = torch.from_numpy(wl.slot_mapping).to(dev)
+    pairs = torch.from_numpy(wl.cow_pairs).to(dev)
+    has_cow = wl.cow_pairs.shape[0] > 0
+    kvd = "fp8" if fp8 else wl.dtype
+    P = partition_size or wl.partition_size or pkv.decode_partition_size(
+        wl.num_seqs, wl.num_q_heads, wl.num_kv_heads, wl.max_blocks, kvd)
+    out = torch.empty_like(q)
+    ws = torch.empty(max(pkv.decode_workspace_bytes(wl.num_seqs, wl.num_q_heads, wl.num_kv_heads,
+                                                    wl.head_dim, wl.max_blocks, P, kvd), 16),
+                     dtype=torch.uint8, device=dev)
+    n_prefix = 0
+    if window:
+        P = partition_size
+        ws = torch.empty(max(pkv.lib().pa_decode_sliding_window_workspace_bytes(
+            wl.num_seqs, wl.num_q_heads, wl.num_kv_heads, wl.head_dim, wl.max_blocks, 16, window,
+            P, 2 if fp8 else (1 if wl.dtype == "bf16" else 0)), 16), dtype=torch.uint8, device=dev)
+    elif decode != "plain":
+        n_prefix = pkv.shared_prefix_blocks(wl.block_tables)
+        if decode == "auto" and n_prefix < 4:
+            n_prefix = 0
+    if n_prefix:
+        P = partition_size or wl.partition_size
+        ws_bytes = (pkv.lib().pa_decode_shared_prefix_fp8_workspace_bytes if fp8 else
+                    pkv.lib().pa_decode_shared_prefix_workspace_bytes)
+        ws = torch.empty(max(ws_bytes(wl.num_seqs, wl.num_q_heads, wl.num_kv_heads, wl.head_dim,
+                                      wl.max_blocks, n_prefix, P), 16),
+                         dtype=torch.uint8, device=dev)
+    ops = [StepOps(pkv, wl, k_, v_, ks, vs, P, ws, n_prefix, window) for k_, v_ in pools]
+    state = {"i": 0}
+
+    def step(ev_pre=None, ev_post=None, q_=q, kn_=kn, vn_=vn, slots_=slots, pairs_=pairs, bt_=bt,
+             lens_=lens):
+        o = ops[state["i"] % copies]
+        state["i"] += 1
+        o.write(kn_, vn_, slots_)
+        if has_cow:
+            pkv.block_copy(o.kc, o.vc, pairs_)
+        if ev_pre is not None:
+            ev_pre.record(stream)
+        o.decode(q_, bt_, lens_, out)
+        if ev_post is not None:
+            ev_post.record(stream)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize(dev)
+    # a first estimate of the step time sizes the clock-sampling loop
+    t0 = time.perf_counter()
+    for _ in range(3):
+        step()
+    torch.cuda.synchronize(dev)
+    est = max((time.perf_counter() - t0) / 3, 1e-5)
+    n_soak = int(max(1, soak_s / est)) if soak_s > 0 else 0
+
+    K = args.steps
+    sampler = ClockSampler(dev.index or 0, pci_bus_id(dev)) if (rank == 0 and sample_clocks) else None
+    barrier()
+    torch.cuda.synchronize(dev)
+    if sampler:
+        sampler.start()
+    # a loop of the same step right before the timed region: the GPU is under
+    # this load when the timed steps begin, and the clock samples cover both
+    es0 = torch.cuda.Event(enable_timing=True)
+    es1 = torch.cuda.Event(enable_timing=True)
+    es0.record(stream)
+    for _ in range(n_soak):
+        step()
+    es1.record(stream)
+    launches0 = pkv.launch_count()
+    # timed region: K whole steps back to back
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(K):
+        step()
+    e1.record(stream)
+    torch.cuda.synchronize(dev)
+    clocks = sampler.stop() if sampler else None
+    barrier()
+    launches = pkv.launch_count() - launches0
+    # K steps again, each decode call bracketed by events on the launching
+    # stream (the roofline's per-call duration)
+    pre = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
+    post = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
+    e2 = torch.cuda.Event(enable_timing=True)
+    e3 = torch.cuda.Event(enable_timing=True)
+    e2.record(stream)
+    for i in range(K):
+        step(pre[i], post[i])
+    e3.record(stream)
+    torch.cuda.synchronize(dev)
+    barrier()
+    ms_total = max_over_ranks(e0.elapsed_time(e1), dev)
+    decode_ms = max_over_ranks(sum(a.elapsed_time(b) for a, b in zip(pre, post)) / K, dev)
+    ms_step_with_events = max_over_ranks(e2.elapsed_time(e3), dev) / K
+    soak_ms = es0.elapsed_time(es1) / n_soak if n_soak else None
+    ms_per_step = ms_total / K
+
+    e2e = run_e2e(args, pkv, wl, q, kn, vn, dev, stream, step, out)
+    res = {
+        "wl": wl, "fp8": fp8, "kv_dtype": kvd, "window": window, "n_prefix": n_prefix, "P": P,
+        "ms_per_step": ms_per_step, "decode_ms": decode_ms,
+        "ms_per_step_with_call_events": ms_step_with_events,
+        "soak": {"steps": n_soak, "ms_per_step": soak_ms,
+                 "s": None if soak_ms is None else n_soak * soak_ms / 1e3},
+        "launches": int(launches), "clocks": clocks, "e2e": e2e,
+        "logical": logical, "unique_kv": unique_kv, "copies": copies,
+        "q": q, "kc": kc, "vc": vc, "ks": ks, "vs": vs,
+    }
+    return res
+
+
+def decode_method(res) -> str:
+    window, n_prefix, fp8 = res["window"], res["n_prefix"], res["fp8"]
+    if window:
+        return f"sliding window of the last {window} positions"
+    if n_prefix:
+        return (f"shared-prefix cascade ({n_prefix} shared blocks read once per KV head; " +
+                ("widen, " if fp8 else "") + "prefix, suffix and merge kernels)")
+    return "paged decode"
+
+
+def decode_kernel_desc(res) -> str:
+    if res["window"]:
+        return ("pa_decode_sliding_window call (partition kernel, plus the merge kernel when a "
+                "window spans several partitions)")
+    if res["n_prefix"]:
+        return ("pa_decode_shared_prefix_fp8 call (widen + prefix + suffix + merge kernels)"
+                if res["fp8"] else "pa_decode_shared_prefix call (prefix + suffix + merge kernels)")
+    return ("pa_decode call (partition kernel, plus the merge kernel when a sequence spans "
+            "several partitions)")
+
+
+def decode_summary(res, args, workload, decode, partition_size, world) -> dict:
+    """The figures of one decode configuration (the per-configuration record)."""
+    wl = res["wl"]
+    hbm_bytes = res["logical"]["total"] - res["logical"]["kv"] + res["unique_kv"]
+    peak, peak_kind = load_peaks()
+    decode_ms = res["decode_ms"]
+    achieved = hbm_bytes / (decode_ms * 1e-3) / 1e9
+    kvd_arg = "fp8" if res["fp8"] else "bf16"
+    traffic = measured_traffic(traffic_key(workload, kvd_arg, res["window"], partition_size, decode))
+    clocks = res["clocks"]
+    mhz = clocks.get("sm_mhz") if clocks else None
+    out = {
+        "workload": workload_config(wl, world, kvd_arg, res["window"], res["unique_kv"])["workload"],
+        "decode_method": decode_method(res),
+        "partition_size": res["P"] or "per window",
+        "ms_per_step": res["ms_per_step"],
+        "decode_ms": decode_ms,
+        "tokens_per_s": wl.num_seqs * world / (res["ms_per_step"] * 1e-3),
+        "context_tokens_per_s": float(wl.step_context_lens.sum()) * world / (res["ms_per_step"] * 1e-3),
+        "kv_gbs": res["unique_kv"] / (decode_ms * 1e-3) / 1e9,
+        "logical_kv_gbs": res["logical"]["kv"] / (decode_ms * 1e-3) / 1e9,
+        "roofline": {
+            "kernel": decode_kernel_desc(res), "bound": "hbm", "achieved": achieved, "peak": peak,
+            "peak_source": f"{peak_kind} (MEASURED_PEAKS.json hbm_gbs)" if peak_kind == "measured"
+            else "fallback 6800 GB/s",
+            "unit": "GB/s", "frac": achieved / peak, "traffic": traffic,
+            "algorithmic_bytes_per_call": hbm_bytes,
+            "bytes_rule": "K/V of every distinct (block, slot) read + Q + O + table entries + "
+                          "context lengths",
+        },
+        "hbm_frac_of_nominal_7900": achieved / NOMINAL_HBM_GBS,
+        "sustained": res["soak"],
+        "clocks": clocks,
+        "decode_kcycles_at_median_clock": (decode_ms * mhz) if mhz else None,
+        "gpu_launches_per_step": res["launches"] / max(args.steps, 1),
+        "e2e": res["e2e"],
+        "l2": l2_note(res["unique_kv"], res["copies"]),
+    }
+    if traffic is not None:
+        out["roofline"]["traffic_over_algorithmic"] = traffic / hbm_bytes
+    return out
+
+
+# the configurations of the per-configuration record (one GPU run): every
+# decode workload, the FP8 pools, the sliding windows, and the plain paged
+# decode of the shared-prefix mix next to its cascade
+PER_CONFIG = [
+    dict(workload="tiny"),
+    dict(workload="llama7b_mha"),
+    dict(workload="llama70b_gqa"),
+    dict(workload="long_splitk"),
+    dict(workload="shared_prefix"),
+    dict(workload="shared_prefix", decode="plain"),
+    dict(workload="llama7b_mha", kv_dtype="fp8"),
+    dict(workload="llama70b_gqa", kv_dtype="fp8"),
+    dict(workload="long_splitk", kv_dtype="fp8"),
+    dict(workload="shared_prefix", kv_dtype="fp8"),
+    dict(workload="long_splitk", window=4096),
+    dict(workload="llama70b_gqa", window=1024),
+    dict(workload="llama70b_gqa", window=1024, kv_dtype="fp8"),
+]
+PER_CONFIG_PREFILL = ["prefill_llama70b_chunked", "prefill_llama7b"]
+
+
+def per_config_key(c) -> str:
+    k = c["workload"]
+    if c.get("kv_dtype", "bf16") == "fp8":
+        k += "+fp8_kv"
+    if c.get("window"):
+        k += f"+window{c['window']}"
+    if c.get("decode", "auto") != "auto":
+        k += f"+{c['decode']}"
+    return k
+
+
 def run_gpu(args):
     import torch
     rank, world, local = dist_env()
@@ -324,172 +589,85 @@ def run_gpu(args):
         build()
     barrier()
     import paged_kv_cache_100_gb300 as pkv
-
-    wl = W.make_workload(args.workload, seed=args.seed)
-    fp8 = args.kv_dtype == "fp8"
-    if fp8:
-        q, kc, vc, kn, vn, ks, vs = W.fp8_device_values(wl, dev, seed=args.seed + 17 + rank)
-    else:
-        q, kc, vc, kn, vn = W.device_values(wl, dev, seed=args.seed + 17 + rank)
-        ks = vs = None
-    bt = torch.from_numpy(wl.block_tables).to(dev)
-    lens = torch.from_numpy(wl.step_context_lens).to(dev)
-    slots = torch.from_numpy(wl.slot_mapping).to(dev)
-    pairs = torch.from_numpy(wl.cow_pairs).to(dev)
-    has_cow = wl.cow_pairs.shape[0] > 0
-    kv_dtype = "fp8" if fp8 else wl.dtype
-    P = args.partition_size or wl.partition_size or pkv.decode_partition_size(
-        wl.num_seqs, wl.num_q_heads, wl.num_kv_heads, wl.max_blocks, kv_dtype)
-    out = torch.empty_like(q)
-    ws = torch.empty(max(pkv.decode_workspace_bytes(wl.num_seqs, wl.num_q_heads, wl.num_kv_heads,
-                                                    wl.head_dim, wl.max_blocks, P, kv_dtype), 16),
-                     dtype=torch.uint8, device=dev)
     stream = torch.cuda.current_stream(dev)
-    n_prefix = 0
-    window = args.window
-    if window:
-        P = args.partition_size
-        ws = torch.empty(max(pkv.lib().pa_decode_sliding_window_workspace_bytes(
-            wl.num_seqs, wl.num_q_heads, wl.num_kv_heads, wl.head_dim, wl.max_blocks, 16, window,
-            P, 2 if fp8 else (1 if wl.dtype == "bf16" else 0)), 16), dtype=torch.uint8, device=dev)
-    elif args.decode != "plain":
-        n_prefix = pkv.shared_prefix_blocks(wl.block_tables)
-        if args.decode == "auto" and n_prefix < 4:
-            n_prefix = 0
-    if n_prefix:
-        P = args.partition_size or wl.partition_size
-        ws_bytes = (pkv.lib().pa_decode_shared_prefix_fp8_workspace_bytes if fp8 else
-                    pkv.lib().pa_decode_shared_prefix_workspace_bytes)
-        ws = torch.empty(max(ws_bytes(wl.num_seqs, wl.num_q_heads, wl.num_kv_heads, wl.head_dim,
-                                      wl.max_blocks, n_prefix, P), 16),
-                         dtype=torch.uint8, device=dev)
-    ops = StepOps(pkv, wl, kc, vc, ks, vs, P, ws, n_prefix, window)
 
-    def step(ev_pre=None, ev_post=None):
-        ops.write(kn, vn, slots)
-        if has_cow:
-            pkv.block_copy(kc, vc, pairs)
-        if ev_pre is not None:
-            ev_pre.record(stream)
-        ops.decode(q, bt, lens, out)
-        if ev_post is not None:
-            ev_post.record(stream)
-
-    for _ in range(args.warmup):
-        step()
-    torch.cuda.synchronize(dev)
-
-    K = args.steps
-    e0 = torch.cuda.Event(enable_timing=True)
-    e1 = torch.cuda.Event(enable_timing=True)
-    sampler = ClockSampler(dev.index or 0, pci_bus_id(dev)) if rank == 0 else None
-    barrier()
-    torch.cuda.synchronize(dev)
-    launches0 = pkv.launch_count()
-    if sampler:
-        sampler.start()
-    # timed region 1: K whole steps back to back
-    e0.record(stream)
-    for _ in range(K):
-        step()
-    e1.record(stream)
-    torch.cuda.synchronize(dev)
-    barrier()
-    launches = pkv.launch_count() - launches0
-    # timed region 2: K steps again, each decode call bracketed by events on the
-    # launching stream (the roofline's per-call duration)
-    pre = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
-    post = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
-    e2 = torch.cuda.Event(enable_timing=True)
-    e3 = torch.cuda.Event(enable_timing=True)
-    e2.record(stream)
-    for i in range(K):
-        step(pre[i], post[i])
-    e3.record(stream)
-    torch.cuda.synchronize(dev)
-    barrier()
-    ms_step_with_events = max_over_ranks(e2.elapsed_time(e3), dev) / K
-    clocks = sampler.stop() if sampler else None
-    ms_total = max_over_ranks(e0.elapsed_time(e1), dev)
-    decode_ms = max_over_ranks(sum(a.elapsed_time(b) for a, b in zip(pre, post)) / K, dev)
-    ms_per_step = ms_total / K
-
-    # end to end through the public API: pinned host inputs in, output back, every step
-    e2e = run_e2e(args, pkv, wl, q, kc, vc, kn, vn, dev, stream, ops)
-
-    if rank != 0:
-        return None
-    kv_e = 1 if fp8 else None
-    logical = decode_algorithmic_bytes(wl, kv_elem_bytes=kv_e, window=window)
-    unique_kv = unique_kv_bytes(wl, kv_elem_bytes=kv_e, window=window)
-    hbm_bytes = logical["total"] - logical["kv"] + unique_kv
-    peak, peak_kind = load_peaks()
-    achieved = hbm_bytes / (decode_ms * 1e-3) / 1e9
-    tokens_per_s = wl.num_seqs * world / (ms_per_step * 1e-3)
-    traffic = measured_traffic(traffic_key(args.workload, args.kv_dtype, window, args.partition_size,
-                                           args.decode))
-    line = {
-        "metric": METRIC,
-        "value": tokens_per_s,
-        "unit": "tokens/s",
-        "n_gpus": world,
-        "steps": K,
-        "warmup": args.warmup,
-        "ms_per_step": ms_per_step,
-        "higher_is_better": True,
-        "scaling": "weak",
-        "vs_baseline": None,
-        "dtype": "fp8_e4m3 K/V, bf16 Q/O" if fp8 else wl.dtype,
-        "data": "synthetic (seeded; N(0, %g) values, shuffled block pool)" % wl.value_std,
-        "config": workload_config(wl, P, world, kv_dtype, window),
-        "decode_ms": decode_ms,
-        "ms_per_step_with_call_events": ms_step_with_events,
-        "kv_gbs": unique_kv / (decode_ms * 1e-3) / 1e9,
-        "logical_kv_gbs": logical["kv"] / (decode_ms * 1e-3) / 1e9,
-        "context_tokens_per_s": float(wl.step_context_lens.sum()) * world / (ms_per_step * 1e-3),
-        "hbm_frac_of_measured": achieved / peak if peak_kind == "measured" else None,
-        "hbm_frac_of_nominal_7900": achieved / NOMINAL_HBM_GBS,
-        "decode_method": (f"sliding window of the last {window} positions" if window else
-                          (f"shared-prefix cascade ({n_prefix} shared blocks read once per KV "
-                           "head; " + ("widen, " if fp8 else "") + "prefix, suffix and merge "
-                           "kernels)") if n_prefix
-                          else "paged decode"),
-        "roofline": {
-            "kernel": ("pa_decode_sliding_window call (partition kernel, plus the merge kernel "
-                       "when a window spans several partitions)" if window else
-                       ("pa_decode_shared_prefix_fp8 call (widen + prefix + suffix + merge "
-                        "kernels)" if fp8 else
-                        "pa_decode_shared_prefix call (prefix + suffix + merge kernels)") if n_prefix
-                       else "pa_decode call (partition kernel, plus the merge kernel when a "
-                            "sequence spans several partitions)"),
-            "bound": "hbm",
-            "achieved": achieved,
-            "peak": peak,
-            "peak_source": f"{peak_kind} (MEASURED_PEAKS.json hbm_gbs)" if peak_kind == "measured"
-            else "fallback 6800 GB/s",
-            "unit": "GB/s",
-            "frac": achieved / peak,
-            "traffic": traffic,
-            "algorithmic_bytes_per_call": hbm_bytes,
-            "bytes_rule": "K/V of every distinct (block, slot) read + Q + O + table entries + "
-                          "context lengths",
-        },
-        "gpu_launches": int(launches),
-        "clocks": clocks,
-        "e2e": e2e,
-    }
-    if unique_kv != logical["kv"]:
-        line["logical_kv_bytes"] = logical["kv"]
-        line["unique_kv_bytes"] = unique_kv
-    if not args.no_cpu_baseline and world == 1:
-        line["cpu_baseline"] = cpu_baseline(args, wl, q, kc, vc, budget_s=args.cpu_seconds,
-                                            ks=ks, vs=vs, window=window)
+    res = measure_decode(pkv, dev, stream, args, args.workload, args.kv_dtype, args.window,
+                         args.decode, args.partition_size, soak_s=args.soak_seconds, rank=rank,
+                         world=world)
+    summ = decode_summary(res, args, args.workload, args.decode, args.partition_size, world)
+    wl = res["wl"]
+    line = None
+    if rank == 0:
+        line = {
+            "metric": METRIC,
+            "value": summ["tokens_per_s"],
+            "unit": "tokens/s",
+            "n_gpus": world,
+            "steps": args.steps,
+            "warmup": args.warmup,
+            "ms_per_step": res["ms_per_step"],
+            "higher_is_better": True,
+            "scaling": "weak",
+            "vs_baseline": None,
+            "dtype": "fp8_e4m3 K/V, bf16 Q/O" if res["fp8"] else wl.dtype,
+            "data": "synthetic (seeded; N(0, %g) values, shuffled block pool)" % wl.value_std,
+            "config": workload_config(wl, world, args.kv_dtype, args.window, res["unique_kv"]),
+            "partition_size_used": res["P"] or "per window",
+            "decode_ms": res["decode_ms"],
+            "ms_per_step_with_call_events": res["ms_per_step_with_call_events"],
+            "kv_gbs": summ["kv_gbs"],
+            "logical_kv_gbs": summ["logical_kv_gbs"],
+            "context_tokens_per_s": summ["context_tokens_per_s"],
+            "hbm_frac_of_measured": summ["roofline"]["frac"]
+            if summ["roofline"]["peak_source"].startswith("measured") else None,
+            "hbm_frac_of_nominal_7900": summ["hbm_frac_of_nominal_7900"],
+            "decode_method": summ["decode_method"],
+            "roofline": summ["roofline"],
+            "gpu_launches": res["launches"],
+            "clocks": res["clocks"],
+            "clocks_window": "NVML every 20 ms over a loop of the same step (%d steps, %.2f s) "
+                             "that ends where the timed region begins, and the timed region"
+                             % (res["soak"]["steps"], res["soak"]["s"] or 0.0),
+            "sustained": res["soak"],
+            "decode_kcycles_at_median_clock": summ["decode_kcycles_at_median_clock"],
+            "e2e": res["e2e"],
+        }
+        if res["unique_kv"] != res["logical"]["kv"]:
+            line["logical_kv_bytes"] = res["logical"]["kv"]
+            line["unique_kv_bytes"] = res["unique_kv"]
+        if not args.no_cpu_baseline and world == 1:
+            line["cpu_baseline"] = cpu_baseline(args, wl, res["q"], res["kc"], res["vc"],
+                                                budget_s=args.cpu_seconds, ks=res["ks"],
+                                                vs=res["vs"], window=args.window)
+    del res
+    torch.cuda.empty_cache()
+    if world == 1 and not args.no_per_config:
+        per = {}
+        for c in PER_CONFIG:
+            r = measure_decode(pkv, dev, stream, args, c["workload"], c.get("kv_dtype", "bf16"),
+                               c.get("window", 0), c.get("decode", "auto"), 0,
+                               soak_s=args.soak_seconds)
+            per[per_config_key(c)] = decode_summary(r, args, c["workload"], c.get("decode", "auto"),
+                                                    0, world)
+            del r
+            torch.cuda.empty_cache()
+        for name in PER_CONFIG_PREFILL:
+            pa = argparse.Namespace(**vars(args))
+            pa.workload, pa.window = name, 0
+            per[name] = prefill_summary(measure_prefill(pkv, dev, stream, pa, soak_s=args.soak_seconds),
+                                        world)
+            torch.cuda.empty_cache()
+        line["per_config"] = per
     return line
 
 
-def workload_config(wl, P, world, kv_dtype=None, window=0):
+def workload_config(wl, world, kv_dtype=None, window=0, unique_kv=None):
+    """The workload as both arms describe it (nothing the library chooses)."""
     lens = wl.step_context_lens
     kv_e = 1 if kv_dtype == "fp8" else None
+    if unique_kv is None:
+        unique_kv = unique_kv_bytes(wl, kv_elem_bytes=kv_e, window=window)
+    copies = rotation_copies(unique_kv)
     cfg = {
         "workload": wl.name + ("+fp8_kv" if kv_dtype == "fp8" else "") +
                     (f"+window{window}" if window else ""),
@@ -502,11 +680,10 @@ def workload_config(wl, P, world, kv_dtype=None, window=0):
         "block_size": wl.block_size,
         "context_lens_min_max_mean": [int(lens.min()), int(lens.max()), float(lens.mean())],
         "num_blocks": wl.num_blocks,
-        "partition_size": P,
+        "partition_size": wl.partition_size or "library choice",
         "cow_pairs_per_step": int(wl.cow_pairs.shape[0]),
         "parallelism": f"weak scaling, {world} independent replica(s)",
-        "l2": "inputs larger than L2: %.2f GB of K/V read per step vs 129 MB L2"
-              % (decode_algorithmic_bytes(wl, kv_elem_bytes=kv_e, window=window)["kv"] / 1e9),
+        "l2": l2_note(unique_kv, copies),
     }
     if window:
         cfg["window"] = window
@@ -539,7 +716,7 @@ class PackedInputs:
         self.device.copy_(self.host, non_blocking=True)
 
 
-def run_e2e(args, pkv, wl, q, kc, vc, kn, vn, dev, stream, ops):
+def run_e2e(args, pkv, wl, q, kn, vn, dev, stream, step, out):
     """Same step through the public API with host inputs: H2D of the step's inputs
     (query, new K/V rows, slots, tables, lengths, copy pairs; packed in one pinned
     buffer, one copy) and D2H of the output inside the timed region."""
@@ -555,21 +732,18 @@ def run_e2e(args, pkv, wl, q, kc, vc, kn, vn, dev, stream, ops):
         inputs["pairs"] = torch.from_numpy(wl.cow_pairs)
     packed = PackedInputs(inputs, dev)
     devb = packed.dev
-    out = torch.empty_like(q)
     out_host = torch.empty(out.shape, dtype=out.dtype).pin_memory()
     h2d = packed.nbytes
     d2h = out.numel() * out.element_size()
 
-    def step():
+    def e2e_step():
         packed.upload()
-        ops.write(devb["kn"], devb["vn"], devb["slots"])
-        if has_cow:
-            pkv.block_copy(kc, vc, devb["pairs"])
-        ops.decode(devb["q"], devb["bt"], devb["lens"], out)
-        out_host.copy_(out, non_blocking=True)
+        step(q_=devb["q"], kn_=devb["kn"], vn_=devb["vn"], slots_=devb["slots"],
+             pairs_=devb.get("pairs"), bt_=devb["bt"], lens_=devb["lens"])
+        out_host.copy_(out, non_blocking=True)   # the output the step wrote
 
-    for _ in range(max(3, args.warmup // 10)):
-        step()
+    for _ in range(3):
+        e2e_step()
     torch.cuda.synchronize(dev)
     K = max(1, min(args.steps, args.e2e_steps))
     e0 = torch.cuda.Event(enable_timing=True)
@@ -577,7 +751,7 @@ def run_e2e(args, pkv, wl, q, kc, vc, kn, vn, dev, stream, ops):
     barrier()
     e0.record(stream)
     for _ in range(K):
-        step()
+        e2e_step()
     e1.record(stream)
     torch.cuda.synchronize(dev)
     barrier()
@@ -635,7 +809,7 @@ def cpu_baseline(args, wl, q, kc, vc, budget_s=10.0, ks=None, vs=None, window=0)
     att = lambda ls: float(sum(min(int(L), window) if window else int(L) for L in ls))
     frac = att(lens) / att(wl.step_context_lens)
     t_batch = dt / reps / frac
-    return {"value": wl.num_seqs / t_batch, "unit": "tokens/s", "cores": threads, "kind": "oracle",
+    return {"value": wl.num_seqs / t_batch, "unit": "tokens/s", "cores": threads, "cpu": cpu_model(), "kind": "oracle",
             "sample": f"{n_seq} of {wl.num_seqs} sequences (all {wl.num_q_heads} heads, "
                       f"{int(lens.sum())} context tokens) x {reps} repetitions in {dt:.1f} s; "
                       "time scaled to the batch by context tokens"}
@@ -713,9 +887,8 @@ def run_reference(args):
         "vs_baseline": None,
         "dtype": "f64",
         "data": "synthetic (seeded)",
-        "config": workload_config(wl, args.partition_size or wl.partition_size or "library choice",
-                                  world, getattr(args, "kv_dtype", "bf16"), args.window),
-        "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": threads, "kind": "oracle",
+        "config": workload_config(wl, world, getattr(args, "kv_dtype", "bf16"), args.window),
+        "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": threads, "cpu": cpu_model(), "kind": "oracle",
                          "sample": sample},
         "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0,
                 "d2h_bytes_per_step": 0},
@@ -776,20 +949,9 @@ def prefill_config(pw, world, window):
     return cfg
 
 
-def run_prefill_gpu(args):
+def measure_prefill(pkv, dev, stream, args, soak_s=0.5, rank=0, world=1):
+    """One chunked-prefill configuration, timed as measure_decode times decode."""
     import torch
-    rank, world, local = dist_env()
-    if world > 1:
-        torch.cuda.set_device(local)
-        init_dist("nccl")
-    dev = torch.device("cuda", local if world > 1 else 0)
-    torch.cuda.set_device(dev)
-    from paged_kv_cache_100_gb300.build import build
-    if rank == 0 or world == 1:
-        build()
-    barrier()
-    import paged_kv_cache_100_gb300 as pkv
-
     pw = W.make_prefill_workload(args.workload, seed=args.seed)
     q, kc, vc, kn, vn = W.prefill_device_values(pw, dev, seed=args.seed + 17 + rank)
     bt = torch.from_numpy(pw.block_tables).to(dev)
@@ -799,7 +961,6 @@ def run_prefill_gpu(args):
     maxq = int(pw.chunk.max())
     out = torch.empty_like(q)
     ws = torch.empty(int(pkv.lib().pa_prefill_workspace_bytes()), dtype=torch.uint8, device=dev)
-    stream = torch.cuda.current_stream(dev)
     window = args.window
 
     def step(ev_pre=None, ev_post=None, q_=q, kn_=kn, vn_=vn, slots_=slots, bt_=bt, lens_=lens,
@@ -815,20 +976,32 @@ def run_prefill_gpu(args):
     for _ in range(args.warmup):
         step()
     torch.cuda.synchronize(dev)
+    t0 = time.perf_counter()
+    step()
+    torch.cuda.synchronize(dev)
+    est = max(time.perf_counter() - t0, 1e-5)
+    n_soak = int(max(1, soak_s / est)) if soak_s > 0 else 0
     K = args.steps
-    e0 = torch.cuda.Event(enable_timing=True)
-    e1 = torch.cuda.Event(enable_timing=True)
     sampler = ClockSampler(dev.index or 0, pci_bus_id(dev)) if rank == 0 else None
     barrier()
     torch.cuda.synchronize(dev)
-    launches0 = pkv.launch_count()
     if sampler:
         sampler.start()
+    es0 = torch.cuda.Event(enable_timing=True)
+    es1 = torch.cuda.Event(enable_timing=True)
+    es0.record(stream)
+    for _ in range(n_soak):
+        step()
+    es1.record(stream)
+    launches0 = pkv.launch_count()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
     e0.record(stream)
     for _ in range(K):
         step()
     e1.record(stream)
     torch.cuda.synchronize(dev)
+    clocks = sampler.stop() if sampler else None
     barrier()
     launches = pkv.launch_count() - launches0
     pre = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
@@ -837,9 +1010,9 @@ def run_prefill_gpu(args):
         step(pre[i], post[i])
     torch.cuda.synchronize(dev)
     barrier()
-    clocks = sampler.stop() if sampler else None
     ms_per_step = max_over_ranks(e0.elapsed_time(e1), dev) / K
     prefill_ms = max_over_ranks(sum(a_.elapsed_time(b_) for a_, b_ in zip(pre, post)) / K, dev)
+    soak_ms = es0.elapsed_time(es1) / n_soak if n_soak else None
 
     # end to end: chunk inputs from pinned host memory (one packed copy), output
     # back, every step
@@ -871,48 +1044,89 @@ def run_prefill_gpu(args):
     torch.cuda.synchronize(dev)
     barrier()
     e2e_ms = max_over_ranks(e2.elapsed_time(e3) / KE, dev)
-    if rank != 0:
-        return None
+    return {"pw": pw, "window": window, "steps": K, "ms_per_step": ms_per_step, "prefill_ms": prefill_ms,
+            "soak": {"steps": n_soak, "ms_per_step": soak_ms,
+                     "s": None if soak_ms is None else n_soak * soak_ms / 1e3},
+            "launches": int(launches), "clocks": clocks,
+            "e2e": {"value": pw.num_tokens * world / (e2e_ms * 1e-3), "unit": "tokens/s",
+                    "ms_per_step": e2e_ms, "steps": KE,
+                    "h2d_bytes_per_step": int(packed.nbytes),
+                    "d2h_bytes_per_step": int(out.numel() * out.element_size())},
+            "q": q, "kc": kc, "vc": vc}
+
+
+def prefill_summary(res, world) -> dict:
+    pw, window = res["pw"], res["window"]
     flops = prefill_flops(pw, window)
     peak, peak_kind = load_tensor_peak()
-    achieved = flops / (prefill_ms * 1e-3) / 1e12
+    achieved = flops / (res["prefill_ms"] * 1e-3) / 1e12
+    clocks = res["clocks"]
+    mhz = clocks.get("sm_mhz") if clocks else None
+    return {
+        "workload": prefill_config(pw, world, window)["workload"],
+        "ms_per_step": res["ms_per_step"],
+        "prefill_ms": res["prefill_ms"],
+        "query_tokens_per_s": pw.num_tokens * world / (res["ms_per_step"] * 1e-3),
+        "roofline": {
+            "kernel": "pa_prefill_kernel (tcgen05 S = QK^T and O = PV, TMEM accumulators)",
+            "bound": "tensor", "achieved": achieved, "peak": peak,
+            "peak_source": f"{peak_kind} (MEASURED_PEAKS.json bf16_tflops_sustained)",
+            "unit": "TFLOP/s", "frac": achieved / peak, "traffic": None,
+            "algorithmic_flops_per_call": flops,
+            "flops_rule": "4 * head_dim flops per (query row, query head, attended position): "
+                          "causal pairs only, masked tile halves not counted",
+        },
+        "sustained": res["soak"],
+        "clocks": clocks,
+        "prefill_kcycles_at_median_clock": (res["prefill_ms"] * mhz) if mhz else None,
+        "gpu_launches_per_step": res["launches"] / max(1, res["steps"]),
+        "e2e": res["e2e"],
+    }
+
+
+def run_prefill_gpu(args):
+    import torch
+    rank, world, local = dist_env()
+    if world > 1:
+        torch.cuda.set_device(local)
+        init_dist("nccl")
+    dev = torch.device("cuda", local if world > 1 else 0)
+    torch.cuda.set_device(dev)
+    from paged_kv_cache_100_gb300.build import build
+    if rank == 0 or world == 1:
+        build()
+    barrier()
+    import paged_kv_cache_100_gb300 as pkv
+    stream = torch.cuda.current_stream(dev)
+    res = measure_prefill(pkv, dev, stream, args, soak_s=args.soak_seconds, rank=rank, world=world)
+    if rank != 0:
+        return None
+    summ = prefill_summary(res, world)
+    pw = res["pw"]
     line = {
         "metric": PREFILL_METRIC,
-        "value": pw.num_tokens * world / (ms_per_step * 1e-3),
+        "value": summ["query_tokens_per_s"],
         "unit": "tokens/s",
         "n_gpus": world,
-        "steps": K,
+        "steps": args.steps,
         "warmup": args.warmup,
-        "ms_per_step": ms_per_step,
+        "ms_per_step": res["ms_per_step"],
         "higher_is_better": True,
         "scaling": "weak",
         "vs_baseline": None,
         "dtype": "bf16",
         "data": "synthetic (seeded; N(0, %g) values, shuffled block pool)" % pw.value_std,
-        "config": prefill_config(pw, world, window),
-        "prefill_ms": prefill_ms,
-        "roofline": {
-            "kernel": "pa_prefill_kernel (tcgen05 S = QK^T and O = PV, TMEM accumulators)",
-            "bound": "tensor",
-            "achieved": achieved,
-            "peak": peak,
-            "peak_source": f"{peak_kind} (MEASURED_PEAKS.json bf16_tflops_sustained)",
-            "unit": "TFLOP/s",
-            "frac": achieved / peak,
-            "traffic": None,
-            "algorithmic_flops_per_call": flops,
-            "flops_rule": "4 * head_dim flops per (query row, query head, attended position): "
-                          "causal pairs only, masked tile halves not counted",
-        },
-        "gpu_launches": int(launches),
-        "clocks": clocks,
-        "e2e": {"value": pw.num_tokens * world / (e2e_ms * 1e-3), "unit": "tokens/s",
-                "ms_per_step": e2e_ms, "steps": KE,
-                "h2d_bytes_per_step": int(packed.nbytes),
-                "d2h_bytes_per_step": int(out.numel() * out.element_size())},
+        "config": prefill_config(pw, world, args.window),
+        "prefill_ms": res["prefill_ms"],
+        "roofline": summ["roofline"],
+        "gpu_launches": res["launches"],
+        "clocks": res["clocks"],
+        "sustained": res["soak"],
+        "e2e": res["e2e"],
     }
     if not args.no_cpu_baseline and world == 1:
-        line["cpu_baseline"] = prefill_cpu_baseline(pw, q, kc, vc, args.cpu_seconds, window)
+        line["cpu_baseline"] = prefill_cpu_baseline(pw, res["q"], res["kc"], res["vc"],
+                                                    args.cpu_seconds, args.window)
     return line
 
 
@@ -950,7 +1164,7 @@ def prefill_cpu_baseline(pw, q, kc, vc, budget_s, window):
     sample_pairs = int((np.minimum(pos, window) if window else pos).sum())
     t_batch = dt / reps * prefill_pairs(pw, window) / sample_pairs
     return {"value": pw.num_tokens / t_batch, "unit": "tokens/s", "cores": threads,
-            "kind": "oracle",
+            "cpu": cpu_model(), "kind": "oracle",
             "sample": f"last {rows} chunk rows of the longest sequence (context {L}, all "
                       f"{pw.num_q_heads} heads) x {reps} repetitions in {dt:.1f} s; time scaled "
                       "to the batch by attended (row, position) pairs"}
@@ -999,7 +1213,7 @@ def run_prefill_reference(args):
         "ms_per_step": dt / max(done, 1) * 1e3, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "f64", "data": "synthetic (seeded)",
         "config": prefill_config(pw, world, args.window),
-        "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": threads, "kind": "oracle",
+        "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": threads, "cpu": cpu_model(), "kind": "oracle",
                          "sample": f"{done} steps, each the last {rows} chunk rows of the longest "
                                    f"sequence (context {L}); rate scaled to the batch by "
                                    "attended (row, position) pairs"},
@@ -1030,6 +1244,12 @@ def main(argv=None):
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--reference-seconds", type=float, default=60.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--soak-seconds", type=float, default=0.5,
+                    help="length of the loop of the same step that precedes each timed region "
+                         "(the NVML clock samples cover it and the timed steps)")
+    ap.add_argument("--no-per-config", action="store_true",
+                    help="skip the per-configuration record (every workload, FP8, windows, "
+                         "prefill) that a one-GPU decode run adds to its line")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")

@@ -104,6 +104,7 @@ static_assert(kDrain + 1 == kNumBars, "barrier count");
 // and the two-entry item queue
 static_assert(kNumBars * 8 + 20 <= 256, "barrier block");
 static_assert(kSmemBytes <= 227 * 1024, "shared memory");
+static_assert(kQT * kRows * kD * 4 <= 2 * kStages * kTile, "prefix partials staged over the K/V rings");
 
 // TMEM columns: S_A, S_B, then O_A, O_B.
 constexpr uint32_t kTmemCols = 512;
@@ -195,6 +196,12 @@ __device__ __forceinline__ uint4 bf16x8_to_f16x8(uint4 w) {
             : "=r"(o[i])
             : "f"(__uint_as_float(in[i] & 0xffff0000u)), "f"(__uint_as_float(in[i] << 16)));
     return make_uint4(o[0], o[1], o[2], o[3]);
+}
+
+// |x| of both halves of an f16 pair (the sign bits cleared)
+__device__ __forceinline__ __half2 abs_f16x2(uint32_t w) {
+    const uint32_t m = w & 0x7fff7fffu;
+    return *reinterpret_cast<const __half2 *>(&m);
 }
 
 __device__ __forceinline__ void named_sync(int id) {
@@ -475,13 +482,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
                 item_issued = it;
                 const int32_t *trow = a.block_tables + (size_t)d.b * a.max_blocks;
-                for (int j = 0; ok && j < d.n_tiles; ++j) {
-                    const uint32_t gs = gstep + j;
-                    const int s = gs % kStages;
-                    const uint32_t ph = (gs / kStages) & 1u;   // this use of stage s
+                // K/V step j of this item, as rows of the pool maps (8 blocks at most)
+                auto step_rows = [&](int j, int (&rows)[8]) {
                     const int blk0 = d.blk_lo + 8 * j;
                     const int nb = min(8, d.blk_hi - blk0);
-                    int rows[8];
                     for (int i = 0; i < nb; ++i) {
                         int phys = a.staged ? blk0 + i : trow[blk0 + i];
                         if ((unsigned)phys >= (unsigned)a.num_blocks) {
@@ -490,6 +494,14 @@ __global__ void __launch_bounds__(kThreads, 1)
                         }
                         rows[i] = (phys * a.num_kv_heads + d.kvh) * kBlockSize;
                     }
+                    return nb;
+                };
+                for (int j = 0; ok && j < d.n_tiles; ++j) {
+                    const uint32_t gs = gstep + j;
+                    const int s = gs % kStages;
+                    const uint32_t ph = (gs / kStages) & 1u;   // this use of stage s
+                    int rows[8];
+                    const int nb = step_rows(j, rows);
                     if (gs >= kStages && !wait_or_fail(&bars[kKEmpty + s], ph ^ 1u, fail, a.status)) {
                         ok = false;
                         break;
@@ -626,7 +638,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         // permutes chunks within a row).
         const int ct = threadIdx.x - kConvWarp0 * 32;
         uint32_t gstep = 0;
-        uint32_t saturated = 0;   // halves that became +-65504: only out-of-range inputs do
+        // running maximum of |f16 value| written (NaN ignored): 65504 is no bf16
+        // value, so a maximum of 65504 means an input outside f16's range saturated
+        __half2 vmax = __float2half2_rn(0.f);
         bool ok = true;
         for (int it = 0;; ++it) {
             int item;
@@ -659,18 +673,16 @@ __global__ void __launch_bounds__(kThreads, 1)
                     const uint4 h = (edge && (kp < d.kv_lo || kp >= d.kv_hi)) ? make_uint4(0, 0, 0, 0)
                                                                               : bf16x8_to_f16x8(w);
                     vt[c] = h;
-                    // 65504 is no bf16 value, so an f16 of magnitude 65504 is a saturated one
-                    saturated |= __vcmpeq2(h.x & 0x7fff7fffu, 0x7bff7bffu) |
-                                 __vcmpeq2(h.y & 0x7fff7fffu, 0x7bff7bffu) |
-                                 __vcmpeq2(h.z & 0x7fff7fffu, 0x7bff7bffu) |
-                                 __vcmpeq2(h.w & 0x7fff7fffu, 0x7bff7bffu);
+                    vmax = __hmax2(__hmax2(vmax, abs_f16x2(h.x)),
+                                   __hmax2(__hmax2(abs_f16x2(h.y), abs_f16x2(h.z)), abs_f16x2(h.w)));
                 }
                 fence_proxy_async_smem();
                 mbar_arrive(&bars[kVConv + st]);
             }
             gstep += d.n_tiles;
         }
-        if (saturated) report(a.status, PA_DEV_RANGE);
+        const uint32_t vm = *reinterpret_cast<const uint32_t *>(&vmax);
+        if ((vm & 0xffffu) == 0x7bffu || (vm >> 16) == 0x7bffu) report(a.status, PA_DEV_RANGE);
     } else {
         // ---------------- softmax groups ----------------
         const int x = (warp - 2) / (kGroup / 32);     // Q tile of this group
@@ -850,30 +862,51 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
                 for (int o = 1; o < kSplit; ++o) l_row += red[(sx * kSplit + ((part + o) % kSplit)) * kRows + r];
                 const bool drained = warp_wait(&bars[kDrain], it & 1, fail, a.status);
-                if (kPrefix && __all_sync(0xffffffffu, ok) && drained) {
+                if constexpr (kPrefix) {
                     // split-K partial of this chunk: (max, sum) and the unnormalised
-                    // output, in the partial row of (sequence, head, chunk)
-                    tc_fence_after();
-                    const size_t prow = ((size_t)(tx0 + tr) * a.num_q_heads + d.kvh * g + (r % g)) * a.max_parts +
-                                        d.zidx;
+                    // output, in the partial row of (sequence, head, chunk).  The
+                    // rows pass through shared memory (the K/V rings are idle once
+                    // the CTA's one item has drained) so that each 512-byte row
+                    // leaves in one coalesced store; a thread's own columns would
+                    // scatter over 32 rows per store.  Chunk c of tile row rr sits
+                    // at c ^ (rr % 32) of the row (fewest bank conflicts both ways).
+                    const bool go = group_all(x, __all_sync(0xffffffffu, ok) && drained);
+                    float4 *stage = reinterpret_cast<float4 *>(sK) + (size_t)x * kRows * (kD / 4);
                     const float vs = a.v_scales != nullptr ? a.v_scales[d.kvh] : 1.f;
+                    if (go) {
+                        tc_fence_after();
+                        float4 *srow = stage + (size_t)r * (kD / 4);
 #pragma unroll 1
-                    for (int c = 0; c < kCols; c += 32) {
-                        uint32_t o[32];
-                        tmem_ld32(o_base + c, o);
-                        tmem_wait_ld();
-                        if (real) {
-                            float4 *dst = reinterpret_cast<float4 *>(a.part_o + prow * kD + part * kCols + c);
+                        for (int c = 0; c < kCols; c += 32) {
+                            uint32_t o[32];
+                            tmem_ld32(o_base + c, o);
+                            tmem_wait_ld();
 #pragma unroll
                             for (int q = 0; q < 8; ++q)
-                                dst[q] = make_float4(__uint_as_float(o[4 * q]) * vs, __uint_as_float(o[4 * q + 1]) * vs,
-                                                     __uint_as_float(o[4 * q + 2]) * vs,
-                                                     __uint_as_float(o[4 * q + 3]) * vs);
+                                srow[((part * kCols + c) / 4 + q) ^ (r & 31)] =
+                                    make_float4(__uint_as_float(o[4 * q]) * vs, __uint_as_float(o[4 * q + 1]) * vs,
+                                                __uint_as_float(o[4 * q + 2]) * vs,
+                                                __uint_as_float(o[4 * q + 3]) * vs);
+                        }
+                        if (real && part == 0) {
+                            const size_t prow = ((size_t)(tx0 + tr) * a.num_q_heads + d.kvh * g + (r % g)) *
+                                                    a.max_parts + d.zidx;
+                            a.part_ml[prow] = make_float2(l_row > 0.f ? m_used : -INFINITY, l_row);
                         }
                     }
-                    if (real && part == 0)
-                        a.part_ml[prow] = make_float2(l_row > 0.f ? m_used : -INFINITY, l_row);
-                } else if (!kPrefix && __all_sync(0xffffffffu, ok) && drained) {
+                    named_sync(1 + x);
+                    if (go) {
+                        // warp gw of the group writes tile rows [16 gw, 16 gw + 16)
+                        for (int rr = gw * (kRows / (kGroup / 32)); rr < (gw + 1) * (kRows / (kGroup / 32)); ++rr) {
+                            const int trr = rr / g;
+                            if (trr >= ntok) continue;
+                            const size_t prow = ((size_t)(tx0 + trr) * a.num_q_heads + d.kvh * g + (rr % g)) *
+                                                    a.max_parts + d.zidx;
+                            reinterpret_cast<float4 *>(a.part_o + prow * kD)[lane] =
+                                stage[(size_t)rr * (kD / 4) + (lane ^ (rr & 31))];
+                        }
+                    }
+                } else if (__all_sync(0xffffffffu, ok) && drained) {
                     tc_fence_after();
                     const float inv = l_row > 0.f ? 1.f / l_row : 0.f;
                     __nv_bfloat16 *orow = static_cast<__nv_bfloat16 *>(a.out) +
