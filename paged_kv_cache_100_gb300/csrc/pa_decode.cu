@@ -1044,6 +1044,9 @@ pa_decode_bf16_kernel(const __grid_constant__ CUtensorMap kmap,
     const int my_count = w.nblk > warp ? (w.nblk - warp + NW - 1) / NW : 0;
     const int row_base = w.head * kBlockSize;   // + phys * Hkv * 16
 
+    // Each K/V tile is read once per call: it leaves L2 first, so that what is
+    // read again (tables, queries, partials, a shared prefix) stays.
+    const uint64_t stream_policy = l2_policy_evict_first();
     auto issue = [&](int it) {
         const int s = it % STAGES;
         const int phys = s_table[warp + it * NW];
@@ -1053,8 +1056,8 @@ pa_decode_bf16_kernel(const __grid_constant__ CUtensorMap kmap,
         mbar_arrive_expect_tx(&my_bars[s], Lay::kStageBytes);
 #pragma unroll
         for (int x = 0; x < D; x += Lay::kBoxElems) {
-            tma_load_2d(kt + (x / Lay::kBoxElems) * 2048, &kmap, x, y, &my_bars[s]);
-            tma_load_2d(vt + (x / Lay::kBoxElems) * 2048, &vmap, x, y, &my_bars[s]);
+            tma_load_2d_hint(kt + (x / Lay::kBoxElems) * 2048, &kmap, x, y, &my_bars[s], stream_policy);
+            tma_load_2d_hint(vt + (x / Lay::kBoxElems) * 2048, &vmap, x, y, &my_bars[s], stream_policy);
         }
     };
 
