@@ -1648,10 +1648,10 @@ cudaError_t allow_smem(K kernel, size_t bytes) {
 #define PA_GQA16_STAGES 2
 #endif
 // FP8 pools (4 KiB per block): MHA 8 warps x 2 stages (64 KiB, three CTAs per
-// SM); GQA 8 warps x 3 stages (96 KiB, two CTAs per SM).  Measured
-// alternatives: MHA 8x3, 12x2, 4x4 (7B-shaped batch 89.4 us at 8x2 against
-// 92.5-99.2 us); GQA, with P.V on single f16 weights, 4x2, 4x3, 4x4, 6x2, 8x2
-// (70B-shaped batch 206.0 us at 8x3 against 208.3-210.6 us).
+// SM); GQA 6 warps x 3 stages (72 KiB, three CTAs per SM).  Measured
+// alternatives: MHA 8x3, 12x2, 6x3, 4x4 (7B-shaped batch 92.3 us at 8x2 against
+// 94.5-105.1 us); GQA 8x3, 8x2, 4x4, 12x2 (70B-shaped batch 198.2 us at 6x3
+// against 200.9-244.0 us).
 #ifndef PA_MHA8_WARPS
 #define PA_MHA8_WARPS 8
 #endif
@@ -1659,7 +1659,7 @@ cudaError_t allow_smem(K kernel, size_t bytes) {
 #define PA_MHA8_STAGES 2
 #endif
 #ifndef PA_GQA8_WARPS
-#define PA_GQA8_WARPS 8
+#define PA_GQA8_WARPS 6
 #endif
 #ifndef PA_GQA8_STAGES
 #define PA_GQA8_STAGES 3
