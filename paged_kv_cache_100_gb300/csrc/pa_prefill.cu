@@ -172,6 +172,32 @@ __device__ __forceinline__ float ex2_approx(float x) {
     return y;
 }
 
+// Packed pairs of floats for the f32x2 arithmetic of sm_100 and later (one
+// instruction for two lanes of work): x = (lo, hi).
+__device__ __forceinline__ uint64_t f2_pack(float lo, float hi) {
+    uint64_t r;
+    asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
+    return r;
+}
+__device__ __forceinline__ void f2_unpack(uint64_t x, float &lo, float &hi) {
+    asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(x));
+}
+__device__ __forceinline__ uint64_t f2_fma(uint64_t a, uint64_t b, uint64_t c) {
+    uint64_t r;
+    asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(r) : "l"(a), "l"(b), "l"(c));
+    return r;
+}
+__device__ __forceinline__ uint64_t f2_add(uint64_t a, uint64_t b) {
+    uint64_t r;
+    asm("add.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
+    return r;
+}
+__device__ __forceinline__ uint64_t f2_mul(uint64_t a, uint64_t b) {
+    uint64_t r;
+    asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
+    return r;
+}
+
 __device__ __forceinline__ uint32_t pack2_bf16(float lo, float hi) {
     __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
     return *reinterpret_cast<uint32_t *>(&v);
@@ -737,10 +763,18 @@ __global__ void __launch_bounds__(kThreads, 1)
                     int L = real ? a.context_lens[tx0 + tr] : 0;
                     L = L < 0 ? 0 : (L > lmax ? lmax : L);
                     qpos = min(L, d.blk_hi * kBlockSize) - 1;   // last attended position
-                    qpos_lo = -1;                                // always mask (short kernel)
+                    qpos_lo = -1;                                // decided per warp below
                     qpos_hi = 0;
                     wlo = INT_MIN;
                 }
+                // Whether the 32 columns from position kc need the per-element
+                // mask: in prefill, unless they lie inside every row's range of
+                // the tile; in prefix mode (rows of many sequences), unless they
+                // lie inside every row's range of this warp (one vote per chunk).
+                auto chunk_masked = [&](int kc) -> bool {
+                    if constexpr (kPrefix) return __any_sync(0xffffffffu, kc + 31 > qpos);
+                    return (kc + 31 > qpos_lo) || (a.window > 0 && kc < qpos_hi + 1 - a.window);
+                };
                 float m_used = -INFINITY, l = 0.f;
                 // Every thread of the group runs every iteration and reaches the
                 // named barrier the same number of times, even after a wait gave
@@ -760,7 +794,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                             tmem_ld32(s_base + c, v);
                             tmem_wait_ld();
                             const int kc = k0 + c;
-                            if ((kc + 31 > qpos_lo) || (!kPrefix && a.window > 0 && kc < qpos_hi + 1 - a.window)) {
+                            if (chunk_masked(kc)) {
 #pragma unroll
                                 for (int i = 0; i < 32; ++i)
                                     if (!(kc + i <= qpos && kc + i >= wlo)) v[i] = __float_as_uint(fill);
@@ -808,8 +842,14 @@ __global__ void __launch_bounds__(kThreads, 1)
                             uint32_t o[32];
                             tmem_ld32(o_base + c, o);
                             tmem_wait_ld();
+                            const uint64_t a2 = f2_pack(alpha, alpha);
 #pragma unroll
-                            for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * alpha);
+                            for (int i = 0; i < 32; i += 2) {
+                                float r0, r1;
+                                f2_unpack(f2_mul(f2_pack(__uint_as_float(o[i]), __uint_as_float(o[i + 1])), a2), r0, r1);
+                                o[i] = __float_as_uint(r0);
+                                o[i + 1] = __float_as_uint(r1);
+                            }
                             tmem_st32(o_base + c, o);
                         }
                         tmem_wait_st();
@@ -824,31 +864,40 @@ __global__ void __launch_bounds__(kThreads, 1)
                     // the output tolerance, where bf16's 8 bits do not), written as
                     // 16 columns of pairs over the first half of the 32 columns it
                     // was read from
-                    float ps4[4] = {0.f, 0.f, 0.f, 0.f};
+                    // pairs of columns on f32x2 arithmetic: one FMA and one add
+                    // instruction for two weights
+                    const uint64_t k2 = f2_pack(sl2k, sl2k), nm2 = f2_pack(-m_ref, -m_ref);
+                    uint64_t ps2[2] = {f2_pack(0.f, 0.f), f2_pack(0.f, 0.f)};
 #pragma unroll 1
                     for (int c = 0; c < kCols; c += 32) {
                         uint32_t v[32];
                         tmem_ld32(s_base + c, v);
                         tmem_wait_ld();
                         const int kc = k0 + c;
-                        const bool masked =
-                            (kc + 31 > qpos_lo) || (!kPrefix && a.window > 0 && kc < qpos_hi + 1 - a.window);
+                        const bool masked = chunk_masked(kc);
                         uint32_t pp[16];
 #pragma unroll
                         for (int i = 0; i < 32; i += 2) {
-                            float p0 = ex2_approx(fmaf(__uint_as_float(v[i]), sl2k, -m_ref));
-                            float p1 = ex2_approx(fmaf(__uint_as_float(v[i + 1]), sl2k, -m_ref));
+                            float x0, x1;
+                            f2_unpack(f2_fma(f2_pack(__uint_as_float(v[i]), __uint_as_float(v[i + 1])), k2, nm2), x0, x1);
+                            float p0 = ex2_approx(x0);
+                            float p1 = ex2_approx(x1);
                             if (masked) {
                                 if (!(kc + i <= qpos && kc + i >= wlo)) p0 = 0.f;
                                 if (!(kc + i + 1 <= qpos && kc + i + 1 >= wlo)) p1 = 0.f;
                             }
-                            ps4[(i >> 1) & 3] += p0 + p1;
+                            ps2[(i >> 1) & 1] = f2_add(ps2[(i >> 1) & 1], f2_pack(p0, p1));
                             pp[i >> 1] = pack2_f16(p0, p1);
                         }
                         tmem_st16(s_base + c, pp);
                     }
                     tmem_wait_st();
-                    l += (ps4[0] + ps4[1]) + (ps4[2] + ps4[3]);
+                    {
+                        float a0, a1, b0, b1;
+                        f2_unpack(ps2[0], a0, a1);
+                        f2_unpack(ps2[1], b0, b1);
+                        l += (a0 + b0) + (a1 + b1);
+                    }
                     tc_fence_before();
                     mbar_arrive(&bars[kPFull + x]);
                 }
