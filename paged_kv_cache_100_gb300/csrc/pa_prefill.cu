@@ -234,6 +234,12 @@ __device__ __forceinline__ void named_sync(int id) {
     asm volatile("bar.sync %0, %1;" ::"r"(id), "n"(kGroup) : "memory");
 }
 
+// The two warps of a softmax group that hold the same 32 rows (one warp per
+// half of the columns) meet here: barriers 5 .. 5 + 4 kQT - 1, 64 threads each.
+__device__ __forceinline__ void pair_sync(int x, int quarter) {
+    asm volatile("bar.sync %0, 64;" ::"r"(5 + 4 * x + quarter) : "memory");
+}
+
 // The work of one CTA step ("item"): two 128-row Q tiles of one KV head
 // against a range of positions.
 struct Item {
@@ -813,7 +819,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     const int rp = ex & 1;
                     ++ex;
                     red[(rp * kSplit + part) * kRows + r] = mrow;
-                    named_sync(1 + x);
+                    pair_sync(x, quarter);
 #pragma unroll
                     for (int o = 1; o < kSplit; ++o) {
                         const float other = red[(rp * kSplit + ((part + o) % kSplit)) * kRows + r];
@@ -906,7 +912,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const int sx = ex & 1;
                 ++ex;
                 red[(sx * kSplit + part) * kRows + r] = l;
-                named_sync(1 + x);
+                pair_sync(x, quarter);
                 float l_row = l;
 #pragma unroll
                 for (int o = 1; o < kSplit; ++o) l_row += red[(sx * kSplit + ((part + o) % kSplit)) * kRows + r];
