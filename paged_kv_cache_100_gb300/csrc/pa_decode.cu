@@ -300,7 +300,7 @@ struct MhaConsumer {
         for (int M = 2; M < 32; M <<= 1) bmax = fmaxf(bmax, __shfl_xor_sync(kFull, bmax, M));
         const float m_new = fmaxf(m, bmax);
         const float alpha = exp2f(m - m_new);
-        const float p = exp2f(s - m_new);
+        const float p = ex2_fast(s - m_new);
         l = l * alpha + ((lane & 1) ? 0.f : p);
         m = m_new;
 #pragma unroll
@@ -414,10 +414,10 @@ struct GqaConsumer {
         float p[2][4];
 #pragma unroll
         for (int j = 0; j < 2; ++j) {
-            p[j][0] = exp2f(s[j][0] - mn0);
-            p[j][1] = exp2f(s[j][1] - mn0);
-            p[j][2] = HI ? exp2f(s[j][2] - mn1) : 0.f;
-            p[j][3] = HI ? exp2f(s[j][3] - mn1) : 0.f;
+            p[j][0] = ex2_fast(s[j][0] - mn0);
+            p[j][1] = ex2_fast(s[j][1] - mn0);
+            p[j][2] = HI ? ex2_fast(s[j][2] - mn1) : 0.f;
+            p[j][3] = HI ? ex2_fast(s[j][3] - mn1) : 0.f;
         }
         l0 = l0 * a0 + (p[0][0] + p[0][1]) + (p[1][0] + p[1][1]);
         if (HI) l1 = l1 * a1 + (p[0][2] + p[0][3]) + (p[1][2] + p[1][3]);
@@ -548,8 +548,8 @@ struct GqaTConsumer {
         const float a0 = exp2f(m0 - mn0), a1 = exp2f(m1 - mn1);
         m0 = mn0;
         m1 = mn1;
-        const float p0 = exp2f(s[0] - mn0), p1 = exp2f(s[1] - mn1);
-        const float p2 = exp2f(s[2] - mn0), p3 = exp2f(s[3] - mn1);
+        const float p0 = ex2_fast(s[0] - mn0), p1 = ex2_fast(s[1] - mn1);
+        const float p2 = ex2_fast(s[2] - mn0), p3 = ex2_fast(s[3] - mn1);
         l0 = l0 * a0 + (p0 + p2);
         l1 = l1 * a1 + (p1 + p3);
 #pragma unroll
@@ -733,7 +733,7 @@ struct MhaFp8Consumer {
             for (int e = 0; e < 16; ++e) acc[e] *= alpha;
             m = bmax;
         }
-        const float p = exp2f(s - m);
+        const float p = ex2_fast(s - m);
         l += (lane & 1) ? 0.f : p;
 #pragma unroll
         for (int i = 0; i < RPL; ++i) {
@@ -887,8 +887,8 @@ struct GqaTFp8Consumer {
                 o[mt][3] *= a1;
             }
         }
-        const float p0 = exp2f(s[0] - m0), p1 = exp2f(s[1] - m1);
-        const float p2 = exp2f(s[2] - m0), p3 = exp2f(s[3] - m1);
+        const float p0 = ex2_fast(s[0] - m0), p1 = ex2_fast(s[1] - m1);
+        const float p2 = ex2_fast(s[2] - m0), p3 = ex2_fast(s[3] - m1);
         l0 += p0 + p2;
         l1 += p1 + p3;
         // P in f16, rounded once: 11 significant bits move an output by at most
@@ -1223,10 +1223,10 @@ struct PrefixWarp {
         float p[2][4];
 #pragma unroll
         for (int j = 0; j < 2; ++j) {
-            p[j][0] = exp2f(s[j][0] - ref0);
-            p[j][1] = exp2f(s[j][1] - ref0);
-            p[j][2] = exp2f(s[j][2] - ref1);
-            p[j][3] = exp2f(s[j][3] - ref1);
+            p[j][0] = ex2_fast(s[j][0] - ref0);
+            p[j][1] = ex2_fast(s[j][1] - ref0);
+            p[j][2] = ex2_fast(s[j][2] - ref1);
+            p[j][3] = ex2_fast(s[j][3] - ref1);
         }
         l0 = l0 * a0 + (p[0][0] + p[0][1]) + (p[1][0] + p[1][1]);
         l1 = l1 * a1 + (p[0][2] + p[0][3]) + (p[1][2] + p[1][3]);
@@ -1436,7 +1436,7 @@ __global__ void __launch_bounds__(NW * 32) pa_decode_f32_kernel(const float *__r
             for (int M = 16; M >= 1; M >>= 1) s += __shfl_xor_sync(kFull, s, M);
             const float m_new = fmaxf(m, s);
             const float alpha = exp2f(m - m_new);
-            const float p = exp2f(s - m_new);
+            const float p = ex2_fast(s - m_new);
             l = l * alpha + p;
 #pragma unroll
             for (int e = 0; e < EPL; ++e) acc[e] = fmaf(p, vrow[lane + 32 * e], acc[e] * alpha);

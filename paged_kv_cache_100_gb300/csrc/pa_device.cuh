@@ -239,6 +239,16 @@ __device__ __forceinline__ uint32_t pack_f16x2(float lo, float hi) {
     return *reinterpret_cast<uint32_t *>(&v);
 }
 
+// 2^x with the single-instruction approximation (ex2.approx.ftz: a relative
+// error of about 2^-22; results below 2^-126 flush to +0, and 2^-inf = +0).
+// Used for the softmax weights, whose rounding to f16 or bf16 afterwards is far
+// coarser.
+__device__ __forceinline__ float ex2_fast(float x) {
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+
 // ---------------------------------------------------------------------------
 // bf16 helpers (bfloat16 is the upper half of a binary32, so widening is exact)
 // ---------------------------------------------------------------------------
