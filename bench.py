@@ -398,13 +398,16 @@ def measure_decode(pkv, dev, stream, args, workload, kv_dtype="bf16", window=0, 
     ops = [StepOps(pkv, wl, k_, v_, ks, vs, P, ws, n_prefix, window) for k_, v_ in pools]
     state = {"i": 0}
 
+    def step_pre(o, kn_=kn, vn_=vn, slots_=slots, pairs_=pairs):
+        o.write(kn_, vn_, slots_)
+        if has_cow:
+            pkv.block_copy(o.kc, o.vc, pairs_)
+
     def step(ev_pre=None, ev_post=None, q_=q, kn_=kn, vn_=vn, slots_=slots, pairs_=pairs, bt_=bt,
              lens_=lens):
         o = ops[state["i"] % copies]
         state["i"] += 1
-        o.write(kn_, vn_, slots_)
-        if has_cow:
-            pkv.block_copy(o.kc, o.vc, pairs_)
+        step_pre(o, kn_, vn_, slots_, pairs_)
         if ev_pre is not None:
             ev_pre.record(stream)
         o.decode(q_, bt_, lens_, out)
@@ -414,10 +417,51 @@ def measure_decode(pkv, dev, stream, args, workload, kv_dtype="bf16", window=0, 
     for _ in range(args.warmup):
         step()
     torch.cuda.synchronize(dev)
+    # With --graphs the device-timed runs replay CUDA graphs of the step's
+    # library calls, one set per pool copy: the whole step (write,
+    # copy-on-write, decode), and its write/copy and its decode call apart (for
+    # the per-call events).  The kernels, their order and their launch
+    # attributes are the captured calls'; replaying them takes the host's
+    # per-call work (argument checks, tensor-map encoding, one launch per
+    # kernel) out of the GPU's way, as a serving loop that replays a captured
+    # decode step does, but each replay starts only when the one before has
+    # ended.  The end-to-end run below calls the public API directly.
+    timed_step = step
+    kernels_per_step = None
+    if args.graphs:
+        graphs = []
+        for o in ops:
+            gs, gp, gd = torch.cuda.CUDAGraph(), torch.cuda.CUDAGraph(), torch.cuda.CUDAGraph()
+            n0 = pkv.launch_count()
+            with torch.cuda.graph(gs, capture_error_mode="thread_local"):
+                step_pre(o)
+                o.decode(q, bt, lens, out)
+            kernels_per_step = pkv.launch_count() - n0
+            with torch.cuda.graph(gp, capture_error_mode="thread_local"):
+                step_pre(o)
+            with torch.cuda.graph(gd, capture_error_mode="thread_local"):
+                o.decode(q, bt, lens, out)
+            graphs.append((gs, gp, gd))
+
+        def graph_step(ev_pre=None, ev_post=None):
+            gs, gp, gd = graphs[state["i"] % copies]
+            state["i"] += 1
+            if ev_pre is None:
+                gs.replay()
+            else:
+                gp.replay()
+                ev_pre.record(stream)
+                gd.replay()
+                ev_post.record(stream)
+
+        timed_step = graph_step
+        for _ in range(max(3, args.warmup)):
+            timed_step()
+        torch.cuda.synchronize(dev)
     # a first estimate of the step time sizes the clock-sampling loop
     t0 = time.perf_counter()
     for _ in range(3):
-        step()
+        timed_step()
     torch.cuda.synchronize(dev)
     est = max((time.perf_counter() - t0) / 3, 1e-5)
     n_soak = int(max(1, soak_s / est)) if soak_s > 0 else 0
@@ -434,7 +478,7 @@ def measure_decode(pkv, dev, stream, args, workload, kv_dtype="bf16", window=0, 
     es1 = torch.cuda.Event(enable_timing=True)
     es0.record(stream)
     for _ in range(n_soak):
-        step()
+        timed_step()
     es1.record(stream)
     launches0 = pkv.launch_count()
     # timed region: K whole steps back to back
@@ -442,12 +486,16 @@ def measure_decode(pkv, dev, stream, args, workload, kv_dtype="bf16", window=0, 
     e1 = torch.cuda.Event(enable_timing=True)
     e0.record(stream)
     for _ in range(K):
-        step()
+        timed_step()
     e1.record(stream)
     torch.cuda.synchronize(dev)
     clocks = sampler.stop() if sampler else None
     barrier()
-    launches = pkv.launch_count() - launches0
+    # kernels of the library launched in the timed region: counted by the
+    # library's own launch counter, or (graphs) as its launches per captured
+    # step times the replays
+    launches = (kernels_per_step * K if kernels_per_step is not None
+                else pkv.launch_count() - launches0)
     # K steps again, each decode call bracketed by events on the launching
     # stream (the roofline's per-call duration)
     pre = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
@@ -456,7 +504,7 @@ def measure_decode(pkv, dev, stream, args, workload, kv_dtype="bf16", window=0, 
     e3 = torch.cuda.Event(enable_timing=True)
     e2.record(stream)
     for i in range(K):
-        step(pre[i], post[i])
+        timed_step(pre[i], post[i])
     e3.record(stream)
     torch.cuda.synchronize(dev)
     barrier()
@@ -474,6 +522,9 @@ def measure_decode(pkv, dev, stream, args, workload, kv_dtype="bf16", window=0, 
         "soak": {"steps": n_soak, "ms_per_step": soak_ms,
                  "s": None if soak_ms is None else n_soak * soak_ms / 1e3},
         "launches": int(launches), "clocks": clocks, "e2e": e2e,
+        "launch_mode": ("CUDA graph replay of the step's captured library calls "
+                        "(%d kernels per step)" % kernels_per_step) if kernels_per_step is not None
+                       else "direct library calls",
         "logical": logical, "unique_kv": unique_kv, "copies": copies,
         "q": q, "kc": kc, "vc": vc, "ks": ks, "vs": vs,
     }
@@ -536,6 +587,7 @@ def decode_summary(res, args, workload, decode, partition_size, world) -> dict:
         "clocks": clocks,
         "decode_kcycles_at_median_clock": (decode_ms * mhz) if mhz else None,
         "gpu_launches_per_step": res["launches"] / max(args.steps, 1),
+        "launch_mode": res["launch_mode"],
         "e2e": res["e2e"],
         "l2": l2_note(res["unique_kv"], res["copies"]),
     }
@@ -624,6 +676,7 @@ def run_gpu(args):
             "decode_method": summ["decode_method"],
             "roofline": summ["roofline"],
             "gpu_launches": res["launches"],
+            "launch_mode": res["launch_mode"],
             "clocks": res["clocks"],
             "clocks_window": "NVML every 20 ms over a loop of the same step (%d steps, %.2f s) "
                              "that ends where the timed region begins, and the timed region"
@@ -1247,6 +1300,9 @@ def main(argv=None):
     ap.add_argument("--soak-seconds", type=float, default=0.5,
                     help="length of the loop of the same step that precedes each timed region "
                          "(the NVML clock samples cover it and the timed steps)")
+    ap.add_argument("--graphs", action="store_true",
+                    help="time CUDA graph replays of the step's library calls instead of the "
+                         "calls themselves")
     ap.add_argument("--no-per-config", action="store_true",
                     help="skip the per-configuration record (every workload, FP8, windows, "
                          "prefill) that a one-GPU decode run adds to its line")

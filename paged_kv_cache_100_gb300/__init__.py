@@ -34,9 +34,15 @@ def library_path() -> str:
     return _lib.LIB_PATH
 
 
+_TORCH = None
+
+
 def _torch():
-    import torch
-    return torch
+    global _TORCH
+    if _TORCH is None:
+        import torch
+        _TORCH = torch
+    return _TORCH
 
 
 def _dtype_code(t) -> int:
@@ -66,10 +72,15 @@ def _dev(t, name, dtype=None):
     return t.data_ptr()
 
 
-def _stream(stream, device):
+def _stream(stream, t):
+    """The given stream, else the current stream of tensor t's device."""
+    if stream is not None:
+        return ctypes.c_void_p(stream.cuda_stream)
     torch = _torch()
-    s = torch.cuda.current_stream(device) if stream is None else stream
-    return ctypes.c_void_p(s.cuda_stream)
+    raw = getattr(torch._C, "_cuda_getCurrentRawStream", None)
+    if raw is not None:
+        return ctypes.c_void_p(raw(t.get_device()))
+    return ctypes.c_void_p(torch.cuda.current_stream(t.device).cuda_stream)
 
 
 def _status_ptr(status):
@@ -121,9 +132,9 @@ def decode(query, key_cache, value_cache, block_tables, context_lens, scale=None
     torch = _torch()
     B, Hq, D = query.shape
     NB, Hkv, BS, D2 = key_cache.shape
-    if BS != BLOCK_SIZE or D2 != D or tuple(value_cache.shape) != tuple(key_cache.shape):
+    if BS != BLOCK_SIZE or D2 != D or value_cache.shape != key_cache.shape:
         raise ValueError("pools must be [num_blocks][num_kv_heads][16][head_dim] like query")
-    if block_tables.dim() != 2 or block_tables.shape[0] != B or tuple(context_lens.shape) != (B,):
+    if block_tables.dim() != 2 or block_tables.shape[0] != B or context_lens.shape != (B,):
         raise ValueError("block_tables must be [num_seqs][max_blocks], context_lens [num_seqs]")
     code = _dtype_code(query)
     if key_cache.dtype != query.dtype or value_cache.dtype != query.dtype:
@@ -135,19 +146,22 @@ def decode(query, key_cache, value_cache, block_tables, context_lens, scale=None
     elif out.shape != query.shape or out.dtype != query.dtype:
         raise ValueError("out must match query")
     max_blocks = block_tables.shape[1]
-    need = decode_workspace_bytes(B, Hq, Hkv, D, max_blocks, partition_size, query.dtype)
-    ws_ptr, ws_bytes = None, 0
-    if need > 0:
-        if workspace is None:
+    if workspace is None:
+        # the library's scratch size for this call (0: none needed); a
+        # caller's workspace is passed as given and sized by the library
+        need = decode_workspace_bytes(B, Hq, Hkv, D, max_blocks, partition_size, query.dtype)
+        if need > 0:
             workspace = torch.empty(need, dtype=torch.uint8, device=query.device)
+    ws_ptr, ws_bytes = None, 0
+    if workspace is not None:
         ws_ptr = _dev(workspace, "workspace")
-        ws_bytes = workspace.numel() * workspace.element_size()
+        ws_bytes = workspace.nbytes
     rc = lib().pa_decode(
         _dev(out, "out"), _dev(query, "query"), _dev(key_cache, "key_cache"),
         _dev(value_cache, "value_cache"), _dev(block_tables, "block_tables", torch.int32),
         _dev(context_lens, "context_lens", torch.int32), B, Hq, Hkv, D, BLOCK_SIZE, max_blocks,
         NB, float(scale), code, int(partition_size), ws_ptr, ws_bytes, _status_ptr(status),
-        _stream(stream, query.device))
+        _stream(stream, query))
     check(rc, "pa_decode")
     return out
 
@@ -160,9 +174,9 @@ def decode_shared_prefix(query, key_cache, value_cache, block_tables, context_le
     torch = _torch()
     B, Hq, D = query.shape
     NB, Hkv, BS, D2 = key_cache.shape
-    if BS != BLOCK_SIZE or D2 != D or tuple(value_cache.shape) != tuple(key_cache.shape):
+    if BS != BLOCK_SIZE or D2 != D or value_cache.shape != key_cache.shape:
         raise ValueError("pools must be [num_blocks][num_kv_heads][16][head_dim] like query")
-    if block_tables.dim() != 2 or block_tables.shape[0] != B or tuple(context_lens.shape) != (B,):
+    if block_tables.dim() != 2 or block_tables.shape[0] != B or context_lens.shape != (B,):
         raise ValueError("block_tables must be [num_seqs][max_blocks], context_lens [num_seqs]")
     code = _dtype_code(query)
     if scale is None:
@@ -170,20 +184,20 @@ def decode_shared_prefix(query, key_cache, value_cache, block_tables, context_le
     if out is None:
         out = torch.empty_like(query)
     max_blocks = block_tables.shape[1]
-    need = lib().pa_decode_shared_prefix_workspace_bytes(B, Hq, Hkv, D, max_blocks,
-                                                         int(num_prefix_blocks),
-                                                         int(partition_size))
-    if need == ctypes.c_size_t(-1).value:
-        raise ValueError("invalid arguments for pa_decode_shared_prefix_workspace_bytes")
     if workspace is None:
+        need = lib().pa_decode_shared_prefix_workspace_bytes(B, Hq, Hkv, D, max_blocks,
+                                                                int(num_prefix_blocks),
+                                                                int(partition_size))
+        if need == ctypes.c_size_t(-1).value:
+            raise ValueError("invalid arguments for pa_decode_shared_prefix_workspace_bytes")
         workspace = torch.empty(max(int(need), 16), dtype=torch.uint8, device=query.device)
     rc = lib().pa_decode_shared_prefix(
         _dev(out, "out"), _dev(query, "query"), _dev(key_cache, "key_cache"),
         _dev(value_cache, "value_cache"), _dev(block_tables, "block_tables", torch.int32),
         _dev(context_lens, "context_lens", torch.int32), B, Hq, Hkv, D, BLOCK_SIZE, max_blocks,
         NB, float(scale), code, int(num_prefix_blocks), int(partition_size),
-        _dev(workspace, "workspace"), workspace.numel() * workspace.element_size(),
-        _status_ptr(status), _stream(stream, query.device))
+        _dev(workspace, "workspace"), workspace.nbytes,
+        _status_ptr(status), _stream(stream, query))
     check(rc, "pa_decode_shared_prefix")
     return out
 
@@ -197,25 +211,25 @@ def decode_shared_prefix_fp8(query, key_cache, value_cache, k_scales, v_scales, 
     torch = _torch()
     B, Hq, D = query.shape
     NB, Hkv, BS, D2 = key_cache.shape
-    if BS != BLOCK_SIZE or D2 != D or tuple(value_cache.shape) != tuple(key_cache.shape):
+    if BS != BLOCK_SIZE or D2 != D or value_cache.shape != key_cache.shape:
         raise ValueError("pools must be [num_blocks][num_kv_heads][16][head_dim] like query")
     if not (_is_fp8(key_cache) and _is_fp8(value_cache)) or query.dtype != torch.bfloat16:
         raise TypeError("pa_decode_shared_prefix_fp8 takes E4M3 pools and a bfloat16 query")
-    if tuple(k_scales.shape) != (Hkv,) or tuple(v_scales.shape) != (Hkv,):
+    if k_scales.shape != (Hkv,) or v_scales.shape != (Hkv,):
         raise ValueError("k_scales / v_scales must be [num_kv_heads]")
-    if block_tables.dim() != 2 or block_tables.shape[0] != B or tuple(context_lens.shape) != (B,):
+    if block_tables.dim() != 2 or block_tables.shape[0] != B or context_lens.shape != (B,):
         raise ValueError("block_tables must be [num_seqs][max_blocks], context_lens [num_seqs]")
     if scale is None:
         scale = 1.0 / math.sqrt(D)
     if out is None:
         out = torch.empty_like(query)
     max_blocks = block_tables.shape[1]
-    need = lib().pa_decode_shared_prefix_fp8_workspace_bytes(B, Hq, Hkv, D, max_blocks,
-                                                             int(num_prefix_blocks),
-                                                             int(partition_size))
-    if need == ctypes.c_size_t(-1).value:
-        raise ValueError("invalid arguments for pa_decode_shared_prefix_fp8_workspace_bytes")
     if workspace is None:
+        need = lib().pa_decode_shared_prefix_fp8_workspace_bytes(B, Hq, Hkv, D, max_blocks,
+                                                                    int(num_prefix_blocks),
+                                                                    int(partition_size))
+        if need == ctypes.c_size_t(-1).value:
+            raise ValueError("invalid arguments for pa_decode_shared_prefix_fp8_workspace_bytes")
         workspace = torch.empty(max(int(need), 16), dtype=torch.uint8, device=query.device)
     rc = lib().pa_decode_shared_prefix_fp8(
         _dev(out, "out"), _dev(query, "query"), _dev(key_cache, "key_cache"),
@@ -224,8 +238,8 @@ def decode_shared_prefix_fp8(query, key_cache, value_cache, k_scales, v_scales, 
         _dev(block_tables, "block_tables", torch.int32),
         _dev(context_lens, "context_lens", torch.int32), B, Hq, Hkv, D, BLOCK_SIZE, max_blocks,
         NB, float(scale), int(num_prefix_blocks), int(partition_size),
-        _dev(workspace, "workspace"), workspace.numel() * workspace.element_size(),
-        _status_ptr(status), _stream(stream, query.device))
+        _dev(workspace, "workspace"), workspace.nbytes,
+        _status_ptr(status), _stream(stream, query))
     check(rc, "pa_decode_shared_prefix_fp8")
     return out
 
@@ -247,26 +261,29 @@ def decode_fp8(query, key_cache, value_cache, k_scales, v_scales, block_tables, 
     torch = _torch()
     B, Hq, D = query.shape
     NB, Hkv, BS, D2 = key_cache.shape
-    if BS != BLOCK_SIZE or D2 != D or tuple(value_cache.shape) != tuple(key_cache.shape):
+    if BS != BLOCK_SIZE or D2 != D or value_cache.shape != key_cache.shape:
         raise ValueError("pools must be [num_blocks][num_kv_heads][16][head_dim] like query")
     if not (_is_fp8(key_cache) and _is_fp8(value_cache)) or query.dtype != torch.bfloat16:
         raise TypeError("pa_decode_fp8 takes E4M3 pools and a bfloat16 query")
-    if tuple(k_scales.shape) != (Hkv,) or tuple(v_scales.shape) != (Hkv,):
+    if k_scales.shape != (Hkv,) or v_scales.shape != (Hkv,):
         raise ValueError("k_scales / v_scales must be [num_kv_heads]")
-    if block_tables.dim() != 2 or block_tables.shape[0] != B or tuple(context_lens.shape) != (B,):
+    if block_tables.dim() != 2 or block_tables.shape[0] != B or context_lens.shape != (B,):
         raise ValueError("block_tables must be [num_seqs][max_blocks], context_lens [num_seqs]")
     if scale is None:
         scale = 1.0 / math.sqrt(D)
     if out is None:
         out = torch.empty_like(query)
     max_blocks = block_tables.shape[1]
-    need = decode_workspace_bytes(B, Hq, Hkv, D, max_blocks, partition_size, "fp8")
-    ws_ptr, ws_bytes = None, 0
-    if need > 0:
-        if workspace is None:
+    if workspace is None:
+        # the library's scratch size for this call (0: none needed); a
+        # caller's workspace is passed as given and sized by the library
+        need = decode_workspace_bytes(B, Hq, Hkv, D, max_blocks, partition_size, "fp8")
+        if need > 0:
             workspace = torch.empty(need, dtype=torch.uint8, device=query.device)
+    ws_ptr, ws_bytes = None, 0
+    if workspace is not None:
         ws_ptr = _dev(workspace, "workspace")
-        ws_bytes = workspace.numel() * workspace.element_size()
+        ws_bytes = workspace.nbytes
     rc = lib().pa_decode_fp8(
         _dev(out, "out"), _dev(query, "query"), _dev(key_cache, "key_cache"),
         _dev(value_cache, "value_cache"), _dev(k_scales, "k_scales", torch.float32),
@@ -274,7 +291,7 @@ def decode_fp8(query, key_cache, value_cache, k_scales, v_scales, block_tables, 
         _dev(block_tables, "block_tables", torch.int32),
         _dev(context_lens, "context_lens", torch.int32), B, Hq, Hkv, D, BLOCK_SIZE, max_blocks,
         NB, float(scale), int(partition_size), ws_ptr, ws_bytes, _status_ptr(status),
-        _stream(stream, query.device))
+        _stream(stream, query))
     check(rc, "pa_decode_fp8")
     return out
 
@@ -288,9 +305,9 @@ def decode_sliding_window(query, key_cache, value_cache, block_tables, context_l
     torch = _torch()
     B, Hq, D = query.shape
     NB, Hkv, BS, D2 = key_cache.shape
-    if BS != BLOCK_SIZE or D2 != D or tuple(value_cache.shape) != tuple(key_cache.shape):
+    if BS != BLOCK_SIZE or D2 != D or value_cache.shape != key_cache.shape:
         raise ValueError("pools must be [num_blocks][num_kv_heads][16][head_dim] like query")
-    if block_tables.dim() != 2 or block_tables.shape[0] != B or tuple(context_lens.shape) != (B,):
+    if block_tables.dim() != 2 or block_tables.shape[0] != B or context_lens.shape != (B,):
         raise ValueError("block_tables must be [num_seqs][max_blocks], context_lens [num_seqs]")
     if int(window) <= 0:
         raise ValueError("window must be positive")
@@ -300,7 +317,7 @@ def decode_sliding_window(query, key_cache, value_cache, block_tables, context_l
             raise TypeError("E4M3 pools take a bfloat16 query")
         if k_scales is None or v_scales is None:
             raise ValueError("E4M3 pools need k_scales and v_scales")
-        if tuple(k_scales.shape) != (Hkv,) or tuple(v_scales.shape) != (Hkv,):
+        if k_scales.shape != (Hkv,) or v_scales.shape != (Hkv,):
             raise ValueError("k_scales / v_scales must be [num_kv_heads]")
         code = _lib.PA_DTYPE_FP8_E4M3
         ks_ptr = _dev(k_scales, "k_scales", torch.float32)
@@ -316,23 +333,25 @@ def decode_sliding_window(query, key_cache, value_cache, block_tables, context_l
     elif out.shape != query.shape or out.dtype != query.dtype:
         raise ValueError("out must match query")
     max_blocks = block_tables.shape[1]
-    need = lib().pa_decode_sliding_window_workspace_bytes(B, Hq, Hkv, D, max_blocks, BLOCK_SIZE,
-                                                          int(window), int(partition_size), code)
-    if need == ctypes.c_size_t(-1).value:
-        raise ValueError("invalid arguments for pa_decode_sliding_window_workspace_bytes")
-    ws_ptr, ws_bytes = None, 0
-    if need > 0:
-        if workspace is None:
+    if workspace is None:
+        need = lib().pa_decode_sliding_window_workspace_bytes(B, Hq, Hkv, D, max_blocks,
+                                                              BLOCK_SIZE, int(window),
+                                                              int(partition_size), code)
+        if need == ctypes.c_size_t(-1).value:
+            raise ValueError("invalid arguments for pa_decode_sliding_window_workspace_bytes")
+        if need > 0:
             workspace = torch.empty(need, dtype=torch.uint8, device=query.device)
+    ws_ptr, ws_bytes = None, 0
+    if workspace is not None:
         ws_ptr = _dev(workspace, "workspace")
-        ws_bytes = workspace.numel() * workspace.element_size()
+        ws_bytes = workspace.nbytes
     rc = lib().pa_decode_sliding_window(
         _dev(out, "out"), _dev(query, "query"), _dev(key_cache, "key_cache"),
         _dev(value_cache, "value_cache"), ks_ptr, vs_ptr,
         _dev(block_tables, "block_tables", torch.int32),
         _dev(context_lens, "context_lens", torch.int32), B, Hq, Hkv, D, BLOCK_SIZE, max_blocks,
         NB, float(scale), code, int(window), int(partition_size), ws_ptr, ws_bytes,
-        _status_ptr(status), _stream(stream, query.device))
+        _status_ptr(status), _stream(stream, query))
     check(rc, "pa_decode_sliding_window")
     return out
 
@@ -343,7 +362,7 @@ def cache_write_fp8(key_cache, value_cache, key, value, slot_mapping, k_scales, 
     torch = _torch()
     NB, Hkv, BS, D = key_cache.shape
     T = slot_mapping.shape[0]
-    if tuple(key.shape) != (T, Hkv, D) or tuple(value.shape) != (T, Hkv, D):
+    if key.shape != (T, Hkv, D) or value.shape != (T, Hkv, D):
         raise ValueError("key/value must be [num_tokens][num_kv_heads][head_dim]")
     if not (_is_fp8(key_cache) and _is_fp8(value_cache)):
         raise TypeError("pools must hold E4M3 codes")
@@ -352,7 +371,7 @@ def cache_write_fp8(key_cache, value_cache, key, value, slot_mapping, k_scales, 
         _dev(key, "key", torch.bfloat16), _dev(value, "value", torch.bfloat16),
         _dev(slot_mapping, "slot_mapping", torch.int64), _dev(k_scales, "k_scales", torch.float32),
         _dev(v_scales, "v_scales", torch.float32), T, Hkv, D, BS, NB, _status_ptr(status),
-        _stream(stream, key_cache.device))
+        _stream(stream, key_cache))
     check(rc, "pa_cache_write_fp8")
 
 
@@ -361,7 +380,7 @@ def cache_write(key_cache, value_cache, key, value, slot_mapping, *, status=None
     torch = _torch()
     NB, Hkv, BS, D = key_cache.shape
     T = slot_mapping.shape[0]
-    if tuple(key.shape) != (T, Hkv, D) or tuple(value.shape) != (T, Hkv, D):
+    if key.shape != (T, Hkv, D) or value.shape != (T, Hkv, D):
         raise ValueError("key/value must be [num_tokens][num_kv_heads][head_dim]")
     code = _dtype_code(key_cache)
     for t, n in ((value_cache, "value_cache"), (key, "key"), (value, "value")):
@@ -370,7 +389,7 @@ def cache_write(key_cache, value_cache, key, value, slot_mapping, *, status=None
     rc = lib().pa_cache_write(
         _dev(key_cache, "key_cache"), _dev(value_cache, "value_cache"), _dev(key, "key"),
         _dev(value, "value"), _dev(slot_mapping, "slot_mapping", torch.int64), T, Hkv, D, BS, NB,
-        code, _status_ptr(status), _stream(stream, key_cache.device))
+        code, _status_ptr(status), _stream(stream, key_cache))
     check(rc, "pa_cache_write")
 
 
@@ -384,7 +403,7 @@ def block_copy(key_cache, value_cache, src_dst, *, status=None, stream=None):
     rc = lib().pa_block_copy(
         _dev(key_cache, "key_cache"), _dev(value_cache, "value_cache"),
         _dev(src_dst, "src_dst", torch.int32), P, Hkv, D, BS, NB, _dtype_code(key_cache),
-        _status_ptr(status), _stream(stream, key_cache.device))
+        _status_ptr(status), _stream(stream, key_cache))
     check(rc, "pa_block_copy")
 
 
@@ -401,7 +420,7 @@ def prefill(query, key_cache, value_cache, block_tables, context_lens, query_sta
     N, Hq, D = query.shape
     NB, Hkv, BS, D2 = key_cache.shape
     B = context_lens.shape[0]
-    if BS != BLOCK_SIZE or D2 != D or tuple(value_cache.shape) != tuple(key_cache.shape):
+    if BS != BLOCK_SIZE or D2 != D or value_cache.shape != key_cache.shape:
         raise ValueError("pools must be [num_blocks][num_kv_heads][16][head_dim] like query")
     if block_tables.dim() != 2 or block_tables.shape[0] != B or tuple(query_start.shape) != (B + 1,):
         raise ValueError("block_tables must be [num_seqs][max_blocks], query_start [num_seqs + 1]")
@@ -425,8 +444,8 @@ def prefill(query, key_cache, value_cache, block_tables, context_lens, query_sta
         _dev(context_lens, "context_lens", torch.int32),
         _dev(query_start, "query_start", torch.int32), B, Hq, Hkv, D, BLOCK_SIZE,
         block_tables.shape[1], NB, N, int(max_query_len), float(scale), _lib.PA_DTYPE_BF16,
-        int(window), _dev(workspace, "workspace"), workspace.numel() * workspace.element_size(),
-        _status_ptr(status), _stream(stream, query.device))
+        int(window), _dev(workspace, "workspace"), workspace.nbytes,
+        _status_ptr(status), _stream(stream, query))
     check(rc, "pa_prefill")
     return out
 
@@ -464,7 +483,7 @@ def swap_out(key_cache, value_cache, block_ids, staging=None, *, status=None, st
         staging = torch.empty((n, 2, Hkv, BS, D), dtype=key_cache.dtype, pin_memory=True)
     rc = lib().pa_swap_out(_dev(key_cache, "key_cache"), _dev(value_cache, "value_cache"), ids,
                            n, _staging_ptr(staging, nbytes), Hkv, D, BS, NB, code,
-                           _status_ptr(status), _stream(stream, key_cache.device))
+                           _status_ptr(status), _stream(stream, key_cache))
     check(rc, "pa_swap_out")
     return staging
 
@@ -474,7 +493,7 @@ def swap_in(key_cache, value_cache, block_ids, staging, *, status=None, stream=N
     NB, Hkv, BS, D, code, n, nbytes, ids = _swap_geometry(key_cache, block_ids)
     rc = lib().pa_swap_in(_dev(key_cache, "key_cache"), _dev(value_cache, "value_cache"), ids,
                           n, _staging_ptr(staging, nbytes), Hkv, D, BS, NB, code,
-                          _status_ptr(status), _stream(stream, key_cache.device))
+                          _status_ptr(status), _stream(stream, key_cache))
     check(rc, "pa_swap_in")
 
 

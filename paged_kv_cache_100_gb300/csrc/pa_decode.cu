@@ -81,9 +81,11 @@ struct DecodeArgs {
     int window;         // > 0: attend only to the last `window` positions
     // 1: only the grid's last CTA waits for the kernel before it in the stream
     // (the shared-prefix kernel), so that the others stream the suffix beside
-    // it.  Safe because that kernel waited for everything before it and let
-    // this one launch only after all of its CTAs had done so; the last CTA's
-    // wait keeps this grid from completing before it.  The last CTA is
+    // it.  Safe because every kernel before that one had completed when it let
+    // this one launch: all of its CTAs had waited for them first, or (FP8
+    // pools) all CTAs of the prefix-widening kernel before it had done so
+    // before it could start.  The last CTA's wait keeps this grid from
+    // completing before the shared-prefix kernel (and what it waits for).  The last CTA is
     // dispatched last, when the prefix kernel is nearly done, so its wait is
     // short (CTA 0 would hold its SM idle for the whole prefix kernel).
     int defer_wait;

@@ -345,8 +345,17 @@ __global__ void __launch_bounds__(kThreads, 1)
     pa_attn_tc_kernel(const __grid_constant__ CUtensorMap qmap,
                       const __grid_constant__ CUtensorMap kmap,
                       const __grid_constant__ CUtensorMap vmap, const PrefillArgs a) {
+    // Prefix mode lets the suffix decode launched after it start once all of
+    // its CTAs have started.  Normally that comes after its own wait for the
+    // kernels before it, since the suffix reads what they wrote without waiting
+    // itself.  With FP8 pools the kernel before it is the prefix widening,
+    // every CTA of which waited for all earlier kernels before this kernel
+    // could start, so the suffix is released at once and only this kernel
+    // waits for the widened prefix.
+    const bool early_release = kPrefix && a.staged;
+    if (early_release) grid_dependents_launch();
     grid_dependency_wait();
-    grid_dependents_launch();
+    if (!early_release) grid_dependents_launch();
     const int g = a.group;
     const int tok_per_tile = kRows / g;
     const int lmax = a.max_blocks * kBlockSize;
