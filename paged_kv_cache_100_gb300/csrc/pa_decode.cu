@@ -1667,11 +1667,14 @@ cudaError_t allow_smem(K kernel, size_t bytes) {
 #define PA_GQA8_STAGES 3
 #endif
 // FP8 GQA CTAs that stream at most PA_GQA8S_MAX_BLOCKS blocks (short contexts,
-// e.g. the part of a context past a shared prefix): 4 warps x 2 stages.  On
-// the 128-sequence shared-prefix mix (suffixes of 1..64 blocks) the FP8
-// suffix took 50.0 us against 55.2 us with 8 warps x 2 stages.
+// e.g. the part of a context past a shared prefix, or a sliding window):
+// 2 warps x 2 stages, many small CTAs per SM so that one CTA's fixed latency
+// (length, table, first tile; merge and store) overlaps the others' streaming.
+// Shared-prefix FP8 call 41.7 us (4 x 2: 43.1, 8 x 2: 54.3, 1 x 3: 50.0);
+// 70B-shaped batch with a 512-token window 57.5 us (4 x 2: 59.9), 1024-token
+// window 91.9 us (4 x 2: 92.8).
 #ifndef PA_GQA8S_WARPS
-#define PA_GQA8S_WARPS 4
+#define PA_GQA8S_WARPS 2
 #endif
 #ifndef PA_GQA8S_STAGES
 #define PA_GQA8S_STAGES 2
