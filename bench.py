@@ -404,13 +404,13 @@ def measure_decode(pkv, dev, stream, args, workload, kv_dtype="bf16", window=0, 
             pkv.block_copy(o.kc, o.vc, pairs_)
 
     def step(ev_pre=None, ev_post=None, q_=q, kn_=kn, vn_=vn, slots_=slots, pairs_=pairs, bt_=bt,
-             lens_=lens):
+             lens_=lens, out_=out):
         o = ops[state["i"] % copies]
         state["i"] += 1
         step_pre(o, kn_, vn_, slots_, pairs_)
         if ev_pre is not None:
             ev_pre.record(stream)
-        o.decode(q_, bt_, lens_, out)
+        o.decode(q_, bt_, lens_, out_)
         if ev_post is not None:
             ev_post.record(stream)
 
@@ -769,10 +769,111 @@ class PackedInputs:
         self.device.copy_(self.host, non_blocking=True)
 
 
+def _cudart():
+    """The CUDA runtime library torch has loaded (for stream-ordered copies
+    without switching torch's current stream), or None."""
+    import ctypes
+    for name in ("libcudart.so.13", "libcudart.so.12", "libcudart.so"):
+        try:
+            lib = ctypes.CDLL(name)
+        except OSError:
+            continue
+        fn = lib.cudaMemcpyAsync
+        fn.restype = ctypes.c_int
+        fn.argtypes = [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_size_t, ctypes.c_int,
+                       ctypes.c_void_p]
+        return lib
+    return None
+
+
+class E2ELoop:
+    """Steps through the public API with host inputs, every step copying its own
+    inputs from pinned host memory (one packed copy) and its output back.
+
+    The uploads and the read-backs run on two streams of their own, with two
+    device input buffers and two output buffers used in turn: step i + 1's
+    inputs go up and step i - 1's output comes back while step i's kernels run,
+    as a serving loop overlaps its transfers with compute.  (On one copy stream
+    the next upload would queue behind the read-back that waits for the current
+    step.)  Events order each copy against the step that uses its buffer.  The
+    timed region starts before the first upload and ends after the last output
+    has reached host memory."""
+
+    H2D, D2H = 1, 2   # cudaMemcpyKind
+
+    def __init__(self, inputs: dict, out, dev, stream, run_step):
+        import torch
+        self.torch, self.stream, self.run_step = torch, stream, run_step
+        self.up = torch.cuda.Stream(dev)
+        self.down = torch.cuda.Stream(dev)
+        self.bufs = [PackedInputs(inputs, dev) for _ in range(2)]
+        self.outs = [out, torch.empty_like(out)]
+        self.hosts = [torch.empty(out.shape, dtype=out.dtype).pin_memory() for _ in range(2)]
+        self.uploaded = [torch.cuda.Event() for _ in range(2)]
+        self.computed = [torch.cuda.Event() for _ in range(2)]
+        self.read_back = [torch.cuda.Event() for _ in range(2)]
+        self.i = 0
+        self.h2d = self.bufs[0].nbytes
+        self.d2h = out.numel() * out.element_size()
+        self.rt = _cudart()
+
+    def _copy(self, dst, src, nbytes, kind, stream):
+        if self.rt is not None:
+            rc = self.rt.cudaMemcpyAsync(dst.data_ptr(), src.data_ptr(), nbytes, kind,
+                                         stream.cuda_stream)
+            if rc != 0:
+                raise RuntimeError(f"cudaMemcpyAsync failed ({rc})")
+        else:
+            with self.torch.cuda.stream(stream):
+                dst.copy_(src, non_blocking=True)
+
+    def step(self):
+        b = self.i & 1
+        self.i += 1
+        buf, up, down = self.bufs[b], self.up, self.down
+        up.wait_event(self.computed[b])          # the step that last read buffer b has run
+        self._copy(buf.device, buf.host, buf.nbytes, self.H2D, up)
+        self.uploaded[b].record(up)
+        self.stream.wait_event(self.uploaded[b])
+        self.stream.wait_event(self.read_back[b])   # output b of two steps back is home
+        self.run_step(buf.dev, self.outs[b])
+        self.computed[b].record(self.stream)
+        down.wait_event(self.computed[b])
+        self._copy(self.hosts[b], self.outs[b], self.d2h, self.D2H, down)
+        self.read_back[b].record(down)
+
+    def time(self, K: int, dev) -> float:
+        """Milliseconds per step over K steps (after three untimed ones)."""
+        torch = self.torch
+        for _ in range(3):
+            self.step()
+        torch.cuda.synchronize(dev)
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        barrier()
+        e0.record(self.stream)
+        self.up.wait_event(e0)
+        self.down.wait_event(e0)
+        for _ in range(K):
+            self.step()
+        for ev in self.read_back:
+            self.stream.wait_event(ev)
+        e1.record(self.stream)
+        torch.cuda.synchronize(dev)
+        barrier()
+        return max_over_ranks(e0.elapsed_time(e1) / K, dev)
+
+
+E2E_NOTE = ("public API with host inputs: every step's inputs copied from pinned host "
+            "memory (one packed copy) and its output copied back, on an upload and a "
+            "read-back stream with two input and two output buffers in turn, overlapping the "
+            "neighbouring steps' kernels")
+
+
 def run_e2e(args, pkv, wl, q, kn, vn, dev, stream, step, out):
-    """Same step through the public API with host inputs: H2D of the step's inputs
-    (query, new K/V rows, slots, tables, lengths, copy pairs; packed in one pinned
-    buffer, one copy) and D2H of the output inside the timed region."""
+    """Same step through the public API with host inputs (query, new K/V rows,
+    slots, tables, lengths, copy pairs) uploaded and the output read back every
+    step, inside the timed region."""
     import torch
     has_cow = wl.cow_pairs.shape[0] > 0
     inputs = {
@@ -783,35 +884,18 @@ def run_e2e(args, pkv, wl, q, kn, vn, dev, stream, step, out):
     }
     if has_cow:
         inputs["pairs"] = torch.from_numpy(wl.cow_pairs)
-    packed = PackedInputs(inputs, dev)
-    devb = packed.dev
-    out_host = torch.empty(out.shape, dtype=out.dtype).pin_memory()
-    h2d = packed.nbytes
-    d2h = out.numel() * out.element_size()
 
-    def e2e_step():
-        packed.upload()
-        step(q_=devb["q"], kn_=devb["kn"], vn_=devb["vn"], slots_=devb["slots"],
-             pairs_=devb.get("pairs"), bt_=devb["bt"], lens_=devb["lens"])
-        out_host.copy_(out, non_blocking=True)   # the output the step wrote
+    def run_step(d, o):
+        step(q_=d["q"], kn_=d["kn"], vn_=d["vn"], slots_=d["slots"], pairs_=d.get("pairs"),
+             bt_=d["bt"], lens_=d["lens"], out_=o)
 
-    for _ in range(3):
-        e2e_step()
-    torch.cuda.synchronize(dev)
+    loop = E2ELoop(inputs, out, dev, stream, run_step)
     K = max(1, min(args.steps, args.e2e_steps))
-    e0 = torch.cuda.Event(enable_timing=True)
-    e1 = torch.cuda.Event(enable_timing=True)
-    barrier()
-    e0.record(stream)
-    for _ in range(K):
-        e2e_step()
-    e1.record(stream)
-    torch.cuda.synchronize(dev)
-    barrier()
-    ms = max_over_ranks(e0.elapsed_time(e1) / K, dev)
+    ms = loop.time(K, dev)
     _, world, _ = dist_env()
     return {"value": wl.num_seqs * world / (ms * 1e-3), "unit": "tokens/s", "ms_per_step": ms,
-            "steps": K, "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h)}
+            "steps": K, "h2d_bytes_per_step": int(loop.h2d), "d2h_bytes_per_step": int(loop.d2h),
+            "how": E2E_NOTE}
 
 
 # ---------------------------------------------------------------------------
@@ -1017,11 +1101,11 @@ def measure_prefill(pkv, dev, stream, args, soak_s=0.5, rank=0, world=1):
     window = args.window
 
     def step(ev_pre=None, ev_post=None, q_=q, kn_=kn, vn_=vn, slots_=slots, bt_=bt, lens_=lens,
-             qs_=qs):
+             qs_=qs, out_=out):
         pkv.cache_write(kc, vc, kn_, vn_, slots_)
         if ev_pre is not None:
             ev_pre.record(stream)
-        pkv.prefill(q_, kc, vc, bt_, lens_, qs_, maxq, pw.scale, window=window, out=out,
+        pkv.prefill(q_, kc, vc, bt_, lens_, qs_, maxq, pw.scale, window=window, out=out_,
                     workspace=ws)
         if ev_post is not None:
             ev_post.record(stream)
@@ -1067,44 +1151,29 @@ def measure_prefill(pkv, dev, stream, args, soak_s=0.5, rank=0, world=1):
     prefill_ms = max_over_ranks(sum(a_.elapsed_time(b_) for a_, b_ in zip(pre, post)) / K, dev)
     soak_ms = es0.elapsed_time(es1) / n_soak if n_soak else None
 
-    # end to end: chunk inputs from pinned host memory (one packed copy), output
-    # back, every step
-    packed = PackedInputs({"q": q.cpu(), "kn": kn.cpu(), "vn": vn.cpu(),
-                           "slots": torch.from_numpy(pw.slot_mapping),
-                           "bt": torch.from_numpy(pw.block_tables),
-                           "lens": torch.from_numpy(pw.context_lens),
-                           "qs": torch.from_numpy(pw.query_start)}, dev)
-    devb = packed.dev
-    out_host = torch.empty(out.shape, dtype=out.dtype).pin_memory()
+    # end to end: the chunk's inputs from pinned host memory and the output back,
+    # every step
+    inputs = {"q": q.cpu(), "kn": kn.cpu(), "vn": vn.cpu(),
+              "slots": torch.from_numpy(pw.slot_mapping),
+              "bt": torch.from_numpy(pw.block_tables),
+              "lens": torch.from_numpy(pw.context_lens),
+              "qs": torch.from_numpy(pw.query_start)}
 
-    def e2e_step():
-        packed.upload()
-        step(q_=devb["q"], kn_=devb["kn"], vn_=devb["vn"], slots_=devb["slots"], bt_=devb["bt"],
-             lens_=devb["lens"], qs_=devb["qs"])
-        out_host.copy_(out, non_blocking=True)
+    def run_step(d, o):
+        step(q_=d["q"], kn_=d["kn"], vn_=d["vn"], slots_=d["slots"], bt_=d["bt"],
+             lens_=d["lens"], qs_=d["qs"], out_=o)
 
-    for _ in range(3):
-        e2e_step()
-    torch.cuda.synchronize(dev)
+    loop = E2ELoop(inputs, out, dev, stream, run_step)
     KE = max(1, min(K, args.e2e_steps))
-    barrier()
-    e2 = torch.cuda.Event(enable_timing=True)
-    e3 = torch.cuda.Event(enable_timing=True)
-    e2.record(stream)
-    for _ in range(KE):
-        e2e_step()
-    e3.record(stream)
-    torch.cuda.synchronize(dev)
-    barrier()
-    e2e_ms = max_over_ranks(e2.elapsed_time(e3) / KE, dev)
+    e2e_ms = loop.time(KE, dev)
     return {"pw": pw, "window": window, "steps": K, "ms_per_step": ms_per_step, "prefill_ms": prefill_ms,
             "soak": {"steps": n_soak, "ms_per_step": soak_ms,
                      "s": None if soak_ms is None else n_soak * soak_ms / 1e3},
             "launches": int(launches), "clocks": clocks,
             "e2e": {"value": pw.num_tokens * world / (e2e_ms * 1e-3), "unit": "tokens/s",
                     "ms_per_step": e2e_ms, "steps": KE,
-                    "h2d_bytes_per_step": int(packed.nbytes),
-                    "d2h_bytes_per_step": int(out.numel() * out.element_size())},
+                    "h2d_bytes_per_step": int(loop.h2d), "d2h_bytes_per_step": int(loop.d2h),
+                    "how": E2E_NOTE},
             "q": q, "kc": kc, "vc": vc}
 
 
