@@ -552,6 +552,15 @@ def decode_kernel_desc(res) -> str:
             "several partitions)")
 
 
+def partition_label(res):
+    """The split-K partition size the run used, or who chose it."""
+    if res["P"]:
+        return res["P"]
+    if res["window"]:
+        return "library choice per window"
+    return "library choice (shared-prefix suffix)" if res["n_prefix"] else "library choice"
+
+
 def decode_summary(res, args, workload, decode, partition_size, world) -> dict:
     """The figures of one decode configuration (the per-configuration record)."""
     wl = res["wl"]
@@ -566,7 +575,7 @@ def decode_summary(res, args, workload, decode, partition_size, world) -> dict:
     out = {
         "workload": workload_config(wl, world, kvd_arg, res["window"], res["unique_kv"])["workload"],
         "decode_method": decode_method(res),
-        "partition_size": res["P"] or "per window",
+        "partition_size": partition_label(res),
         "ms_per_step": res["ms_per_step"],
         "decode_ms": decode_ms,
         "tokens_per_s": wl.num_seqs * world / (res["ms_per_step"] * 1e-3),
@@ -664,7 +673,7 @@ def run_gpu(args):
             "dtype": "fp8_e4m3 K/V, bf16 Q/O" if res["fp8"] else wl.dtype,
             "data": "synthetic (seeded; N(0, %g) values, shuffled block pool)" % wl.value_std,
             "config": workload_config(wl, world, args.kv_dtype, args.window, res["unique_kv"]),
-            "partition_size_used": res["P"] or "per window",
+            "partition_size_used": partition_label(res),
             "decode_ms": res["decode_ms"],
             "ms_per_step_with_call_events": res["ms_per_step_with_call_events"],
             "kv_gbs": summ["kv_gbs"],
