@@ -668,11 +668,16 @@ struct MhaFp8Consumer {
     float ck;            // softmax scale * log2(e) * k scale
     float vs;
     int lane, c, rg;
+    // byte offsets of this lane's 16-byte chunk c in rows 4rg .. 4rg + 3 of a
+    // swizzled tile (the same for K and V tiles)
+    uint32_t off[RPL];
 
     __device__ __forceinline__ void init(const DecodeArgs &a, const Work &w, int lane_) {
         lane = lane_;
         c = lane & (CH - 1);
         rg = lane / CH;
+#pragma unroll
+        for (int i = 0; i < RPL; ++i) off[i] = swz(0u, rg * RPL + i, c);
         const __nv_bfloat16 *qrow =
             static_cast<const __nv_bfloat16 *>(a.query) + ((size_t)w.b * a.num_q_heads + w.head) * D;
         const uint4 r0 = *reinterpret_cast<const uint4 *>(qrow + 16 * c);
@@ -697,7 +702,7 @@ struct MhaFp8Consumer {
         float v[RPL];
 #pragma unroll
         for (int i = 0; i < RPL; ++i) {
-            const uint4 kw = lds128(swz(ktile, rg * RPL + i, c));
+            const uint4 kw = lds128(ktile + off[i]);
             const uint32_t w4[4] = {kw.x, kw.y, kw.z, kw.w};
             float dot = 0.f;
 #pragma unroll
@@ -737,13 +742,16 @@ struct MhaFp8Consumer {
         }
         const float p = ex2_fast(s - m);
         l += (lane & 1) ? 0.f : p;
+        // rows outside [nlo, nvalid) may hold anything (NaN included), so their
+        // products are skipped; a full block (the common case) needs no test
+        const bool full = nlo == 0 && nvalid == 16;
 #pragma unroll
         for (int i = 0; i < RPL; ++i) {
             const int r = rg * RPL + i;
             // the weight enters the products as f16 (relative error <= 2^-11)
             const uint32_t p16 = pack_f16x2(__shfl_sync(kFull, p, rg * CH + 2 * i), 0.f);
-            const uint4 vw = lds128(swz(vtile, r, c));
-            if (r >= nlo && r < nvalid) {
+            const uint4 vw = lds128(vtile + off[i]);
+            if (full || (r >= nlo && r < nvalid)) {
                 const uint32_t w4[4] = {vw.x, vw.y, vw.z, vw.w};
 #pragma unroll
                 for (int j = 0; j < 4; ++j) {
