@@ -75,3 +75,24 @@ def test_unique_bytes_count_a_shared_block_once():
     per_row = bench.kv_bytes_per_token(1, 4, 64, 2)
     assert bench.unique_kv_bytes(wl, lens=lens) == (80 - 16) * per_row
     assert bench.decode_algorithmic_bytes(wl, lens=lens)["kv"] == 80 * per_row
+
+
+def test_causal_pair_count_is_the_pages_cost_table(golden_dir):
+    """The prefill roofline counts (query row, attended position) pairs.  A fresh
+    prompt of N tokens (nothing cached) has N(N+1)/2 of them: the "without a KV
+    cache" column of the pages' cost table, where step i attends i tokens."""
+    with open(os.path.join(golden_dir, "attention_cost.json")) as f:
+        rows = json.load(f)["cost_table"]["rows"]
+    for r in rows:
+        n = r["tokens"]
+        pw = W.PrefillWorkload("fresh", 1, 1, 1, 128, 1.0, np.zeros(1, np.int32),
+                               np.asarray([n], np.int32), np.zeros((1, 1), np.int32), 1)
+        pairs = bench.prefill_pairs(pw)
+        assert pairs == r["without_cache"], n
+        assert pairs // r["with_cache"] == r["ratio"], n
+        # QK^T and PV: 2 * head_dim flops each per pair and head
+        assert bench.prefill_flops(pw) == 4 * 128 * pairs
+    # a window caps each row's pairs: the last W positions only
+    pw = W.PrefillWorkload("fresh", 1, 1, 1, 128, 1.0, np.zeros(1, np.int32),
+                           np.asarray([1024], np.int32), np.zeros((1, 1), np.int32), 1)
+    assert bench.prefill_pairs(pw, window=128) == 8256 + (1024 - 128) * 128
