@@ -23,11 +23,13 @@
 //                memory; owns the TMEM allocation (S_A, S_B, O_A, O_B);
 //   warps 2..9   softmax of tile A, warps 10..17 softmax of tile B: two threads
 //                per row (= TMEM lane), each owning 64 of the 128 columns of S
-//                and of O.  They agree on the row maximum through shared memory
-//                once per K/V tile, keep their part of the running sum, write P
-//                (f16) over the S columns they read, rescale their part of O
-//                only when the maximum grew by more than 2^8, and write their
-//                part of the output row;
+//                and of O.  In one pass over S per K/V tile they write P (f16)
+//                over the S columns they read, against an integer reference
+//                that rises only when a chunk's weights would grow past 2^15;
+//                they agree on the row's reference through shared memory once
+//                per K/V tile, keep their part of the running sum, rescale
+//                their part of O (by a power of two) only when the reference
+//                rose, and write their part of the output row;
 //   warps 18..19 convert each landed V tile to f16 in place (P.V runs on f16
 //                operands: bf16 weights would be too coarse for the output
 //                tolerance) and zero the rows of positions outside the tile's
@@ -76,7 +78,7 @@ constexpr int kThreads = 64 + kQT * kGroup + kConvThreads;
 #define PA_PREFILL_STAGES 2
 #endif
 constexpr int kStages = PA_PREFILL_STAGES;   // depth of the K and V rings
-constexpr float kRescaleLog2 = 8.0f;     // lazy rescale threshold (factor 256)
+constexpr float kChunkSumMax = 32768.f;  // largest weight sum of a 32-column chunk kept as computed
 constexpr size_t kPrefillWorkspaceBytes = 256;   // the ticket counter (rounded up)
 
 // shared memory map (offsets from the 1024-byte aligned dynamic base)
@@ -198,6 +200,14 @@ __device__ __forceinline__ uint64_t f2_mul(uint64_t a, uint64_t b) {
     return r;
 }
 
+// 2^(a - b) for references a <= b that are integers or -inf (b may be +inf
+// after infinite scores): exact, 0 when a is -inf or far below b.
+__device__ __forceinline__ float pow2_diff(float a, float b) {
+    if (a == b) return 1.f;
+    if (!(a > -INFINITY) || !(b - a < 256.f)) return 0.f;
+    return ldexpf(1.f, (int)(a - b));
+}
+
 __device__ __forceinline__ uint32_t pack2_bf16(float lo, float hi) {
     __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
     return *reinterpret_cast<uint32_t *>(&v);
@@ -208,6 +218,63 @@ __device__ __forceinline__ uint32_t pack2_f16(float lo, float hi) {
     uint32_t r;
     asm("cvt.rn.f16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
     return r;
+}
+
+// The softmax's rare paths, kept out of line so that the registers of the
+// common path stay free.  Both are called by all lanes of a warp together
+// (their tensor-memory accesses are warp-wide).
+
+// Weights of the 32-column chunk of S at taddr (its first column is position
+// kc) written over it as 16 f16 pairs: P = 2^(s * sl2k - ref).  A lane whose
+// first attempt summed past the limit (over) first raises its reference ref to
+// the next integer at or above the chunk's largest scaled attended score.
+// Returns (weight sum, reference).
+__device__ __noinline__ float2 chunk_weights_again(uint32_t taddr, float sl2k, float ref, bool over,
+                                                   bool masked, int kc, int qpos, int wlo) {
+    uint32_t v[32];
+    tmem_ld32(taddr, v);
+    tmem_wait_ld();
+    if (over) {
+        float rmax = -INFINITY;
+#pragma unroll
+        for (int i = 0; i < 32; ++i)
+            if (!masked || (kc + i <= qpos && kc + i >= wlo))
+                rmax = fmaxf(rmax, __uint_as_float(v[i]) * sl2k);
+        const float nref = ceilf(rmax);
+        if (nref > ref) ref = nref;   // else non-finite scores: as computed before
+    }
+    uint32_t pp[16];
+    float sum = 0.f;
+#pragma unroll
+    for (int i = 0; i < 32; i += 2) {
+        float p0 = ex2_approx(__uint_as_float(v[i]) * sl2k - ref);
+        float p1 = ex2_approx(__uint_as_float(v[i + 1]) * sl2k - ref);
+        if (masked) {
+            if (!(kc + i <= qpos && kc + i >= wlo)) p0 = 0.f;
+            if (!(kc + i + 1 <= qpos && kc + i + 1 >= wlo)) p1 = 0.f;
+        }
+        sum += p0 + p1;
+        pp[i >> 1] = pack2_f16(p0, p1);
+    }
+    tmem_st16(taddr, pp);
+    return make_float2(sum, ref);
+}
+
+// Scales the f16 weights of this thread's two 32-column chunks (first 16
+// columns of each, from taddr) by f0 and f1.
+__device__ __noinline__ void scale_chunk_weights(uint32_t taddr, float f0, float f1) {
+#pragma unroll 1
+    for (int c = 0; c < 64; c += 32) {
+        const float f = c == 0 ? f0 : f1;
+        uint32_t w[32];
+        tmem_ld32(taddr + c, w);
+        tmem_wait_ld();
+        uint32_t q[16];
+#pragma unroll
+        for (int i = 0; i < 16; ++i) q[i] = pack2_f16(f16lo(w[i]) * f, f16hi(w[i]) * f);
+        tmem_st16(taddr + c, q);
+    }
+    tmem_wait_st();
 }
 
 // Eight bf16 values (a 16-byte chunk) as eight f16 values in place order:
@@ -758,10 +825,6 @@ __global__ void __launch_bounds__(kThreads, 1)
             const int n_tiles = d.n_tiles;
             if (x == 0 || d.has_b) {
                 const float sl2k = a.k_scales != nullptr ? a.scale_log2 * a.k_scales[d.kvh] : a.scale_log2;
-                // a negative scale reverses the order of the scores; masked
-                // positions take the raw value that never wins
-                const bool neg = sl2k < 0.f;
-                const float fill = neg ? INFINITY : -INFINITY;
                 const int tx0 = d.t0 + x * tok_per_tile;      // first token (sequence) of this tile
                 const int ntok = max(0, min(tok_per_tile, d.T - tx0));
                 const bool real = tr < ntok;
@@ -790,6 +853,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                     if constexpr (kPrefix) return __any_sync(0xffffffffu, kc + 31 > qpos);
                     return (kc + 31 > qpos_lo) || (a.window > 0 && kc < qpos_hi + 1 - a.window);
                 };
+                // The row's reference (log2 units): an integer, or -inf before the
+                // row has seen a position; O and l are relative to it.
                 float m_used = -INFINITY, l = 0.f;
                 // Every thread of the group runs every iteration and reaches the
                 // named barrier the same number of times, even after a wait gave
@@ -797,55 +862,102 @@ __global__ void __launch_bounds__(kThreads, 1)
                 for (int j = 0; j < n_tiles; ++j) {
                     const bool got = ok && warp_wait(&bars[kSFull + x], sc & 1, fail, a.status);
                     const int k0 = (d.blk_lo + 8 * j) * kBlockSize + part * kCols;   // column 0's position
-                    // pass 1: the raw score whose scaled value is the row maximum
-                    // over this thread's columns (the largest raw score, or the
-                    // smallest when the scale is negative)
-                    float mx4[4] = {fill, fill, fill, fill};
+                    // One pass over S: each 32-column chunk's weights P = 2^(s *
+                    // scale_log2 - ref) are computed against this thread's current
+                    // reference ref and written over the chunk in f16, unless they
+                    // sum to more than 2^15 (a weight could leave f16's range, or
+                    // there is no reference yet and the sum is infinite): then ref
+                    // rises to the next integer at or above the chunk's largest
+                    // scaled score and the chunk is computed again.  Each chunk keeps
+                    // the reference it was written with (cref) and its weight sum.
+                    float mref = m_used;
+                    float cref0 = m_used, cref1 = m_used, csum0 = 0.f, csum1 = 0.f;
+                    static_assert(kCols == 64, "two 32-column chunks per softmax thread");
                     if (got) {
                         tc_fence_after();
+                        const uint64_t k2 = f2_pack(sl2k, sl2k);
 #pragma unroll 1
                         for (int c = 0; c < kCols; c += 32) {
-                            uint32_t v[32];
-                            tmem_ld32(s_base + c, v);
-                            tmem_wait_ld();
                             const int kc = k0 + c;
-                            if (chunk_masked(kc)) {
+                            const bool masked = chunk_masked(kc);
+                            uint32_t pp[16];
+                            float sum;
+                            {
+                                uint32_t v[32];
+                                tmem_ld32(s_base + c, v);
+                                tmem_wait_ld();
+                                // pairs of columns on f32x2 arithmetic: one FMA and
+                                // one add instruction for two weights; 11 significant
+                                // bits (f16) keep the weights within the output
+                                // tolerance, where bf16's 8 bits do not
+                                const uint64_t nm2 = f2_pack(-mref, -mref);
+                                uint64_t ps2[2] = {f2_pack(0.f, 0.f), f2_pack(0.f, 0.f)};
 #pragma unroll
-                                for (int i = 0; i < 32; ++i)
-                                    if (!(kc + i <= qpos && kc + i >= wlo)) v[i] = __float_as_uint(fill);
+                                for (int i = 0; i < 32; i += 2) {
+                                    float x0, x1;
+                                    f2_unpack(f2_fma(f2_pack(__uint_as_float(v[i]), __uint_as_float(v[i + 1])), k2, nm2), x0, x1);
+                                    float p0 = ex2_approx(x0);
+                                    float p1 = ex2_approx(x1);
+                                    if (masked) {
+                                        if (!(kc + i <= qpos && kc + i >= wlo)) p0 = 0.f;
+                                        if (!(kc + i + 1 <= qpos && kc + i + 1 >= wlo)) p1 = 0.f;
+                                    }
+                                    ps2[(i >> 1) & 1] = f2_add(ps2[(i >> 1) & 1], f2_pack(p0, p1));
+                                    pp[i >> 1] = pack2_f16(p0, p1);
+                                }
+                                float a0, a1, b0, b1;
+                                f2_unpack(ps2[0], a0, a1);
+                                f2_unpack(ps2[1], b0, b1);
+                                sum = (a0 + b0) + (a1 + b1);
                             }
-                            if (!neg) {
-#pragma unroll
-                                for (int i = 0; i < 32; ++i) mx4[i & 3] = fmaxf(mx4[i & 3], __uint_as_float(v[i]));
+                            const bool over = !(sum <= kChunkSumMax);
+                            if (__any_sync(0xffffffffu, over)) {
+                                // the whole warp (warp-wide tensor-memory access); S is
+                                // still in place, P not yet written
+                                const float2 r2 = chunk_weights_again(s_base + c, sl2k, mref, over, masked,
+                                                                      kc, qpos, wlo);
+                                sum = r2.x;
+                                mref = r2.y;
                             } else {
-#pragma unroll
-                                for (int i = 0; i < 32; ++i) mx4[i & 3] = fminf(mx4[i & 3], __uint_as_float(v[i]));
+                                tmem_st16(s_base + c, pp);
+                            }
+                            if (c == 0) {
+                                cref0 = mref;
+                                csum0 = sum;
+                            } else {
+                                cref1 = mref;
+                                csum1 = sum;
                             }
                         }
+                        tmem_wait_st();
                     }
-                    float mrow = neg ? fminf(fminf(mx4[0], mx4[1]), fminf(mx4[2], mx4[3]))
-                                     : fmaxf(fmaxf(mx4[0], mx4[1]), fmaxf(mx4[2], mx4[3]));
+                    // the two threads of the row agree on the larger reference
                     const int rp = ex & 1;
                     ++ex;
-                    red[(rp * kSplit + part) * kRows + r] = mrow;
+                    red[(rp * kSplit + part) * kRows + r] = mref;
                     pair_sync(x, quarter);
+                    float rref = mref;
 #pragma unroll
-                    for (int o = 1; o < kSplit; ++o) {
-                        const float other = red[(rp * kSplit + ((part + o) % kSplit)) * kRows + r];
-                        mrow = neg ? fminf(mrow, other) : fmaxf(mrow, other);
-                    }
+                    for (int o = 1; o < kSplit; ++o)
+                        rref = fmaxf(rref, red[(rp * kSplit + ((part + o) % kSplit)) * kRows + r]);
                     const uint32_t my_sc = sc++;
                     if (!got) {
                         ok = false;
                         continue;
                     }
-                    const float m_new = fmaxf(m_used, mrow * sl2k);
-                    // Lazy rescale: only rows whose maximum grew by more than 2^8
-                    // move their reference; the warp rescales O together (warp-wide
-                    // tensor-memory access, factor 1 on the other rows) once every
-                    // PV of this tile issued so far has landed.
-                    const bool need = m_new > m_used + kRescaleLog2;
-                    const float alpha = need ? exp2f(m_used - m_new) : 1.f;   // 0 while m_used is -inf
+                    // chunks written against a smaller reference than the row's are
+                    // scaled by the exact power of two between them (0 when their
+                    // reference was -inf: all their weights are 0); the warp does it
+                    // together (warp-wide tensor-memory access, factor 1 elsewhere)
+                    const float f0 = pow2_diff(cref0, rref);
+                    const float f1 = pow2_diff(cref1, rref);
+                    if (__any_sync(0xffffffffu, f0 != 1.f || f1 != 1.f)) scale_chunk_weights(s_base, f0, f1);
+                    const float psum = csum0 * f0 + csum1 * f1;
+                    // O and l follow when the row's reference moved; the warp
+                    // rescales O together once every PV of this tile issued so far
+                    // has landed
+                    const bool need = rref > m_used;
+                    const float alpha = need ? pow2_diff(m_used, rref) : 1.f;   // 0 while m_used is -inf
                     if (j >= 1 && __any_sync(0xffffffffu, need)) {
                         if (!warp_wait(&bars[kPvDone + x], (my_sc - 1) & 1, fail, a.status)) {
                             ok = false;
@@ -871,48 +983,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                     }
                     if (need) {
                         l *= alpha;
-                        m_used = m_new;
+                        m_used = rref;
                     }
-                    const float m_ref = m_used == -INFINITY ? 0.f : m_used;
-                    // pass 2: P = 2^(s * scale_log2 - m_ref) in f16 (at most 2^8, so
-                    // always finite; 11 significant bits keep the weights within
-                    // the output tolerance, where bf16's 8 bits do not), written as
-                    // 16 columns of pairs over the first half of the 32 columns it
-                    // was read from
-                    // pairs of columns on f32x2 arithmetic: one FMA and one add
-                    // instruction for two weights
-                    const uint64_t k2 = f2_pack(sl2k, sl2k), nm2 = f2_pack(-m_ref, -m_ref);
-                    uint64_t ps2[2] = {f2_pack(0.f, 0.f), f2_pack(0.f, 0.f)};
-#pragma unroll 1
-                    for (int c = 0; c < kCols; c += 32) {
-                        uint32_t v[32];
-                        tmem_ld32(s_base + c, v);
-                        tmem_wait_ld();
-                        const int kc = k0 + c;
-                        const bool masked = chunk_masked(kc);
-                        uint32_t pp[16];
-#pragma unroll
-                        for (int i = 0; i < 32; i += 2) {
-                            float x0, x1;
-                            f2_unpack(f2_fma(f2_pack(__uint_as_float(v[i]), __uint_as_float(v[i + 1])), k2, nm2), x0, x1);
-                            float p0 = ex2_approx(x0);
-                            float p1 = ex2_approx(x1);
-                            if (masked) {
-                                if (!(kc + i <= qpos && kc + i >= wlo)) p0 = 0.f;
-                                if (!(kc + i + 1 <= qpos && kc + i + 1 >= wlo)) p1 = 0.f;
-                            }
-                            ps2[(i >> 1) & 1] = f2_add(ps2[(i >> 1) & 1], f2_pack(p0, p1));
-                            pp[i >> 1] = pack2_f16(p0, p1);
-                        }
-                        tmem_st16(s_base + c, pp);
-                    }
-                    tmem_wait_st();
-                    {
-                        float a0, a1, b0, b1;
-                        f2_unpack(ps2[0], a0, a1);
-                        f2_unpack(ps2[1], b0, b1);
-                        l += (a0 + b0) + (a1 + b1);
-                    }
+                    l += psum;
                     tc_fence_before();
                     mbar_arrive(&bars[kPFull + x]);
                 }

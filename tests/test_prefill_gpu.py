@@ -236,3 +236,46 @@ def test_large_values_within_f16_range(pkv):
     got, st = _run(pkv, wl, hv, q, qs, tables, lens)
     assert st == 0
     H.assert_close(H.as_f64(got), _oracle(wl, hv, q, qs, tables, lens), "bf16", "large V")
+
+
+# Key rows scaled up at some positions make those scores jump by tens of log2
+# units in a later K/V tile: a 32-column chunk's weights then overflow the
+# reference the row carries from the tiles before, and the chunk is computed
+# again against a higher one.  [288, 320) is the second chunk of the first
+# thread of the third tile (its first chunk is rescaled afterwards), [320, 384)
+# the second thread's columns (the first thread's chunks follow it), [130, 140)
+# a jump within the second tile.
+@pytest.mark.parametrize("hq,hkv", [(8, 2), (8, 8)])
+@pytest.mark.parametrize("lo,hi,factor", [(288, 320, 8.0), (320, 384, 8.0), (130, 140, 30.0),
+                                          (0, 128, 8.0)])
+def test_scores_rising_in_later_tiles(pkv, hq, hkv, lo, hi, factor):
+    specs = [(0, 400), (200, 250), (100, 60)]
+    wl, hv, q, qs, tables, lens = _case(hq, hkv, specs, seed=71 + lo)
+    k = W.bf16_bits_to_f32(hv.key_cache)
+    for b in range(len(specs)):
+        for pos in range(lo, min(hi, int(lens[b]))):
+            phys = int(tables[b, pos // 16])
+            k[phys, :, pos % 16] *= np.float32(factor)
+    keep = np.isnan(k)
+    hv.key_cache = np.where(keep, hv.key_cache, W.to_bf16_bits(k))
+    got, st = _run(pkv, wl, hv, q, qs, tables, lens)
+    assert st == 0
+    H.assert_close(H.as_f64(got), _oracle(wl, hv, q, qs, tables, lens), "bf16",
+                   f"keys x{factor} at [{lo}, {hi})")
+
+
+def test_scores_rising_with_a_negative_scale(pkv):
+    """The same jump seen through a negative scale: the smallest raw scores win."""
+    specs = [(0, 400), (150, 200)]
+    wl, hv, q, qs, tables, lens = _case(8, 2, specs, seed=91)
+    k = W.bf16_bits_to_f32(hv.key_cache)
+    for b in range(len(specs)):
+        for pos in range(300, 340):
+            phys = int(tables[b, pos // 16])
+            k[phys, :, pos % 16] *= np.float32(-8.0)
+    keep = np.isnan(k)
+    hv.key_cache = np.where(keep, hv.key_cache, W.to_bf16_bits(k))
+    got, st = _run(pkv, wl, hv, q, qs, tables, lens, scale=-0.0883883)
+    assert st == 0
+    H.assert_close(H.as_f64(got), _oracle(wl, hv, q, qs, tables, lens, scale=-0.0883883), "bf16",
+                   "negative scale, keys x-8 at [300, 340)")

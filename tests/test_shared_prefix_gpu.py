@@ -267,3 +267,22 @@ def test_shared_prefix_fp8_workload_full_size(pkv):
     torch.cuda.synchronize()
     assert int(status.item()) == 0
     H.assert_close(H.as_f64(out), H.as_f64(plain), "bf16", "fp8 cascade vs plain FP8 decode")
+
+
+@pytest.mark.parametrize("lo,hi", [(288, 320), (320, 384), (600, 700)])
+def test_prefix_scores_rising_in_later_tiles(pkv, lo, hi):
+    """Keys of the shared prefix scaled up at [lo, hi): the prefix kernel's rows see
+    their scores jump in a later K/V tile and move their reference there."""
+    suffix = [0, 1, 15, 200, 640, 3, 90, 33]
+    wl = _shared_workload(len(suffix), 32, 8, 128, 48, suffix, seed=lo)
+    hv = W.host_values(wl)
+    k = W.bf16_bits_to_f32(hv.key_cache)
+    for pos in range(lo, hi):
+        phys = int(wl.block_tables[0, pos // 16])
+        k[phys, :, pos % 16] *= np.float32(8.0)
+    hv.key_cache = np.where(np.isnan(k), hv.key_cache, W.to_bf16_bits(k))
+    out, ref_gpu = _run(pkv, wl, hv, 48)
+    ref = oracle.paged_decode(hv.query, hv.key_cache, hv.value_cache, wl.block_tables,
+                              wl.context_lens, wl.scale, threads=4)
+    H.assert_close(H.as_f64(out), ref, "bf16", f"prefix keys x8 at [{lo}, {hi})")
+    H.assert_close(H.as_f64(out), H.as_f64(ref_gpu), "bf16", "against pa_decode")
