@@ -989,7 +989,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     tc_fence_before();
                     mbar_arrive(&bars[kPFull + x]);
                 }
-                // the row sum is the parts' sums (all against the same maximum),
+                // the row sum is the parts' sums (all against the row's reference),
                 // exchanged in the slots of the other parity
                 const int sx = ex & 1;
                 ++ex;
