@@ -659,7 +659,8 @@ struct MhaFp8Consumer {
     static constexpr int ROWS = 1;
     static constexpr int kElemBytes = 1;
     // table entries and query loaded after the length (as one chain): loaded
-    // beside it they made the 7B-shaped FP8 batch 2 % slower (94.8 -> 97.0 us)
+    // beside it they gain nothing on the 7B-shaped FP8 batch (92.1 us either
+    // way; 2 % slower with an earlier form of this consumer)
     static constexpr bool kEarlyLoads = false;
 
     uint32_t q[8];       // f16x2: elements 16c + 2i, 16c + 2i + 1
